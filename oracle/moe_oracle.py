@@ -1,0 +1,323 @@
+"""CPU oracle of the sparse token-choice Mixture-of-Experts FFN layer forward.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the library imports this file; only the
+tests, the smoke check and the CPU-baseline leg of the benchmark call it.  It
+shares no code with the CUDA path.
+
+Plain numpy, float64 arithmetic, written for a reader checking it against the
+pages by eye:
+
+  * "Lecture29" (CS25 lecture 29 notes, Mixtral): section "Top-two routing: from
+    logits to weighted expert output" -- router logits z, top-k set S_k(x), gate
+    g_i = exp(z_i) / sum_{j in S_k} exp(z_j), output y = sum_i g_i Expert_i(x);
+    section "A dense Transformer layer" -- the SwiGLU expert W2(SiLU(W1 x) * W3 x);
+    section "Inference load balance" -- capacity C = ceil(alpha T k / E);
+    section "Myth 3" -- the imbalance ratio I = max_i n_i / (T k / E).
+  * "Chapter 19: MoE" (awesome-ai-roadmap): 19.3.2 -- softmax over the selected
+    logits equals the full softmax renormalised over the top-k; 19.3.3 -- the
+    Switch balance quantities f_i and P_i; 19.3.4 -- DeepSeek-V3 selection bias
+    used only for choosing experts, mixing weights from the raw affinities;
+    19.6.1 -- T k / N assignments per expert on average, overflow dropped with
+    the residual path kept.
+  * "Stanford CS336 lecture 4: Mixture of Experts": section 5 (top-K routing,
+    the router is a linear scorer); section 6 (shared experts, always on);
+    section 9 (loss N * sum_i f_i P_i; DeepSeek-V3 bias b_i used only for
+    routing); section 10 (a dropped token's expert output is zero, the residual
+    passes); section 11 (router kept in float32).
+  * "Outrageously Large Neural Networks" notes (Shazeer et al. 2017): the gate
+    matrix W_g is d x n; each expert is a one-hidden-layer ReLU network
+    512 -> 1024 -> 512 with no biases.
+
+Readings where the pages leave a step open (each is listed in the design notes):
+  - top-k order: selection score descending, ties to the lower expert index;
+  - capacity keeps, per expert, the first C assignments in ascending token
+    index regardless of the slot j; no renormalisation after a drop;
+  - f_i counts routed assignments before capacity, divided by T*k;
+  - P_i: the full N-way softmax of z (softmax gate) or s_i / sum_l s_l
+    (sigmoid gate, without the selection bias);
+  - the sigmoid affinity s = fl32(1 / (1 + exp(-z))) computed in double, the
+    selection score fl32(s + b);
+  - the output is the MoE branch only (the residual add belongs to the caller).
+"""
+from __future__ import annotations
+
+import dataclasses
+from fractions import Fraction
+from typing import Optional
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------- inputs
+def widen(a: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact float64 value of a stored tensor: bf16 bit patterns (uint16) or float32."""
+    if dtype == "bf16":
+        return (np.asarray(a).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.asarray(a, dtype=np.float32).astype(np.float64)
+
+
+# --------------------------------------------------------------------------- routing
+def router_logits(x64: np.ndarray, Wg: np.ndarray, logit_bias: Optional[np.ndarray]) -> np.ndarray:
+    """z = x . W_g (+ beta), summed in double and rounded once to float32.
+
+    Lecture29, "Top-two routing" (z = W_r x); CS336 lecture 4, section 5 (the
+    router is a linear scorer, not an MLP) and section 11 (router in float32).
+    beta is the workload's additive logit skew (zero unless given)."""
+    z = x64 @ Wg.astype(np.float64)
+    if logit_bias is not None:
+        z = z + logit_bias.astype(np.float64)[None, :]
+    return z.astype(np.float32)
+
+
+def sigmoid_affinity(z: np.ndarray) -> np.ndarray:
+    """DeepSeek-V3 affinity s = sigmoid(z), computed in double, rounded to float32.
+
+    Chapter 19, 19.3.2 and 19.3.4 (sigmoid affinity, not a softmax)."""
+    z64 = z.astype(np.float64)
+    return (1.0 / (1.0 + np.exp(-z64))).astype(np.float32)
+
+
+def selection_scores(z: np.ndarray, gate: str, sel_bias: Optional[np.ndarray]):
+    """Returns (sel, s): the scores top-k ranks on, and the sigmoid affinities (or None).
+
+    softmax gate: sel = z (softmax is monotone, so ranking z ranks the
+    probabilities).  sigmoid gate: sel = fl32(s + b), where the bias b only
+    steers the choice (Chapter 19, 19.3.4; CS336 lecture 4, section 9)."""
+    if gate == "softmax":
+        return z, None
+    s = sigmoid_affinity(z)
+    if sel_bias is None:
+        return s, s
+    sel = (s.astype(np.float64) + sel_bias.astype(np.float64)[None, :]).astype(np.float32)
+    return sel, s
+
+
+def topk(sel: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest scores per token, ordered by (score desc, index asc).
+
+    Lecture29, "Top-two routing" (S_k(x) = indices of the k largest logits).
+    A stable sort of the negated scores keeps equal scores in index order."""
+    order = np.argsort(-sel, axis=1, kind="stable")
+    return order[:, :k].astype(np.int32)
+
+
+def gate_weights(z: np.ndarray, s: Optional[np.ndarray], idx: np.ndarray, gate: str) -> np.ndarray:
+    """Gate weight of each selected slot, float64.
+
+    softmax: g_j = exp(z_j) / sum_{l in S} exp(z_l)  (Lecture29 "Top-two routing";
+      shifted by the selected maximum, which cancels).
+    sigmoid: g_j = s_j / sum_{l in S} s_l from the raw affinities, no bias
+      (Chapter 19, 19.3.4)."""
+    T, k = idx.shape
+    w = np.zeros((T, k), dtype=np.float64)
+    for t in range(T):
+        if gate == "softmax":
+            zs = z[t, idx[t]].astype(np.float64)
+            e = np.exp(zs - zs.max())
+            w[t] = e / e.sum()
+        else:
+            ss = s[t, idx[t]].astype(np.float64)
+            w[t] = ss / ss.sum()
+    return w
+
+
+# --------------------------------------------------------------------------- dispatch
+def capacity(alpha: float, T: int, k: int, N: int) -> int:
+    """C = ceil(alpha * T * k / N), exactly (alpha taken as its exact binary value).
+
+    Lecture29, "Inference load balance"; Chapter 19, 19.6.1."""
+    return int(-((-Fraction(alpha) * T * k) // N))
+
+
+@dataclasses.dataclass
+class Dispatch:
+    counts_routed: np.ndarray   # [N] int32
+    counts_kept: np.ndarray     # [N] int32
+    offsets: np.ndarray         # [N+1] int32, exclusive scan of counts_kept
+    dest_row: np.ndarray        # [T, k] int32, -1 = dropped
+    src_token: np.ndarray       # [S] int32, token of each permuted row
+
+
+def dispatch(idx: np.ndarray, N: int, cap: int) -> Dispatch:
+    """Group the (token, slot) assignments by expert.
+
+    Lecture29, "Top-k routing semantics" (rearrange tokens by expert, then
+    restore the order) and "Inference load balance" (an expert holds at most C
+    assignments; overflow is dropped).  Per expert, assignments are ranked by
+    token index -- a token picks an expert at most once, so the token alone
+    orders them, whatever the slot j -- and rank r is kept iff r < C.
+    cap <= 0 means no limit."""
+    T, k = idx.shape
+    counts_routed = np.zeros(N, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            counts_routed[idx[t, j]] += 1
+    limit = cap if cap > 0 else T * k
+    counts_kept = np.minimum(counts_routed, limit)
+    offsets = np.zeros(N + 1, dtype=np.int64)
+    for e in range(N):
+        offsets[e + 1] = offsets[e] + counts_kept[e]
+    seen = np.zeros(N, dtype=np.int64)
+    dest_row = np.full((T, k), -1, dtype=np.int64)
+    src_token = np.zeros(offsets[N], dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            r = seen[e]
+            seen[e] += 1
+            if r < limit:
+                dest_row[t, j] = offsets[e] + r
+                src_token[offsets[e] + r] = t
+    return Dispatch(counts_routed.astype(np.int32), counts_kept.astype(np.int32),
+                    offsets.astype(np.int32), dest_row.astype(np.int32), src_token.astype(np.int32))
+
+
+# --------------------------------------------------------------------------- experts
+def silu(a: np.ndarray) -> np.ndarray:
+    return a / (1.0 + np.exp(-a))
+
+
+def expert_ffn(xr: np.ndarray, W1: np.ndarray, W3: Optional[np.ndarray], W2: np.ndarray, act: str) -> np.ndarray:
+    """One expert on rows xr [m, d] (float64); W1, W3: [F, d]; W2: [d, F].
+
+    swiglu: W2 (SiLU(W1 x) * W3 x)   (Lecture29, "A dense Transformer layer")
+    relu:   W2 ReLU(W1 x)            (Shazeer et al. notes: one ReLU hidden layer)
+    The hidden activation stays in float64 (no rounding)."""
+    a = xr @ W1.T
+    if act == "swiglu":
+        h = silu(a) * (xr @ W3.T)
+    else:
+        h = np.maximum(a, 0.0)
+    return h @ W2.T
+
+
+# --------------------------------------------------------------------------- stats
+@dataclasses.dataclass
+class LoadStats:
+    f: np.ndarray        # [N] routed fraction
+    P: np.ndarray        # [N] mean router probability
+    aux: float           # N * sum f_i P_i
+    imbalance: float     # max_i n_i / (T k / N)
+    drop_rate: float     # 1 - kept / (T k)
+
+
+def router_probabilities(z: np.ndarray, gate: str) -> np.ndarray:
+    """p_i(t): the full N-way softmax of z, or s_i / sum_l s_l for the sigmoid gate."""
+    z64 = z.astype(np.float64)
+    if gate == "softmax":
+        e = np.exp(z64 - z64.max(axis=1, keepdims=True))
+        return e / e.sum(axis=1, keepdims=True)
+    s = sigmoid_affinity(z).astype(np.float64)
+    return s / s.sum(axis=1, keepdims=True)
+
+
+def load_stats(z: np.ndarray, gate: str, d: Dispatch, k: int) -> LoadStats:
+    """Switch balance quantities.  Chapter 19, 19.3.3 (f_i, P_i); CS336 lecture 4,
+    section 9 (loss = N sum_i f_i P_i); Lecture29, "Myth 3" (imbalance I)."""
+    T, N = z.shape
+    f = d.counts_routed.astype(np.float64) / (T * k)
+    P = router_probabilities(z, gate).mean(axis=0)
+    aux = N * float(np.sum(f * P))
+    imb = float(d.counts_routed.max()) / (T * k / N)
+    drop = 1.0 - float(d.offsets[N]) / (T * k)
+    return LoadStats(f, P, aux, imb, drop)
+
+
+# --------------------------------------------------------------------------- layer
+@dataclasses.dataclass
+class LayerResult:
+    z: np.ndarray            # [T, N] float32 logits
+    sel: np.ndarray          # [T, N] float32 selection scores
+    idx: np.ndarray          # [T, k] int32
+    w: np.ndarray            # [T, k] float64 gate weights
+    disp: Dispatch
+    out: np.ndarray          # [T, d] float64 (rows outside `tokens` are NaN)
+    y_sh: Optional[np.ndarray]
+    stats: LoadStats
+
+
+def layer_forward(inp, tokens: Optional[np.ndarray] = None, idx_override: Optional[np.ndarray] = None,
+                  cap: Optional[int] = None) -> LayerResult:
+    """The whole layer: route every token, dispatch, run the experts and combine.
+
+    `inp` carries the workload and its tensors (see the input module).
+    `tokens`: compute the output only for these token rows (routing, dispatch and
+    stats are always computed for all tokens, since capacity couples them).
+    `idx_override`: use this top-k instead of the oracle's own (gate weights are
+    still computed from the oracle's logits at those indices)."""
+    wl = inp.wl
+    dt = wl.dtype
+    x64 = widen(inp.x, dt)
+    z = router_logits(x64, inp.Wg, inp.logit_bias)
+    sel, s = selection_scores(z, wl.gate, inp.sel_bias)
+    idx = topk(sel, wl.k) if idx_override is None else np.asarray(idx_override, dtype=np.int32)
+    w = gate_weights(z, s, idx, wl.gate)
+    if cap is None:
+        cap = capacity(wl.capacity_factor, wl.T, wl.k, wl.N) if wl.capacity_factor > 0 else 0
+    disp = dispatch(idx, wl.N, cap)
+    stats = load_stats(z, wl.gate, disp, wl.k)
+
+    T = wl.T
+    want = np.arange(T) if tokens is None else np.asarray(tokens)
+    want_set = np.zeros(T, dtype=bool)
+    want_set[want] = True
+    out = np.full((T, wl.d), np.nan)
+    out[want] = 0.0
+    y_sh = None
+    if wl.shared_F:
+        # CS336 lecture 4, section 6: the shared expert runs for every token.
+        sw3 = widen(inp.sw3, dt) if inp.sw3 is not None else None
+        y_sh = np.full((T, wl.d), np.nan)
+        y_sh[want] = expert_ffn(x64[want], widen(inp.sw1, dt), sw3, widen(inp.sw2, dt), wl.act)
+        out[want] += y_sh[want]
+    # expert outputs for the kept rows that feed a wanted token
+    for e in range(wl.N):
+        rows = np.arange(disp.offsets[e], disp.offsets[e + 1])
+        rows = rows[want_set[disp.src_token[rows]]]
+        if rows.size == 0:
+            continue
+        W1 = widen(inp.w1[e], dt)
+        W3 = widen(inp.w3[e], dt) if inp.w3 is not None else None
+        W2 = widen(inp.w2[e], dt)
+        y = expert_ffn(x64[disp.src_token[rows]], W1, W3, W2, wl.act)
+        # combine: y_out[t] += g_tj * Expert_e(x_t)  (Lecture29, "Top-two routing")
+        for r, yr in zip(rows, y):
+            t = disp.src_token[r]
+            j = int(np.nonzero(idx[t] == e)[0][0])
+            out[t] += w[t, j] * yr
+    return LayerResult(z, sel, idx, w, disp, out, y_sh, stats)
+
+
+def dense_mask_forward(inp, cap: Optional[int] = None) -> np.ndarray:
+    """Second formulation, with no permutation: y[t] = y_sh[t] + sum_e G[t,e] FFN_e(x_t).
+
+    G[t,e] is the gate weight if expert e was selected for token t and that
+    assignment survived the capacity limit (counted in token order), else 0;
+    every expert runs on every token.  Lecture29, "Top-two routing"
+    (y = sum_{i=1..E} g_i(x) Expert_i(x), with g_i = 0 outside S_k)."""
+    wl = inp.wl
+    dt = wl.dtype
+    x64 = widen(inp.x, dt)
+    z = router_logits(x64, inp.Wg, inp.logit_bias)
+    sel, s = selection_scores(z, wl.gate, inp.sel_bias)
+    idx = topk(sel, wl.k)
+    w = gate_weights(z, s, idx, wl.gate)
+    if cap is None:
+        cap = capacity(wl.capacity_factor, wl.T, wl.k, wl.N) if wl.capacity_factor > 0 else 0
+    limit = cap if cap > 0 else wl.T * wl.k
+    G = np.zeros((wl.T, wl.N))
+    used = np.zeros(wl.N, dtype=np.int64)
+    for t in range(wl.T):
+        for j in range(wl.k):
+            e = idx[t, j]
+            if used[e] < limit:
+                G[t, e] = w[t, j]
+            used[e] += 1
+    y = np.zeros((wl.T, wl.d))
+    if wl.shared_F:
+        sw3 = widen(inp.sw3, dt) if inp.sw3 is not None else None
+        y += expert_ffn(x64, widen(inp.sw1, dt), sw3, widen(inp.sw2, dt), wl.act)
+    for e in range(wl.N):
+        W3 = widen(inp.w3[e], dt) if inp.w3 is not None else None
+        y += G[:, e:e + 1] * expert_ffn(x64, widen(inp.w1[e], dt), W3, widen(inp.w2[e], dt), wl.act)
+    return y

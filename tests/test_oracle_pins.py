@@ -1,0 +1,386 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix (no GPU).
+
+Each test pins one part of the oracle to something other than the oracle
+itself: an identity stated on the pages, a closed form, brute force on tiny
+inputs, or an invariant.  They are chosen so that a dropped term, a wrong sign,
+a wrong index or a transposed operand in the oracle fails at least one.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def tiny(T=24, d=16, N=6, k=2, F=32, act="swiglu", gate="softmax", dtype="bf16", shared_F=0,
+         capacity_factor=0.0, sel_bias_range=0.0, zipf_s=0.0, seed=7):
+    wl = synth.Workload("tiny", seed, T=T, d=d, N=N, k=k, F=F, act=act, gate=gate, dtype=dtype,
+                        shared_F=shared_F, capacity_factor=capacity_factor,
+                        sel_bias_range=sel_bias_range, zipf_s=zipf_s)
+    return synth.make_inputs(wl)
+
+
+# --------------------------------------------------------------------------- gate
+@pytest.mark.parametrize("N,k", [(8, 2), (64, 6), (256, 8), (5, 5)])
+def test_softmax_gate_equals_renormalised_full_softmax(N, k):
+    """Chapter 19, 19.3.2: softmax over the selected logits equals the full
+    softmax taken over all logits and renormalised over the top-k."""
+    rng = np.random.default_rng(N * 100 + k)
+    z = (rng.standard_normal((200, N)) * 3).astype(np.float32)
+    idx = oracle.topk(z, k)
+    w = oracle.gate_weights(z, None, idx, "softmax")
+    p = scipy.special.softmax(z.astype(np.float64), axis=1)
+    ps = np.take_along_axis(p, idx.astype(np.int64), axis=1)
+    ref = ps / ps.sum(axis=1, keepdims=True)
+    assert np.max(np.abs(w - ref)) < 1e-12
+    # the selected ones are the k largest probabilities
+    assert np.all(ps.min(axis=1) >= np.sort(p, axis=1)[:, -k] - 1e-15)
+
+
+def test_softmax_gate_two_expert_closed_form():
+    """Two selected logits a > b: g = (1/(1+e^{b-a}), 1/(1+e^{a-b}))."""
+    z = np.array([[0.25, 2.0, -1.0, 1.5]], dtype=np.float32)
+    idx = oracle.topk(z, 2)
+    assert idx.tolist() == [[1, 3]]
+    w = oracle.gate_weights(z, None, idx, "softmax")
+    a, b = 2.0, 1.5
+    assert abs(w[0, 0] - 1.0 / (1.0 + math.exp(b - a))) < 1e-15
+    assert abs(w[0, 1] - 1.0 / (1.0 + math.exp(a - b))) < 1e-15
+
+
+def _brute_force_topk(sel_row, k):
+    """The unique k-subset in which every chosen score beats every unchosen one,
+    equal scores going to the lower index; listed by (score desc, index asc)."""
+    N = len(sel_row)
+    found = []
+    for S in itertools.combinations(range(N), k):
+        rest = [u for u in range(N) if u not in S]
+        if all(sel_row[i] > sel_row[u] or (sel_row[i] == sel_row[u] and i < u) for i in S for u in rest):
+            found.append(S)
+    assert len(found) == 1
+    S = found[0]
+    return sorted(S, key=lambda i: (-float(sel_row[i]), i))
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 8])
+def test_topk_matches_brute_force_with_ties(N):
+    rng = np.random.default_rng(N)
+    # scores from a 3-value alphabet force many exact ties
+    sel = rng.choice(np.array([-1.0, 0.5, 2.0], dtype=np.float32), size=(60, N))
+    for k in range(1, N + 1):
+        idx = oracle.topk(sel, k)
+        for t in range(sel.shape[0]):
+            assert idx[t].tolist() == _brute_force_topk(sel[t], k)
+
+
+def test_topk_distinct_scores_brute_force():
+    rng = np.random.default_rng(3)
+    sel = rng.standard_normal((100, 7)).astype(np.float32)
+    for k in (1, 2, 4, 7):
+        idx = oracle.topk(sel, k)
+        for t in range(100):
+            assert idx[t].tolist() == _brute_force_topk(sel[t], k)
+
+
+# --------------------------------------------------------------------------- sigmoid gate
+def test_sigmoid_gate_properties():
+    """Chapter 19, 19.3.4 / CS336 lecture 4, section 9: the bias only steers the
+    choice; the mixing weights come from the raw affinities and sum to 1."""
+    inp = tiny(gate="sigmoid", N=8, k=3, sel_bias_range=0.05)
+    r = oracle.layer_forward(inp)
+    assert np.allclose(r.w.sum(axis=1), 1.0, atol=1e-14)
+    z64 = r.z.astype(np.float64)
+    s_ref = 1.0 / (1.0 + np.exp(-z64))                 # raw affinities
+    sel_ref = s_ref.astype(np.float32).astype(np.float64) + inp.sel_bias.astype(np.float64)
+    # selected set = top-k of s + b
+    for t in range(inp.wl.T):
+        chosen = set(r.idx[t].tolist())
+        order = sorted(range(8), key=lambda i: (-sel_ref[t, i], i))
+        assert chosen == set(order[:3])
+        ss = s_ref[t, r.idx[t]]
+        assert np.allclose(r.w[t], ss / ss.sum(), rtol=1e-6)
+
+
+def test_sigmoid_without_bias_selects_topk_of_logits():
+    """sigma is monotone, so with b = 0 the selection is the top-k of z."""
+    inp = tiny(gate="sigmoid", N=16, k=4)
+    r = oracle.layer_forward(inp)
+    idx_z = oracle.topk(r.z, 4)
+    # compare where the logit gap is clear of float32 sigmoid rounding
+    zs = np.sort(r.z, axis=1)[:, ::-1]
+    clear = (zs[:, 3] - zs[:, 4]) > 1e-4
+    assert np.array_equal(np.sort(r.idx[clear], 1), np.sort(idx_z[clear], 1))
+
+
+def test_sigmoid_bias_flips_selection_but_not_weights():
+    """A large bias on one expert forces it into every token's top-k, yet its
+    gate weight is its raw affinity's share, not the biased one."""
+    inp = tiny(gate="sigmoid", N=8, k=2)
+    inp.sel_bias = np.zeros(8, dtype=np.float32)
+    inp.sel_bias[5] = 10.0
+    r = oracle.layer_forward(inp)
+    assert np.all(r.idx[:, 0] == 5)
+    s = 1.0 / (1.0 + np.exp(-r.z.astype(np.float64)))
+    for t in range(inp.wl.T):
+        ss = s[t, r.idx[t]]
+        assert np.allclose(r.w[t], ss / ss.sum(), rtol=1e-6)
+        assert r.w[t, 0] < 0.99   # an unbiased share, nowhere near 1
+
+
+# --------------------------------------------------------------------------- experts
+def test_swiglu_and_relu_closed_form():
+    """d = F = 1: the expert is a scalar function.  Lecture29 (SwiGLU
+    W2(SiLU(W1 x) * W3 x)) and the Shazeer notes (one ReLU hidden layer)."""
+    x = np.array([[1.5]])
+    W1, W3, W2 = np.array([[0.8]]), np.array([[-2.0]]), np.array([[3.0]])
+    a = 0.8 * 1.5
+    expect = 3.0 * (a / (1.0 + math.exp(-a))) * (-2.0 * 1.5)
+    assert abs(oracle.expert_ffn(x, W1, W3, W2, "swiglu")[0, 0] - expect) < 1e-14
+    assert oracle.expert_ffn(x, W1, None, W2, "relu")[0, 0] == pytest.approx(3.0 * 1.2, abs=1e-15)
+    assert oracle.expert_ffn(-x, W1, None, W2, "relu")[0, 0] == 0.0
+    # SiLU(1) = 1 / (1 + e^-1)
+    assert abs(oracle.silu(np.array(1.0)) - 0.7310585786300049) < 1e-15
+
+
+def _loop_ffn(xr, W1, W3, W2, act):
+    """Dense FFN written with scalar loops (independent of the oracle's matmuls)."""
+    F, d = W1.shape
+    y = np.zeros(W2.shape[0])
+    for f in range(F):
+        a = sum(W1[f, i] * xr[i] for i in range(d))
+        if act == "swiglu":
+            u = sum(W3[f, i] * xr[i] for i in range(d))
+            h = a / (1.0 + math.exp(-a)) * u
+        else:
+            h = max(a, 0.0)
+        for o in range(W2.shape[0]):
+            y[o] += W2[o, f] * h
+    return y
+
+
+@pytest.mark.parametrize("act", ["swiglu", "relu"])
+def test_k_equals_N_identical_experts_is_dense_ffn(act):
+    """Lecture29, "Top-two routing": y = sum_i g_i Expert_i(x) with the g_i
+    summing to 1, so k = N identical experts give the dense FFN."""
+    inp = tiny(T=6, d=8, N=4, k=4, F=12, act=act)
+    for e in range(1, 4):
+        inp.w1[e] = inp.w1[0]
+        inp.w2[e] = inp.w2[0]
+        if inp.w3 is not None:
+            inp.w3[e] = inp.w3[0]
+    r = oracle.layer_forward(inp)
+    W1 = oracle.widen(inp.w1[0], "bf16")
+    W3 = oracle.widen(inp.w3[0], "bf16") if inp.w3 is not None else None
+    W2 = oracle.widen(inp.w2[0], "bf16")
+    x = oracle.widen(inp.x, "bf16")
+    for t in range(6):
+        ref = _loop_ffn(x[t], W1, W3, W2, act)
+        assert np.allclose(r.out[t], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_zero_input_gives_zero_output():
+    inp = tiny(shared_F=16)
+    inp.x[:] = 0
+    r = oracle.layer_forward(inp)
+    assert np.all(r.out == 0.0)
+
+
+# --------------------------------------------------------------------------- dispatch / capacity
+def test_capacity_formula_values():
+    """Lecture29, "Inference load balance": C = ceil(alpha T k / E)."""
+    with open(os.path.join(GOLDEN, "page_values.json")) as f:
+        g = json.load(f)
+    c = g["qwen3_skew_capacity"]
+    assert oracle.capacity(c["alpha"], c["T"], c["k"], c["N"]) == c["C"]
+    assert oracle.capacity(1.0, 10, 2, 3) == 7           # ceil(20/3)
+    assert oracle.capacity(1.0, 9, 2, 3) == 6            # exact, no round-up
+    assert oracle.capacity(0.5, 3, 1, 2) == 1            # ceil(0.75)
+    for (T, k, N) in [(16, 2, 8), (100, 3, 7), (4096, 2, 8), (16384, 8, 128)]:
+        # alpha >= N/k gives C >= T: no expert can overflow
+        assert oracle.capacity(N / k, T, k, N) >= T
+
+
+def _routing(T, N, k, rng, skew=0.0):
+    scores = rng.standard_normal((T, N)) + skew * np.linspace(2, -2, N)[None, :]
+    return oracle.topk(scores.astype(np.float32), k)
+
+
+@pytest.mark.parametrize("T,N,k,cap", [(50, 8, 2, 0), (200, 16, 4, 13), (333, 5, 5, 40), (64, 3, 1, 1),
+                                       (1, 4, 2, 0), (0, 4, 2, 0), (100, 8, 2, 1000)])
+def test_dispatch_invariants(T, N, k, cap):
+    """Chapter 19, 19.6.1: T k assignments in all; per expert at most C kept,
+    the first C in token order, the rest dropped (their branch contributes 0)."""
+    rng = np.random.default_rng(T + N + k)
+    idx = _routing(T, N, k, rng, skew=1.5).reshape(T, k)
+    d = oracle.dispatch(idx, N, cap)
+    assert int(d.counts_routed.sum()) == T * k
+    limit = cap if cap > 0 else T * k
+    assert np.array_equal(d.counts_kept, np.minimum(d.counts_routed, limit))
+    assert d.offsets[0] == 0 and np.array_equal(np.diff(d.offsets), d.counts_kept)
+    for e in range(N):
+        toks = [t for t in range(T) if e in idx[t].tolist()]        # token order
+        assert len(toks) == d.counts_routed[e]
+        kept = toks[:limit]
+        rows = list(range(d.offsets[e], d.offsets[e + 1]))
+        assert d.src_token[rows].tolist() == kept
+        for t in toks[limit:]:
+            j = idx[t].tolist().index(e)
+            assert d.dest_row[t, j] == -1
+    # dest_row and src_token are inverse maps on kept assignments
+    for t in range(T):
+        for j in range(k):
+            r = d.dest_row[t, j]
+            if r >= 0:
+                assert d.src_token[r] == t
+                assert d.offsets[idx[t, j]] <= r < d.offsets[idx[t, j] + 1]
+
+
+def test_no_drops_when_alpha_at_least_N_over_k():
+    rng = np.random.default_rng(11)
+    T, N, k = 300, 8, 2
+    idx = _routing(T, N, k, rng, skew=4.0)
+    cap = oracle.capacity(N / k, T, k, N)
+    d = oracle.dispatch(idx, N, cap)
+    assert np.all(d.dest_row >= 0)
+
+
+# --------------------------------------------------------------------------- whole layer
+CASES = [
+    dict(),
+    dict(act="relu", dtype="f32", N=8, k=2),
+    dict(gate="sigmoid", N=12, k=4, shared_F=24, sel_bias_range=0.05),
+    dict(N=8, k=3, capacity_factor=0.6, zipf_s=1.2, T=40),
+    dict(N=1, k=1),
+    dict(N=5, k=5, T=9),
+]
+
+
+@pytest.mark.parametrize("kw", CASES)
+def test_dense_mask_formulation_agrees(kw):
+    """The permuted layer (dispatch, expert groups, combine) equals the dense
+    per-token sum y = sum_e G[t,e] FFN_e(x_t) with G zero off the kept top-k."""
+    inp = tiny(**kw)
+    r = oracle.layer_forward(inp)
+    y = oracle.dense_mask_forward(inp)
+    scale = max(1.0, np.max(np.abs(y)))
+    assert np.max(np.abs(r.out - y)) <= 1e-12 * scale
+
+
+def test_dense_mask_on_the_tiny_fp32_workload():
+    inp = synth.make_inputs(synth.WORKLOADS["shazeer_tiny_f32"])
+    r = oracle.layer_forward(inp)
+    y = oracle.dense_mask_forward(inp)
+    assert np.max(np.abs(r.out - y)) <= 1e-12 * np.max(np.abs(y))
+
+
+def test_capacity_drop_contributes_zero():
+    """CS336 lecture 4, section 10: a dropped assignment's expert output is 0.
+    With C = 1, a token whose both experts were already taken gets 0."""
+    inp = tiny(T=30, N=4, k=2, capacity_factor=0.01)
+    r = oracle.layer_forward(inp)
+    assert oracle.capacity(0.01, 30, 2, 4) == 1
+    for t in range(30):
+        if np.all(r.disp.dest_row[t] < 0):
+            assert np.all(r.out[t] == 0.0)
+    assert r.disp.offsets[-1] == np.count_nonzero(r.disp.counts_routed)
+
+
+def test_expert_permutation_symmetry():
+    """Lecture29, "Myth 1": permuting the experts together with the router's
+    output channels leaves the layer's function unchanged."""
+    inp = tiny(N=7, k=3, T=30, shared_F=8)
+    r = oracle.layer_forward(inp)
+    perm = np.array([3, 0, 6, 1, 5, 2, 4])
+    inp2 = synth.LayerInputs(inp.wl, inp.x, inp.Wg[:, perm], inp.w1[perm], inp.w3[perm], inp.w2[perm],
+                             inp.sw1, inp.sw3, inp.sw2)
+    r2 = oracle.layer_forward(inp2)
+    assert np.max(np.abs(r.out - r2.out)) <= 1e-12 * np.max(np.abs(r.out))
+    # and the routing maps through the permutation
+    assert np.array_equal(perm[r2.idx], r.idx)
+
+
+def test_logit_bias_shift_invariance():
+    """Adding a constant to every logit changes neither top-k nor the softmax gate
+    (the Zipf skew's normalisation constant is irrelevant)."""
+    inp = tiny(N=16, k=4, zipf_s=1.2, T=64)
+    r = oracle.layer_forward(inp)
+    inp.logit_bias = (inp.logit_bias.astype(np.float64) + 3.0).astype(np.float32)
+    r2 = oracle.layer_forward(inp)
+    zs = np.sort(r.z, axis=1)[:, ::-1]
+    clear = (zs[:, 3] - zs[:, 4]) > 1e-4
+    assert np.array_equal(r.idx[clear], r2.idx[clear])
+    assert np.max(np.abs(r.w[clear] - r2.w[clear])) < 1e-5
+
+
+# --------------------------------------------------------------------------- stats
+def test_uniform_load_gives_aux_one():
+    """CS336 lecture 4, section 9: with uniform routing and uniform router
+    probabilities the loss N sum f_i P_i equals 1; imbalance is 1."""
+    T, N, k = 64, 8, 1
+    z = np.zeros((T, N), dtype=np.float32)
+    idx = (np.arange(T) % N).reshape(T, 1).astype(np.int32)
+    d = oracle.dispatch(idx, N, 0)
+    st = oracle.load_stats(z, "softmax", d, k)
+    assert st.aux == pytest.approx(1.0, abs=1e-14)
+    assert st.imbalance == pytest.approx(1.0)
+    assert st.drop_rate == 0.0
+    assert np.allclose(st.f, 1.0 / N) and np.allclose(st.P, 1.0 / N)
+
+
+def test_stats_sum_to_one_and_imbalance():
+    inp = tiny(N=8, k=2, T=200, zipf_s=1.2, capacity_factor=1.0)
+    r = oracle.layer_forward(inp)
+    st = r.stats
+    assert st.f.sum() == pytest.approx(1.0, abs=1e-14)
+    assert st.P.sum() == pytest.approx(1.0, abs=1e-12)
+    n = r.disp.counts_routed
+    assert st.imbalance == pytest.approx(n.max() / (200 * 2 / 8))
+    assert st.drop_rate == pytest.approx(1 - r.disp.counts_kept.sum() / 400)
+    # all mass on one expert: f = e_0, aux = N * P_0
+    z = np.zeros((10, 4), dtype=np.float32)
+    z[:, 0] = 50.0
+    d = oracle.dispatch(np.zeros((10, 1), dtype=np.int32), 4, 0)
+    st = oracle.load_stats(z, "softmax", d, 1)
+    assert st.aux == pytest.approx(4.0, rel=1e-12)
+    assert st.imbalance == pytest.approx(4.0)
+
+
+# --------------------------------------------------------------------------- workload shapes
+def test_workload_shapes_match_published_model_sizes():
+    """The expert shapes reproduce the pages' parameter counts."""
+    with open(os.path.join(GOLDEN, "page_values.json")) as f:
+        g = json.load(f)
+    W = synth.WORKLOADS
+    c1 = W["shazeer_tiny_f32"]
+    assert c1.d * c1.F + c1.F * c1.d == g["shazeer_expert_weights"]["value"]
+    for key, wname in [("mixtral", "mixtral_prefill"), ("dsv3", "dsv3_finegrained"), ("qwen3", "qwen3_skew_drop")]:
+        m = g["moe_layers_from_totals"][key]
+        wl = W[wname]
+        P_e = 3 * wl.d * wl.F
+        layers = (m["total"] - m["active"]) / ((wl.N - wl.k) * P_e)
+        assert abs(layers - m["layers"]) < 0.1, (key, layers)
+
+
+def test_logit_bias_closed_form_zipf_probabilities():
+    """With W_g = 0 the logits are the skew beta_i = log p_i, so the full softmax
+    P_i equals the Zipf popularity p_i exactly and top-k picks the k most
+    popular experts (CS336 lecture 4, section 9: P_i is the router's share)."""
+    inp = tiny(N=16, k=4, T=20, zipf_s=1.2)
+    inp.Wg[:] = 0.0
+    r = oracle.layer_forward(inp)
+    p = np.array([rk ** -1.2 for rk in range(1, 17)])
+    p /= p.sum()
+    beta = inp.logit_bias.astype(np.float64)
+    assert np.allclose(np.sort(np.exp(beta))[::-1], p, rtol=1e-6)
+    assert np.allclose(r.stats.P, np.exp(beta) / np.exp(beta).sum(), rtol=1e-6)
+    assert np.allclose(np.sort(r.stats.P)[::-1], p, rtol=1e-6)
+    top = sorted(range(16), key=lambda i: -beta[i])[:4]
+    assert np.all(r.idx == np.array(top)[None, :])
