@@ -1,0 +1,392 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse MoE FFN layer forward on B300.
+
+One step = one pass of the whole layer over one batch: router (logits, top-k,
+gate), dispatch, routed expert FFN (tcgen05 grouped GEMM), shared expert (if
+the workload has one), combine, and the per-expert load statistics.  Inputs
+and all expert weights are resident in HBM before the timed region.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun (N > 1) every rank runs an
+independent replica of the layer on its own GPU (the layer does not shard:
+replicas only); the time is the max over ranks and the value counts the tokens
+of all ranks.  ``--impl reference`` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer fwd tokens/s at Mixtral shape; % of BF16 tensor / HBM roofline"
+DEFAULT_WORKLOAD = "mixtral_prefill"
+
+
+# ----------------------------------------------------------------------------- accounting
+def layer_flops(wl, kept_rows: int) -> dict:
+    """Algorithmic FLOPs: router + kept assignments' experts + shared expert."""
+    mats = 3 if wl.act == "swiglu" else 2
+    router = 2.0 * wl.T * wl.d * wl.N
+    ffn = 2.0 * kept_rows * wl.d * wl.F * mats
+    shared = 2.0 * wl.T * wl.d * wl.shared_F * mats if wl.shared_F else 0.0
+    return {"router": router, "expert_ffn": ffn, "shared_ffn": shared, "total": router + ffn + shared}
+
+
+def layer_bytes(wl, touched_experts: int) -> float:
+    """Algorithmic bytes: weights of experts with kept rows, x once, out once, W_g."""
+    es = 2 if wl.dtype == "bf16" else 4
+    mats = 3 if wl.act == "swiglu" else 2
+    w = touched_experts * mats * wl.d * wl.F * es
+    sw = mats * wl.d * wl.shared_F * es if wl.shared_F else 0
+    return float(w + sw + 2 * wl.T * wl.d * es + wl.d * wl.N * 4)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        # under load: the upper half of the samples (the timed region dominates the window)
+        busy = sorted(sm)[len(sm) // 2:]
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group("gloo")
+    return dist
+
+
+def max_over_ranks(dist, v: float) -> float:
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, wl):
+    """The CPU oracle, as it stands, on a bounded sample of the same workload per step."""
+    import threadpoolctl
+
+    import oracle
+    inp = synth.make_inputs(wl)
+    sample = args.ref_sample
+    rng = np.random.default_rng(wl.seed)
+
+    def step():
+        toks = np.sort(rng.choice(wl.T, size=min(sample, wl.T), replace=False))
+        t0 = time.perf_counter()
+        oracle.layer_forward(inp, tokens=np.array([], dtype=np.int64))      # routing + dispatch + stats, all T
+        t1 = time.perf_counter()
+        oracle.layer_forward(inp, tokens=toks)                                # + experts on the sample
+        t2 = time.perf_counter()
+        ffn_per_token = max(0.0, (t2 - t1) - (t1 - t0)) / len(toks)
+        return (t1 - t0) + ffn_per_token * wl.T                               # extrapolated full-layer seconds
+
+    for _ in range(args.warmup):
+        step()
+    secs = [step() for _ in range(args.steps)]
+    per_step = float(np.mean(secs))
+    cores = max((p.get("num_threads", 1) for p in threadpoolctl.threadpool_info()), default=1)
+    value = wl.T / per_step
+    desc = (f"oracle (numpy float64): routing, dispatch and statistics on all {wl.T} tokens, expert FFN on "
+            f"{min(sample, wl.T)} sampled tokens per step, extrapolated linearly to {wl.T} tokens")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(wl, inp, budget_tokens: int):
+    import threadpoolctl
+
+    import oracle
+    toks = np.sort(np.random.default_rng(wl.seed + 1).choice(wl.T, size=min(budget_tokens, wl.T), replace=False))
+    t0 = time.perf_counter()
+    oracle.layer_forward(inp, tokens=np.array([], dtype=np.int64))
+    t1 = time.perf_counter()
+    oracle.layer_forward(inp, tokens=toks)
+    t2 = time.perf_counter()
+    per_token = max(0.0, (t2 - t1) - (t1 - t0)) / len(toks)
+    est = (t1 - t0) + per_token * wl.T
+    cores = max((p.get("num_threads", 1) for p in threadpoolctl.threadpool_info()), default=1)
+    return {"value": wl.T / est, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": (f"numpy float64 oracle: routing, dispatch and statistics on all {wl.T} tokens, expert FFN "
+                       f"on {len(toks)} sampled tokens, extrapolated linearly to {wl.T} tokens "
+                       f"({t2 - t0:.1f} s of CPU work)")}
+
+
+def config_of(wl):
+    return {"workload": wl.name, "T": wl.T, "d": wl.d, "N": wl.N, "k": wl.k, "ffn": wl.F, "act": wl.act,
+            "gate": wl.gate, "shared_ffn": wl.shared_F, "capacity_factor": wl.capacity_factor,
+            "l2": "no flush: inputs larger than L2 (every step streams all touched expert weights)"}
+
+
+# ----------------------------------------------------------------------------- our arm
+def _to_dev(a, dtype):
+    import torch
+    if a is None:
+        return None
+    if dtype == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def build_layer(moe, inp):
+    wl = inp.wl
+    cap = moe.moe_capacity(wl.capacity_factor, wl.T, wl.k, wl.N) if wl.capacity_factor > 0 else 0
+    cfg = moe.make_config(wl.T, wl.d, wl.N, wl.k, wl.F, wl.shared_F,
+                          moe.GATE_SIGMOID_BIAS if wl.gate == "sigmoid" else moe.GATE_SOFTMAX_TOPK,
+                          moe.ACT_SWIGLU if wl.act == "swiglu" else moe.ACT_RELU,
+                          moe.DTYPE_BF16 if wl.dtype == "bf16" else moe.DTYPE_F32, cap)
+    dt = wl.dtype
+    return moe.MoELayer(cfg, _to_dev(inp.Wg, "f32"), _to_dev(inp.w1, dt), _to_dev(inp.w3, dt), _to_dev(inp.w2, dt),
+                        _to_dev(inp.sw1, dt), _to_dev(inp.sw3, dt), _to_dev(inp.sw2, dt),
+                        _to_dev(inp.logit_bias, "f32"), _to_dev(inp.sel_bias, "f32"))
+
+
+def run_ours(args, wl, dist, rank, local):
+    import torch
+
+    import sparse_mixture_experts_62_b300 as moe
+
+    torch.cuda.set_device(local)
+    inp = synth.make_inputs(wl)
+    to_dev = _to_dev
+    layer = build_layer(moe, inp)
+    x = to_dev(inp.x, wl.dtype)
+    out = torch.empty((wl.T, wl.d), dtype=x.dtype, device="cuda")
+    cfg, ws, v = layer.cfg, layer.ws, layer.views()
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    stats = torch.zeros(2 * wl.N + 4, dtype=torch.float32, device="cuda")
+    has_shared = wl.shared_F > 0
+    stages = ["route", "dispatch", "expert_ffn"] + (["shared_ffn"] if has_shared else []) + ["combine", "load_stats"]
+
+    def step(ev=None):
+        # the launches of moe_layer_forward, stage by stage, + the statistics
+        rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
+        rec(0)
+        moe.moe_route(cfg, x, layer.Wg, layer.logit_bias, layer.sel_bias, v["logits"], v["topk_idx"], v["topk_w"],
+                      ws, s)
+        rec(1)
+        moe.moe_dispatch(cfg, v["topk_idx"], x, v["counts_routed"], v["counts_kept"], v["offsets"], v["dest_row"],
+                         v["src_token"], v["x_perm"], ws, s)
+        rec(2)
+        moe.moe_expert_ffn(cfg, v["x_perm"], v["offsets"], layer.w1, layer.w3, layer.w2, v["y_perm"], ws, s)
+        i = 3
+        if has_shared:
+            rec(i)
+            moe.moe_shared_ffn(cfg, x, layer.sw1, layer.sw3, layer.sw2, v["y_shared"], ws, s)
+            i += 1
+        rec(i)
+        moe.moe_combine(cfg, v["y_perm"], v["dest_row"], v["topk_w"], v["y_shared"] if has_shared else None, out, s)
+        rec(i + 1)
+        moe.moe_load_stats(cfg, v["logits"], v["counts_routed"], v["counts_kept"], stats[:wl.N],
+                           stats[wl.N:2 * wl.N], stats[2 * wl.N:2 * wl.N + 3], ws, s)
+        rec(i + 2)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if layer.device_status() != 0:
+        raise RuntimeError("device status not clean after warm-up")
+    nev = len(stages) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for k in range(args.steps):
+            step(evs[k])
+        end.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    stage_ms = {n: float(np.mean([evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps)]))
+                for j, n in enumerate(stages)}
+    t_max = max_over_ranks(dist, total_ms)
+    ms_per_step = t_max / args.steps
+    world = dist.get_world_size() if dist is not None else 1
+    value = wl.T * args.steps * world / (t_max / 1e3)
+
+    # routing facts of this run (for the algorithmic counts)
+    counts_kept = v["counts_kept"].cpu().numpy()
+    kept_rows = int(counts_kept.sum())
+    touched = int(np.count_nonzero(counts_kept))
+    fl = layer_flops(wl, kept_rows)
+    peaks, peak_src = measured_peaks()
+    ffn_s = stage_ms["expert_ffn"] / 1e3
+    achieved_tflops = fl["expert_ffn"] / ffn_s / 1e12
+    peak_tf = peaks["bf16_tflops"]
+    roof = {"bound": "tensor", "achieved": achieved_tflops, "peak": peak_tf, "unit": "TFLOP/s",
+            "frac": achieved_tflops / peak_tf, "traffic": None,
+            "kernel": "grouped_gemm_kernel (tcgen05), moe_expert_ffn: gate/up + down launches",
+            "peak_source": f"{peak_src} bf16_tflops (burst)"}
+    if wl.T <= 64:  # decode: the layer streams weights; HBM governs
+        byts = layer_bytes(wl, touched)
+        gbs = byts / (ms_per_step / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "whole layer step",
+                "peak_source": f"{peak_src} hbm_gbs"}
+
+    # end to end through the public API: pinned host x in, out + stats back, every step
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(out, device="cpu").pin_memory()
+    stats_host = torch.empty_like(stats, device="cpu").pin_memory()
+    x_dev = torch.empty_like(x)
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        layer.forward(x_dev, out)
+        f, P, summ = layer.load_stats()
+        out_host.copy_(out, non_blocking=True)
+        stats_host.copy_(layer._stats, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
+    e2e_val = wl.T * args.steps * world / (e2e_ms / 1e3)
+    h2d = x.numel() * x.element_size()
+    d2h = out.numel() * out.element_size() + stats.numel() * 4
+
+    launches_per_step = 2 + 4 + 2 + (2 if has_shared else 0) + 1 + 2
+    if rank == 0:
+        sys.stderr.write("per-stage ms: " + json.dumps({k: round(val, 4) for k, val in stage_ms.items()}) + "\n")
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic", "config": config_of(wl),
+                "roofline": roof,
+                "stage_ms": stage_ms,
+                "layer": {"flops": fl["total"], "tflops": fl["total"] / (ms_per_step / 1e3) / 1e12,
+                          "kept_rows": kept_rows, "touched_experts": touched,
+                          "algorithmic_bytes": layer_bytes(wl, touched)},
+                "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "gpu_launches": launches_per_step * args.steps,
+                "clocks": clk.summary()}
+        if args.cpu_baseline_tokens > 0:
+            line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_baseline_tokens)
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-baseline-tokens", type=int, default=16,
+                    help="tokens the oracle runs the expert FFN on for cpu_baseline (0 = skip)")
+    ap.add_argument("--ref-sample", type=int, default=4, help="tokens per reference-arm step")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, wl)
+        return
+    dist = init_dist(world)
+    run_ours(args, wl, dist, rank, local)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

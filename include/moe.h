@@ -1,0 +1,194 @@
+/*
+ * moe.h -- C ABI of the sparse token-choice Mixture-of-Experts FFN layer
+ * (forward pass) for NVIDIA B300 (sm_103a), library libmoe_b300.so.
+ *
+ * The layer (notation of the pages): for each token row x (length d),
+ *   z      = x . W_g (+ beta)                    router logits, float32, N experts
+ *   S_k(x) = the k experts with the largest selection score
+ *   g_i    = softmax of z over S_k      (MOE_GATE_SOFTMAX_TOPK), or
+ *            s_i / sum_{j in S_k} s_j with s = sigmoid(z), chosen on s + b
+ *                                               (MOE_GATE_SIGMOID_BIAS)
+ *   y      = sum_{i in S_k, kept} g_i Expert_i(x)  (+ SharedExpert(x))
+ *   Expert(x) = W2 (SiLU(W1 x) * W3 x)  (MOE_ACT_SWIGLU) or W2 ReLU(W1 x) (MOE_ACT_RELU)
+ * Sources: "Lecture29" (CS25 lecture 29 notes, Mixtral), sections "Top-two
+ * routing: from logits to weighted expert output", "A dense Transformer layer"
+ * (SwiGLU expert) and "Inference load balance" (capacity); "Chapter 19: MoE"
+ * (awesome-ai-roadmap) 19.3.2 (top-k softmax = renormalised full softmax),
+ * 19.3.3 (f_i, P_i), 19.3.4 (DeepSeek-V3 selection-only bias), 19.6.1
+ * (capacity, dropped overflow); "Stanford CS336 lecture 4: Mixture of Experts",
+ * sections 5, 6 (shared expert), 9 (N sum f_i P_i), 10 (dropped token -> zero
+ * expert output, residual passes), 11 (float32 router); Shazeer et al. 2017
+ * notes (ReLU expert, gate matrix d x n).
+ *
+ * Conventions (all entry points):
+ *  - Every tensor argument is a DEVICE pointer to caller-owned memory on the
+ *    current CUDA device; the library never allocates device memory.  Scratch
+ *    comes from a caller-provided workspace `ws` of moe_workspace_size() bytes
+ *    (256-byte aligned).  The workspace also holds the device status word.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work
+ *    is enqueued asynchronously on it; no call synchronises except
+ *    moe_get_device_status.  Results are deterministic: the same inputs give
+ *    bitwise identical outputs.
+ *  - Layouts are row-major:
+ *      x       [T, d]        activations, dtype cfg->dtype
+ *      Wg      [d, N]        float32 router weight (logits = x . Wg)
+ *      w1, w3  [N, F, d]     expert e's W1, W3 as F x d ("W1 x" maps d -> F)
+ *      w2      [N, d, F]     expert e's W2 as d x F
+ *      sw1, sw3 [Fs, d], sw2 [d, Fs]   the shared expert (Fs = cfg->shared_ffn)
+ *    bf16 tensors hold raw bfloat16 values (uint16 storage).
+ *  - Alignment: every pointer 16-byte aligned; d and ffn (and shared_ffn) a
+ *    multiple of 8 (bf16) or 4 (float32).  Otherwise MOE_ERR_UNSUPPORTED.
+ *  - Limits: 1 <= N <= 256, 1 <= k <= min(N, 8), T >= 0 (T = 0 is a no-op),
+ *    d, ffn <= 65536.  Otherwise MOE_ERR_UNSUPPORTED or MOE_ERR_INVALID_ARG.
+ *  - Errors: argument errors are returned synchronously and launch nothing.
+ *    Errors found on the device (non-finite logits, a pipeline wait that ran
+ *    past its time limit) are recorded in the workspace status word, read by
+ *    moe_get_device_status.  Kernels never trap.
+ *  - The output is the MoE branch only; the residual add is the caller's.
+ */
+#ifndef MOE_B300_H
+#define MOE_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null pointer, negative size, bad enum */
+  MOE_ERR_UNSUPPORTED = 2,  /* shape or alignment outside the limits above */
+  MOE_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+  MOE_ERR_NONFINITE = 4,    /* device: a router logit was NaN or infinite */
+  MOE_ERR_TIMEOUT = 5,      /* device: a pipeline wait exceeded its limit */
+  MOE_ERR_BOUNDS = 6        /* device: an index left its range */
+} moe_status;
+
+typedef enum { MOE_GATE_SOFTMAX_TOPK = 0, MOE_GATE_SIGMOID_BIAS = 1 } moe_gate;
+typedef enum { MOE_ACT_RELU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef struct {
+  int32_t T;          /* tokens */
+  int32_t d;          /* hidden size */
+  int32_t N;          /* routed experts */
+  int32_t k;          /* experts per token */
+  int32_t ffn;        /* routed expert hidden width F */
+  int32_t shared_ffn; /* shared expert hidden width, 0 = no shared expert */
+  int32_t gate;       /* moe_gate */
+  int32_t act;        /* moe_act */
+  int32_t dtype;      /* moe_dtype of x, weights, out */
+  int32_t capacity;   /* per-expert capacity C, <= 0 = unlimited (see moe_capacity) */
+} moe_config;
+
+/* Byte offsets of the intermediates inside the workspace (for inspection after
+ * moe_layer_forward; every offset is 256-byte aligned). */
+typedef struct {
+  size_t status;         /* int32 status word */
+  size_t logits;         /* float [T, N] */
+  size_t topk_idx;       /* int32 [T, k] */
+  size_t topk_w;         /* float [T, k] */
+  size_t counts_routed;  /* int32 [N] */
+  size_t counts_kept;    /* int32 [N] */
+  size_t offsets;        /* int32 [N + 1] */
+  size_t dest_row;       /* int32 [T, k], -1 = dropped */
+  size_t src_token;      /* int32 [T * k] */
+  size_t x_perm;         /* dtype [T * k, d] */
+  size_t h;              /* dtype [T * k, F]  expert hidden activations */
+  size_t y_perm;         /* bf16 or float [T * k, d]  expert outputs */
+  size_t h_shared;       /* dtype [T, Fs] */
+  size_t y_shared;       /* bf16 or float [T, d] */
+  size_t scratch;        /* internal scratch */
+  size_t total;          /* = moe_workspace_size */
+} moe_ws_layout;
+
+/* Human-readable name of a status code (static string, never NULL). */
+MOE_API const char *moe_status_string(int status);
+
+/* C = ceil(alpha * T * k / N) computed exactly, alpha taken as the exact value
+ * of the double (Lecture29, "Inference load balance": C = ceil(alpha T k / E);
+ * Chapter 19, 19.6.1).  alpha > 0, T >= 0, k >= 1, N >= 1; C written to *C. */
+MOE_API int moe_capacity(double alpha, int32_t T, int32_t k, int32_t N, int32_t *C);
+
+/* Workspace bytes needed by any call below for this config. */
+MOE_API int moe_workspace_size(const moe_config *cfg, size_t *bytes);
+MOE_API int moe_workspace_layout(const moe_config *cfg, moe_ws_layout *layout);
+
+/* Router: logits z = x . Wg (+ logit_bias), top-k with ties to the lower expert
+ * index, and the gate weights (Lecture29 "Top-two routing"; Chapter 19, 19.3.2
+ * and 19.3.4).  logit_bias [N] (float, may be NULL) is added to every logit;
+ * sel_bias [N] (float, sigmoid gate only, may be NULL) shifts the selection
+ * score s + b but not the weights.  Outputs: logits [T, N] float, topk_idx
+ * [T, k] int32 ordered by (selection score desc, index asc), topk_w [T, k]
+ * float (sum to 1 per token).  The sigmoid s is fl32(1/(1+exp(-z))) evaluated
+ * in double.  Non-finite logits set MOE_ERR_NONFINITE on the device. */
+MOE_API int moe_route(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias,
+              const float *sel_bias, float *logits, int32_t *topk_idx, float *topk_w, void *ws,
+              void *stream);
+
+/* Dispatch (Lecture29, "Top-k routing semantics"; "Inference load balance"):
+ * counts_routed[e] = assignments to e; counts_kept[e] = min(counts_routed, C);
+ * offsets [N+1] = exclusive scan of counts_kept; per expert the first C
+ * assignments in ascending token order are kept, at rows offsets[e] + rank;
+ * dest_row[t, j] = that row or -1 (dropped); src_token[row] = t; and
+ * x_perm[row, :] = x[t, :].  x_perm needs room for T * k rows; rows at or
+ * beyond offsets[N] are left untouched. */
+MOE_API int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x, int32_t *counts_routed,
+                 int32_t *counts_kept, int32_t *offsets, int32_t *dest_row, int32_t *src_token,
+                 void *x_perm, void *ws, void *stream);
+
+/* Routed experts over the permuted rows: for each expert e, rows
+ * [offsets[e], offsets[e+1]) of x_perm go through Expert_e; results in y_perm
+ * (same rows).  y_perm is bf16 for bf16 configs, float for float32 configs.
+ * The hidden activations (bf16 / float) live in the workspace. */
+MOE_API int moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const void *w1,
+                   const void *w3, const void *w2, void *y_perm, void *ws, void *stream);
+
+/* The always-on shared expert on every token (CS336 lecture 4, section 6):
+ * y_shared [T, d] (bf16 / float) = SharedExpert(x).  Needs cfg->shared_ffn > 0. */
+MOE_API int moe_shared_ffn(const moe_config *cfg, const void *x, const void *sw1, const void *sw3,
+                   const void *sw2, void *y_shared, void *ws, void *stream);
+
+/* Combine (Lecture29, "Top-two routing": y = sum_i g_i Expert_i(x)):
+ * out[t] = y_shared[t] + sum_{j: dest_row[t,j] >= 0} topk_w[t,j] * y_perm[dest_row[t,j]],
+ * accumulated in float32 in slot order j = 0..k-1.  y_shared may be NULL.
+ * out [T, d] has the config dtype. */
+MOE_API int moe_combine(const moe_config *cfg, const void *y_perm, const int32_t *dest_row, const float *topk_w,
+                const void *y_shared, void *out, void *stream);
+
+/* The whole layer: route, dispatch, routed experts, shared expert (if
+ * cfg->shared_ffn > 0, sw1/sw3/sw2 non-NULL), combine.  Intermediates stay in
+ * the workspace at the offsets of moe_workspace_layout. */
+MOE_API int moe_layer_forward(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias,
+                      const float *sel_bias, const void *w1, const void *w3, const void *w2,
+                      const void *sw1, const void *sw3, const void *sw2, void *out, void *ws,
+                      void *stream);
+
+/* Switch load statistics (Chapter 19, 19.3.3; CS336 lecture 4, section 9;
+ * Lecture29, "Myth 3"): f[e] = counts_routed[e] / (T k); P[e] = mean over
+ * tokens of the router probability p_e(t) (full softmax of the logits, or
+ * s_e / sum_l s_l for the sigmoid gate); summary[0] = N sum_e f_e P_e,
+ * summary[1] = imbalance max_e counts_routed / (T k / N), summary[2] = drop
+ * rate 1 - sum(counts_kept) / (T k).  All float device pointers; the per-chunk
+ * partial sums use the workspace scratch. */
+MOE_API int moe_load_stats(const moe_config *cfg, const float *logits, const int32_t *counts_routed,
+                   const int32_t *counts_kept, float *f, float *P, float *summary, void *ws, void *stream);
+
+/* Synchronises `stream`, reads and clears the workspace status word, and
+ * writes the first device-side error code found (MOE_OK if none) to *status.
+ * Returns MOE_ERR_CUDA if the stream itself reports an error. */
+MOE_API int moe_get_device_status(void *ws, void *stream, int *status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_B300_H */

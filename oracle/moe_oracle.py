@@ -191,6 +191,22 @@ def expert_ffn(xr: np.ndarray, W1: np.ndarray, W3: Optional[np.ndarray], W2: np.
     return h @ W2.T
 
 
+def combine(y_rows: np.ndarray, dest_row: np.ndarray, w: np.ndarray, y_shared: Optional[np.ndarray]) -> np.ndarray:
+    """out[t] = y_shared[t] + sum over kept slots j of w[t, j] * y_rows[dest_row[t, j]].
+
+    Lecture29, "Top-two routing" (y = sum_i g_i Expert_i(x)) and "Top-k routing
+    semantics" (restore the token order); CS336 lecture 4, section 10 (a dropped
+    slot, dest_row = -1, adds nothing)."""
+    T, k = dest_row.shape
+    out = np.zeros((T, y_rows.shape[1])) if y_shared is None else np.array(y_shared, dtype=np.float64)
+    for t in range(T):
+        for j in range(k):
+            r = dest_row[t, j]
+            if r >= 0:
+                out[t] += w[t, j] * y_rows[r]
+    return out
+
+
 # --------------------------------------------------------------------------- stats
 @dataclasses.dataclass
 class LoadStats:

@@ -1,0 +1,175 @@
+"""Python binding of libmoe_b300: the sparse token-choice MoE FFN layer forward on B300.
+
+Argument marshalling only.  Every step of the layer runs in the CUDA kernels of
+libmoe_b300.so (built in-tree by ``python -m sparse_mixture_experts_62_b300.build``);
+importing this package without that library raises ImportError -- there is no
+other implementation to fall back to.  PyTorch supplies device memory and
+streams: tensor arguments are passed to the C ABI as raw device pointers.
+
+Functions carry the C names (see include/moe.h for layouts and semantics):
+moe_route, moe_dispatch, moe_expert_ffn, moe_shared_ffn, moe_combine,
+moe_layer_forward, moe_load_stats, moe_capacity, moe_workspace_size,
+moe_workspace_layout, moe_get_device_status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT, \
+    MOE_ERR_BOUNDS = range(7)
+GATE_SOFTMAX_TOPK, GATE_SIGMOID_BIAS = 0, 1
+ACT_RELU, ACT_SWIGLU = 0, 1
+DTYPE_F32, DTYPE_BF16 = 0, 1
+
+EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_workspace_layout", "moe_route",
+           "moe_dispatch", "moe_expert_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
+           "moe_load_stats", "moe_get_device_status")
+
+
+class MoeConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("T", "d", "N", "k", "ffn", "shared_ffn", "gate", "act", "dtype", "capacity")]
+
+
+class MoeWsLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("status", "logits", "topk_idx", "topk_w", "counts_routed", "counts_kept", "offsets", "dest_row",
+                 "src_token", "x_perm", "h", "y_perm", "h_shared", "y_shared", "scratch", "total")]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+        self.code = code
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m sparse_mixture_experts_62_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.c_void_p
+    C = ctypes.POINTER(MoeConfig)
+    lib.moe_status_string.argtypes = [ctypes.c_int]
+    lib.moe_status_string.restype = ctypes.c_char_p
+    sig = {
+        "moe_capacity": [ctypes.c_double, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
+        "moe_workspace_size": [C, ctypes.POINTER(ctypes.c_size_t)],
+        "moe_workspace_layout": [C, ctypes.POINTER(MoeWsLayout)],
+        "moe_route": [C, P, P, P, P, P, P, P, P, P],
+        "moe_dispatch": [C, P, P, P, P, P, P, P, P, P, P],
+        "moe_expert_ffn": [C, P, P, P, P, P, P, P, P],
+        "moe_shared_ffn": [C, P, P, P, P, P, P, P],
+        "moe_combine": [C, P, P, P, P, P, P],
+        "moe_layer_forward": [C, P, P, P, P, P, P, P, P, P, P, P, P, P],
+        "moe_load_stats": [C, P, P, P, P, P, P, P, P],
+        "moe_get_device_status": [P, P, ctypes.POINTER(ctypes.c_int)],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    return lib
+
+
+_lib = _load()
+
+
+def status_string(code: int) -> str:
+    return _lib.moe_status_string(int(code)).decode()
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code: int, where: str):
+    if code != MOE_OK:
+        raise MoeError(code, where)
+
+
+def make_config(T, d, N, k, ffn, shared_ffn=0, gate=GATE_SOFTMAX_TOPK, act=ACT_SWIGLU, dtype=DTYPE_BF16,
+                capacity=0) -> MoeConfig:
+    return MoeConfig(T, d, N, k, ffn, shared_ffn, gate, act, dtype, capacity)
+
+
+def moe_capacity(alpha: float, T: int, k: int, N: int) -> int:
+    c = ctypes.c_int32(0)
+    _check(_lib.moe_capacity(float(alpha), T, k, N, ctypes.byref(c)), "moe_capacity")
+    return c.value
+
+
+def moe_workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def moe_workspace_layout(cfg: MoeConfig) -> MoeWsLayout:
+    L = MoeWsLayout()
+    _check(_lib.moe_workspace_layout(ctypes.byref(cfg), ctypes.byref(L)), "moe_workspace_layout")
+    return L
+
+
+def moe_route(cfg, x, Wg, logit_bias, sel_bias, logits, topk_idx, topk_w, ws, stream=None):
+    _check(_lib.moe_route(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(logit_bias), _ptr(sel_bias), _ptr(logits),
+                          _ptr(topk_idx), _ptr(topk_w), _ptr(ws), _stream(stream)), "moe_route")
+
+
+def moe_dispatch(cfg, topk_idx, x, counts_routed, counts_kept, offsets, dest_row, src_token, x_perm, ws,
+                 stream=None):
+    _check(_lib.moe_dispatch(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts_routed), _ptr(counts_kept),
+                             _ptr(offsets), _ptr(dest_row), _ptr(src_token), _ptr(x_perm), _ptr(ws),
+                             _stream(stream)), "moe_dispatch")
+
+
+def moe_expert_ffn(cfg, x_perm, offsets, w1, w3, w2, y_perm, ws, stream=None):
+    _check(_lib.moe_expert_ffn(ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(w1), _ptr(w3), _ptr(w2),
+                               _ptr(y_perm), _ptr(ws), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_shared_ffn(cfg, x, sw1, sw3, sw2, y_shared, ws, stream=None):
+    _check(_lib.moe_shared_ffn(ctypes.byref(cfg), _ptr(x), _ptr(sw1), _ptr(sw3), _ptr(sw2), _ptr(y_shared),
+                               _ptr(ws), _stream(stream)), "moe_shared_ffn")
+
+
+def moe_combine(cfg, y_perm, dest_row, topk_w, y_shared, out, stream=None):
+    _check(_lib.moe_combine(ctypes.byref(cfg), _ptr(y_perm), _ptr(dest_row), _ptr(topk_w), _ptr(y_shared),
+                            _ptr(out), _stream(stream)), "moe_combine")
+
+
+def moe_layer_forward(cfg, x, Wg, logit_bias, sel_bias, w1, w3, w2, sw1, sw3, sw2, out, ws, stream=None):
+    _check(_lib.moe_layer_forward(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(logit_bias), _ptr(sel_bias), _ptr(w1),
+                                  _ptr(w3), _ptr(w2), _ptr(sw1), _ptr(sw3), _ptr(sw2), _ptr(out), _ptr(ws),
+                                  _stream(stream)), "moe_layer_forward")
+
+
+def moe_load_stats(cfg, logits, counts_routed, counts_kept, f, P, summary, ws, stream=None):
+    _check(_lib.moe_load_stats(ctypes.byref(cfg), _ptr(logits), _ptr(counts_routed), _ptr(counts_kept), _ptr(f),
+                               _ptr(P), _ptr(summary), _ptr(ws), _stream(stream)), "moe_load_stats")
+
+
+def moe_get_device_status(ws, stream=None) -> int:
+    st = ctypes.c_int(0)
+    _check(_lib.moe_get_device_status(_ptr(ws), _stream(stream), ctypes.byref(st)), "moe_get_device_status")
+    return st.value
+
+
+from .layer import MoELayer  # noqa: E402,F401

@@ -1,0 +1,334 @@
+// C ABI of libmoe_b300: argument checks, workspace layout and the order of the
+// launches.  Every function returns a moe_status; argument errors launch nothing.
+#include <mutex>
+#include <string.h>
+#include <vector>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+
+int device_sm_count(int device) {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  if (device < 0) return -1;
+  if ((int)cache.size() <= device) cache.resize(device + 1, 0);
+  if (cache[device] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return -1;
+    cache[device] = n;
+  }
+  return cache[device];
+}
+
+namespace {
+
+inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+inline bool is_bf16(const moe_config *c) { return c->dtype == MOE_BF16; }
+inline size_t esize(const moe_config *c) { return is_bf16(c) ? 2 : 4; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_config(const moe_config *c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->d < 1 || c->N < 1 || c->k < 1 || c->ffn < 1 || c->shared_ffn < 0) return MOE_ERR_INVALID_ARG;
+  if (c->gate != MOE_GATE_SOFTMAX_TOPK && c->gate != MOE_GATE_SIGMOID_BIAS) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->N > 256 || c->k > 8 || c->k > c->N) return MOE_ERR_UNSUPPORTED;
+  if (c->d > 65536 || c->ffn > 65536 || c->shared_ffn > 65536) return MOE_ERR_UNSUPPORTED;
+  const int q = is_bf16(c) ? 8 : 4;  // 16-byte rows
+  if (c->d % q || c->ffn % q || c->shared_ffn % q) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->T * c->k >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int layout(const moe_config *c, moe_ws_layout *L) {
+  const size_t T = (size_t)c->T, N = (size_t)c->N, k = (size_t)c->k, d = (size_t)c->d, F = (size_t)c->ffn;
+  const size_t Fs = (size_t)c->shared_ffn, es = esize(c);
+  const size_t rows = T * k;
+  const size_t nch_d = (T + kDispatchChunk - 1) / kDispatchChunk;
+  const size_t nch_s = (T + kStatsChunk - 1) / kStatsChunk;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + (bytes ? bytes : 1));
+    return at;
+  };
+  L->status = take(4);
+  L->logits = take(T * N * 4);
+  L->topk_idx = take(rows * 4);
+  L->topk_w = take(rows * 4);
+  L->counts_routed = take(N * 4);
+  L->counts_kept = take(N * 4);
+  L->offsets = take((N + 1) * 4);
+  L->dest_row = take(rows * 4);
+  L->src_token = take(rows * 4);
+  L->x_perm = take(rows * d * es);
+  L->h = take(rows * F * es);
+  L->y_perm = take(rows * d * es);
+  L->h_shared = take(Fs ? T * Fs * es : 0);
+  L->y_shared = take(Fs ? T * d * es : 0);
+  L->scratch = take(2 * nch_d * N * 4 + nch_s * N * 4);
+  L->total = o;
+  return MOE_OK;
+}
+
+struct Ws {
+  moe_ws_layout L;
+  uint8_t *base;
+  template <typename P>
+  P *at(size_t off) const {
+    return reinterpret_cast<P *>(base + off);
+  }
+  int *status() const { return at<int>(L.status); }
+  int32_t *hist() const { return at<int32_t>(L.scratch); }
+  int32_t *chunk_base(const moe_config *c) const {
+    const size_t nch = ((size_t)c->T + kDispatchChunk - 1) / kDispatchChunk;
+    return at<int32_t>(L.scratch + nch * c->N * 4);
+  }
+  float *stats_partial(const moe_config *c) const {
+    const size_t nch = ((size_t)c->T + kDispatchChunk - 1) / kDispatchChunk;
+    return at<float>(L.scratch + 2 * nch * c->N * 4);
+  }
+};
+
+int make_ws(const moe_config *c, void *ws, Ws *w) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255)) return MOE_ERR_INVALID_ARG;
+  layout(c, &w->L);
+  w->base = static_cast<uint8_t *>(ws);
+  return MOE_OK;
+}
+
+#define MOE_TRY(x)        \
+  do {                    \
+    const int rc_ = (x);  \
+    if (rc_) return rc_;  \
+  } while (0)
+
+int ffn_routed(const moe_config *c, const void *x_perm, const int32_t *offsets, const void *w1, const void *w3,
+               const void *w2, void *h, void *y_perm, int *status, cudaStream_t s) {
+  const int64_t rows = (int64_t)c->T * c->k;
+  const int mode1 = c->act == MOE_ACT_SWIGLU ? 0 : 1;
+  if (is_bf16(c)) {
+    MOE_TRY(tc_grouped_gemm(mode1, x_perm, rows, c->d, w1, w3, (int64_t)c->N * c->ffn, c->ffn, offsets, c->N, 0,
+                            c->ffn, h, status, s));
+    MOE_TRY(tc_grouped_gemm(2, h, rows, c->ffn, w2, nullptr, (int64_t)c->N * c->d, c->d, offsets, c->N, 0, c->d,
+                            y_perm, status, s));
+  } else {
+    MOE_TRY(simt_grouped_gemm(mode1, false, x_perm, rows, c->d, w1, w3, c->ffn, offsets, c->N, 0, c->ffn, h, s));
+    MOE_TRY(simt_grouped_gemm(2, false, h, rows, c->ffn, w2, nullptr, c->d, offsets, c->N, 0, c->d, y_perm, s));
+  }
+  return MOE_OK;
+}
+
+int ffn_shared(const moe_config *c, const void *x, const void *sw1, const void *sw3, const void *sw2, void *h,
+               void *y, int *status, cudaStream_t s) {
+  const int mode1 = c->act == MOE_ACT_SWIGLU ? 0 : 1;
+  const int Fs = c->shared_ffn;
+  if (is_bf16(c)) {
+    MOE_TRY(tc_grouped_gemm(mode1, x, c->T, c->d, sw1, sw3, Fs, Fs, nullptr, 1, c->T, Fs, h, status, s));
+    MOE_TRY(tc_grouped_gemm(2, h, c->T, Fs, sw2, nullptr, c->d, c->d, nullptr, 1, c->T, c->d, y, status, s));
+  } else {
+    MOE_TRY(simt_grouped_gemm(mode1, false, x, c->T, c->d, sw1, sw3, Fs, nullptr, 1, c->T, Fs, h, s));
+    MOE_TRY(simt_grouped_gemm(2, false, h, c->T, Fs, sw2, nullptr, c->d, nullptr, 1, c->T, c->d, y, s));
+  }
+  return MOE_OK;
+}
+
+bool weights_ok(const moe_config *c, const void *w1, const void *w3, const void *w2) {
+  if (!w1 || !w2 || !aligned16(w1) || !aligned16(w2)) return false;
+  if (c->act == MOE_ACT_SWIGLU && (!w3 || !aligned16(w3))) return false;
+  return true;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_NONFINITE: return "non-finite router logit";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_BOUNDS: return "index out of range";
+    default: return "unknown status";
+  }
+}
+
+int moe_capacity(double alpha, int32_t T, int32_t k, int32_t N, int32_t *C) {
+  if (!C || !(alpha > 0.0) || alpha > 1e9 || T < 0 || k < 1 || N < 1) return MOE_ERR_INVALID_ARG;
+  // alpha = m * 2^e exactly, m a 53-bit integer
+  int e = 0;
+  const double fr = frexp(alpha, &e);        // alpha = fr * 2^e, fr in [0.5, 1)
+  const int64_t m = (int64_t)ldexp(fr, 53);  // exact
+  e -= 53;
+  // C = ceil(m * T * k * 2^e / N)
+  __int128 num = (__int128)m * T * k;
+  __int128 den = N;
+  if (e >= 0) {
+    if (e > 60) return MOE_ERR_UNSUPPORTED;
+    num <<= e;
+  } else {
+    if (-e > 100) return MOE_ERR_UNSUPPORTED;
+    den <<= -e;
+  }
+  const __int128 q = (num + den - 1) / den;
+  if (q > 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+  *C = (int32_t)q;
+  return MOE_OK;
+}
+
+int moe_workspace_layout(const moe_config *cfg, moe_ws_layout *out) {
+  MOE_TRY(check_config(cfg));
+  if (!out) return MOE_ERR_INVALID_ARG;
+  return layout(cfg, out);
+}
+
+int moe_workspace_size(const moe_config *cfg, size_t *bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  moe_ws_layout L;
+  MOE_TRY(moe_workspace_layout(cfg, &L));
+  *bytes = L.total;
+  return MOE_OK;
+}
+
+int moe_route(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias, const float *sel_bias,
+              float *logits, int32_t *topk_idx, float *topk_w, void *ws, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (!x || !Wg || !logits || !topk_idx || !topk_w || !aligned16(x)) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  MOE_TRY(make_ws(cfg, ws, &w));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_TRY(launch_router_logits(x, is_bf16(cfg), Wg, logit_bias, cfg->T, cfg->d, cfg->N, logits, s));
+  return launch_router_topk(logits, cfg->gate == MOE_GATE_SIGMOID_BIAS ? sel_bias : nullptr, cfg->T, cfg->N, cfg->k,
+                            cfg->gate, topk_idx, topk_w, w.status(), s);
+}
+
+int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x, int32_t *counts_routed,
+                 int32_t *counts_kept, int32_t *offsets, int32_t *dest_row, int32_t *src_token, void *x_perm,
+                 void *ws, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (!counts_routed || !counts_kept || !offsets) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  MOE_TRY(make_ws(cfg, ws, &w));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cfg->T > 0 && (!topk_idx || !x || !dest_row || !src_token || !x_perm || !aligned16(x) || !aligned16(x_perm)))
+    return MOE_ERR_INVALID_ARG;
+  MOE_TRY(launch_dispatch(topk_idx, cfg->T, cfg->k, cfg->N, cfg->capacity, w.hist(), w.chunk_base(cfg), counts_routed,
+                          counts_kept, offsets, dest_row, src_token, w.status(), s));
+  if (cfg->T == 0) return MOE_OK;
+  return launch_gather_rows(x, src_token, offsets + cfg->N, (int64_t)cfg->T * cfg->k, (int)(cfg->d * esize(cfg)),
+                            x_perm, s);
+}
+
+int moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const void *w1, const void *w3,
+                   const void *w2, void *y_perm, void *ws, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (!x_perm || !offsets || !y_perm || !aligned16(x_perm) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(cfg, w1, w3, w2)) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  MOE_TRY(make_ws(cfg, ws, &w));
+  return ffn_routed(cfg, x_perm, offsets, w1, w3, w2, w.at<void>(w.L.h), y_perm, w.status(),
+                    static_cast<cudaStream_t>(stream));
+}
+
+int moe_shared_ffn(const moe_config *cfg, const void *x, const void *sw1, const void *sw3, const void *sw2,
+                   void *y_shared, void *ws, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->shared_ffn <= 0) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  if (!x || !y_shared || !aligned16(x) || !aligned16(y_shared) || !weights_ok(cfg, sw1, sw3, sw2))
+    return MOE_ERR_INVALID_ARG;
+  Ws w;
+  MOE_TRY(make_ws(cfg, ws, &w));
+  return ffn_shared(cfg, x, sw1, sw3, sw2, w.at<void>(w.L.h_shared), y_shared, w.status(),
+                    static_cast<cudaStream_t>(stream));
+}
+
+int moe_combine(const moe_config *cfg, const void *y_perm, const int32_t *dest_row, const float *topk_w,
+                const void *y_shared, void *out, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (!y_perm || !dest_row || !topk_w || !out || !aligned16(y_perm) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (y_shared && !aligned16(y_shared)) return MOE_ERR_INVALID_ARG;
+  return launch_combine(is_bf16(cfg), y_perm, dest_row, topk_w, y_shared, out, cfg->T, cfg->d, cfg->k,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int moe_layer_forward(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias,
+                      const float *sel_bias, const void *w1, const void *w3, const void *w2, const void *sw1,
+                      const void *sw3, const void *sw2, void *out, void *ws, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (!x || !Wg || !out || !aligned16(x) || !aligned16(out) || !weights_ok(cfg, w1, w3, w2)) return MOE_ERR_INVALID_ARG;
+  const bool shared = cfg->shared_ffn > 0;
+  if (shared && !weights_ok(cfg, sw1, sw3, sw2)) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  MOE_TRY(make_ws(cfg, ws, &w));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const moe_ws_layout &L = w.L;
+  float *logits = w.at<float>(L.logits);
+  int32_t *idx = w.at<int32_t>(L.topk_idx);
+  float *gw = w.at<float>(L.topk_w);
+  int32_t *offsets = w.at<int32_t>(L.offsets);
+  int32_t *dest_row = w.at<int32_t>(L.dest_row);
+  int32_t *src_token = w.at<int32_t>(L.src_token);
+  void *x_perm = w.at<void>(L.x_perm);
+  void *y_perm = w.at<void>(L.y_perm);
+  MOE_TRY(launch_router_logits(x, is_bf16(cfg), Wg, logit_bias, cfg->T, cfg->d, cfg->N, logits, s));
+  MOE_TRY(launch_router_topk(logits, cfg->gate == MOE_GATE_SIGMOID_BIAS ? sel_bias : nullptr, cfg->T, cfg->N, cfg->k,
+                             cfg->gate, idx, gw, w.status(), s));
+  MOE_TRY(launch_dispatch(idx, cfg->T, cfg->k, cfg->N, cfg->capacity, w.hist(), w.chunk_base(cfg),
+                          w.at<int32_t>(L.counts_routed), w.at<int32_t>(L.counts_kept), offsets, dest_row, src_token,
+                          w.status(), s));
+  MOE_TRY(launch_gather_rows(x, src_token, offsets + cfg->N, (int64_t)cfg->T * cfg->k, (int)(cfg->d * esize(cfg)),
+                             x_perm, s));
+  MOE_TRY(ffn_routed(cfg, x_perm, offsets, w1, w3, w2, w.at<void>(L.h), y_perm, w.status(), s));
+  void *y_sh = nullptr;
+  if (shared) {
+    y_sh = w.at<void>(L.y_shared);
+    MOE_TRY(ffn_shared(cfg, x, sw1, sw3, sw2, w.at<void>(L.h_shared), y_sh, w.status(), s));
+  }
+  return launch_combine(is_bf16(cfg), y_perm, dest_row, gw, y_sh, out, cfg->T, cfg->d, cfg->k, s);
+}
+
+int moe_load_stats(const moe_config *cfg, const float *logits, const int32_t *counts_routed,
+                   const int32_t *counts_kept, float *f, float *P, float *summary, void *ws, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  if (!logits || !counts_routed || !counts_kept || !f || !P || !summary) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  MOE_TRY(make_ws(cfg, ws, &w));
+  return launch_load_stats(logits, counts_routed, counts_kept, cfg->T, cfg->N, cfg->k, cfg->gate,
+                           w.stats_partial(cfg), f, P, summary, static_cast<cudaStream_t>(stream));
+}
+
+int moe_get_device_status(void *ws, void *stream, int *status) {
+  if (!ws || !status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  if (cudaMemcpyAsync(&word, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyAsync(ws, &zero, sizeof(int), cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  *status = MOE_OK;
+  for (int c = 1; c < 31; ++c)
+    if (word & (1 << c)) {
+      *status = c;
+      break;
+    }
+  return MOE_OK;
+}
+
+}  // extern "C"

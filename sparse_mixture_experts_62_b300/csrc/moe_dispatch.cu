@@ -1,0 +1,169 @@
+// Dispatch: group the (token, slot) assignments by expert, apply the capacity
+// limit in token order, and gather the token rows into the permuted buffer.
+//
+// "Lecture29" (CS25 lecture 29 notes), section "Top-k routing semantics": tokens
+// are rearranged by expert, run, and restored to their order; section
+// "Inference load balance": an expert takes at most C = ceil(alpha T k / E)
+// assignments, the rest are dropped.  "Chapter 19: MoE" 19.6.1 and CS336
+// lecture 4 section 10: a dropped assignment contributes nothing; the residual
+// path (owned by the caller) carries the token on.
+//
+// Deterministic without ordered atomics:
+//   1. per 128-token chunk, a histogram of expert ids (shared-memory counts);
+//   2. one CTA scans the histograms: per-expert totals, kept = min(total, C),
+//      offsets = exclusive scan of kept, and each chunk's starting rank;
+//   3. per chunk, each assignment's rank among the expert's assignments in
+//      token order = chunk start + earlier warps + earlier lanes (bit masks);
+//   4. a gather copies x[src_token[row]] into x_perm[row] with 16-byte vectors.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int CH = kDispatchChunk;  // tokens per chunk = threads per CTA
+constexpr int CH_WARPS = CH / 32;
+
+__global__ void __launch_bounds__(CH) dispatch_hist_kernel(const int32_t *__restrict__ idx, int T, int k, int N,
+                                                           int32_t *__restrict__ hist, int *status) {
+  __shared__ int cnt[256];
+  for (int e = threadIdx.x; e < N; e += CH) cnt[e] = 0;
+  __syncthreads();
+  const int t = blockIdx.x * CH + threadIdx.x;
+  if (t < T) {
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[(size_t)t * k + j];
+      if (e < 0 || e >= N) {
+        set_status(status, MOE_ERR_BOUNDS);
+        continue;
+      }
+      atomicAdd(&cnt[e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < N; e += CH) hist[(size_t)blockIdx.x * N + e] = cnt[e];
+}
+
+// One CTA of 256 threads; thread e owns expert e.
+__global__ void __launch_bounds__(256) dispatch_scan_kernel(const int32_t *__restrict__ hist, int nchunks, int N,
+                                                            int capacity, int32_t *__restrict__ chunk_base,
+                                                            int32_t *__restrict__ counts_routed,
+                                                            int32_t *__restrict__ counts_kept,
+                                                            int32_t *__restrict__ offsets) {
+  __shared__ int kept_s[256];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < N) {
+    for (int c = 0; c < nchunks; ++c) {
+      chunk_base[(size_t)c * N + e] = run;
+      run += hist[(size_t)c * N + e];
+    }
+    counts_routed[e] = run;
+  }
+  const int kept = (e < N) ? (capacity > 0 ? min(run, capacity) : run) : 0;
+  if (e < N) counts_kept[e] = kept;
+  kept_s[e] = kept;
+  __syncthreads();
+  // exclusive scan of kept over experts (Hillis-Steele in shared memory)
+  for (int off = 1; off < 256; off <<= 1) {
+    const int v = (e >= off) ? kept_s[e - off] : 0;
+    __syncthreads();
+    kept_s[e] += v;
+    __syncthreads();
+  }
+  if (e < N) offsets[e] = kept_s[e] - kept;
+  if (e == N - 1) offsets[N] = kept_s[e];
+}
+
+__global__ void __launch_bounds__(CH) dispatch_rank_kernel(const int32_t *__restrict__ idx, int T, int k, int N,
+                                                           int capacity, const int32_t *__restrict__ chunk_base,
+                                                           const int32_t *__restrict__ offsets,
+                                                           int32_t *__restrict__ dest_row,
+                                                           int32_t *__restrict__ src_token) {
+  __shared__ uint32_t lanes_with[CH_WARPS][256];  // which lanes of the warp picked expert e
+  __shared__ int warp_before[CH_WARPS][256];      // assignments to e in earlier warps of the chunk
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int v = threadIdx.x; v < CH_WARPS * 256; v += CH) (&lanes_with[0][0])[v] = 0u;
+  __syncthreads();
+  const int t = blockIdx.x * CH + threadIdx.x;
+  int ex[8];
+  for (int j = 0; j < k; ++j) {
+    ex[j] = -1;
+    if (t < T) {
+      const int e = idx[(size_t)t * k + j];
+      if (e >= 0 && e < N) {
+        ex[j] = e;
+        atomicOr(&lanes_with[warp][e], 1u << lane);
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < N; e += CH) {
+    int run = 0;
+    for (int w = 0; w < CH_WARPS; ++w) {
+      warp_before[w][e] = run;
+      run += __popc(lanes_with[w][e]);
+    }
+  }
+  __syncthreads();
+  if (t >= T) return;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int j = 0; j < k; ++j) {
+    const int e = ex[j];
+    int row = -1;
+    if (e >= 0) {
+      const int rank = chunk_base[(size_t)blockIdx.x * N + e] + warp_before[warp][e] +
+                       __popc(lanes_with[warp][e] & lt_mask);
+      if (capacity <= 0 || rank < capacity) {
+        row = offsets[e] + rank;
+        src_token[row] = t;
+      }
+    }
+    dest_row[(size_t)t * k + j] = row;
+  }
+}
+
+// x_perm[row] = x[src_token[row]] for row < offsets[N]; one warp per row.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t *__restrict__ x,
+                                                          const int32_t *__restrict__ src_token,
+                                                          const int32_t *__restrict__ offsets_end, int row_bytes,
+                                                          uint8_t *__restrict__ x_perm) {
+  const int rows = *offsets_end;
+  const int nvec = row_bytes / 16;
+  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += warps_total) {
+    const int t = src_token[row];
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * row_bytes);
+    uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)row * row_bytes);
+    for (int v = threadIdx.x & 31; v < nvec; v += 32) dst[v] = src[v];
+  }
+}
+
+}  // namespace
+
+int launch_dispatch(const int32_t *idx, int T, int k, int N, int capacity, int32_t *hist, int32_t *chunk_base,
+                    int32_t *counts_routed, int32_t *counts_kept, int32_t *offsets, int32_t *dest_row,
+                    int32_t *src_token, int *status, cudaStream_t s) {
+  const int nchunks = (T + CH - 1) / CH;
+  if (nchunks > 0) dispatch_hist_kernel<<<nchunks, CH, 0, s>>>(idx, T, k, N, hist, status);
+  dispatch_scan_kernel<<<1, 256, 0, s>>>(hist, nchunks, N, capacity, chunk_base, counts_routed, counts_kept, offsets);
+  if (nchunks > 0)
+    dispatch_rank_kernel<<<nchunks, CH, 0, s>>>(idx, T, k, N, capacity, chunk_base, offsets, dest_row, src_token);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_gather_rows(const void *x, const int32_t *src_token, const int32_t *offsets_end, int64_t max_rows,
+                       int row_bytes, void *x_perm, cudaStream_t s) {
+  if (max_rows <= 0) return MOE_OK;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int sms = device_sm_count(dev);
+  int64_t blocks = (max_rows + 7) / 8;
+  const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;
+  if (blocks > cap) blocks = cap;
+  gather_rows_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(x), src_token, offsets_end, row_bytes,
+                                                  static_cast<uint8_t *>(x_perm));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

@@ -1,0 +1,381 @@
+// Grouped GEMM over ragged per-expert row groups on the 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory), operands staged by TMA.
+//
+// This is the expert FFN of the layer: "Lecture29" (CS25 lecture 29 notes),
+// section "A dense Transformer layer" (expert = W2(SiLU(W1 x) * W3 x)) and the
+// Shazeer et al. notes (expert = one ReLU hidden layer); grouped over experts
+// the way the CS336 lecture 4 notes, section 10, describe the block-sparse
+// matmul: every expert's rows form one contiguous group, no padding per expert.
+//
+//   out[r, n] = EPI( sum_k A[r, k] * B_g[n, k] )        for rows r of group g
+//
+// A: [rows, K] bf16 row-major (x_perm or h), one TMA map over all groups.
+// B_g: rows [g * b_rows, (g + 1) * b_rows) of a [G * b_rows, K] bf16 view of the
+//      stacked expert weights (K-major, i.e. the "W x" layout).
+// Modes:
+//   kSwiGLU: two weight maps (W1, W3); a 128x256 accumulator holds W1 rows
+//            n0..n0+127 in columns 0..127 and W3 rows in 128..255; the epilogue
+//            writes SiLU(a) * u as bf16, 128 output columns per tile.
+//   kReLU:   one map; 256 output columns per tile; epilogue max(acc, 0) -> bf16.
+//   kPlain:  one map; 256 output columns per tile; epilogue acc -> bf16.
+//
+// Kernel shape (one CTA per SM, persistent over output tiles):
+//   warp 0      TMA producer (one lane): 4-stage ring of {A 128x64, B 256x64}.
+//   warp 1      TMEM owner + MMA issuer (one lane): 4 x tcgen05.mma
+//               M=128,N=256,K=16 per stage into one of two TMEM accumulators.
+//   warps 2..5  epilogue: tcgen05.ld of its 32-lane quadrant, activation,
+//               16-byte stores masked to the group's rows and the output width.
+// Tiles are enumerated group by group, n-tile-major within a group, so the
+// CTAs of one wave share each weight tile through L2.
+#include <mutex>
+#include <vector>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128;              // rows per tile (TMEM lanes)
+constexpr int BN = 256;              // accumulator columns per tile
+constexpr int BK = 64;               // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB
+constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr uint32_t STAGE_TX = STAGE_BYTES;
+constexpr int MAX_GROUPS = 257;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;  // two 256-column accumulators
+constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_BYTES + 256 /*barriers*/ +
+                              (size_t)(4 * MAX_GROUPS + 8) * 4;
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+
+enum Mode { kSwiGLU = 0, kReLU = 1, kPlain = 2 };
+
+struct Args {
+  const int32_t *offsets;  // [G + 1] group row offsets in A / out, or nullptr: one group of M rows
+  int32_t G;
+  int32_t M;
+  int32_t a_rows;      // rows of A and out; a group reaching past them is rejected
+  int32_t n_out;       // output columns of every group
+  int32_t K;           // reduction length
+  int32_t b_rows;      // weight-view rows per group
+  uint16_t *out;       // [rows, n_out] bf16
+  int *status;
+};
+
+__device__ __forceinline__ float silu(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                        const __grid_constant__ CUtensorMap tmB1, const Args args) {
+  constexpr int OUT_COLS = (MODE == kSwiGLU) ? 128 : 256;  // output columns per tile
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled operand tiles
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  int *tile_start = reinterpret_cast<int *>(smem + STAGES * STAGE_BYTES + 256);  // [G + 1]
+  int *mtiles = tile_start + MAX_GROUPS + 1;                                     // [G]
+  int *rowbeg = mtiles + MAX_GROUPS;                                             // [G]
+  int *rowend = rowbeg + MAX_GROUPS;                                             // [G]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = args.G;
+  const int n_tiles = (args.n_out + OUT_COLS - 1) / OUT_COLS;
+  const int num_kb = (args.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    fence_barrier_init();
+    int acc = 0;
+    for (int g = 0; g < G; ++g) {
+      int b = args.offsets ? args.offsets[g] : 0;
+      int e = args.offsets ? args.offsets[g + 1] : args.M;
+      if (b < 0 || e < b || e > args.a_rows) {  // malformed group: flag it, run nothing
+        set_status(args.status, MOE_ERR_BOUNDS);
+        b = e = 0;
+      }
+      rowbeg[g] = b;
+      rowend[g] = e;
+      const int mt = e > b ? (e - b + BM - 1) / BM : 0;
+      mtiles[g] = mt;
+      tile_start[g] = acc;
+      acc += mt * n_tiles;
+    }
+    tile_start[G] = acc;
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB0);
+    if (MODE == kSwiGLU) tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = tile_start[G];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int issued_parity[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      int g = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        while (tile >= tile_start[g + 1]) ++g;
+        const int local = tile - tile_start[g];
+        const int n_tile = local / mtiles[g];
+        const int m_tile = local - n_tile * mtiles[g];
+        const int a_row = rowbeg[g] + m_tile * BM;
+        const int b_row = g * args.b_rows + n_tile * OUT_COLS;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, args.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t *sa = smem + stage * STAGE_BYTES;
+          uint8_t *sb = sa + A_BYTES;
+          mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+          tma_load_2d(sa, &tmA, &full[stage], kb * BK, a_row);
+          if (MODE == kSwiGLU) {
+            tma_load_2d(sb, &tmB0, &full[stage], kb * BK, b_row);
+            tma_load_2d(sb + B_BYTES / 2, &tmB1, &full[stage], kb * BK, b_row);
+          } else {
+            tma_load_2d(sb, &tmB0, &full[stage], kb * BK, b_row);
+            tma_load_2d(sb + B_BYTES / 2, &tmB0, &full[stage], kb * BK, b_row + BN / 2);
+          }
+          issued_parity[stage] = (int)phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // never leave the CTA with a bulk copy still writing its shared memory
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_parity[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_parity[s], args.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, args.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint64_t adesc = smem_desc_sw128(sa);
+          const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
+            tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, IDESC, (kb | kk) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) tc_commit(&tfull[acc]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+    const int r = quad * 32 + lane;
+    int g = 0;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+      while (tile >= tile_start[g + 1]) ++g;
+      const int local = tile - tile_start[g];
+      const int n_tile = local / mtiles[g];
+      const int m_tile = local - n_tile * mtiles[g];
+      const int row0 = rowbeg[g] + m_tile * BM;
+      const int rows_valid = min(BM, rowend[g] - row0);
+      const int n0 = n_tile * OUT_COLS;
+      const int acc = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!mbar_wait(&tfull[acc], use & 1u, args.status)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
+      const bool row_ok = r < rows_valid;
+      uint16_t *orow = args.out + (size_t)(row0 + (row_ok ? r : 0)) * args.n_out;
+      if (MODE == kSwiGLU) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 16) {
+          float a[16], u[16];
+          tmem_ld16x2(taddr + c, taddr + 128 + c, a, u);
+          uint32_t p[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) p[i] = pack_bf16x2(silu(a[2 * i]) * u[2 * i], silu(a[2 * i + 1]) * u[2 * i + 1]);
+          const int col = n0 + c;
+          if (row_ok) {
+            if (col + 8 <= args.n_out) *reinterpret_cast<uint4 *>(orow + col) = make_uint4(p[0], p[1], p[2], p[3]);
+            if (col + 16 <= args.n_out)
+              *reinterpret_cast<uint4 *>(orow + col + 8) = make_uint4(p[4], p[5], p[6], p[7]);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          float v0[16], v1[16];
+          tmem_ld16x2(taddr + c, taddr + c + 16, v0, v1);
+          uint32_t p[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float x0 = v0[2 * i], x1 = v0[2 * i + 1], y0 = v1[2 * i], y1 = v1[2 * i + 1];
+            if (MODE == kReLU) {
+              x0 = fmaxf(x0, 0.f);
+              x1 = fmaxf(x1, 0.f);
+              y0 = fmaxf(y0, 0.f);
+              y1 = fmaxf(y1, 0.f);
+            }
+            p[i] = pack_bf16x2(x0, x1);
+            p[8 + i] = pack_bf16x2(y0, y1);
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int col = n0 + c + 8 * q;
+              if (col + 8 <= args.n_out)
+                *reinterpret_cast<uint4 *>(orow + col) = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over a [rows, cols] row-major matrix, box 64 (cols) x 128 (rows),
+// 128-byte swizzle; out-of-range elements read as zero.
+static int make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return MOE_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16 || rows == 0 || cols == 0) return MOE_ERR_UNSUPPORTED;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {BK, BM};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+template <int MODE>
+static int prepare_kernel(int device) {
+  static std::mutex mu;
+  static std::vector<int> done;
+  std::lock_guard<std::mutex> lk(mu);
+  if ((int)done.size() <= device) done.resize(device + 1, 0);
+  if (!done[device]) {
+    if (cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    done[device] = 1;
+  }
+  return MOE_OK;
+}
+
+}  // namespace tc
+
+int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
+                    int64_t b_rows_total, int b_rows_per_group, const int32_t *offsets, int G, int M, int n_out,
+                    void *out, int *status, cudaStream_t stream) {
+  using namespace tc;
+  if (G < 1 || G > MAX_GROUPS || K < 1 || n_out < 1 || a_rows < 1 || b_rows_total < 1) return MOE_ERR_INVALID_ARG;
+  if (a_rows > INT32_MAX || n_out > b_rows_per_group || (int64_t)G * b_rows_per_group > b_rows_total)
+    return MOE_ERR_INVALID_ARG;
+  if (mode == kSwiGLU && !B1) return MOE_ERR_INVALID_ARG;
+  CUtensorMap ma, mb0, mb1;
+  int rc;
+  if ((rc = make_map(&ma, A, (uint64_t)a_rows, (uint64_t)K))) return rc;
+  if ((rc = make_map(&mb0, B0, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
+  if (mode == kSwiGLU) {
+    if ((rc = make_map(&mb1, B1, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
+  } else {
+    mb1 = mb0;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return MOE_ERR_CUDA;
+  Args args{offsets, G, M, (int32_t)a_rows, n_out, K, b_rows_per_group, static_cast<uint16_t *>(out), status};
+  dim3 grid(sms), block(THREADS);
+  switch (mode) {
+    case kSwiGLU:
+      if ((rc = prepare_kernel<kSwiGLU>(dev))) return rc;
+      grouped_gemm_kernel<kSwiGLU><<<grid, block, SMEM_BYTES, stream>>>(ma, mb0, mb1, args);
+      break;
+    case kReLU:
+      if ((rc = prepare_kernel<kReLU>(dev))) return rc;
+      grouped_gemm_kernel<kReLU><<<grid, block, SMEM_BYTES, stream>>>(ma, mb0, mb1, args);
+      break;
+    default:
+      if ((rc = prepare_kernel<kPlain>(dev))) return rc;
+      grouped_gemm_kernel<kPlain><<<grid, block, SMEM_BYTES, stream>>>(ma, mb0, mb1, args);
+      break;
+  }
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

@@ -1,0 +1,45 @@
+// Host-side launchers shared between the translation units of libmoe_b300.
+// Every launcher enqueues on `stream` and returns a moe_status code.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+int device_sm_count(int device);
+
+// router: logits = x . Wg (+ logit_bias); then top-k + gate weights
+int launch_router_logits(const void *x, bool x_bf16, const float *Wg, const float *logit_bias, int T, int d, int N,
+                         float *logits, cudaStream_t s);
+int launch_router_topk(const float *logits, const float *sel_bias, int T, int N, int k, int gate, int32_t *idx,
+                       float *w, int *status, cudaStream_t s);
+
+// dispatch
+constexpr int kDispatchChunk = 128;  // tokens per histogram / rank chunk
+int launch_dispatch(const int32_t *idx, int T, int k, int N, int capacity, int32_t *hist, int32_t *chunk_base,
+                    int32_t *counts_routed, int32_t *counts_kept, int32_t *offsets, int32_t *dest_row,
+                    int32_t *src_token, int *status, cudaStream_t s);
+int launch_gather_rows(const void *x, const int32_t *src_token, const int32_t *offsets_end, int64_t max_rows,
+                       int row_bytes, void *x_perm, cudaStream_t s);
+
+// grouped GEMM on tcgen05 (bf16); mode 0 = SwiGLU (B0 = W1, B1 = W3), 1 = ReLU, 2 = plain
+int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
+                    int64_t b_rows_total, int b_rows_per_group, const int32_t *offsets, int G, int M, int n_out,
+                    void *out, int *status, cudaStream_t stream);
+
+// grouped GEMM on the CUDA cores (float32 workloads); same modes, out in the input dtype
+int simt_grouped_gemm(int mode, bool bf16, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
+                      int b_rows_per_group, const int32_t *offsets, int G, int M, int n_out, void *out,
+                      cudaStream_t stream);
+
+// combine
+int launch_combine(bool bf16, const void *y_perm, const int32_t *dest_row, const float *w, const void *y_shared,
+                   void *out, int T, int d, int k, cudaStream_t s);
+
+// load statistics
+constexpr int kStatsChunk = 256;
+int launch_load_stats(const float *logits, const int32_t *counts_routed, const int32_t *counts_kept, int T, int N,
+                      int k, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s);
+
+}  // namespace moe

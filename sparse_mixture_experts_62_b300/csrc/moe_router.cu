@@ -1,0 +1,219 @@
+// Router of the layer: logits z = x . W_g (+ beta), top-k selection with ties to
+// the lower expert index, and the gate weights.
+//
+// "Lecture29" (CS25 lecture 29 notes), section "Top-two routing": z = W_r x,
+// S_k(x) = the k largest logits, g_i = exp(z_i) / sum_{j in S_k} exp(z_j).
+// "Chapter 19: MoE" 19.3.4 and CS336 lecture 4 section 9: DeepSeek-V3 chooses on
+// sigmoid(z) + b and mixes with the raw sigmoid affinities.  CS336 lecture 4,
+// section 11: the router runs in float32.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int RT_TOK = 32;   // tokens per CTA (one per lane)
+constexpr int RT_KC = 128;   // K chunk staged in shared memory
+constexpr int RT_WARPS = 8;  // each warp owns RT_KC / RT_WARPS consecutive k of a chunk
+
+// Logits for 32 tokens x EN experts.  Lane = token; the 8 warps split each K
+// chunk, and their partial sums are added in warp order (deterministic).
+template <int EN, bool BF16>
+__global__ void __launch_bounds__(256) router_logits_kernel(const void *__restrict__ x, const float *__restrict__ Wg,
+                                                            const float *__restrict__ logit_bias, int T, int d, int N,
+                                                            float *__restrict__ logits) {
+  constexpr int XS_LD = RT_KC + 1;
+  constexpr int XS_FLOATS = RT_TOK * XS_LD;
+  constexpr int WS_FLOATS = RT_KC * EN;
+  constexpr int RED_FLOATS = RT_WARPS * RT_TOK * EN;
+  constexpr int SMEM_FLOATS = (XS_FLOATS + WS_FLOATS) > RED_FLOATS ? (XS_FLOATS + WS_FLOATS) : RED_FLOATS;
+  __shared__ __align__(16) float sm[SMEM_FLOATS];
+  float *xs = sm;
+  float *ws = sm + XS_FLOATS;
+
+  const int t0 = blockIdx.x * RT_TOK;
+  const int e0 = blockIdx.y * EN;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float acc[EN];
+#pragma unroll
+  for (int e = 0; e < EN; ++e) acc[e] = 0.f;
+
+  for (int k0 = 0; k0 < d; k0 += RT_KC) {
+    // stage x[t0.., k0..k0+127] as float (8-element vectors; d % 8 == 0 / 4)
+    for (int v = threadIdx.x; v < RT_TOK * (RT_KC / 8); v += blockDim.x) {
+      const int tt = v / (RT_KC / 8), kk = (v % (RT_KC / 8)) * 8;
+      const int t = t0 + tt, kg = k0 + kk;
+      float f[8];
+      if (t < T && kg < d) {
+        if (BF16) {
+          const uint4 q = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + (size_t)t * d + kg);
+          f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x); f[2] = bf16_lo(q.y); f[3] = bf16_hi(q.y);
+          f[4] = bf16_lo(q.z); f[5] = bf16_hi(q.z); f[6] = bf16_lo(q.w); f[7] = bf16_hi(q.w);
+        } else {
+          const float *src = static_cast<const float *>(x) + (size_t)t * d + kg;
+          const float4 a = *reinterpret_cast<const float4 *>(src);
+          const float4 b = *reinterpret_cast<const float4 *>(src + 4);
+          f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) xs[tt * XS_LD + kk + i] = f[i];
+    }
+    // stage Wg[k0.., e0..e0+EN-1]
+    for (int v = threadIdx.x; v < RT_KC * EN; v += blockDim.x) {
+      const int kk = v / EN, e = v % EN;
+      const int kg = k0 + kk, eg = e0 + e;
+      ws[v] = (kg < d && eg < N) ? Wg[(size_t)kg * N + eg] : 0.f;
+    }
+    __syncthreads();
+    const int kb = warp * (RT_KC / RT_WARPS);
+#pragma unroll 4
+    for (int kk = kb; kk < kb + RT_KC / RT_WARPS; ++kk) {
+      const float xv = xs[lane * XS_LD + kk];
+      const float4 *wr = reinterpret_cast<const float4 *>(ws + kk * EN);
+#pragma unroll
+      for (int q = 0; q < EN / 4; ++q) {
+        const float4 w4 = wr[q];
+        acc[4 * q + 0] = fmaf(xv, w4.x, acc[4 * q + 0]);
+        acc[4 * q + 1] = fmaf(xv, w4.y, acc[4 * q + 1]);
+        acc[4 * q + 2] = fmaf(xv, w4.z, acc[4 * q + 2]);
+        acc[4 * q + 3] = fmaf(xv, w4.w, acc[4 * q + 3]);
+      }
+    }
+    __syncthreads();
+  }
+  // deterministic cross-warp reduction
+  float *red = sm;
+#pragma unroll
+  for (int e = 0; e < EN; ++e) red[(warp * RT_TOK + lane) * EN + e] = acc[e];
+  __syncthreads();
+  for (int v = threadIdx.x; v < RT_TOK * EN; v += blockDim.x) {
+    const int tt = v / EN, e = v % EN;
+    const int t = t0 + tt, eg = e0 + e;
+    if (t >= T || eg >= N) continue;
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < RT_WARPS; ++w) s += red[(w * RT_TOK + tt) * EN + e];
+    if (logit_bias) s += logit_bias[eg];
+    logits[(size_t)t * N + eg] = s;
+  }
+}
+
+// Orderable key of (score desc, index asc): larger key = preferred expert.
+__device__ __forceinline__ unsigned long long topk_key(float v, int e) {
+  if (v == 0.0f) v = 0.0f;  // -0 and +0 are the same score
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)u << 32) | (uint32_t)(0xFFFFu - (uint32_t)e);
+}
+
+__device__ __forceinline__ float sigmoid_f32(float z) {
+  // evaluated in double and rounded once, as the selection decision is
+  return (float)(1.0 / (1.0 + exp(-(double)z)));
+}
+
+// One warp per token; lane l holds experts l, l+32, ... (N <= 256).
+__global__ void __launch_bounds__(256) router_topk_kernel(const float *__restrict__ logits,
+                                                          const float *__restrict__ sel_bias, int T, int N, int k,
+                                                          int gate, int32_t *__restrict__ idx, float *__restrict__ w,
+                                                          int *status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const float *zr = logits + (size_t)t * N;
+  float sel[8];
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    sel[i] = -INFINITY;
+    if (e < N) {
+      const float z = zr[e];
+      if (!isfinite(z)) bad = true;
+      float s = z;
+      if (gate == MOE_GATE_SIGMOID_BIAS) {
+        s = sigmoid_f32(z);
+        if (sel_bias) s = s + sel_bias[e];
+      }
+      sel[i] = s;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
+  uint32_t taken = 0;
+  int chosen[8];
+  for (int j = 0; j < k; ++j) {
+    unsigned long long best = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      if (e < N && !((taken >> i) & 1u)) {
+        const unsigned long long key = topk_key(sel[i], e);
+        best = key > best ? key : best;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+      best = o > best ? o : best;
+    }
+    const int e_best = (int)(0xFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+    if ((e_best & 31) == lane) taken |= 1u << (e_best >> 5);
+    chosen[j] = e_best;
+  }
+  // gate weights of the selected experts, in float32
+  if (lane == 0) {
+    float g[8];
+    float sum = 0.f;
+    if (gate == MOE_GATE_SOFTMAX_TOPK) {
+      const float m = zr[chosen[0]];  // the first pick has the largest logit
+      for (int j = 0; j < k; ++j) {
+        g[j] = expf(zr[chosen[j]] - m);
+        sum += g[j];
+      }
+    } else {
+      for (int j = 0; j < k; ++j) {
+        g[j] = sigmoid_f32(zr[chosen[j]]);
+        sum += g[j];
+      }
+    }
+    for (int j = 0; j < k; ++j) {
+      idx[(size_t)t * k + j] = chosen[j];
+      w[(size_t)t * k + j] = g[j] / sum;
+    }
+  }
+}
+
+}  // namespace
+
+int launch_router_logits(const void *x, bool x_bf16, const float *Wg, const float *logit_bias, int T, int d, int N,
+                         float *logits, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  const int en = N <= 8 ? 8 : (N <= 16 ? 16 : 32);
+  dim3 grid((T + RT_TOK - 1) / RT_TOK, (N + en - 1) / en), block(256);
+#define MOE_RL(EN)                                                                                           \
+  if (x_bf16)                                                                                                \
+    router_logits_kernel<EN, true><<<grid, block, 0, s>>>(x, Wg, logit_bias, T, d, N, logits);              \
+  else                                                                                                       \
+    router_logits_kernel<EN, false><<<grid, block, 0, s>>>(x, Wg, logit_bias, T, d, N, logits);
+  if (en == 8) {
+    MOE_RL(8)
+  } else if (en == 16) {
+    MOE_RL(16)
+  } else {
+    MOE_RL(32)
+  }
+#undef MOE_RL
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_router_topk(const float *logits, const float *sel_bias, int T, int N, int k, int gate, int32_t *idx,
+                       float *w, int *status, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  router_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, sel_bias, T, N, k, gate, idx, w, status);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

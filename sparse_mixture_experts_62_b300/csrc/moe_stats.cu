@@ -1,0 +1,122 @@
+// Per-expert load statistics of the Switch balance loss.
+//
+// "Chapter 19: MoE" 19.3.3: f_i = fraction of assignments routed to expert i,
+// P_i = mean router probability of expert i over the batch.  CS336 lecture 4,
+// section 9: loss = N * sum_i f_i P_i.  "Lecture29" (CS25 lecture 29 notes),
+// "Myth 3": imbalance I = max_i n_i / (T k / N).  Drop rate = share of
+// assignments removed by the capacity limit.
+//
+// p_i(t) is the full N-way softmax of the logits (softmax gate) or
+// s_i / sum_l s_l with s = sigmoid(z) (sigmoid gate).  Partial sums per
+// 256-token chunk are reduced in a fixed order, so the result is deterministic.
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int SC = kStatsChunk;  // tokens per chunk
+
+__global__ void __launch_bounds__(256) stats_partial_kernel(const float *__restrict__ logits, int T, int N, int gate,
+                                                            float *__restrict__ partial) {
+  __shared__ float red[8][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  const int tb = blockIdx.x * SC;
+  for (int tt = warp; tt < SC; tt += 8) {
+    const int t = tb + tt;
+    if (t >= T) break;
+    const float *zr = logits + (size_t)t * N;
+    float v[8];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < N) ? zr[e] : -INFINITY;
+      m = fmaxf(m, v[i]);
+    }
+    if (gate == MOE_GATE_SOFTMAX_TOPK) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      float p = 0.f;
+      if (e < N) p = (gate == MOE_GATE_SOFTMAX_TOPK) ? expf(v[i] - m) : (float)(1.0 / (1.0 + exp(-(double)v[i])));
+      v[i] = p;
+      sum += p;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    const float inv = 1.0f / sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += v[i] * inv;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[warp][lane + 32 * i] = acc[i];
+  __syncthreads();
+  for (int e = threadIdx.x; e < N; e += blockDim.x) {
+    float s = 0.f;
+    for (int w = 0; w < 8; ++w) s += red[w][e];
+    partial[(size_t)blockIdx.x * N + e] = s;
+  }
+}
+
+__global__ void __launch_bounds__(256) stats_final_kernel(const float *__restrict__ partial, int nchunks,
+                                                          const int32_t *__restrict__ counts_routed,
+                                                          const int32_t *__restrict__ counts_kept, int T, int N, int k,
+                                                          float *__restrict__ f, float *__restrict__ P,
+                                                          float *__restrict__ summary) {
+  __shared__ double fp[256];
+  __shared__ int maxc[256];
+  __shared__ long long kept[256];
+  const int e = threadIdx.x;
+  const double tk = (double)T * (double)k;
+  double fe = 0.0, pe = 0.0;
+  int ce = 0;
+  long long ke = 0;
+  if (e < N) {
+    double s = 0.0;
+    for (int c = 0; c < nchunks; ++c) s += (double)partial[(size_t)c * N + e];
+    pe = s / (double)T;
+    ce = counts_routed[e];
+    ke = counts_kept[e];
+    fe = (double)ce / tk;
+    f[e] = (float)fe;
+    P[e] = (float)pe;
+  }
+  fp[e] = fe * pe;
+  maxc[e] = ce;
+  kept[e] = ke;
+  __syncthreads();
+  for (int off = 128; off > 0; off >>= 1) {
+    if (e < off) {
+      fp[e] += fp[e + off];
+      maxc[e] = max(maxc[e], maxc[e + off]);
+      kept[e] += kept[e + off];
+    }
+    __syncthreads();
+  }
+  if (e == 0) {
+    summary[0] = (float)((double)N * fp[0]);
+    summary[1] = (float)((double)maxc[0] / (tk / (double)N));
+    summary[2] = (float)(1.0 - (double)kept[0] / tk);
+  }
+}
+
+}  // namespace
+
+int launch_load_stats(const float *logits, const int32_t *counts_routed, const int32_t *counts_kept, int T, int N,
+                      int k, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  const int nchunks = (T + SC - 1) / SC;
+  stats_partial_kernel<<<nchunks, 256, 0, s>>>(logits, T, N, gate, partial);
+  stats_final_kernel<<<1, 256, 0, s>>>(partial, nchunks, counts_routed, counts_kept, T, N, k, f, P, summary);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

@@ -1,0 +1,99 @@
+"""Whole-layer parity of moe_layer_forward + moe_load_stats against the oracle (B300).
+
+Small layers are compared on every output; the full-size workloads (the
+Mixtral-shaped prefill and decode layers, the DeepSeek-V3-shaped and the
+Qwen3-shaped layers) are run in the launch configuration the benchmark times,
+with routing, dispatch and statistics compared on all tokens and the layer
+output on all tokens or on a seeded sample of them.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import assert_close_out, check_dispatch, check_routing, layer_on_device, to_dev, to_np_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def run_and_check(inp, sample=None):
+    wl = inp.wl
+    layer = layer_on_device(inp)
+    x = to_dev(inp.x, wl.dtype)
+    out = layer.forward(x)
+    f, P, summ = layer.load_stats()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    v = layer.views()
+    z = v["logits"].cpu().numpy()
+    idx = v["topk_idx"].cpu().numpy()
+    w = v["topk_w"].cpu().numpy().astype(np.float64)
+    tokens = None if sample is None else np.sort(np.random.default_rng(wl.seed).choice(wl.T, sample, replace=False))
+    ref = oracle.layer_forward(inp, tokens=tokens, idx_override=idx)
+    ref_own = oracle.layer_forward(inp, tokens=np.array([], dtype=np.int64))  # the oracle's own routing
+    near = check_routing(inp, z, idx, w, ref_own)
+    cap = layer.cfg.capacity
+    check_dispatch(wl, idx, v["counts_routed"].cpu().numpy(), v["counts_kept"].cpu().numpy(),
+                   v["offsets"].cpu().numpy(), v["dest_row"].cpu().numpy(), v["src_token"].cpu().numpy(), cap)
+    got = to_np_f64(out)
+    rows = np.arange(wl.T) if tokens is None else tokens
+    err, tol = assert_close_out(got[rows], ref.out[rows], wl.dtype)
+    # statistics
+    assert np.array_equal(f.cpu().numpy(), ref.stats.f.astype(np.float32))
+    assert np.max(np.abs(P.cpu().numpy() - ref.stats.P)) < 1e-5
+    s = summ.cpu().numpy().astype(np.float64)
+    assert s[0] == pytest.approx(ref.stats.aux, rel=1e-5)
+    assert s[1] == pytest.approx(ref.stats.imbalance, rel=1e-6)
+    assert s[2] == pytest.approx(ref.stats.drop_rate, rel=1e-6, abs=1e-7)
+    return dict(err=err, tol=tol, near_ties=near, kept=int(v["offsets"][-1]))
+
+
+SMALL = [
+    dict(T=333, d=256, N=8, k=2, F=384),                                   # ragged tails everywhere
+    dict(T=200, d=512, N=16, k=4, F=256, gate="sigmoid", shared_F=384, sel_bias_range=0.05),
+    dict(T=500, d=256, N=8, k=3, F=128, capacity_factor=0.75, zipf_s=1.2),
+    dict(T=64, d=64, N=1, k=1, F=64),
+    dict(T=50, d=128, N=4, k=4, F=192),
+    dict(T=129, d=320, N=7, k=2, F=136, act="relu"),
+    dict(T=1, d=64, N=8, k=2, F=64),
+]
+
+
+@pytest.mark.parametrize("kw", SMALL)
+def test_layer_small(kw):
+    kw = dict(kw)
+    wl = synth.Workload("small", 21, act=kw.pop("act", "swiglu"), gate=kw.pop("gate", "softmax"), dtype="bf16", **kw)
+    run_and_check(synth.make_inputs(wl))
+
+
+def test_layer_shazeer_tiny_f32_full():
+    """The float32 workload at full size: T=256, d=512, 8 ReLU experts 512->1024->512."""
+    run_and_check(synth.make_inputs(synth.WORKLOADS["shazeer_tiny_f32"]))
+
+
+def test_layer_mixtral_decode_full():
+    run_and_check(synth.make_inputs(synth.WORKLOADS["mixtral_decode"]))
+
+
+def test_layer_qwen3_skew_drop_full():
+    r = run_and_check(synth.make_inputs(synth.WORKLOADS["qwen3_skew_drop"]))
+    assert r["kept"] < 16384 * 8  # capacity actually drops assignments
+
+
+def test_layer_mixtral_prefill_full():
+    run_and_check(synth.make_inputs(synth.WORKLOADS["mixtral_prefill"]), sample=96)
+
+
+def test_layer_dsv3_finegrained_full():
+    run_and_check(synth.make_inputs(synth.WORKLOADS["dsv3_finegrained"]), sample=48)
+
+
+def test_layer_deterministic():
+    wl = synth.Workload("det", 5, T=300, d=256, N=8, k=2, F=256, act="swiglu", gate="softmax", dtype="bf16")
+    inp = synth.make_inputs(wl)
+    layer = layer_on_device(inp)
+    x = to_dev(inp.x, "bf16")
+    a = layer.forward(x).clone()
+    b = layer.forward(x).clone()
+    assert torch.equal(a, b)

@@ -384,3 +384,15 @@ def test_logit_bias_closed_form_zipf_probabilities():
     assert np.allclose(np.sort(r.stats.P)[::-1], p, rtol=1e-6)
     top = sorted(range(16), key=lambda i: -beta[i])[:4]
     assert np.all(r.idx == np.array(top)[None, :])
+
+
+def test_combine_hand_computed():
+    """A 2-token example worked by hand: token 0 keeps both slots, token 1's
+    second slot was dropped (-1) and adds nothing."""
+    y_rows = np.array([[1.0, 2.0], [10.0, 20.0], [100.0, 200.0]])
+    dest = np.array([[2, 0], [1, -1]])
+    w = np.array([[0.75, 0.25], [0.5, 0.5]])
+    out = oracle.combine(y_rows, dest, w, None)
+    assert out.tolist() == [[75.25, 150.5], [5.0, 10.0]]
+    out = oracle.combine(y_rows, dest, w, np.array([[1.0, 1.0], [2.0, 2.0]]))
+    assert out.tolist() == [[76.25, 151.5], [7.0, 12.0]]
