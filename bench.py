@@ -53,6 +53,13 @@ def layer_bytes(wl, touched_experts: int) -> float:
     return float(w + sw + 2 * wl.T * wl.d * es + wl.d * wl.N * 4)
 
 
+# dram__bytes_read.sum + dram__bytes_write.sum of the two grouped-GEMM launches of
+# one step, from one ncu capture of the kernel revision named here (None once the
+# kernel changes until it is captured again).
+NCU_TRAFFIC = {"mixtral_prefill": {"bytes": 3.675e9, "kernel_rev": "tc1"}}
+KERNEL_REV = "tc1"
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -60,6 +67,23 @@ def measured_peaks():
             d = json.load(f)
         return d, "measured"
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def blas_threads() -> int:
+    """Threads the oracle's float64 matmuls run on (BLAS pool), else the host's cores."""
+    try:
+        import threadpoolctl
+        return max((p.get("num_threads", 1) for p in threadpoolctl.threadpool_info()), default=1)
+    except ImportError:
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+            if os.environ.get(var, "").isdigit():
+                return int(os.environ[var])
+        return os.cpu_count() or 1
+
+
+def _traffic(name):
+    t = NCU_TRAFFIC.get(name)
+    return t["bytes"] if t and t["kernel_rev"] == KERNEL_REV else None
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -145,8 +169,6 @@ def max_over_ranks(dist, v: float) -> float:
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args, wl):
     """The CPU oracle, as it stands, on a bounded sample of the same workload per step."""
-    import threadpoolctl
-
     import oracle
     inp = synth.make_inputs(wl)
     sample = args.ref_sample
@@ -166,7 +188,7 @@ def run_reference(args, wl):
         step()
     secs = [step() for _ in range(args.steps)]
     per_step = float(np.mean(secs))
-    cores = max((p.get("num_threads", 1) for p in threadpoolctl.threadpool_info()), default=1)
+    cores = blas_threads()
     value = wl.T / per_step
     desc = (f"oracle (numpy float64): routing, dispatch and statistics on all {wl.T} tokens, expert FFN on "
             f"{min(sample, wl.T)} sampled tokens per step, extrapolated linearly to {wl.T} tokens")
@@ -180,8 +202,6 @@ def run_reference(args, wl):
 
 
 def cpu_baseline(wl, inp, budget_tokens: int):
-    import threadpoolctl
-
     import oracle
     toks = np.sort(np.random.default_rng(wl.seed + 1).choice(wl.T, size=min(budget_tokens, wl.T), replace=False))
     t0 = time.perf_counter()
@@ -191,7 +211,7 @@ def cpu_baseline(wl, inp, budget_tokens: int):
     t2 = time.perf_counter()
     per_token = max(0.0, (t2 - t1) - (t1 - t0)) / len(toks)
     est = (t1 - t0) + per_token * wl.T
-    cores = max((p.get("num_threads", 1) for p in threadpoolctl.threadpool_info()), default=1)
+    cores = blas_threads()
     return {"value": wl.T / est, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": (f"numpy float64 oracle: routing, dispatch and statistics on all {wl.T} tokens, expert FFN "
                        f"on {len(toks)} sampled tokens, extrapolated linearly to {wl.T} tokens "
@@ -305,7 +325,7 @@ def run_ours(args, wl, dist, rank, local):
     achieved_tflops = fl["expert_ffn"] / ffn_s / 1e12
     peak_tf = peaks["bf16_tflops"]
     roof = {"bound": "tensor", "achieved": achieved_tflops, "peak": peak_tf, "unit": "TFLOP/s",
-            "frac": achieved_tflops / peak_tf, "traffic": None,
+            "frac": achieved_tflops / peak_tf, "traffic": _traffic(wl.name),
             "kernel": "grouped_gemm_kernel (tcgen05), moe_expert_ffn: gate/up + down launches",
             "peak_source": f"{peak_src} bf16_tflops (burst)"}
     if wl.T <= 64:  # decode: the layer streams weights; HBM governs
