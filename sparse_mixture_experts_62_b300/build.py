@@ -1,6 +1,6 @@
 """Build libmoe_b300.so in-tree with nvcc for sm_103a (B300).
 
-    python -m sparse_mixture_experts_62_b300.build [--force]
+    python sparse_mixture_experts_62_b300/build.py [--force]
 
 Each .cu under csrc/ compiles to an object in _build/ (in parallel), then nvcc
 links them into sparse_mixture_experts_62_b300/libmoe_b300.so with the CUDA
