@@ -145,6 +145,28 @@ MOE_API int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const v
                  int32_t *counts_kept, int32_t *offsets, int32_t *dest_row, int32_t *src_token,
                  void *x_perm, void *ws, void *stream);
 
+/* moe_dispatch without a workspace, for callers that cannot allocate device
+ * memory and cannot pass a workspace: typically a plug-in or custom operator in a
+ * host program that has already reserved the GPU's memory for its own pool and
+ * whose interface hands the operator only its input and output buffers.  The
+ * pages describe no such variant; it has no counterpart there.
+ * Inputs, outputs and results are exactly those of moe_dispatch.  `status` is an
+ * optional device int32 (may be NULL) in which bit MOE_ERR_BOUNDS is set when an
+ * expert id is out of range; the caller clears it.
+ * Scratch: a fixed 1 MiB array inside the library (a `static __device__`
+ * variable), resident on every GPU that loads the library until the process
+ * exits.  It bounds the size: ceil(T / 128) * N <= 131072 (for example T up to
+ * 65536 with N = 256), else MOE_ERR_UNSUPPORTED.  Every call overwrites every
+ * scratch entry it reads, so nothing needs clearing between calls.
+ * The first call on each device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the one array: calls whose executions overlap on the GPU (two streams,
+ * two host threads) race on it and give wrong results; serialise them. */
+MOE_API int moe_dispatch_noalloc(const moe_config *cfg, const int32_t *topk_idx, const void *x,
+                                 int32_t *counts_routed, int32_t *counts_kept, int32_t *offsets,
+                                 int32_t *dest_row, int32_t *src_token, void *x_perm, int32_t *status,
+                                 void *stream);
+
 /* Routed experts over the permuted rows: for each expert e, rows
  * [offsets[e], offsets[e+1]) of x_perm go through Expert_e; results in y_perm
  * (same rows).  y_perm is bf16 for bf16 configs, float for float32 configs.

@@ -1,7 +1,7 @@
 """Python binding of libmoe_b300: the sparse token-choice MoE FFN layer forward on B300.
 
 Argument marshalling only.  Every step of the layer runs in the CUDA kernels of
-libmoe_b300.so (built in-tree by ``python -m sparse_mixture_experts_62_b300.build``);
+libmoe_b300.so (built in-tree by ``python sparse_mixture_experts_62_b300/build.py``);
 importing this package without that library raises ImportError -- there is no
 other implementation to fall back to.  PyTorch supplies device memory and
 streams: tensor arguments are passed to the C ABI as raw device pointers.
@@ -9,7 +9,7 @@ streams: tensor arguments are passed to the C ABI as raw device pointers.
 Functions carry the C names (see include/moe.h for layouts and semantics):
 moe_route, moe_dispatch, moe_expert_ffn, moe_shared_ffn, moe_combine,
 moe_layer_forward, moe_load_stats, moe_capacity, moe_workspace_size,
-moe_workspace_layout, moe_get_device_status.
+moe_workspace_layout, moe_get_device_status, moe_dispatch_noalloc.
 """
 from __future__ import annotations
 
@@ -28,7 +28,7 @@ DTYPE_F32, DTYPE_BF16 = 0, 1
 
 EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_workspace_layout", "moe_route",
            "moe_dispatch", "moe_expert_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
-           "moe_load_stats", "moe_get_device_status")
+           "moe_load_stats", "moe_get_device_status", "moe_dispatch_noalloc")
 
 
 class MoeConfig(ctypes.Structure):
@@ -50,7 +50,7 @@ class MoeError(RuntimeError):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it with `python -m sparse_mixture_experts_62_b300.build`")
+        raise ImportError(f"{LIB_PATH} is missing: build it with `python sparse_mixture_experts_62_b300/build.py`")
     lib = ctypes.CDLL(LIB_PATH)
     P = ctypes.c_void_p
     C = ctypes.POINTER(MoeConfig)
@@ -62,6 +62,7 @@ def _load():
         "moe_workspace_layout": [C, ctypes.POINTER(MoeWsLayout)],
         "moe_route": [C, P, P, P, P, P, P, P, P, P],
         "moe_dispatch": [C, P, P, P, P, P, P, P, P, P, P],
+        "moe_dispatch_noalloc": [C, P, P, P, P, P, P, P, P, P, P],
         "moe_expert_ffn": [C, P, P, P, P, P, P, P, P],
         "moe_shared_ffn": [C, P, P, P, P, P, P, P],
         "moe_combine": [C, P, P, P, P, P, P],
@@ -138,6 +139,17 @@ def moe_dispatch(cfg, topk_idx, x, counts_routed, counts_kept, offsets, dest_row
     _check(_lib.moe_dispatch(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts_routed), _ptr(counts_kept),
                              _ptr(offsets), _ptr(dest_row), _ptr(src_token), _ptr(x_perm), _ptr(ws),
                              _stream(stream)), "moe_dispatch")
+
+
+def moe_dispatch_noalloc(cfg, topk_idx, x, counts_routed, counts_kept, offsets, dest_row, src_token, x_perm,
+                         status=None, stream=None):
+    """moe_dispatch with its scratch in a fixed array inside the library: no workspace, no allocation.
+
+    For callers that cannot allocate device memory or pass a workspace (see
+    include/moe.h).  Calls that overlap on the GPU race on the shared array."""
+    _check(_lib.moe_dispatch_noalloc(ctypes.byref(cfg), _ptr(topk_idx), _ptr(x), _ptr(counts_routed),
+                                     _ptr(counts_kept), _ptr(offsets), _ptr(dest_row), _ptr(src_token),
+                                     _ptr(x_perm), _ptr(status), _stream(stream)), "moe_dispatch_noalloc")
 
 
 def moe_expert_ffn(cfg, x_perm, offsets, w1, w3, w2, y_perm, ws, stream=None):
