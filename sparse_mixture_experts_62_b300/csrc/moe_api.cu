@@ -70,7 +70,12 @@ int layout(const moe_config *c, moe_ws_layout *L) {
   L->y_perm = take(rows * d * es);
   L->h_shared = take(Fs ? T * Fs * es : 0);
   L->y_shared = take(Fs ? T * d * es : 0);
-  L->scratch = take(2 * nch_d * N * 4 + nch_s * N * 4);
+  size_t router_bytes = 0;
+  if (is_bf16(c)) {
+    const size_t Np = (size_t)router_tc_npad(c->N), dp = (size_t)router_tc_dpad(c->d);
+    router_bytes = align256(Np * 3 * dp * 2) + (size_t)router_tc_max_splits(c->T, c->d) * T * Np * 4;
+  }
+  L->scratch = take(align256(2 * nch_d * N * 4) + align256(nch_s * N * 4) + router_bytes);
   L->total = o;
   return MOE_OK;
 }
@@ -90,7 +95,17 @@ struct Ws {
   }
   float *stats_partial(const moe_config *c) const {
     const size_t nch = ((size_t)c->T + kDispatchChunk - 1) / kDispatchChunk;
-    return at<float>(L.scratch + 2 * nch * c->N * 4);
+    return at<float>(L.scratch + align256(2 * nch * c->N * 4));
+  }
+  size_t router_off(const moe_config *c) const {
+    const size_t nch = ((size_t)c->T + kDispatchChunk - 1) / kDispatchChunk;
+    const size_t nchs = ((size_t)c->T + kStatsChunk - 1) / kStatsChunk;
+    return L.scratch + align256(2 * nch * c->N * 4) + align256(nchs * c->N * 4);
+  }
+  uint16_t *router_wsplit(const moe_config *c) const { return at<uint16_t>(router_off(c)); }
+  float *router_partial(const moe_config *c) const {
+    const size_t Np = (size_t)router_tc_npad(c->N), dp = (size_t)router_tc_dpad(c->d);
+    return at<float>(router_off(c) + align256(Np * 3 * dp * 2));
   }
 };
 
@@ -135,6 +150,21 @@ int ffn_shared(const moe_config *c, const void *x, const void *sw1, const void *
     MOE_TRY(simt_grouped_gemm(2, false, h, c->T, Fs, sw2, nullptr, c->d, nullptr, 1, c->T, c->d, y, s));
   }
   return MOE_OK;
+}
+
+// logits, top-k and gate weights: tensor-core router for bf16 x, CUDA-core router for float32 x
+int route(const moe_config *c, const Ws &w, const void *x, const float *Wg, const float *logit_bias,
+          const float *sel_bias, float *logits, int32_t *idx, float *gw, cudaStream_t s) {
+  const float *sb = c->gate == MOE_GATE_SIGMOID_BIAS ? sel_bias : nullptr;
+  if (is_bf16(c)) {
+    int S = 1;
+    float *part = w.router_partial(c);
+    MOE_TRY(launch_router_tc(x, Wg, c->T, c->d, c->N, w.router_wsplit(c), part, &S, w.status(), s));
+    return launch_router_topk(part, S, router_tc_npad(c->N), logit_bias, logits, sb, c->T, c->N, c->k, c->gate, idx,
+                              gw, w.status(), s);
+  }
+  MOE_TRY(launch_router_logits(x, false, Wg, logit_bias, c->T, c->d, c->N, logits, s));
+  return launch_router_topk(logits, 1, c->N, nullptr, logits, sb, c->T, c->N, c->k, c->gate, idx, gw, w.status(), s);
 }
 
 bool weights_ok(const moe_config *c, const void *w1, const void *w3, const void *w2) {
@@ -207,10 +237,7 @@ int moe_route(const moe_config *cfg, const void *x, const float *Wg, const float
   if (!x || !Wg || !logits || !topk_idx || !topk_w || !aligned16(x)) return MOE_ERR_INVALID_ARG;
   Ws w;
   MOE_TRY(make_ws(cfg, ws, &w));
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MOE_TRY(launch_router_logits(x, is_bf16(cfg), Wg, logit_bias, cfg->T, cfg->d, cfg->N, logits, s));
-  return launch_router_topk(logits, cfg->gate == MOE_GATE_SIGMOID_BIAS ? sel_bias : nullptr, cfg->T, cfg->N, cfg->k,
-                            cfg->gate, topk_idx, topk_w, w.status(), s);
+  return route(cfg, w, x, Wg, logit_bias, sel_bias, logits, topk_idx, topk_w, static_cast<cudaStream_t>(stream));
 }
 
 int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x, int32_t *counts_routed,
@@ -285,9 +312,7 @@ int moe_layer_forward(const moe_config *cfg, const void *x, const float *Wg, con
   int32_t *src_token = w.at<int32_t>(L.src_token);
   void *x_perm = w.at<void>(L.x_perm);
   void *y_perm = w.at<void>(L.y_perm);
-  MOE_TRY(launch_router_logits(x, is_bf16(cfg), Wg, logit_bias, cfg->T, cfg->d, cfg->N, logits, s));
-  MOE_TRY(launch_router_topk(logits, cfg->gate == MOE_GATE_SIGMOID_BIAS ? sel_bias : nullptr, cfg->T, cfg->N, cfg->k,
-                             cfg->gate, idx, gw, w.status(), s));
+  MOE_TRY(route(cfg, w, x, Wg, logit_bias, sel_bias, logits, idx, gw, s));
   MOE_TRY(launch_dispatch(idx, cfg->T, cfg->k, cfg->N, cfg->capacity, w.hist(), w.chunk_base(cfg),
                           w.at<int32_t>(L.counts_routed), w.at<int32_t>(L.counts_kept), offsets, dest_row, src_token,
                           w.status(), s));

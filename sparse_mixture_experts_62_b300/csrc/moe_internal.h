@@ -12,8 +12,15 @@ int device_sm_count(int device);
 // router: logits = x . Wg (+ logit_bias); then top-k + gate weights
 int launch_router_logits(const void *x, bool x_bf16, const float *Wg, const float *logit_bias, int T, int d, int N,
                          float *logits, cudaStream_t s);
-int launch_router_topk(const float *logits, const float *sel_bias, int T, int N, int k, int gate, int32_t *idx,
-                       float *w, int *status, cudaStream_t s);
+int launch_router_topk(const float *partial, int S, int pstride, const float *logit_bias, float *logits,
+                       const float *sel_bias, int T, int N, int k, int gate, int32_t *idx, float *w, int *status,
+                       cudaStream_t s);
+// tensor-core router (bf16 x): W_g split into bf16 hi+mid+lo, split-K partial sums
+int router_tc_npad(int N);
+int router_tc_dpad(int d);
+int router_tc_max_splits(int T, int d);
+int launch_router_tc(const void *x, const float *Wg, int T, int d, int N, uint16_t *wsplit, float *partial,
+                     int *splits_out, int *status, cudaStream_t s);
 
 // dispatch
 constexpr int kDispatchChunk = 128;  // tokens per histogram / rank chunk
@@ -38,7 +45,7 @@ int launch_combine(bool bf16, const void *y_perm, const int32_t *dest_row, const
                    void *out, int T, int d, int k, cudaStream_t s);
 
 // load statistics
-constexpr int kStatsChunk = 256;
+constexpr int kStatsChunk = 32;  // tokens per partial-sum chunk
 int launch_load_stats(const float *logits, const int32_t *counts_routed, const int32_t *counts_kept, int T, int N,
                       int k, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s);
 

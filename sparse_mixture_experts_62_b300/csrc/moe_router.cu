@@ -115,8 +115,12 @@ __device__ __forceinline__ float sigmoid_f32(float z) {
   return (float)(1.0 / (1.0 + exp(-(double)z)));
 }
 
-// One warp per token; lane l holds experts l, l+32, ... (N <= 256).
-__global__ void __launch_bounds__(256) router_topk_kernel(const float *__restrict__ logits,
+// One warp per token; lane l holds experts l, l+32, ... (N <= 256).  The logits
+// are the sum of S partial tiles (row stride pstride, tile stride T * pstride),
+// added in split order, plus the optional logit bias; they are written to
+// `logits` (which may alias the only partial when S == 1 and no bias is added).
+__global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, int S, int pstride,
+                                                          const float *__restrict__ logit_bias, float *logits,
                                                           const float *__restrict__ sel_bias, int T, int N, int k,
                                                           int gate, int32_t *__restrict__ idx, float *__restrict__ w,
                                                           int *status) {
@@ -129,19 +133,74 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *__restric
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int e = lane + 32 * i;
+    if (e < N) {
+      float z = 0.f;
+      for (int sp = 0; sp < S; ++sp) z += partial[((size_t)sp * T + t) * pstride + e];
+      if (logit_bias) z += logit_bias[e];
+      logits[(size_t)t * N + e] = z;
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
     sel[i] = -INFINITY;
     if (e < N) {
       const float z = zr[e];
       if (!isfinite(z)) bad = true;
       float s = z;
       if (gate == MOE_GATE_SIGMOID_BIAS) {
-        s = sigmoid_f32(z);
+        s = 1.0f / (1.0f + expf(-z));  // estimate, see below
         if (sel_bias) s = s + sel_bias[e];
       }
       sel[i] = s;
     }
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
+  if (gate == MOE_GATE_SIGMOID_BIAS) {
+    // The selection score is fl32(s + b) with s = fl32(sigmoid(z)) evaluated in
+    // double.  The float32 estimate above (expf within 2 ulp, then one add and
+    // one division) is within 5.4e-7 of it, so an expert whose estimate is more
+    // than kSelMargin below the k-th largest estimate cannot be in the top k.
+    // Only the remaining candidates (almost always exactly k) are evaluated in
+    // double; the others drop out.
+    constexpr float kSelMargin = 4e-6f;
+    uint32_t taken0 = 0;
+    unsigned long long kth = 0;
+    for (int j = 0; j < k; ++j) {
+      unsigned long long best = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        if (e < N && !((taken0 >> i) & 1u)) {
+          const unsigned long long key = topk_key(sel[i], e);
+          best = key > best ? key : best;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+        best = o > best ? o : best;
+      }
+      const int e_best = (int)(0xFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+      if ((e_best & 31) == lane) taken0 |= 1u << (e_best >> 5);
+      kth = best;
+    }
+    const uint32_t ku = (uint32_t)(kth >> 32);
+    const float vk = __uint_as_float((ku & 0x80000000u) ? (ku & 0x7FFFFFFFu) : ~ku);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      if (e >= N) continue;
+      if (sel[i] >= vk - kSelMargin) {
+        float se = sigmoid_f32(zr[e]);
+        if (sel_bias) se = se + sel_bias[e];
+        sel[i] = se;
+      } else {
+        sel[i] = -INFINITY;
+      }
+    }
+  }
   uint32_t taken = 0;
   int chosen[8];
   for (int j = 0; j < k; ++j) {
@@ -209,10 +268,12 @@ int launch_router_logits(const void *x, bool x_bf16, const float *Wg, const floa
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-int launch_router_topk(const float *logits, const float *sel_bias, int T, int N, int k, int gate, int32_t *idx,
-                       float *w, int *status, cudaStream_t s) {
+int launch_router_topk(const float *partial, int S, int pstride, const float *logit_bias, float *logits,
+                       const float *sel_bias, int T, int N, int k, int gate, int32_t *idx, float *w, int *status,
+                       cudaStream_t s) {
   if (T == 0) return MOE_OK;
-  router_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, sel_bias, T, N, k, gate, idx, w, status);
+  router_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(partial, S, pstride, logit_bias, logits, sel_bias, T, N, k, gate,
+                                                 idx, w, status);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -7,8 +7,8 @@
 // assignments removed by the capacity limit.
 //
 // p_i(t) is the full N-way softmax of the logits (softmax gate) or
-// s_i / sum_l s_l with s = sigmoid(z) (sigmoid gate).  Partial sums per
-// 256-token chunk are reduced in a fixed order, so the result is deterministic.
+// s_i / sum_l s_l with s = sigmoid(z) (sigmoid gate), in float32.  Partial sums
+// per 32-token chunk are reduced in a fixed order, so the result is deterministic.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(const float *__restr
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
   const int tb = blockIdx.x * SC;
-  for (int tt = warp; tt < SC; tt += 8) {
+  for (int tt = warp; tt < SC; tt += 8) {  // SC / 8 tokens per warp
     const int t = tb + tt;
     if (t >= T) break;
     const float *zr = logits + (size_t)t * N;
@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(const float *__restr
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
       float p = 0.f;
-      if (e < N) p = (gate == MOE_GATE_SOFTMAX_TOPK) ? expf(v[i] - m) : (float)(1.0 / (1.0 + exp(-(double)v[i])));
+      if (e < N) p = (gate == MOE_GATE_SOFTMAX_TOPK) ? expf(v[i] - m) : 1.0f / (1.0f + expf(-v[i]));
       v[i] = p;
       sum += p;
     }
