@@ -56,8 +56,45 @@ def layer_bytes(wl, touched_experts: int) -> float:
 # dram__bytes_read.sum + dram__bytes_write.sum of the two grouped-GEMM launches of
 # one step, from one ncu capture of the kernel revision named here (None once the
 # kernel changes until it is captured again).
-NCU_TRAFFIC = {"mixtral_prefill": {"bytes": 3.675e9, "kernel_rev": "tc1"}}
-KERNEL_REV = "tc1"
+NCU_TRAFFIC = {"mixtral_prefill": {"bytes": 3.819e9, "kernel_rev": "pair1"}}
+KERNEL_REV = "pair1"
+
+
+def stage_work(wl, kept_rows: int, touched: int) -> dict:
+    """Algorithmic (flops, bytes) per stage of one layer step.
+
+    route: x read once, W_g, logits written, top-k ids + weights written;
+    dispatch: ids read, x rows read once, x_perm written, index arrays;
+    expert_ffn: kept rows' FLOPs; weights of touched experts, x_perm read, y_perm written;
+    shared_ffn: every token; its weights, x read, y written;
+    combine: y_perm (+ shared y) read, out written, ids + weights read;
+    load_stats: logits and counts read."""
+    es = 2 if wl.dtype == "bf16" else 4
+    mats = 3 if wl.act == "swiglu" else 2
+    T, d, N, k, F, S = wl.T, wl.d, wl.N, wl.k, wl.F, kept_rows
+    w = {
+        "route": (2.0 * T * d * N, T * d * es + d * N * 4 + T * N * 4 + T * k * 8),
+        "dispatch": (0.0, T * k * 4 + T * d * es + S * d * es + T * k * 4 + S * 4 + 3 * N * 4),
+        "expert_ffn": (2.0 * S * d * F * mats, touched * mats * d * F * es + 2 * S * d * es),
+        "combine": (0.0, S * d * es + T * d * es + T * k * 8 + (T * d * es if wl.shared_F else 0)),
+        "load_stats": (0.0, T * N * 4 + 2 * N * 4),
+    }
+    if wl.shared_F:
+        w["shared_ffn"] = (2.0 * T * d * wl.shared_F * mats, mats * d * wl.shared_F * es + 2 * T * d * es)
+    return w
+
+
+def stage_roofline(flops, nbytes, ms, peaks, sustained):
+    """The bound whose time is longer at peak; achieved rate and fraction of that peak."""
+    tf_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    t_tensor = flops / (tf_peak * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    s = ms / 1e3
+    if flops > 0 and t_tensor >= t_hbm:
+        return {"ms": ms, "bound": "tensor", "achieved": flops / s / 1e12, "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": t_tensor / s}
+    return {"ms": ms, "bound": "hbm", "achieved": nbytes / s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": t_hbm / s}
 
 
 def measured_peaks():
@@ -99,7 +136,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -134,10 +171,8 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        # under load: the upper half of the samples (the timed region dominates the window)
-        busy = sorted(sm)[len(sm) // 2:]
-        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -321,19 +356,17 @@ def run_ours(args, wl, dist, rank, local):
     touched = int(np.count_nonzero(counts_kept))
     fl = layer_flops(wl, kept_rows)
     peaks, peak_src = measured_peaks()
-    ffn_s = stage_ms["expert_ffn"] / 1e3
-    achieved_tflops = fl["expert_ffn"] / ffn_s / 1e12
-    peak_tf = peaks["bf16_tflops"]
-    roof = {"bound": "tensor", "achieved": achieved_tflops, "peak": peak_tf, "unit": "TFLOP/s",
-            "frac": achieved_tflops / peak_tf, "traffic": _traffic(wl.name),
-            "kernel": "grouped_gemm_kernel (tcgen05), moe_expert_ffn: gate/up + down launches",
-            "peak_source": f"{peak_src} bf16_tflops (burst)"}
-    if wl.T <= 64:  # decode: the layer streams weights; HBM governs
-        byts = layer_bytes(wl, touched)
-        gbs = byts / (ms_per_step / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": gbs / peaks["hbm_gbs"], "traffic": None, "kernel": "whole layer step",
-                "peak_source": f"{peak_src} hbm_gbs"}
+    clocks = clk.summary()
+    sustained = "sw_power_cap" in clocks.get("reasons", [])
+    work = stage_work(wl, kept_rows, touched)
+    stages = {n: stage_roofline(work[n][0], work[n][1], stage_ms[n], peaks, sustained) for n in stages}
+    ffn = stages["expert_ffn"]
+    roof = {"bound": ffn["bound"], "achieved": ffn["achieved"], "peak": ffn["peak"], "unit": ffn["unit"],
+            "frac": ffn["frac"], "traffic": _traffic(wl.name),
+            "kernel": "grouped_gemm (tcgen05), moe_expert_ffn: gate/up + down launches",
+            "peak_source": (f"{peak_src} " + ("hbm_gbs" if ffn["bound"] == "hbm" else
+                            ("bf16_tflops_sustained (power cap seen in the timed region)" if sustained
+                             else "bf16_tflops (burst)")))}
 
     # end to end through the public API: pinned host x in, out + stats back, every step
     x_host = x.cpu().pin_memory()
@@ -364,20 +397,22 @@ def run_ours(args, wl, dist, rank, local):
     h2d = x.numel() * x.element_size()
     d2h = out.numel() * out.element_size() + stats.numel() * 4
 
-    launches_per_step = 2 + 4 + 2 + (2 if has_shared else 0) + 1 + 2
+    # route: split W_g + tensor-core logits + top-k (bf16) or logits + top-k (float32);
+    # dispatch: histogram, scan, rank, gather; experts: 2; shared: 2; combine: 1; stats: 2
+    launches_per_step = (3 if wl.dtype == "bf16" else 2) + 4 + 2 + (2 if has_shared else 0) + 1 + 2
     if rank == 0:
         sys.stderr.write("per-stage ms: " + json.dumps({k: round(val, 4) for k, val in stage_ms.items()}) + "\n")
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic", "config": config_of(wl),
                 "roofline": roof,
-                "stage_ms": stage_ms,
+                "stages": stages,
                 "layer": {"flops": fl["total"], "tflops": fl["total"] / (ms_per_step / 1e3) / 1e12,
                           "kept_rows": kept_rows, "touched_experts": touched,
                           "algorithmic_bytes": layer_bytes(wl, touched)},
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches_per_step * args.steps,
-                "clocks": clk.summary()}
+                "clocks": clocks}
         if args.cpu_baseline_tokens > 0:
             line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_baseline_tokens)
         print(json.dumps(line), flush=True)
@@ -386,18 +421,25 @@ def run_ours(args, wl, dist, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-baseline-tokens", type=int, default=16,
                     help="tokens the oracle runs the expert FFN on for cpu_baseline (0 = skip)")
     ap.add_argument("--ref-sample", type=int, default=4, help="tokens per reference-arm step")
+    ap.add_argument("--override", nargs="*", default=[], help="workload fields to change, e.g. N=32 T=1024")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
     wl = synth.WORKLOADS[args.workload]
+    if args.override:  # smaller variants of a workload, for profiling captures
+        kw = {}
+        for item in args.override:
+            key, val = item.split("=")
+            kw[key] = type(getattr(wl, key))(val)
+        wl = wl.scaled(name=wl.name + "+" + ",".join(args.override), **kw)
     if args.impl == "reference":
         if rank == 0:
             run_reference(args, wl)

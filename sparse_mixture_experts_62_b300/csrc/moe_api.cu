@@ -127,10 +127,11 @@ int ffn_routed(const moe_config *c, const void *x_perm, const int32_t *offsets, 
   const int64_t rows = (int64_t)c->T * c->k;
   const int mode1 = c->act == MOE_ACT_SWIGLU ? 0 : 1;
   if (is_bf16(c)) {
+    const bool pair = use_pair_tiles(rows, c->N, c->capacity);
     MOE_TRY(tc_grouped_gemm(mode1, x_perm, rows, c->d, w1, w3, (int64_t)c->N * c->ffn, c->ffn, offsets, c->N, 0,
-                            c->ffn, h, status, s));
+                            c->ffn, h, status, pair, s));
     MOE_TRY(tc_grouped_gemm(2, h, rows, c->ffn, w2, nullptr, (int64_t)c->N * c->d, c->d, offsets, c->N, 0, c->d,
-                            y_perm, status, s));
+                            y_perm, status, pair, s));
   } else {
     MOE_TRY(simt_grouped_gemm(mode1, false, x_perm, rows, c->d, w1, w3, c->ffn, offsets, c->N, 0, c->ffn, h, s));
     MOE_TRY(simt_grouped_gemm(2, false, h, rows, c->ffn, w2, nullptr, c->d, offsets, c->N, 0, c->d, y_perm, s));
@@ -143,8 +144,9 @@ int ffn_shared(const moe_config *c, const void *x, const void *sw1, const void *
   const int mode1 = c->act == MOE_ACT_SWIGLU ? 0 : 1;
   const int Fs = c->shared_ffn;
   if (is_bf16(c)) {
-    MOE_TRY(tc_grouped_gemm(mode1, x, c->T, c->d, sw1, sw3, Fs, Fs, nullptr, 1, c->T, Fs, h, status, s));
-    MOE_TRY(tc_grouped_gemm(2, h, c->T, Fs, sw2, nullptr, c->d, c->d, nullptr, 1, c->T, c->d, y, status, s));
+    const bool pair = use_pair_tiles(c->T, 1, 0);
+    MOE_TRY(tc_grouped_gemm(mode1, x, c->T, c->d, sw1, sw3, Fs, Fs, nullptr, 1, c->T, Fs, h, status, pair, s));
+    MOE_TRY(tc_grouped_gemm(2, h, c->T, Fs, sw2, nullptr, c->d, c->d, nullptr, 1, c->T, c->d, y, status, pair, s));
   } else {
     MOE_TRY(simt_grouped_gemm(mode1, false, x, c->T, c->d, sw1, sw3, Fs, nullptr, 1, c->T, Fs, h, s));
     MOE_TRY(simt_grouped_gemm(2, false, h, c->T, Fs, sw2, nullptr, c->d, nullptr, 1, c->T, c->d, y, s));

@@ -287,6 +287,252 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------- CTA-pair form
+// The same grouped GEMM on pairs of SMs (a cluster of two CTAs) with
+// tcgen05.mma.cta_group::2: one pair computes a 256-row x 256-column tile.  Each
+// CTA stages its own 128 rows of A and its half of the B tile (128 rows), so a
+// CTA moves 32 KB per K block instead of 48 KB, which leaves room for six stages.
+// CTA rank 0 (the leader) issues the MMAs; each CTA's tensor memory receives its
+// 128 rows of the accumulator, which its own epilogue warps drain.
+//   full[s]   in the leader: both CTAs' bulk copies complete on it; the leader
+//             posts the expected bytes of both.
+//   empty[s]  in each CTA: the leader's MMA commit arrives on both.
+//   tfull[a]  in each CTA: the leader's commit after a tile arrives on both.
+//   tempty[a] in the leader: all 8 epilogue warps of the pair arrive on it.
+namespace pair {
+constexpr int BM = 128;                          // rows per CTA; 256 per pair
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;             // 16 KB
+constexpr int BH_BYTES = 128 * BK * 2;           // 16 KB: this CTA's half of B
+constexpr int STAGE_BYTES = A_BYTES + BH_BYTES;  // 32 KB
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + (size_t)(4 * MAX_GROUPS + 8) * 4;
+constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
+}  // namespace pair
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                             const __grid_constant__ CUtensorMap tmB1, const Args args) {
+  constexpr int STAGES = pair::STAGES, STAGE_BYTES = pair::STAGE_BYTES, A_BYTES = pair::A_BYTES;
+  constexpr int BM = pair::BM;
+  constexpr uint32_t IDESC = pair::IDESC;
+  constexpr int OUT_COLS = (MODE == kSwiGLU) ? 128 : 256;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
+  uint64_t *tempty = tfull + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  int *tile_start = reinterpret_cast<int *>(smem + STAGES * STAGE_BYTES + 256);
+  int *mtiles = tile_start + MAX_GROUPS + 1;
+  int *rowbeg = mtiles + MAX_GROUPS;
+  int *rowend = rowbeg + MAX_GROUPS;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair_id = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int G = args.G;
+  const int n_tiles = (args.n_out + OUT_COLS - 1) / OUT_COLS;
+  const int num_kb = (args.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);
+    }
+    fence_barrier_init();
+    int acc = 0;
+    for (int g = 0; g < G; ++g) {
+      int b = args.offsets ? args.offsets[g] : 0;
+      int e = args.offsets ? args.offsets[g + 1] : args.M;
+      if (b < 0 || e < b || e > args.a_rows) {
+        set_status(args.status, MOE_ERR_BOUNDS);
+        b = e = 0;
+      }
+      rowbeg[g] = b;
+      rowend[g] = e;
+      const int mt = e > b ? (e - b + 2 * BM - 1) / (2 * BM) : 0;
+      mtiles[g] = mt;
+      tile_start[g] = acc;
+      acc += mt * n_tiles;
+    }
+    tile_start[G] = acc;
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB0);
+    if (MODE == kSwiGLU) tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA use
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = tile_start[G];
+  const uint32_t full_lead = mapa_shared(smem_u32(&full[0]), 0);
+  const uint32_t tempty_lead = mapa_shared(smem_u32(&tempty[0]), 0);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    if (lane == 0) {
+      int issued_parity[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      int g = 0;
+      bool ok = true;
+      const CUtensorMap *mb = (MODE == kSwiGLU && rank == 1) ? &tmB1 : &tmB0;
+      for (int tile = pair_id; tile < total_tiles && ok; tile += npairs) {
+        while (tile >= tile_start[g + 1]) ++g;
+        const int local = tile - tile_start[g];
+        const int n_tile = local / mtiles[g];
+        const int m_tile = local - n_tile * mtiles[g];
+        const int a_row = rowbeg[g] + m_tile * 2 * BM + (int)rank * BM;
+        const int b_row = (MODE == kSwiGLU) ? g * args.b_rows + n_tile * OUT_COLS
+                                            : g * args.b_rows + n_tile * OUT_COLS + (int)rank * 128;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, args.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t *sa = smem + stage * STAGE_BYTES;
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2u * STAGE_BYTES);
+          const uint32_t fb = full_lead + 8u * stage;
+          tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row);
+          tma_load_2d_pair(sa + A_BYTES, mb, fb, kb * BK, b_row);
+          issued_parity[stage] = (int)phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // the leader's full barriers count both CTAs' copies: wait for the last ones
+      if (leader)
+        for (int s = 0; s < STAGES; ++s)
+          if (issued_parity[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_parity[s], args.status);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader only)
+    if (leader && lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = pair_id; tile < total_tiles && ok; tile += npairs, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, args.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+          const uint64_t adesc = smem_desc_sw128(sa);
+          const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16_pair(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, IDESC, (kb | kk) != 0);
+          tc_commit_pair(&empty[stage], 0x3);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) tc_commit_pair(&tfull[acc], 0x3);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    int g = 0;
+    int it = 0;
+    for (int tile = pair_id; tile < total_tiles; tile += npairs, ++it) {
+      while (tile >= tile_start[g + 1]) ++g;
+      const int local = tile - tile_start[g];
+      const int n_tile = local / mtiles[g];
+      const int m_tile = local - n_tile * mtiles[g];
+      const int row0 = rowbeg[g] + m_tile * 2 * BM + (int)rank * BM;
+      const int rows_valid = min(BM, rowend[g] - row0);
+      const int n0 = n_tile * OUT_COLS;
+      const int acc = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!mbar_wait(&tfull[acc], use & 1u, args.status)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
+      const bool row_ok = r < rows_valid;
+      uint16_t *orow = args.out + (size_t)(row_ok ? row0 + r : 0) * args.n_out;
+      if (MODE == kSwiGLU) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 16) {
+          float a[16], u[16];
+          tmem_ld16x2(taddr + c, taddr + 128 + c, a, u);
+          uint32_t p[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) p[i] = pack_bf16x2(silu(a[2 * i]) * u[2 * i], silu(a[2 * i + 1]) * u[2 * i + 1]);
+          const int col = n0 + c;
+          if (row_ok) {
+            if (col + 8 <= args.n_out) *reinterpret_cast<uint4 *>(orow + col) = make_uint4(p[0], p[1], p[2], p[3]);
+            if (col + 16 <= args.n_out)
+              *reinterpret_cast<uint4 *>(orow + col + 8) = make_uint4(p[4], p[5], p[6], p[7]);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          float v0[16], v1[16];
+          tmem_ld16x2(taddr + c, taddr + c + 16, v0, v1);
+          uint32_t p[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float x0 = v0[2 * i], x1 = v0[2 * i + 1], y0 = v1[2 * i], y1 = v1[2 * i + 1];
+            if (MODE == kReLU) {
+              x0 = fmaxf(x0, 0.f);
+              x1 = fmaxf(x1, 0.f);
+              y0 = fmaxf(y0, 0.f);
+              y1 = fmaxf(y1, 0.f);
+            }
+            p[i] = pack_bf16x2(x0, x1);
+            p[8 + i] = pack_bf16x2(y0, y1);
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int col = n0 + c + 8 * q;
+              if (col + 8 <= args.n_out)
+                *reinterpret_cast<uint4 *>(orow + col) = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_lead + 8u * acc);
+    }
+  }
+
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal its barriers
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -321,6 +567,57 @@ static int make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t co
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// CTA pairs that can run at once (cluster occupancy), per device.
+template <int MODE>
+static int pair_grid(int device) {
+  static std::mutex mu;
+  static std::vector<int> cache;
+  std::lock_guard<std::mutex> lk(mu);
+  if ((int)cache.size() <= device) cache.resize(device + 1, 0);
+  if (!cache[device]) {
+    if (cudaFuncSetAttribute(grouped_gemm_pair_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)pair::SMEM_BYTES) != cudaSuccess)
+      return -1;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * device_sm_count(device));
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_pair_kernel<MODE>, &cfg) != cudaSuccess || clusters < 1)
+      return -1;
+    cache[device] = 2 * clusters;
+  }
+  return cache[device];
+}
+
+template <int MODE>
+static int launch_pair(const CUtensorMap &ma, const CUtensorMap &mb0, const CUtensorMap &mb1, const Args &args,
+                       int device, cudaStream_t stream) {
+  const int grid = pair_grid<MODE>(device);
+  if (grid < 2) return MOE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = pair::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ma, mb0, mb1, args) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 template <int MODE>
 static int prepare_kernel(int device) {
   static std::mutex mu;
@@ -340,7 +637,7 @@ static int prepare_kernel(int device) {
 
 int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
                     int64_t b_rows_total, int b_rows_per_group, const int32_t *offsets, int G, int M, int n_out,
-                    void *out, int *status, cudaStream_t stream) {
+                    void *out, int *status, bool pair_tiles, cudaStream_t stream) {
   using namespace tc;
   if (G < 1 || G > MAX_GROUPS || K < 1 || n_out < 1 || a_rows < 1 || b_rows_total < 1) return MOE_ERR_INVALID_ARG;
   if (a_rows > INT32_MAX || n_out > b_rows_per_group || (int64_t)G * b_rows_per_group > b_rows_total)
@@ -360,6 +657,13 @@ int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *
   const int sms = device_sm_count(dev);
   if (sms <= 0) return MOE_ERR_CUDA;
   Args args{offsets, G, M, (int32_t)a_rows, n_out, K, b_rows_per_group, static_cast<uint16_t *>(out), status};
+  if (pair_tiles) {
+    switch (mode) {
+      case kSwiGLU: return launch_pair<kSwiGLU>(ma, mb0, mb1, args, dev, stream);
+      case kReLU: return launch_pair<kReLU>(ma, mb0, mb1, args, dev, stream);
+      default: return launch_pair<kPlain>(ma, mb0, mb1, args, dev, stream);
+    }
+  }
   dim3 grid(sms), block(THREADS);
   switch (mode) {
     case kSwiGLU:

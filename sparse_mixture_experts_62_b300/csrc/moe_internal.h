@@ -30,10 +30,17 @@ int launch_dispatch(const int32_t *idx, int T, int k, int N, int capacity, int32
 int launch_gather_rows(const void *x, const int32_t *src_token, const int32_t *offsets_end, int64_t max_rows,
                        int row_bytes, void *x_perm, cudaStream_t s);
 
-// grouped GEMM on tcgen05 (bf16); mode 0 = SwiGLU (B0 = W1, B1 = W3), 1 = ReLU, 2 = plain
+// grouped GEMM on tcgen05 (bf16); mode 0 = SwiGLU (B0 = W1, B1 = W3), 1 = ReLU, 2 = plain.
+// pair_tiles: 256-row tiles on CTA pairs (cta_group::2) instead of 128-row tiles on
+// single CTAs -- faster when groups hold many rows, wasteful when they are small.
 int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
                     int64_t b_rows_total, int b_rows_per_group, const int32_t *offsets, int G, int M, int n_out,
-                    void *out, int *status, cudaStream_t stream);
+                    void *out, int *status, bool pair_tiles, cudaStream_t stream);
+// Tile choice for expert groups: pairs when the mean group holds >= 512 rows and no
+// capacity limit can skew the groups.
+inline bool use_pair_tiles(int64_t rows, int groups, int capacity) {
+  return capacity <= 0 && rows >= (int64_t)512 * groups;
+}
 
 // grouped GEMM on the CUDA cores (float32 workloads); same modes, out in the input dtype
 int simt_grouped_gemm(int mode, bool bf16, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,

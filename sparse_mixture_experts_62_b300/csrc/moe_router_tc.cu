@@ -76,7 +76,8 @@ __global__ void __launch_bounds__(256) split_wg_kernel(const float *__restrict__
 // same way; over a K of several thousand that bias reaches 1e-4.  So the MMAs
 // of one k-block (K = 64, four MMAs) go into a fresh tensor-memory buffer and
 // the epilogue warps add that buffer into float32 registers (round to nearest)
-// while the MMAs of the next k-block fill the other buffer.
+// while the MMAs of the next k-blocks fill the other buffers (up to eight in
+// rotation, so the MMAs are not held up by each buffer's round trip).
 template <int NP>
 __global__ void __launch_bounds__(64 + 32 * (NP > 128 ? 8 : 4), 1)
     router_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
@@ -84,15 +85,18 @@ __global__ void __launch_bounds__(64 + 32 * (NP > 128 ? 8 : 4), 1)
   constexpr int COLS = NP / (EW / 4);           // accumulator columns per epilogue thread
   constexpr int B_BYTES = NP * BK * 2;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  constexpr uint32_t TMEM_COLS = (2 * NP) < 32 ? 32 : 2 * NP;
+  // tensor-memory buffers in rotation, sized so that the CTAs that fit on one SM
+  // by shared memory (two for NP <= 64, one above) share its 512 columns
+  constexpr int NBUF = NP == 32 ? 8 : (NP == 64 ? 4 : (NP == 128 ? 4 : 2));
+  constexpr uint32_t TMEM_COLS = NBUF * NP;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;
-  uint64_t *tempty = tfull + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  uint64_t *tempty = tfull + NBUF;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + NBUF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tile = blockIdx.x / a.S, split = blockIdx.x % a.S;
@@ -104,7 +108,7 @@ __global__ void __launch_bounds__(64 + 32 * (NP > 128 ? 8 : 4), 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NBUF; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], EW);
     }
@@ -146,8 +150,8 @@ __global__ void __launch_bounds__(64 + 32 * (NP > 128 ? 8 : 4), 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
-        const int b = it & 1;
-        const uint32_t use = (uint32_t)(it >> 1);
+        const int b = it % NBUF;
+        const uint32_t use = (uint32_t)(it / NBUF);
         if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, a.status)) break;
         if (!mbar_wait(&full[stage], phase, a.status)) break;
         tc_fence_after();
@@ -176,8 +180,8 @@ __global__ void __launch_bounds__(64 + 32 * (NP > 128 ? 8 : 4), 1)
     for (int i = 0; i < COLS; ++i) acc[i] = 0.f;
     bool ok = true;
     for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
-      const int b = it & 1;
-      const uint32_t use = (uint32_t)(it >> 1);
+      const int b = it % NBUF;
+      const uint32_t use = (uint32_t)(it / NBUF);
       if (!mbar_wait(&tfull[b], use & 1u, a.status)) {
         ok = false;
         break;
@@ -242,7 +246,7 @@ static int make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t co
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
-static size_t smem_bytes(int Npad) { return 1024 + (size_t)STAGES * (A_BYTES + Npad * BK * 2) + 128; }
+static size_t smem_bytes(int Npad) { return 1024 + (size_t)STAGES * (A_BYTES + Npad * BK * 2) + 256; }
 static int threads_for(int Npad) { return 64 + 32 * (Npad > 128 ? 8 : 4); }
 
 template <int NP>
@@ -271,7 +275,7 @@ int router_tc_dpad(int d) { return (d + 63) / 64 * 64; }
 int router_tc_max_splits(int T, int d) {
   const int mtiles = std::max(1, (T + 127) / 128);
   const int nkb = 3 * (router_tc_dpad(d) / 64);
-  return std::max(1, std::min(nkb, 512 / mtiles));
+  return std::max(1, std::min(std::min(nkb, 64), 512 / mtiles));
 }
 
 static int plan_splits(int T, int d, int Npad, int sms) {

@@ -66,43 +66,53 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(const float *__restr
   }
 }
 
-__global__ void __launch_bounds__(256) stats_final_kernel(const float *__restrict__ partial, int nchunks,
-                                                          const int32_t *__restrict__ counts_routed,
-                                                          const int32_t *__restrict__ counts_kept, int T, int N, int k,
-                                                          float *__restrict__ f, float *__restrict__ P,
-                                                          float *__restrict__ summary) {
-  __shared__ double fp[256];
+// One CTA of 1024 threads: four threads per expert each add every fourth chunk,
+// then the four partial sums are added in a fixed order.
+__global__ void __launch_bounds__(1024) stats_final_kernel(const float *__restrict__ partial, int nchunks,
+                                                           const int32_t *__restrict__ counts_routed,
+                                                           const int32_t *__restrict__ counts_kept, int T, int N,
+                                                           int k, float *__restrict__ f, float *__restrict__ P,
+                                                           float *__restrict__ summary) {
+  __shared__ float quarter[4][256];
+  __shared__ float fp[256];
   __shared__ int maxc[256];
   __shared__ long long kept[256];
-  const int e = threadIdx.x;
-  const double tk = (double)T * (double)k;
-  double fe = 0.0, pe = 0.0;
-  int ce = 0;
-  long long ke = 0;
-  if (e < N) {
-    double s = 0.0;
-    for (int c = 0; c < nchunks; ++c) s += (double)partial[(size_t)c * N + e];
-    pe = s / (double)T;
-    ce = counts_routed[e];
-    ke = counts_kept[e];
-    fe = (double)ce / tk;
-    f[e] = (float)fe;
-    P[e] = (float)pe;
+  const int e = threadIdx.x & 255, q = threadIdx.x >> 8;
+  float s = 0.f;
+  if (e < N)
+    for (int c = q; c < nchunks; c += 4) s += partial[(size_t)c * N + e];
+  quarter[q][e] = s;
+  __syncthreads();
+  if (q == 0) {
+    const float tk = (float)T * (float)k;
+    float fe = 0.f, pe = 0.f;
+    int ce = 0;
+    long long ke = 0;
+    if (e < N) {
+      pe = (((quarter[0][e] + quarter[1][e]) + quarter[2][e]) + quarter[3][e]) / (float)T;
+      ce = counts_routed[e];
+      ke = counts_kept[e];
+      fe = (float)((double)ce / ((double)T * (double)k));
+      f[e] = fe;
+      P[e] = pe;
+    }
+    fp[e] = fe * pe;
+    maxc[e] = ce;
+    kept[e] = ke;
+    (void)tk;
   }
-  fp[e] = fe * pe;
-  maxc[e] = ce;
-  kept[e] = ke;
   __syncthreads();
   for (int off = 128; off > 0; off >>= 1) {
-    if (e < off) {
+    if (q == 0 && e < off) {
       fp[e] += fp[e + off];
       maxc[e] = max(maxc[e], maxc[e + off]);
       kept[e] += kept[e + off];
     }
     __syncthreads();
   }
-  if (e == 0) {
-    summary[0] = (float)((double)N * fp[0]);
+  if (threadIdx.x == 0) {
+    const double tk = (double)T * (double)k;
+    summary[0] = (float)N * fp[0];
     summary[1] = (float)((double)maxc[0] / (tk / (double)N));
     summary[2] = (float)(1.0 - (double)kept[0] / tk);
   }
@@ -115,7 +125,7 @@ int launch_load_stats(const float *logits, const int32_t *counts_routed, const i
   if (T == 0) return MOE_OK;
   const int nchunks = (T + SC - 1) / SC;
   stats_partial_kernel<<<nchunks, 256, 0, s>>>(logits, T, N, gate, partial);
-  stats_final_kernel<<<1, 256, 0, s>>>(partial, nchunks, counts_routed, counts_kept, T, N, k, f, P, summary);
+  stats_final_kernel<<<1, 1024, 0, s>>>(partial, nchunks, counts_routed, counts_kept, T, N, k, f, P, summary);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

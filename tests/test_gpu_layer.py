@@ -57,6 +57,7 @@ SMALL = [
     dict(T=50, d=128, N=4, k=4, F=192),
     dict(T=129, d=320, N=7, k=2, F=136, act="relu"),
     dict(T=1, d=64, N=8, k=2, F=64),
+    dict(T=1500, d=256, N=4, k=2, F=384),                                  # CTA-pair tiles (750 rows/expert)
 ]
 
 

@@ -64,6 +64,13 @@ def test_tc_gemm_ragged_groups(act):
     _expert_ffn_case(5, [0, 1, 130, 257, 64], d=192, F=320, act=act, seed=2)
 
 
+@pytest.mark.parametrize("act", ["swiglu", "relu"])
+def test_tc_gemm_pair_tiles(act):
+    """Groups averaging >= 512 rows run on CTA pairs (256-row tiles): a last pair
+    tile with rows for one CTA only, F and d not multiples of the tile width."""
+    _expert_ffn_case(3, [600, 1100, 301], d=320, F=520, act=act, seed=4)
+
+
 def test_tc_gemm_many_experts_deep_k():
     _expert_ffn_case(16, [3, 40, 0, 200, 129, 1, 77, 128, 256, 5, 0, 9, 64, 300, 17, 2], d=1024, F=512,
                      act="swiglu", seed=3)
