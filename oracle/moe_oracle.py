@@ -80,10 +80,10 @@ def sigmoid_affinity(z: np.ndarray) -> np.ndarray:
 def selection_scores(z: np.ndarray, gate: str, sel_bias: Optional[np.ndarray]):
     """Returns (sel, s): the scores top-k ranks on, and the sigmoid affinities (or None).
 
-    softmax gate: sel = z (softmax is monotone, so ranking z ranks the
+    softmax gates: sel = z (softmax is monotone, so ranking z ranks the
     probabilities).  sigmoid gate: sel = fl32(s + b), where the bias b only
     steers the choice (Chapter 19, 19.3.4; CS336 lecture 4, section 9)."""
-    if gate == "softmax":
+    if gate in ("softmax", "softmax_full"):
         return z, None
     s = sigmoid_affinity(z)
     if sel_bias is None:
@@ -106,6 +106,9 @@ def gate_weights(z: np.ndarray, s: Optional[np.ndarray], idx: np.ndarray, gate: 
 
     softmax: g_j = exp(z_j) / sum_{l in S} exp(z_l)  (Lecture29 "Top-two routing";
       shifted by the selected maximum, which cancels).
+    softmax_full: g_j = exp(z_j) / sum_{l=1..N} exp(z_l), the full softmax kept
+      on the top-k and not renormalised (CS336 lecture 4, section 5 pseudocode:
+      s = softmax(u . e); g_i = s_i if i in TopK(s) else 0).
     sigmoid: g_j = s_j / sum_{l in S} s_l from the raw affinities, no bias
       (Chapter 19, 19.3.4)."""
     T, k = idx.shape
@@ -115,6 +118,10 @@ def gate_weights(z: np.ndarray, s: Optional[np.ndarray], idx: np.ndarray, gate: 
             zs = z[t, idx[t]].astype(np.float64)
             e = np.exp(zs - zs.max())
             w[t] = e / e.sum()
+        elif gate == "softmax_full":
+            zt = z[t].astype(np.float64)
+            e = np.exp(zt - zt.max())
+            w[t] = e[idx[t]] / e.sum()
         else:
             ss = s[t, idx[t]].astype(np.float64)
             w[t] = ss / ss.sum()
@@ -220,7 +227,7 @@ class LoadStats:
 def router_probabilities(z: np.ndarray, gate: str) -> np.ndarray:
     """p_i(t): the full N-way softmax of z, or s_i / sum_l s_l for the sigmoid gate."""
     z64 = z.astype(np.float64)
-    if gate == "softmax":
+    if gate in ("softmax", "softmax_full"):
         e = np.exp(z64 - z64.max(axis=1, keepdims=True))
         return e / e.sum(axis=1, keepdims=True)
     s = sigmoid_affinity(z).astype(np.float64)
@@ -237,6 +244,34 @@ def load_stats(z: np.ndarray, gate: str, d: Dispatch, k: int) -> LoadStats:
     imb = float(d.counts_routed.max()) / (T * k / N)
     drop = 1.0 - float(d.offsets[N]) / (T * k)
     return LoadStats(f, P, aux, imb, drop)
+
+
+# --------------------------------------------------------------------------- router training-side reductions
+def router_z_loss(z: np.ndarray) -> float:
+    """mean over tokens of (log Z)^2, Z = sum_i exp(z_i): the router z-loss.
+
+    CS336 lecture 4, section 11 (the square of the softmax normaliser's log is
+    added as a loss); Chapter 19, 19.6.2 (it penalises the log-sum-exp of the
+    logits, not their L2 norm).  log Z is taken as m + log sum exp(z - m)."""
+    z64 = z.astype(np.float64)
+    m = z64.max(axis=1, keepdims=True)
+    lse = m[:, 0] + np.log(np.exp(z64 - m).sum(axis=1))
+    return float(np.mean(lse ** 2))
+
+
+def bias_update(sel_bias: np.ndarray, counts_routed: np.ndarray, T: int, k: int, gamma: float) -> np.ndarray:
+    """DeepSeek-V3 auxiliary-loss-free balancing, one step after a batch:
+    b_i + gamma if expert i got fewer than the mean T k / N assignments,
+    b_i - gamma if it got more, unchanged if exactly the mean (CS336 lecture 4,
+    section 9; Chapter 19, 19.3.4).  Returned in float32."""
+    N = len(counts_routed)
+    out = sel_bias.astype(np.float64).copy()
+    for i in range(N):
+        if counts_routed[i] * N < T * k:
+            out[i] += gamma
+        elif counts_routed[i] * N > T * k:
+            out[i] -= gamma
+    return out.astype(np.float32)
 
 
 # --------------------------------------------------------------------------- layer

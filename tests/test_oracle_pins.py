@@ -396,3 +396,42 @@ def test_combine_hand_computed():
     assert out.tolist() == [[75.25, 150.5], [5.0, 10.0]]
     out = oracle.combine(y_rows, dest, w, np.array([[1.0, 1.0], [2.0, 2.0]]))
     assert out.tolist() == [[76.25, 151.5], [7.0, 12.0]]
+
+
+# --------------------------------------------------------------------------- gate variants, router reductions
+def test_softmax_full_gate_is_unrenormalised_full_softmax():
+    """CS336 lecture 4, section 5: g_i = softmax(z)_i on the top-k, 0 elsewhere;
+    renormalising it over the top-k gives the top-k softmax gate (Chapter 19,
+    19.3.2), and with k = N it sums to 1."""
+    rng = np.random.default_rng(5)
+    z = (rng.standard_normal((100, 16)) * 2).astype(np.float32)
+    idx = oracle.topk(z, 4)
+    w_full = oracle.gate_weights(z, None, idx, "softmax_full")
+    p = scipy.special.softmax(z.astype(np.float64), axis=1)
+    assert np.max(np.abs(w_full - np.take_along_axis(p, idx.astype(np.int64), axis=1))) < 1e-14
+    assert np.all(w_full.sum(axis=1) < 1.0)
+    w_top = oracle.gate_weights(z, None, idx, "softmax")
+    assert np.max(np.abs(w_full / w_full.sum(axis=1, keepdims=True) - w_top)) < 1e-12
+    idx_all = oracle.topk(z, 16)
+    assert np.allclose(oracle.gate_weights(z, None, idx_all, "softmax_full").sum(axis=1), 1.0, atol=1e-14)
+
+
+def test_router_z_loss_closed_forms():
+    """All logits equal to c: log Z = c + log N exactly, so the loss is (c + log N)^2;
+    one dominant logit L: log Z -> L."""
+    for c, N in [(0.0, 8), (1.5, 4), (-2.0, 256)]:
+        z = np.full((7, N), c, dtype=np.float32)
+        assert oracle.router_z_loss(z) == pytest.approx((c + math.log(N)) ** 2, rel=1e-12)
+    z = np.array([[30.0, 0.0, 0.0]], dtype=np.float32)
+    assert oracle.router_z_loss(z) == pytest.approx((30.0 + math.log1p(2 * math.exp(-30.0))) ** 2, rel=1e-14)
+    # shift invariance fails on purpose: the loss penalises the scale of the logits
+    z2 = np.random.default_rng(1).standard_normal((50, 8)).astype(np.float32)
+    assert oracle.router_z_loss(z2 + 3) > oracle.router_z_loss(z2)
+
+
+def test_bias_update_signs():
+    """+gamma below the mean load, -gamma above it, unchanged at exactly the mean."""
+    counts = np.array([0, 5, 10, 25], dtype=np.int64)   # T k / N = 40 / 4 = 10
+    b = np.array([0.5, -0.1, 0.0, 0.2], dtype=np.float32)
+    out = oracle.bias_update(b, counts, T=20, k=2, gamma=0.01)
+    assert out.tolist() == pytest.approx([0.51, -0.09, 0.0, 0.19], abs=1e-7)
