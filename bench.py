@@ -84,15 +84,22 @@ def stage_work(wl, kept_rows: int, touched: int) -> dict:
     return w
 
 
-def stage_roofline(flops, nbytes, ms, peaks, sustained):
+# float32 CUDA-core peak: 148 SMs x 128 FP32 lanes x 2 FLOP (one FMA) x 2032 MHz
+# (maximum SM clock) = 77.0 TFLOP/s; the float32 workload's GEMMs run there.
+F32_ALU_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
+
+
+def stage_roofline(flops, nbytes, ms, peaks, sustained, alu=False):
     """The bound whose time is longer at peak; achieved rate and fraction of that peak."""
     tf_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    if alu:
+        tf_peak = F32_ALU_TFLOPS
     t_tensor = flops / (tf_peak * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     s = ms / 1e3
     if flops > 0 and t_tensor >= t_hbm:
-        return {"ms": ms, "bound": "tensor", "achieved": flops / s / 1e12, "peak": tf_peak, "unit": "TFLOP/s",
-                "frac": t_tensor / s}
+        return {"ms": ms, "bound": "alu" if alu else "tensor", "achieved": flops / s / 1e12, "peak": tf_peak,
+                "unit": "TFLOP/s", "frac": t_tensor / s}
     return {"ms": ms, "bound": "hbm", "achieved": nbytes / s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": t_hbm / s}
 
@@ -273,7 +280,8 @@ def build_layer(moe, inp):
     wl = inp.wl
     cap = moe.moe_capacity(wl.capacity_factor, wl.T, wl.k, wl.N) if wl.capacity_factor > 0 else 0
     cfg = moe.make_config(wl.T, wl.d, wl.N, wl.k, wl.F, wl.shared_F,
-                          moe.GATE_SIGMOID_BIAS if wl.gate == "sigmoid" else moe.GATE_SOFTMAX_TOPK,
+                          {"softmax": moe.GATE_SOFTMAX_TOPK, "sigmoid": moe.GATE_SIGMOID_BIAS,
+                           "softmax_full": moe.GATE_SOFTMAX_FULL}[wl.gate],
                           moe.ACT_SWIGLU if wl.act == "swiglu" else moe.ACT_RELU,
                           moe.DTYPE_BF16 if wl.dtype == "bf16" else moe.DTYPE_F32, cap)
     dt = wl.dtype
@@ -295,14 +303,16 @@ def run_ours(args, wl, dist, rank, local):
     out = torch.empty((wl.T, wl.d), dtype=x.dtype, device="cuda")
     cfg, ws, v = layer.cfg, layer.ws, layer.views()
     stream = torch.cuda.current_stream()
-    s = stream.cuda_stream
     stats = torch.zeros(2 * wl.N + 4, dtype=torch.float32, device="cuda")
     has_shared = wl.shared_F > 0
     stages = ["route", "dispatch", "expert_ffn"] + (["shared_ffn"] if has_shared else []) + ["combine", "load_stats"]
 
     def step(ev=None):
-        # the launches of moe_layer_forward, stage by stage, + the statistics
-        rec = (lambda i: ev[i].record(stream)) if ev is not None else (lambda i: None)
+        # the launches of moe_layer_forward, stage by stage, + the statistics, on
+        # the current stream (which is the capture stream while a graph records)
+        cur = torch.cuda.current_stream()
+        s = cur.cuda_stream
+        rec = (lambda i: ev[i].record(cur)) if ev is not None else (lambda i: None)
         rec(0)
         moe.moe_route(cfg, x, layer.Wg, layer.logit_bias, layer.sel_bias, v["logits"], v["topk_idx"], v["topk_w"],
                       ws, s)
@@ -328,8 +338,29 @@ def run_ours(args, wl, dist, rank, local):
     torch.cuda.synchronize()
     if layer.device_status() != 0:
         raise RuntimeError("device status not clean after warm-up")
+    # per-stage durations: an eager pass with events between the stages
     nev = len(stages) + 1
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
+    for k in range(args.steps):
+        step(evs[k])
+    torch.cuda.synchronize()
+    stage_ms = {n: float(np.mean([evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps)]))
+                for j, n in enumerate(stages)}
+    # the timed region: the step captured once as a CUDA graph and replayed (the
+    # same launches, without the host's per-call overhead); eager if capture fails
+    graph = None
+    if not args.eager:
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step()
+            for _ in range(args.warmup):
+                graph.replay()
+            torch.cuda.synchronize()
+        except RuntimeError as exc:  # pragma: no cover - reported, then timed eagerly
+            sys.stderr.write(f"graph capture failed ({exc}); timing eager launches\n")
+            graph = None
+    run = graph.replay if graph is not None else step
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
@@ -337,14 +368,14 @@ def run_ours(args, wl, dist, rank, local):
     with ClockSampler(local) as clk:
         start.record(stream)
         for k in range(args.steps):
-            step(evs[k])
+            run()
         end.record(stream)
         torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
+    if layer.device_status() != 0:
+        raise RuntimeError("device status not clean after the timed region")
     total_ms = start.elapsed_time(end)
-    stage_ms = {n: float(np.mean([evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps)]))
-                for j, n in enumerate(stages)}
     t_max = max_over_ranks(dist, total_ms)
     ms_per_step = t_max / args.steps
     world = dist.get_world_size() if dist is not None else 1
@@ -359,37 +390,84 @@ def run_ours(args, wl, dist, rank, local):
     clocks = clk.summary()
     sustained = "sw_power_cap" in clocks.get("reasons", [])
     work = stage_work(wl, kept_rows, touched)
-    stages = {n: stage_roofline(work[n][0], work[n][1], stage_ms[n], peaks, sustained) for n in stages}
+    f32 = wl.dtype == "f32"
+    stages = {n: stage_roofline(work[n][0], work[n][1], stage_ms[n], peaks, sustained,
+                                alu=f32 and n in ("route", "expert_ffn", "shared_ffn")) for n in stages}
     ffn = stages["expert_ffn"]
     roof = {"bound": ffn["bound"], "achieved": ffn["achieved"], "peak": ffn["peak"], "unit": ffn["unit"],
             "frac": ffn["frac"], "traffic": _traffic(wl.name),
             "kernel": "grouped_gemm (tcgen05), moe_expert_ffn: gate/up + down launches",
-            "peak_source": (f"{peak_src} " + ("hbm_gbs" if ffn["bound"] == "hbm" else
+            "peak_source": ("derived float32 CUDA-core peak (148 SMs x 128 lanes x 2 FLOP x 2032 MHz)"
+                            if ffn["bound"] == "alu" else f"{peak_src} " + ("hbm_gbs" if ffn["bound"] == "hbm" else
                             ("bf16_tflops_sustained (power cap seen in the timed region)" if sustained
                              else "bf16_tflops (burst)")))}
 
-    # end to end through the public API: pinned host x in, out + stats back, every step
+    # End to end through the public API: every step copies its x in from pinned host
+    # memory and its output and statistics back.  Copies run on their own streams
+    # with two device buffers, so step i+1's upload and step i-1's readback overlap
+    # step i's compute (the layer's workspace keeps compute on one stream).
     x_host = x.cpu().pin_memory()
-    out_host = torch.empty_like(out, device="cpu").pin_memory()
-    stats_host = torch.empty_like(stats, device="cpu").pin_memory()
-    x_dev = torch.empty_like(x)
+    out_host = [torch.empty_like(out, device="cpu").pin_memory() for _ in range(2)]
+    stats_host = [torch.empty_like(stats, device="cpu").pin_memory() for _ in range(2)]
+    x_dev = [torch.empty_like(x) for _ in range(2)]
+    out_dev = [torch.empty_like(out) for _ in range(2)]
+    stats_dev = [torch.empty_like(stats) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    x_ready, comp_done, x_free, out_free = ([ev(), ev()] for _ in range(4))
+    for b in range(2):
+        x_free[b].record(stream)
+        out_free[b].record(stream)
 
-    def e2e_step():
-        x_dev.copy_(x_host, non_blocking=True)
-        layer.forward(x_dev, out)
-        f, P, summ = layer.load_stats()
-        out_host.copy_(out, non_blocking=True)
-        stats_host.copy_(layer._stats, non_blocking=True)
+    def compute(b):
+        layer.forward(x_dev[b], out_dev[b])
+        layer.load_stats()
+        stats_dev[b].copy_(layer._stats)  # this step's statistics, off the shared buffer
 
-    for _ in range(args.warmup):
-        e2e_step()
+    # the compute of each buffer slot as a CUDA graph (the copies stay on their streams)
+    slot_graphs = None
+    if graph is not None:
+        slot_graphs = []
+        for b in range(2):
+            compute(b)  # warm
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                compute(b)
+            slot_graphs.append(g)
+        torch.cuda.synchronize()
+
+    def e2e_step(i):
+        b = i & 1
+        s_in.wait_event(x_free[b])
+        with torch.cuda.stream(s_in):
+            x_dev[b].copy_(x_host, non_blocking=True)
+        x_ready[b].record(s_in)
+        stream.wait_event(x_ready[b])
+        stream.wait_event(out_free[b])
+        if slot_graphs is not None:
+            slot_graphs[b].replay()
+        else:
+            compute(b)
+        x_free[b].record(stream)
+        comp_done[b].record(stream)
+        s_out.wait_event(comp_done[b])
+        with torch.cuda.stream(s_out):
+            out_host[b].copy_(out_dev[b], non_blocking=True)
+            stats_host[b].copy_(stats_dev[b], non_blocking=True)
+        out_free[b].record(s_out)
+
+    for i in range(args.warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    e0.record(s_in)
+    s_in.wait_stream(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    stream.wait_stream(s_out)
+    stream.wait_stream(s_in)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1))
@@ -404,7 +482,8 @@ def run_ours(args, wl, dist, rank, local):
         sys.stderr.write("per-stage ms: " + json.dumps({k: round(val, 4) for k, val in stage_ms.items()}) + "\n")
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic", "config": config_of(wl),
+                "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+                "config": {**config_of(wl), "launch": "cuda_graph" if graph is not None else "eager"},
                 "roofline": roof,
                 "stages": stages,
                 "layer": {"flops": fl["total"], "tflops": fl["total"] / (ms_per_step / 1e3) / 1e12,
@@ -429,6 +508,7 @@ def main():
                     help="tokens the oracle runs the expert FFN on for cpu_baseline (0 = skip)")
     ap.add_argument("--ref-sample", type=int, default=4, help="tokens per reference-arm step")
     ap.add_argument("--override", nargs="*", default=[], help="workload fields to change, e.g. N=32 T=1024")
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA-graph replay")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

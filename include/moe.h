@@ -72,7 +72,11 @@ typedef enum {
   MOE_ERR_BOUNDS = 6        /* device: an index left its range */
 } moe_status;
 
-typedef enum { MOE_GATE_SOFTMAX_TOPK = 0, MOE_GATE_SIGMOID_BIAS = 1 } moe_gate;
+/* MOE_GATE_SOFTMAX_TOPK: softmax over the k selected logits (Mixtral).
+ * MOE_GATE_SIGMOID_BIAS: sigmoid affinities, chosen on s + b, weights s / sum s (DeepSeek-V3).
+ * MOE_GATE_SOFTMAX_FULL: softmax over all N logits kept on the top-k, not
+ *   renormalised (DeepSeek v1; CS336 lecture 4, section 5 pseudocode). */
+typedef enum { MOE_GATE_SOFTMAX_TOPK = 0, MOE_GATE_SIGMOID_BIAS = 1, MOE_GATE_SOFTMAX_FULL = 2 } moe_gate;
 typedef enum { MOE_ACT_RELU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
@@ -203,6 +207,27 @@ MOE_API int moe_layer_forward(const moe_config *cfg, const void *x, const float 
  * partial sums use the workspace scratch. */
 MOE_API int moe_load_stats(const moe_config *cfg, const float *logits, const int32_t *counts_routed,
                    const int32_t *counts_kept, float *f, float *P, float *summary, void *ws, void *stream);
+
+/* Self-check of the device-side wait limit: launches one kernel whose pipeline
+ * wait can never complete (an mbarrier nobody arrives on) with the given limit
+ * (0 <= limit_ns <= 1e10).  The wait gives up after limit_ns and records
+ * MOE_ERR_TIMEOUT in the workspace status word, exactly as a stalled pipeline in
+ * any kernel of this library would; the GPU context stays usable.  The pages
+ * have no counterpart: this only tests the library's failure handling. */
+MOE_API int moe_check_wait_timeout(void *ws, int64_t limit_ns, void *stream);
+
+/* Router z-loss (CS336 lecture 4, section 11; Chapter 19, 19.6.2):
+ * *z_loss = mean over tokens of (log sum_i exp(logits[t, i]))^2, a device float.
+ * Partial sums use the workspace scratch; the result is deterministic. */
+MOE_API int moe_router_zloss(const moe_config *cfg, const float *logits, float *z_loss, void *ws, void *stream);
+
+/* DeepSeek-V3 auxiliary-loss-free balancing step (CS336 lecture 4, section 9;
+ * Chapter 19, 19.3.4): for each expert, sel_bias[e] += gamma when
+ * counts_routed[e] < T k / N, -= gamma when it is larger, unchanged when equal
+ * (compared exactly as counts_routed[e] * N against T * k).  sel_bias [N] float
+ * is updated in place on the device. */
+MOE_API int moe_bias_update(const moe_config *cfg, const int32_t *counts_routed, float *sel_bias, float gamma,
+                            void *stream);
 
 /* Synchronises `stream`, reads and clears the workspace status word, and
  * writes the first device-side error code found (MOE_OK if none) to *status.

@@ -22,13 +22,14 @@ LIB_PATH = os.path.join(_HERE, "libmoe_b300.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT, \
     MOE_ERR_BOUNDS = range(7)
-GATE_SOFTMAX_TOPK, GATE_SIGMOID_BIAS = 0, 1
+GATE_SOFTMAX_TOPK, GATE_SIGMOID_BIAS, GATE_SOFTMAX_FULL = 0, 1, 2
 ACT_RELU, ACT_SWIGLU = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
 EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_workspace_layout", "moe_route",
            "moe_dispatch", "moe_expert_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
-           "moe_load_stats", "moe_get_device_status", "moe_dispatch_noalloc")
+           "moe_load_stats", "moe_get_device_status", "moe_dispatch_noalloc", "moe_check_wait_timeout",
+           "moe_router_zloss", "moe_bias_update")
 
 
 class MoeConfig(ctypes.Structure):
@@ -69,6 +70,9 @@ def _load():
         "moe_layer_forward": [C, P, P, P, P, P, P, P, P, P, P, P, P, P],
         "moe_load_stats": [C, P, P, P, P, P, P, P, P],
         "moe_get_device_status": [P, P, ctypes.POINTER(ctypes.c_int)],
+        "moe_check_wait_timeout": [P, ctypes.c_int64, P],
+        "moe_router_zloss": [C, P, P, P, P],
+        "moe_bias_update": [C, P, P, ctypes.c_float, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -176,6 +180,20 @@ def moe_layer_forward(cfg, x, Wg, logit_bias, sel_bias, w1, w3, w2, sw1, sw3, sw
 def moe_load_stats(cfg, logits, counts_routed, counts_kept, f, P, summary, ws, stream=None):
     _check(_lib.moe_load_stats(ctypes.byref(cfg), _ptr(logits), _ptr(counts_routed), _ptr(counts_kept), _ptr(f),
                                _ptr(P), _ptr(summary), _ptr(ws), _stream(stream)), "moe_load_stats")
+
+
+def moe_router_zloss(cfg, logits, z_loss, ws, stream=None):
+    _check(_lib.moe_router_zloss(ctypes.byref(cfg), _ptr(logits), _ptr(z_loss), _ptr(ws), _stream(stream)),
+           "moe_router_zloss")
+
+
+def moe_bias_update(cfg, counts_routed, sel_bias, gamma: float, stream=None):
+    _check(_lib.moe_bias_update(ctypes.byref(cfg), _ptr(counts_routed), _ptr(sel_bias), float(gamma),
+                                _stream(stream)), "moe_bias_update")
+
+
+def moe_check_wait_timeout(ws, limit_ns: int, stream=None):
+    _check(_lib.moe_check_wait_timeout(_ptr(ws), int(limit_ns), _stream(stream)), "moe_check_wait_timeout")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

@@ -33,7 +33,8 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 int check_config(const moe_config *c) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->T < 0 || c->d < 1 || c->N < 1 || c->k < 1 || c->ffn < 1 || c->shared_ffn < 0) return MOE_ERR_INVALID_ARG;
-  if (c->gate != MOE_GATE_SOFTMAX_TOPK && c->gate != MOE_GATE_SIGMOID_BIAS) return MOE_ERR_INVALID_ARG;
+  if (c->gate != MOE_GATE_SOFTMAX_TOPK && c->gate != MOE_GATE_SIGMOID_BIAS && c->gate != MOE_GATE_SOFTMAX_FULL)
+    return MOE_ERR_INVALID_ARG;
   if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c->N > 256 || c->k > 8 || c->k > c->N) return MOE_ERR_UNSUPPORTED;
@@ -133,8 +134,8 @@ int ffn_routed(const moe_config *c, const void *x_perm, const int32_t *offsets, 
     MOE_TRY(tc_grouped_gemm(2, h, rows, c->ffn, w2, nullptr, (int64_t)c->N * c->d, c->d, offsets, c->N, 0, c->d,
                             y_perm, status, pair, s));
   } else {
-    MOE_TRY(simt_grouped_gemm(mode1, false, x_perm, rows, c->d, w1, w3, c->ffn, offsets, c->N, 0, c->ffn, h, s));
-    MOE_TRY(simt_grouped_gemm(2, false, h, rows, c->ffn, w2, nullptr, c->d, offsets, c->N, 0, c->d, y_perm, s));
+    MOE_TRY(simt_grouped_gemm(mode1, x_perm, rows, c->d, w1, w3, c->ffn, offsets, c->N, 0, c->ffn, h, s));
+    MOE_TRY(simt_grouped_gemm(2, h, rows, c->ffn, w2, nullptr, c->d, offsets, c->N, 0, c->d, y_perm, s));
   }
   return MOE_OK;
 }
@@ -148,8 +149,8 @@ int ffn_shared(const moe_config *c, const void *x, const void *sw1, const void *
     MOE_TRY(tc_grouped_gemm(mode1, x, c->T, c->d, sw1, sw3, Fs, Fs, nullptr, 1, c->T, Fs, h, status, pair, s));
     MOE_TRY(tc_grouped_gemm(2, h, c->T, Fs, sw2, nullptr, c->d, c->d, nullptr, 1, c->T, c->d, y, status, pair, s));
   } else {
-    MOE_TRY(simt_grouped_gemm(mode1, false, x, c->T, c->d, sw1, sw3, Fs, nullptr, 1, c->T, Fs, h, s));
-    MOE_TRY(simt_grouped_gemm(2, false, h, c->T, Fs, sw2, nullptr, c->d, nullptr, 1, c->T, c->d, y, s));
+    MOE_TRY(simt_grouped_gemm(mode1, x, c->T, c->d, sw1, sw3, Fs, nullptr, 1, c->T, Fs, h, s));
+    MOE_TRY(simt_grouped_gemm(2, h, c->T, Fs, sw2, nullptr, c->d, nullptr, 1, c->T, c->d, y, s));
   }
   return MOE_OK;
 }
@@ -173,6 +174,18 @@ bool weights_ok(const moe_config *c, const void *w1, const void *w3, const void 
   if (!w1 || !w2 || !aligned16(w1) || !aligned16(w2)) return false;
   if (c->act == MOE_ACT_SWIGLU && (!w3 || !aligned16(w3))) return false;
   return true;
+}
+
+// A wait that nothing can end: an mbarrier expecting one arrival that never
+// comes.  The bounded wait gives up after limit_ns and records MOE_ERR_TIMEOUT.
+__global__ void wait_timeout_kernel(int *status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, status, limit_ns);
 }
 
 }  // namespace
@@ -338,6 +351,28 @@ int moe_load_stats(const moe_config *cfg, const float *logits, const int32_t *co
   MOE_TRY(make_ws(cfg, ws, &w));
   return launch_load_stats(logits, counts_routed, counts_kept, cfg->T, cfg->N, cfg->k, cfg->gate,
                            w.stats_partial(cfg), f, P, summary, static_cast<cudaStream_t>(stream));
+}
+
+int moe_router_zloss(const moe_config *cfg, const float *logits, float *z_loss, void *ws, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (!logits || !z_loss) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_ERR_INVALID_ARG;  // a mean over no tokens
+  Ws w;
+  MOE_TRY(make_ws(cfg, ws, &w));
+  return launch_router_zloss(logits, cfg->T, cfg->N, w.stats_partial(cfg), z_loss, static_cast<cudaStream_t>(stream));
+}
+
+int moe_bias_update(const moe_config *cfg, const int32_t *counts_routed, float *sel_bias, float gamma, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (!counts_routed || !sel_bias || !(gamma >= 0.0f) || gamma > 1e30f) return MOE_ERR_INVALID_ARG;
+  return launch_bias_update(counts_routed, cfg->T, cfg->k, cfg->N, sel_bias, gamma, static_cast<cudaStream_t>(stream));
+}
+
+int moe_check_wait_timeout(void *ws, int64_t limit_ns, void *stream) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255) || limit_ns < 0 || limit_ns > 10000000000ll)
+    return MOE_ERR_INVALID_ARG;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<int *>(ws), (uint64_t)limit_ns);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int moe_get_device_status(void *ws, void *stream, int *status) {

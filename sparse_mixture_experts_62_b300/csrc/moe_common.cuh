@@ -67,13 +67,13 @@ MOE_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 // Wait for the phase of `parity` to complete.  Returns false (and records
-// MOE_ERR_TIMEOUT) if it has not completed within kWaitLimitNs.
-MOE_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int *status) {
+// MOE_ERR_TIMEOUT) if it has not completed within limit_ns.
+MOE_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int *status, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+    if ((it & 63u) == 0 && global_ns() - t0 > limit_ns) {
       set_status(status, MOE_ERR_TIMEOUT);
       return false;
     }

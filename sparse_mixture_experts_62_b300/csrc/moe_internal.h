@@ -42,8 +42,8 @@ inline bool use_pair_tiles(int64_t rows, int groups, int capacity) {
   return capacity <= 0 && rows >= (int64_t)512 * groups;
 }
 
-// grouped GEMM on the CUDA cores (float32 workloads); same modes, out in the input dtype
-int simt_grouped_gemm(int mode, bool bf16, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
+// grouped GEMM on the CUDA cores (float32 workloads); same modes and layouts, float32 out
+int simt_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
                       int b_rows_per_group, const int32_t *offsets, int G, int M, int n_out, void *out,
                       cudaStream_t stream);
 
@@ -55,5 +55,8 @@ int launch_combine(bool bf16, const void *y_perm, const int32_t *dest_row, const
 constexpr int kStatsChunk = 32;  // tokens per partial-sum chunk
 int launch_load_stats(const float *logits, const int32_t *counts_routed, const int32_t *counts_kept, int T, int N,
                       int k, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s);
+int launch_router_zloss(const float *logits, int T, int N, float *partial, float *z_loss, cudaStream_t s);
+int launch_bias_update(const int32_t *counts_routed, int T, int k, int N, float *sel_bias, float gamma,
+                       cudaStream_t s);
 
 }  // namespace moe

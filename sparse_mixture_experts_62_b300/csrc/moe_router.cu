@@ -233,16 +233,27 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, 
     if ((e_best & 31) == lane) taken |= 1u << (e_best >> 5);
     chosen[j] = e_best;
   }
+  // full-softmax gate: the normaliser over all N experts (warp sum, fixed order)
+  float full_den = 0.f;
+  if (gate == MOE_GATE_SOFTMAX_FULL) {
+    const float m = zr[chosen[0]];  // the largest logit
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (lane + 32 * i < N) full_den += expf(zr[lane + 32 * i] - m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) full_den += __shfl_xor_sync(0xffffffffu, full_den, off);
+  }
   // gate weights of the selected experts, in float32
   if (lane == 0) {
     float g[8];
     float sum = 0.f;
-    if (gate == MOE_GATE_SOFTMAX_TOPK) {
+    if (gate == MOE_GATE_SOFTMAX_TOPK || gate == MOE_GATE_SOFTMAX_FULL) {
       const float m = zr[chosen[0]];  // the first pick has the largest logit
       for (int j = 0; j < k; ++j) {
         g[j] = expf(zr[chosen[j]] - m);
         sum += g[j];
       }
+      if (gate == MOE_GATE_SOFTMAX_FULL) sum = full_den;
     } else {
       // float32 affinities (within 3e-7 relative of the rounded exact ones)
       for (int j = 0; j < k; ++j) {

@@ -37,7 +37,8 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(const float *__restr
       v[i] = (e < N) ? zr[e] : -INFINITY;
       m = fmaxf(m, v[i]);
     }
-    if (gate == MOE_GATE_SOFTMAX_TOPK) {
+    const bool softmax = gate != MOE_GATE_SIGMOID_BIAS;
+    if (softmax) {
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     }
@@ -46,7 +47,7 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(const float *__restr
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
       float p = 0.f;
-      if (e < N) p = (gate == MOE_GATE_SOFTMAX_TOPK) ? expf(v[i] - m) : 1.0f / (1.0f + expf(-v[i]));
+      if (e < N) p = softmax ? expf(v[i] - m) : 1.0f / (1.0f + expf(-v[i]));
       v[i] = p;
       sum += p;
     }
@@ -118,7 +119,82 @@ __global__ void __launch_bounds__(1024) stats_final_kernel(const float *__restri
   }
 }
 
+// Router z-loss: per token log Z = m + log sum exp(z - m) (one warp per token),
+// squared and summed per 32-token chunk; one CTA adds the chunks in order.
+__global__ void __launch_bounds__(256) zloss_partial_kernel(const float *__restrict__ logits, int T, int N,
+                                                            float *__restrict__ partial) {
+  __shared__ float red[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float acc = 0.f;
+  for (int tt = warp; tt < SC; tt += 8) {
+    const int t = blockIdx.x * SC + tt;
+    if (t >= T) break;
+    const float *zr = logits + (size_t)t * N;
+    float v[8];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < N) ? zr[e] : -INFINITY;
+      m = fmaxf(m, v[i]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (lane + 32 * i < N) sum += expf(v[i] - m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    const float lse = m + logf(sum);
+    acc += lse * lse;
+  }
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int w = 0; w < 8; ++w) s += red[w];
+    partial[blockIdx.x] = s;
+  }
+}
+
+__global__ void __launch_bounds__(1024) zloss_final_kernel(const float *__restrict__ partial, int nchunks, int T,
+                                                           float *__restrict__ z_loss) {
+  __shared__ float red[1024];
+  float s = 0.f;
+  for (int c = threadIdx.x; c < nchunks; c += 1024) s += partial[c];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int off = 512; off > 0; off >>= 1) {
+    if (threadIdx.x < off) red[threadIdx.x] += red[threadIdx.x + off];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *z_loss = red[0] / (float)T;
+}
+
+__global__ void __launch_bounds__(256) bias_update_kernel(const int32_t *__restrict__ counts, int T, int k, int N,
+                                                          float *__restrict__ sel_bias, float gamma) {
+  const int e = threadIdx.x;
+  if (e >= N) return;
+  const long long lhs = (long long)counts[e] * N, rhs = (long long)T * k;
+  if (lhs < rhs) sel_bias[e] += gamma;
+  else if (lhs > rhs) sel_bias[e] -= gamma;
+}
+
 }  // namespace
+
+int launch_router_zloss(const float *logits, int T, int N, float *partial, float *z_loss, cudaStream_t s) {
+  const int nchunks = (T + SC - 1) / SC;
+  zloss_partial_kernel<<<nchunks, 256, 0, s>>>(logits, T, N, partial);
+  zloss_final_kernel<<<1, 1024, 0, s>>>(partial, nchunks, T, z_loss);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_bias_update(const int32_t *counts_routed, int T, int k, int N, float *sel_bias, float gamma,
+                       cudaStream_t s) {
+  bias_update_kernel<<<1, 256, 0, s>>>(counts_routed, T, k, N, sel_bias, gamma);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 int launch_load_stats(const float *logits, const int32_t *counts_routed, const int32_t *counts_kept, int T, int N,
                       int k, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s) {

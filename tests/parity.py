@@ -41,7 +41,8 @@ def to_np_f64(t: torch.Tensor) -> np.ndarray:
 def config_of(wl: synth.Workload):
     cap = oracle.capacity(wl.capacity_factor, wl.T, wl.k, wl.N) if wl.capacity_factor > 0 else 0
     return moe.make_config(wl.T, wl.d, wl.N, wl.k, wl.F, wl.shared_F,
-                           moe.GATE_SIGMOID_BIAS if wl.gate == "sigmoid" else moe.GATE_SOFTMAX_TOPK,
+                           {"softmax": moe.GATE_SOFTMAX_TOPK, "sigmoid": moe.GATE_SIGMOID_BIAS,
+                           "softmax_full": moe.GATE_SOFTMAX_FULL}[wl.gate],
                            moe.ACT_SWIGLU if wl.act == "swiglu" else moe.ACT_RELU,
                            moe.DTYPE_BF16 if wl.dtype == "bf16" else moe.DTYPE_F32, cap)
 

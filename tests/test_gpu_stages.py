@@ -97,6 +97,8 @@ ROUTER_CASES = [
     dict(T=64, d=64, N=5, k=5, gate="softmax"),
     dict(T=64, d=64, N=1, k=1, gate="softmax"),
     dict(T=100, d=512, N=8, k=2, gate="softmax", dtype="f32", act="relu"),
+    dict(T=300, d=256, N=16, k=4, gate="softmax_full"),
+    dict(T=64, d=128, N=64, k=1, gate="softmax"),                        # Switch-style top-1
 ]
 
 
@@ -202,3 +204,41 @@ def test_load_stats_parity(gate, T, N, k):
     assert s[0] == pytest.approx(ref.aux, rel=1e-5)
     assert s[1] == pytest.approx(ref.imbalance, rel=1e-6)
     assert s[2] == pytest.approx(ref.drop_rate, rel=1e-6, abs=1e-7)
+
+
+def test_device_wait_gives_up_and_reports_timeout():
+    """A pipeline wait that nothing can end returns after its limit with
+    MOE_ERR_TIMEOUT in the status word; the context stays usable."""
+    cfg = moe.make_config(8, 64, 2, 1, 64)
+    ws = _ws(cfg)
+    moe.moe_check_wait_timeout(ws, 20_000_000)  # 20 ms
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_TIMEOUT
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    x = torch.ones(4, device="cuda")
+    assert float((x * 2).sum().item()) == 8.0  # the GPU still works
+
+
+@pytest.mark.parametrize("T,N", [(1000, 8), (333, 256), (4096, 128), (1, 4)])
+def test_router_zloss_parity(T, N):
+    rng = np.random.default_rng(T + N)
+    z = (rng.standard_normal((T, N)) * 3 + 1).astype(np.float32)
+    cfg = moe.make_config(T, 64, N, 1, 64)
+    ws = _ws(cfg)
+    out = torch.zeros(1, device="cuda")
+    moe.moe_router_zloss(cfg, torch.from_numpy(z).cuda(), out, ws)
+    ref = oracle.router_z_loss(z)
+    assert abs(float(out.item()) - ref) <= 1e-5 * ref
+
+
+def test_bias_update_parity():
+    T, N, k = 1000, 16, 2
+    rng = np.random.default_rng(3)
+    counts = rng.multinomial(T * k, np.ones(N) / N).astype(np.int32)
+    counts[3] = T * k // N  # exactly the mean: unchanged
+    b = rng.uniform(-0.05, 0.05, N).astype(np.float32)
+    cfg = moe.make_config(T, 64, N, k, 64, gate=moe.GATE_SIGMOID_BIAS)
+    bd = torch.from_numpy(b.copy()).cuda()
+    gamma = float(np.float32(0.001))  # the C ABI takes gamma as float32: give the oracle that value
+    moe.moe_bias_update(cfg, torch.from_numpy(counts).cuda(), bd, gamma)
+    ref = oracle.bias_update(b, counts.astype(np.int64), T, k, gamma)
+    assert np.array_equal(bd.cpu().numpy(), ref)
