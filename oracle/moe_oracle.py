@@ -246,6 +246,65 @@ def load_stats(z: np.ndarray, gate: str, d: Dispatch, k: int) -> LoadStats:
     return LoadStats(f, P, aux, imb, drop)
 
 
+# --------------------------------------------------------------------------- expert-choice routing
+@dataclasses.dataclass
+class ExpertChoice:
+    scores: np.ndarray      # [T, N] float64: full softmax over experts per token
+    chosen: np.ndarray      # [N, C] int32: expert e's tokens, ascending token index
+    dest_row: np.ndarray    # [T, N] int32: row e*C + r of token t in expert e, or -1
+    offsets: np.ndarray     # [N+1] int32: e*C
+
+
+def expert_choice(z: np.ndarray, C: int) -> ExpertChoice:
+    """Each expert picks the C tokens with the largest scores.
+
+    "Chapter 19: MoE", 19.6.1 (expert choice: every expert selects a fixed number
+    of tokens; a token may be processed by any number of experts, zero included)
+    and CS336 lecture 4, section 4 (top-K taken along the token axis of the score
+    matrix, so each expert gets exactly the same number of tokens).  Scores are
+    the full softmax over experts of each token's logits (CS336 lecture 4,
+    section 5); ties go to the lower token index; C is capped at T.  An expert's
+    rows are its tokens in ascending token order."""
+    T, N = z.shape
+    C = min(C, T)
+    z64 = z.astype(np.float64)
+    e_ = np.exp(z64 - z64.max(axis=1, keepdims=True))
+    sc = e_ / e_.sum(axis=1, keepdims=True)
+    chosen = np.zeros((N, C), dtype=np.int32)
+    dest = np.full((T, N), -1, dtype=np.int32)
+    for e in range(N):
+        order = sorted(range(T), key=lambda t: (-sc[t, e], t))[:C]
+        toks = sorted(order)
+        chosen[e] = toks
+        for r, t in enumerate(toks):
+            dest[t, e] = e * C + r
+    offsets = (np.arange(N + 1) * C).astype(np.int32)
+    return ExpertChoice(sc, chosen, dest, offsets)
+
+
+def expert_choice_forward(inp, C: int) -> tuple:
+    """y[t] = shared(x_t) + sum over experts e that chose t of s[t, e] * FFN_e(x_t).
+    Returns (out [T, d] float64, the ExpertChoice routing).  Logits as in
+    router_logits (with the optional logit bias); the gate is the score itself."""
+    wl = inp.wl
+    dt = wl.dtype
+    x64 = widen(inp.x, dt)
+    z = router_logits(x64, inp.Wg, inp.logit_bias)
+    ec = expert_choice(z, C)
+    out = np.zeros((wl.T, wl.d))
+    if wl.shared_F:
+        sw3 = widen(inp.sw3, dt) if inp.sw3 is not None else None
+        out += expert_ffn(x64, widen(inp.sw1, dt), sw3, widen(inp.sw2, dt), wl.act)
+    for e in range(wl.N):
+        toks = ec.chosen[e]
+        if toks.size == 0:
+            continue
+        W3 = widen(inp.w3[e], dt) if inp.w3 is not None else None
+        y = expert_ffn(x64[toks], widen(inp.w1[e], dt), W3, widen(inp.w2[e], dt), wl.act)
+        out[toks] += ec.scores[toks, e][:, None] * y
+    return out, ec
+
+
 # --------------------------------------------------------------------------- router training-side reductions
 def router_z_loss(z: np.ndarray) -> float:
     """mean over tokens of (log Z)^2, Z = sum_i exp(z_i): the router z-loss.

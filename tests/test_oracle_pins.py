@@ -435,3 +435,45 @@ def test_bias_update_signs():
     b = np.array([0.5, -0.1, 0.0, 0.2], dtype=np.float32)
     out = oracle.bias_update(b, counts, T=20, k=2, gamma=0.01)
     assert out.tolist() == pytest.approx([0.51, -0.09, 0.0, 0.19], abs=1e-7)
+
+
+# --------------------------------------------------------------------------- expert choice
+@pytest.mark.parametrize("T,N,C", [(9, 3, 4), (6, 4, 6), (5, 2, 9), (12, 5, 1)])
+def test_expert_choice_brute_force_and_equal_loads(T, N, C):
+    """Every expert gets exactly min(C, T) tokens (CS336 lecture 4, section 4);
+    its set is the one where every chosen score beats every unchosen one, ties to
+    the lower token index (brute force over all subsets)."""
+    rng = np.random.default_rng(T * N)
+    z = rng.choice(np.array([-1.0, 0.0, 0.5, 2.0], dtype=np.float32), size=(T, N))   # many ties
+    ec = oracle.expert_choice(z, C)
+    Ce = min(C, T)
+    assert ec.chosen.shape == (N, Ce)
+    for e in range(N):
+        col = ec.scores[:, e]
+        best = _brute_force_topk(col, Ce)
+        assert sorted(best) == ec.chosen[e].tolist()
+        for r, t in enumerate(ec.chosen[e]):
+            assert ec.dest_row[t, e] == e * Ce + r
+    assert np.sum(ec.dest_row >= 0) == N * Ce
+    assert np.allclose(ec.scores.sum(axis=1), 1.0)
+
+
+def test_expert_choice_all_tokens_is_dense_softmax_mixture():
+    """C = T: every expert processes every token, so y = sum_e softmax(z)_e FFN_e(x);
+    with identical experts that is the dense FFN (the softmax weights sum to 1)."""
+    inp = tiny(T=5, d=8, N=3, k=1, F=12)
+    for e in range(1, 3):
+        inp.w1[e], inp.w3[e], inp.w2[e] = inp.w1[0], inp.w3[0], inp.w2[0]
+    out, ec = oracle.expert_choice_forward(inp, C=5)
+    x = oracle.widen(inp.x, "bf16")
+    W1, W3, W2 = (oracle.widen(a[0], "bf16") for a in (inp.w1, inp.w3, inp.w2))
+    for t in range(5):
+        assert np.allclose(out[t], _loop_ffn(x[t], W1, W3, W2, "swiglu"), rtol=1e-12, atol=1e-12)
+
+
+def test_expert_choice_unchosen_token_gets_zero():
+    inp = tiny(T=20, d=8, N=2, k=1, F=12)
+    out, ec = oracle.expert_choice_forward(inp, C=3)
+    unchosen = np.all(ec.dest_row < 0, axis=1)
+    assert unchosen.sum() >= 14
+    assert np.all(out[unchosen] == 0.0)
