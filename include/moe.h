@@ -79,6 +79,11 @@ typedef enum {
 typedef enum { MOE_GATE_SOFTMAX_TOPK = 0, MOE_GATE_SIGMOID_BIAS = 1, MOE_GATE_SOFTMAX_FULL = 2 } moe_gate;
 typedef enum { MOE_ACT_RELU = 0, MOE_ACT_SWIGLU = 1 } moe_act;
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+/* MOE_ROUTING_TOKEN_CHOICE: each token picks its top-k experts (the gates above).
+ * MOE_ROUTING_EXPERT_CHOICE: each expert picks the `capacity` tokens with the
+ *   largest scores, scores = softmax over all N experts of each token's logits;
+ *   the gate of (token, expert) is that score; k and gate are ignored. */
+typedef enum { MOE_ROUTING_TOKEN_CHOICE = 0, MOE_ROUTING_EXPERT_CHOICE = 1 } moe_routing;
 
 typedef struct {
   int32_t T;          /* tokens */
@@ -90,7 +95,9 @@ typedef struct {
   int32_t gate;       /* moe_gate */
   int32_t act;        /* moe_act */
   int32_t dtype;      /* moe_dtype of x, weights, out */
-  int32_t capacity;   /* per-expert capacity C, <= 0 = unlimited (see moe_capacity) */
+  int32_t capacity;   /* per-expert capacity C, <= 0 = unlimited (see moe_capacity);
+                         expert choice: tokens per expert (>= 1, capped at T) */
+  int32_t routing;    /* moe_routing */
 } moe_config;
 
 /* Byte offsets of the intermediates inside the workspace (for inspection after
@@ -98,16 +105,16 @@ typedef struct {
 typedef struct {
   size_t status;         /* int32 status word */
   size_t logits;         /* float [T, N] */
-  size_t topk_idx;       /* int32 [T, k] */
-  size_t topk_w;         /* float [T, k] */
+  size_t topk_idx;       /* int32 [T, k] (token choice) */
+  size_t topk_w;         /* float [T, k]; expert choice: the scores [T, N] */
   size_t counts_routed;  /* int32 [N] */
   size_t counts_kept;    /* int32 [N] */
   size_t offsets;        /* int32 [N + 1] */
-  size_t dest_row;       /* int32 [T, k], -1 = dropped */
-  size_t src_token;      /* int32 [T * k] */
-  size_t x_perm;         /* dtype [T * k, d] */
-  size_t h;              /* dtype [T * k, F]  expert hidden activations */
-  size_t y_perm;         /* bf16 or float [T * k, d]  expert outputs */
+  size_t dest_row;       /* int32 [T, k], -1 = dropped; expert choice: [T, N], -1 = not chosen */
+  size_t src_token;      /* int32 [R], R = T * k (token choice) or N * min(C, T) (expert choice) */
+  size_t x_perm;         /* dtype [R, d] */
+  size_t h;              /* dtype [R, F]  expert hidden activations */
+  size_t y_perm;         /* bf16 or float [R, d]  expert outputs */
   size_t h_shared;       /* dtype [T, Fs] */
   size_t y_shared;       /* bf16 or float [T, d] */
   size_t scratch;        /* internal scratch */
@@ -192,11 +199,24 @@ MOE_API int moe_combine(const moe_config *cfg, const void *y_perm, const int32_t
 
 /* The whole layer: route, dispatch, routed experts, shared expert (if
  * cfg->shared_ffn > 0, sw1/sw3/sw2 non-NULL), combine.  Intermediates stay in
- * the workspace at the offsets of moe_workspace_layout. */
+ * the workspace at the offsets of moe_workspace_layout.  With
+ * cfg->routing == MOE_ROUTING_EXPERT_CHOICE the routing is moe_ec_route's
+ * (sel_bias is ignored) and the combine sums over the experts that chose a token. */
 MOE_API int moe_layer_forward(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias,
                       const float *sel_bias, const void *w1, const void *w3, const void *w2,
                       const void *sw1, const void *sw3, const void *sw2, void *out, void *ws,
                       void *stream);
+
+/* Expert-choice routing (Chapter 19, 19.6.1; CS336 lecture 4, section 4):
+ * logits [T, N] as in moe_route; scores [T, N] = softmax over the N experts of
+ * each token's logits; expert e takes the C = min(cfg->capacity, T) tokens with
+ * the largest scores (ties: lower token index), in ascending token order, at rows
+ * e*C .. e*C+C-1: src_token [N*C] holds their tokens, dest_row [T, N] the row of
+ * (t, e) or -1, offsets [N+1] = e*C.  Needs cfg->routing == MOE_ROUTING_EXPERT_CHOICE
+ * and cfg->capacity >= 1; bf16 or float32 x. */
+MOE_API int moe_ec_route(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias,
+                         float *logits, float *scores, int32_t *offsets, int32_t *src_token, int32_t *dest_row,
+                         void *ws, void *stream);
 
 /* Switch load statistics (Chapter 19, 19.3.3; CS336 lecture 4, section 9;
  * Lecture29, "Myth 3"): f[e] = counts_routed[e] / (T k); P[e] = mean over

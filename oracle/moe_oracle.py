@@ -265,11 +265,15 @@ def expert_choice(z: np.ndarray, C: int) -> ExpertChoice:
     the full softmax over experts of each token's logits (CS336 lecture 4,
     section 5); ties go to the lower token index; C is capped at T.  An expert's
     rows are its tokens in ascending token order."""
-    T, N = z.shape
-    C = min(C, T)
     z64 = z.astype(np.float64)
     e_ = np.exp(z64 - z64.max(axis=1, keepdims=True))
-    sc = e_ / e_.sum(axis=1, keepdims=True)
+    return expert_choice_select(e_ / e_.sum(axis=1, keepdims=True), C)
+
+
+def expert_choice_select(sc: np.ndarray, C: int) -> ExpertChoice:
+    """The selection step of expert_choice on given scores [T, N]."""
+    T, N = sc.shape
+    C = min(C, T)
     chosen = np.zeros((N, C), dtype=np.int32)
     dest = np.full((T, N), -1, dtype=np.int32)
     for e in range(N):

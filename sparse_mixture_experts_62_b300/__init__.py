@@ -25,16 +25,17 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_NONFINIT
 GATE_SOFTMAX_TOPK, GATE_SIGMOID_BIAS, GATE_SOFTMAX_FULL = 0, 1, 2
 ACT_RELU, ACT_SWIGLU = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
+ROUTING_TOKEN_CHOICE, ROUTING_EXPERT_CHOICE = 0, 1
 
 EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_workspace_layout", "moe_route",
            "moe_dispatch", "moe_expert_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
            "moe_load_stats", "moe_get_device_status", "moe_dispatch_noalloc", "moe_check_wait_timeout",
-           "moe_router_zloss", "moe_bias_update")
+           "moe_router_zloss", "moe_bias_update", "moe_ec_route")
 
 
 class MoeConfig(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("T", "d", "N", "k", "ffn", "shared_ffn", "gate", "act", "dtype", "capacity")]
+                ("T", "d", "N", "k", "ffn", "shared_ffn", "gate", "act", "dtype", "capacity", "routing")]
 
 
 class MoeWsLayout(ctypes.Structure):
@@ -72,6 +73,7 @@ def _load():
         "moe_get_device_status": [P, P, ctypes.POINTER(ctypes.c_int)],
         "moe_check_wait_timeout": [P, ctypes.c_int64, P],
         "moe_router_zloss": [C, P, P, P, P],
+        "moe_ec_route": [C, P, P, P, P, P, P, P, P, P, P],
         "moe_bias_update": [C, P, P, ctypes.c_float, P],
     }
     for name, args in sig.items():
@@ -111,8 +113,8 @@ def _check(code: int, where: str):
 
 
 def make_config(T, d, N, k, ffn, shared_ffn=0, gate=GATE_SOFTMAX_TOPK, act=ACT_SWIGLU, dtype=DTYPE_BF16,
-                capacity=0) -> MoeConfig:
-    return MoeConfig(T, d, N, k, ffn, shared_ffn, gate, act, dtype, capacity)
+                capacity=0, routing=ROUTING_TOKEN_CHOICE) -> MoeConfig:
+    return MoeConfig(T, d, N, k, ffn, shared_ffn, gate, act, dtype, capacity, routing)
 
 
 def moe_capacity(alpha: float, T: int, k: int, N: int) -> int:
@@ -180,6 +182,12 @@ def moe_layer_forward(cfg, x, Wg, logit_bias, sel_bias, w1, w3, w2, sw1, sw3, sw
 def moe_load_stats(cfg, logits, counts_routed, counts_kept, f, P, summary, ws, stream=None):
     _check(_lib.moe_load_stats(ctypes.byref(cfg), _ptr(logits), _ptr(counts_routed), _ptr(counts_kept), _ptr(f),
                                _ptr(P), _ptr(summary), _ptr(ws), _stream(stream)), "moe_load_stats")
+
+
+def moe_ec_route(cfg, x, Wg, logit_bias, logits, scores, offsets, src_token, dest_row, ws, stream=None):
+    _check(_lib.moe_ec_route(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(logit_bias), _ptr(logits), _ptr(scores),
+                             _ptr(offsets), _ptr(src_token), _ptr(dest_row), _ptr(ws), _stream(stream)),
+           "moe_ec_route")
 
 
 def moe_router_zloss(cfg, logits, z_loss, ws, stream=None):

@@ -37,18 +37,29 @@ int check_config(const moe_config *c) {
     return MOE_ERR_INVALID_ARG;
   if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->routing != MOE_ROUTING_TOKEN_CHOICE && c->routing != MOE_ROUTING_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
+  if (c->routing == MOE_ROUTING_EXPERT_CHOICE && c->capacity < 1) return MOE_ERR_INVALID_ARG;
   if (c->N > 256 || c->k > 8 || c->k > c->N) return MOE_ERR_UNSUPPORTED;
   if (c->d > 65536 || c->ffn > 65536 || c->shared_ffn > 65536) return MOE_ERR_UNSUPPORTED;
   const int q = is_bf16(c) ? 8 : 4;  // 16-byte rows
   if (c->d % q || c->ffn % q || c->shared_ffn % q) return MOE_ERR_UNSUPPORTED;
   if ((int64_t)c->T * c->k >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
+  if ((int64_t)c->T * c->N >= (int64_t)1 << 31) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
+
+inline bool is_ec(const moe_config *c) { return c->routing == MOE_ROUTING_EXPERT_CHOICE; }
+// tokens per expert under expert choice
+inline int ec_c(const moe_config *c) { return c->capacity < c->T ? c->capacity : c->T; }
+// routed rows (x_perm, h, y_perm) and routing slots per token (dest_row, gate weights)
+inline int64_t routed_rows(const moe_config *c) { return is_ec(c) ? (int64_t)c->N * ec_c(c) : (int64_t)c->T * c->k; }
+inline int slots(const moe_config *c) { return is_ec(c) ? c->N : c->k; }
 
 int layout(const moe_config *c, moe_ws_layout *L) {
   const size_t T = (size_t)c->T, N = (size_t)c->N, k = (size_t)c->k, d = (size_t)c->d, F = (size_t)c->ffn;
   const size_t Fs = (size_t)c->shared_ffn, es = esize(c);
-  const size_t rows = T * k;
+  const size_t rows = (size_t)routed_rows(c);
+  const size_t sl = (size_t)slots(c);
   const size_t nch_d = (T + kDispatchChunk - 1) / kDispatchChunk;
   const size_t nch_s = (T + kStatsChunk - 1) / kStatsChunk;
   size_t o = 0;
@@ -59,12 +70,12 @@ int layout(const moe_config *c, moe_ws_layout *L) {
   };
   L->status = take(4);
   L->logits = take(T * N * 4);
-  L->topk_idx = take(rows * 4);
-  L->topk_w = take(rows * 4);
+  L->topk_idx = take(T * k * 4);
+  L->topk_w = take(T * sl * 4);
   L->counts_routed = take(N * 4);
   L->counts_kept = take(N * 4);
   L->offsets = take((N + 1) * 4);
-  L->dest_row = take(rows * 4);
+  L->dest_row = take(T * sl * 4);
   L->src_token = take(rows * 4);
   L->x_perm = take(rows * d * es);
   L->h = take(rows * F * es);
@@ -125,10 +136,11 @@ int make_ws(const moe_config *c, void *ws, Ws *w) {
 
 int ffn_routed(const moe_config *c, const void *x_perm, const int32_t *offsets, const void *w1, const void *w3,
                const void *w2, void *h, void *y_perm, int *status, cudaStream_t s) {
-  const int64_t rows = (int64_t)c->T * c->k;
+  const int64_t rows = routed_rows(c);
   const int mode1 = c->act == MOE_ACT_SWIGLU ? 0 : 1;
   if (is_bf16(c)) {
-    const bool pair = use_pair_tiles(rows, c->N, c->capacity);
+    // expert choice gives every group exactly C rows: no capacity skew
+    const bool pair = use_pair_tiles(rows, c->N, is_ec(c) ? 0 : c->capacity);
     MOE_TRY(tc_grouped_gemm(mode1, x_perm, rows, c->d, w1, w3, (int64_t)c->N * c->ffn, c->ffn, offsets, c->N, 0,
                             c->ffn, h, status, pair, s));
     MOE_TRY(tc_grouped_gemm(2, h, rows, c->ffn, w2, nullptr, (int64_t)c->N * c->d, c->d, offsets, c->N, 0, c->d,
@@ -168,6 +180,21 @@ int route(const moe_config *c, const Ws &w, const void *x, const float *Wg, cons
   }
   MOE_TRY(launch_router_logits(x, false, Wg, logit_bias, c->T, c->d, c->N, logits, s));
   return launch_router_topk(logits, 1, c->N, nullptr, logits, sb, c->T, c->N, c->k, c->gate, idx, gw, w.status(), s);
+}
+
+// expert choice: logits, scores, per-expert top-C; counts in the workspace read C
+int ec_route(const moe_config *c, const Ws &w, const void *x, const float *Wg, const float *logit_bias,
+             float *logits, float *scores, int32_t *offsets, int32_t *src_token, int32_t *dest_row, cudaStream_t s) {
+  if (is_bf16(c)) {
+    int S = 1;
+    float *part = w.router_partial(c);
+    MOE_TRY(launch_router_tc(x, Wg, c->T, c->d, c->N, w.router_wsplit(c), part, &S, w.status(), s));
+    MOE_TRY(launch_router_sum(part, S, router_tc_npad(c->N), logit_bias, logits, c->T, c->N, s));
+  } else {
+    MOE_TRY(launch_router_logits(x, false, Wg, logit_bias, c->T, c->d, c->N, logits, s));
+  }
+  MOE_TRY(launch_expert_choice(logits, c->T, c->N, ec_c(c), scores, offsets, src_token, dest_row, s));
+  return launch_fill_counts(w.at<int32_t>(w.L.counts_routed), w.at<int32_t>(w.L.counts_kept), c->N, ec_c(c), s);
 }
 
 bool weights_ok(const moe_config *c, const void *w1, const void *w3, const void *w2) {
@@ -248,6 +275,7 @@ int moe_workspace_size(const moe_config *cfg, size_t *bytes) {
 int moe_route(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias, const float *sel_bias,
               float *logits, int32_t *topk_idx, float *topk_w, void *ws, void *stream) {
   MOE_TRY(check_config(cfg));
+  if (is_ec(cfg)) return MOE_ERR_INVALID_ARG;  // expert choice: moe_ec_route
   if (cfg->T == 0) return MOE_OK;
   if (!x || !Wg || !logits || !topk_idx || !topk_w || !aligned16(x)) return MOE_ERR_INVALID_ARG;
   Ws w;
@@ -259,6 +287,7 @@ int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x, 
                  int32_t *counts_kept, int32_t *offsets, int32_t *dest_row, int32_t *src_token, void *x_perm,
                  void *ws, void *stream) {
   MOE_TRY(check_config(cfg));
+  if (is_ec(cfg)) return MOE_ERR_INVALID_ARG;  // expert choice routes and dispatches in moe_ec_route
   if (!counts_routed || !counts_kept || !offsets) return MOE_ERR_INVALID_ARG;
   Ws w;
   MOE_TRY(make_ws(cfg, ws, &w));
@@ -303,7 +332,7 @@ int moe_combine(const moe_config *cfg, const void *y_perm, const int32_t *dest_r
   if (cfg->T == 0) return MOE_OK;
   if (!y_perm || !dest_row || !topk_w || !out || !aligned16(y_perm) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
   if (y_shared && !aligned16(y_shared)) return MOE_ERR_INVALID_ARG;
-  return launch_combine(is_bf16(cfg), y_perm, dest_row, topk_w, y_shared, out, cfg->T, cfg->d, cfg->k,
+  return launch_combine(is_bf16(cfg), y_perm, dest_row, topk_w, y_shared, out, cfg->T, cfg->d, slots(cfg),
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -327,19 +356,23 @@ int moe_layer_forward(const moe_config *cfg, const void *x, const float *Wg, con
   int32_t *src_token = w.at<int32_t>(L.src_token);
   void *x_perm = w.at<void>(L.x_perm);
   void *y_perm = w.at<void>(L.y_perm);
-  MOE_TRY(route(cfg, w, x, Wg, logit_bias, sel_bias, logits, idx, gw, s));
-  MOE_TRY(launch_dispatch(idx, cfg->T, cfg->k, cfg->N, cfg->capacity, w.hist(), w.chunk_base(cfg),
-                          w.at<int32_t>(L.counts_routed), w.at<int32_t>(L.counts_kept), offsets, dest_row, src_token,
-                          w.status(), s));
-  MOE_TRY(launch_gather_rows(x, src_token, offsets + cfg->N, (int64_t)cfg->T * cfg->k, (int)(cfg->d * esize(cfg)),
-                             x_perm, s));
+  if (is_ec(cfg)) {
+    MOE_TRY(ec_route(cfg, w, x, Wg, logit_bias, logits, gw, offsets, src_token, dest_row, s));
+  } else {
+    MOE_TRY(route(cfg, w, x, Wg, logit_bias, sel_bias, logits, idx, gw, s));
+    MOE_TRY(launch_dispatch(idx, cfg->T, cfg->k, cfg->N, cfg->capacity, w.hist(), w.chunk_base(cfg),
+                            w.at<int32_t>(L.counts_routed), w.at<int32_t>(L.counts_kept), offsets, dest_row,
+                            src_token, w.status(), s));
+  }
+  MOE_TRY(launch_gather_rows(x, src_token, offsets + cfg->N, routed_rows(cfg), (int)(cfg->d * esize(cfg)), x_perm,
+                             s));
   MOE_TRY(ffn_routed(cfg, x_perm, offsets, w1, w3, w2, w.at<void>(L.h), y_perm, w.status(), s));
   void *y_sh = nullptr;
   if (shared) {
     y_sh = w.at<void>(L.y_shared);
     MOE_TRY(ffn_shared(cfg, x, sw1, sw3, sw2, w.at<void>(L.h_shared), y_sh, w.status(), s));
   }
-  return launch_combine(is_bf16(cfg), y_perm, dest_row, gw, y_sh, out, cfg->T, cfg->d, cfg->k, s);
+  return launch_combine(is_bf16(cfg), y_perm, dest_row, gw, y_sh, out, cfg->T, cfg->d, slots(cfg), s);
 }
 
 int moe_load_stats(const moe_config *cfg, const float *logits, const int32_t *counts_routed,
@@ -349,8 +382,23 @@ int moe_load_stats(const moe_config *cfg, const float *logits, const int32_t *co
   if (!logits || !counts_routed || !counts_kept || !f || !P || !summary) return MOE_ERR_INVALID_ARG;
   Ws w;
   MOE_TRY(make_ws(cfg, ws, &w));
-  return launch_load_stats(logits, counts_routed, counts_kept, cfg->T, cfg->N, cfg->k, cfg->gate,
-                           w.stats_partial(cfg), f, P, summary, static_cast<cudaStream_t>(stream));
+  const long long total = is_ec(cfg) ? (long long)routed_rows(cfg) : (long long)cfg->T * cfg->k;
+  return launch_load_stats(logits, counts_routed, counts_kept, cfg->T, cfg->N, total,
+                           is_ec(cfg) ? MOE_GATE_SOFTMAX_FULL : cfg->gate, w.stats_partial(cfg), f, P, summary,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int moe_ec_route(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias, float *logits,
+                 float *scores, int32_t *offsets, int32_t *src_token, int32_t *dest_row, void *ws, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (!is_ec(cfg)) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_OK;
+  if (!x || !Wg || !logits || !scores || !offsets || !src_token || !dest_row || !aligned16(x))
+    return MOE_ERR_INVALID_ARG;
+  Ws w;
+  MOE_TRY(make_ws(cfg, ws, &w));
+  return ec_route(cfg, w, x, Wg, logit_bias, logits, scores, offsets, src_token, dest_row,
+                  static_cast<cudaStream_t>(stream));
 }
 
 int moe_router_zloss(const moe_config *cfg, const float *logits, float *z_loss, void *ws, void *stream) {

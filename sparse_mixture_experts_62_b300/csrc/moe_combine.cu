@@ -34,13 +34,24 @@ __global__ void __launch_bounds__(128) combine_kernel(const void *__restrict__ y
                                                       const float *__restrict__ w, const void *__restrict__ y_shared,
                                                       void *__restrict__ out, int T, int d, int k) {
   const int t = blockIdx.x;
-  __shared__ int rows[8];
-  __shared__ float gates[8];
-  if (threadIdx.x < k) {
-    rows[threadIdx.x] = dest_row[(size_t)t * k + threadIdx.x];
-    gates[threadIdx.x] = w[(size_t)t * k + threadIdx.x];
+  __shared__ int rows[256];
+  __shared__ float gates[256];
+  __shared__ int nslots;
+  // the token's kept slots, in slot order (k <= 8 for token choice, N <= 256 for expert choice)
+  if (threadIdx.x == 0) {
+    int n = 0;
+    for (int j = 0; j < k; ++j) {
+      const int r = dest_row[(size_t)t * k + j];
+      if (r >= 0) {
+        rows[n] = r;
+        gates[n] = w[(size_t)t * k + j];
+        ++n;
+      }
+    }
+    nslots = n;
   }
   __syncthreads();
+  const int ns = nslots;
   const int step = BF16 ? 8 : 4;
   for (int c = threadIdx.x * step; c < d; c += blockDim.x * step) {
     if (BF16) {
@@ -49,9 +60,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const void *__restrict__ y
         load8<true>(y_shared, (size_t)t * d + c, acc);
       else
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int j = 0; j < k; ++j) {
+      for (int j = 0; j < ns; ++j) {
         const int r = rows[j];
-        if (r < 0) continue;
         float v[8];
         load8<true>(y_perm, (size_t)r * d + c, v);
         const float g = gates[j];
@@ -64,9 +74,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const void *__restrict__ y
     } else {
       float4 acc = y_shared ? *reinterpret_cast<const float4 *>(static_cast<const float *>(y_shared) + (size_t)t * d + c)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j = 0; j < k; ++j) {
+      for (int j = 0; j < ns; ++j) {
         const int r = rows[j];
-        if (r < 0) continue;
         const float4 v = *reinterpret_cast<const float4 *>(static_cast<const float *>(y_perm) + (size_t)r * d + c);
         const float g = gates[j];
         acc.x = fmaf(g, v.x, acc.x);

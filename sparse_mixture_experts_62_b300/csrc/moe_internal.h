@@ -47,14 +47,24 @@ int simt_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void
                       int b_rows_per_group, const int32_t *offsets, int G, int M, int n_out, void *out,
                       cudaStream_t stream);
 
-// combine
+// sum of split router partials + logit bias -> logits (no top-k)
+int launch_router_sum(const float *partial, int S, int pstride, const float *logit_bias, float *logits, int T, int N,
+                      cudaStream_t s);
+// counts_routed = counts_kept = C for every expert (expert choice)
+int launch_fill_counts(int32_t *counts_routed, int32_t *counts_kept, int N, int C, cudaStream_t s);
+// expert choice: scores + per-expert top-C selection
+int launch_expert_choice(const float *logits, int T, int N, int C, float *scores, int32_t *offsets,
+                         int32_t *src_token, int32_t *dest_row, cudaStream_t s);
+
+// combine (up to 256 slots per token)
 int launch_combine(bool bf16, const void *y_perm, const int32_t *dest_row, const float *w, const void *y_shared,
                    void *out, int T, int d, int k, cudaStream_t s);
 
 // load statistics
 constexpr int kStatsChunk = 32;  // tokens per partial-sum chunk
+// total = all routed assignments (T * k, or N * C under expert choice)
 int launch_load_stats(const float *logits, const int32_t *counts_routed, const int32_t *counts_kept, int T, int N,
-                      int k, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s);
+                      long long total, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s);
 int launch_router_zloss(const float *logits, int T, int N, float *partial, float *z_loss, cudaStream_t s);
 int launch_bias_update(const int32_t *counts_routed, int T, int k, int N, float *sel_bias, float gamma,
                        cudaStream_t s);

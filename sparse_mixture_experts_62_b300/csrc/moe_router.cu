@@ -268,7 +268,38 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, 
   }
 }
 
+// logits[t, e] = sum of the S split partials in split order + logit bias
+__global__ void __launch_bounds__(256) router_sum_kernel(const float *__restrict__ partial, int S, int pstride,
+                                                         const float *__restrict__ logit_bias,
+                                                         float *__restrict__ logits, int T, int N) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (size_t)T * N) return;
+  const int t = (int)(i / N), e = (int)(i % N);
+  const float *p = partial + (size_t)t * pstride + e;
+  const size_t tile = (size_t)T * pstride;
+  float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+  int sp = 0;
+  for (; sp + 4 <= S; sp += 4) {
+    z0 += p[(sp + 0) * tile];
+    z1 += p[(sp + 1) * tile];
+    z2 += p[(sp + 2) * tile];
+    z3 += p[(sp + 3) * tile];
+  }
+  for (; sp < S; ++sp) z0 += p[sp * tile];
+  float z = (z0 + z1) + (z2 + z3);
+  if (logit_bias) z += logit_bias[e];
+  logits[i] = z;
+}
+
 }  // namespace
+
+int launch_router_sum(const float *partial, int S, int pstride, const float *logit_bias, float *logits, int T, int N,
+                      cudaStream_t s) {
+  const size_t n = (size_t)T * N;
+  if (n == 0) return MOE_OK;
+  router_sum_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(partial, S, pstride, logit_bias, logits, T, N);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 int launch_router_logits(const void *x, bool x_bf16, const float *Wg, const float *logit_bias, int T, int d, int N,
                          float *logits, cudaStream_t s) {

@@ -72,8 +72,8 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(const float *__restr
 __global__ void __launch_bounds__(1024) stats_final_kernel(const float *__restrict__ partial, int nchunks,
                                                            const int32_t *__restrict__ counts_routed,
                                                            const int32_t *__restrict__ counts_kept, int T, int N,
-                                                           int k, float *__restrict__ f, float *__restrict__ P,
-                                                           float *__restrict__ summary) {
+                                                           long long total, float *__restrict__ f,
+                                                           float *__restrict__ P, float *__restrict__ summary) {
   __shared__ float quarter[4][256];
   __shared__ float fp[256];
   __shared__ int maxc[256];
@@ -85,7 +85,6 @@ __global__ void __launch_bounds__(1024) stats_final_kernel(const float *__restri
   quarter[q][e] = s;
   __syncthreads();
   if (q == 0) {
-    const float tk = (float)T * (float)k;
     float fe = 0.f, pe = 0.f;
     int ce = 0;
     long long ke = 0;
@@ -93,14 +92,13 @@ __global__ void __launch_bounds__(1024) stats_final_kernel(const float *__restri
       pe = (((quarter[0][e] + quarter[1][e]) + quarter[2][e]) + quarter[3][e]) / (float)T;
       ce = counts_routed[e];
       ke = counts_kept[e];
-      fe = (float)((double)ce / ((double)T * (double)k));
+      fe = (float)((double)ce / (double)total);
       f[e] = fe;
       P[e] = pe;
     }
     fp[e] = fe * pe;
     maxc[e] = ce;
     kept[e] = ke;
-    (void)tk;
   }
   __syncthreads();
   for (int off = 128; off > 0; off >>= 1) {
@@ -112,7 +110,7 @@ __global__ void __launch_bounds__(1024) stats_final_kernel(const float *__restri
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    const double tk = (double)T * (double)k;
+    const double tk = (double)total;
     summary[0] = (float)N * fp[0];
     summary[1] = (float)((double)maxc[0] / (tk / (double)N));
     summary[2] = (float)(1.0 - (double)kept[0] / tk);
@@ -197,11 +195,11 @@ int launch_bias_update(const int32_t *counts_routed, int T, int k, int N, float 
 }
 
 int launch_load_stats(const float *logits, const int32_t *counts_routed, const int32_t *counts_kept, int T, int N,
-                      int k, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s) {
+                      long long total, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s) {
   if (T == 0) return MOE_OK;
   const int nchunks = (T + SC - 1) / SC;
   stats_partial_kernel<<<nchunks, 256, 0, s>>>(logits, T, N, gate, partial);
-  stats_final_kernel<<<1, 1024, 0, s>>>(partial, nchunks, counts_routed, counts_kept, T, N, k, f, P, summary);
+  stats_final_kernel<<<1, 1024, 0, s>>>(partial, nchunks, counts_routed, counts_kept, T, N, total, f, P, summary);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -59,7 +59,10 @@ class MoELayer:
         """Typed views of the workspace intermediates of the last forward."""
         c, L = self.cfg, self.layout
         T, N, k, d, F, Fs = c.T, c.N, c.k, c.d, c.ffn, c.shared_ffn
-        rows = T * k
+        ec = c.routing == 1
+        C = min(c.capacity, T) if ec else 0
+        rows = N * C if ec else T * k
+        sl = N if ec else k
         ws = self.ws
 
         def view(off, n, dtype, shape):
@@ -68,12 +71,12 @@ class MoELayer:
 
         out = {
             "logits": view(L.logits, T * N, torch.float32, (T, N)),
-            "topk_idx": view(L.topk_idx, rows, torch.int32, (T, k)),
-            "topk_w": view(L.topk_w, rows, torch.float32, (T, k)),
+            "topk_idx": view(L.topk_idx, T * k, torch.int32, (T, k)),
+            "topk_w": view(L.topk_w, T * sl, torch.float32, (T, sl)),
             "counts_routed": view(L.counts_routed, N, torch.int32, (N,)),
             "counts_kept": view(L.counts_kept, N, torch.int32, (N,)),
             "offsets": view(L.offsets, N + 1, torch.int32, (N + 1,)),
-            "dest_row": view(L.dest_row, rows, torch.int32, (T, k)),
+            "dest_row": view(L.dest_row, T * sl, torch.int32, (T, sl)),
             "src_token": view(L.src_token, rows, torch.int32, (rows,)),
             "x_perm": view(L.x_perm, rows * d, self.act_dtype, (rows, d)),
             "h": view(L.h, rows * F, self.act_dtype, (rows, F)),

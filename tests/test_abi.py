@@ -68,12 +68,14 @@ BAD_CONFIGS = [
     (dict(gate=7), moe.MOE_ERR_INVALID_ARG),
     (dict(act=3), moe.MOE_ERR_INVALID_ARG),
     (dict(dtype=5), moe.MOE_ERR_INVALID_ARG),
+    (dict(routing=2), moe.MOE_ERR_INVALID_ARG),
+    (dict(routing=1, capacity=0), moe.MOE_ERR_INVALID_ARG),   # expert choice needs C >= 1
 ]
 
 
 @pytest.mark.parametrize("kw,code", BAD_CONFIGS)
 def test_bad_configs_rejected(kw, code):
-    base = dict(T=64, d=64, N=8, k=2, ffn=128, shared_ffn=0, gate=0, act=1, dtype=1, capacity=0)
+    base = dict(T=64, d=64, N=8, k=2, ffn=128, shared_ffn=0, gate=0, act=1, dtype=1, capacity=0, routing=0)
     base.update(kw)
     cfg = moe.MoeConfig(*[base[f] for f, _ in moe.MoeConfig._fields_])
     with pytest.raises(moe.MoeError) as e:
@@ -102,6 +104,19 @@ def test_null_and_misaligned_pointers_rejected_without_launch():
         with pytest.raises(moe.MoeError) as e:
             fn()
         assert e.value.code == moe.MOE_ERR_INVALID_ARG
+
+
+def test_expert_choice_config_sizes_the_workspace_for_N_times_C_rows():
+    tc = moe.make_config(1000, 64, 16, 2, 128)
+    ec = moe.make_config(1000, 64, 16, 1, 128, capacity=300, routing=moe.ROUTING_EXPERT_CHOICE)
+    Lt, Le = moe.moe_workspace_layout(tc), moe.moe_workspace_layout(ec)
+    assert Le.x_perm - Le.src_token >= 16 * 300 * 4
+    assert Le.h - Le.x_perm >= 16 * 300 * 64 * 2
+    assert Le.src_token - Le.dest_row >= 1000 * 16 * 4          # dest_row [T, N]
+    assert Lt.src_token - Lt.dest_row >= 1000 * 2 * 4
+    A = 1 << 20
+    with pytest.raises(moe.MoeError):   # token-choice route on an expert-choice config
+        moe.moe_route(ec, A, A, None, None, A, A, A, A, 0)
 
 
 def test_zero_tokens_is_a_noop_for_the_layer():

@@ -1,0 +1,113 @@
+"""Expert-choice routing on the GPU against the oracle (B300).
+
+Scores compare within 1e-6; each expert's chosen set compares exactly where the
+oracle's gap between its C-th and (C+1)-th scores exceeds 1e-6, and otherwise
+must be the oracle's selection run on the GPU's own scores.  Rows, offsets and
+the row map compare exactly; the layer output within the bf16 tolerance, with the
+oracle run on the GPU's selection.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_mixture_experts_62_b300 as moe
+import synth
+from parity import assert_close_out, to_dev, to_np_f64
+
+pytestmark = pytest.mark.gpu
+
+GAP = 1e-6
+
+
+def ec_inputs(T, N, d=128, F=192, seed=31, shared_F=0, zipf_s=0.0):
+    wl = synth.Workload("ec", seed, T=T, d=d, N=N, k=1, F=F, act="swiglu", gate="softmax", dtype="bf16",
+                        shared_F=shared_F, zipf_s=zipf_s)
+    return synth.make_inputs(wl)
+
+
+def ec_config(wl, C):
+    return moe.make_config(wl.T, wl.d, wl.N, 1, wl.F, wl.shared_F, capacity=C, routing=moe.ROUTING_EXPERT_CHOICE)
+
+
+def check_selection(sc_gpu, sc_ref, chosen_gpu, C):
+    T, N = sc_ref.shape
+    C = min(C, T)
+    ref = oracle.expert_choice_select(sc_ref, C)
+    from_gpu_scores = oracle.expert_choice_select(sc_gpu.astype(np.float64), C)
+    for e in range(N):
+        col = np.sort(sc_ref[:, e])[::-1]
+        gap = col[C - 1] - col[C] if C < T else np.inf
+        if gap > GAP:
+            assert chosen_gpu[e].tolist() == ref.chosen[e].tolist(), f"expert {e}"
+        else:
+            assert chosen_gpu[e].tolist() == from_gpu_scores.chosen[e].tolist(), f"expert {e} (near tie)"
+
+
+@pytest.mark.parametrize("T,N,C", [(300, 8, 80), (1000, 16, 250), (2048, 128, 16), (64, 4, 64), (100, 6, 500),
+                                   (4096, 64, 128), (5, 3, 1)])
+def test_ec_route_parity(T, N, C):
+    inp = ec_inputs(T, N)
+    wl = inp.wl
+    cfg = ec_config(wl, C)
+    ws = torch.zeros(moe.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    Ce = min(C, T)
+    z = torch.empty((T, N), device="cuda")
+    sc = torch.empty((T, N), device="cuda")
+    off = torch.full((N + 1,), -3, dtype=torch.int32, device="cuda")
+    src = torch.full((N * Ce,), -3, dtype=torch.int32, device="cuda")
+    dest = torch.full((T, N), -3, dtype=torch.int32, device="cuda")
+    moe.moe_ec_route(cfg, to_dev(inp.x, "bf16"), to_dev(inp.Wg, "f32"), None, z, sc, off, src, dest, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    z_ref = oracle.router_logits(oracle.widen(inp.x, "bf16"), inp.Wg, None)
+    ec_ref = oracle.expert_choice(z_ref, C)
+    sc_g = sc.cpu().numpy()
+    assert np.max(np.abs(sc_g - ec_ref.scores)) < 1e-6
+    src_g, off_g, dest_g = src.cpu().numpy(), off.cpu().numpy(), dest.cpu().numpy()
+    assert np.array_equal(off_g, np.arange(N + 1) * Ce)
+    chosen = src_g.reshape(N, Ce)
+    assert np.all(np.diff(chosen, axis=1) > 0)          # ascending token order within an expert
+    check_selection(sc_g, ec_ref.scores, chosen, C)
+    # the row map is the inverse of the row list
+    expect = np.full((T, N), -1, dtype=np.int32)
+    for e in range(N):
+        for r, t in enumerate(chosen[e]):
+            expect[t, e] = e * Ce + r
+    assert np.array_equal(dest_g, expect)
+
+
+@pytest.mark.parametrize("T,N,C,shared_F", [(600, 8, 150, 0), (1024, 16, 128, 256), (256, 4, 512, 0)])
+def test_ec_layer_parity(T, N, C, shared_F):
+    inp = ec_inputs(T, N, shared_F=shared_F, seed=T + N)
+    wl = inp.wl
+    cfg = ec_config(wl, C)
+    layer = moe.MoELayer(cfg, to_dev(inp.Wg, "f32"), to_dev(inp.w1, "bf16"), to_dev(inp.w3, "bf16"),
+                         to_dev(inp.w2, "bf16"), to_dev(inp.sw1, "bf16"), to_dev(inp.sw3, "bf16"),
+                         to_dev(inp.sw2, "bf16"))
+    out = layer.forward(to_dev(inp.x, "bf16"))
+    f, P, summ = layer.load_stats()
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    v = layer.views()
+    Ce = min(C, T)
+    chosen = v["src_token"].cpu().numpy().reshape(N, Ce)
+    z_ref = oracle.router_logits(oracle.widen(inp.x, "bf16"), inp.Wg, None)
+    ec_ref = oracle.expert_choice(z_ref, C)
+    check_selection(v["topk_w"].cpu().numpy(), ec_ref.scores, chosen, C)
+    # reference output on the GPU's selection, oracle scores as gates
+    x64 = oracle.widen(inp.x, "bf16")
+    ref = np.zeros((T, wl.d))
+    if shared_F:
+        ref += oracle.expert_ffn(x64, oracle.widen(inp.sw1, "bf16"), oracle.widen(inp.sw3, "bf16"),
+                                 oracle.widen(inp.sw2, "bf16"), "swiglu")
+    for e in range(N):
+        toks = chosen[e]
+        y = oracle.expert_ffn(x64[toks], oracle.widen(inp.w1[e], "bf16"), oracle.widen(inp.w3[e], "bf16"),
+                              oracle.widen(inp.w2[e], "bf16"), "swiglu")
+        ref[toks] += ec_ref.scores[toks, e][:, None] * y
+    assert_close_out(to_np_f64(out), ref, "bf16")
+    # statistics: every expert holds C of the N*C assignments
+    assert np.allclose(f.cpu().numpy(), 1.0 / N)
+    assert np.max(np.abs(P.cpu().numpy() - ec_ref.scores.mean(axis=0))) < 1e-5
+    s = summ.cpu().numpy()
+    assert s[1] == pytest.approx(1.0) and s[2] == pytest.approx(0.0, abs=1e-7)
