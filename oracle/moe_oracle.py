@@ -402,6 +402,158 @@ def layer_forward(inp, tokens: Optional[np.ndarray] = None, idx_override: Option
     return LayerResult(z, sel, idx, w, disp, out, y_sh, stats)
 
 
+# --------------------------------------------------------------------------- backward
+@dataclasses.dataclass
+class Params:
+    """float64 parameters of one layer (shared expert optional)."""
+    Wg: np.ndarray
+    w1: np.ndarray
+    w3: Optional[np.ndarray]
+    w2: np.ndarray
+    sw1: Optional[np.ndarray] = None
+    sw3: Optional[np.ndarray] = None
+    sw2: Optional[np.ndarray] = None
+
+
+def params64(inp) -> Params:
+    dt = inp.wl.dtype
+    w = lambda a: None if a is None else widen(a, dt)  # noqa: E731
+    return Params(inp.Wg.astype(np.float64), w(inp.w1), w(inp.w3), w(inp.w2), w(inp.sw1), w(inp.sw3), w(inp.sw2))
+
+
+def _gates64(z64: np.ndarray, idx: np.ndarray, gate: str) -> np.ndarray:
+    """Gate weights from float64 logits at fixed indices (no float32 rounding)."""
+    T, k = idx.shape
+    w = np.zeros((T, k))
+    for t in range(T):
+        if gate == "softmax":
+            zs = z64[t, idx[t]]
+            e = np.exp(zs - zs.max())
+            w[t] = e / e.sum()
+        elif gate == "softmax_full":
+            e = np.exp(z64[t] - z64[t].max())
+            w[t] = e[idx[t]] / e.sum()
+        else:
+            ss = 1.0 / (1.0 + np.exp(-z64[t, idx[t]]))
+            w[t] = ss / ss.sum()
+    return w
+
+
+def forward_fixed_routing(x64, beta, P: Params, act: str, gate: str, idx: np.ndarray, disp: Dispatch) -> np.ndarray:
+    """The layer in float64 with the top-k indices and the kept set held fixed
+    (a smooth function of x and the parameters; used for gradient checks)."""
+    z = x64 @ P.Wg + (0.0 if beta is None else beta.astype(np.float64)[None, :])
+    w = _gates64(z, idx, gate)
+    T, k = idx.shape
+    out = np.zeros((T, P.w2.shape[1]))
+    if P.sw1 is not None:
+        out += expert_ffn(x64, P.sw1, P.sw3, P.sw2, act)
+    for t in range(T):
+        for j in range(k):
+            if disp.dest_row[t, j] >= 0:
+                e = idx[t, j]
+                out[t] += w[t, j] * expert_ffn(x64[t:t + 1], P.w1[e], None if P.w3 is None else P.w3[e], P.w2[e], act)[0]
+    return out
+
+
+@dataclasses.dataclass
+class Grads:
+    dx: np.ndarray
+    dWg: np.ndarray
+    dw1: np.ndarray
+    dw3: Optional[np.ndarray]
+    dw2: np.ndarray
+    dsw1: Optional[np.ndarray] = None
+    dsw3: Optional[np.ndarray] = None
+    dsw2: Optional[np.ndarray] = None
+    dgate: Optional[np.ndarray] = None   # [T, k] dL/dw of the kept slots
+
+
+def _expert_backward(xr, W1, W3, W2, dy, act):
+    """Gradients of y = W2 act(W1 x [, W3 x]) for rows xr, given dy; float64."""
+    a = xr @ W1.T
+    if act == "swiglu":
+        u = xr @ W3.T
+        sig = 1.0 / (1.0 + np.exp(-a))
+        h = a * sig * u
+        dh = dy @ W2
+        da = dh * u * (sig * (1.0 + a * (1.0 - sig)))   # d SiLU(a) / da = sig (1 + a (1 - sig))
+        du = dh * a * sig
+        dW2 = dy.T @ h
+        dW1 = da.T @ xr
+        dW3 = du.T @ xr
+        dx = da @ W1 + du @ W3
+        return dx, dW1, dW3, dW2
+    h = np.maximum(a, 0.0)
+    dh = dy @ W2
+    da = dh * (a > 0)
+    return da @ W1, da.T @ xr, None, dy.T @ h
+
+
+def layer_backward(x64, beta, P: Params, act: str, gate: str, idx: np.ndarray, disp: Dispatch,
+                   dout: np.ndarray) -> Grads:
+    """Gradients of L = <dout, out> with the routing held fixed.
+
+    The top-k choice is piecewise constant, so gradients reach the router only
+    through the gate weights of the chosen, kept experts, and the experts only
+    through the tokens they processed ("Chapter 19: MoE", 19.6.2: the main task's
+    gradient flows through the selected gates and experts; unselected experts get
+    none from that token).  Gate derivatives: softmax over the selected logits
+    dz_j = w_j (dw_j - sum_l w_l dw_l); full softmax dz_i = p_i (g_i - sum_l p_l g_l)
+    with g = dw on the selected, 0 elsewhere; sigmoid w_j = s_j / sum s gives
+    ds_j = (dw_j - sum_l w_l dw_l) / sum s and dz_j = ds_j s_j (1 - s_j)."""
+    T, k = idx.shape
+    N = P.Wg.shape[1]
+    z = x64 @ P.Wg + (0.0 if beta is None else beta.astype(np.float64)[None, :])
+    w = _gates64(z, idx, gate)
+    dx = np.zeros_like(x64)
+    dw1 = np.zeros_like(P.w1)
+    dw3 = None if P.w3 is None else np.zeros_like(P.w3)
+    dw2 = np.zeros_like(P.w2)
+    dgate = np.zeros((T, k))
+    for e in range(N):
+        rows = [(t, j) for t in range(T) for j in range(k) if idx[t, j] == e and disp.dest_row[t, j] >= 0]
+        if not rows:
+            continue
+        toks = np.array([t for t, _ in rows])
+        slots = np.array([j for _, j in rows])
+        xr = x64[toks]
+        W3 = None if P.w3 is None else P.w3[e]
+        y = expert_ffn(xr, P.w1[e], W3, P.w2[e], act)
+        dgate[toks, slots] = np.sum(dout[toks] * y, axis=1)
+        dy = w[toks, slots][:, None] * dout[toks]
+        gx, g1, g3, g2 = _expert_backward(xr, P.w1[e], W3, P.w2[e], dy, act)
+        np.add.at(dx, toks, gx)
+        dw1[e] += g1
+        dw2[e] += g2
+        if g3 is not None:
+            dw3[e] += g3
+    # through the gates into the logits
+    dz = np.zeros((T, N))
+    for t in range(T):
+        kept = disp.dest_row[t] >= 0
+        g = np.where(kept, dgate[t], 0.0)
+        if gate == "softmax":
+            dz[t, idx[t]] = w[t] * (g - np.sum(w[t] * g))
+        elif gate == "softmax_full":
+            e_ = np.exp(z[t] - z[t].max())
+            p = e_ / e_.sum()
+            gfull = np.zeros(N)
+            gfull[idx[t]] = g
+            dz[t] = p * (gfull - np.sum(p * gfull))
+        else:
+            s = 1.0 / (1.0 + np.exp(-z[t, idx[t]]))
+            ds = (g - np.sum(w[t] * g)) / s.sum()
+            dz[t, idx[t]] = ds * s * (1.0 - s)
+    dWg = x64.T @ dz
+    dx += dz @ P.Wg.T
+    gr = Grads(dx, dWg, dw1, dw3, dw2, dgate=dgate)
+    if P.sw1 is not None:
+        gx, gr.dsw1, gr.dsw3, gr.dsw2 = _expert_backward(x64, P.sw1, P.sw3, P.sw2, dout, act)
+        gr.dx = gr.dx + gx
+    return gr
+
+
 def dense_mask_forward(inp, cap: Optional[int] = None) -> np.ndarray:
     """Second formulation, with no permutation: y[t] = y_sh[t] + sum_e G[t,e] FFN_e(x_t).
 

@@ -5,6 +5,7 @@ itself: an identity stated on the pages, a closed form, brute force on tiny
 inputs, or an invariant.  They are chosen so that a dropped term, a wrong sign,
 a wrong index or a transposed operand in the oracle fails at least one.
 """
+import dataclasses
 import itertools
 import json
 import math
@@ -477,3 +478,72 @@ def test_expert_choice_unchosen_token_gets_zero():
     unchosen = np.all(ec.dest_row < 0, axis=1)
     assert unchosen.sum() >= 14
     assert np.all(out[unchosen] == 0.0)
+
+
+# --------------------------------------------------------------------------- backward
+BWD_CASES = [
+    dict(act="swiglu", gate="softmax"),
+    dict(act="relu", gate="softmax", dtype="f32"),
+    dict(act="swiglu", gate="sigmoid", shared_F=10, sel_bias_range=0.05),
+    dict(act="swiglu", gate="softmax_full"),
+    dict(act="swiglu", gate="softmax", capacity_factor=0.5, zipf_s=1.2),
+    dict(act="swiglu", gate="softmax", N=3, k=3),
+]
+
+
+@pytest.mark.parametrize("kw", BWD_CASES)
+def test_backward_matches_central_differences(kw):
+    """<grad, v> of L = <dout, out> equals (L(p + eps v) - L(p - eps v)) / (2 eps)
+    for random directions v, routing held fixed, for x and every parameter."""
+    kw = dict(kw)
+    N, k = kw.pop("N", 5), kw.pop("k", 2)
+    inp = tiny(T=9, d=6, N=N, k=k, F=7, **kw)
+    wl = inp.wl
+    ref = oracle.layer_forward(inp)
+    P = oracle.params64(inp)
+    x64 = oracle.widen(inp.x, wl.dtype)
+    rng = np.random.default_rng(17)
+    dout = rng.standard_normal((wl.T, wl.d))
+    g = oracle.layer_backward(x64, inp.logit_bias, P, wl.act, wl.gate, ref.idx, ref.disp, dout)
+
+    def L(x_, P_):
+        return float(np.sum(dout * oracle.forward_fixed_routing(x_, inp.logit_bias, P_, wl.act, wl.gate,
+                                                                 ref.idx, ref.disp)))
+    # the fixed-routing forward is the oracle's layer (up to the float32 rounding of
+    # the logits the layer's gates see)
+    assert np.allclose(oracle.forward_fixed_routing(x64, inp.logit_bias, P, wl.act, wl.gate, ref.idx, ref.disp),
+                       ref.out, rtol=1e-6, atol=1e-7)
+    eps = 1e-6
+    names = ["x", "Wg", "w1", "w3", "w2", "sw1", "sw3", "sw2"]
+    grads = {"x": g.dx, "Wg": g.dWg, "w1": g.dw1, "w3": g.dw3, "w2": g.dw2, "sw1": g.dsw1, "sw3": g.dsw3,
+             "sw2": g.dsw2}
+    for name in names:
+        base = x64 if name == "x" else getattr(P, name)
+        if base is None:
+            assert grads[name] is None
+            continue
+        v = rng.standard_normal(base.shape)
+
+        def shifted(sign):
+            if name == "x":
+                return L(x64 + sign * eps * v, P)
+            P2 = dataclasses.replace(P, **{name: base + sign * eps * v})
+            return L(x64, P2)
+        fd = (shifted(1) - shifted(-1)) / (2 * eps)
+        an = float(np.sum(grads[name] * v))
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_backward_dropped_slots_get_no_gradient():
+    """CS336 lecture 4, section 10: a dropped assignment has no expert output, so
+    neither its gate nor its expert receives gradient from it."""
+    inp = tiny(T=12, d=6, N=4, k=2, F=7, capacity_factor=0.01)
+    wl = inp.wl
+    ref = oracle.layer_forward(inp)
+    P = oracle.params64(inp)
+    dout = np.ones((wl.T, wl.d))
+    g = oracle.layer_backward(oracle.widen(inp.x, "bf16"), None, P, wl.act, wl.gate, ref.idx, ref.disp, dout)
+    assert np.all(g.dgate[ref.disp.dest_row < 0] == 0.0)
+    fully_dropped = np.all(ref.disp.dest_row < 0, axis=1)
+    assert fully_dropped.any()
+    assert np.all(g.dx[fully_dropped] == 0.0)
