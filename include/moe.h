@@ -236,6 +236,25 @@ MOE_API int moe_load_stats(const moe_config *cfg, const float *logits, const int
  * have no counterpart: this only tests the library's failure handling. */
 MOE_API int moe_check_wait_timeout(void *ws, int64_t limit_ns, void *stream);
 
+/* Backward pass of the layer, bf16 token-choice configs (Chapter 19, 19.6.2: the
+ * top-k choice is discrete, so gradients reach the router through the gate weights
+ * of the chosen, kept experts only, and each expert through the tokens it
+ * processed; dropped assignments get none -- CS336 lecture 4, section 10).
+ * Call it after moe_layer_forward on the same inputs with the same forward
+ * workspace `fwd_ws`, whose intermediates it reads (logits, top-k, gate weights,
+ * dispatch, x_perm, h, y_perm, the shared expert's h).  dout [T, d] bf16 is the
+ * gradient of the loss with respect to the layer output.  Outputs, all float32
+ * and fully overwritten: dx [T, d], dWg [d, N], dw1 and dw3 [N, F, d], dw2
+ * [N, d, F] (dw3 NULL for ReLU experts), dsw1, dsw3 [Fs, d], dsw2 [d, Fs] when
+ * cfg->shared_ffn > 0 (else NULL).  The logit and selection biases are inputs,
+ * not parameters: no gradient.  Scratch: `bwd_ws` of moe_backward_workspace_size
+ * bytes (256-byte aligned). */
+MOE_API int moe_backward_workspace_size(const moe_config *cfg, size_t *bytes);
+MOE_API int moe_layer_backward(const moe_config *cfg, const void *x, const float *Wg, const void *w1, const void *w3,
+                               const void *w2, const void *sw1, const void *sw3, const void *sw2, const void *dout,
+                               float *dx, float *dWg, float *dw1, float *dw3, float *dw2, float *dsw1, float *dsw3,
+                               float *dsw2, void *fwd_ws, void *bwd_ws, void *stream);
+
 /* Router z-loss (CS336 lecture 4, section 11; Chapter 19, 19.6.2):
  * *z_loss = mean over tokens of (log sum_i exp(logits[t, i]))^2, a device float.
  * Partial sums use the workspace scratch; the result is deterministic. */

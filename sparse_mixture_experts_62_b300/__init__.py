@@ -30,7 +30,8 @@ ROUTING_TOKEN_CHOICE, ROUTING_EXPERT_CHOICE = 0, 1
 EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_workspace_layout", "moe_route",
            "moe_dispatch", "moe_expert_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
            "moe_load_stats", "moe_get_device_status", "moe_dispatch_noalloc", "moe_check_wait_timeout",
-           "moe_router_zloss", "moe_bias_update", "moe_ec_route")
+           "moe_router_zloss", "moe_bias_update", "moe_ec_route",
+           "moe_backward_workspace_size", "moe_layer_backward")
 
 
 class MoeConfig(ctypes.Structure):
@@ -74,6 +75,8 @@ def _load():
         "moe_check_wait_timeout": [P, ctypes.c_int64, P],
         "moe_router_zloss": [C, P, P, P, P],
         "moe_ec_route": [C, P, P, P, P, P, P, P, P, P, P],
+        "moe_backward_workspace_size": [C, ctypes.POINTER(ctypes.c_size_t)],
+        "moe_layer_backward": [C] + [P] * 20,
         "moe_bias_update": [C, P, P, ctypes.c_float, P],
     }
     for name, args in sig.items():
@@ -188,6 +191,20 @@ def moe_ec_route(cfg, x, Wg, logit_bias, logits, scores, offsets, src_token, des
     _check(_lib.moe_ec_route(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(logit_bias), _ptr(logits), _ptr(scores),
                              _ptr(offsets), _ptr(src_token), _ptr(dest_row), _ptr(ws), _stream(stream)),
            "moe_ec_route")
+
+
+def moe_backward_workspace_size(cfg: MoeConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.moe_backward_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_backward_workspace_size")
+    return n.value
+
+
+def moe_layer_backward(cfg, x, Wg, w1, w3, w2, sw1, sw3, sw2, dout, dx, dWg, dw1, dw3, dw2, dsw1, dsw3, dsw2,
+                       fwd_ws, bwd_ws, stream=None):
+    _check(_lib.moe_layer_backward(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(w1), _ptr(w3), _ptr(w2), _ptr(sw1),
+                                   _ptr(sw3), _ptr(sw2), _ptr(dout), _ptr(dx), _ptr(dWg), _ptr(dw1), _ptr(dw3),
+                                   _ptr(dw2), _ptr(dsw1), _ptr(dsw3), _ptr(dsw2), _ptr(fwd_ws), _ptr(bwd_ws),
+                                   _stream(stream)), "moe_layer_backward")
 
 
 def moe_router_zloss(cfg, logits, z_loss, ws, stream=None):

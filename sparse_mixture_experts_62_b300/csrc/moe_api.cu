@@ -197,6 +197,108 @@ int ec_route(const moe_config *c, const Ws &w, const void *x, const float *Wg, c
   return launch_fill_counts(w.at<int32_t>(w.L.counts_routed), w.at<int32_t>(w.L.counts_kept), c->N, ec_c(c), s);
 }
 
+// ---------------------------------------------------------------- backward workspace
+struct BwdLayout {
+  size_t dgate, dz, koff, koff_sh, off_sh, dy, dh, a, u, dA, dxp, w2t, w13t, dyT, hT, dAT, xT;
+  size_t dh_s, a_s, u_s, dA_s, dx_s, sw2t, sw13t, doutT, hsT, dAsT, xTs, total;
+  int64_t rp, tp;
+};
+
+BwdLayout bwd_layout(const moe_config *c) {
+  BwdLayout L{};
+  const size_t T = c->T, N = c->N, k = c->k, d = c->d, F = c->ffn, Fs = c->shared_ffn;
+  const size_t R = (size_t)c->T * c->k;
+  const bool sw = c->act == MOE_ACT_SWIGLU;
+  const size_t FA = sw ? 2 * F : F, FAs = sw ? 2 * Fs : Fs;  // width of dA
+  L.rp = (int64_t)(R + 64 * N);
+  L.rp = (L.rp + 63) / 64 * 64;
+  L.tp = (int64_t)((T + 63) / 64 * 64);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align256(o + (bytes ? bytes : 1));
+    return at;
+  };
+  L.dgate = take(T * k * 4);
+  L.dz = take(T * N * 4);
+  L.koff = take((N + 1) * 4);
+  L.koff_sh = take(2 * 4);
+  L.off_sh = take(2 * 4);
+  L.dy = take(R * d * 2);
+  L.dh = take(R * F * 2);
+  L.a = take(R * F * 2);
+  L.u = take(sw ? R * F * 2 : 0);
+  L.dA = take(R * FA * 2);
+  L.dxp = take(R * d * 2);
+  L.w2t = take(N * F * d * 2);
+  L.w13t = take(N * d * FA * 2);
+  L.dyT = take(d * L.rp * 2);
+  L.hT = take(F * L.rp * 2);
+  L.dAT = take(FA * L.rp * 2);
+  L.xT = take(d * L.rp * 2);
+  if (Fs) {
+    L.dh_s = take(T * Fs * 2);
+    L.a_s = take(T * Fs * 2);
+    L.u_s = take(sw ? T * Fs * 2 : 0);
+    L.dA_s = take(T * FAs * 2);
+    L.dx_s = take(T * d * 2);
+    L.sw2t = take(Fs * d * 2);
+    L.sw13t = take(d * FAs * 2);
+    L.doutT = take(d * L.tp * 2);
+    L.hsT = take(Fs * L.tp * 2);
+    L.dAsT = take(FAs * L.tp * 2);
+    L.xTs = take(d * L.tp * 2);
+  }
+  L.total = o;
+  return L;
+}
+
+int check_backward(const moe_config *c) {
+  MOE_TRY(check_config(c));
+  if (!is_bf16(c) || is_ec(c)) return MOE_ERR_UNSUPPORTED;  // bf16 token choice only
+  return MOE_OK;
+}
+
+// One expert set (routed: G = N with offsets; shared: G = 1) through the FFN backward.
+// dy [R, d], the forward's x rows (x_perm or x), h; writes dx rows (bf16) and float32 grads.
+int ffn_backward(const moe_config *c, bool shared, int G, int64_t R, const int32_t *offsets, const int32_t *off_dev,
+                 const void *xrows, const void *h, const void *dy, const void *w1, const void *w3, const void *w2,
+                 int F, uint8_t *bws, const BwdLayout &L, float *dw1, float *dw3, float *dw2, void *dxrows,
+                 int *status, cudaStream_t s) {
+  const bool sw = c->act == MOE_ACT_SWIGLU;
+  const int d = c->d, FA = sw ? 2 * F : F;
+  const bool pair = use_pair_tiles(R, G, shared ? 0 : c->capacity);
+  auto B = [&](size_t off) { return bws + off; };
+  void *dh = B(shared ? L.dh_s : L.dh), *a = B(shared ? L.a_s : L.a), *u = B(shared ? L.u_s : L.u);
+  void *dA = B(shared ? L.dA_s : L.dA), *w2t = B(shared ? L.sw2t : L.w2t), *w13t = B(shared ? L.sw13t : L.w13t);
+  const int M = shared ? c->T : 0;
+  // dh = dy W2: B = W2 transposed per expert to [F, d]
+  MOE_TRY(launch_transpose_weights(w2, G, d, F, d, 0, w2t, s));
+  MOE_TRY(tc_grouped_gemm(2, dy, R, d, w2t, nullptr, (int64_t)G * F, F, offsets, G, M, F, dh, status, pair, s));
+  // recompute a = x W1^T (and u = x W3^T); then dA = [da | du]
+  MOE_TRY(tc_grouped_gemm(2, xrows, R, d, w1, nullptr, (int64_t)G * F, F, offsets, G, M, F, a, status, pair, s));
+  if (sw) MOE_TRY(tc_grouped_gemm(2, xrows, R, d, w3, nullptr, (int64_t)G * F, F, offsets, G, M, F, u, status, pair, s));
+  MOE_TRY(launch_act_bwd(a, sw ? u : nullptr, dh, off_dev + G, R, F, sw, dA, s));
+  // dx rows = [da | du] [W1 | W3]: B = [W1^T | W3^T] per expert ([d, 2F])
+  MOE_TRY(launch_transpose_weights(w1, G, F, d, FA, 0, w13t, s));
+  if (sw) MOE_TRY(launch_transpose_weights(w3, G, F, d, FA, F, w13t, s));
+  MOE_TRY(tc_grouped_gemm(2, dA, R, FA, w13t, nullptr, (int64_t)G * d, d, offsets, G, M, d, dxrows, status, pair, s));
+  // weight gradients: sums over each expert's rows of transposed, 64-padded activations
+  int32_t *koff = reinterpret_cast<int32_t *>(B(shared ? L.koff_sh : L.koff));
+  const int64_t kp = shared ? L.tp : L.rp;
+  void *dyT = B(shared ? L.doutT : L.dyT), *hT = B(shared ? L.hsT : L.hT), *dAT = B(shared ? L.dAsT : L.dAT);
+  void *xT = B(shared ? L.xTs : L.xT);
+  MOE_TRY(launch_wgrad_koff(off_dev, G, koff, s));
+  MOE_TRY(launch_transpose_rows(dy, d, off_dev, koff, G, kp, dyT, s));
+  MOE_TRY(launch_transpose_rows(h, F, off_dev, koff, G, kp, hT, s));
+  MOE_TRY(launch_transpose_rows(dA, FA, off_dev, koff, G, kp, dAT, s));
+  MOE_TRY(launch_transpose_rows(xrows, d, off_dev, koff, G, kp, xT, s));
+  MOE_TRY(tc_wgrad_gemm(dyT, hT, koff, G, d, F, kp, dw2, status, s));
+  MOE_TRY(tc_wgrad_gemm(dAT, xT, koff, G, F, d, kp, dw1, status, s));
+  if (sw) MOE_TRY(tc_wgrad_gemm(static_cast<uint8_t *>(dAT) + (size_t)F * kp * 2, xT, koff, G, F, d, kp, dw3, status, s));
+  return MOE_OK;
+}
+
 bool weights_ok(const moe_config *c, const void *w1, const void *w3, const void *w2) {
   if (!w1 || !w2 || !aligned16(w1) || !aligned16(w2)) return false;
   if (c->act == MOE_ACT_SWIGLU && (!w3 || !aligned16(w3))) return false;
@@ -414,6 +516,59 @@ int moe_bias_update(const moe_config *cfg, const int32_t *counts_routed, float *
   MOE_TRY(check_config(cfg));
   if (!counts_routed || !sel_bias || !(gamma >= 0.0f) || gamma > 1e30f) return MOE_ERR_INVALID_ARG;
   return launch_bias_update(counts_routed, cfg->T, cfg->k, cfg->N, sel_bias, gamma, static_cast<cudaStream_t>(stream));
+}
+
+int moe_backward_workspace_size(const moe_config *cfg, size_t *bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  MOE_TRY(check_backward(cfg));
+  *bytes = bwd_layout(cfg).total;
+  return MOE_OK;
+}
+
+int moe_layer_backward(const moe_config *cfg, const void *x, const float *Wg, const void *w1, const void *w3,
+                       const void *w2, const void *sw1, const void *sw3, const void *sw2, const void *dout, float *dx,
+                       float *dWg, float *dw1, float *dw3, float *dw2, float *dsw1, float *dsw3, float *dsw2,
+                       void *fwd_ws, void *bwd_ws, void *stream) {
+  MOE_TRY(check_backward(cfg));
+  if (cfg->T == 0) return MOE_OK;
+  const bool sw = cfg->act == MOE_ACT_SWIGLU, shared = cfg->shared_ffn > 0;
+  if (!x || !Wg || !dout || !dx || !dWg || !dw1 || !dw2 || (sw && !dw3) || !weights_ok(cfg, w1, w3, w2))
+    return MOE_ERR_INVALID_ARG;
+  if (shared && (!weights_ok(cfg, sw1, sw3, sw2) || !dsw1 || !dsw2 || (sw && !dsw3))) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(dout) || !aligned16(dx)) return MOE_ERR_INVALID_ARG;
+  if (!bwd_ws || (reinterpret_cast<uintptr_t>(bwd_ws) & 255)) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  MOE_TRY(make_ws(cfg, fwd_ws, &w));
+  const moe_ws_layout &FL = w.L;
+  const BwdLayout L = bwd_layout(cfg);
+  uint8_t *bws = static_cast<uint8_t *>(bwd_ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int T = cfg->T, N = cfg->N, k = cfg->k, d = cfg->d;
+  const int64_t R = (int64_t)T * k;
+  const int32_t *offsets = w.at<int32_t>(FL.offsets);
+  const int32_t *dest_row = w.at<int32_t>(FL.dest_row);
+  float *dgate = reinterpret_cast<float *>(bws + L.dgate);
+  float *dz = reinterpret_cast<float *>(bws + L.dz);
+  // gates and router
+  MOE_TRY(launch_zero_f32(dgate, (size_t)T * k, s));
+  MOE_TRY(launch_dy_dgate(dout, w.at<void>(FL.y_perm), w.at<float>(FL.topk_w), dest_row, w.at<int32_t>(FL.src_token),
+                          offsets + N, R, k, d, bws + L.dy, dgate, s));
+  MOE_TRY(launch_router_bwd(w.at<float>(FL.logits), w.at<int32_t>(FL.topk_idx), w.at<float>(FL.topk_w), dgate,
+                            cfg->gate, T, N, k, dz, s));
+  MOE_TRY(launch_dwg(x, dz, T, d, N, dWg, s));
+  // routed experts
+  MOE_TRY(ffn_backward(cfg, false, N, R, offsets, offsets, w.at<void>(FL.x_perm), w.at<void>(FL.h), bws + L.dy, w1, w3,
+                       w2, cfg->ffn, bws, L, dw1, dw3, dw2, bws + L.dxp, w.status(), s));
+  // the shared expert: one group of all T rows, dy = dout
+  void *dx_sh = nullptr;
+  if (shared) {
+    int32_t *off_sh = reinterpret_cast<int32_t *>(bws + L.off_sh);
+    MOE_TRY(launch_set_offsets2(off_sh, T, s));
+    dx_sh = bws + L.dx_s;
+    MOE_TRY(ffn_backward(cfg, true, 1, T, nullptr, off_sh, x, w.at<void>(FL.h_shared), dout, sw1, sw3, sw2,
+                         cfg->shared_ffn, bws, L, dsw1, dsw3, dsw2, dx_sh, w.status(), s));
+  }
+  return launch_dx_combine(bws + L.dxp, dest_row, dz, Wg, dx_sh, T, d, N, k, dx, s);
 }
 
 int moe_check_wait_timeout(void *ws, int64_t limit_ns, void *stream) {

@@ -1,0 +1,334 @@
+// Backward pass of the layer with the routing held fixed: the element-wise,
+// transposition and router kernels around the tensor-core GEMMs.
+//
+// "Chapter 19: MoE", 19.6.2: the top-k choice is discrete, so the task gradient
+// reaches the router only through the gate weights of the chosen experts and
+// each expert only through the tokens it processed.  With out[t] = sum_j w_tj y_tj:
+//   dy_tj = w_tj dout[t]                      (into the expert backward)
+//   dw_tj = <dout[t], y_tj>                   (into the gate backward)
+//   softmax over the selected:  dz_j = w_j (dw_j - sum_l w_l dw_l)
+//   full softmax:               dz_i = p_i (g_i - sum_l p_l g_l), g = dw on the selected
+//   sigmoid, w = s / sum s:     dz_j = (dw_j - sum_l w_l dw_l) / sum s * s_j (1 - s_j)
+//   SwiGLU h = SiLU(a) u:       da = dh u SiLU'(a), du = dh SiLU(a),
+//                               SiLU'(a) = sig(a) (1 + a (1 - sig(a)))
+// Dropped assignments contribute nothing (CS336 lecture 4, section 10).
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+// koff[e] = column offset of expert e in the transposed, 64-padded activations
+__global__ void wgrad_koff_kernel(const int32_t *__restrict__ offsets, int N, int32_t *__restrict__ koff) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  int acc = 0;
+  for (int e = 0; e < N; ++e) {
+    koff[e] = acc;
+    const int r = offsets[e + 1] - offsets[e];
+    acc += (r + 63) / 64 * 64;
+  }
+  koff[N] = acc;
+}
+
+// XT[c][koff[e] + i] = X[offsets[e] + i][c] for i < rows of e, 0 in the padding.
+// 32 x 32 tiles through shared memory; the group of a padded column is found by
+// binary search over koff.
+__global__ void __launch_bounds__(256) transpose_rows_kernel(const uint16_t *__restrict__ X, int C,
+                                                             const int32_t *__restrict__ offsets,
+                                                             const int32_t *__restrict__ koff, int N, int64_t kp,
+                                                             uint16_t *__restrict__ XT) {
+  __shared__ uint16_t tile[32][34];
+  __shared__ int s_src[32];
+  const int p0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const int kp_used = koff[N];
+  if (p0 >= kp_used) {
+    // columns past the last group: zeros, so the GEMM's K blocks read nothing stale
+    for (int i = threadIdx.x; i < 32 * 32; i += 256) {
+      const int c = c0 + i / 32, p = p0 + i % 32;
+      if (c < C && p < kp) XT[(size_t)c * kp + p] = 0;
+    }
+    return;
+  }
+  if (threadIdx.x < 32) {
+    const int p = p0 + threadIdx.x;
+    int src = -1;
+    if (p < kp_used) {
+      int lo = 0, hi = N;  // largest e with koff[e] <= p
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) / 2;
+        if (koff[mid] <= p) lo = mid;
+        else hi = mid;
+      }
+      const int i = p - koff[lo];
+      if (i < offsets[lo + 1] - offsets[lo]) src = offsets[lo] + i;
+    }
+    s_src[threadIdx.x] = src;
+  }
+  __syncthreads();
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  for (int r = ty; r < 32; r += 8) {
+    const int src = s_src[r], c = c0 + tx;
+    tile[r][tx] = (src >= 0 && c < C) ? X[(size_t)src * C + c] : (uint16_t)0;
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int c = c0 + r, p = p0 + tx;
+    if (c < C && p < kp) XT[(size_t)c * kp + p] = tile[tx][r];
+  }
+}
+
+// WT[g][b][col_off + a] = W[g][a][b]; W is [G][A][B], WT rows have out_stride elements.
+__global__ void __launch_bounds__(256) transpose_weights_kernel(const uint16_t *__restrict__ W, int A, int B,
+                                                                int out_stride, int col_off,
+                                                                uint16_t *__restrict__ WT) {
+  __shared__ uint16_t tile[32][34];
+  const int b0 = blockIdx.x * 32, a0 = blockIdx.y * 32, g = blockIdx.z;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const uint16_t *Wg = W + (size_t)g * A * B;
+  uint16_t *WTg = WT + (size_t)g * B * out_stride;
+  for (int r = ty; r < 32; r += 8) {
+    const int a = a0 + r, b = b0 + tx;
+    tile[r][tx] = (a < A && b < B) ? Wg[(size_t)a * B + b] : (uint16_t)0;
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int b = b0 + r, a = a0 + tx;
+    if (a < A && b < B) WTg[(size_t)b * out_stride + col_off + a] = tile[tx][r];
+  }
+}
+
+__global__ void zero_f32_kernel(float *p, size_t n) {
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) p[i] = 0.f;
+}
+
+// One warp per kept row r: dy[r] = w_tj dout[t] (bf16), dgate[t, j] = <dout[t], y_perm[r]>.
+__global__ void __launch_bounds__(256) dy_dgate_kernel(const uint16_t *__restrict__ dout,
+                                                       const uint16_t *__restrict__ y_perm,
+                                                       const float *__restrict__ topk_w,
+                                                       const int32_t *__restrict__ dest_row,
+                                                       const int32_t *__restrict__ src_token,
+                                                       const int32_t *__restrict__ rows_end, int k, int d,
+                                                       uint16_t *__restrict__ dy, float *__restrict__ dgate) {
+  const int rows = *rows_end;
+  const int warps = gridDim.x * 8;
+  for (int r = blockIdx.x * 8 + (threadIdx.x >> 5); r < rows; r += warps) {
+    const int lane = threadIdx.x & 31;
+    const int t = src_token[r];
+    int j = 0;
+    while (j < k - 1 && dest_row[(size_t)t * k + j] != r) ++j;
+    const float w = topk_w[(size_t)t * k + j];
+    float dot = 0.f;
+    for (int c = lane * 8; c < d; c += 256) {
+      const uint4 g = *reinterpret_cast<const uint4 *>(dout + (size_t)t * d + c);
+      const uint4 y = *reinterpret_cast<const uint4 *>(y_perm + (size_t)r * d + c);
+      const uint32_t gv[4] = {g.x, g.y, g.z, g.w}, yv[4] = {y.x, y.y, y.z, y.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float g0 = bf16_lo(gv[q]), g1 = bf16_hi(gv[q]);
+        dot = fmaf(g0, bf16_lo(yv[q]), dot);
+        dot = fmaf(g1, bf16_hi(yv[q]), dot);
+        o[q] = pack_bf16x2(w * g0, w * g1);
+      }
+      *reinterpret_cast<uint4 *>(dy + (size_t)r * d + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+    if (lane == 0) dgate[(size_t)t * k + j] = dot;
+  }
+}
+
+// One warp per token: dz [T, N] from the gate gradients of the kept slots.
+__global__ void __launch_bounds__(256) router_bwd_kernel(const float *__restrict__ logits,
+                                                         const int32_t *__restrict__ idx,
+                                                         const float *__restrict__ topk_w,
+                                                         const float *__restrict__ dgate, int gate, int T, int N,
+                                                         int k, float *__restrict__ dz) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const float *zr = logits + (size_t)t * N;
+  float *dzr = dz + (size_t)t * N;
+  // sum_l w_l g_l over the selected slots (dropped slots have g = 0)
+  float wg = 0.f;
+  for (int j = 0; j < k; ++j) wg += topk_w[(size_t)t * k + j] * dgate[(size_t)t * k + j];
+  if (gate == MOE_GATE_SOFTMAX_FULL) {
+    float m = -INFINITY;
+    for (int e = lane; e < N; e += 32) m = fmaxf(m, zr[e]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float sum = 0.f;
+    for (int e = lane; e < N; e += 32) sum += expf(zr[e] - m);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    // sum_l p_l g_l = sum_l w_l g_l (the gate weights are the selected p)
+    for (int e = lane; e < N; e += 32) {
+      float g = 0.f;
+      for (int j = 0; j < k; ++j)
+        if (idx[(size_t)t * k + j] == e) g = dgate[(size_t)t * k + j];
+      dzr[e] = expf(zr[e] - m) / sum * (g - wg);
+    }
+    return;
+  }
+  for (int e = lane; e < N; e += 32) dzr[e] = 0.f;
+  __syncwarp();
+  if (lane == 0) {
+    float ssum = 0.f;
+    if (gate == MOE_GATE_SIGMOID_BIAS)
+      for (int j = 0; j < k; ++j) ssum += 1.0f / (1.0f + expf(-zr[idx[(size_t)t * k + j]]));
+    for (int j = 0; j < k; ++j) {
+      const int e = idx[(size_t)t * k + j];
+      const float g = dgate[(size_t)t * k + j], w = topk_w[(size_t)t * k + j];
+      if (gate == MOE_GATE_SOFTMAX_TOPK) {
+        dzr[e] = w * (g - wg);
+      } else {
+        const float s = 1.0f / (1.0f + expf(-zr[e]));
+        dzr[e] = (g - wg) / ssum * s * (1.0f - s);
+      }
+    }
+  }
+}
+
+// dA from the recomputed a (and u) and dh: SwiGLU [da | du] ([R, 2F]) or ReLU da ([R, F]).
+__global__ void __launch_bounds__(256) act_bwd_kernel(const uint16_t *__restrict__ a, const uint16_t *__restrict__ u,
+                                                      const uint16_t *__restrict__ dh,
+                                                      const int32_t *__restrict__ rows_end, int F, bool swiglu,
+                                                      uint16_t *__restrict__ dA) {
+  const size_t n = (size_t)(*rows_end) * F;
+  for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 2; i < n; i += (size_t)gridDim.x * blockDim.x * 2) {
+    const size_t r = i / F, f = i % F;  // F is even: the pair stays in one row
+    const uint32_t av = *reinterpret_cast<const uint32_t *>(a + i);
+    const uint32_t gv = *reinterpret_cast<const uint32_t *>(dh + i);
+    const float a0 = bf16_lo(av), a1 = bf16_hi(av), g0 = bf16_lo(gv), g1 = bf16_hi(gv);
+    if (swiglu) {
+      const uint32_t uv = *reinterpret_cast<const uint32_t *>(u + i);
+      const float u0 = bf16_lo(uv), u1 = bf16_hi(uv);
+      const float s0 = 1.0f / (1.0f + expf(-a0)), s1 = 1.0f / (1.0f + expf(-a1));
+      const float da0 = g0 * u0 * s0 * (1.0f + a0 * (1.0f - s0)), da1 = g1 * u1 * s1 * (1.0f + a1 * (1.0f - s1));
+      const float du0 = g0 * a0 * s0, du1 = g1 * a1 * s1;
+      *reinterpret_cast<uint32_t *>(dA + r * 2 * F + f) = pack_bf16x2(da0, da1);
+      *reinterpret_cast<uint32_t *>(dA + r * 2 * F + F + f) = pack_bf16x2(du0, du1);
+    } else {
+      *reinterpret_cast<uint32_t *>(dA + r * F + f) = pack_bf16x2(a0 > 0.f ? g0 : 0.f, a1 > 0.f ? g1 : 0.f);
+    }
+  }
+}
+
+// dWg[c][e] = sum_t x[t][c] dz[t][e]; one thread per (c, e), c fastest.
+__global__ void __launch_bounds__(256) dwg_kernel(const uint16_t *__restrict__ x, const float *__restrict__ dz, int T,
+                                                  int d, int N, float *__restrict__ dWg) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x, e = blockIdx.y;
+  if (c >= d) return;
+  float acc = 0.f;
+  for (int t = 0; t < T; ++t) acc = fmaf(__uint_as_float((uint32_t)x[(size_t)t * d + c] << 16), dz[(size_t)t * N + e], acc);
+  dWg[(size_t)c * N + e] = acc;
+}
+
+// dx[t] = sum_j kept dx_perm[row_tj] + sum_e dz[t][e] Wg[:, e] (+ the shared expert's dx).
+__global__ void __launch_bounds__(256) dx_combine_kernel(const uint16_t *__restrict__ dxp,
+                                                         const int32_t *__restrict__ dest_row,
+                                                         const float *__restrict__ dz, const float *__restrict__ Wg,
+                                                         const uint16_t *__restrict__ dx_sh, int T, int d, int N, int k,
+                                                         float *__restrict__ dx) {
+  const int t = blockIdx.x;
+  __shared__ int rows[8];
+  __shared__ float dzs[256];
+  if (threadIdx.x < k) rows[threadIdx.x] = dest_row[(size_t)t * k + threadIdx.x];
+  for (int e = threadIdx.x; e < N; e += blockDim.x) dzs[e] = dz[(size_t)t * N + e];
+  __syncthreads();
+  for (int c = threadIdx.x; c < d; c += blockDim.x) {
+    float acc = dx_sh ? __uint_as_float((uint32_t)dx_sh[(size_t)t * d + c] << 16) : 0.f;
+    for (int j = 0; j < k; ++j)
+      if (rows[j] >= 0) acc += __uint_as_float((uint32_t)dxp[(size_t)rows[j] * d + c] << 16);
+    const float *wr = Wg + (size_t)c * N;
+    for (int e = 0; e < N; ++e) acc = fmaf(dzs[e], wr[e], acc);
+    dx[(size_t)t * d + c] = acc;
+  }
+}
+
+__global__ void set_offsets2_kernel(int32_t *offsets, int rows) {
+  if (threadIdx.x == 0) {
+    offsets[0] = 0;
+    offsets[1] = rows;
+  }
+}
+
+inline int grid_for(size_t n, int per_block) {
+  size_t g = (n + per_block - 1) / per_block;
+  return (int)(g > 65535 * 8 ? 65535 * 8 : (g < 1 ? 1 : g));
+}
+
+}  // namespace
+
+int launch_set_offsets2(int32_t *offsets, int rows, cudaStream_t s) {
+  set_offsets2_kernel<<<1, 32, 0, s>>>(offsets, rows);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_wgrad_koff(const int32_t *offsets, int N, int32_t *koff, cudaStream_t s) {
+  wgrad_koff_kernel<<<1, 32, 0, s>>>(offsets, N, koff);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_transpose_rows(const void *X, int C, const int32_t *offsets, const int32_t *koff, int N, int64_t kp,
+                          void *XT, cudaStream_t s) {
+  dim3 grid((unsigned)((kp + 31) / 32), (unsigned)((C + 31) / 32));
+  transpose_rows_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(X), C, offsets, koff, N, kp,
+                                             static_cast<uint16_t *>(XT));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_transpose_weights(const void *W, int G, int A, int B, int out_stride, int col_off, void *WT, cudaStream_t s) {
+  dim3 grid((B + 31) / 32, (A + 31) / 32, G);
+  transpose_weights_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(W), A, B, out_stride, col_off,
+                                                static_cast<uint16_t *>(WT));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_zero_f32(float *p, size_t n, cudaStream_t s) {
+  if (n == 0) return MOE_OK;
+  zero_f32_kernel<<<grid_for(n, 256 * 4), 256, 0, s>>>(p, n);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_dy_dgate(const void *dout, const void *y_perm, const float *topk_w, const int32_t *dest_row,
+                    const int32_t *src_token, const int32_t *rows_end, int64_t max_rows, int k, int d, void *dy,
+                    float *dgate, cudaStream_t s) {
+  if (max_rows <= 0) return MOE_OK;
+  dy_dgate_kernel<<<grid_for((size_t)max_rows, 8), 256, 0, s>>>(
+      static_cast<const uint16_t *>(dout), static_cast<const uint16_t *>(y_perm), topk_w, dest_row, src_token, rows_end,
+      k, d, static_cast<uint16_t *>(dy), dgate);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_router_bwd(const float *logits, const int32_t *idx, const float *topk_w, const float *dgate, int gate, int T,
+                      int N, int k, float *dz, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  router_bwd_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, idx, topk_w, dgate, gate, T, N, k, dz);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_act_bwd(const void *a, const void *u, const void *dh, const int32_t *rows_end, int64_t max_rows, int F,
+                   bool swiglu, void *dA, cudaStream_t s) {
+  if (max_rows <= 0) return MOE_OK;
+  act_bwd_kernel<<<grid_for((size_t)max_rows * F / 2, 256), 256, 0, s>>>(
+      static_cast<const uint16_t *>(a), static_cast<const uint16_t *>(u), static_cast<const uint16_t *>(dh), rows_end, F,
+      swiglu, static_cast<uint16_t *>(dA));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_dwg(const void *x, const float *dz, int T, int d, int N, float *dWg, cudaStream_t s) {
+  dim3 grid((d + 255) / 256, N);
+  dwg_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(x), dz, T, d, N, dWg);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_dx_combine(const void *dxp, const int32_t *dest_row, const float *dz, const float *Wg, const void *dx_sh,
+                      int T, int d, int N, int k, float *dx, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  dx_combine_kernel<<<T, 256, 0, s>>>(static_cast<const uint16_t *>(dxp), dest_row, dz, Wg,
+                                      static_cast<const uint16_t *>(dx_sh), T, d, N, k, dx);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

@@ -52,6 +52,26 @@ int launch_router_sum(const float *partial, int S, int pstride, const float *log
                       cudaStream_t s);
 // counts_routed = counts_kept = C for every expert (expert choice)
 int launch_fill_counts(int32_t *counts_routed, int32_t *counts_kept, int N, int C, cudaStream_t s);
+// backward pieces
+int tc_wgrad_gemm(const void *AT, const void *BT, const int32_t *koff, int G, int M, int Nn, int64_t kp, float *out,
+                  int *status, cudaStream_t stream);
+int launch_wgrad_koff(const int32_t *offsets, int N, int32_t *koff, cudaStream_t s);
+int launch_transpose_rows(const void *X, int C, const int32_t *offsets, const int32_t *koff, int N, int64_t kp,
+                          void *XT, cudaStream_t s);
+int launch_transpose_weights(const void *W, int G, int A, int B, int out_stride, int col_off, void *WT, cudaStream_t s);
+int launch_zero_f32(float *p, size_t n, cudaStream_t s);
+int launch_dy_dgate(const void *dout, const void *y_perm, const float *topk_w, const int32_t *dest_row,
+                    const int32_t *src_token, const int32_t *rows_end, int64_t max_rows, int k, int d, void *dy,
+                    float *dgate, cudaStream_t s);
+int launch_router_bwd(const float *logits, const int32_t *idx, const float *topk_w, const float *dgate, int gate, int T,
+                      int N, int k, float *dz, cudaStream_t s);
+int launch_act_bwd(const void *a, const void *u, const void *dh, const int32_t *rows_end, int64_t max_rows, int F,
+                   bool swiglu, void *dA, cudaStream_t s);
+int launch_dwg(const void *x, const float *dz, int T, int d, int N, float *dWg, cudaStream_t s);
+int launch_dx_combine(const void *dxp, const int32_t *dest_row, const float *dz, const float *Wg, const void *dx_sh,
+                      int T, int d, int N, int k, float *dx, cudaStream_t s);
+int launch_set_offsets2(int32_t *offsets, int rows, cudaStream_t s);
+
 // expert choice: scores + per-expert top-C selection
 int launch_expert_choice(const float *logits, int T, int N, int C, float *scores, int32_t *offsets,
                          int32_t *src_token, int32_t *dest_row, cudaStream_t s);

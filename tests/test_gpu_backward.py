@@ -1,0 +1,78 @@
+"""Backward pass on the GPU against the oracle's (B300).
+
+The forward runs through moe_layer_forward; moe_layer_backward then produces
+float32 gradients, compared with oracle.layer_backward on the GPU's routing
+(top-k and the kept set) under the bf16 rule max|gpu - ref| <= 2e-2 max|ref| + 1e-3
+per tensor: the backward's intermediates (dy, dh, a, u, dA, dx rows) are bf16.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_mixture_experts_62_b300 as moe
+import synth
+from parity import assert_close_out, layer_on_device, to_dev
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    dict(T=200, d=128, N=8, k=2, F=192),
+    dict(T=300, d=256, N=16, k=4, F=128, gate="sigmoid", shared_F=192, sel_bias_range=0.05),
+    dict(T=256, d=128, N=8, k=3, F=256, gate="softmax_full"),
+    dict(T=400, d=128, N=8, k=2, F=128, capacity_factor=0.6, zipf_s=1.2),
+    dict(T=150, d=192, N=5, k=2, F=160, act="relu"),
+    dict(T=1500, d=256, N=4, k=2, F=256),            # CTA-pair tiles in the GEMMs
+    dict(T=512, d=1024, N=8, k=2, F=2048),
+]
+
+
+@pytest.mark.parametrize("kw", CASES)
+def test_backward_parity(kw):
+    kw = dict(kw)
+    wl = synth.Workload("bwd", 41, act=kw.pop("act", "swiglu"), gate=kw.pop("gate", "softmax"), dtype="bf16", **kw)
+    inp = synth.make_inputs(wl)
+    layer = layer_on_device(inp)
+    x = to_dev(inp.x, "bf16")
+    layer.forward(x)
+    cfg = layer.cfg
+    dout_np = synth.normal(wl.seed, 77, (wl.T, wl.d), 1.0, "bf16")
+    dout = to_dev(dout_np, "bf16")
+    f32 = lambda shape: torch.full(shape, float("nan"), device="cuda")  # noqa: E731  (all must be overwritten)
+    sw = wl.act == "swiglu"
+    g = dict(dx=f32((wl.T, wl.d)), dWg=f32((wl.d, wl.N)), dw1=f32((wl.N, wl.F, wl.d)),
+             dw3=f32((wl.N, wl.F, wl.d)) if sw else None, dw2=f32((wl.N, wl.d, wl.F)))
+    Fs = wl.shared_F
+    if Fs:
+        g.update(dsw1=f32((Fs, wl.d)), dsw3=f32((Fs, wl.d)) if sw else None, dsw2=f32((wl.d, Fs)))
+    bws = torch.zeros(moe.moe_backward_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    moe.moe_layer_backward(cfg, x, layer.Wg, layer.w1, layer.w3, layer.w2, layer.sw1, layer.sw3, layer.sw2, dout,
+                           g["dx"], g["dWg"], g["dw1"], g.get("dw3"), g["dw2"], g.get("dsw1"), g.get("dsw3"),
+                           g.get("dsw2"), layer.ws, bws)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    idx = layer.views()["topk_idx"].cpu().numpy()
+    cap = cfg.capacity
+    disp = oracle.dispatch(idx, wl.N, cap)
+    ref = oracle.layer_backward(oracle.widen(inp.x, "bf16"), inp.logit_bias, oracle.params64(inp), wl.act, wl.gate,
+                                idx, disp, oracle.widen(dout_np, "bf16"))
+    pairs = [("dx", ref.dx), ("dWg", ref.dWg), ("dw1", ref.dw1), ("dw2", ref.dw2)]
+    if sw:
+        pairs.append(("dw3", ref.dw3))
+    if Fs:
+        pairs += [("dsw1", ref.dsw1), ("dsw2", ref.dsw2)] + ([("dsw3", ref.dsw3)] if sw else [])
+    for name, r in pairs:
+        got = g[name].cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(got)), name
+        assert_close_out(got, r, "bf16", what=name)
+    # experts that processed no token get exactly zero gradient
+    unused = np.nonzero(disp.counts_kept == 0)[0]
+    for e in unused:
+        assert np.all(g["dw1"][e].cpu().numpy() == 0.0) and np.all(g["dw2"][e].cpu().numpy() == 0.0)
+
+
+def test_backward_rejects_unsupported_configs():
+    cfg = moe.make_config(64, 64, 8, 2, 128, dtype=moe.DTYPE_F32)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_backward_workspace_size(cfg)
+    assert e.value.code == moe.MOE_ERR_UNSUPPORTED
