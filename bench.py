@@ -381,6 +381,11 @@ def run_ours(args, wl, dist, rank, local):
     world = dist.get_world_size() if dist is not None else 1
     value = wl.T * args.steps * world / (t_max / 1e3)
 
+    # optional: the backward step (gradients of a fixed dout), graph-replayed
+    bwd = None
+    if args.backward:
+        bwd = time_backward(args, moe, layer, x, wl, stream)
+
     # routing facts of this run (for the algorithmic counts)
     counts_kept = v["counts_kept"].cpu().numpy()
     kept_rows = int(counts_kept.sum())
@@ -491,10 +496,54 @@ def run_ours(args, wl, dist, rank, local):
                           "algorithmic_bytes": layer_bytes(wl, touched)},
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches_per_step * args.steps,
+                **({"backward": bwd} if bwd is not None else {}),
                 "clocks": clocks}
         if args.cpu_baseline_tokens > 0:
             line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_baseline_tokens)
         print(json.dumps(line), flush=True)
+
+
+def time_backward(args, moe, layer, x, wl, stream):
+    """Time moe_layer_backward (after a forward) as a CUDA-graph replay; FLOPs of its
+    GEMMs: dh, the a/u recompute, dx rows, dW2, dW1/dW3 = 7 (SwiGLU) or 4 (ReLU)
+    times 2 R d F, R the kept rows."""
+    import torch
+    cfg = layer.cfg
+    sw = wl.act == "swiglu"
+    dout = torch.randn((wl.T, wl.d), device="cuda").to(x.dtype)
+    f32 = lambda *shape: torch.empty(shape, device="cuda")  # noqa: E731
+    dx, dWg = f32(wl.T, wl.d), f32(wl.d, wl.N)
+    dw1, dw3, dw2 = f32(wl.N, wl.F, wl.d), (f32(wl.N, wl.F, wl.d) if sw else None), f32(wl.N, wl.d, wl.F)
+    Fs = wl.shared_F
+    dsw1, dsw3, dsw2 = (f32(Fs, wl.d), f32(Fs, wl.d) if sw else None, f32(wl.d, Fs)) if Fs else (None, None, None)
+    bws = torch.empty(moe.moe_backward_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+
+    def step():
+        moe.moe_layer_backward(cfg, x, layer.Wg, layer.w1, layer.w3, layer.w2, layer.sw1, layer.sw3, layer.sw2,
+                               dout, dx, dWg, dw1, dw3, dw2, dsw1, dsw3, dsw2, layer.ws, bws)
+
+    layer.forward(x)
+    for _ in range(args.warmup):
+        step()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if layer.device_status() != 0:
+        raise RuntimeError("device status not clean after the backward")
+    ms = e0.elapsed_time(e1) / args.steps
+    R = int(layer.views()["counts_kept"].sum().item())
+    gemm_flops = (7 if sw else 4) * 2.0 * R * wl.d * wl.F + ((7 if sw else 4) * 2.0 * wl.T * wl.d * Fs if Fs else 0.0)
+    return {"ms_per_step": ms, "tokens_per_s": wl.T / (ms / 1e3), "gemm_flops": gemm_flops,
+            "gemm_tflops_over_step": gemm_flops / (ms / 1e3) / 1e12}
 
 
 def main():
@@ -509,6 +558,7 @@ def main():
     ap.add_argument("--ref-sample", type=int, default=4, help="tokens per reference-arm step")
     ap.add_argument("--override", nargs="*", default=[], help="workload fields to change, e.g. N=32 T=1024")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA-graph replay")
+    ap.add_argument("--backward", action="store_true", help="also time the backward step (bf16 token choice)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

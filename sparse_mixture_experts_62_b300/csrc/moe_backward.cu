@@ -30,26 +30,37 @@ __global__ void wgrad_koff_kernel(const int32_t *__restrict__ offsets, int N, in
   koff[N] = acc;
 }
 
-// XT[c][koff[e] + i] = X[offsets[e] + i][c] for i < rows of e, 0 in the padding.
-// 32 x 32 tiles through shared memory; the group of a padded column is found by
-// binary search over koff.
+// 64 x 64 bf16 tiles through shared memory with 16-byte global loads and stores
+// (every dimension is a multiple of 8 elements, so an 8-element vector is
+// either wholly inside or wholly outside the matrix).  The tile is read as 64
+// source rows of 8 vectors and written as 64 output rows of 8 vectors.
+constexpr int TT = 64, TPAD = 8;
+
+__device__ __forceinline__ void tile_store_transposed(uint16_t (*tile)[TT + TPAD], uint16_t *out, size_t out_stride,
+                                                      int orow0, int ocol0, int orows, int ocols) {
+  for (int v = threadIdx.x; v < TT * (TT / 8); v += blockDim.x) {
+    const int orow = v / (TT / 8), oc = (v % (TT / 8)) * 8;
+    if (orow0 + orow >= orows || ocol0 + oc >= ocols) continue;
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      w[q] = (uint32_t)tile[oc + 2 * q][orow] | ((uint32_t)tile[oc + 2 * q + 1][orow] << 16);
+    *reinterpret_cast<uint4 *>(out + (size_t)(orow0 + orow) * out_stride + ocol0 + oc) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// XT[c][koff[e] + i] = X[offsets[e] + i][c] for i < rows of e, 0 in the padding;
+// the group of a padded column is found by binary search over koff.
 __global__ void __launch_bounds__(256) transpose_rows_kernel(const uint16_t *__restrict__ X, int C,
                                                              const int32_t *__restrict__ offsets,
                                                              const int32_t *__restrict__ koff, int N, int64_t kp,
                                                              uint16_t *__restrict__ XT) {
-  __shared__ uint16_t tile[32][34];
-  __shared__ int s_src[32];
-  const int p0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  __shared__ __align__(16) uint16_t tile[TT][TT + TPAD];
+  __shared__ int s_src[TT];
+  const int p0 = blockIdx.x * TT, c0 = blockIdx.y * TT;
   const int kp_used = koff[N];
-  if (p0 >= kp_used) {
-    // columns past the last group: zeros, so the GEMM's K blocks read nothing stale
-    for (int i = threadIdx.x; i < 32 * 32; i += 256) {
-      const int c = c0 + i / 32, p = p0 + i % 32;
-      if (c < C && p < kp) XT[(size_t)c * kp + p] = 0;
-    }
-    return;
-  }
-  if (threadIdx.x < 32) {
+  if (threadIdx.x < TT) {
     const int p = p0 + threadIdx.x;
     int src = -1;
     if (p < kp_used) {
@@ -65,36 +76,34 @@ __global__ void __launch_bounds__(256) transpose_rows_kernel(const uint16_t *__r
     s_src[threadIdx.x] = src;
   }
   __syncthreads();
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  for (int r = ty; r < 32; r += 8) {
-    const int src = s_src[r], c = c0 + tx;
-    tile[r][tx] = (src >= 0 && c < C) ? X[(size_t)src * C + c] : (uint16_t)0;
+  // tile[r][*] = source row of padded column p0 + r, columns c0 ..
+  for (int v = threadIdx.x; v < TT * (TT / 8); v += blockDim.x) {
+    const int r = v / (TT / 8), cc = (v % (TT / 8)) * 8;
+    const int src = s_src[r];
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    if (src >= 0 && c0 + cc < C) q = *reinterpret_cast<const uint4 *>(X + (size_t)src * C + c0 + cc);
+    *reinterpret_cast<uint4 *>(&tile[r][cc]) = q;
   }
   __syncthreads();
-  for (int r = ty; r < 32; r += 8) {
-    const int c = c0 + r, p = p0 + tx;
-    if (c < C && p < kp) XT[(size_t)c * kp + p] = tile[tx][r];
-  }
+  tile_store_transposed(tile, XT, (size_t)kp, c0, p0, C, (int)kp);
 }
 
 // WT[g][b][col_off + a] = W[g][a][b]; W is [G][A][B], WT rows have out_stride elements.
 __global__ void __launch_bounds__(256) transpose_weights_kernel(const uint16_t *__restrict__ W, int A, int B,
                                                                 int out_stride, int col_off,
                                                                 uint16_t *__restrict__ WT) {
-  __shared__ uint16_t tile[32][34];
-  const int b0 = blockIdx.x * 32, a0 = blockIdx.y * 32, g = blockIdx.z;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  __shared__ __align__(16) uint16_t tile[TT][TT + TPAD];
+  const int b0 = blockIdx.x * TT, a0 = blockIdx.y * TT, g = blockIdx.z;
   const uint16_t *Wg = W + (size_t)g * A * B;
-  uint16_t *WTg = WT + (size_t)g * B * out_stride;
-  for (int r = ty; r < 32; r += 8) {
-    const int a = a0 + r, b = b0 + tx;
-    tile[r][tx] = (a < A && b < B) ? Wg[(size_t)a * B + b] : (uint16_t)0;
+  uint16_t *WTg = WT + (size_t)g * B * out_stride + col_off;
+  for (int v = threadIdx.x; v < TT * (TT / 8); v += blockDim.x) {
+    const int r = v / (TT / 8), cc = (v % (TT / 8)) * 8;
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    if (a0 + r < A && b0 + cc < B) q = *reinterpret_cast<const uint4 *>(Wg + (size_t)(a0 + r) * B + b0 + cc);
+    *reinterpret_cast<uint4 *>(&tile[r][cc]) = q;
   }
   __syncthreads();
-  for (int r = ty; r < 32; r += 8) {
-    const int b = b0 + r, a = a0 + tx;
-    if (a < A && b < B) WTg[(size_t)b * out_stride + col_off + a] = tile[tx][r];
-  }
+  tile_store_transposed(tile, WTg, (size_t)out_stride, b0, a0, B, A);
 }
 
 __global__ void zero_f32_kernel(float *p, size_t n) {
@@ -272,14 +281,14 @@ int launch_wgrad_koff(const int32_t *offsets, int N, int32_t *koff, cudaStream_t
 
 int launch_transpose_rows(const void *X, int C, const int32_t *offsets, const int32_t *koff, int N, int64_t kp,
                           void *XT, cudaStream_t s) {
-  dim3 grid((unsigned)((kp + 31) / 32), (unsigned)((C + 31) / 32));
+  dim3 grid((unsigned)((kp + TT - 1) / TT), (unsigned)((C + TT - 1) / TT));
   transpose_rows_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(X), C, offsets, koff, N, kp,
                                              static_cast<uint16_t *>(XT));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int launch_transpose_weights(const void *W, int G, int A, int B, int out_stride, int col_off, void *WT, cudaStream_t s) {
-  dim3 grid((B + 31) / 32, (A + 31) / 32, G);
+  dim3 grid((B + TT - 1) / TT, (A + TT - 1) / TT, G);
   transpose_weights_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(W), A, B, out_stride, col_off,
                                                 static_cast<uint16_t *>(WT));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
