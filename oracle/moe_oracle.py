@@ -322,6 +322,34 @@ def router_z_loss(z: np.ndarray) -> float:
     return float(np.mean(lse ** 2))
 
 
+def sequence_balance_loss(z: np.ndarray, idx: np.ndarray, gate: str, seq_len: int) -> float:
+    """DeepSeek-V3's sequence-wise balance loss: the Switch loss N sum_i f_i P_i
+    computed within each sequence and averaged over the sequences.
+
+    "Chapter 19: MoE", 19.3.4 (V3 keeps a small sequence-wise auxiliary balance
+    loss against extreme imbalance inside one sequence); CS336 lecture 4,
+    section 9 (it is the removed auxiliary loss with the unit of statistics
+    changed from the batch to one sequence).  Tokens form consecutive sequences
+    of seq_len (the last may be shorter); f_i counts the routed assignments of the
+    sequence (before any capacity) over its L k; P_i is the mean router
+    probability (as in load_stats) over the sequence's tokens."""
+    T, N = z.shape
+    k = idx.shape[1]
+    p = router_probabilities(z, gate)
+    losses = []
+    for s0 in range(0, T, seq_len):
+        s1 = min(T, s0 + seq_len)
+        L = s1 - s0
+        f = np.zeros(N)
+        for t in range(s0, s1):
+            for j in range(k):
+                f[idx[t, j]] += 1.0
+        f /= L * k
+        P = p[s0:s1].mean(axis=0)
+        losses.append(N * float(np.sum(f * P)))
+    return float(np.mean(losses))
+
+
 def bias_update(sel_bias: np.ndarray, counts_routed: np.ndarray, T: int, k: int, gamma: float) -> np.ndarray:
     """DeepSeek-V3 auxiliary-loss-free balancing, one step after a batch:
     b_i + gamma if expert i got fewer than the mean T k / N assignments,

@@ -547,3 +547,31 @@ def test_backward_dropped_slots_get_no_gradient():
     fully_dropped = np.all(ref.disp.dest_row < 0, axis=1)
     assert fully_dropped.any()
     assert np.all(g.dx[fully_dropped] == 0.0)
+
+
+def test_sequence_balance_loss_pins():
+    """One sequence spanning the batch gives the batch loss; sequences that are
+    each uniform give 1; a sequence routed entirely to one expert with all its
+    probability there gives N (CS336 lecture 4, section 9: the batch loss with the
+    unit changed to a sequence)."""
+    rng = np.random.default_rng(8)
+    T, N, k = 60, 6, 2
+    z = rng.standard_normal((T, N)).astype(np.float32)
+    idx = oracle.topk(z, k)
+    d = oracle.dispatch(idx, N, 0)
+    batch = oracle.load_stats(z, "softmax", d, k).aux
+    assert oracle.sequence_balance_loss(z, idx, "softmax", seq_len=T) == pytest.approx(batch, rel=1e-12)
+    assert oracle.sequence_balance_loss(z, idx, "softmax", seq_len=1000) == pytest.approx(batch, rel=1e-12)
+    # uniform inside every sequence of 6 tokens, k = 1: f = P = 1/N -> 1
+    zu = np.zeros((T, N), dtype=np.float32)
+    iu = (np.arange(T) % N).reshape(T, 1).astype(np.int32)
+    assert oracle.sequence_balance_loss(zu, iu, "softmax", seq_len=6) == pytest.approx(1.0, abs=1e-14)
+    # second sequence collapsed onto expert 2 with all probability there: its loss is N
+    zc = np.zeros((12, N), dtype=np.float32)
+    zc[6:, 2] = 60.0
+    ic = np.concatenate([np.arange(6), np.full(6, 2)]).reshape(12, 1).astype(np.int32)
+    assert oracle.sequence_balance_loss(zc, ic, "softmax", seq_len=6) == pytest.approx((1.0 + N) / 2, rel=1e-12)
+    # averaging: the mean of the per-sequence losses, the short last sequence included
+    l1 = oracle.sequence_balance_loss(z[:50], idx[:50], "softmax", seq_len=50)
+    l2 = oracle.sequence_balance_loss(z[50:], idx[50:], "softmax", seq_len=50)
+    assert oracle.sequence_balance_loss(z, idx, "softmax", seq_len=50) == pytest.approx((l1 + l2) / 2, rel=1e-12)
