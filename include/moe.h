@@ -260,6 +260,21 @@ MOE_API int moe_layer_backward(const moe_config *cfg, const void *x, const float
  * Partial sums use the workspace scratch; the result is deterministic. */
 MOE_API int moe_router_zloss(const moe_config *cfg, const float *logits, float *z_loss, void *ws, void *stream);
 
+/* DeepSeek-V3 sequence-wise balance loss (Chapter 19, 19.3.4: a small auxiliary
+ * loss kept against extreme imbalance inside one sequence; CS336 lecture 4,
+ * section 9: the Switch loss of moe_load_stats with its statistics taken over
+ * one sequence instead of the batch).  The T tokens form consecutive sequences
+ * of seq_len (>= 1; the last may be shorter, a seq_len above T is one sequence);
+ * for each, loss_s = N sum_e f_e P_e with f_e = (assignments of the sequence's
+ * tokens to e in topk_idx [T, k], before any capacity) / (L k) and P_e the mean
+ * router probability of e over its L tokens (as in moe_load_stats for
+ * cfg->gate).  *loss (a device float) = the mean of loss_s over the sequences,
+ * summed in a fixed order (deterministic).  Token-choice configs only; T >= 1.
+ * An index outside [0, N) in topk_idx is skipped and MOE_ERR_BOUNDS is recorded
+ * in the workspace status word. */
+MOE_API int moe_seq_balance_loss(const moe_config *cfg, const float *logits, const int32_t *topk_idx,
+                                 int32_t seq_len, float *loss, void *ws, void *stream);
+
 /* DeepSeek-V3 auxiliary-loss-free balancing step (CS336 lecture 4, section 9;
  * Chapter 19, 19.3.4): for each expert, sel_bias[e] += gamma when
  * counts_routed[e] < T k / N, -= gamma when it is larger, unchanged when equal

@@ -378,21 +378,19 @@ class LayerResult:
     stats: LoadStats
 
 
-def layer_forward(inp, tokens: Optional[np.ndarray] = None, idx_override: Optional[np.ndarray] = None,
-                  cap: Optional[int] = None) -> LayerResult:
+def layer_forward(inp, tokens: Optional[np.ndarray] = None, cap: Optional[int] = None) -> LayerResult:
     """The whole layer: route every token, dispatch, run the experts and combine.
 
     `inp` carries the workload and its tensors (see the input module).
     `tokens`: compute the output only for these token rows (routing, dispatch and
     stats are always computed for all tokens, since capacity couples them).
-    `idx_override`: use this top-k instead of the oracle's own (gate weights are
-    still computed from the oracle's logits at those indices)."""
+    `cap`: a capacity in place of the workload's capacity factor."""
     wl = inp.wl
     dt = wl.dtype
     x64 = widen(inp.x, dt)
     z = router_logits(x64, inp.Wg, inp.logit_bias)
     sel, s = selection_scores(z, wl.gate, inp.sel_bias)
-    idx = topk(sel, wl.k) if idx_override is None else np.asarray(idx_override, dtype=np.int32)
+    idx = topk(sel, wl.k)
     w = gate_weights(z, s, idx, wl.gate)
     if cap is None:
         cap = capacity(wl.capacity_factor, wl.T, wl.k, wl.N) if wl.capacity_factor > 0 else 0

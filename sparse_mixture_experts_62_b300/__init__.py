@@ -30,7 +30,7 @@ ROUTING_TOKEN_CHOICE, ROUTING_EXPERT_CHOICE = 0, 1
 EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_workspace_layout", "moe_route",
            "moe_dispatch", "moe_expert_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
            "moe_load_stats", "moe_get_device_status", "moe_dispatch_noalloc", "moe_check_wait_timeout",
-           "moe_router_zloss", "moe_bias_update", "moe_ec_route",
+           "moe_router_zloss", "moe_bias_update", "moe_ec_route", "moe_seq_balance_loss",
            "moe_backward_workspace_size", "moe_layer_backward")
 
 
@@ -74,6 +74,7 @@ def _load():
         "moe_get_device_status": [P, P, ctypes.POINTER(ctypes.c_int)],
         "moe_check_wait_timeout": [P, ctypes.c_int64, P],
         "moe_router_zloss": [C, P, P, P, P],
+        "moe_seq_balance_loss": [C, P, P, ctypes.c_int32, P, P, P],
         "moe_ec_route": [C, P, P, P, P, P, P, P, P, P, P],
         "moe_backward_workspace_size": [C, ctypes.POINTER(ctypes.c_size_t)],
         "moe_layer_backward": [C] + [P] * 20,
@@ -210,6 +211,11 @@ def moe_layer_backward(cfg, x, Wg, w1, w3, w2, sw1, sw3, sw2, dout, dx, dWg, dw1
 def moe_router_zloss(cfg, logits, z_loss, ws, stream=None):
     _check(_lib.moe_router_zloss(ctypes.byref(cfg), _ptr(logits), _ptr(z_loss), _ptr(ws), _stream(stream)),
            "moe_router_zloss")
+
+
+def moe_seq_balance_loss(cfg, logits, topk_idx, seq_len: int, loss, ws, stream=None):
+    _check(_lib.moe_seq_balance_loss(ctypes.byref(cfg), _ptr(logits), _ptr(topk_idx), int(seq_len), _ptr(loss),
+                                     _ptr(ws), _stream(stream)), "moe_seq_balance_loss")
 
 
 def moe_bias_update(cfg, counts_routed, sel_bias, gamma: float, stream=None):

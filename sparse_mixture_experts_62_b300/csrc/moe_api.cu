@@ -55,13 +55,20 @@ inline int ec_c(const moe_config *c) { return c->capacity < c->T ? c->capacity :
 inline int64_t routed_rows(const moe_config *c) { return is_ec(c) ? (int64_t)c->N * ec_c(c) : (int64_t)c->T * c->k; }
 inline int slots(const moe_config *c) { return is_ec(c) ? c->N : c->k; }
 
+// Scratch for the load statistics, the z-loss and the sequence-wise balance
+// loss: up to 2 ceil(T / 32) + 2 rows of N float partials, then T floats.
+inline size_t stats_rows_bytes(const moe_config *c) {
+  const size_t nch_s = ((size_t)c->T + kStatsChunk - 1) / kStatsChunk;
+  return align256((2 * nch_s + 2) * (size_t)c->N * 4);
+}
+inline size_t stats_bytes(const moe_config *c) { return stats_rows_bytes(c) + align256((size_t)c->T * 4); }
+
 int layout(const moe_config *c, moe_ws_layout *L) {
   const size_t T = (size_t)c->T, N = (size_t)c->N, k = (size_t)c->k, d = (size_t)c->d, F = (size_t)c->ffn;
   const size_t Fs = (size_t)c->shared_ffn, es = esize(c);
   const size_t rows = (size_t)routed_rows(c);
   const size_t sl = (size_t)slots(c);
   const size_t nch_d = (T + kDispatchChunk - 1) / kDispatchChunk;
-  const size_t nch_s = (T + kStatsChunk - 1) / kStatsChunk;
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -87,7 +94,7 @@ int layout(const moe_config *c, moe_ws_layout *L) {
     const size_t Np = (size_t)router_tc_npad(c->N), dp = (size_t)router_tc_dpad(c->d);
     router_bytes = align256(Np * 3 * dp * 2) + (size_t)router_tc_max_splits(c->T, c->d) * T * Np * 4;
   }
-  L->scratch = take(align256(2 * nch_d * N * 4) + align256(nch_s * N * 4) + router_bytes);
+  L->scratch = take(align256(2 * nch_d * N * 4) + stats_bytes(c) + router_bytes);
   L->total = o;
   return MOE_OK;
 }
@@ -109,10 +116,13 @@ struct Ws {
     const size_t nch = ((size_t)c->T + kDispatchChunk - 1) / kDispatchChunk;
     return at<float>(L.scratch + align256(2 * nch * c->N * 4));
   }
+  float *seq_loss(const moe_config *c) const {
+    const size_t nch = ((size_t)c->T + kDispatchChunk - 1) / kDispatchChunk;
+    return at<float>(L.scratch + align256(2 * nch * c->N * 4) + stats_rows_bytes(c));
+  }
   size_t router_off(const moe_config *c) const {
     const size_t nch = ((size_t)c->T + kDispatchChunk - 1) / kDispatchChunk;
-    const size_t nchs = ((size_t)c->T + kStatsChunk - 1) / kStatsChunk;
-    return L.scratch + align256(2 * nch * c->N * 4) + align256(nchs * c->N * 4);
+    return L.scratch + align256(2 * nch * c->N * 4) + stats_bytes(c);
   }
   uint16_t *router_wsplit(const moe_config *c) const { return at<uint16_t>(router_off(c)); }
   float *router_partial(const moe_config *c) const {
@@ -510,6 +520,21 @@ int moe_router_zloss(const moe_config *cfg, const float *logits, float *z_loss, 
   Ws w;
   MOE_TRY(make_ws(cfg, ws, &w));
   return launch_router_zloss(logits, cfg->T, cfg->N, w.stats_partial(cfg), z_loss, static_cast<cudaStream_t>(stream));
+}
+
+int moe_seq_balance_loss(const moe_config *cfg, const float *logits, const int32_t *topk_idx, int32_t seq_len,
+                         float *loss, void *ws, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (is_ec(cfg)) return MOE_ERR_INVALID_ARG;  // expert choice has no per-token top-k to count
+  if (!logits || !topk_idx || !loss || seq_len < 1) return MOE_ERR_INVALID_ARG;
+  if (cfg->T == 0) return MOE_ERR_INVALID_ARG;  // a mean over no sequences
+  Ws w;
+  MOE_TRY(make_ws(cfg, ws, &w));
+  const int L = seq_len < cfg->T ? seq_len : cfg->T;
+  if (L >= kStatsChunk && (size_t)seq_balance_chunks(cfg->T, L) * cfg->N * 4 > stats_rows_bytes(cfg))
+    return MOE_ERR_UNSUPPORTED;  // cannot happen: the bound above holds for every L >= 32
+  return launch_seq_balance_loss(logits, topk_idx, cfg->T, cfg->N, cfg->k, cfg->gate, L, w.stats_partial(cfg),
+                                 w.seq_loss(cfg), loss, w.status(), static_cast<cudaStream_t>(stream));
 }
 
 int moe_bias_update(const moe_config *cfg, const int32_t *counts_routed, float *sel_bias, float gamma, void *stream) {

@@ -86,6 +86,11 @@ constexpr int kStatsChunk = 32;  // tokens per partial-sum chunk
 int launch_load_stats(const float *logits, const int32_t *counts_routed, const int32_t *counts_kept, int T, int N,
                       long long total, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s);
 int launch_router_zloss(const float *logits, int T, int N, float *partial, float *z_loss, cudaStream_t s);
+// Sequence-wise balance loss: chunks of the P partials it needs for T tokens in
+// sequences of L (at most 2 ceil(T / 32) + 2 rows of N floats), then the launch.
+int seq_balance_chunks(int T, int L);
+int launch_seq_balance_loss(const float *logits, const int32_t *topk_idx, int T, int N, int k, int gate, int L,
+                            float *partial, float *seq_loss, float *loss, int *status, cudaStream_t s);
 int launch_bias_update(const int32_t *counts_routed, int T, int k, int N, float *sel_bias, float gamma,
                        cudaStream_t s);
 

@@ -9,6 +9,12 @@
 // p_i(t) is the full N-way softmax of the logits (softmax gate) or
 // s_i / sum_l s_l with s = sigmoid(z) (sigmoid gate), in float32.  Partial sums
 // per 32-token chunk are reduced in a fixed order, so the result is deterministic.
+//
+// The sequence-wise balance loss of DeepSeek-V3 ("Chapter 19: MoE" 19.3.4;
+// CS336 lecture 4, section 9) is the same N sum_i f_i P_i taken inside each
+// sequence of L consecutive tokens and averaged over the sequences.  For L >= 32
+// the P partials come from chunks that never cross a sequence boundary and one
+// CTA per sequence finishes it; for L < 32 one warp takes a whole sequence.
 #include "moe_common.cuh"
 #include "moe_internal.h"
 
@@ -17,45 +23,58 @@ namespace {
 
 constexpr int SC = kStatsChunk;  // tokens per chunk
 
+// Router probabilities of one token, lane + 32 i holding expert lane + 32 i
+// (zero past N); called by a whole warp.
+__device__ __forceinline__ void token_probs(const float *__restrict__ zr, int N, bool softmax, int lane, float v[8]) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < N) ? zr[e] : -INFINITY;
+    m = fmaxf(m, v[i]);
+  }
+  if (softmax) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    float p = 0.f;
+    if (e < N) p = softmax ? expf(v[i] - m) : 1.0f / (1.0f + expf(-v[i]));
+    v[i] = p;
+    sum += p;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  const float inv = 1.0f / sum;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] *= inv;
+}
+
+// Sum of p over one chunk of at most SC tokens.  Chunk c is chunk c % cps of
+// sequence c / cps (sequences of L tokens, the last one possibly shorter); a
+// chunk past its sequence's end writes zeros.  The batch statistics use L = T.
 __global__ void __launch_bounds__(256) stats_partial_kernel(const float *__restrict__ logits, int T, int N, int gate,
-                                                            float *__restrict__ partial) {
+                                                            int L, int cps, float *__restrict__ partial) {
   __shared__ float red[8][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  const int tb = blockIdx.x * SC;
+  const int seq = blockIdx.x / cps, j = blockIdx.x - seq * cps;
+  const long long s0 = (long long)seq * L;
+  const long long tb = s0 + (long long)j * SC;
+  const long long te = min(min(s0 + L, (long long)T), tb + SC);
+  const bool softmax = gate != MOE_GATE_SIGMOID_BIAS;
   for (int tt = warp; tt < SC; tt += 8) {  // SC / 8 tokens per warp
-    const int t = tb + tt;
-    if (t >= T) break;
-    const float *zr = logits + (size_t)t * N;
+    const long long t = tb + tt;
+    if (t >= te) break;
     float v[8];
-    float m = -INFINITY;
+    token_probs(logits + (size_t)t * N, N, softmax, lane, v);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      v[i] = (e < N) ? zr[e] : -INFINITY;
-      m = fmaxf(m, v[i]);
-    }
-    const bool softmax = gate != MOE_GATE_SIGMOID_BIAS;
-    if (softmax) {
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    }
-    float sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      float p = 0.f;
-      if (e < N) p = softmax ? expf(v[i] - m) : 1.0f / (1.0f + expf(-v[i]));
-      v[i] = p;
-      sum += p;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    const float inv = 1.0f / sum;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] += v[i] * inv;
+    for (int i = 0; i < 8; ++i) acc[i] += v[i];
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) red[warp][lane + 32 * i] = acc[i];
@@ -117,6 +136,84 @@ __global__ void __launch_bounds__(1024) stats_final_kernel(const float *__restri
   }
 }
 
+// One CTA per sequence (L >= 32): P_e L = the sequence's chunk partials added in
+// order, n_e = its assignments to e (counted from topk_idx), and
+// loss_s = N sum_e (n_e / (L k)) (P_e L / L).
+__global__ void __launch_bounds__(256) seq_final_kernel(const float *__restrict__ partial, int cps,
+                                                        const int32_t *__restrict__ topk_idx, int T, int N, int k,
+                                                        int L, float *__restrict__ seq_loss, int *status) {
+  __shared__ int cnt[256];
+  __shared__ float red[256];
+  const int e = threadIdx.x;
+  const int seq = blockIdx.x;
+  const long long t0 = (long long)seq * L, t1 = min((long long)T, t0 + L);
+  cnt[e] = 0;
+  __syncthreads();
+  for (long long i = t0 * k + threadIdx.x; i < t1 * k; i += blockDim.x) {
+    const int v = topk_idx[i];
+    if ((unsigned)v < (unsigned)N) atomicAdd(&cnt[v], 1);
+    else set_status(status, MOE_ERR_BOUNDS);
+  }
+  float psum = 0.f;
+  if (e < N)
+    for (int j = 0; j < cps; ++j) psum += partial[((size_t)seq * cps + j) * N + e];
+  __syncthreads();
+  red[e] = (e < N) ? (float)cnt[e] * psum : 0.f;
+  __syncthreads();
+  for (int off = 128; off > 0; off >>= 1) {
+    if (e < off) red[e] += red[e + off];
+    __syncthreads();
+  }
+  if (e == 0) {
+    const float Ls = (float)(t1 - t0);
+    seq_loss[seq] = (float)N * (red[0] / (Ls * (float)k)) / Ls;
+  }
+}
+
+// One warp per sequence (L < 32): p and the counts of the sequence's tokens in
+// registers (lane + 32 i holds expert lane + 32 i), then the same loss_s.
+__global__ void __launch_bounds__(256) seq_short_kernel(const float *__restrict__ logits,
+                                                        const int32_t *__restrict__ topk_idx, int T, int N, int k,
+                                                        int gate, int L, int nseq, float *__restrict__ seq_loss,
+                                                        int *status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int seq = blockIdx.x * 8 + warp;
+  if (seq >= nseq) return;
+  const int t0 = seq * L, t1 = min(T, t0 + L);
+  const bool softmax = gate != MOE_GATE_SIGMOID_BIAS;
+  float P[8];
+  int n[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    P[i] = 0.f;
+    n[i] = 0;
+  }
+  for (int t = t0; t < t1; ++t) {
+    float v[8];
+    token_probs(logits + (size_t)t * N, N, softmax, lane, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) P[i] += v[i];
+    for (int j = 0; j < k; ++j) {
+      const int e = topk_idx[(size_t)t * k + j];
+      if ((unsigned)e >= (unsigned)N) {
+        if (lane == 0) set_status(status, MOE_ERR_BOUNDS);
+        continue;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) n[i] += (e == lane + 32 * i);
+    }
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc += (float)n[i] * P[i];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    const float Ls = (float)(t1 - t0);
+    seq_loss[seq] = (float)N * (acc / (Ls * (float)k)) / Ls;
+  }
+}
+
 // Router z-loss: per token log Z = m + log sum exp(z - m) (one warp per token),
 // squared and summed per 32-token chunk; one CTA adds the chunks in order.
 __global__ void __launch_bounds__(256) zloss_partial_kernel(const float *__restrict__ logits, int T, int N,
@@ -156,6 +253,8 @@ __global__ void __launch_bounds__(256) zloss_partial_kernel(const float *__restr
   }
 }
 
+// Sum of partial[0 .. nchunks) in a fixed order, divided by T: the mean of the
+// z-loss over tokens, or of the sequence losses over sequences.
 __global__ void __launch_bounds__(1024) zloss_final_kernel(const float *__restrict__ partial, int nchunks, int T,
                                                            float *__restrict__ z_loss) {
   __shared__ float red[1024];
@@ -198,8 +297,29 @@ int launch_load_stats(const float *logits, const int32_t *counts_routed, const i
                       long long total, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s) {
   if (T == 0) return MOE_OK;
   const int nchunks = (T + SC - 1) / SC;
-  stats_partial_kernel<<<nchunks, 256, 0, s>>>(logits, T, N, gate, partial);
+  stats_partial_kernel<<<nchunks, 256, 0, s>>>(logits, T, N, gate, T, nchunks, partial);
   stats_final_kernel<<<1, 1024, 0, s>>>(partial, nchunks, counts_routed, counts_kept, T, N, total, f, P, summary);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int seq_balance_chunks(int T, int L) {
+  L = min(L, T);
+  return (int)(((long long)T + L - 1) / L) * ((L + SC - 1) / SC);
+}
+
+int launch_seq_balance_loss(const float *logits, const int32_t *topk_idx, int T, int N, int k, int gate, int L,
+                            float *partial, float *seq_loss, float *loss, int *status, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  L = min(L, T);
+  const int nseq = (int)(((long long)T + L - 1) / L);
+  if (L >= SC) {
+    const int cps = (L + SC - 1) / SC;
+    stats_partial_kernel<<<nseq * cps, 256, 0, s>>>(logits, T, N, gate, L, cps, partial);
+    seq_final_kernel<<<nseq, 256, 0, s>>>(partial, cps, topk_idx, T, N, k, L, seq_loss, status);
+  } else {
+    seq_short_kernel<<<(nseq + 7) / 8, 256, 0, s>>>(logits, topk_idx, T, N, k, gate, L, nseq, seq_loss, status);
+  }
+  zloss_final_kernel<<<1, 1024, 0, s>>>(seq_loss, nseq, nseq, loss);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

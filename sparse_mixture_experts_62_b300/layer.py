@@ -11,7 +11,7 @@ from typing import Optional
 import torch
 
 from . import (DTYPE_BF16, MoeConfig, moe_get_device_status, moe_layer_forward, moe_load_stats,
-               moe_workspace_layout, moe_workspace_size)
+               moe_seq_balance_loss, moe_workspace_layout, moe_workspace_size)
 
 
 class MoELayer:
@@ -50,6 +50,13 @@ class MoELayer:
         summary = self._stats[2 * c.N:2 * c.N + 3]
         moe_load_stats(c, v["logits"], v["counts_routed"], v["counts_kept"], f, P, summary, self.ws, stream)
         return f, P, summary
+
+    def seq_balance_loss(self, seq_len: int, stream=None) -> torch.Tensor:
+        """Sequence-wise balance loss of the last forward (token choice), a device scalar."""
+        v = self.views()
+        out = self._stats[2 * self.cfg.N + 3:2 * self.cfg.N + 4]
+        moe_seq_balance_loss(self.cfg, v["logits"], v["topk_idx"], seq_len, out, self.ws, stream)
+        return out
 
     def device_status(self, stream=None) -> int:
         return moe_get_device_status(self.ws, stream)

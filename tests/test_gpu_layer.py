@@ -4,7 +4,8 @@ Small layers are compared on every output; the full-size workloads (the
 Mixtral-shaped prefill and decode layers, the DeepSeek-V3-shaped and the
 Qwen3-shaped layers) are run in the launch configuration the benchmark times,
 with routing, dispatch and statistics compared on all tokens and the layer
-output on all tokens or on a seeded sample of them.
+output on all tokens or on a seeded sample of them.  The oracle routes on its
+own; the rules for the rare token the two route differently are in parity.py.
 """
 import numpy as np
 import pytest
@@ -12,7 +13,7 @@ import torch
 
 import oracle
 import synth
-from parity import assert_close_out, check_dispatch, check_routing, layer_on_device, to_dev, to_np_f64
+from parity import assert_close_out, check_layer_dispatch, check_routing, layer_on_device, to_dev, to_np_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -30,23 +31,33 @@ def run_and_check(inp, sample=None):
     idx = v["topk_idx"].cpu().numpy()
     w = v["topk_w"].cpu().numpy().astype(np.float64)
     tokens = None if sample is None else np.sort(np.random.default_rng(wl.seed).choice(wl.T, sample, replace=False))
-    ref = oracle.layer_forward(inp, tokens=tokens, idx_override=idx)
-    ref_own = oracle.layer_forward(inp, tokens=np.array([], dtype=np.int64))  # the oracle's own routing
-    near = check_routing(inp, z, idx, w, ref_own)
+    ref = oracle.layer_forward(inp, tokens=tokens)  # the oracle's own routing, from the inputs alone
+    same = check_routing(inp, z, idx, w, ref)
     cap = layer.cfg.capacity
-    check_dispatch(wl, idx, v["counts_routed"].cpu().numpy(), v["counts_kept"].cpu().numpy(),
-                   v["offsets"].cpu().numpy(), v["dest_row"].cpu().numpy(), v["src_token"].cpu().numpy(), cap)
+    agree = check_layer_dispatch(wl, idx, same, v["counts_routed"].cpu().numpy(), v["counts_kept"].cpu().numpy(),
+                                 v["offsets"].cpu().numpy(), v["dest_row"].cpu().numpy(),
+                                 v["src_token"].cpu().numpy(), cap, ref)
     got = to_np_f64(out)
     rows = np.arange(wl.T) if tokens is None else tokens
+    rows = rows[agree[rows]]
     err, tol = assert_close_out(got[rows], ref.out[rows], wl.dtype)
-    # statistics
-    assert np.array_equal(f.cpu().numpy(), ref.stats.f.astype(np.float32))
+    # statistics: exact where no differing token touches an expert
+    fg = f.cpu().numpy()
+    if np.all(same):
+        assert np.array_equal(fg, ref.stats.f.astype(np.float32))
+    assert np.max(np.abs(fg - ref.stats.f)) <= 2.0 * np.sum(~same) / (wl.T * wl.k) + 1e-7
     assert np.max(np.abs(P.cpu().numpy() - ref.stats.P)) < 1e-5
     s = summ.cpu().numpy().astype(np.float64)
-    assert s[0] == pytest.approx(ref.stats.aux, rel=1e-5)
-    assert s[1] == pytest.approx(ref.stats.imbalance, rel=1e-6)
-    assert s[2] == pytest.approx(ref.stats.drop_rate, rel=1e-6, abs=1e-7)
-    return dict(err=err, tol=tol, near_ties=near, kept=int(v["offsets"][-1]))
+    exact = bool(np.all(same))
+    assert s[0] == pytest.approx(ref.stats.aux, rel=1e-5 if exact else 1e-3)
+    assert s[1] == pytest.approx(ref.stats.imbalance, rel=1e-6 if exact else 1e-2)
+    assert s[2] == pytest.approx(ref.stats.drop_rate, rel=1e-6 if exact else 1e-2, abs=1e-7 if exact else 1e-3)
+    # sequence-wise balance loss over sequences of a quarter of the batch
+    L = max(1, wl.T // 4)
+    sbl = float(layer.seq_balance_loss(L).item())
+    sref = oracle.sequence_balance_loss(ref.z, ref.idx, wl.gate, L)
+    assert sbl == pytest.approx(sref, rel=1e-5 if exact else 1e-3)
+    return dict(err=err, tol=tol, differing=int(np.sum(~same)), kept=int(v["offsets"][-1]))
 
 
 SMALL = [

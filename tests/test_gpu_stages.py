@@ -1,7 +1,8 @@
 """Per-stage parity of the CUDA path against the oracle (B300).
 
-Each stage gets the GPU's own upstream outputs, so integer stages compare
-exactly and float stages compare within the stated tolerance.
+Each stage gets the same host-made inputs on both sides (never an output of
+the GPU), so integer stages compare exactly and float stages compare within the
+stated tolerance.
 """
 import numpy as np
 import pytest
@@ -242,3 +243,50 @@ def test_bias_update_parity():
     moe.moe_bias_update(cfg, torch.from_numpy(counts).cuda(), bd, gamma)
     ref = oracle.bias_update(b, counts.astype(np.int64), T, k, gamma)
     assert np.array_equal(bd.cpu().numpy(), ref)
+
+
+def _skewed_topk(rng, T, N, k):
+    """Distinct experts per token, drawn with Zipf-like preferences (host-made input)."""
+    keys = np.log(1.0 / np.arange(1, N + 1) ** 1.1)[None, :] + rng.gumbel(size=(T, N))
+    return np.argsort(-keys, axis=1, kind="stable")[:, :k].astype(np.int32)
+
+
+@pytest.mark.parametrize("gate,T,N,k,seq_lens", [
+    ("softmax", 1000, 8, 2, [1, 5, 31, 32, 33, 100, 256, 999, 1000, 5000]),
+    ("sigmoid", 777, 256, 8, [1, 7, 32, 64, 300, 777]),
+    ("softmax_full", 4096, 128, 8, [4096, 1024, 96, 3]),
+    ("softmax", 1, 4, 2, [1, 8]),
+])
+def test_seq_balance_loss_parity(gate, T, N, k, seq_lens):
+    rng = np.random.default_rng(T + N + k)
+    z = (rng.standard_normal((T, N)) * 1.5).astype(np.float32)
+    idx = _skewed_topk(rng, T, N, k)
+    g = {"softmax": moe.GATE_SOFTMAX_TOPK, "sigmoid": moe.GATE_SIGMOID_BIAS, "softmax_full": moe.GATE_SOFTMAX_FULL}
+    cfg = moe.make_config(T, 64, N, k, 64, 0, g[gate])
+    ws = _ws(cfg)
+    zd, idd = torch.from_numpy(z).cuda(), torch.from_numpy(idx).cuda()
+    out = torch.full((1,), float("nan"), device="cuda")
+    for L in seq_lens:
+        moe.moe_seq_balance_loss(cfg, zd, idd, L, out, ws)
+        ref = oracle.sequence_balance_loss(z, idx, "sigmoid" if gate == "sigmoid" else "softmax", L)
+        got = float(out.item())
+        assert abs(got - ref) <= 1e-5 * abs(ref) + 1e-7, (L, got, ref)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    # deterministic
+    moe.moe_seq_balance_loss(cfg, zd, idd, seq_lens[0], out, ws)
+    a = out.clone()
+    moe.moe_seq_balance_loss(cfg, zd, idd, seq_lens[0], out, ws)
+    assert torch.equal(a, out)
+
+
+def test_seq_balance_loss_flags_bad_indices():
+    T, N, k = 100, 8, 2
+    z = np.zeros((T, N), np.float32)
+    idx = np.tile(np.array([[0, 1]], np.int32), (T, 1))
+    idx[40, 1] = 8  # out of range
+    cfg = moe.make_config(T, 64, N, k, 64)
+    ws = _ws(cfg)
+    out = torch.zeros(1, device="cuda")
+    for L in (10, 50):
+        moe.moe_seq_balance_loss(cfg, torch.from_numpy(z).cuda(), torch.from_numpy(idx).cuda(), L, out, ws)
+        assert moe.moe_get_device_status(ws) == moe.MOE_ERR_BOUNDS
