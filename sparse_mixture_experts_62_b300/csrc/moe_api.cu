@@ -209,9 +209,8 @@ int ec_route(const moe_config *c, const Ws &w, const void *x, const float *Wg, c
 
 // ---------------------------------------------------------------- backward workspace
 struct BwdLayout {
-  size_t dgate, dz, koff, koff_sh, off_sh, dy, dh, a, u, dA, dxp, w2t, w13t, dyT, hT, dAT, xT;
-  size_t dh_s, a_s, u_s, dA_s, dx_s, sw2t, sw13t, doutT, hsT, dAsT, xTs, total;
-  int64_t rp, tp;
+  size_t dgate, dz, off_sh, dy, dh, a, u, dA, dxp;
+  size_t dh_s, a_s, u_s, dA_s, dx_s, total;
 };
 
 BwdLayout bwd_layout(const moe_config *c) {
@@ -220,9 +219,6 @@ BwdLayout bwd_layout(const moe_config *c) {
   const size_t R = (size_t)c->T * c->k;
   const bool sw = c->act == MOE_ACT_SWIGLU;
   const size_t FA = sw ? 2 * F : F, FAs = sw ? 2 * Fs : Fs;  // width of dA
-  L.rp = (int64_t)(R + 64 * N);
-  L.rp = (L.rp + 63) / 64 * 64;
-  L.tp = (int64_t)((T + 63) / 64 * 64);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -231,8 +227,6 @@ BwdLayout bwd_layout(const moe_config *c) {
   };
   L.dgate = take(T * k * 4);
   L.dz = take(T * N * 4);
-  L.koff = take((N + 1) * 4);
-  L.koff_sh = take(2 * 4);
   L.off_sh = take(2 * 4);
   L.dy = take(R * d * 2);
   L.dh = take(R * F * 2);
@@ -240,24 +234,12 @@ BwdLayout bwd_layout(const moe_config *c) {
   L.u = take(sw ? R * F * 2 : 0);
   L.dA = take(R * FA * 2);
   L.dxp = take(R * d * 2);
-  L.w2t = take(N * F * d * 2);
-  L.w13t = take(N * d * FA * 2);
-  L.dyT = take(d * L.rp * 2);
-  L.hT = take(F * L.rp * 2);
-  L.dAT = take(FA * L.rp * 2);
-  L.xT = take(d * L.rp * 2);
   if (Fs) {
     L.dh_s = take(T * Fs * 2);
     L.a_s = take(T * Fs * 2);
     L.u_s = take(sw ? T * Fs * 2 : 0);
     L.dA_s = take(T * FAs * 2);
     L.dx_s = take(T * d * 2);
-    L.sw2t = take(Fs * d * 2);
-    L.sw13t = take(d * FAs * 2);
-    L.doutT = take(d * L.tp * 2);
-    L.hsT = take(Fs * L.tp * 2);
-    L.dAsT = take(FAs * L.tp * 2);
-    L.xTs = take(d * L.tp * 2);
   }
   L.total = o;
   return L;
@@ -280,32 +262,25 @@ int ffn_backward(const moe_config *c, bool shared, int G, int64_t R, const int32
   const bool pair = use_pair_tiles(R, G, shared ? 0 : c->capacity);
   auto B = [&](size_t off) { return bws + off; };
   void *dh = B(shared ? L.dh_s : L.dh), *a = B(shared ? L.a_s : L.a), *u = B(shared ? L.u_s : L.u);
-  void *dA = B(shared ? L.dA_s : L.dA), *w2t = B(shared ? L.sw2t : L.w2t), *w13t = B(shared ? L.sw13t : L.w13t);
+  void *dA = B(shared ? L.dA_s : L.dA);
   const int M = shared ? c->T : 0;
-  // dh = dy W2: B = W2 transposed per expert to [F, d]
-  MOE_TRY(launch_transpose_weights(w2, G, d, F, d, 0, w2t, s));
-  MOE_TRY(tc_grouped_gemm(2, dy, R, d, w2t, nullptr, (int64_t)G * F, F, offsets, G, M, F, dh, status, pair, s));
+  // dh = dy W2, W2 read in place as [G][d][F]
+  MOE_TRY(tc_grouped_gemm_bt(dy, nullptr, R, d, d, 0, w2, nullptr, G, F, offsets, M, dh, status, pair, s));
   // recompute a = x W1^T (and u = x W3^T); then dA = [da | du]
   MOE_TRY(tc_grouped_gemm(2, xrows, R, d, w1, nullptr, (int64_t)G * F, F, offsets, G, M, F, a, status, pair, s));
   if (sw) MOE_TRY(tc_grouped_gemm(2, xrows, R, d, w3, nullptr, (int64_t)G * F, F, offsets, G, M, F, u, status, pair, s));
   MOE_TRY(launch_act_bwd(a, sw ? u : nullptr, dh, off_dev + G, R, F, sw, dA, s));
-  // dx rows = [da | du] [W1 | W3]: B = [W1^T | W3^T] per expert ([d, 2F])
-  MOE_TRY(launch_transpose_weights(w1, G, F, d, FA, 0, w13t, s));
-  if (sw) MOE_TRY(launch_transpose_weights(w3, G, F, d, FA, F, w13t, s));
-  MOE_TRY(tc_grouped_gemm(2, dA, R, FA, w13t, nullptr, (int64_t)G * d, d, offsets, G, M, d, dxrows, status, pair, s));
-  // weight gradients: sums over each expert's rows of transposed, 64-padded activations
-  int32_t *koff = reinterpret_cast<int32_t *>(B(shared ? L.koff_sh : L.koff));
-  const int64_t kp = shared ? L.tp : L.rp;
-  void *dyT = B(shared ? L.doutT : L.dyT), *hT = B(shared ? L.hsT : L.hT), *dAT = B(shared ? L.dAsT : L.dAT);
-  void *xT = B(shared ? L.xTs : L.xT);
-  MOE_TRY(launch_wgrad_koff(off_dev, G, koff, s));
-  MOE_TRY(launch_transpose_rows(dy, d, off_dev, koff, G, kp, dyT, s));
-  MOE_TRY(launch_transpose_rows(h, F, off_dev, koff, G, kp, hT, s));
-  MOE_TRY(launch_transpose_rows(dA, FA, off_dev, koff, G, kp, dAT, s));
-  MOE_TRY(launch_transpose_rows(xrows, d, off_dev, koff, G, kp, xT, s));
-  MOE_TRY(tc_wgrad_gemm(dyT, hT, koff, G, d, F, kp, dw2, status, s));
-  MOE_TRY(tc_wgrad_gemm(dAT, xT, koff, G, F, d, kp, dw1, status, s));
-  if (sw) MOE_TRY(tc_wgrad_gemm(static_cast<uint8_t *>(dAT) + (size_t)F * kp * 2, xT, koff, G, F, d, kp, dw3, status, s));
+  // dx rows = da W1 + du W3, W1 and W3 read in place as [G][F][d]
+  MOE_TRY(tc_grouped_gemm_bt(dA, sw ? static_cast<uint8_t *>(dA) + (size_t)F * 2 : nullptr, R, FA, F, F, w1,
+                             sw ? w3 : nullptr, G, d, offsets, M, dxrows, status, pair, s));
+  // weight gradients: sums over each expert's rows, the activations read in place
+  const int64_t rows = shared ? (int64_t)c->T : R;
+  const int32_t *goff = shared ? nullptr : off_dev;
+  MOE_TRY(tc_wgrad_gemm(dy, d, h, F, rows, goff, G, d, F, dw2, status, s));
+  MOE_TRY(tc_wgrad_gemm(dA, FA, xrows, d, rows, goff, G, F, d, dw1, status, s));
+  if (sw)
+    MOE_TRY(tc_wgrad_gemm(static_cast<uint8_t *>(dA) + (size_t)F * 2, FA, xrows, d, rows, goff, G, F, d, dw3, status,
+                          s));
   return MOE_OK;
 }
 

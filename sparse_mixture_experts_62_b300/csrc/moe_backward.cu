@@ -1,5 +1,5 @@
-// Backward pass of the layer with the routing held fixed: the element-wise,
-// transposition and router kernels around the tensor-core GEMMs.
+// Backward pass of the layer with the routing held fixed: the element-wise and
+// router kernels around the tensor-core GEMMs.
 //
 // "Chapter 19: MoE", 19.6.2: the top-k choice is discrete, so the task gradient
 // reaches the router only through the gate weights of the chosen experts and
@@ -17,94 +17,6 @@
 
 namespace moe {
 namespace {
-
-// koff[e] = column offset of expert e in the transposed, 64-padded activations
-__global__ void wgrad_koff_kernel(const int32_t *__restrict__ offsets, int N, int32_t *__restrict__ koff) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  int acc = 0;
-  for (int e = 0; e < N; ++e) {
-    koff[e] = acc;
-    const int r = offsets[e + 1] - offsets[e];
-    acc += (r + 63) / 64 * 64;
-  }
-  koff[N] = acc;
-}
-
-// 64 x 64 bf16 tiles through shared memory with 16-byte global loads and stores
-// (every dimension is a multiple of 8 elements, so an 8-element vector is
-// either wholly inside or wholly outside the matrix).  The tile is read as 64
-// source rows of 8 vectors and written as 64 output rows of 8 vectors.
-constexpr int TT = 64, TPAD = 8;
-
-__device__ __forceinline__ void tile_store_transposed(uint16_t (*tile)[TT + TPAD], uint16_t *out, size_t out_stride,
-                                                      int orow0, int ocol0, int orows, int ocols) {
-  for (int v = threadIdx.x; v < TT * (TT / 8); v += blockDim.x) {
-    const int orow = v / (TT / 8), oc = (v % (TT / 8)) * 8;
-    if (orow0 + orow >= orows || ocol0 + oc >= ocols) continue;
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-      w[q] = (uint32_t)tile[oc + 2 * q][orow] | ((uint32_t)tile[oc + 2 * q + 1][orow] << 16);
-    *reinterpret_cast<uint4 *>(out + (size_t)(orow0 + orow) * out_stride + ocol0 + oc) =
-        make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
-// XT[c][koff[e] + i] = X[offsets[e] + i][c] for i < rows of e, 0 in the padding;
-// the group of a padded column is found by binary search over koff.
-__global__ void __launch_bounds__(256) transpose_rows_kernel(const uint16_t *__restrict__ X, int C,
-                                                             const int32_t *__restrict__ offsets,
-                                                             const int32_t *__restrict__ koff, int N, int64_t kp,
-                                                             uint16_t *__restrict__ XT) {
-  __shared__ __align__(16) uint16_t tile[TT][TT + TPAD];
-  __shared__ int s_src[TT];
-  const int p0 = blockIdx.x * TT, c0 = blockIdx.y * TT;
-  const int kp_used = koff[N];
-  if (threadIdx.x < TT) {
-    const int p = p0 + threadIdx.x;
-    int src = -1;
-    if (p < kp_used) {
-      int lo = 0, hi = N;  // largest e with koff[e] <= p
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) / 2;
-        if (koff[mid] <= p) lo = mid;
-        else hi = mid;
-      }
-      const int i = p - koff[lo];
-      if (i < offsets[lo + 1] - offsets[lo]) src = offsets[lo] + i;
-    }
-    s_src[threadIdx.x] = src;
-  }
-  __syncthreads();
-  // tile[r][*] = source row of padded column p0 + r, columns c0 ..
-  for (int v = threadIdx.x; v < TT * (TT / 8); v += blockDim.x) {
-    const int r = v / (TT / 8), cc = (v % (TT / 8)) * 8;
-    const int src = s_src[r];
-    uint4 q = make_uint4(0u, 0u, 0u, 0u);
-    if (src >= 0 && c0 + cc < C) q = *reinterpret_cast<const uint4 *>(X + (size_t)src * C + c0 + cc);
-    *reinterpret_cast<uint4 *>(&tile[r][cc]) = q;
-  }
-  __syncthreads();
-  tile_store_transposed(tile, XT, (size_t)kp, c0, p0, C, (int)kp);
-}
-
-// WT[g][b][col_off + a] = W[g][a][b]; W is [G][A][B], WT rows have out_stride elements.
-__global__ void __launch_bounds__(256) transpose_weights_kernel(const uint16_t *__restrict__ W, int A, int B,
-                                                                int out_stride, int col_off,
-                                                                uint16_t *__restrict__ WT) {
-  __shared__ __align__(16) uint16_t tile[TT][TT + TPAD];
-  const int b0 = blockIdx.x * TT, a0 = blockIdx.y * TT, g = blockIdx.z;
-  const uint16_t *Wg = W + (size_t)g * A * B;
-  uint16_t *WTg = WT + (size_t)g * B * out_stride + col_off;
-  for (int v = threadIdx.x; v < TT * (TT / 8); v += blockDim.x) {
-    const int r = v / (TT / 8), cc = (v % (TT / 8)) * 8;
-    uint4 q = make_uint4(0u, 0u, 0u, 0u);
-    if (a0 + r < A && b0 + cc < B) q = *reinterpret_cast<const uint4 *>(Wg + (size_t)(a0 + r) * B + b0 + cc);
-    *reinterpret_cast<uint4 *>(&tile[r][cc]) = q;
-  }
-  __syncthreads();
-  tile_store_transposed(tile, WTg, (size_t)out_stride, b0, a0, B, A);
-}
 
 __global__ void zero_f32_kernel(float *p, size_t n) {
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) p[i] = 0.f;
@@ -271,26 +183,6 @@ inline int grid_for(size_t n, int per_block) {
 
 int launch_set_offsets2(int32_t *offsets, int rows, cudaStream_t s) {
   set_offsets2_kernel<<<1, 32, 0, s>>>(offsets, rows);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
-
-int launch_wgrad_koff(const int32_t *offsets, int N, int32_t *koff, cudaStream_t s) {
-  wgrad_koff_kernel<<<1, 32, 0, s>>>(offsets, N, koff);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
-
-int launch_transpose_rows(const void *X, int C, const int32_t *offsets, const int32_t *koff, int N, int64_t kp,
-                          void *XT, cudaStream_t s) {
-  dim3 grid((unsigned)((kp + TT - 1) / TT), (unsigned)((C + TT - 1) / TT));
-  transpose_rows_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(X), C, offsets, koff, N, kp,
-                                             static_cast<uint16_t *>(XT));
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
-
-int launch_transpose_weights(const void *W, int G, int A, int B, int out_stride, int col_off, void *WT, cudaStream_t s) {
-  dim3 grid((B + TT - 1) / TT, (A + TT - 1) / TT, G);
-  transpose_weights_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(W), A, B, out_stride, col_off,
-                                                static_cast<uint16_t *>(WT));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -66,18 +66,39 @@ MOE_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// The same with acquire semantics at cluster scope: for phases completed by
+// arrivals (release.cluster) from the other CTA of a pair.
+MOE_DEV bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase of `parity` to complete.  Returns false (and records
 // MOE_ERR_TIMEOUT) if it has not completed within limit_ns.
-MOE_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int *status, uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
+template <bool CLUSTER = false>
+MOE_DEV bool mbar_wait_t(uint64_t *bar, uint32_t parity, int *status, uint64_t limit_ns = kWaitLimitNs) {
+  auto probe = [&] { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (probe()) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (probe()) return true;
     if ((it & 63u) == 0 && global_ns() - t0 > limit_ns) {
       set_status(status, MOE_ERR_TIMEOUT);
       return false;
     }
   }
+}
+MOE_DEV bool mbar_wait(uint64_t *bar, uint32_t parity, int *status, uint64_t limit_ns = kWaitLimitNs) {
+  return mbar_wait_t<false>(bar, parity, status, limit_ns);
+}
+MOE_DEV bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, int *status, uint64_t limit_ns = kWaitLimitNs) {
+  return mbar_wait_t<true>(bar, parity, status, limit_ns);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -92,6 +113,14 @@ MOE_DEV void tma_load_2d(void *smem_dst, const CUtensorMap *m, uint64_t *bar, in
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::
           "r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+MOE_DEV void tma_load_3d(void *smem_dst, const CUtensorMap *m, uint64_t *bar, int32_t c0, int32_t c1, int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
 
@@ -115,12 +144,32 @@ MOE_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for an MN-major operand tile: TMA writes each 64-wide (128-byte) slice
+// of the M or N extent as a [K rows][128 B] block with the 128-byte swizzle, the
+// slices `mn_stride` bytes apart.  In the canonical MN-major layout the leading
+// byte offset is the stride between 64-element MN slices and the stride byte
+// offset the distance between 8-row K groups (8 rows x 128 B = 1024 B).  A K step
+// of 16 rows is +2048 bytes of start address.
+MOE_DEV uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
 // Instruction descriptor for tcgen05.mma kind::f16 with bf16 A and B (both
 // K-major), float32 accumulator, shape M x N:
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format
 //   (1 = bf16); 15/16 A/B major (0 = K); 17-22 N >> 3; 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// ... with A and/or B MN-major (bits 15 / 16 set).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_major(int M, int N, bool a_mn, bool b_mn) {
+  return idesc_bf16_f32(M, N) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
 }
 
 MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -197,6 +246,14 @@ MOE_DEV void tma_load_2d_pair(void *smem_dst, const CUtensorMap *m, uint32_t mba
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::
           "r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(mbar_caddr), "r"(c0), "r"(c1)
+      : "memory");
+}
+MOE_DEV void tma_load_3d_pair(void *smem_dst, const CUtensorMap *m, uint32_t mbar_caddr, int32_t c0, int32_t c1,
+                              int32_t c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(mbar_caddr), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
 // D (+)= A * B^T over a CTA pair: A rows 0..127 and B rows 0..N/2-1 come from

@@ -18,6 +18,11 @@
 //            writes SiLU(a) * u as bf16, 128 output columns per tile.
 //   kReLU:   one map; 256 output columns per tile; epilogue max(acc, 0) -> bf16.
 //   kPlain:  one map; 256 output columns per tile; epilogue acc -> bf16.
+//   kPlainBT: B_g stored the other way round, [K, n_out] per group (the stacked
+//            weights read in place as [G][K][n_out] through a 3-D map, MN-major
+//            tiles); epilogue as kPlain.  dh = dy W2 in the backward.
+//   kDualBT: two (A, B) pairs concatenated along K, both B's as in kPlainBT:
+//            out = A1 B1 + A2 B2.  dx rows = da W1 + du W3 in the backward.
 //
 // Kernel shape (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer (one lane): 4-stage ring of {A 128x64, B 256x64}.
@@ -51,7 +56,9 @@ constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_
                               (size_t)(4 * MAX_GROUPS + 8) * 4;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
-enum Mode { kSwiGLU = 0, kReLU = 1, kPlain = 2 };
+enum Mode { kSwiGLU = 0, kReLU = 1, kPlain = 2, kPlainBT = 3, kDualBT = 4 };
+constexpr uint32_t IDESC_BT = idesc_bf16_f32_major(BM, BN, false, true);
+constexpr int B_SLICE = BK * 64 * 2;  // one MN-major B slice: 64 K rows x 64 columns = 8 KB
 
 struct Args {
   const int32_t *offsets;  // [G + 1] group row offsets in A / out, or nullptr: one group of M rows
@@ -63,14 +70,17 @@ struct Args {
   int32_t b_rows;      // weight-view rows per group
   uint16_t *out;       // [rows, n_out] bf16
   int *status;
+  int32_t num_kb;      // K blocks per tile
+  int32_t kb1;         // kDualBT: K blocks taken from the first (A, B) pair
 };
 
 __device__ __forceinline__ float silu(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                        const __grid_constant__ CUtensorMap tmB1, const Args args) {
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                        const Args args) {
   constexpr int OUT_COLS = (MODE == kSwiGLU) ? 128 : 256;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles
@@ -90,7 +100,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int lane = threadIdx.x & 31;
   const int G = args.G;
   const int n_tiles = (args.n_out + OUT_COLS - 1) / OUT_COLS;
-  const int num_kb = (args.K + BK - 1) / BK;
+  const int num_kb = args.num_kb;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -122,7 +132,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
-    if (MODE == kSwiGLU) tma_prefetch_desc(&tmB1);
+    if (MODE == kSwiGLU || MODE == kDualBT) tma_prefetch_desc(&tmB1);
+    if (MODE == kDualBT) tma_prefetch_desc(&tmA2);
   }
   if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
   tc_fence_before();
@@ -155,11 +166,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint8_t *sa = smem + stage * STAGE_BYTES;
           uint8_t *sb = sa + A_BYTES;
           mbar_arrive_expect_tx(&full[stage], STAGE_TX);
-          tma_load_2d(sa, &tmA, &full[stage], kb * BK, a_row);
-          if (MODE == kSwiGLU) {
+          if (MODE == kPlainBT || MODE == kDualBT) {
+            const bool second = MODE == kDualBT && kb >= args.kb1;
+            const int k0 = (second ? kb - args.kb1 : kb) * BK;
+            const CUtensorMap *mb = second ? &tmB1 : &tmB0;
+            tma_load_2d(sa, second ? &tmA2 : &tmA, &full[stage], k0, a_row);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j)
+              tma_load_3d(sb + j * B_SLICE, mb, &full[stage], n_tile * OUT_COLS + 64 * j, k0, g);
+          } else if (MODE == kSwiGLU) {
+            tma_load_2d(sa, &tmA, &full[stage], kb * BK, a_row);
             tma_load_2d(sb, &tmB0, &full[stage], kb * BK, b_row);
             tma_load_2d(sb + B_BYTES / 2, &tmB1, &full[stage], kb * BK, b_row);
           } else {
+            tma_load_2d(sa, &tmA, &full[stage], kb * BK, a_row);
             tma_load_2d(sb, &tmB0, &full[stage], kb * BK, b_row);
             tma_load_2d(sb + B_BYTES / 2, &tmB0, &full[stage], kb * BK, b_row + BN / 2);
           }
@@ -195,11 +215,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint64_t adesc = smem_desc_sw128(sa);
-          const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
+          if (MODE == kPlainBT || MODE == kDualBT) {
+            const uint64_t bdesc = smem_desc_sw128_mn(sa + A_BYTES, B_SLICE);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
-            tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, IDESC, (kb | kk) != 0);
+            for (int kk = 0; kk < BK / 16; ++kk)  // A: +32 B along K; B: +16 rows = +2048 B
+              tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 128ull * kk, IDESC_BT, (kb | kk) != 0);
+          } else {
+            const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
+              tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, IDESC, (kb | kk) != 0);
+            }
           }
           tc_commit(&empty[stage]);
           if (++stage == STAGES) {
@@ -307,12 +334,14 @@ constexpr int BH_BYTES = 128 * BK * 2;           // 16 KB: this CTA's half of B
 constexpr int STAGE_BYTES = A_BYTES + BH_BYTES;  // 32 KB
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + (size_t)(4 * MAX_GROUPS + 8) * 4;
 constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
+constexpr uint32_t IDESC_BT = idesc_bf16_f32_major(2 * BM, BN, false, true);
 }  // namespace pair
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                             const __grid_constant__ CUtensorMap tmB1, const Args args) {
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                             const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                             const Args args) {
   constexpr int STAGES = pair::STAGES, STAGE_BYTES = pair::STAGE_BYTES, A_BYTES = pair::A_BYTES;
   constexpr int BM = pair::BM;
   constexpr uint32_t IDESC = pair::IDESC;
@@ -337,7 +366,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int pair_id = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int G = args.G;
   const int n_tiles = (args.n_out + OUT_COLS - 1) / OUT_COLS;
-  const int num_kb = (args.K + BK - 1) / BK;
+  const int num_kb = args.num_kb;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -369,7 +398,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
-    if (MODE == kSwiGLU) tma_prefetch_desc(&tmB1);
+    if (MODE == kSwiGLU || MODE == kDualBT) tma_prefetch_desc(&tmB1);
+    if (MODE == kDualBT) tma_prefetch_desc(&tmA2);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, TMEM_COLS);
   tc_fence_before();
@@ -407,8 +437,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint8_t *sa = smem + stage * STAGE_BYTES;
           if (leader) mbar_arrive_expect_tx(&full[stage], 2u * STAGE_BYTES);
           const uint32_t fb = full_lead + 8u * stage;
-          tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row);
-          tma_load_2d_pair(sa + A_BYTES, mb, fb, kb * BK, b_row);
+          if (MODE == kPlainBT || MODE == kDualBT) {
+            const bool second = MODE == kDualBT && kb >= args.kb1;
+            const int k0 = (second ? kb - args.kb1 : kb) * BK;
+            const CUtensorMap *mbt = second ? &tmB1 : &tmB0;
+            tma_load_2d_pair(sa, second ? &tmA2 : &tmA, fb, k0, a_row);
+            const int nb = n_tile * OUT_COLS + (int)rank * 128;  // this CTA's half of the tile's columns
+#pragma unroll
+            for (int j = 0; j < 2; ++j) tma_load_3d_pair(sa + A_BYTES + j * B_SLICE, mbt, fb, nb + 64 * j, k0, g);
+          } else {
+            tma_load_2d_pair(sa, &tmA, fb, kb * BK, a_row);
+            tma_load_2d_pair(sa + A_BYTES, mb, fb, kb * BK, b_row);
+          }
           issued_parity[stage] = (int)phase;
           if (++stage == STAGES) {
             stage = 0;
@@ -431,7 +471,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int tile = pair_id; tile < total_tiles && ok; tile += npairs, ++it) {
         const int acc = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
-        if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, args.status)) break;
+        if (!mbar_wait_cluster(&tempty[acc], (use & 1u) ^ 1u, args.status)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
@@ -442,10 +482,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint64_t adesc = smem_desc_sw128(sa);
-          const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
+          if (MODE == kPlainBT || MODE == kDualBT) {
+            const uint64_t bdesc = smem_desc_sw128_mn(sa + A_BYTES, B_SLICE);
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc_mma_bf16_pair(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, IDESC, (kb | kk) != 0);
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc_mma_bf16_pair(d_tmem, adesc + 2ull * kk, bdesc + 128ull * kk, pair::IDESC_BT, (kb | kk) != 0);
+          } else {
+            const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk)
+              tc_mma_bf16_pair(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, IDESC, (kb | kk) != 0);
+          }
           tc_commit_pair(&empty[stage], 0x3);
           if (++stage == STAGES) {
             stage = 0;
@@ -551,17 +598,36 @@ static EncodeTiledFn get_encode() {
   return fn;
 }
 
-// 2-D bf16 map over a [rows, cols] row-major matrix, box 64 (cols) x 128 (rows),
-// 128-byte swizzle; out-of-range elements read as zero.
-static int make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+// 2-D bf16 map over a [rows, cols] row-major matrix (row stride `stride`
+// elements, default cols), box 64 (cols) x 128 (rows), 128-byte swizzle;
+// out-of-range elements read as zero.
+static int make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint64_t stride = 0) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return MOE_ERR_CUDA;
-  if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16 || rows == 0 || cols == 0) return MOE_ERR_UNSUPPORTED;
+  if (!stride) stride = cols;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (stride * 2) % 16 || rows == 0 || cols == 0 || stride < cols)
+    return MOE_ERR_UNSUPPORTED;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {stride * 2};
   cuuint32_t box[2] = {BK, BM};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// 3-D bf16 map over G stacked [k, n] row-major matrices, box 64 (n) x 64 (k) x 1,
+// 128-byte swizzle: one MN-major B slice.  Reads past k or n of a matrix are zero.
+static int make_map_3d(CUtensorMap *m, const void *base, uint64_t G, uint64_t k, uint64_t n) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return MOE_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (n * 2) % 16 || G == 0 || k == 0 || n == 0) return MOE_ERR_UNSUPPORTED;
+  cuuint64_t dims[3] = {n, k, G};
+  cuuint64_t strides[2] = {n * 2, n * k * 2};
+  cuuint32_t box[3] = {64, BK, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
@@ -598,8 +664,8 @@ static int pair_grid(int device) {
 }
 
 template <int MODE>
-static int launch_pair(const CUtensorMap &ma, const CUtensorMap &mb0, const CUtensorMap &mb1, const Args &args,
-                       int device, cudaStream_t stream) {
+static int launch_pair(const CUtensorMap &ma, const CUtensorMap &ma2, const CUtensorMap &mb0, const CUtensorMap &mb1,
+                       const Args &args, int device, cudaStream_t stream) {
   const int grid = pair_grid<MODE>(device);
   if (grid < 2) return MOE_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
@@ -614,7 +680,8 @@ static int launch_pair(const CUtensorMap &ma, const CUtensorMap &mb0, const CUte
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ma, mb0, mb1, args) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ma, ma2, mb0, mb1, args) != cudaSuccess)
+    return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
@@ -633,6 +700,36 @@ static int prepare_kernel(int device) {
   return MOE_OK;
 }
 
+template <int MODE>
+static int launch_single(const CUtensorMap &ma, const CUtensorMap &ma2, const CUtensorMap &mb0,
+                         const CUtensorMap &mb1, const Args &args, int device, int sms, cudaStream_t stream) {
+  int rc;
+  if ((rc = prepare_kernel<MODE>(device))) return rc;
+  grouped_gemm_kernel<MODE><<<dim3(sms), dim3(THREADS), SMEM_BYTES, stream>>>(ma, ma2, mb0, mb1, args);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+static int launch_mode(int mode, const CUtensorMap &ma, const CUtensorMap &ma2, const CUtensorMap &mb0,
+                       const CUtensorMap &mb1, const Args &args, int device, int sms, bool pair_tiles,
+                       cudaStream_t stream) {
+  if (pair_tiles) {
+    switch (mode) {
+      case kSwiGLU: return launch_pair<kSwiGLU>(ma, ma2, mb0, mb1, args, device, stream);
+      case kReLU: return launch_pair<kReLU>(ma, ma2, mb0, mb1, args, device, stream);
+      case kPlain: return launch_pair<kPlain>(ma, ma2, mb0, mb1, args, device, stream);
+      case kPlainBT: return launch_pair<kPlainBT>(ma, ma2, mb0, mb1, args, device, stream);
+      default: return launch_pair<kDualBT>(ma, ma2, mb0, mb1, args, device, stream);
+    }
+  }
+  switch (mode) {
+    case kSwiGLU: return launch_single<kSwiGLU>(ma, ma2, mb0, mb1, args, device, sms, stream);
+    case kReLU: return launch_single<kReLU>(ma, ma2, mb0, mb1, args, device, sms, stream);
+    case kPlain: return launch_single<kPlain>(ma, ma2, mb0, mb1, args, device, sms, stream);
+    case kPlainBT: return launch_single<kPlainBT>(ma, ma2, mb0, mb1, args, device, sms, stream);
+    default: return launch_single<kDualBT>(ma, ma2, mb0, mb1, args, device, sms, stream);
+  }
+}
+
 }  // namespace tc
 
 int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
@@ -642,7 +739,7 @@ int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *
   if (G < 1 || G > MAX_GROUPS || K < 1 || n_out < 1 || a_rows < 1 || b_rows_total < 1) return MOE_ERR_INVALID_ARG;
   if (a_rows > INT32_MAX || n_out > b_rows_per_group || (int64_t)G * b_rows_per_group > b_rows_total)
     return MOE_ERR_INVALID_ARG;
-  if (mode == kSwiGLU && !B1) return MOE_ERR_INVALID_ARG;
+  if (mode < kSwiGLU || mode > kPlain || (mode == kSwiGLU && !B1)) return MOE_ERR_INVALID_ARG;
   CUtensorMap ma, mb0, mb1;
   int rc;
   if ((rc = make_map(&ma, A, (uint64_t)a_rows, (uint64_t)K))) return rc;
@@ -656,30 +753,40 @@ int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   const int sms = device_sm_count(dev);
   if (sms <= 0) return MOE_ERR_CUDA;
-  Args args{offsets, G, M, (int32_t)a_rows, n_out, K, b_rows_per_group, static_cast<uint16_t *>(out), status};
-  if (pair_tiles) {
-    switch (mode) {
-      case kSwiGLU: return launch_pair<kSwiGLU>(ma, mb0, mb1, args, dev, stream);
-      case kReLU: return launch_pair<kReLU>(ma, mb0, mb1, args, dev, stream);
-      default: return launch_pair<kPlain>(ma, mb0, mb1, args, dev, stream);
-    }
+  const int num_kb = (K + BK - 1) / BK;
+  Args args{offsets, G, M, (int32_t)a_rows, n_out, K, b_rows_per_group, static_cast<uint16_t *>(out), status,
+            num_kb, num_kb};
+  return launch_mode(mode, ma, ma, mb0, mb1, args, dev, sms, pair_tiles, stream);
+}
+
+int tc_grouped_gemm_bt(const void *A, const void *A2, int64_t a_rows, int64_t a_stride, int K1, int K2,
+                       const void *B0, const void *B1, int G, int n_out, const int32_t *offsets, int M, void *out,
+                       int *status, bool pair_tiles, cudaStream_t stream) {
+  using namespace tc;
+  const bool dual = A2 != nullptr;
+  if (G < 1 || G > MAX_GROUPS || K1 < 1 || n_out < 1 || a_rows < 1 || a_rows > INT32_MAX || !A || !B0 || !out)
+    return MOE_ERR_INVALID_ARG;
+  if (dual && (K2 < 1 || !B1)) return MOE_ERR_INVALID_ARG;
+  if (a_stride < K1 || (dual && a_stride < K2)) return MOE_ERR_INVALID_ARG;
+  CUtensorMap ma, ma2, mb0, mb1;
+  int rc;
+  if ((rc = make_map(&ma, A, (uint64_t)a_rows, (uint64_t)K1, (uint64_t)a_stride))) return rc;
+  if ((rc = make_map_3d(&mb0, B0, (uint64_t)G, (uint64_t)K1, (uint64_t)n_out))) return rc;
+  if (dual) {
+    if ((rc = make_map(&ma2, A2, (uint64_t)a_rows, (uint64_t)K2, (uint64_t)a_stride))) return rc;
+    if ((rc = make_map_3d(&mb1, B1, (uint64_t)G, (uint64_t)K2, (uint64_t)n_out))) return rc;
+  } else {
+    ma2 = ma;
+    mb1 = mb0;
   }
-  dim3 grid(sms), block(THREADS);
-  switch (mode) {
-    case kSwiGLU:
-      if ((rc = prepare_kernel<kSwiGLU>(dev))) return rc;
-      grouped_gemm_kernel<kSwiGLU><<<grid, block, SMEM_BYTES, stream>>>(ma, mb0, mb1, args);
-      break;
-    case kReLU:
-      if ((rc = prepare_kernel<kReLU>(dev))) return rc;
-      grouped_gemm_kernel<kReLU><<<grid, block, SMEM_BYTES, stream>>>(ma, mb0, mb1, args);
-      break;
-    default:
-      if ((rc = prepare_kernel<kPlain>(dev))) return rc;
-      grouped_gemm_kernel<kPlain><<<grid, block, SMEM_BYTES, stream>>>(ma, mb0, mb1, args);
-      break;
-  }
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const int kb1 = (K1 + BK - 1) / BK;
+  const int num_kb = kb1 + (dual ? (K2 + BK - 1) / BK : 0);
+  Args args{offsets, G, M, (int32_t)a_rows, n_out, K1, 0, static_cast<uint16_t *>(out), status, num_kb, kb1};
+  return launch_mode(dual ? kDualBT : kPlainBT, ma, ma2, mb0, mb1, args, dev, sms, pair_tiles, stream);
 }
 
 }  // namespace moe

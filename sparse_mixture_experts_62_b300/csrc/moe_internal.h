@@ -36,6 +36,13 @@ int launch_gather_rows(const void *x, const int32_t *src_token, const int32_t *o
 int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
                     int64_t b_rows_total, int b_rows_per_group, const int32_t *offsets, int G, int M, int n_out,
                     void *out, int *status, bool pair_tiles, cudaStream_t stream);
+// The same GEMM with each group's B stored [K, n_out] (the stacked weights read in
+// place, MN-major tiles): out = A[:, :K1] B0_g, or with A2 (dual) out = A B0_g +
+// A2 B1_g where A2 is a second [a_rows, K2] view with the same row stride.
+// A rows are a_stride elements apart; B0/B1 are [G][K][n_out] bf16.  Plain epilogue.
+int tc_grouped_gemm_bt(const void *A, const void *A2, int64_t a_rows, int64_t a_stride, int K1, int K2,
+                       const void *B0, const void *B1, int G, int n_out, const int32_t *offsets, int M, void *out,
+                       int *status, bool pair_tiles, cudaStream_t stream);
 // Tile choice for expert groups: pairs when the mean group holds >= 512 rows and no
 // capacity limit can skew the groups.
 inline bool use_pair_tiles(int64_t rows, int groups, int capacity) {
@@ -53,12 +60,11 @@ int launch_router_sum(const float *partial, int S, int pstride, const float *log
 // counts_routed = counts_kept = C for every expert (expert choice)
 int launch_fill_counts(int32_t *counts_routed, int32_t *counts_kept, int N, int C, cudaStream_t s);
 // backward pieces
-int tc_wgrad_gemm(const void *AT, const void *BT, const int32_t *koff, int G, int M, int Nn, int64_t kp, float *out,
-                  int *status, cudaStream_t stream);
-int launch_wgrad_koff(const int32_t *offsets, int N, int32_t *koff, cudaStream_t s);
-int launch_transpose_rows(const void *X, int C, const int32_t *offsets, const int32_t *koff, int N, int64_t kp,
-                          void *XT, cudaStream_t s);
-int launch_transpose_weights(const void *W, int G, int A, int B, int out_stride, int col_off, void *WT, cudaStream_t s);
+// out[g][m][n] = sum over rows r of group g of A[r][m] B[r][n] (tcgen05, float32
+// out); A [rows, M] and B [rows, Nn] bf16 row-major with row strides a_stride /
+// b_stride; offsets [G + 1] device (nullptr: one group of all rows).
+int tc_wgrad_gemm(const void *A, int64_t a_stride, const void *B, int64_t b_stride, int64_t rows,
+                  const int32_t *offsets, int G, int M, int Nn, float *out, int *status, cudaStream_t stream);
 int launch_zero_f32(float *p, size_t n, cudaStream_t s);
 int launch_dy_dgate(const void *dout, const void *y_perm, const float *topk_w, const int32_t *dest_row,
                     const int32_t *src_token, const int32_t *rows_end, int64_t max_rows, int k, int d, void *dy,
