@@ -13,8 +13,9 @@
 // Both operands are MN-major: TMA copies 64-row x 64-column boxes (128-byte
 // swizzle), K running along the rows.  A group's K blocks start at its first row,
 // so its last block may hold rows of the next group (or rows past the data): the
-// MMA warp zeroes those rows of the staged tiles before issuing the MMAs (a
-// 128-byte row of a swizzled box stays one row of shared memory).
+// MMA warp issues that block's K=16 MMAs only up to the group's last row and
+// zeroes the rows of the last one that lie past the group (a 128-byte row of a
+// swizzled box stays one row of shared memory).
 //
 // Same machinery as the forward kernel: one CTA per SM, warp 0 loads a 128x64 A
 // and a 256x64 B tile per stage into a 4-stage ring, warp 1 issues tcgen05.mma
@@ -187,10 +188,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         uint8_t *st = smem + stage * STAGE_BYTES;
+        // a group's last block: MMAs of K=16 up to its last row; the rows of the
+        // last MMA past the group belong to no row of this group: zero them
         const int valid = kend - k0;
-        if (valid < BK) {
-          // rows valid..63 of every box belong to no row of this group: zero them
-          const int nrow = BK - valid;
+        const int nk = valid >= BK ? BK / 16 : (valid + 15) / 16;
+        if (valid < nk * 16) {
+          const int nrow = nk * 16 - valid;
           for (int v = lane; v < (STAGE_BYTES / SLICE) * nrow * 8; v += 32) {
             const int box = v / (nrow * 8), rr = (v / 8) % nrow, ch = v % 8;
             *reinterpret_cast<uint4 *>(st + box * SLICE + (valid + rr) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -203,8 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t sa = smem_u32(st);
           const uint64_t adesc = smem_desc_sw128_mn(sa, SLICE);
           const uint64_t bdesc = smem_desc_sw128_mn(sa + A_BYTES, SLICE);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)  // +16 K rows = +2048 bytes in both tiles
+          for (int kk = 0; kk < nk; ++kk)  // +16 K rows = +2048 bytes in both tiles
             tc_mma_bf16(d_tmem, adesc + 128ull * kk, bdesc + 128ull * kk, IDESC, (k0 > kbeg || kk > 0) ? 1u : 0u);
           tc_commit(&empty[stage]);
         }
@@ -248,10 +250,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 // a pair computes a 256 x 256 output tile, each CTA staging 128 columns of A and
 // 128 of B per K block (32 KB, 6 stages), which halves the shared-memory traffic
 // per MMA of the single-CTA form.  Both CTAs' copies complete on the leader's
-// full[s] and the leader issues the MMAs.  Only a group's last block, whose rows
-// past the group must be zeroed in both CTAs, takes a round trip: the leader
-// tells the peer its copy landed (landed[s] in the peer), both zero their tail
-// rows, and the peer reports back (ready[s] in the leader) before the MMAs.
+// full[s] and the leader issues the MMAs.  In a group's last block the leader's
+// warp zeroes the rows past the group (up to the last K=16 step) in its own tiles
+// and, through distributed shared memory, in the peer's, then fences them for the
+// tensor core: no round trip between the CTAs.
 //   empty[s], tfull[a]  in each CTA: the leader's multicast commits.
 //   tempty[a]           in the leader: the 8 epilogue warps of the pair.
 namespace pr {
@@ -263,15 +265,21 @@ constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + TABLE_
 constexpr uint32_t IDESC = idesc_bf16_f32_major(2 * HALF, 2 * HALF, true, true);
 }  // namespace pr
 
-// Zero rows valid..63 of every 64-row box of a staged K block (a 128-byte row of
-// a swizzled box stays one row), then make the writes visible to the tensor core.
-__device__ __forceinline__ void zero_tail_rows(uint8_t *st, int nbox, int valid, int lane) {
-  const int nrow = BK - valid;
+// Zero rows valid .. end-1 of every 64-row box of a staged K block (a 128-byte
+// row of a swizzled box stays one row), in this CTA and, through its cluster
+// address, in the peer's copy at the same offset; then order the writes before
+// the tensor core's reads of both.
+__device__ __forceinline__ void zero_tail_rows_pair(uint8_t *st, int nbox, int valid, int end, int lane) {
+  const int nrow = end - valid;
+  const uint32_t local = smem_u32(st);
+  const uint32_t remote = mapa_shared(local, 1);
   for (int v = lane; v < nbox * nrow * 8; v += 32) {
     const int box = v / (nrow * 8), rr = (v / 8) % nrow, ch = v % 8;
-    *reinterpret_cast<uint4 *>(st + box * SLICE + (valid + rr) * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t off = (uint32_t)(box * SLICE + (valid + rr) * 128 + ch * 16);
+    *reinterpret_cast<uint4 *>(st + off) = make_uint4(0u, 0u, 0u, 0u);
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(remote + off), "r"(0u) : "memory");
   }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -283,9 +291,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
   uint64_t *empty = full + STAGES;
-  uint64_t *landed = empty + STAGES;
-  uint64_t *ready = landed + STAGES;
-  uint64_t *tfull = ready + STAGES;
+  uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
   int *rowbeg = reinterpret_cast<int *>(smem + STAGES * STAGE_BYTES + 256);
@@ -304,8 +310,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
-      mbar_init(&landed[s], 1);
-      mbar_init(&ready[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -334,8 +338,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t full_lead = mapa_shared(smem_u32(&full[0]), 0);
-  const uint32_t ready_lead = mapa_shared(smem_u32(&ready[0]), 0);
-  const uint32_t landed_peer = mapa_shared(smem_u32(&landed[0]), 1);
   const uint32_t tempty_lead = mapa_shared(smem_u32(&tempty[0]), 0);
 
   if (warp == 0) {
@@ -375,68 +377,51 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (issued_parity[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_parity[s], args.status);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issue (leader), tail zeroing (both)
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t tail_phase = 0;  // bit s: parity of the next landed / ready use of stage s
-    int it = 0;
-    bool ok = true;
-    for (int tile = pair_id; tile < total_tiles && ok; tile += npairs, ++it) {
-      const int g = tile / per_group;
-      const int acc = it & 1;
-      const uint32_t use = (uint32_t)(it >> 1);
-      if (leader && !__all_sync(0xffffffffu, mbar_wait_cluster(&tempty[acc], (use & 1u) ^ 1u, args.status))) break;
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 2 * HALF);
-      const int kbeg = rowbeg[g], kend = rowend[g];
-      for (int k0 = kbeg; k0 < kend; k0 += BK) {
-        const int valid = kend - k0;
-        const bool tail = valid < BK;
-        uint8_t *st = smem + stage * STAGE_BYTES;
-        const uint32_t tp = (tail_phase >> stage) & 1u;
-        if (leader) {
+    // ------------------------------------------------------------ MMA issue and tail zeroing (leader)
+    if (leader) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = pair_id; tile < total_tiles && ok; tile += npairs, ++it) {
+        const int g = tile / per_group;
+        const int acc = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(&tempty[acc], (use & 1u) ^ 1u, args.status))) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * 2 * HALF);
+        const int kbeg = rowbeg[g], kend = rowend[g];
+        for (int k0 = kbeg; k0 < kend; k0 += BK) {
           if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], phase, args.status))) {
             ok = false;
             break;
           }
-          if (tail) {
-            if (lane == 0) mbar_arrive_cluster(landed_peer + 8u * stage);
-            zero_tail_rows(st, STAGE_BYTES / SLICE, valid, lane);
-            __syncwarp();
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(&ready[stage], tp, args.status))) {
-              ok = false;
-              break;
-            }
-          }
+          uint8_t *st = smem + stage * STAGE_BYTES;
+          // a group's last block: MMAs of K=16 up to its last row, the rows of
+          // the last MMA past the group zeroed
+          const int valid = kend - k0;
+          const int nk = valid >= BK ? BK / 16 : (valid + 15) / 16;
+          if (valid < nk * 16) zero_tail_rows_pair(st, STAGE_BYTES / SLICE, valid, nk * 16, lane);
+          __syncwarp();
           if (lane == 0) {
             tc_fence_after();
             const uint32_t sa = smem_u32(st);
             const uint64_t adesc = smem_desc_sw128_mn(sa, SLICE);
             const uint64_t bdesc = smem_desc_sw128_mn(sa + A_BYTES, SLICE);
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
+            for (int kk = 0; kk < nk; ++kk)
               tc_mma_bf16_pair(d_tmem, adesc + 128ull * kk, bdesc + 128ull * kk, pr::IDESC,
                                (k0 > kbeg || kk > 0) ? 1u : 0u);
             tc_commit_pair(&empty[stage], 0x3);
           }
           __syncwarp();
-        } else if (tail) {
-          if (!__all_sync(0xffffffffu, mbar_wait_cluster(&landed[stage], tp, args.status))) {
-            ok = false;
-            break;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
-          zero_tail_rows(st, STAGE_BYTES / SLICE, valid, lane);
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(ready_lead + 8u * stage);
         }
-        if (tail) tail_phase ^= 1u << stage;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
+        if (ok && lane == 0) tc_commit_pair(&tfull[acc], 0x3);
+        __syncwarp();
       }
-      if (ok && leader && lane == 0) tc_commit_pair(&tfull[acc], 0x3);
-      __syncwarp();
     }
   } else {
     // ------------------------------------------------------------ epilogue (both CTAs)
