@@ -505,8 +505,8 @@ def run_ours(args, wl, dist, rank, local):
 
 def time_backward(args, moe, layer, x, wl, stream):
     """Time moe_layer_backward (after a forward) as a CUDA-graph replay; FLOPs of its
-    GEMMs: dh, the a/u recompute, dx rows, dW2, dW1/dW3 = 7 (SwiGLU) or 4 (ReLU)
-    times 2 R d F, R the kept rows."""
+    GEMMs in units of 2 R d F (R the kept rows): dh 1, the a/u recompute 2, dx rows
+    2, dW2 1, dW1/dW3 2 = 8 for SwiGLU; 5 for ReLU (no u, du or dW3)."""
     import torch
     cfg = layer.cfg
     sw = wl.act == "swiglu"
@@ -541,7 +541,8 @@ def time_backward(args, moe, layer, x, wl, stream):
         raise RuntimeError("device status not clean after the backward")
     ms = e0.elapsed_time(e1) / args.steps
     R = int(layer.views()["counts_kept"].sum().item())
-    gemm_flops = (7 if sw else 4) * 2.0 * R * wl.d * wl.F + ((7 if sw else 4) * 2.0 * wl.T * wl.d * Fs if Fs else 0.0)
+    units = 8 if sw else 5
+    gemm_flops = units * 2.0 * R * wl.d * wl.F + (units * 2.0 * wl.T * wl.d * Fs if Fs else 0.0)
     return {"ms_per_step": ms, "tokens_per_s": wl.T / (ms / 1e3), "gemm_flops": gemm_flops,
             "gemm_tflops_over_step": gemm_flops / (ms / 1e3) / 1e12}
 

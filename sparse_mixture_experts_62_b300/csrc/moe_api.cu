@@ -209,8 +209,8 @@ int ec_route(const moe_config *c, const Ws &w, const void *x, const float *Wg, c
 
 // ---------------------------------------------------------------- backward workspace
 struct BwdLayout {
-  size_t dgate, dz, off_sh, dy, dh, a, u, dA, dxp;
-  size_t dh_s, a_s, u_s, dA_s, dx_s, total;
+  size_t dgate, dz, dz2, dwg2, off_sh, dy, dh, dA, dxp;
+  size_t dh_s, dA_s, dx_s, total;
 };
 
 BwdLayout bwd_layout(const moe_config *c) {
@@ -227,17 +227,16 @@ BwdLayout bwd_layout(const moe_config *c) {
   };
   L.dgate = take(T * k * 4);
   L.dz = take(T * N * 4);
+  const size_t Np = (N + 3) / 4 * 4;
+  L.dz2 = take(T * 2 * Np * 2);  // dz as bf16 [hi | lo]
+  L.dwg2 = take(d * 2 * Np * 4);  // x^T [hi | lo]
   L.off_sh = take(2 * 4);
   L.dy = take(R * d * 2);
   L.dh = take(R * F * 2);
-  L.a = take(R * F * 2);
-  L.u = take(sw ? R * F * 2 : 0);
   L.dA = take(R * FA * 2);
   L.dxp = take(R * d * 2);
   if (Fs) {
     L.dh_s = take(T * Fs * 2);
-    L.a_s = take(T * Fs * 2);
-    L.u_s = take(sw ? T * Fs * 2 : 0);
     L.dA_s = take(T * FAs * 2);
     L.dx_s = take(T * d * 2);
   }
@@ -261,15 +260,14 @@ int ffn_backward(const moe_config *c, bool shared, int G, int64_t R, const int32
   const int d = c->d, FA = sw ? 2 * F : F;
   const bool pair = use_pair_tiles(R, G, shared ? 0 : c->capacity);
   auto B = [&](size_t off) { return bws + off; };
-  void *dh = B(shared ? L.dh_s : L.dh), *a = B(shared ? L.a_s : L.a), *u = B(shared ? L.u_s : L.u);
+  void *dh = B(shared ? L.dh_s : L.dh);
   void *dA = B(shared ? L.dA_s : L.dA);
   const int M = shared ? c->T : 0;
   // dh = dy W2, W2 read in place as [G][d][F]
   MOE_TRY(tc_grouped_gemm_bt(dy, nullptr, R, d, d, 0, w2, nullptr, G, F, offsets, M, dh, status, pair, s));
-  // recompute a = x W1^T (and u = x W3^T); then dA = [da | du]
-  MOE_TRY(tc_grouped_gemm(2, xrows, R, d, w1, nullptr, (int64_t)G * F, F, offsets, G, M, F, a, status, pair, s));
-  if (sw) MOE_TRY(tc_grouped_gemm(2, xrows, R, d, w3, nullptr, (int64_t)G * F, F, offsets, G, M, F, u, status, pair, s));
-  MOE_TRY(launch_act_bwd(a, sw ? u : nullptr, dh, off_dev + G, R, F, sw, dA, s));
+  // a = x W1^T and u = x W3^T recomputed, the activation's backward in the epilogue: dA = [da | du]
+  MOE_TRY(tc_grouped_gemm_act_bwd(sw, xrows, R, d, w1, sw ? w3 : nullptr, (int64_t)G * F, F, offsets, G, M, dh, dA,
+                                  status, pair, s));
   // dx rows = da W1 + du W3, W1 and W3 read in place as [G][F][d]
   MOE_TRY(tc_grouped_gemm_bt(dA, sw ? static_cast<uint8_t *>(dA) + (size_t)F * 2 : nullptr, R, FA, F, F, w1,
                              sw ? w3 : nullptr, G, d, offsets, M, dxrows, status, pair, s));
@@ -555,7 +553,13 @@ int moe_layer_backward(const moe_config *cfg, const void *x, const float *Wg, co
                           offsets + N, R, k, d, bws + L.dy, dgate, s));
   MOE_TRY(launch_router_bwd(w.at<float>(FL.logits), w.at<int32_t>(FL.topk_idx), w.at<float>(FL.topk_w), dgate,
                             cfg->gate, T, N, k, dz, s));
-  MOE_TRY(launch_dwg(x, dz, T, d, N, dWg, s));
+  {  // dW_g = x^T dz
+    const int Np = (N + 3) / 4 * 4;
+    MOE_TRY(launch_split_dz(dz, T, N, Np, bws + L.dz2, s));
+    float *part = reinterpret_cast<float *>(bws + L.dwg2);
+    MOE_TRY(tc_wgrad_gemm(x, d, bws + L.dz2, 2 * Np, T, nullptr, 1, d, 2 * Np, part, w.status(), s));
+    MOE_TRY(launch_dwg_sum(part, d, N, Np, dWg, s));
+  }
   // routed experts
   MOE_TRY(ffn_backward(cfg, false, N, R, offsets, offsets, w.at<void>(FL.x_perm), w.at<void>(FL.h), bws + L.dy, w1, w3,
                        w2, cfg->ffn, bws, L, dw1, dw3, dw2, bws + L.dxp, w.status(), s));

@@ -110,39 +110,28 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(const float *__restrict
   }
 }
 
-// dA from the recomputed a (and u) and dh: SwiGLU [da | du] ([R, 2F]) or ReLU da ([R, F]).
-__global__ void __launch_bounds__(256) act_bwd_kernel(const uint16_t *__restrict__ a, const uint16_t *__restrict__ u,
-                                                      const uint16_t *__restrict__ dh,
-                                                      const int32_t *__restrict__ rows_end, int F, bool swiglu,
-                                                      uint16_t *__restrict__ dA) {
-  const size_t n = (size_t)(*rows_end) * F;
-  for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 2; i < n; i += (size_t)gridDim.x * blockDim.x * 2) {
-    const size_t r = i / F, f = i % F;  // F is even: the pair stays in one row
-    const uint32_t av = *reinterpret_cast<const uint32_t *>(a + i);
-    const uint32_t gv = *reinterpret_cast<const uint32_t *>(dh + i);
-    const float a0 = bf16_lo(av), a1 = bf16_hi(av), g0 = bf16_lo(gv), g1 = bf16_hi(gv);
-    if (swiglu) {
-      const uint32_t uv = *reinterpret_cast<const uint32_t *>(u + i);
-      const float u0 = bf16_lo(uv), u1 = bf16_hi(uv);
-      const float s0 = 1.0f / (1.0f + expf(-a0)), s1 = 1.0f / (1.0f + expf(-a1));
-      const float da0 = g0 * u0 * s0 * (1.0f + a0 * (1.0f - s0)), da1 = g1 * u1 * s1 * (1.0f + a1 * (1.0f - s1));
-      const float du0 = g0 * a0 * s0, du1 = g1 * a1 * s1;
-      *reinterpret_cast<uint32_t *>(dA + r * 2 * F + f) = pack_bf16x2(da0, da1);
-      *reinterpret_cast<uint32_t *>(dA + r * 2 * F + F + f) = pack_bf16x2(du0, du1);
-    } else {
-      *reinterpret_cast<uint32_t *>(dA + r * F + f) = pack_bf16x2(a0 > 0.f ? g0 : 0.f, a1 > 0.f ? g1 : 0.f);
-    }
+// dz [T, N] float32 -> [T, 2 Np] bf16: columns e = bf16(dz), Np + e = bf16(dz -
+// bf16(dz)), zero past N.  With x exact in bf16, x^T [hi | lo] on the tensor cores
+// gives x^T dz to about 2^-16 relative (two-term split, every product exact).
+__global__ void split_dz_kernel(const float *__restrict__ dz, int T, int N, int Np, uint16_t *__restrict__ out) {
+  const size_t n = (size_t)T * Np;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int t = (int)(i / Np), e = (int)(i % Np);
+    const float v = e < N ? dz[(size_t)t * N + e] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    out[(size_t)t * 2 * Np + e] = __bfloat16_as_ushort(hi);
+    out[(size_t)t * 2 * Np + Np + e] = __bfloat16_as_ushort(lo);
   }
 }
 
-// dWg[c][e] = sum_t x[t][c] dz[t][e]; one thread per (c, e), c fastest.
-__global__ void __launch_bounds__(256) dwg_kernel(const uint16_t *__restrict__ x, const float *__restrict__ dz, int T,
-                                                  int d, int N, float *__restrict__ dWg) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x, e = blockIdx.y;
-  if (c >= d) return;
-  float acc = 0.f;
-  for (int t = 0; t < T; ++t) acc = fmaf(__uint_as_float((uint32_t)x[(size_t)t * d + c] << 16), dz[(size_t)t * N + e], acc);
-  dWg[(size_t)c * N + e] = acc;
+// dWg[c][e] = part[c][e] + part[c][Np + e]: the hi and lo halves of x^T [hi | lo].
+__global__ void dwg_sum_kernel(const float *__restrict__ part, int d, int N, int Np, float *__restrict__ dWg) {
+  const size_t n = (size_t)d * N;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i / N), e = (int)(i % N);
+    dWg[i] = part[(size_t)c * 2 * Np + e] + part[(size_t)c * 2 * Np + Np + e];
+  }
 }
 
 // dx[t] = sum_j kept dx_perm[row_tj] + sum_e dz[t][e] Wg[:, e] (+ the shared expert's dx).
@@ -209,18 +198,14 @@ int launch_router_bwd(const float *logits, const int32_t *idx, const float *topk
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-int launch_act_bwd(const void *a, const void *u, const void *dh, const int32_t *rows_end, int64_t max_rows, int F,
-                   bool swiglu, void *dA, cudaStream_t s) {
-  if (max_rows <= 0) return MOE_OK;
-  act_bwd_kernel<<<grid_for((size_t)max_rows * F / 2, 256), 256, 0, s>>>(
-      static_cast<const uint16_t *>(a), static_cast<const uint16_t *>(u), static_cast<const uint16_t *>(dh), rows_end, F,
-      swiglu, static_cast<uint16_t *>(dA));
+int launch_split_dz(const float *dz, int T, int N, int Np, void *out, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  split_dz_kernel<<<grid_for((size_t)T * Np, 256), 256, 0, s>>>(dz, T, N, Np, static_cast<uint16_t *>(out));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-int launch_dwg(const void *x, const float *dz, int T, int d, int N, float *dWg, cudaStream_t s) {
-  dim3 grid((d + 255) / 256, N);
-  dwg_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t *>(x), dz, T, d, N, dWg);
+int launch_dwg_sum(const float *part, int d, int N, int Np, float *dWg, cudaStream_t s) {
+  dwg_sum_kernel<<<grid_for((size_t)d * N, 256), 256, 0, s>>>(part, d, N, Np, dWg);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -23,6 +23,10 @@
 //            tiles); epilogue as kPlain.  dh = dy W2 in the backward.
 //   kDualBT: two (A, B) pairs concatenated along K, both B's as in kPlainBT:
 //            out = A1 B1 + A2 B2.  dx rows = da W1 + du W3 in the backward.
+//   kSwiGLUBwd: the kSwiGLU tile (a = x W1^T, u = x W3^T recomputed), epilogue
+//            the activation's backward with dh read from memory:
+//            da = dh u SiLU'(a) into columns n, du = dh SiLU(a) into n_out + n.
+//   kReLUBwd: the kReLU tile (a = x W1^T), epilogue da = dh [a > 0].
 //
 // Kernel shape (one CTA per SM, persistent over output tiles):
 //   warp 0      TMA producer (one lane): 4-stage ring of {A 128x64, B 256x64}.
@@ -56,7 +60,9 @@ constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_
                               (size_t)(4 * MAX_GROUPS + 8) * 4;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
-enum Mode { kSwiGLU = 0, kReLU = 1, kPlain = 2, kPlainBT = 3, kDualBT = 4 };
+enum Mode { kSwiGLU = 0, kReLU = 1, kPlain = 2, kPlainBT = 3, kDualBT = 4, kSwiGLUBwd = 5, kReLUBwd = 6 };
+// modes whose tile pairs W1 and W3 rows (128 output columns per tile)
+__host__ __device__ constexpr bool paired_b(int mode) { return mode == kSwiGLU || mode == kSwiGLUBwd; }
 constexpr uint32_t IDESC_BT = idesc_bf16_f32_major(BM, BN, false, true);
 constexpr int B_SLICE = BK * 64 * 2;  // one MN-major B slice: 64 K rows x 64 columns = 8 KB
 
@@ -72,16 +78,100 @@ struct Args {
   int *status;
   int32_t num_kb;      // K blocks per tile
   int32_t kb1;         // kDualBT: K blocks taken from the first (A, B) pair
+  int32_t out_stride;  // elements between output rows
+  const uint16_t *dh;  // kSwiGLUBwd / kReLUBwd: [rows, n_out] bf16 gradient of h
 };
 
 __device__ __forceinline__ float silu(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
+
+// Epilogue of one accumulator row (this thread's TMEM lane at taddr): output row
+// `row`, columns n0 .. of the tile; nothing is stored when !row_ok.
+template <int MODE>
+__device__ __forceinline__ void epilogue_row(uint32_t taddr, const Args &args, int row, bool row_ok, int n0) {
+  uint16_t *orow = args.out + (size_t)(row_ok ? row : 0) * args.out_stride;
+  if (MODE == kSwiGLU) {
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 16) {
+      float a[16], u[16];
+      tmem_ld16x2(taddr + c, taddr + 128 + c, a, u);
+      uint32_t p[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) p[i] = pack_bf16x2(silu(a[2 * i]) * u[2 * i], silu(a[2 * i + 1]) * u[2 * i + 1]);
+      const int col = n0 + c;
+      if (row_ok) {
+        if (col + 8 <= args.n_out) *reinterpret_cast<uint4 *>(orow + col) = make_uint4(p[0], p[1], p[2], p[3]);
+        if (col + 16 <= args.n_out) *reinterpret_cast<uint4 *>(orow + col + 8) = make_uint4(p[4], p[5], p[6], p[7]);
+      }
+    }
+  } else if (MODE == kSwiGLUBwd) {
+    const uint16_t *grow = args.dh + (size_t)(row_ok ? row : 0) * args.n_out;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 16) {
+      float a[16], u[16];
+      tmem_ld16x2(taddr + c, taddr + 128 + c, a, u);
+      const int col = n0 + c;
+      if (!row_ok) continue;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (col + 8 * h + 8 > args.n_out) break;
+        const uint4 gq = *reinterpret_cast<const uint4 *>(grow + col + 8 * h);
+        const uint32_t gv[4] = {gq.x, gq.y, gq.z, gq.w};
+        uint32_t pa[4], pu[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float da[2], du[2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const float av = a[8 * h + 2 * i + j], uv = u[8 * h + 2 * i + j];
+            const float g = j ? bf16_hi(gv[i]) : bf16_lo(gv[i]);
+            const float sg = 1.0f / (1.0f + __expf(-av));
+            da[j] = g * uv * sg * (1.0f + av * (1.0f - sg));
+            du[j] = g * av * sg;
+          }
+          pa[i] = pack_bf16x2(da[0], da[1]);
+          pu[i] = pack_bf16x2(du[0], du[1]);
+        }
+        *reinterpret_cast<uint4 *>(orow + col + 8 * h) = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+        *reinterpret_cast<uint4 *>(orow + args.n_out + col + 8 * h) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+      }
+    }
+  } else {
+    const uint16_t *grow = (MODE == kReLUBwd) ? args.dh + (size_t)(row_ok ? row : 0) * args.n_out : nullptr;
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+      float v0[16], v1[16];
+      tmem_ld16x2(taddr + c, taddr + c + 16, v0, v1);
+      if (!row_ok) continue;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int col = n0 + c + 8 * q;
+        if (col + 8 > args.n_out) continue;
+        const float *v = q < 2 ? v0 + 8 * q : v1 + 8 * (q - 2);
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = (MODE == kReLU) ? fmaxf(v[i], 0.f) : v[i];
+        if (MODE == kReLUBwd) {
+          const uint4 gq = *reinterpret_cast<const uint4 *>(grow + col);
+          const uint32_t gv[4] = {gq.x, gq.y, gq.z, gq.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            x[2 * i] = v[2 * i] > 0.f ? bf16_lo(gv[i]) : 0.f;
+            x[2 * i + 1] = v[2 * i + 1] > 0.f ? bf16_hi(gv[i]) : 0.f;
+          }
+        }
+        *reinterpret_cast<uint4 *>(orow + col) =
+            make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+      }
+    }
+  }
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
                         const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                         const Args args) {
-  constexpr int OUT_COLS = (MODE == kSwiGLU) ? 128 : 256;  // output columns per tile
+  constexpr int OUT_COLS = paired_b(MODE) ? 128 : 256;  // output columns per tile
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled operand tiles
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -132,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
-    if (MODE == kSwiGLU || MODE == kDualBT) tma_prefetch_desc(&tmB1);
+    if (paired_b(MODE) || MODE == kDualBT) tma_prefetch_desc(&tmB1);
     if (MODE == kDualBT) tma_prefetch_desc(&tmA2);
   }
   if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
@@ -174,7 +264,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
               tma_load_3d(sb + j * B_SLICE, mb, &full[stage], n_tile * OUT_COLS + 64 * j, k0, g);
-          } else if (MODE == kSwiGLU) {
+          } else if (paired_b(MODE)) {
             tma_load_2d(sa, &tmA, &full[stage], kb * BK, a_row);
             tma_load_2d(sb, &tmB0, &full[stage], kb * BK, b_row);
             tma_load_2d(sb + B_BYTES / 2, &tmB1, &full[stage], kb * BK, b_row);
@@ -256,51 +346,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(&tfull[acc], use & 1u, args.status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
-      const bool row_ok = r < rows_valid;
-      uint16_t *orow = args.out + (size_t)(row0 + (row_ok ? r : 0)) * args.n_out;
-      if (MODE == kSwiGLU) {
-#pragma unroll 1
-        for (int c = 0; c < 128; c += 16) {
-          float a[16], u[16];
-          tmem_ld16x2(taddr + c, taddr + 128 + c, a, u);
-          uint32_t p[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) p[i] = pack_bf16x2(silu(a[2 * i]) * u[2 * i], silu(a[2 * i + 1]) * u[2 * i + 1]);
-          const int col = n0 + c;
-          if (row_ok) {
-            if (col + 8 <= args.n_out) *reinterpret_cast<uint4 *>(orow + col) = make_uint4(p[0], p[1], p[2], p[3]);
-            if (col + 16 <= args.n_out)
-              *reinterpret_cast<uint4 *>(orow + col + 8) = make_uint4(p[4], p[5], p[6], p[7]);
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          float v0[16], v1[16];
-          tmem_ld16x2(taddr + c, taddr + c + 16, v0, v1);
-          uint32_t p[16];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float x0 = v0[2 * i], x1 = v0[2 * i + 1], y0 = v1[2 * i], y1 = v1[2 * i + 1];
-            if (MODE == kReLU) {
-              x0 = fmaxf(x0, 0.f);
-              x1 = fmaxf(x1, 0.f);
-              y0 = fmaxf(y0, 0.f);
-              y1 = fmaxf(y1, 0.f);
-            }
-            p[i] = pack_bf16x2(x0, x1);
-            p[8 + i] = pack_bf16x2(y0, y1);
-          }
-          if (row_ok) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int col = n0 + c + 8 * q;
-              if (col + 8 <= args.n_out)
-                *reinterpret_cast<uint4 *>(orow + col) = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
-            }
-          }
-        }
-      }
+      epilogue_row<MODE>(taddr, args, row0 + r, r < rows_valid, n0);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -345,7 +391,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int STAGES = pair::STAGES, STAGE_BYTES = pair::STAGE_BYTES, A_BYTES = pair::A_BYTES;
   constexpr int BM = pair::BM;
   constexpr uint32_t IDESC = pair::IDESC;
-  constexpr int OUT_COLS = (MODE == kSwiGLU) ? 128 : 256;
+  constexpr int OUT_COLS = paired_b(MODE) ? 128 : 256;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
@@ -398,7 +444,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
-    if (MODE == kSwiGLU || MODE == kDualBT) tma_prefetch_desc(&tmB1);
+    if (paired_b(MODE) || MODE == kDualBT) tma_prefetch_desc(&tmB1);
     if (MODE == kDualBT) tma_prefetch_desc(&tmA2);
   }
   if (warp == 1) tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -420,15 +466,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int g = 0;
       bool ok = true;
-      const CUtensorMap *mb = (MODE == kSwiGLU && rank == 1) ? &tmB1 : &tmB0;
+      const CUtensorMap *mb = (paired_b(MODE) && rank == 1) ? &tmB1 : &tmB0;
       for (int tile = pair_id; tile < total_tiles && ok; tile += npairs) {
         while (tile >= tile_start[g + 1]) ++g;
         const int local = tile - tile_start[g];
         const int n_tile = local / mtiles[g];
         const int m_tile = local - n_tile * mtiles[g];
         const int a_row = rowbeg[g] + m_tile * 2 * BM + (int)rank * BM;
-        const int b_row = (MODE == kSwiGLU) ? g * args.b_rows + n_tile * OUT_COLS
-                                            : g * args.b_rows + n_tile * OUT_COLS + (int)rank * 128;
+        const int b_row = paired_b(MODE) ? g * args.b_rows + n_tile * OUT_COLS
+                                         : g * args.b_rows + n_tile * OUT_COLS + (int)rank * 128;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, args.status)) {
             ok = false;
@@ -521,51 +567,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(&tfull[acc], use & 1u, args.status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
-      const bool row_ok = r < rows_valid;
-      uint16_t *orow = args.out + (size_t)(row_ok ? row0 + r : 0) * args.n_out;
-      if (MODE == kSwiGLU) {
-#pragma unroll 1
-        for (int c = 0; c < 128; c += 16) {
-          float a[16], u[16];
-          tmem_ld16x2(taddr + c, taddr + 128 + c, a, u);
-          uint32_t p[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) p[i] = pack_bf16x2(silu(a[2 * i]) * u[2 * i], silu(a[2 * i + 1]) * u[2 * i + 1]);
-          const int col = n0 + c;
-          if (row_ok) {
-            if (col + 8 <= args.n_out) *reinterpret_cast<uint4 *>(orow + col) = make_uint4(p[0], p[1], p[2], p[3]);
-            if (col + 16 <= args.n_out)
-              *reinterpret_cast<uint4 *>(orow + col + 8) = make_uint4(p[4], p[5], p[6], p[7]);
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          float v0[16], v1[16];
-          tmem_ld16x2(taddr + c, taddr + c + 16, v0, v1);
-          uint32_t p[16];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float x0 = v0[2 * i], x1 = v0[2 * i + 1], y0 = v1[2 * i], y1 = v1[2 * i + 1];
-            if (MODE == kReLU) {
-              x0 = fmaxf(x0, 0.f);
-              x1 = fmaxf(x1, 0.f);
-              y0 = fmaxf(y0, 0.f);
-              y1 = fmaxf(y1, 0.f);
-            }
-            p[i] = pack_bf16x2(x0, x1);
-            p[8 + i] = pack_bf16x2(y0, y1);
-          }
-          if (row_ok) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int col = n0 + c + 8 * q;
-              if (col + 8 <= args.n_out)
-                *reinterpret_cast<uint4 *>(orow + col) = make_uint4(p[4 * q], p[4 * q + 1], p[4 * q + 2], p[4 * q + 3]);
-            }
-          }
-        }
-      }
+      epilogue_row<MODE>(taddr, args, row0 + r, r < rows_valid, n0);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty_lead + 8u * acc);
@@ -718,7 +720,9 @@ static int launch_mode(int mode, const CUtensorMap &ma, const CUtensorMap &ma2, 
       case kReLU: return launch_pair<kReLU>(ma, ma2, mb0, mb1, args, device, stream);
       case kPlain: return launch_pair<kPlain>(ma, ma2, mb0, mb1, args, device, stream);
       case kPlainBT: return launch_pair<kPlainBT>(ma, ma2, mb0, mb1, args, device, stream);
-      default: return launch_pair<kDualBT>(ma, ma2, mb0, mb1, args, device, stream);
+      case kDualBT: return launch_pair<kDualBT>(ma, ma2, mb0, mb1, args, device, stream);
+      case kSwiGLUBwd: return launch_pair<kSwiGLUBwd>(ma, ma2, mb0, mb1, args, device, stream);
+      default: return launch_pair<kReLUBwd>(ma, ma2, mb0, mb1, args, device, stream);
     }
   }
   switch (mode) {
@@ -726,7 +730,9 @@ static int launch_mode(int mode, const CUtensorMap &ma, const CUtensorMap &ma2, 
     case kReLU: return launch_single<kReLU>(ma, ma2, mb0, mb1, args, device, sms, stream);
     case kPlain: return launch_single<kPlain>(ma, ma2, mb0, mb1, args, device, sms, stream);
     case kPlainBT: return launch_single<kPlainBT>(ma, ma2, mb0, mb1, args, device, sms, stream);
-    default: return launch_single<kDualBT>(ma, ma2, mb0, mb1, args, device, sms, stream);
+    case kDualBT: return launch_single<kDualBT>(ma, ma2, mb0, mb1, args, device, sms, stream);
+    case kSwiGLUBwd: return launch_single<kSwiGLUBwd>(ma, ma2, mb0, mb1, args, device, sms, stream);
+    default: return launch_single<kReLUBwd>(ma, ma2, mb0, mb1, args, device, sms, stream);
   }
 }
 
@@ -755,8 +761,35 @@ int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *
   if (sms <= 0) return MOE_ERR_CUDA;
   const int num_kb = (K + BK - 1) / BK;
   Args args{offsets, G, M, (int32_t)a_rows, n_out, K, b_rows_per_group, static_cast<uint16_t *>(out), status,
-            num_kb, num_kb};
+            num_kb, num_kb, n_out, nullptr};
   return launch_mode(mode, ma, ma, mb0, mb1, args, dev, sms, pair_tiles, stream);
+}
+
+int tc_grouped_gemm_act_bwd(bool swiglu, const void *A, int64_t a_rows, int K, const void *W1, const void *W3,
+                            int64_t b_rows_total, int F, const int32_t *offsets, int G, int M, const void *dh,
+                            void *dA, int *status, bool pair_tiles, cudaStream_t stream) {
+  using namespace tc;
+  if (G < 1 || G > MAX_GROUPS || K < 1 || F < 1 || a_rows < 1 || a_rows > INT32_MAX || b_rows_total < 1)
+    return MOE_ERR_INVALID_ARG;
+  if ((int64_t)G * F > b_rows_total || !A || !W1 || (swiglu && !W3) || !dh || !dA) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(dh) | reinterpret_cast<uintptr_t>(dA)) & 15 || F % 8) return MOE_ERR_UNSUPPORTED;
+  CUtensorMap ma, mb0, mb1;
+  int rc;
+  if ((rc = make_map(&ma, A, (uint64_t)a_rows, (uint64_t)K))) return rc;
+  if ((rc = make_map(&mb0, W1, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
+  if (swiglu) {
+    if ((rc = make_map(&mb1, W3, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
+  } else {
+    mb1 = mb0;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const int num_kb = (K + BK - 1) / BK;
+  Args args{offsets, G, M, (int32_t)a_rows, F, K, F, static_cast<uint16_t *>(dA), status,
+            num_kb, num_kb, swiglu ? 2 * F : F, static_cast<const uint16_t *>(dh)};
+  return launch_mode(swiglu ? kSwiGLUBwd : kReLUBwd, ma, ma, mb0, mb1, args, dev, sms, pair_tiles, stream);
 }
 
 int tc_grouped_gemm_bt(const void *A, const void *A2, int64_t a_rows, int64_t a_stride, int K1, int K2,
@@ -785,7 +818,8 @@ int tc_grouped_gemm_bt(const void *A, const void *A2, int64_t a_rows, int64_t a_
   if (sms <= 0) return MOE_ERR_CUDA;
   const int kb1 = (K1 + BK - 1) / BK;
   const int num_kb = kb1 + (dual ? (K2 + BK - 1) / BK : 0);
-  Args args{offsets, G, M, (int32_t)a_rows, n_out, K1, 0, static_cast<uint16_t *>(out), status, num_kb, kb1};
+  Args args{offsets, G, M, (int32_t)a_rows, n_out, K1, 0, static_cast<uint16_t *>(out), status, num_kb, kb1, n_out,
+            nullptr};
   return launch_mode(dual ? kDualBT : kPlainBT, ma, ma2, mb0, mb1, args, dev, sms, pair_tiles, stream);
 }
 

@@ -36,6 +36,13 @@ int launch_gather_rows(const void *x, const int32_t *src_token, const int32_t *o
 int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
                     int64_t b_rows_total, int b_rows_per_group, const int32_t *offsets, int G, int M, int n_out,
                     void *out, int *status, bool pair_tiles, cudaStream_t stream);
+// The gate/up GEMM recomputed for the backward with the activation's backward
+// fused into its epilogue: a = A W1_g^T (and u = A W3_g^T), dh [rows, F] read,
+// dA written: SwiGLU [rows, 2F] = [dh u SiLU'(a) | dh SiLU(a)], ReLU [rows, F] =
+// dh [a > 0].  W1/W3 as in tc_grouped_gemm (K-major [G * F, K]).
+int tc_grouped_gemm_act_bwd(bool swiglu, const void *A, int64_t a_rows, int K, const void *W1, const void *W3,
+                            int64_t b_rows_total, int F, const int32_t *offsets, int G, int M, const void *dh,
+                            void *dA, int *status, bool pair_tiles, cudaStream_t stream);
 // The same GEMM with each group's B stored [K, n_out] (the stacked weights read in
 // place, MN-major tiles): out = A[:, :K1] B0_g, or with A2 (dual) out = A B0_g +
 // A2 B1_g where A2 is a second [a_rows, K2] view with the same row stride.
@@ -71,9 +78,10 @@ int launch_dy_dgate(const void *dout, const void *y_perm, const float *topk_w, c
                     float *dgate, cudaStream_t s);
 int launch_router_bwd(const float *logits, const int32_t *idx, const float *topk_w, const float *dgate, int gate, int T,
                       int N, int k, float *dz, cudaStream_t s);
-int launch_act_bwd(const void *a, const void *u, const void *dh, const int32_t *rows_end, int64_t max_rows, int F,
-                   bool swiglu, void *dA, cudaStream_t s);
-int launch_dwg(const void *x, const float *dz, int T, int d, int N, float *dWg, cudaStream_t s);
+// dW_g = x^T dz on the tensor cores: dz split into bf16 [hi | lo] columns (Np =
+// N rounded up to 4), one weight-gradient GEMM over all T rows, halves added.
+int launch_split_dz(const float *dz, int T, int N, int Np, void *out, cudaStream_t s);
+int launch_dwg_sum(const float *part, int d, int N, int Np, float *dWg, cudaStream_t s);
 int launch_dx_combine(const void *dxp, const int32_t *dest_row, const float *dz, const float *Wg, const void *dx_sh,
                       int T, int d, int N, int k, float *dx, cudaStream_t s);
 int launch_set_offsets2(int32_t *offsets, int rows, cudaStream_t s);
