@@ -468,9 +468,10 @@ int moe_load_stats(const moe_config *cfg, const float *logits, const int32_t *co
   Ws w;
   MOE_TRY(make_ws(cfg, ws, &w));
   const long long total = is_ec(cfg) ? (long long)routed_rows(cfg) : (long long)cfg->T * cfg->k;
+  // the ticket of the statistics' last CTA lives in the (here unused) sequence-loss scratch
   return launch_load_stats(logits, counts_routed, counts_kept, cfg->T, cfg->N, total,
-                           is_ec(cfg) ? MOE_GATE_SOFTMAX_FULL : cfg->gate, w.stats_partial(cfg), f, P, summary,
-                           static_cast<cudaStream_t>(stream));
+                           is_ec(cfg) ? MOE_GATE_SOFTMAX_FULL : cfg->gate, w.stats_partial(cfg),
+                           reinterpret_cast<int *>(w.seq_loss(cfg)), f, P, summary, static_cast<cudaStream_t>(stream));
 }
 
 int moe_ec_route(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias, float *logits,

@@ -98,7 +98,8 @@ int launch_combine(bool bf16, const void *y_perm, const int32_t *dest_row, const
 constexpr int kStatsChunk = 32;  // tokens per partial-sum chunk
 // total = all routed assignments (T * k, or N * C under expert choice)
 int launch_load_stats(const float *logits, const int32_t *counts_routed, const int32_t *counts_kept, int T, int N,
-                      long long total, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s);
+                      long long total, int gate, float *partial, int *ticket, float *f, float *P, float *summary,
+                      cudaStream_t s);
 int launch_router_zloss(const float *logits, int T, int N, float *partial, float *z_loss, cudaStream_t s);
 // Sequence-wise balance loss: chunks of the P partials it needs for T tokens in
 // sequences of L (at most 2 ceil(T / 32) + 2 rows of N floats), then the launch.

@@ -102,12 +102,35 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const void *__restri
   }
 }
 
-// Orderable key of (score desc, index asc): larger key = preferred expert.
-__device__ __forceinline__ unsigned long long topk_key(float v, int e) {
-  if (v == 0.0f) v = 0.0f;  // -0 and +0 are the same score
-  uint32_t u = __float_as_uint(v);
-  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((unsigned long long)u << 32) | (uint32_t)(0xFFFFu - (uint32_t)e);
+// 32-bit key whose unsigned order is the float order (-0 and +0 equal).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  if (v == 0.0f) v = 0.0f;
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// One round of the warp's top-k: the untaken expert (lane + 32 i) with the largest
+// key, the lowest index among equal keys (warp max of the keys, then warp min of
+// the indices holding it).  Every valid key is > 0; key 0 marks "none".
+template <int NV>
+__device__ __forceinline__ int warp_select(const uint32_t (&key)[NV], uint32_t &taken, int lane, uint32_t *kmax) {
+  uint32_t best = 0;
+  int bi = 0;
+#pragma unroll
+  for (int i = 0; i < NV; ++i)
+    if (!((taken >> i) & 1u) && key[i] > best) {  // strict: the lowest i wins a tie within the lane
+      best = key[i];
+      bi = i;
+    }
+  const uint32_t m = __reduce_max_sync(0xffffffffu, best);
+  const uint32_t cand = (best == m && m != 0u) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
+  const int e = (int)__reduce_min_sync(0xffffffffu, cand);
+  if ((e & 31) == lane) taken |= 1u << (e >> 5);
+  *kmax = m;
+  return e;
 }
 
 __device__ __forceinline__ float sigmoid_f32(float z) {
@@ -119,6 +142,7 @@ __device__ __forceinline__ float sigmoid_f32(float z) {
 // are the sum of S partial tiles (row stride pstride, tile stride T * pstride),
 // added in split order, plus the optional logit bias; they are written to
 // `logits` (which may alias the only partial when S == 1 and no bias is added).
+template <int NV>  // expert slots per lane: N <= 32 NV
 __global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, int S, int pstride,
                                                           const float *__restrict__ logit_bias, float *logits,
                                                           const float *__restrict__ sel_bias, int T, int N, int k,
@@ -128,10 +152,10 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, 
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
   const float *zr = logits + (size_t)t * N;
-  float sel[8];
+  float sel[NV];
   bool bad = false;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
     if (e < N) {
       // four independent running sums over the splits, combined in a fixed order
@@ -153,7 +177,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, 
   }
   __syncwarp();
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
     sel[i] = -INFINITY;
     if (e < N) {
@@ -168,103 +192,96 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, 
     }
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, MOE_ERR_NONFINITE);
+  uint32_t key[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) key[i] = (lane + 32 * i < N) ? order_key(sel[i]) : 0u;
+  int chosen[8];
+  bool done = false;
   if (gate == MOE_GATE_SIGMOID_BIAS) {
     // The selection score is fl32(s + b) with s = fl32(sigmoid(z)) evaluated in
     // double.  The float32 estimate above (expf within 2 ulp, then one add and
-    // one division) is within 5.4e-7 of it, so an expert whose estimate is more
-    // than kSelMargin below the k-th largest estimate cannot be in the top k.
-    // Only the remaining candidates (almost always exactly k) are evaluated in
-    // double; the others drop out.
-    constexpr float kSelMargin = 4e-6f;
-    uint32_t taken0 = 0;
-    unsigned long long kth = 0;
-    for (int j = 0; j < k; ++j) {
-      unsigned long long best = 0;
+    // one division) is within kEstErr of it.  If the k + 1 largest estimates are
+    // more than 2 kEstErr apart from one another (checked with a factor 2 to spare),
+    // the exact scores rank exactly as
+    // the estimates do (and nothing below the (k+1)-th can overtake the k-th), so
+    // the estimates decide.  Otherwise (a near tie) every expert within kSelMargin
+    // of the k-th estimate is evaluated in double and ranked again; the rest
+    // cannot be in the top k.
+    constexpr float kEstErr = 5.4e-7f, kSelMargin = 4e-6f;
+    uint32_t taken0 = 0, kv[9];
+    int ch0[9];
+    const int rounds = min(k + 1, N);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+    for (int j = 0; j < 9; ++j)
+      if (j < rounds) ch0[j] = warp_select(key, taken0, lane, &kv[j]);
+    bool clear = true;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)  // 4 kEstErr: twice the bound, covering the rounding of the gap itself
+      if (j + 1 < rounds) clear = clear && (key_value(kv[j]) - key_value(kv[j + 1]) > 4.0f * kEstErr);
+    if (clear) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) chosen[j] = ch0[j];
+      done = true;
+    } else {
+      uint32_t kk = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j == k - 1) kk = kv[j];
+      const float vk = key_value(kk);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
         const int e = lane + 32 * i;
-        if (e < N && !((taken0 >> i) & 1u)) {
-          const unsigned long long key = topk_key(sel[i], e);
-          best = key > best ? key : best;
+        if (e >= N) continue;
+        if (sel[i] >= vk - kSelMargin) {
+          float se = sigmoid_f32(zr[e]);
+          if (sel_bias) se = se + sel_bias[e];
+          key[i] = order_key(se);
+        } else {
+          key[i] = order_key(-INFINITY);
         }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
-        best = o > best ? o : best;
-      }
-      const int e_best = (int)(0xFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
-      if ((e_best & 31) == lane) taken0 |= 1u << (e_best >> 5);
-      kth = best;
-    }
-    const uint32_t ku = (uint32_t)(kth >> 32);
-    const float vk = __uint_as_float((ku & 0x80000000u) ? (ku & 0x7FFFFFFFu) : ~ku);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e >= N) continue;
-      if (sel[i] >= vk - kSelMargin) {
-        float se = sigmoid_f32(zr[e]);
-        if (sel_bias) se = se + sel_bias[e];
-        sel[i] = se;
-      } else {
-        sel[i] = -INFINITY;
       }
     }
   }
-  uint32_t taken = 0;
-  int chosen[8];
-  for (int j = 0; j < k; ++j) {
-    unsigned long long best = 0;
+  if (!done) {
+    uint32_t taken = 0, kmax;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane + 32 * i;
-      if (e < N && !((taken >> i) & 1u)) {
-        const unsigned long long key = topk_key(sel[i], e);
-        best = key > best ? key : best;
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
-      best = o > best ? o : best;
-    }
-    const int e_best = (int)(0xFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
-    if ((e_best & 31) == lane) taken |= 1u << (e_best >> 5);
-    chosen[j] = e_best;
+    for (int j = 0; j < 8; ++j)
+      if (j < k) chosen[j] = warp_select(key, taken, lane, &kmax);
   }
   // full-softmax gate: the normaliser over all N experts (warp sum, fixed order)
   float full_den = 0.f;
   if (gate == MOE_GATE_SOFTMAX_FULL) {
     const float m = zr[chosen[0]];  // the largest logit
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < NV; ++i)
       if (lane + 32 * i < N) full_den += expf(zr[lane + 32 * i] - m);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) full_den += __shfl_xor_sync(0xffffffffu, full_den, off);
   }
-  // gate weights of the selected experts, in float32
-  if (lane == 0) {
-    float g[8];
-    float sum = 0.f;
-    if (gate == MOE_GATE_SOFTMAX_TOPK || gate == MOE_GATE_SOFTMAX_FULL) {
-      const float m = zr[chosen[0]];  // the first pick has the largest logit
-      for (int j = 0; j < k; ++j) {
-        g[j] = expf(zr[chosen[j]] - m);
-        sum += g[j];
-      }
-      if (gate == MOE_GATE_SOFTMAX_FULL) sum = full_den;
-    } else {
-      // float32 affinities (within 3e-7 relative of the rounded exact ones)
-      for (int j = 0; j < k; ++j) {
-        g[j] = 1.0f / (1.0f + expf(-zr[chosen[j]]));
-        sum += g[j];
-      }
-    }
-    for (int j = 0; j < k; ++j) {
-      idx[(size_t)t * k + j] = chosen[j];
-      w[(size_t)t * k + j] = g[j] / sum;
-    }
+  // gate weights of the selected experts, in float32: lane j < k takes slot j;
+  // the normaliser is a warp sum in a fixed order
+  float zj = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (j < k && lane == j) zj = zr[chosen[j]];
+  float g = 0.f;
+  if (gate == MOE_GATE_SOFTMAX_TOPK || gate == MOE_GATE_SOFTMAX_FULL) {
+    const float m = zr[chosen[0]];  // the first pick has the largest logit
+    if (lane < k) g = expf(zj - m);
+  } else if (lane < k) {
+    g = 1.0f / (1.0f + expf(-zj));  // float32 affinity (within 3e-7 relative of the rounded exact one)
+  }
+  float sum = g;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if (gate == MOE_GATE_SOFTMAX_FULL) sum = full_den;
+  if (lane < k) {
+    int cj = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j < k && lane == j) cj = chosen[j];
+    idx[(size_t)t * k + lane] = cj;
+    w[(size_t)t * k + lane] = g / sum;
   }
 }
 
@@ -326,8 +343,19 @@ int launch_router_topk(const float *partial, int S, int pstride, const float *lo
                        const float *sel_bias, int T, int N, int k, int gate, int32_t *idx, float *w, int *status,
                        cudaStream_t s) {
   if (T == 0) return MOE_OK;
-  router_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(partial, S, pstride, logit_bias, logits, sel_bias, T, N, k, gate,
-                                                 idx, w, status);
+  const dim3 grid((T + 7) / 8), block(256);
+  if (N <= 32)
+    router_topk_kernel<1><<<grid, block, 0, s>>>(partial, S, pstride, logit_bias, logits, sel_bias, T, N, k, gate, idx,
+                                                 w, status);
+  else if (N <= 64)
+    router_topk_kernel<2><<<grid, block, 0, s>>>(partial, S, pstride, logit_bias, logits, sel_bias, T, N, k, gate, idx,
+                                                 w, status);
+  else if (N <= 128)
+    router_topk_kernel<4><<<grid, block, 0, s>>>(partial, S, pstride, logit_bias, logits, sel_bias, T, N, k, gate, idx,
+                                                 w, status);
+  else
+    router_topk_kernel<8><<<grid, block, 0, s>>>(partial, S, pstride, logit_bias, logits, sel_bias, T, N, k, gate, idx,
+                                                 w, status);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -57,8 +57,10 @@ __device__ __forceinline__ void token_probs(const float *__restrict__ zr, int N,
 // sequence c / cps (sequences of L tokens, the last one possibly shorter); a
 // chunk past its sequence's end writes zeros.  The batch statistics use L = T.
 __global__ void __launch_bounds__(256) stats_partial_kernel(const float *__restrict__ logits, int T, int N, int gate,
-                                                            int L, int cps, float *__restrict__ partial) {
+                                                            int L, int cps, float *__restrict__ partial,
+                                                            int *ticket) {
   __shared__ float red[8][256];
+  if (ticket && blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float acc[8];
 #pragma unroll
@@ -86,53 +88,75 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(const float *__restr
   }
 }
 
-// One CTA of 1024 threads: four threads per expert each add every fourth chunk,
-// then the four partial sums are added in a fixed order.
+// ceil(N / 32) CTAs of 1024 threads: CTA b takes experts 32 b + lane; warp w adds
+// the chunks w, w + 32, .. of each (loads coalesced across the experts), then the
+// 32 warp sums are added in warp order.  The CTA that finishes last (a ticket
+// counter, cleared by stats_partial) forms the summary over all experts in a
+// fixed order from f, P and the counts: deterministic.
 __global__ void __launch_bounds__(1024) stats_final_kernel(const float *__restrict__ partial, int nchunks,
                                                            const int32_t *__restrict__ counts_routed,
                                                            const int32_t *__restrict__ counts_kept, int T, int N,
                                                            long long total, float *__restrict__ f,
-                                                           float *__restrict__ P, float *__restrict__ summary) {
-  __shared__ float quarter[4][256];
+                                                           float *__restrict__ P, float *__restrict__ summary,
+                                                           int *ticket) {
+  __shared__ float red[32][33];
   __shared__ float fp[256];
   __shared__ int maxc[256];
   __shared__ long long kept[256];
-  const int e = threadIdx.x & 255, q = threadIdx.x >> 8;
+  __shared__ bool last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 32 + lane;
   float s = 0.f;
   if (e < N)
-    for (int c = q; c < nchunks; c += 4) s += partial[(size_t)c * N + e];
-  quarter[q][e] = s;
+    for (int c = warp; c < nchunks; c += 32) s += partial[(size_t)c * N + e];
+  red[warp][lane] = s;
   __syncthreads();
-  if (q == 0) {
+  if (warp == 0 && e < N) {
+    float sum = 0.f;
+    for (int w = 0; w < 32; ++w) sum += red[w][lane];
+    P[e] = sum / (float)T;
+    f[e] = (float)((double)counts_routed[e] / (double)total);
+  }
+  if (gridDim.x > 1) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) last = atomicAdd(ticket, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+  } else {
+    __syncthreads();  // one CTA: it is the last
+  }
+  const int x = threadIdx.x;
+  if (x < 256) {
     float fe = 0.f, pe = 0.f;
     int ce = 0;
     long long ke = 0;
-    if (e < N) {
-      pe = (((quarter[0][e] + quarter[1][e]) + quarter[2][e]) + quarter[3][e]) / (float)T;
-      ce = counts_routed[e];
-      ke = counts_kept[e];
-      fe = (float)((double)ce / (double)total);
-      f[e] = fe;
-      P[e] = pe;
+    if (x < N) {
+      fe = __ldcg(f + x);
+      pe = __ldcg(P + x);
+      ce = counts_routed[x];
+      ke = counts_kept[x];
     }
-    fp[e] = fe * pe;
-    maxc[e] = ce;
-    kept[e] = ke;
+    fp[x] = fe * pe;
+    maxc[x] = ce;
+    kept[x] = ke;
   }
   __syncthreads();
   for (int off = 128; off > 0; off >>= 1) {
-    if (q == 0 && e < off) {
-      fp[e] += fp[e + off];
-      maxc[e] = max(maxc[e], maxc[e + off]);
-      kept[e] += kept[e + off];
+    if (x < off) {
+      fp[x] += fp[x + off];
+      maxc[x] = max(maxc[x], maxc[x + off]);
+      kept[x] += kept[x + off];
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
+  if (x == 0) {
     const double tk = (double)total;
     summary[0] = (float)N * fp[0];
     summary[1] = (float)((double)maxc[0] / (tk / (double)N));
     summary[2] = (float)(1.0 - (double)kept[0] / tk);
+    if (gridDim.x > 1) *ticket = 0;
   }
 }
 
@@ -294,11 +318,13 @@ int launch_bias_update(const int32_t *counts_routed, int T, int k, int N, float 
 }
 
 int launch_load_stats(const float *logits, const int32_t *counts_routed, const int32_t *counts_kept, int T, int N,
-                      long long total, int gate, float *partial, float *f, float *P, float *summary, cudaStream_t s) {
+                      long long total, int gate, float *partial, int *ticket, float *f, float *P, float *summary,
+                      cudaStream_t s) {
   if (T == 0) return MOE_OK;
   const int nchunks = (T + SC - 1) / SC;
-  stats_partial_kernel<<<nchunks, 256, 0, s>>>(logits, T, N, gate, T, nchunks, partial);
-  stats_final_kernel<<<1, 1024, 0, s>>>(partial, nchunks, counts_routed, counts_kept, T, N, total, f, P, summary);
+  stats_partial_kernel<<<nchunks, 256, 0, s>>>(logits, T, N, gate, T, nchunks, partial, ticket);
+  stats_final_kernel<<<(N + 31) / 32, 1024, 0, s>>>(partial, nchunks, counts_routed, counts_kept, T, N, total, f, P,
+                                                    summary, ticket);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -314,7 +340,7 @@ int launch_seq_balance_loss(const float *logits, const int32_t *topk_idx, int T,
   const int nseq = (int)(((long long)T + L - 1) / L);
   if (L >= SC) {
     const int cps = (L + SC - 1) / SC;
-    stats_partial_kernel<<<nseq * cps, 256, 0, s>>>(logits, T, N, gate, L, cps, partial);
+    stats_partial_kernel<<<nseq * cps, 256, 0, s>>>(logits, T, N, gate, L, cps, partial, nullptr);
     seq_final_kernel<<<nseq, 256, 0, s>>>(partial, cps, topk_idx, T, N, k, L, seq_loss, status);
   } else {
     seq_short_kernel<<<(nseq + 7) / 8, 256, 0, s>>>(logits, topk_idx, T, N, k, gate, L, nseq, seq_loss, status);
