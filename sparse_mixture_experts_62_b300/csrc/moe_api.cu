@@ -209,7 +209,7 @@ int ec_route(const moe_config *c, const Ws &w, const void *x, const float *Wg, c
 
 // ---------------------------------------------------------------- backward workspace
 struct BwdLayout {
-  size_t dgate, dz, dz2, dwg2, off_sh, dy, dh, dA, dxp;
+  size_t dgate, dz, dz2, dwg2, dzT3, wgT3, rterm, off_sh, dy, dh, dA, dxp;
   size_t dh_s, dA_s, dx_s, total;
 };
 
@@ -230,6 +230,10 @@ BwdLayout bwd_layout(const moe_config *c) {
   const size_t Np = (N + 3) / 4 * 4;
   L.dz2 = take(T * 2 * Np * 2);  // dz as bf16 [hi | lo]
   L.dwg2 = take(d * 2 * Np * 4);  // x^T [hi | lo]
+  const size_t Tp = (T + 7) / 8 * 8;
+  L.dzT3 = take(3 * Np * Tp * 2);  // dz^T [hi; lo; hi]
+  L.wgT3 = take(3 * Np * d * 2);   // W_g^T [hi; hi; lo]
+  L.rterm = take(T * d * 4);       // dz W_g^T
   L.off_sh = take(2 * 4);
   L.dy = take(R * d * 2);
   L.dh = take(R * F * 2);
@@ -573,7 +577,12 @@ int moe_layer_backward(const moe_config *cfg, const void *x, const float *Wg, co
     MOE_TRY(ffn_backward(cfg, true, 1, T, nullptr, off_sh, x, w.at<void>(FL.h_shared), dout, sw1, sw3, sw2,
                          cfg->shared_ffn, bws, L, dsw1, dsw3, dsw2, dx_sh, w.status(), s));
   }
-  return launch_dx_combine(bws + L.dxp, dest_row, dz, Wg, dx_sh, T, d, N, k, dx, s);
+  // x's router term dz W_g^T, then dx
+  const int Np = (N + 3) / 4 * 4, Tp = (T + 7) / 8 * 8;
+  float *rterm = reinterpret_cast<float *>(bws + L.rterm);
+  MOE_TRY(launch_split_router_term(dz, Wg, T, d, N, Np, Tp, bws + L.dzT3, bws + L.wgT3, s));
+  MOE_TRY(tc_wgrad_gemm(bws + L.dzT3, Tp, bws + L.wgT3, d, 3 * Np, nullptr, 1, T, d, rterm, w.status(), s));
+  return launch_dx_combine(bws + L.dxp, dest_row, rterm, dx_sh, T, d, k, dx, s);
 }
 
 int moe_check_wait_timeout(void *ws, int64_t limit_ns, void *stream) {

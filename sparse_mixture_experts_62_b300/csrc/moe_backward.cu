@@ -135,24 +135,75 @@ __global__ void dwg_sum_kernel(const float *__restrict__ part, int d, int N, int
 }
 
 // dx[t] = sum_j kept dx_perm[row_tj] + sum_e dz[t][e] Wg[:, e] (+ the shared expert's dx).
+// dx[t] = sum_j kept dx_perm[row_tj] + router term [t] (+ the shared expert's dx);
+// 8 columns per thread with 16-byte loads (d is a multiple of 8).
 __global__ void __launch_bounds__(256) dx_combine_kernel(const uint16_t *__restrict__ dxp,
                                                          const int32_t *__restrict__ dest_row,
-                                                         const float *__restrict__ dz, const float *__restrict__ Wg,
-                                                         const uint16_t *__restrict__ dx_sh, int T, int d, int N, int k,
+                                                         const float *__restrict__ rterm,
+                                                         const uint16_t *__restrict__ dx_sh, int T, int d, int k,
                                                          float *__restrict__ dx) {
   const int t = blockIdx.x;
   __shared__ int rows[8];
-  __shared__ float dzs[256];
   if (threadIdx.x < k) rows[threadIdx.x] = dest_row[(size_t)t * k + threadIdx.x];
-  for (int e = threadIdx.x; e < N; e += blockDim.x) dzs[e] = dz[(size_t)t * N + e];
   __syncthreads();
-  for (int c = threadIdx.x; c < d; c += blockDim.x) {
-    float acc = dx_sh ? __uint_as_float((uint32_t)dx_sh[(size_t)t * d + c] << 16) : 0.f;
-    for (int j = 0; j < k; ++j)
-      if (rows[j] >= 0) acc += __uint_as_float((uint32_t)dxp[(size_t)rows[j] * d + c] << 16);
-    const float *wr = Wg + (size_t)c * N;
-    for (int e = 0; e < N; ++e) acc = fmaf(dzs[e], wr[e], acc);
-    dx[(size_t)t * d + c] = acc;
+  for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    float acc[8];
+    const float4 r0 = *reinterpret_cast<const float4 *>(rterm + (size_t)t * d + c);
+    const float4 r1 = *reinterpret_cast<const float4 *>(rterm + (size_t)t * d + c + 4);
+    acc[0] = r0.x, acc[1] = r0.y, acc[2] = r0.z, acc[3] = r0.w, acc[4] = r1.x, acc[5] = r1.y, acc[6] = r1.z,
+    acc[7] = r1.w;
+    if (dx_sh) {
+      const uint4 q = *reinterpret_cast<const uint4 *>(dx_sh + (size_t)t * d + c);
+      const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += bf16_lo(v[i]);
+        acc[2 * i + 1] += bf16_hi(v[i]);
+      }
+    }
+    for (int j = 0; j < k; ++j) {
+      if (rows[j] < 0) continue;
+      const uint4 q = *reinterpret_cast<const uint4 *>(dxp + (size_t)rows[j] * d + c);
+      const uint32_t v[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] += bf16_lo(v[i]);
+        acc[2 * i + 1] += bf16_hi(v[i]);
+      }
+    }
+    *reinterpret_cast<float4 *>(dx + (size_t)t * d + c) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4 *>(dx + (size_t)t * d + c + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
+// The router term dz W_g^T as a weight-gradient GEMM over the experts: rows e,
+// Np + e, 2 Np + e of A = dz^T [hi; lo; hi] ([3 Np, Tp] bf16, zero past N and T)
+// and of B = W_g^T [hi; hi; lo] ([3 Np, d] bf16), so the sum over the rows gives
+// dz_hi W_hi + dz_lo W_hi + dz_hi W_lo (the lo x lo term is below 2^-16 relative).
+__global__ void split_dzT_kernel(const float *__restrict__ dz, int T, int N, int Np, int Tp,
+                                 uint16_t *__restrict__ out) {
+  const size_t n = (size_t)Np * Tp;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i / Tp), t = (int)(i % Tp);
+    const float v = (e < N && t < T) ? dz[(size_t)t * N + e] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    out[(size_t)e * Tp + t] = __bfloat16_as_ushort(hi);
+    out[(size_t)(Np + e) * Tp + t] = __bfloat16_as_ushort(lo);
+    out[(size_t)(2 * Np + e) * Tp + t] = __bfloat16_as_ushort(hi);
+  }
+}
+
+__global__ void split_wgT_kernel(const float *__restrict__ Wg, int d, int N, int Np, uint16_t *__restrict__ out) {
+  const size_t n = (size_t)Np * d;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i / d), c = (int)(i % d);
+    const float v = e < N ? Wg[(size_t)c * N + e] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+    out[(size_t)e * d + c] = __bfloat16_as_ushort(hi);
+    out[(size_t)(Np + e) * d + c] = __bfloat16_as_ushort(hi);
+    out[(size_t)(2 * Np + e) * d + c] = __bfloat16_as_ushort(lo);
   }
 }
 
@@ -209,11 +260,18 @@ int launch_dwg_sum(const float *part, int d, int N, int Np, float *dWg, cudaStre
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-int launch_dx_combine(const void *dxp, const int32_t *dest_row, const float *dz, const float *Wg, const void *dx_sh,
-                      int T, int d, int N, int k, float *dx, cudaStream_t s) {
+int launch_split_router_term(const float *dz, const float *Wg, int T, int d, int N, int Np, int Tp, void *dzT,
+                             void *wgT, cudaStream_t s) {
+  split_dzT_kernel<<<grid_for((size_t)Np * Tp, 256), 256, 0, s>>>(dz, T, N, Np, Tp, static_cast<uint16_t *>(dzT));
+  split_wgT_kernel<<<grid_for((size_t)Np * d, 256), 256, 0, s>>>(Wg, d, N, Np, static_cast<uint16_t *>(wgT));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_dx_combine(const void *dxp, const int32_t *dest_row, const float *rterm, const void *dx_sh, int T, int d,
+                      int k, float *dx, cudaStream_t s) {
   if (T == 0) return MOE_OK;
-  dx_combine_kernel<<<T, 256, 0, s>>>(static_cast<const uint16_t *>(dxp), dest_row, dz, Wg,
-                                      static_cast<const uint16_t *>(dx_sh), T, d, N, k, dx);
+  dx_combine_kernel<<<T, 256, 0, s>>>(static_cast<const uint16_t *>(dxp), dest_row, rterm,
+                                      static_cast<const uint16_t *>(dx_sh), T, d, k, dx);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

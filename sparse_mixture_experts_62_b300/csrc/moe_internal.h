@@ -82,8 +82,13 @@ int launch_router_bwd(const float *logits, const int32_t *idx, const float *topk
 // N rounded up to 4), one weight-gradient GEMM over all T rows, halves added.
 int launch_split_dz(const float *dz, int T, int N, int Np, void *out, cudaStream_t s);
 int launch_dwg_sum(const float *part, int d, int N, int Np, float *dWg, cudaStream_t s);
-int launch_dx_combine(const void *dxp, const int32_t *dest_row, const float *dz, const float *Wg, const void *dx_sh,
-                      int T, int d, int N, int k, float *dx, cudaStream_t s);
+// dz W_g^T on the tensor cores: dz^T and W_g^T split into bf16 [hi; lo; hi] and
+// [hi; hi; lo] row blocks (Np = N rounded up to 4, Tp = T rounded up to 8).
+int launch_split_router_term(const float *dz, const float *Wg, int T, int d, int N, int Np, int Tp, void *dzT,
+                             void *wgT, cudaStream_t s);
+// dx = router term + the kept rows of dx_perm (+ the shared expert's dx)
+int launch_dx_combine(const void *dxp, const int32_t *dest_row, const float *rterm, const void *dx_sh, int T, int d,
+                      int k, float *dx, cudaStream_t s);
 int launch_set_offsets2(int32_t *offsets, int rows, cudaStream_t s);
 
 // expert choice: scores + per-expert top-C selection
