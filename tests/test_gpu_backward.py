@@ -28,6 +28,7 @@ CASES = [
     dict(T=150, d=192, N=5, k=2, F=160, act="relu"),
     dict(T=1500, d=256, N=4, k=2, F=256),            # CTA-pair tiles in the GEMMs
     dict(T=512, d=1024, N=8, k=2, F=2048),
+    dict(T=2000, d=128, N=8, k=2, F=128, capacity_factor=1.25, zipf_s=1.2),  # pair tiles for the capped groups
 ]
 
 

@@ -71,6 +71,7 @@ SMALL = [
     dict(T=1500, d=256, N=4, k=2, F=384),                                  # CTA-pair tiles (750 rows/expert)
     dict(T=400, d=256, N=16, k=4, F=256, gate="softmax_full"),             # full softmax, no renormalisation
     dict(T=300, d=256, N=32, k=1, F=256, capacity_factor=1.0),             # Switch-style top-1 with capacity
+    dict(T=2000, d=256, N=8, k=2, F=256, capacity_factor=1.25, zipf_s=1.2),  # capacity: pair and single tiles
 ]
 
 
