@@ -516,6 +516,25 @@ def _expert_backward(xr, W1, W3, W2, dy, act):
     return da @ W1, da.T @ xr, None, dy.T @ h
 
 
+def _dz_row(z_t: np.ndarray, idx_t: np.ndarray, w_t: np.ndarray, g: np.ndarray, gate: str) -> np.ndarray:
+    """dL/dz of one token from the gradients g of its gate weights (0 on dropped slots)."""
+    N = z_t.shape[0]
+    dz = np.zeros(N)
+    if gate == "softmax":
+        dz[idx_t] = w_t * (g - np.sum(w_t * g))
+    elif gate == "softmax_full":
+        e_ = np.exp(z_t - z_t.max())
+        p = e_ / e_.sum()
+        gfull = np.zeros(N)
+        gfull[idx_t] = g
+        dz = p * (gfull - np.sum(p * gfull))
+    else:
+        s = 1.0 / (1.0 + np.exp(-z_t[idx_t]))
+        ds = (g - np.sum(w_t * g)) / s.sum()
+        dz[idx_t] = ds * s * (1.0 - s)
+    return dz
+
+
 def layer_backward(x64, beta, P: Params, act: str, gate: str, idx: np.ndarray, disp: Dispatch,
                    dout: np.ndarray) -> Grads:
     """Gradients of L = <dout, out> with the routing held fixed.
@@ -557,20 +576,7 @@ def layer_backward(x64, beta, P: Params, act: str, gate: str, idx: np.ndarray, d
     # through the gates into the logits
     dz = np.zeros((T, N))
     for t in range(T):
-        kept = disp.dest_row[t] >= 0
-        g = np.where(kept, dgate[t], 0.0)
-        if gate == "softmax":
-            dz[t, idx[t]] = w[t] * (g - np.sum(w[t] * g))
-        elif gate == "softmax_full":
-            e_ = np.exp(z[t] - z[t].max())
-            p = e_ / e_.sum()
-            gfull = np.zeros(N)
-            gfull[idx[t]] = g
-            dz[t] = p * (gfull - np.sum(p * gfull))
-        else:
-            s = 1.0 / (1.0 + np.exp(-z[t, idx[t]]))
-            ds = (g - np.sum(w[t] * g)) / s.sum()
-            dz[t, idx[t]] = ds * s * (1.0 - s)
+        dz[t] = _dz_row(z[t], idx[t], w[t], np.where(disp.dest_row[t] >= 0, dgate[t], 0.0), gate)
     dWg = x64.T @ dz
     dx += dz @ P.Wg.T
     gr = Grads(dx, dWg, dw1, dw3, dw2, dgate=dgate)
@@ -578,6 +584,87 @@ def layer_backward(x64, beta, P: Params, act: str, gate: str, idx: np.ndarray, d
         gx, gr.dsw1, gr.dsw3, gr.dsw2 = _expert_backward(x64, P.sw1, P.sw3, P.sw2, dout, act)
         gr.dx = gr.dx + gx
     return gr
+
+
+def _logits64(inp, rows: np.ndarray) -> np.ndarray:
+    x64 = widen(inp.x[rows], inp.wl.dtype)
+    z = x64 @ inp.Wg.astype(np.float64)
+    if inp.logit_bias is not None:
+        z = z + inp.logit_bias.astype(np.float64)[None, :]
+    return z
+
+
+def backward_dx_tokens(inp, idx: np.ndarray, disp: Dispatch, dout: np.ndarray, tokens: np.ndarray) -> np.ndarray:
+    """Rows `tokens` of layer_backward's dx, computed from those tokens alone (a
+    token's dx involves only its own experts, gates and logits), with one expert's
+    float64 weights in memory at a time: sampled gradient checks of full-size layers.
+    dout: float64 [T, d]."""
+    wl = inp.wl
+    dt = wl.dtype
+    tokens = np.asarray(tokens)
+    x64 = widen(inp.x[tokens], dt)
+    z = _logits64(inp, tokens)
+    idx_s = idx[tokens]
+    w = _gates64(z, idx_s, wl.gate)
+    dx = np.zeros_like(x64)
+    dgate = np.zeros(idx_s.shape)
+    kept = disp.dest_row[tokens] >= 0
+    for e in np.unique(idx_s):
+        ii, jj = np.nonzero((idx_s == e) & kept)
+        if ii.size == 0:
+            continue
+        W1, W2 = widen(inp.w1[e], dt), widen(inp.w2[e], dt)
+        W3 = widen(inp.w3[e], dt) if inp.w3 is not None else None
+        xr = x64[ii]
+        y = expert_ffn(xr, W1, W3, W2, wl.act)
+        dgate[ii, jj] = np.sum(dout[tokens[ii]] * y, axis=1)
+        gx = _expert_backward(xr, W1, W3, W2, w[ii, jj][:, None] * dout[tokens[ii]], wl.act)[0]
+        np.add.at(dx, ii, gx)
+    Wg64 = inp.Wg.astype(np.float64)
+    for i in range(tokens.size):
+        dx[i] += _dz_row(z[i], idx_s[i], w[i], np.where(kept[i], dgate[i], 0.0), wl.gate) @ Wg64.T
+    if wl.shared_F:
+        sw3 = widen(inp.sw3, dt) if inp.sw3 is not None else None
+        dx += _expert_backward(x64, widen(inp.sw1, dt), sw3, widen(inp.sw2, dt), dout[tokens], wl.act)[0]
+    return dx
+
+
+def backward_dw_entries(inp, idx: np.ndarray, disp: Dispatch, dout: np.ndarray, which: str,
+                        entries) -> np.ndarray:
+    """Entries (e, i, j) of layer_backward's dw1 / dw3 ([N, F, d]: i = hidden unit f,
+    j = input column) or dw2 ([N, d, F]: i = output column, j = f), each summed over
+    the kept rows of expert e from the columns it needs: sampled gradient checks of
+    full-size layers.  dout: float64 [T, d]."""
+    wl = inp.wl
+    dt = wl.dtype
+    out = np.zeros(len(entries))
+    for n, (e, i, j) in enumerate(entries):
+        toks, slots = np.nonzero((idx == e) & (disp.dest_row >= 0))   # row-major: token order
+        if toks.size == 0:
+            continue
+        xr = widen(inp.x[toks], dt)
+        w = _gates64(_logits64(inp, toks), idx[toks], wl.gate)[np.arange(toks.size), slots]
+        dy = w[:, None] * dout[toks]
+        f = i if which in ("w1", "w3") else j
+        a = xr @ widen(inp.w1[e][f], dt)
+        dh = dy @ widen(inp.w2[e][:, f], dt)
+        if wl.act == "swiglu":
+            u = xr @ widen(inp.w3[e][f], dt)
+            sig = 1.0 / (1.0 + np.exp(-a))
+            h = a * sig * u
+            da = dh * u * (sig * (1.0 + a * (1.0 - sig)))
+            du = dh * a * sig
+        else:
+            h = np.maximum(a, 0.0)
+            da = dh * (a > 0)
+            du = None
+        if which == "w2":
+            out[n] = np.sum(dy[:, i] * h)
+        elif which == "w1":
+            out[n] = np.sum(da * xr[:, j])
+        else:
+            out[n] = np.sum(du * xr[:, j])
+    return out
 
 
 def dense_mask_forward(inp, cap: Optional[int] = None) -> np.ndarray:

@@ -575,3 +575,31 @@ def test_sequence_balance_loss_pins():
     l1 = oracle.sequence_balance_loss(z[:50], idx[:50], "softmax", seq_len=50)
     l2 = oracle.sequence_balance_loss(z[50:], idx[50:], "softmax", seq_len=50)
     assert oracle.sequence_balance_loss(z, idx, "softmax", seq_len=50) == pytest.approx((l1 + l2) / 2, rel=1e-12)
+
+
+@pytest.mark.parametrize("kw", BWD_CASES)
+def test_sampled_backward_matches_full_backward(kw):
+    """The per-token dx and per-entry weight gradients used for sampled checks of
+    full-size layers equal the corresponding entries of the full backward (itself
+    pinned by central differences above)."""
+    kw = dict(kw)
+    N, k = kw.pop("N", 5), kw.pop("k", 2)
+    inp = tiny(T=40, d=16, N=N, k=k, F=24, **kw)
+    wl = inp.wl
+    ref = oracle.layer_forward(inp)
+    P = oracle.params64(inp)
+    rng = np.random.default_rng(23)
+    dout = rng.standard_normal((wl.T, wl.d))
+    g = oracle.layer_backward(oracle.widen(inp.x, wl.dtype), inp.logit_bias, P, wl.act, wl.gate, ref.idx, ref.disp,
+                              dout)
+    tokens = np.array([0, 3, 7, 8, 19, 39])
+    dx = oracle.backward_dx_tokens(inp, ref.idx, ref.disp, dout, tokens)
+    assert np.allclose(dx, g.dx[tokens], rtol=1e-10, atol=1e-12)
+    for which, full in (("w1", g.dw1), ("w3", g.dw3), ("w2", g.dw2)):
+        if full is None:
+            continue
+        entries = [(int(rng.integers(N)), int(rng.integers(full.shape[1])), int(rng.integers(full.shape[2])))
+                   for _ in range(12)]
+        got = oracle.backward_dw_entries(inp, ref.idx, ref.disp, dout, which, entries)
+        want = np.array([full[e, i, j] for e, i, j in entries])
+        assert np.allclose(got, want, rtol=1e-10, atol=1e-12), which
