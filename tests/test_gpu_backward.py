@@ -87,3 +87,48 @@ def test_backward_rejects_unsupported_configs():
     with pytest.raises(moe.MoeError) as e:
         moe.moe_backward_workspace_size(cfg)
     assert e.value.code == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_backward_mixtral_prefill_full_sampled():
+    """The backward at the Mixtral prefill size in the launch configuration the
+    bench times (CTA-pair tiles, pair weight-gradient GEMMs): dx on a seeded sample
+    of tokens and 16 seeded entries of each expert weight gradient against the
+    oracle's per-token / per-entry gradients, under the bf16 rule per tensor."""
+    wl = synth.WORKLOADS["mixtral_prefill"]
+    inp = synth.make_inputs(wl)
+    layer = layer_on_device(inp)
+    x = to_dev(inp.x, "bf16")
+    layer.forward(x)
+    cfg = layer.cfg
+    dout_np = synth.normal(wl.seed, 77, (wl.T, wl.d), 1.0, "bf16")
+    dout = to_dev(dout_np, "bf16")
+    f32 = lambda shape: torch.full(shape, float("nan"), device="cuda")  # noqa: E731
+    dx, dWg = f32((wl.T, wl.d)), f32((wl.d, wl.N))
+    dw1, dw3, dw2 = f32((wl.N, wl.F, wl.d)), f32((wl.N, wl.F, wl.d)), f32((wl.N, wl.d, wl.F))
+    bws = torch.zeros(moe.moe_backward_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    moe.moe_layer_backward(cfg, x, layer.Wg, layer.w1, layer.w3, layer.w2, None, None, None, dout, dx, dWg, dw1, dw3,
+                           dw2, None, None, None, layer.ws, bws)
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    v = layer.views()
+    own = oracle.layer_forward(inp, tokens=np.array([], dtype=np.int64))  # the oracle's routing
+    idx = v["topk_idx"].cpu().numpy()
+    same = check_routing(inp, v["logits"].cpu().numpy(), idx, v["topk_w"].cpu().numpy().astype(np.float64), own)
+    agree = check_layer_dispatch(wl, idx, same, v["counts_routed"].cpu().numpy(), v["counts_kept"].cpu().numpy(),
+                                 v["offsets"].cpu().numpy(), v["dest_row"].cpu().numpy(),
+                                 v["src_token"].cpu().numpy(), cfg.capacity, own)
+    assert np.all(agree), "the GPU routed a token differently from the oracle"
+    dout64 = oracle.widen(dout_np, "bf16")
+    rng = np.random.default_rng(wl.seed)
+    tokens = np.sort(rng.choice(wl.T, 24, replace=False))
+    ref_dx = oracle.backward_dx_tokens(inp, own.idx, own.disp, dout64, tokens)
+    got_dx = dx[torch.from_numpy(tokens).cuda()].cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got_dx))
+    assert_close_out(got_dx, ref_dx, "bf16", what="dx (sampled tokens)")
+    for which, t, shape in (("w1", dw1, (wl.N, wl.F, wl.d)), ("w3", dw3, (wl.N, wl.F, wl.d)),
+                            ("w2", dw2, (wl.N, wl.d, wl.F))):
+        entries = [(int(rng.integers(shape[0])), int(rng.integers(shape[1])), int(rng.integers(shape[2])))
+                   for _ in range(16)]
+        ref = oracle.backward_dw_entries(inp, own.idx, own.disp, dout64, which, entries)
+        got = np.array([float(t[e, i, j].item()) for e, i, j in entries])
+        assert_close_out(got, ref, "bf16", what=f"d{which} (sampled entries)")
