@@ -210,14 +210,26 @@ def max_over_ranks(dist, v: float) -> float:
 
 # ----------------------------------------------------------------------------- reference arm
 def run_reference(args, wl):
-    """The CPU oracle, as it stands, on a bounded sample of the same workload per step."""
+    """The CPU oracle, as it stands, on a bounded sample of the same workload per step.
+
+    Without a capacity limit every token is routed and processed on its own, so a
+    step is the oracle's layer on `--ref-sample` seeded tokens taken as a layer of
+    their own (routing, gate, their experts, combine, statistics); with a capacity
+    limit the routing and dispatch of all tokens come first, then the experts on
+    the sampled tokens, extrapolated to all tokens."""
+    import dataclasses
     import oracle
     inp = synth.make_inputs(wl)
-    sample = args.ref_sample
+    sample = min(args.ref_sample, wl.T)
     rng = np.random.default_rng(wl.seed)
 
     def step():
-        toks = np.sort(rng.choice(wl.T, size=min(sample, wl.T), replace=False))
+        toks = np.sort(rng.choice(wl.T, size=sample, replace=False))
+        if wl.capacity_factor <= 0:
+            sub = dataclasses.replace(inp, wl=wl.scaled(T=sample), x=inp.x[toks])
+            t0 = time.perf_counter()
+            oracle.layer_forward(sub)
+            return (time.perf_counter() - t0) * wl.T / sample                # seconds per full layer
         t0 = time.perf_counter()
         oracle.layer_forward(inp, tokens=np.array([], dtype=np.int64))      # routing + dispatch + stats, all T
         t1 = time.perf_counter()
@@ -232,8 +244,13 @@ def run_reference(args, wl):
     per_step = float(np.mean(secs))
     cores = blas_threads()
     value = wl.T / per_step
-    desc = (f"oracle (numpy float64): routing, dispatch and statistics on all {wl.T} tokens, expert FFN on "
-            f"{min(sample, wl.T)} sampled tokens per step, extrapolated linearly to {wl.T} tokens")
+    if wl.capacity_factor <= 0:
+        desc = (f"oracle (numpy float64): each step the whole layer on {sample} seeded token(s) taken as a layer "
+                f"of their own (tokens are independent without a capacity limit), including the float64 widening "
+                f"of each touched expert's weights, scaled to {wl.T} tokens")
+    else:
+        desc = (f"oracle (numpy float64): routing, dispatch and statistics on all {wl.T} tokens, expert FFN on "
+                f"{sample} sampled tokens per step, extrapolated linearly to {wl.T} tokens")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -365,12 +382,15 @@ def run_ours(args, wl, dist, rank, local):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         start.record(stream)
         for k in range(args.steps):
             run()
+            marks[k].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
+    step_ms = [start.elapsed_time(marks[0])] + [marks[k - 1].elapsed_time(marks[k]) for k in range(1, args.steps)]
     if dist is not None:
         dist.barrier()
     if layer.device_status() != 0:
@@ -487,6 +507,8 @@ def run_ours(args, wl, dist, rank, local):
         sys.stderr.write("per-stage ms: " + json.dumps({k: round(val, 4) for k, val in stage_ms.items()}) + "\n")
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "step_ms": {"p10": float(np.percentile(step_ms, 10)), "p50": float(np.percentile(step_ms, 50)),
+                            "p90": float(np.percentile(step_ms, 90))},
                 "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
                 "config": {**config_of(wl), "launch": "cuda_graph" if graph is not None else "eager"},
                 "roofline": roof,
@@ -554,9 +576,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-baseline-tokens", type=int, default=16,
+    ap.add_argument("--cpu-baseline-tokens", type=int, default=512,
                     help="tokens the oracle runs the expert FFN on for cpu_baseline (0 = skip)")
-    ap.add_argument("--ref-sample", type=int, default=4, help="tokens per reference-arm step")
+    ap.add_argument("--ref-sample", type=int, default=1, help="tokens per reference-arm step")
     ap.add_argument("--override", nargs="*", default=[], help="workload fields to change, e.g. N=32 T=1024")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA-graph replay")
     ap.add_argument("--backward", action="store_true", help="also time the backward step (bf16 token choice)")
