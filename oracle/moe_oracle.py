@@ -667,6 +667,91 @@ def backward_dw_entries(inp, idx: np.ndarray, disp: Dispatch, dout: np.ndarray, 
     return out
 
 
+# --------------------------------------------------------------------------- FP8 expert weights
+# Quantisation of the experts is an open question on the pages ("Stanford CS336
+# lecture 4", the section on compressing sparse MoEs: quantisation lowers the
+# bits per weight at the cost of scales and a dequantisation step; the Q&A finds a
+# heavily quantised Mixtral 8x7B practical on one GPU).  The plainest reading is
+# taken: weight-only FP8 E4M3 with one float32 scale per output row (channel),
+# activations and accumulation unchanged.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_value(code: np.ndarray) -> np.ndarray:
+    """Value of FP8 E4M3 codes (OCP 8-bit floating point: sign, 4 exponent bits with
+    bias 7, 3 mantissa bits; exponent 0 is subnormal, m/8 * 2^-6; no infinities;
+    S.1111.111 is NaN, so the largest finite value is 1.75 * 2^8 = 448)."""
+    c = np.asarray(code, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = c & 7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+_E4M3_POS = e4m3_value(np.arange(0, 0x7F))   # codes 0 .. 126: 0 .. 448, increasing
+
+
+def e4m3_round(v: np.ndarray) -> np.ndarray:
+    """float32 values -> E4M3 codes: round to the nearest representable value, ties to
+    the even code (mantissa LSB 0), magnitudes above 448 saturated to 448; -0 keeps
+    its sign.  The rounding decision is taken on the float32 value."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    neg = np.signbit(np.asarray(v, dtype=np.float32))
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 126)   # first value >= a
+    lo = np.clip(hi - 1, 0, 126)
+    dl, dh = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    pick_hi = (dh < dl) | ((dh == dl) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(a >= _E4M3_POS[126], 126, code)
+    code = np.where(a == _E4M3_POS[hi], hi, code)
+    return (code | np.where(neg, 0x80, 0)).astype(np.uint8)
+
+
+def quantize_fp8_rows(w: np.ndarray):
+    """One scale per row: s = fl32(max |w| / 448) (1 for an all-zero row), codes =
+    E4M3 rounding of fl32(w / s).  w: [..., C] float32 (bf16 values widened).
+    Returns (codes uint8 [..., C], scales float32 [...])."""
+    w32 = np.asarray(w, dtype=np.float32)
+    amax = np.max(np.abs(w32), axis=-1)
+    s = np.where(amax > 0, (amax / np.float32(E4M3_MAX)).astype(np.float32), np.float32(1.0)).astype(np.float32)
+    q = e4m3_round((w32 / s[..., None]).astype(np.float32))
+    return q, s
+
+
+def dequantize_fp8_rows(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """float64 weights q * s (exact: 4 significant bits times a float32)."""
+    return e4m3_value(q) * np.asarray(s, dtype=np.float64)[..., None]
+
+
+def layer_forward_fp8(inp, q1, s1, q3, s3, q2, s2, tokens: Optional[np.ndarray] = None) -> LayerResult:
+    """The layer of layer_forward with the expert weights replaced by their FP8
+    dequantisation (the router, the shared expert and the activations unchanged);
+    outputs for `tokens` (default: all)."""
+    wl = inp.wl
+    dt = wl.dtype
+    ref = layer_forward(inp, tokens=np.array([], dtype=np.int64))
+    x64 = widen(inp.x, dt)
+    rows = np.arange(wl.T) if tokens is None else np.asarray(tokens)
+    out = np.full((wl.T, wl.d), np.nan)
+    out[rows] = 0.0
+    if wl.shared_F:
+        sw3 = widen(inp.sw3, dt) if inp.sw3 is not None else None
+        out[rows] += expert_ffn(x64[rows], widen(inp.sw1, dt), sw3, widen(inp.sw2, dt), wl.act)
+    want = np.zeros(wl.T, dtype=bool)
+    want[rows] = True
+    for e in range(wl.N):
+        tt, jj = np.nonzero((ref.idx == e) & (ref.disp.dest_row >= 0) & want[:, None])
+        if tt.size == 0:
+            continue
+        W3 = dequantize_fp8_rows(q3[e], s3[e]) if q3 is not None else None
+        y = expert_ffn(x64[tt], dequantize_fp8_rows(q1[e], s1[e]), W3, dequantize_fp8_rows(q2[e], s2[e]), wl.act)
+        np.add.at(out, tt, ref.w[tt, jj][:, None] * y)
+    return dataclasses.replace(ref, out=out)
+
+
 def dense_mask_forward(inp, cap: Optional[int] = None) -> np.ndarray:
     """Second formulation, with no permutation: y[t] = y_sh[t] + sum_e G[t,e] FFN_e(x_t).
 

@@ -603,3 +603,77 @@ def test_sampled_backward_matches_full_backward(kw):
         got = oracle.backward_dw_entries(inp, ref.idx, ref.disp, dout, which, entries)
         want = np.array([full[e, i, j] for e, i, j in entries])
         assert np.allclose(got, want, rtol=1e-10, atol=1e-12), which
+
+
+# --------------------------------------------------------------------------- FP8 expert weights
+def test_e4m3_codes_round_trip_and_known_values():
+    """OCP FP8 E4M3: every finite code decodes and encodes back to itself; a few
+    values worked by hand from the format (bias 7, 3 mantissa bits, max 448)."""
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    assert np.array_equal(oracle.e4m3_round(oracle.e4m3_value(codes).astype(np.float32)), codes.astype(np.uint8))
+    cases = {1.0: 0x38, 448.0: 0x7E, 500.0: 0x7E, 1e9: 0x7E, -448.0: 0xFE, 2.0 ** -9: 0x01, 2.0 ** -6: 0x08,
+             0.0: 0x00, 1.5: 0x3C, 240.0: 0x77, 0.875 * 2.0 ** -6: 0x07}
+    for v, c in cases.items():
+        assert oracle.e4m3_round(np.float32(v)) == c, (v, hex(c))
+    assert oracle.e4m3_round(np.float32(-0.0)) == 0x80
+    assert np.isnan(oracle.e4m3_value(0x7F)) and oracle.e4m3_value(0x7E) == 448.0
+
+
+def test_e4m3_rounding_is_nearest_with_ties_to_even():
+    """Midpoints of adjacent codes go to the even code, anything off the midpoint to
+    the nearer value; brute force over all codes and random values."""
+    vals = oracle.e4m3_value(np.arange(0, 0x7F))
+    for c in range(0, 0x7E):
+        mid = (vals[c] + vals[c + 1]) / 2
+        if np.float32(mid) != mid:
+            continue
+        want = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_round(np.float32(mid)) == want
+        assert oracle.e4m3_round(np.nextafter(np.float32(mid), np.float32(0))) == c
+        assert oracle.e4m3_round(np.nextafter(np.float32(mid), np.float32(1e9))) == c + 1
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal(20000) * rng.choice([1e-3, 1e-1, 10.0, 300.0], 20000)).astype(np.float32)
+    got = oracle.e4m3_value(oracle.e4m3_round(v))
+    allv = oracle.e4m3_value(np.arange(256))
+    finite = allv[np.isfinite(allv)]
+    best = np.min(np.abs(finite[None, :] - np.clip(v, -448, 448).astype(np.float64)[:, None]), axis=1)
+    assert np.allclose(np.abs(got - np.clip(v, -448, 448)), best, rtol=0, atol=1e-12)
+
+
+def test_fp8_row_quantisation():
+    """The largest magnitude of each row maps to +-448; the dequantised weights are
+    within half an E4M3 step (2^-4 relative) of the originals for normal values; a
+    zero row gets scale 1 and zero codes; weights that are already E4M3 values times
+    a scale round-trip exactly, so the FP8 layer then equals the bf16 layer."""
+    rng = np.random.default_rng(4)
+    w = (rng.standard_normal((6, 40)) * 0.02).astype(np.float32)
+    w[2] = 0.0
+    q, s = oracle.quantize_fp8_rows(w)
+    assert q.dtype == np.uint8 and s.dtype == np.float32
+    nz = [0, 1, 3, 4, 5]
+    assert np.all(np.max(np.abs(oracle.e4m3_value(q[nz])), axis=1) == 448.0)
+    assert s[2] == 1.0 and np.all(q[2] == 0)
+    deq = oracle.dequantize_fp8_rows(q, s)
+    normal = np.abs(w) >= (2.0 ** -6) * s[:, None]
+    assert np.all(np.abs(deq - w)[normal] <= 2.0 ** -4 * np.abs(w)[normal] + 1e-12)
+    # layer: bf16 weights that are E4M3 values times per-row scales
+    inp = tiny(T=12, d=16, N=4, k=2, F=24)
+    wl = inp.wl
+
+    def exact_fp8_bf16(shape, seed):
+        r = np.random.default_rng(seed)
+        codes = r.integers(0, 0x7E, size=shape)
+        codes[..., 0] = 0x7E                                   # every row reaches 448
+        codes = codes | np.where(r.random(shape) < 0.5, 0x80, 0)
+        scale = 2.0 ** r.integers(-12, -6, size=shape[:-1])    # powers of two: products stay in bf16
+        vals = (oracle.e4m3_value(codes) * scale[..., None]).astype(np.float32)
+        return (vals.view(np.uint32) >> 16).astype(np.uint16)  # exact: at most 4 significant bits
+    import dataclasses as dc
+    inp = dc.replace(inp, w1=exact_fp8_bf16(inp.w1.shape, 1), w3=exact_fp8_bf16(inp.w3.shape, 2),
+                     w2=exact_fp8_bf16(inp.w2.shape, 3))
+    qs = [oracle.quantize_fp8_rows(oracle.widen(w_, "bf16")) for w_ in (inp.w1, inp.w3, inp.w2)]
+    for w_, (q_, s_) in zip((inp.w1, inp.w3, inp.w2), qs):
+        assert np.array_equal(oracle.dequantize_fp8_rows(q_, s_), oracle.widen(w_, "bf16"))
+    ref = oracle.layer_forward(inp)
+    f8 = oracle.layer_forward_fp8(inp, qs[0][0], qs[0][1], qs[1][0], qs[1][1], qs[2][0], qs[2][1])
+    assert np.allclose(f8.out, ref.out, rtol=0, atol=1e-12)
