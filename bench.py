@@ -44,11 +44,20 @@ def layer_flops(wl, kept_rows: int) -> dict:
     return {"router": router, "expert_ffn": ffn, "shared_ffn": shared, "total": router + ffn + shared}
 
 
-def layer_bytes(wl, touched_experts: int) -> float:
+def expert_weight_bytes(wl, fp8: bool) -> float:
+    """Bytes of one expert's weights: 2 (bf16) / 4 (float32) per weight, or 1 per E4M3
+    code plus a float32 scale per row (W1, W3: F rows; W2: d rows)."""
+    mats = 3 if wl.act == "swiglu" else 2
+    if fp8:
+        return float(mats * wl.d * wl.F + ((mats - 1) * wl.F + wl.d) * 4)
+    return float(mats * wl.d * wl.F * (2 if wl.dtype == "bf16" else 4))
+
+
+def layer_bytes(wl, touched_experts: int, fp8: bool = False) -> float:
     """Algorithmic bytes: weights of experts with kept rows, x once, out once, W_g."""
     es = 2 if wl.dtype == "bf16" else 4
     mats = 3 if wl.act == "swiglu" else 2
-    w = touched_experts * mats * wl.d * wl.F * es
+    w = touched_experts * expert_weight_bytes(wl, fp8)
     sw = mats * wl.d * wl.shared_F * es if wl.shared_F else 0
     return float(w + sw + 2 * wl.T * wl.d * es + wl.d * wl.N * 4)
 
@@ -60,7 +69,7 @@ NCU_TRAFFIC = {"mixtral_prefill": {"bytes": 3.819e9, "kernel_rev": "pair1"}}
 KERNEL_REV = "pair1"
 
 
-def stage_work(wl, kept_rows: int, touched: int) -> dict:
+def stage_work(wl, kept_rows: int, touched: int, fp8: bool = False) -> dict:
     """Algorithmic (flops, bytes) per stage of one layer step.
 
     route: x read once, W_g, logits written, top-k ids + weights written;
@@ -75,7 +84,7 @@ def stage_work(wl, kept_rows: int, touched: int) -> dict:
     w = {
         "route": (2.0 * T * d * N, T * d * es + d * N * 4 + T * N * 4 + T * k * 8),
         "dispatch": (0.0, T * k * 4 + T * d * es + S * d * es + T * k * 4 + S * 4 + 3 * N * 4),
-        "expert_ffn": (2.0 * S * d * F * mats, touched * mats * d * F * es + 2 * S * d * es),
+        "expert_ffn": (2.0 * S * d * F * mats, touched * expert_weight_bytes(wl, fp8) + 2 * S * d * es),
         "combine": (0.0, S * d * es + T * d * es + T * k * 8 + (T * d * es if wl.shared_F else 0)),
         "load_stats": (0.0, T * N * 4 + 2 * N * 4),
     }
@@ -316,6 +325,11 @@ def run_ours(args, wl, dist, rank, local):
     inp = synth.make_inputs(wl)
     to_dev = _to_dev
     layer = build_layer(moe, inp)
+    if args.fp8:  # weights quantised once, outside the timed region (like any weight packing)
+        if wl.dtype != "bf16":
+            raise SystemExit("--fp8 needs a bf16 workload")
+        layer.quantize_fp8()
+        torch.cuda.synchronize()
     x = to_dev(inp.x, wl.dtype)
     out = torch.empty((wl.T, wl.d), dtype=x.dtype, device="cuda")
     cfg, ws, v = layer.cfg, layer.ws, layer.views()
@@ -337,7 +351,10 @@ def run_ours(args, wl, dist, rank, local):
         moe.moe_dispatch(cfg, v["topk_idx"], x, v["counts_routed"], v["counts_kept"], v["offsets"], v["dest_row"],
                          v["src_token"], v["x_perm"], ws, s)
         rec(2)
-        moe.moe_expert_ffn(cfg, v["x_perm"], v["offsets"], layer.w1, layer.w3, layer.w2, v["y_perm"], ws, s)
+        if layer.fp8 is not None:
+            moe.moe_expert_ffn_fp8(cfg, v["x_perm"], v["offsets"], *layer.fp8, v["y_perm"], ws, s)
+        else:
+            moe.moe_expert_ffn(cfg, v["x_perm"], v["offsets"], layer.w1, layer.w3, layer.w2, v["y_perm"], ws, s)
         i = 3
         if has_shared:
             rec(i)
@@ -414,14 +431,16 @@ def run_ours(args, wl, dist, rank, local):
     peaks, peak_src = measured_peaks()
     clocks = clk.summary()
     sustained = "sw_power_cap" in clocks.get("reasons", [])
-    work = stage_work(wl, kept_rows, touched)
+    work = stage_work(wl, kept_rows, touched, args.fp8)
     f32 = wl.dtype == "f32"
     stages = {n: stage_roofline(work[n][0], work[n][1], stage_ms[n], peaks, sustained,
                                 alu=f32 and n in ("route", "expert_ffn", "shared_ffn")) for n in stages}
     ffn = stages["expert_ffn"]
     roof = {"bound": ffn["bound"], "achieved": ffn["achieved"], "peak": ffn["peak"], "unit": ffn["unit"],
-            "frac": ffn["frac"], "traffic": _traffic(wl.name),
-            "kernel": "grouped_gemm (tcgen05), moe_expert_ffn: gate/up + down launches",
+            "frac": ffn["frac"], "traffic": None if args.fp8 else _traffic(wl.name),
+            "kernel": ("grouped_gemm_fp8 (tcgen05, E4M3 weights converted in shared memory), moe_expert_ffn_fp8: "
+                       "gate/up + down launches" if args.fp8 else
+                       "grouped_gemm (tcgen05), moe_expert_ffn: gate/up + down launches"),
             "peak_source": ("derived float32 CUDA-core peak (148 SMs x 128 lanes x 2 FLOP x 2032 MHz)"
                             if ffn["bound"] == "alu" else f"{peak_src} " + ("hbm_gbs" if ffn["bound"] == "hbm" else
                             ("bf16_tflops_sustained (power cap seen in the timed region)" if sustained
@@ -510,12 +529,13 @@ def run_ours(args, wl, dist, rank, local):
                 "step_ms": {"p10": float(np.percentile(step_ms, 10)), "p50": float(np.percentile(step_ms, 50)),
                             "p90": float(np.percentile(step_ms, 90))},
                 "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-                "config": {**config_of(wl), "launch": "cuda_graph" if graph is not None else "eager"},
+                "config": {**config_of(wl), "launch": "cuda_graph" if graph is not None else "eager",
+                           **({"expert_weights": "fp8 e4m3, one float32 scale per row"} if args.fp8 else {})},
                 "roofline": roof,
                 "stages": stages,
                 "layer": {"flops": fl["total"], "tflops": fl["total"] / (ms_per_step / 1e3) / 1e12,
                           "kept_rows": kept_rows, "touched_experts": touched,
-                          "algorithmic_bytes": layer_bytes(wl, touched)},
+                          "algorithmic_bytes": layer_bytes(wl, touched, args.fp8)},
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
                 "gpu_launches": launches_per_step * args.steps,
                 **({"backward": bwd} if bwd is not None else {}),
@@ -582,6 +602,7 @@ def main():
     ap.add_argument("--override", nargs="*", default=[], help="workload fields to change, e.g. N=32 T=1024")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA-graph replay")
     ap.add_argument("--backward", action="store_true", help="also time the backward step (bf16 token choice)")
+    ap.add_argument("--fp8", action="store_true", help="FP8 E4M3 expert weights with per-row scales (bf16 workloads)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

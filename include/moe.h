@@ -283,6 +283,30 @@ MOE_API int moe_seq_balance_loss(const moe_config *cfg, const float *logits, con
 MOE_API int moe_bias_update(const moe_config *cfg, const int32_t *counts_routed, float *sel_bias, float gamma,
                             void *stream);
 
+/* FP8 expert weights ("Stanford CS336 lecture 4", the section on compressing
+ * sparse MoEs: quantisation lowers the bytes per weight at the cost of scales and
+ * a dequantisation step; the pages leave the scheme open).  Weight-only OCP FP8
+ * E4M3 with one float32 scale per row of a weight matrix (its output channel):
+ * scales[r] = max_c |w[r, c]| / 448 (1 for an all-zero row), q[r, c] = E4M3 of
+ * w[r, c] / scales[r], rounded to nearest even and saturated to +-448.
+ * moe_quantize_fp8: w [rows, cols] bf16 device -> q [rows, cols] bytes and scales
+ * [rows] float32 device; quantise w1 and w3 as [N * F, d], w2 as [N * d, F]. */
+MOE_API int moe_quantize_fp8(const void *w, int64_t rows, int32_t cols, uint8_t *q, float *scales, void *stream);
+
+/* moe_expert_ffn / moe_layer_forward with FP8 expert weights: w1q, w3q [N, F, d]
+ * and w2q [N, d, F] E4M3 codes (16-byte aligned), w1s, w3s [N, F] and w2s [N, d]
+ * their row scales; the result is the layer whose expert weights are q * s
+ * (activations, router, shared expert and accumulation as in the bf16 layer).
+ * bf16 configs with d and ffn multiples of 16 (else MOE_ERR_UNSUPPORTED); token or
+ * expert choice; the shared expert (sw1, sw3, sw2) stays bf16. */
+MOE_API int moe_expert_ffn_fp8(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const uint8_t *w1q,
+                               const float *w1s, const uint8_t *w3q, const float *w3s, const uint8_t *w2q,
+                               const float *w2s, void *y_perm, void *ws, void *stream);
+MOE_API int moe_layer_forward_fp8(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias,
+                                  const float *sel_bias, const uint8_t *w1q, const float *w1s, const uint8_t *w3q,
+                                  const float *w3s, const uint8_t *w2q, const float *w2s, const void *sw1,
+                                  const void *sw3, const void *sw2, void *out, void *ws, void *stream);
+
 /* Synchronises `stream`, reads and clears the workspace status word, and
  * writes the first device-side error code found (MOE_OK if none) to *status.
  * Returns MOE_ERR_CUDA if the stream itself reports an error. */

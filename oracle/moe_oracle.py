@@ -41,7 +41,9 @@ Readings where the pages leave a step open (each is listed in the design notes):
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
 from fractions import Fraction
 from typing import Optional
 
@@ -678,7 +680,7 @@ def backward_dw_entries(inp, idx: np.ndarray, disp: Dispatch, dout: np.ndarray, 
 E4M3_MAX = 448.0
 
 
-def e4m3_value(code: np.ndarray) -> np.ndarray:
+def _e4m3_value_def(code: np.ndarray) -> np.ndarray:
     """Value of FP8 E4M3 codes (OCP 8-bit floating point: sign, 4 exponent bits with
     bias 7, 3 mantissa bits; exponent 0 is subnormal, m/8 * 2^-6; no infinities;
     S.1111.111 is NaN, so the largest finite value is 1.75 * 2^8 = 448)."""
@@ -691,23 +693,32 @@ def e4m3_value(code: np.ndarray) -> np.ndarray:
     return sign * mag
 
 
-_E4M3_POS = e4m3_value(np.arange(0, 0x7F))   # codes 0 .. 126: 0 .. 448, increasing
+_E4M3_TABLE = _e4m3_value_def(np.arange(256))
+
+
+def e4m3_value(code: np.ndarray) -> np.ndarray:
+    """Value of FP8 E4M3 codes (the definition above, tabulated for all 256 codes)."""
+    return _E4M3_TABLE[np.asarray(code, dtype=np.int64)]
 
 
 def e4m3_round(v: np.ndarray) -> np.ndarray:
     """float32 values -> E4M3 codes: round to the nearest representable value, ties to
-    the even code (mantissa LSB 0), magnitudes above 448 saturated to 448; -0 keeps
-    its sign.  The rounding decision is taken on the float32 value."""
-    a = np.abs(np.asarray(v, dtype=np.float64))
-    neg = np.signbit(np.asarray(v, dtype=np.float32))
-    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 126)   # first value >= a
-    lo = np.clip(hi - 1, 0, 126)
-    dl, dh = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
-    pick_hi = (dh < dl) | ((dh == dl) & (hi % 2 == 0))
-    code = np.where(pick_hi, hi, lo)
-    code = np.where(a >= _E4M3_POS[126], 126, code)
-    code = np.where(a == _E4M3_POS[hi], hi, code)
-    return (code | np.where(neg, 0x80, 0)).astype(np.uint8)
+    even (rint), magnitudes above 448 saturated to 448; -0 keeps its sign.  The
+    grid: in the binade [2^e, 2^(e+1)) with e >= -6 the values are 2^e (1 + m/8),
+    spaced 2^(e-3); below 2^-6 (subnormal) they are spaced 2^-9.  The rounding
+    decision is taken on the float32 value."""
+    v32 = np.asarray(v, dtype=np.float32)
+    a = np.abs(v32.astype(np.float64))
+    _, ex = np.frexp(a)                                  # a = f 2^ex with f in [0.5, 1): binade 2^(ex - 1)
+    quantum = np.ldexp(1.0, np.maximum(ex - 1, -6) - 3)  # 2^(e - 3), e = max(binade exponent, -6)
+    r = np.minimum(np.rint(a / quantum) * quantum, 448.0)  # exact: division by a power of two
+    # encode the rounded value (a carry into the next binade is already in r)
+    _, er = np.frexp(r)
+    eb = np.maximum(er - 1, -6)                          # binade exponent of r (subnormals: -6)
+    normal = r >= 2.0 ** -6
+    mant = np.where(normal, r / np.ldexp(1.0, eb - 3) - 8.0, r / 2.0 ** -9)
+    code = np.where(normal, ((eb + 7) << 3) + mant.astype(np.int64), mant.astype(np.int64))
+    return (code | np.where(np.signbit(v32), 0x80, 0)).astype(np.uint8)
 
 
 def quantize_fp8_rows(w: np.ndarray):
@@ -717,8 +728,21 @@ def quantize_fp8_rows(w: np.ndarray):
     w32 = np.asarray(w, dtype=np.float32)
     amax = np.max(np.abs(w32), axis=-1)
     s = np.where(amax > 0, (amax / np.float32(E4M3_MAX)).astype(np.float32), np.float32(1.0)).astype(np.float32)
-    q = e4m3_round((w32 / s[..., None]).astype(np.float32))
-    return q, s
+    # rows are independent: large matrices are rounded in row blocks on all cores
+    flat_w, flat_s = w32.reshape(-1, w32.shape[-1]), s.reshape(-1)
+    q = np.empty(flat_w.shape, dtype=np.uint8)
+
+    def block(r0):
+        r1 = min(r0 + 256, flat_w.shape[0])
+        q[r0:r1] = e4m3_round((flat_w[r0:r1] / flat_s[r0:r1, None]).astype(np.float32))
+    starts = range(0, flat_w.shape[0], 256)
+    if flat_w.size > (1 << 22):
+        with concurrent.futures.ThreadPoolExecutor(max_workers=os.cpu_count() or 1) as pool:
+            list(pool.map(block, starts))
+    else:
+        for r0 in starts:
+            block(r0)
+    return q.reshape(w32.shape), s
 
 
 def dequantize_fp8_rows(q: np.ndarray, s: np.ndarray) -> np.ndarray:

@@ -31,7 +31,8 @@ EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_works
            "moe_dispatch", "moe_expert_ffn", "moe_shared_ffn", "moe_combine", "moe_layer_forward",
            "moe_load_stats", "moe_get_device_status", "moe_dispatch_noalloc", "moe_check_wait_timeout",
            "moe_router_zloss", "moe_bias_update", "moe_ec_route", "moe_seq_balance_loss",
-           "moe_backward_workspace_size", "moe_layer_backward")
+           "moe_backward_workspace_size", "moe_layer_backward", "moe_quantize_fp8", "moe_expert_ffn_fp8",
+           "moe_layer_forward_fp8")
 
 
 class MoeConfig(ctypes.Structure):
@@ -79,6 +80,9 @@ def _load():
         "moe_backward_workspace_size": [C, ctypes.POINTER(ctypes.c_size_t)],
         "moe_layer_backward": [C] + [P] * 20,
         "moe_bias_update": [C, P, P, ctypes.c_float, P],
+        "moe_quantize_fp8": [P, ctypes.c_int64, ctypes.c_int32, P, P, P],
+        "moe_expert_ffn_fp8": [C] + [P] * 11,
+        "moe_layer_forward_fp8": [C] + [P] * 16,
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -216,6 +220,27 @@ def moe_router_zloss(cfg, logits, z_loss, ws, stream=None):
 def moe_seq_balance_loss(cfg, logits, topk_idx, seq_len: int, loss, ws, stream=None):
     _check(_lib.moe_seq_balance_loss(ctypes.byref(cfg), _ptr(logits), _ptr(topk_idx), int(seq_len), _ptr(loss),
                                      _ptr(ws), _stream(stream)), "moe_seq_balance_loss")
+
+
+def moe_quantize_fp8(w, q, scales, stream=None):
+    """w [..., cols] bf16 (device) -> q [..., cols] uint8 E4M3 codes, scales [...] float32, one per row."""
+    cols = int(w.shape[-1])
+    rows = int(w.numel() // cols) if cols else 0
+    _check(_lib.moe_quantize_fp8(_ptr(w), rows, cols, _ptr(q), _ptr(scales), _stream(stream)), "moe_quantize_fp8")
+
+
+def moe_expert_ffn_fp8(cfg, x_perm, offsets, w1q, w1s, w3q, w3s, w2q, w2s, y_perm, ws, stream=None):
+    _check(_lib.moe_expert_ffn_fp8(ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(w1q), _ptr(w1s), _ptr(w3q),
+                                   _ptr(w3s), _ptr(w2q), _ptr(w2s), _ptr(y_perm), _ptr(ws), _stream(stream)),
+           "moe_expert_ffn_fp8")
+
+
+def moe_layer_forward_fp8(cfg, x, Wg, logit_bias, sel_bias, w1q, w1s, w3q, w3s, w2q, w2s, sw1, sw3, sw2, out, ws,
+                          stream=None):
+    _check(_lib.moe_layer_forward_fp8(ctypes.byref(cfg), _ptr(x), _ptr(Wg), _ptr(logit_bias), _ptr(sel_bias),
+                                      _ptr(w1q), _ptr(w1s), _ptr(w3q), _ptr(w3s), _ptr(w2q), _ptr(w2s), _ptr(sw1),
+                                      _ptr(sw3), _ptr(sw2), _ptr(out), _ptr(ws), _stream(stream)),
+           "moe_layer_forward_fp8")
 
 
 def moe_bias_update(cfg, counts_routed, sel_bias, gamma: float, stream=None):

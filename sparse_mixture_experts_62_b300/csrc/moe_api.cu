@@ -162,6 +162,34 @@ int ffn_routed(const moe_config *c, const void *x_perm, const int32_t *offsets, 
   return MOE_OK;
 }
 
+// FP8 E4M3 expert weights with per-row float32 scales (codes [N, rows, K] bytes)
+struct Fp8Weights {
+  const uint8_t *w1q;
+  const float *w1s;
+  const uint8_t *w3q;
+  const float *w3s;
+  const uint8_t *w2q;
+  const float *w2s;
+};
+
+int check_fp8(const moe_config *c, const Fp8Weights &f) {
+  if (!is_bf16(c) || c->d % 16 || c->ffn % 16) return MOE_ERR_UNSUPPORTED;  // code rows: 16-byte multiples
+  if (!f.w1q || !f.w1s || !f.w2q || !f.w2s) return MOE_ERR_INVALID_ARG;
+  if (c->act == MOE_ACT_SWIGLU && (!f.w3q || !f.w3s)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(f.w1q) || !aligned16(f.w2q) || (f.w3q && !aligned16(f.w3q))) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+int ffn_routed_fp8(const moe_config *c, const void *x_perm, const int32_t *offsets, const Fp8Weights &f, void *h,
+                   void *y_perm, int *status, cudaStream_t s) {
+  const int64_t rows = routed_rows(c);
+  const int mode1 = c->act == MOE_ACT_SWIGLU ? 0 : 1;
+  MOE_TRY(tc_grouped_gemm_fp8(mode1, x_perm, rows, c->d, f.w1q, f.w1s, f.w3q, f.w3s, (int64_t)c->N * c->ffn, c->ffn,
+                              offsets, c->N, 0, c->ffn, h, status, s));
+  return tc_grouped_gemm_fp8(2, h, rows, c->ffn, f.w2q, f.w2s, nullptr, nullptr, (int64_t)c->N * c->d, c->d, offsets,
+                             c->N, 0, c->d, y_perm, status, s);
+}
+
 int ffn_shared(const moe_config *c, const void *x, const void *sw1, const void *sw3, const void *sw2, void *h,
                void *y, int *status, cudaStream_t s) {
   const int mode1 = c->act == MOE_ACT_SWIGLU ? 0 : 1;
@@ -425,12 +453,21 @@ int moe_combine(const moe_config *cfg, const void *y_perm, const int32_t *dest_r
                         static_cast<cudaStream_t>(stream));
 }
 
-int moe_layer_forward(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias,
-                      const float *sel_bias, const void *w1, const void *w3, const void *w2, const void *sw1,
-                      const void *sw3, const void *sw2, void *out, void *ws, void *stream) {
+}  // extern "C"
+
+namespace {
+// The layer with bf16 / float32 expert weights (f8 == nullptr) or FP8 ones.
+int layer_forward_impl(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias,
+                       const float *sel_bias, const void *w1, const void *w3, const void *w2, const Fp8Weights *f8,
+                       const void *sw1, const void *sw3, const void *sw2, void *out, void *ws, void *stream) {
   MOE_TRY(check_config(cfg));
   if (cfg->T == 0) return MOE_OK;
-  if (!x || !Wg || !out || !aligned16(x) || !aligned16(out) || !weights_ok(cfg, w1, w3, w2)) return MOE_ERR_INVALID_ARG;
+  if (!x || !Wg || !out || !aligned16(x) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  if (f8) {
+    MOE_TRY(check_fp8(cfg, *f8));
+  } else if (!weights_ok(cfg, w1, w3, w2)) {
+    return MOE_ERR_INVALID_ARG;
+  }
   const bool shared = cfg->shared_ffn > 0;
   if (shared && !weights_ok(cfg, sw1, sw3, sw2)) return MOE_ERR_INVALID_ARG;
   Ws w;
@@ -455,13 +492,54 @@ int moe_layer_forward(const moe_config *cfg, const void *x, const float *Wg, con
   }
   MOE_TRY(launch_gather_rows(x, src_token, offsets + cfg->N, routed_rows(cfg), (int)(cfg->d * esize(cfg)), x_perm,
                              s));
-  MOE_TRY(ffn_routed(cfg, x_perm, offsets, w1, w3, w2, w.at<void>(L.h), y_perm, w.status(), s));
+  if (f8)
+    MOE_TRY(ffn_routed_fp8(cfg, x_perm, offsets, *f8, w.at<void>(L.h), y_perm, w.status(), s));
+  else
+    MOE_TRY(ffn_routed(cfg, x_perm, offsets, w1, w3, w2, w.at<void>(L.h), y_perm, w.status(), s));
   void *y_sh = nullptr;
   if (shared) {
     y_sh = w.at<void>(L.y_shared);
     MOE_TRY(ffn_shared(cfg, x, sw1, sw3, sw2, w.at<void>(L.h_shared), y_sh, w.status(), s));
   }
   return launch_combine(is_bf16(cfg), y_perm, dest_row, gw, y_sh, out, cfg->T, cfg->d, slots(cfg), s);
+}
+}  // namespace
+
+extern "C" {
+
+int moe_layer_forward(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias,
+                      const float *sel_bias, const void *w1, const void *w3, const void *w2, const void *sw1,
+                      const void *sw3, const void *sw2, void *out, void *ws, void *stream) {
+  return layer_forward_impl(cfg, x, Wg, logit_bias, sel_bias, w1, w3, w2, nullptr, sw1, sw3, sw2, out, ws, stream);
+}
+
+int moe_layer_forward_fp8(const moe_config *cfg, const void *x, const float *Wg, const float *logit_bias,
+                          const float *sel_bias, const uint8_t *w1q, const float *w1s, const uint8_t *w3q,
+                          const float *w3s, const uint8_t *w2q, const float *w2s, const void *sw1, const void *sw3,
+                          const void *sw2, void *out, void *ws, void *stream) {
+  const Fp8Weights f{w1q, w1s, w3q, w3s, w2q, w2s};
+  return layer_forward_impl(cfg, x, Wg, logit_bias, sel_bias, nullptr, nullptr, nullptr, &f, sw1, sw3, sw2, out, ws,
+                            stream);
+}
+
+int moe_expert_ffn_fp8(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const uint8_t *w1q,
+                       const float *w1s, const uint8_t *w3q, const float *w3s, const uint8_t *w2q, const float *w2s,
+                       void *y_perm, void *ws, void *stream) {
+  MOE_TRY(check_config(cfg));
+  const Fp8Weights f{w1q, w1s, w3q, w3s, w2q, w2s};
+  MOE_TRY(check_fp8(cfg, f));
+  if (cfg->T == 0) return MOE_OK;
+  if (!x_perm || !offsets || !y_perm || !aligned16(x_perm) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  MOE_TRY(make_ws(cfg, ws, &w));
+  return ffn_routed_fp8(cfg, x_perm, offsets, f, w.at<void>(w.L.h), y_perm, w.status(), static_cast<cudaStream_t>(stream));
+}
+
+int moe_quantize_fp8(const void *w, int64_t rows, int32_t cols, uint8_t *q, float *scales, void *stream) {
+  if (rows < 0 || cols < 1) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!w || !q || !scales) return MOE_ERR_INVALID_ARG;
+  return launch_quantize_fp8(w, rows, cols, q, scales, static_cast<cudaStream_t>(stream));
 }
 
 int moe_load_stats(const moe_config *cfg, const float *logits, const int32_t *counts_routed,

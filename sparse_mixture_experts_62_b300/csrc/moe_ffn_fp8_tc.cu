@@ -1,0 +1,494 @@
+// Expert FFN with FP8 E4M3 weights (one float32 scale per output row) on the
+// tcgen05 tensor cores.
+//
+// The pages leave the quantisation of experts open ("Stanford CS336 lecture 4",
+// the section on compressing sparse MoEs: fewer bits per weight, paid for with
+// scales and a dequantisation step); the reading taken is weight-only E4M3 with
+// a float32 scale per output row: W[n, :] = s[n] * q[n, :].  Then
+//   out[r, n] = EPI( s[n] * sum_k A[r, k] q[n, k] ),
+// so the scale factors out of the K sum.  Every E4M3 value is a bf16 value, so the
+// codes are turned into bf16 exactly and the product runs as the bf16 grouped
+// GEMM; the epilogue multiplies each accumulator column by its row's scale.  The
+// weights stream from HBM at one byte each: the memory-bound decode reads half the
+// bytes of bf16 weights.
+//
+// Kernel shape (one CTA per SM, persistent over output tiles, 352 threads), three
+// rings so that many weight bytes are in flight (the decode this path is for is
+// bound by streaming the weights):
+//   codes  6 x 16 KB  (E4M3, 256 rows x 64 bytes, no swizzle)   warp 0 loads (TMA)
+//   A      2 x 16 KB  (bf16, 128 x 64, 128-byte swizzle)        warp 10 loads (TMA)
+//   B      2 x 32 KB  (bf16, 256 x 64, K-major, 128-byte swizzle)
+//   warps 6-9   convert a code tile into a B tile, fence it for the tensor core,
+//               and signal it; the code buffer is released at once.
+//   warp 1      MMA issuer: M=128, N=256, K=16 into one of two TMEM accumulators;
+//               its commits release the A and B buffers.
+//   warps 2-5   epilogue: scale, activation, bf16 stores masked to the group.
+// Tiles run group by group as in the bf16 kernel.  Waits are bounded as there.
+#include <cuda_fp8.h>
+
+#include <mutex>
+#include <vector>
+
+#include "moe_common.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace f8 {
+
+constexpr int BM = 128, BN = 256, BK = 64, THREADS = 352;
+constexpr int NR = 6, NA = 2, NC = 2;                      // ring depths: codes, A, converted B
+constexpr int A_BYTES = BM * BK * 2;                       // 16 KB
+constexpr int R_BYTES = BN * BK;                           // 16 KB of E4M3 codes
+constexpr int C_BYTES = BN * BK * 2;                       // 32 KB of converted bf16
+constexpr int RING_BYTES = NR * R_BYTES + NA * A_BYTES + NC * C_BYTES;  // 192 KB
+constexpr int MAX_GROUPS = 257;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr size_t SMEM_BYTES = 1024 + (size_t)RING_BYTES + 256 + (size_t)(4 * MAX_GROUPS + 8) * 4;
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+
+enum Mode { kSwiGLU = 0, kReLU = 1, kPlain = 2 };
+
+struct Args {
+  const int32_t *offsets;  // [G + 1] group row offsets, or nullptr: one group of M rows
+  int32_t G;
+  int32_t M;
+  int32_t a_rows;
+  int32_t n_out;
+  int32_t b_rows;          // weight rows per group
+  int32_t num_kb;
+  const float *scale0;     // [G * b_rows] scales of the first weight (W1 or W2)
+  const float *scale1;     // [G * b_rows] scales of W3 (kSwiGLU)
+  uint16_t *out;           // [a_rows, n_out] bf16
+  int *status;
+};
+
+__device__ __forceinline__ float silu(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
+
+// Two E4M3 codes -> two bf16 (exact) packed low/high.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+  const float2 f = __half22float2(__half2(h));
+  return pack_bf16x2(f.x, f.y);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmQ0,
+                            const __grid_constant__ CUtensorMap tmQ1, const Args args) {
+  constexpr int OUT_COLS = (MODE == kSwiGLU) ? 128 : 256;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint8_t *cbuf = smem;                                // NC x 32 KB (1024-aligned)
+  uint8_t *abuf = cbuf + NC * C_BYTES;                 // NA x 16 KB
+  uint8_t *rbuf = abuf + NA * A_BYTES;                 // NR x 16 KB
+  uint64_t *r_full = reinterpret_cast<uint64_t *>(smem + RING_BYTES);
+  uint64_t *r_empty = r_full + NR;
+  uint64_t *a_full = r_empty + NR;
+  uint64_t *a_empty = a_full + NA;
+  uint64_t *c_full = a_empty + NA;
+  uint64_t *c_empty = c_full + NC;
+  uint64_t *tfull = c_empty + NC;
+  uint64_t *tempty = tfull + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  int *tile_start = reinterpret_cast<int *>(smem + RING_BYTES + 256);
+  int *mtiles = tile_start + MAX_GROUPS + 1;
+  int *rowbeg = mtiles + MAX_GROUPS;
+  int *rowend = rowbeg + MAX_GROUPS;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = args.G;
+  const int n_tiles = (args.n_out + OUT_COLS - 1) / OUT_COLS;
+  const int num_kb = args.num_kb;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NR; ++s) {
+      mbar_init(&r_full[s], 1);
+      mbar_init(&r_empty[s], 4);  // one arrival per converter warp
+    }
+    for (int s = 0; s < NA; ++s) {
+      mbar_init(&a_full[s], 1);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int s = 0; s < NC; ++s) {
+      mbar_init(&c_full[s], 4);
+      mbar_init(&c_empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    fence_barrier_init();
+    int acc = 0;
+    for (int g = 0; g < G; ++g) {
+      int b = args.offsets ? args.offsets[g] : 0;
+      int e = args.offsets ? args.offsets[g + 1] : args.M;
+      if (b < 0 || e < b || e > args.a_rows) {
+        set_status(args.status, MOE_ERR_BOUNDS);
+        b = e = 0;
+      }
+      rowbeg[g] = b;
+      rowend[g] = e;
+      const int mt = e > b ? (e - b + BM - 1) / BM : 0;
+      mtiles[g] = mt;
+      tile_start[g] = acc;
+      acc += mt * n_tiles;
+    }
+    tile_start[G] = acc;
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ0);
+    if (MODE == kSwiGLU) tma_prefetch_desc(&tmQ1);
+  }
+  if (warp == 10 && lane == 0) tma_prefetch_desc(&tmA);
+  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total_tiles = tile_start[G];
+
+  if (warp == 0 || warp == 10) {
+    // ------------------------------------------------------------ TMA producers: codes (warp 0), A (warp 10)
+    if (lane == 0) {
+      const bool codes = warp == 0;
+      const int depth = codes ? NR : NA;
+      uint64_t *fullb = codes ? r_full : a_full;
+      uint64_t *emptyb = codes ? r_empty : a_empty;
+      int issued_parity[NR];
+      for (int s = 0; s < NR; ++s) issued_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      int g = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        while (tile >= tile_start[g + 1]) ++g;
+        const int local = tile - tile_start[g];
+        const int n_tile = local / mtiles[g];
+        const int m_tile = local - n_tile * mtiles[g];
+        const int a_row = rowbeg[g] + m_tile * BM;
+        const int b_row = g * args.b_rows + n_tile * OUT_COLS;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&emptyb[stage], phase ^ 1u, args.status)) {
+            ok = false;
+            break;
+          }
+          if (codes) {
+            uint8_t *sr = rbuf + stage * R_BYTES;
+            mbar_arrive_expect_tx(&fullb[stage], R_BYTES);
+            if (MODE == kSwiGLU) {
+              tma_load_2d(sr, &tmQ0, &fullb[stage], kb * BK, b_row);
+              tma_load_2d(sr + R_BYTES / 2, &tmQ1, &fullb[stage], kb * BK, b_row);
+            } else {
+              tma_load_2d(sr, &tmQ0, &fullb[stage], kb * BK, b_row);
+              tma_load_2d(sr + R_BYTES / 2, &tmQ0, &fullb[stage], kb * BK, b_row + BN / 2);
+            }
+          } else {
+            mbar_arrive_expect_tx(&fullb[stage], A_BYTES);
+            tma_load_2d(abuf + stage * A_BYTES, &tmA, &fullb[stage], kb * BK, a_row);
+          }
+          issued_parity[stage] = (int)phase;
+          if (++stage == depth) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // never leave the CTA with a bulk copy still writing its shared memory
+      for (int s = 0; s < depth; ++s)
+        if (issued_parity[s] >= 0) mbar_wait(&fullb[s], (uint32_t)issued_parity[s], args.status);
+    }
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------ E4M3 -> bf16 converters (warps 6-9)
+    const int tid = threadIdx.x - 192;  // 0..127: rows tid and tid + 128
+    int rs = 0, cs = 0;
+    uint32_t rph = 0, cph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&r_full[rs], rph, args.status)) ||
+            !__all_sync(0xffffffffu, mbar_wait(&c_empty[cs], cph ^ 1u, args.status))) {
+          ok = false;
+          break;
+        }
+        const uint8_t *sr = rbuf + rs * R_BYTES;
+        uint8_t *sc = cbuf + cs * C_BYTES;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int row = tid + 128 * q;
+          const uint4 *src = reinterpret_cast<const uint4 *>(sr + row * BK);
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {  // 16 codes -> two 16-byte chunks of bf16
+            const uint4 v = src[h];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              o[2 * i] = e4m3x2_to_bf16x2((uint16_t)(w[i] & 0xFFFFu));
+              o[2 * i + 1] = e4m3x2_to_bf16x2((uint16_t)(w[i] >> 16));
+            }
+            const int c0 = 2 * h, c1 = 2 * h + 1;
+            *reinterpret_cast<uint4 *>(sc + row * 128 + ((c0 ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4 *>(sc + row * 128 + ((c1 ^ (row & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&r_empty[rs]);
+          mbar_arrive(&c_full[cs]);
+        }
+        if (++rs == NR) {
+          rs = 0;
+          rph ^= 1u;
+        }
+        if (++cs == NC) {
+          cs = 0;
+          cph ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int as = 0, cs = 0;
+      uint32_t aph = 0, cph = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, args.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&a_full[as], aph, args.status) || !mbar_wait(&c_full[cs], cph, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = smem_desc_sw128(smem_u32(abuf + as * A_BYTES));
+          const uint64_t bdesc = smem_desc_sw128(smem_u32(cbuf + cs * C_BYTES));
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, IDESC, (kb | kk) != 0);
+          tc_commit(&a_empty[as]);
+          tc_commit(&c_empty[cs]);
+          if (++as == NA) {
+            as = 0;
+            aph ^= 1u;
+          }
+          if (++cs == NC) {
+            cs = 0;
+            cph ^= 1u;
+          }
+        }
+        if (ok) tc_commit(&tfull[acc]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2-5)
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    int g = 0;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
+      while (tile >= tile_start[g + 1]) ++g;
+      const int local = tile - tile_start[g];
+      const int n_tile = local / mtiles[g];
+      const int m_tile = local - n_tile * mtiles[g];
+      const int row0 = rowbeg[g] + m_tile * BM;
+      const int rows_valid = min(BM, rowend[g] - row0);
+      const int n0 = n_tile * OUT_COLS;
+      const float *s0 = args.scale0 + (size_t)g * args.b_rows;
+      const float *s1 = (MODE == kSwiGLU) ? args.scale1 + (size_t)g * args.b_rows : nullptr;
+      const int acc = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!mbar_wait(&tfull[acc], use & 1u, args.status)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
+      const bool row_ok = r < rows_valid;
+      uint16_t *orow = args.out + (size_t)(row0 + (row_ok ? r : 0)) * args.n_out;
+      if (MODE == kSwiGLU) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 16) {
+          float a[16], u[16];
+          tmem_ld16x2(taddr + c, taddr + 128 + c, a, u);
+          const int col = n0 + c;
+          if (!row_ok || col >= args.n_out) continue;
+          uint32_t p[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int c2 = min(col + 2 * i, args.n_out - 2);  // columns past n_out are not stored
+            const float a0 = a[2 * i] * s0[c2], a1 = a[2 * i + 1] * s0[c2 + 1];
+            const float u0 = u[2 * i] * s1[c2], u1 = u[2 * i + 1] * s1[c2 + 1];
+            p[i] = pack_bf16x2(silu(a0) * u0, silu(a1) * u1);
+          }
+          if (col + 8 <= args.n_out) *reinterpret_cast<uint4 *>(orow + col) = make_uint4(p[0], p[1], p[2], p[3]);
+          if (col + 16 <= args.n_out) *reinterpret_cast<uint4 *>(orow + col + 8) = make_uint4(p[4], p[5], p[6], p[7]);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          float v0[16], v1[16];
+          tmem_ld16x2(taddr + c, taddr + c + 16, v0, v1);
+          if (!row_ok) continue;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int col = n0 + c + 8 * q;
+            if (col + 8 > args.n_out) continue;
+            const float *v = q < 2 ? v0 + 8 * q : v1 + 8 * (q - 2);
+            float x[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              x[i] = v[i] * s0[col + i];
+              if (MODE == kReLU) x[i] = fmaxf(x[i], 0.f);
+            }
+            *reinterpret_cast<uint4 *>(orow + col) = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                                                                pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// Per-row quantisation: one warp per row; s = max |w| / 448 (1 for a zero row),
+// q = E4M3 (round to nearest even, saturating) of w / s.
+__global__ void __launch_bounds__(256) quantize_rows_fp8_kernel(const uint16_t *__restrict__ w, int64_t rows, int cols,
+                                                                uint8_t *__restrict__ q, float *__restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const uint16_t *wr = w + row * cols;
+  float amax = 0.f;
+  for (int c = lane; c < cols; c += 32) amax = fmaxf(amax, fabsf(__uint_as_float((uint32_t)wr[c] << 16)));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float s = amax > 0.f ? amax / 448.0f : 1.0f;
+  if (lane == 0) scales[row] = s;
+  uint8_t *qr = q + row * cols;
+  for (int c = lane; c < cols; c += 32) {
+    const float v = __uint_as_float((uint32_t)wr[c] << 16) / s;
+    qr[c] = (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 [rows, cols], box 64 x 128, 128-byte swizzle (the A tile)
+static int make_map_bf16(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return MOE_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16 || !rows || !cols) return MOE_ERR_UNSUPPORTED;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {BK, BM};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+// E4M3 codes [rows, cols] bytes, box 64 x 128, no swizzle (the raw weight tile)
+static int make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return MOE_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || cols % 16 || !rows || !cols) return MOE_ERR_UNSUPPORTED;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {BK, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+template <int MODE>
+static int launch(const CUtensorMap &ma, const CUtensorMap &mq0, const CUtensorMap &mq1, const Args &args, int dev,
+                  cudaStream_t stream) {
+  static std::mutex mu;
+  static std::vector<int> done;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if ((int)done.size() <= dev) done.resize(dev + 1, 0);
+    if (!done[dev]) {
+      if (cudaFuncSetAttribute(grouped_gemm_fp8_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)SMEM_BYTES) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      done[dev] = 1;
+    }
+  }
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return MOE_ERR_CUDA;
+  grouped_gemm_fp8_kernel<MODE><<<sms, THREADS, SMEM_BYTES, stream>>>(ma, mq0, mq1, args);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace f8
+
+int tc_grouped_gemm_fp8(int mode, const void *A, int64_t a_rows, int K, const uint8_t *Q0, const float *S0,
+                        const uint8_t *Q1, const float *S1, int64_t b_rows_total, int b_rows_per_group,
+                        const int32_t *offsets, int G, int M, int n_out, void *out, int *status, cudaStream_t stream) {
+  using namespace f8;
+  if (G < 1 || G > MAX_GROUPS || K < 1 || n_out < 1 || a_rows < 1 || a_rows > INT32_MAX || b_rows_total < 1)
+    return MOE_ERR_INVALID_ARG;
+  if (mode < kSwiGLU || mode > kPlain || !Q0 || !S0 || (mode == kSwiGLU && (!Q1 || !S1)) ||
+      n_out > b_rows_per_group || (int64_t)G * b_rows_per_group > b_rows_total || (n_out % 8))
+    return MOE_ERR_INVALID_ARG;
+  CUtensorMap ma, mq0, mq1;
+  int rc;
+  if ((rc = make_map_bf16(&ma, A, (uint64_t)a_rows, (uint64_t)K))) return rc;
+  if ((rc = make_map_u8(&mq0, Q0, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
+  if (mode == kSwiGLU) {
+    if ((rc = make_map_u8(&mq1, Q1, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
+  } else {
+    mq1 = mq0;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  Args args{offsets, G, M, (int32_t)a_rows, n_out, b_rows_per_group, (K + BK - 1) / BK, S0, S1,
+            static_cast<uint16_t *>(out), status};
+  switch (mode) {
+    case kSwiGLU: return launch<kSwiGLU>(ma, mq0, mq1, args, dev, stream);
+    case kReLU: return launch<kReLU>(ma, mq0, mq1, args, dev, stream);
+    default: return launch<kPlain>(ma, mq0, mq1, args, dev, stream);
+  }
+}
+
+int launch_quantize_fp8(const void *w, int64_t rows, int cols, uint8_t *q, float *scales, cudaStream_t s) {
+  if (rows == 0) return MOE_OK;
+  f8::quantize_rows_fp8_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(static_cast<const uint16_t *>(w), rows,
+                                                                           cols, q, scales);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

@@ -36,6 +36,12 @@ int launch_gather_rows(const void *x, const int32_t *src_token, const int32_t *o
 int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
                     int64_t b_rows_total, int b_rows_per_group, const int32_t *offsets, int G, int M, int n_out,
                     void *out, int *status, bool pair_tiles, cudaStream_t stream);
+// The forward GEMM (modes 0-2) with FP8 E4M3 weights Q [G * b_rows, K] bytes and
+// per-row float32 scales S [G * b_rows]: out = EPI(S[n] * sum_k A[r, k] Q[n, k]).
+int tc_grouped_gemm_fp8(int mode, const void *A, int64_t a_rows, int K, const uint8_t *Q0, const float *S0,
+                        const uint8_t *Q1, const float *S1, int64_t b_rows_total, int b_rows_per_group,
+                        const int32_t *offsets, int G, int M, int n_out, void *out, int *status, cudaStream_t stream);
+int launch_quantize_fp8(const void *w, int64_t rows, int cols, uint8_t *q, float *scales, cudaStream_t s);
 // The gate/up GEMM recomputed for the backward with the activation's backward
 // fused into its epilogue: a = A W1_g^T (and u = A W3_g^T), dh [rows, F] read,
 // dA written: SwiGLU [rows, 2F] = [dh u SiLU'(a) | dh SiLU(a)], ReLU [rows, F] =

@@ -10,8 +10,8 @@ from typing import Optional
 
 import torch
 
-from . import (DTYPE_BF16, MoeConfig, moe_get_device_status, moe_layer_forward, moe_load_stats,
-               moe_seq_balance_loss, moe_workspace_layout, moe_workspace_size)
+from . import (DTYPE_BF16, MoeConfig, moe_get_device_status, moe_layer_forward, moe_layer_forward_fp8, moe_load_stats,
+               moe_quantize_fp8, moe_seq_balance_loss, moe_workspace_layout, moe_workspace_size)
 
 
 class MoELayer:
@@ -31,14 +31,32 @@ class MoELayer:
         self.ws.zero_()
         self.layout = moe_workspace_layout(cfg)
         self._stats = torch.zeros(2 * cfg.N + 4, dtype=torch.float32, device=self.device)
+        self.fp8 = None  # (w1q, w1s, w3q, w3s, w2q, w2s) once quantize_fp8 has run
+
+    def quantize_fp8(self, stream=None):
+        """Quantise the routed experts to FP8 E4M3 with one float32 scale per weight row
+        (on the device); forward then runs the FP8 layer.  The shared expert stays bf16."""
+        def q(w):
+            if w is None:
+                return None, None
+            codes = torch.empty(w.shape, dtype=torch.uint8, device=self.device)
+            scales = torch.empty(w.shape[:-1], dtype=torch.float32, device=self.device)
+            moe_quantize_fp8(w, codes, scales, stream)
+            return codes, scales
+        self.fp8 = (*q(self.w1), *q(self.w3), *q(self.w2))
+        return self.fp8
 
     # ------------------------------------------------------------------ forward
     def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
         c = self.cfg
         if out is None:
             out = torch.empty((c.T, c.d), dtype=self.act_dtype, device=self.device)
-        moe_layer_forward(c, x, self.Wg, self.logit_bias, self.sel_bias, self.w1, self.w3, self.w2,
-                          self.sw1, self.sw3, self.sw2, out, self.ws, stream)
+        if self.fp8 is not None:
+            moe_layer_forward_fp8(c, x, self.Wg, self.logit_bias, self.sel_bias, *self.fp8, self.sw1, self.sw3,
+                                  self.sw2, out, self.ws, stream)
+        else:
+            moe_layer_forward(c, x, self.Wg, self.logit_bias, self.sel_bias, self.w1, self.w3, self.w2,
+                              self.sw1, self.sw3, self.sw2, out, self.ws, stream)
         return out
 
     def load_stats(self, stream=None):
