@@ -63,6 +63,16 @@ inline size_t stats_rows_bytes(const moe_config *c) {
 }
 inline size_t stats_bytes(const moe_config *c) { return stats_rows_bytes(c) + align256((size_t)c->T * 4); }
 
+// A group's rows are bounded by T (a token reaches an expert at most once) and by
+// the capacity (expert choice's C included).
+inline int group_bound(const moe_config *c) { return c->capacity > 0 && c->capacity < c->T ? c->capacity : c->T; }
+
+inline size_t router_scratch_bytes(const moe_config *c) {
+  if (!is_bf16(c)) return 0;
+  const size_t Np = (size_t)router_tc_npad(c->N), dp = (size_t)router_tc_dpad(c->d);
+  return align256(align256(Np * 3 * dp * 2) + (size_t)router_tc_max_splits(c->T, c->d) * c->T * Np * 4);
+}
+
 int layout(const moe_config *c, moe_ws_layout *L) {
   const size_t T = (size_t)c->T, N = (size_t)c->N, k = (size_t)c->k, d = (size_t)c->d, F = (size_t)c->ffn;
   const size_t Fs = (size_t)c->shared_ffn, es = esize(c);
@@ -89,12 +99,7 @@ int layout(const moe_config *c, moe_ws_layout *L) {
   L->y_perm = take(rows * d * es);
   L->h_shared = take(Fs ? T * Fs * es : 0);
   L->y_shared = take(Fs ? T * d * es : 0);
-  size_t router_bytes = 0;
-  if (is_bf16(c)) {
-    const size_t Np = (size_t)router_tc_npad(c->N), dp = (size_t)router_tc_dpad(c->d);
-    router_bytes = align256(Np * 3 * dp * 2) + (size_t)router_tc_max_splits(c->T, c->d) * T * Np * 4;
-  }
-  L->scratch = take(align256(2 * nch_d * N * 4) + stats_bytes(c) + router_bytes);
+  L->scratch = take(align256(2 * nch_d * N * 4) + stats_bytes(c) + router_scratch_bytes(c));
   L->total = o;
   return MOE_OK;
 }
@@ -180,14 +185,15 @@ int check_fp8(const moe_config *c, const Fp8Weights &f) {
   return MOE_OK;
 }
 
-int ffn_routed_fp8(const moe_config *c, const void *x_perm, const int32_t *offsets, const Fp8Weights &f, void *h,
-                   void *y_perm, int *status, cudaStream_t s) {
+int ffn_routed_fp8(const moe_config *c, const Ws &w, const void *x_perm, const int32_t *offsets,
+                   const Fp8Weights &f, void *h, void *y_perm, cudaStream_t s) {
   const int64_t rows = routed_rows(c);
   const int mode1 = c->act == MOE_ACT_SWIGLU ? 0 : 1;
+  const int bound = group_bound(c);
   MOE_TRY(tc_grouped_gemm_fp8(mode1, x_perm, rows, c->d, f.w1q, f.w1s, f.w3q, f.w3s, (int64_t)c->N * c->ffn, c->ffn,
-                              offsets, c->N, 0, c->ffn, h, status, s));
+                              offsets, c->N, 0, c->ffn, bound, h, w.status(), s));
   return tc_grouped_gemm_fp8(2, h, rows, c->ffn, f.w2q, f.w2s, nullptr, nullptr, (int64_t)c->N * c->d, c->d, offsets,
-                             c->N, 0, c->d, y_perm, status, s);
+                             c->N, 0, c->d, bound, y_perm, w.status(), s);
 }
 
 int ffn_shared(const moe_config *c, const void *x, const void *sw1, const void *sw3, const void *sw2, void *h,
@@ -493,7 +499,7 @@ int layer_forward_impl(const moe_config *cfg, const void *x, const float *Wg, co
   MOE_TRY(launch_gather_rows(x, src_token, offsets + cfg->N, routed_rows(cfg), (int)(cfg->d * esize(cfg)), x_perm,
                              s));
   if (f8)
-    MOE_TRY(ffn_routed_fp8(cfg, x_perm, offsets, *f8, w.at<void>(L.h), y_perm, w.status(), s));
+    MOE_TRY(ffn_routed_fp8(cfg, w, x_perm, offsets, *f8, w.at<void>(L.h), y_perm, s));
   else
     MOE_TRY(ffn_routed(cfg, x_perm, offsets, w1, w3, w2, w.at<void>(L.h), y_perm, w.status(), s));
   void *y_sh = nullptr;
@@ -532,7 +538,7 @@ int moe_expert_ffn_fp8(const moe_config *cfg, const void *x_perm, const int32_t 
   if (!x_perm || !offsets || !y_perm || !aligned16(x_perm) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
   Ws w;
   MOE_TRY(make_ws(cfg, ws, &w));
-  return ffn_routed_fp8(cfg, x_perm, offsets, f, w.at<void>(w.L.h), y_perm, w.status(), static_cast<cudaStream_t>(stream));
+  return ffn_routed_fp8(cfg, w, x_perm, offsets, f, w.at<void>(w.L.h), y_perm, static_cast<cudaStream_t>(stream));
 }
 
 int moe_quantize_fp8(const void *w, int64_t rows, int32_t cols, uint8_t *q, float *scales, void *stream) {

@@ -12,9 +12,13 @@
 // weights stream from HBM at one byte each: the memory-bound decode reads half the
 // bytes of bf16 weights.
 //
+// Two kernels.  Groups of at most 64 rows (decode) take the second one below, which
+// puts the weights on the M side of the MMA and their converted bf16 in tensor
+// memory.  Larger groups take this first one, which tiles the tokens on M and the
+// weight rows on N and converts the codes into a shared-memory B operand.
+//
 // Kernel shape (one CTA per SM, persistent over output tiles, 352 threads), three
-// rings so that many weight bytes are in flight (the decode this path is for is
-// bound by streaming the weights):
+// rings so that many weight bytes are in flight:
 //   codes  6 x 16 KB  (E4M3, 256 rows x 64 bytes, no swizzle)   warp 0 loads (TMA)
 //   A      2 x 16 KB  (bf16, 128 x 64, 128-byte swizzle)        warp 10 loads (TMA)
 //   B      2 x 32 KB  (bf16, 256 x 64, K-major, 128-byte swizzle)
@@ -362,6 +366,404 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+}  // namespace f8
+
+// ---------------------------------------------------------------------------
+// The same product for groups of at most a few dozen rows (decode): the weights
+// take the M side of the MMA and the group's tokens the N side,
+//   D[n, t] = sum_k q[n, k] A[t, k]   (M = 128 weight rows, N = NT tokens),
+// and the converted weights never touch shared memory: each converter thread
+// turns its weight row's codes into bf16 in registers and writes them with
+// tcgen05.st into tensor memory, where the MMA reads them as its A operand.
+// Shared memory only holds the TMA-loaded codes (64-byte swizzle, so that the
+// row-per-thread reads are free of bank conflicts) and the small token tiles,
+// each in a ring of its own.
+//   warps 0-3    epilogue (one TMEM lane quadrant each)
+//   warps 4-11   converters, two sets of four taking alternate stages
+//   warp 12      TMA producer of the codes of one 128-wide K stage
+//   warp 13      TMEM owner and MMA issuer
+//   warp 14      TMA producer of the stage's token tile
+// One stage covers K = 128: 128 weight rows x 128 codes per weight (two 64-byte
+// boxes), and NT token rows x 128 bf16 (two 128-byte-swizzled boxes).
+namespace f8s {
+
+using f8::kPlain;
+using f8::kReLU;
+using f8::kSwiGLU;
+
+constexpr int BMW = 128, KS = 128, MAX_GROUPS = 257;
+constexpr int W_TMA = 12, W_MMA = 13, W_TOK = 14, THREADS = 480;
+constexpr int BOX_BYTES = BMW * 64;  // one 128 x 64 box of codes
+
+template <int MODE, int NT>
+struct Shape {
+  static constexpr int NW = MODE == kSwiGLU ? 2 : 1;  // weights streamed per stage
+  static constexpr int NB = 2 * NW;                   // 128 x 64 boxes of codes per stage
+  static constexpr int CODE_BYTES = NW * BMW * KS;
+  static constexpr int TOK_BYTES = NT * KS * 2;
+  // Codes and tokens have rings of their own: a code stage is free once converted,
+  // a token stage once its MMAs are done.
+  static constexpr int NTR = NT <= 32 ? 8 : 4;
+  static constexpr int NR_FIT = (196608 - NTR * TOK_BYTES) / CODE_BYTES;
+  static constexpr int NR = NR_FIT < 12 ? NR_FIT : 12;
+  static constexpr int RING = NR * CODE_BYTES + NTR * TOK_BYTES;
+  static constexpr int ACOLS = NW * KS / 2;  // TMEM columns of one converted stage
+  static constexpr int DCOLS = 4 * NT;       // two accumulators of 2 x NT columns
+  static constexpr int NA = (512 - DCOLS) / ACOLS;
+  static constexpr size_t SMEM = 1024 + (size_t)RING + 512 + (size_t)(4 * MAX_GROUPS + 8) * 4;
+  static_assert(CODE_BYTES % 1024 == 0 && TOK_BYTES % 1024 == 0 && NA >= 2 && NR >= 3, "stage layout");
+};
+
+struct Args {
+  const int32_t *offsets;
+  int32_t G;
+  int32_t M;
+  int32_t a_rows;
+  int32_t n_out;
+  int32_t b_rows;
+  int32_t num_kb;   // stages of K = 128
+  const float *scale0;
+  const float *scale1;
+  uint16_t *out;
+  int *status;
+};
+
+// Four E4M3 codes (the bytes of w, lowest first) -> four bf16, two per word.
+// Each code's sign, 4-bit exponent field and 3-bit mantissa are placed in a bf16
+// with the same sign, the same exponent field and the mantissa at its top: that
+// bf16 is the code's value times 2^-120 (bias 127 against 7; with a zero field
+// both are subnormal with the same mantissa), so one multiplication by 2^120,
+// exact in bf16, yields the value.  The two NaN codes come out as +-480, so
+// they are not valid weights.
+__device__ __forceinline__ uint32_t bf16x2_mul_exact(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t a = __byte_perm(w, 0u, 0x1404);  // code1 << 24 | code0 << 8
+  const uint32_t b = __byte_perm(w, 0u, 0x3424);  // code3 << 24 | code2 << 8
+  lo = bf16x2_mul_exact((a & 0x80008000u) | ((a >> 4) & 0x07F007F0u), 0x7B807B80u);  // x 2^120
+  hi = bf16x2_mul_exact((b & 0x80008000u) | ((b >> 4) & 0x07F007F0u), 0x7B807B80u);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),
+      "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+      "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+// Each thread reads 16 consecutive 32-bit columns of its lane (load and wait in one statement).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *a) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) a[i] = __uint_as_float(r[i]);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T
+__device__ __forceinline__ void tc_mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <int MODE, int NT>
+__global__ void __launch_bounds__(THREADS, 1)
+    fp8_decode_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmQ0,
+                      const __grid_constant__ CUtensorMap tmQ1, const Args args) {
+  using S = Shape<MODE, NT>;
+  constexpr int NR = S::NR, NA = S::NA, NTR = S::NTR;
+  constexpr uint32_t IDESC = idesc_bf16_f32(BMW, NT);
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint8_t *tok_ring = smem + NR * S::CODE_BYTES;
+  uint64_t *r_full = reinterpret_cast<uint64_t *>(smem + S::RING);
+  uint64_t *r_empty = r_full + NR;
+  uint64_t *k_full = r_empty + NR;
+  uint64_t *k_empty = k_full + NTR;
+  uint64_t *a_full = k_empty + NTR;
+  uint64_t *a_empty = a_full + NA;
+  uint64_t *tfull = a_empty + NA;
+  uint64_t *tempty = tfull + 2;
+  uint64_t *done = tempty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+  int *tile_start = reinterpret_cast<int *>(smem + S::RING + 512);
+  int *ttiles = tile_start + MAX_GROUPS + 1;
+  int *rowbeg = ttiles + MAX_GROUPS;
+  int *rowend = rowbeg + MAX_GROUPS;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = args.G;
+  const int w_tiles = (args.n_out + BMW - 1) / BMW;
+  const int num_kb = args.num_kb;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NR; ++s) {
+      mbar_init(&r_full[s], 1);
+      mbar_init(&r_empty[s], 4);  // the four converter warps of a set
+    }
+    for (int s = 0; s < NTR; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);  // the MMA's commit
+    }
+    for (int s = 0; s < NA; ++s) {
+      mbar_init(&a_full[s], 4);
+      mbar_init(&a_empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    mbar_init(done, 1);
+    fence_barrier_init();
+    int acc = 0;
+    for (int g = 0; g < G; ++g) {
+      int b = args.offsets ? args.offsets[g] : 0;
+      int e = args.offsets ? args.offsets[g + 1] : args.M;
+      if (b < 0 || e < b || e > args.a_rows) {
+        set_status(args.status, MOE_ERR_BOUNDS);
+        b = e = 0;
+      }
+      rowbeg[g] = b;
+      rowend[g] = e;
+      const int tt = (e - b + NT - 1) / NT;
+      ttiles[g] = tt;
+      tile_start[g] = acc;
+      acc += tt * w_tiles;
+    }
+    tile_start[G] = acc;
+  }
+  if (warp == W_TMA && lane == 0) {
+    tma_prefetch_desc(&tmQ0);
+    if (MODE == kSwiGLU) tma_prefetch_desc(&tmQ1);
+  }
+  if (warp == W_TOK && lane == 0) tma_prefetch_desc(&tmA);
+  if (warp == W_MMA) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int total_tiles = tile_start[G];
+
+  if (warp == W_TMA || warp == W_TOK) {
+    // ------------------------------------------------------------ TMA producers: codes (W_TMA), tokens (W_TOK)
+    if (lane == 0) {
+      const bool codes = warp == W_TMA;
+      const int depth = codes ? NR : NTR;
+      uint64_t *fullb = codes ? r_full : k_full;
+      uint64_t *emptyb = codes ? r_empty : k_empty;
+      int issued_parity[NR > NTR ? NR : NTR];
+      for (int s = 0; s < depth; ++s) issued_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      int g = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        while (t >= tile_start[g + 1]) ++g;
+        const int local = t - tile_start[g];
+        const int wt = local / ttiles[g];
+        const int tt = local - wt * ttiles[g];
+        const int w_row = g * args.b_rows + wt * BMW;
+        const int t_row = rowbeg[g] + tt * NT;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&emptyb[stage], phase ^ 1u, args.status)) {
+            ok = false;
+            break;
+          }
+          if (codes) {
+            uint8_t *st = smem + stage * S::CODE_BYTES;
+            mbar_arrive_expect_tx(&fullb[stage], S::CODE_BYTES);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int x = kb * KS + h * 64;
+              tma_load_2d(st + h * BOX_BYTES, &tmQ0, &fullb[stage], x, w_row);
+              if (MODE == kSwiGLU) tma_load_2d(st + (2 + h) * BOX_BYTES, &tmQ1, &fullb[stage], x, w_row);
+            }
+          } else {
+            uint8_t *st = tok_ring + stage * S::TOK_BYTES;
+            mbar_arrive_expect_tx(&fullb[stage], S::TOK_BYTES);
+            tma_load_2d(st, &tmA, &fullb[stage], kb * KS, t_row);
+            tma_load_2d(st + NT * 128, &tmA, &fullb[stage], kb * KS + 64, t_row);
+          }
+          issued_parity[stage] = (int)phase;
+          if (++stage == depth) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      for (int s = 0; s < depth; ++s)
+        if (issued_parity[s] >= 0) mbar_wait(&fullb[s], (uint32_t)issued_parity[s], args.status);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------------ converters
+    const int set = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;  // weight row of this thread = TMEM lane
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)S::DCOLS;
+    const int swz = (r >> 1) & 3;
+    int c = 0;  // stage counter of this CTA
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      for (int kb = 0; kb < num_kb; ++kb, ++c) {
+        if ((c & 1) != set) continue;
+        const int rs = c % NR, as = c % NA;
+        const uint32_t rph = (uint32_t)(c / NR) & 1u, aph = (uint32_t)(c / NA) & 1u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&r_full[rs], rph, args.status)) ||
+            !__all_sync(0xffffffffu, mbar_wait(&a_empty[as], aph ^ 1u, args.status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint8_t *st = smem + rs * S::CODE_BYTES + r * 64;
+#pragma unroll
+        for (int b = 0; b < S::NB; ++b) {  // boxes: weight b / 2, K half b % 2
+          uint32_t o[32];
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(st + b * BOX_BYTES + ((ch ^ swz) << 4));
+            e4m3x4_to_bf16(v.x, o[8 * ch + 0], o[8 * ch + 1]);
+            e4m3x4_to_bf16(v.y, o[8 * ch + 2], o[8 * ch + 3]);
+            e4m3x4_to_bf16(v.z, o[8 * ch + 4], o[8 * ch + 5]);
+            e4m3x4_to_bf16(v.w, o[8 * ch + 6], o[8 * ch + 7]);
+          }
+          tmem_st32(lane_base + (uint32_t)(as * S::ACOLS + b * 32), o);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&r_empty[rs]);
+          mbar_arrive(&a_full[as]);
+        }
+      }
+    }
+  } else if (warp == W_MMA) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int ks = 0, as = 0;
+      uint32_t kph = 0, aph = 0;
+      int it = 0;
+      bool ok = true, issued = false;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, args.status)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + (uint32_t)(acc * 2 * NT);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&k_full[ks], kph, args.status) || !mbar_wait(&a_full[as], aph, args.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = tmem_base + (uint32_t)(S::DCOLS + as * S::ACOLS);
+          const uint32_t tok = smem_u32(tok_ring + ks * S::TOK_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < KS / 16; ++kk) {
+            const uint64_t bdesc = smem_desc_sw128(tok + (uint32_t)((kk >> 2) * NT * 128)) + 2ull * (kk & 3);
+            const uint32_t accum = (kb | kk) != 0;
+            tc_mma_bf16_ta(d0, a0 + 8u * kk, bdesc, IDESC, accum);
+            if (MODE == kSwiGLU) tc_mma_bf16_ta(d0 + NT, a0 + 64u + 8u * kk, bdesc, IDESC, accum);
+          }
+          issued = true;
+          tc_commit(&a_empty[as]);
+          tc_commit(&k_empty[ks]);
+          if (++ks == NTR) {
+            ks = 0;
+            kph ^= 1u;
+          }
+          if (++as == NA) {
+            as = 0;
+            aph ^= 1u;
+          }
+        }
+        if (ok) tc_commit(&tfull[acc]);
+      }
+      if (issued) {  // every MMA has finished with tensor memory before it is freed
+        tc_commit(done);
+        mbar_wait(done, 0, args.status);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 0-3)
+    const int quad = warp;
+    int g = 0;
+    int it = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+      while (t >= tile_start[g + 1]) ++g;
+      const int local = t - tile_start[g];
+      const int wt = local / ttiles[g];
+      const int tt = local - wt * ttiles[g];
+      const int t_row = rowbeg[g] + tt * NT;
+      const int nvalid = min(NT, rowend[g] - t_row);
+      const int f = wt * BMW + quad * 32 + lane;
+      const bool f_ok = f < args.n_out;
+      const float s0 = f_ok ? args.scale0[(size_t)g * args.b_rows + f] : 0.f;
+      const float s1 = (MODE == kSwiGLU && f_ok) ? args.scale1[(size_t)g * args.b_rows + f] : 0.f;
+      const int acc = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      if (!mbar_wait(&tfull[acc], use & 1u, args.status)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (uint32_t)(acc * 2 * NT) + ((uint32_t)(quad * 32) << 16);
+      uint16_t *ocol = args.out + (size_t)t_row * args.n_out + f;
+#pragma unroll 1
+      for (int c = 0; c < NT; c += 16) {
+        float a[16], u[16];
+        if (MODE == kSwiGLU) {
+          tmem_ld16x2(taddr + c, taddr + NT + c, a, u);
+        } else {
+          tmem_ld16(taddr + c, a);
+        }
+        if (!f_ok) continue;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          if (c + j >= nvalid) break;
+          float v;
+          if (MODE == kSwiGLU) {
+            v = f8::silu(a[j] * s0) * (u[j] * s1);
+          } else {
+            v = a[j] * s0;
+            if (MODE == kReLU) v = fmaxf(v, 0.f);
+          }
+          ocol[(size_t)(c + j) * args.n_out] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xFFFFu);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == W_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+}  // namespace f8s
+
+namespace f8 {
+
 // Per-row quantisation: one warp per row; s = max |w| / 448 (1 for a zero row),
 // q = E4M3 (round to nearest even, saturating) of w / s.
 __global__ void __launch_bounds__(256) quantize_rows_fp8_kernel(const uint16_t *__restrict__ w, int64_t rows, int cols,
@@ -416,6 +818,40 @@ static int make_map_bf16(CUtensorMap *m, const void *base, uint64_t rows, uint64
              : MOE_ERR_CUDA;
 }
 
+// bf16 [rows, cols], box 64 x box_rows, 128-byte swizzle (the token tile of the decode kernel)
+static int make_map_tokens(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return MOE_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (cols * 2) % 16 || !rows || !cols) return MOE_ERR_UNSUPPORTED;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+// E4M3 codes [rows, cols] bytes, box 64 x 128 with the 64-byte swizzle: the
+// 16-byte chunk c of row r lands at chunk c ^ ((r >> 1) & 3) of its 64-byte row
+// (the weight tile of the decode kernel)
+static int make_map_u8_sw64(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return MOE_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || cols % 16 || !rows || !cols) return MOE_ERR_UNSUPPORTED;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
 // E4M3 codes [rows, cols] bytes, box 64 x 128, no swizzle (the raw weight tile)
 static int make_map_u8(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
   EncodeTiledFn enc = get_encode();
@@ -453,17 +889,79 @@ static int launch(const CUtensorMap &ma, const CUtensorMap &mq0, const CUtensorM
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+template <int MODE, int NT>
+static int launch_decode(const CUtensorMap &ma, const CUtensorMap &mq0, const CUtensorMap &mq1,
+                         const f8s::Args &args, int dev, cudaStream_t stream) {
+  static std::mutex mu;
+  static std::vector<int> done;
+  constexpr size_t smem = f8s::Shape<MODE, NT>::SMEM;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if ((int)done.size() <= dev) done.resize(dev + 1, 0);
+    if (!done[dev]) {
+      if (cudaFuncSetAttribute(f8s::fp8_decode_kernel<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      done[dev] = 1;
+    }
+  }
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return MOE_ERR_CUDA;
+  f8s::fp8_decode_kernel<MODE, NT><<<sms, f8s::THREADS, smem, stream>>>(ma, mq0, mq1, args);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+template <int NT>
+static int run_decode(int mode, const void *A, int64_t a_rows, int K, const uint8_t *Q0, const float *S0,
+                      const uint8_t *Q1, const float *S1, int64_t b_rows_total, int b_rows_per_group,
+                      const int32_t *offsets, int G, int M, int n_out, void *out, int *status, int dev,
+                      cudaStream_t stream) {
+  CUtensorMap ma, mq0, mq1;
+  int rc;
+  if ((rc = make_map_tokens(&ma, A, (uint64_t)a_rows, (uint64_t)K, NT))) return rc;
+  if ((rc = make_map_u8_sw64(&mq0, Q0, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
+  if (mode == kSwiGLU) {
+    if ((rc = make_map_u8_sw64(&mq1, Q1, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
+  } else {
+    mq1 = mq0;
+  }
+  f8s::Args args{offsets, G, M, (int32_t)a_rows, n_out, b_rows_per_group, (K + f8s::KS - 1) / f8s::KS, S0, S1,
+                 static_cast<uint16_t *>(out), status};
+  switch (mode) {
+    case kSwiGLU: return launch_decode<kSwiGLU, NT>(ma, mq0, mq1, args, dev, stream);
+    case kReLU: return launch_decode<kReLU, NT>(ma, mq0, mq1, args, dev, stream);
+    default: return launch_decode<kPlain, NT>(ma, mq0, mq1, args, dev, stream);
+  }
+}
+
 }  // namespace f8
 
 int tc_grouped_gemm_fp8(int mode, const void *A, int64_t a_rows, int K, const uint8_t *Q0, const float *S0,
                         const uint8_t *Q1, const float *S1, int64_t b_rows_total, int b_rows_per_group,
-                        const int32_t *offsets, int G, int M, int n_out, void *out, int *status, cudaStream_t stream) {
+                        const int32_t *offsets, int G, int M, int n_out, int max_group_rows, void *out, int *status,
+                        cudaStream_t stream) {
   using namespace f8;
   if (G < 1 || G > MAX_GROUPS || K < 1 || n_out < 1 || a_rows < 1 || a_rows > INT32_MAX || b_rows_total < 1)
     return MOE_ERR_INVALID_ARG;
   if (mode < kSwiGLU || mode > kPlain || !Q0 || !S0 || (mode == kSwiGLU && (!Q1 || !S1)) ||
       n_out > b_rows_per_group || (int64_t)G * b_rows_per_group > b_rows_total || (n_out % 8))
     return MOE_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  // Groups of at most 64 rows (decode): weights on the M side, read once per group.
+  // Any group size is still correct there (larger groups take several token tiles).
+  switch (fp8_decode_tile_rows(max_group_rows)) {
+    case 16:
+      return run_decode<16>(mode, A, a_rows, K, Q0, S0, Q1, S1, b_rows_total, b_rows_per_group, offsets, G, M, n_out,
+                            out, status, dev, stream);
+    case 32:
+      return run_decode<32>(mode, A, a_rows, K, Q0, S0, Q1, S1, b_rows_total, b_rows_per_group, offsets, G, M, n_out,
+                            out, status, dev, stream);
+    case 64:
+      return run_decode<64>(mode, A, a_rows, K, Q0, S0, Q1, S1, b_rows_total, b_rows_per_group, offsets, G, M, n_out,
+                            out, status, dev, stream);
+    default: break;
+  }
   CUtensorMap ma, mq0, mq1;
   int rc;
   if ((rc = make_map_bf16(&ma, A, (uint64_t)a_rows, (uint64_t)K))) return rc;
@@ -473,8 +971,6 @@ int tc_grouped_gemm_fp8(int mode, const void *A, int64_t a_rows, int K, const ui
   } else {
     mq1 = mq0;
   }
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   Args args{offsets, G, M, (int32_t)a_rows, n_out, b_rows_per_group, (K + BK - 1) / BK, S0, S1,
             static_cast<uint16_t *>(out), status};
   switch (mode) {

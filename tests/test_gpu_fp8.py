@@ -35,11 +35,14 @@ def test_quantize_matches_oracle(shape, std):
     assert np.array_equal(q.cpu().numpy(), q_ref)
 
 
-def _fp8_ffn_case(N, counts, d, F, act, seed):
-    T = int(sum(counts))
-    cfg = moe.make_config(T, d, N, 1, F, 0, moe.GATE_SOFTMAX_TOPK,
+def _fp8_ffn_case(N, counts, d, F, act, seed, T=None, k=1):
+    """counts must sum to T * k (the routed rows); T bounds a group's rows for the kernel choice."""
+    R = int(sum(counts))
+    T = R if T is None else T
+    assert R == T * k
+    cfg = moe.make_config(T, d, N, k, F, 0, moe.GATE_SOFTMAX_TOPK,
                           moe.ACT_SWIGLU if act == "swiglu" else moe.ACT_RELU, moe.DTYPE_BF16, 0)
-    xp = synth.normal(seed, 99, (T, d), 1.0, "bf16")
+    xp = synth.normal(seed, 99, (R, d), 1.0, "bf16")
     w1 = synth.normal(seed, 3, (N, F, d), d ** -0.5, "bf16")
     w3 = synth.normal(seed, 4, (N, F, d), d ** -0.5, "bf16") if act == "swiglu" else None
     w2 = synth.normal(seed, 5, (N, d, F), F ** -0.5, "bf16")
@@ -47,7 +50,7 @@ def _fp8_ffn_case(N, counts, d, F, act, seed):
     q3, s3 = _quantize_on_gpu(w3) if w3 is not None else (None, None)
     offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     ws = torch.zeros(moe.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
-    y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((R, d), dtype=torch.bfloat16, device="cuda")
     moe.moe_expert_ffn_fp8(cfg, to_dev(xp, "bf16"), torch.from_numpy(offsets).cuda(), q1, s1, q3, s3, q2, s2, y, ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_OK
     y = to_np_f64(y)
@@ -72,6 +75,75 @@ def test_fp8_expert_ffn_ragged_groups(act):
 
 def test_fp8_expert_ffn_deep_k():
     _fp8_ffn_case(4, [40, 3, 200, 129], d=1024, F=512, act="swiglu", seed=3)
+
+
+# Decode-sized groups (at most 64 rows per group by the config's T): the weights
+# take the M side of the MMA and the tokens come in tiles of 16, 32 or 64 rows.
+# Groups larger than T (possible through moe_expert_ffn_fp8's own offsets) take
+# several token tiles; widths are not multiples of the 128-row or 128-wide K tiles.
+@pytest.mark.parametrize("act", ["swiglu", "relu"])
+@pytest.mark.parametrize("T,k,counts", [(16, 4, [0, 1, 40, 23]), (30, 3, [30, 0, 29, 31]),
+                                        (64, 2, [64, 0, 50, 14]), (5, 1, [0, 0, 5, 0])])
+def test_fp8_expert_ffn_decode_groups(act, T, k, counts):
+    _fp8_ffn_case(len(counts), counts, d=208, F=336, act=act, seed=4, T=T, k=k)
+
+
+def test_fp8_expert_ffn_decode_deep_k():
+    _fp8_ffn_case(4, [16, 3, 9, 4], d=1024, F=1536, act="swiglu", seed=5, T=16, k=2)
+
+
+_NAN_CODES = (0x7F, 0xFF)
+
+
+def _all_codes(n):
+    c = (np.arange(n) % 256).astype(np.uint8)
+    c[np.isin(c, _NAN_CODES)] = 0
+    return c
+
+
+@pytest.mark.parametrize("T", [16, 100])
+@pytest.mark.parametrize("path", ["down", "up"])
+def test_fp8_every_code_exact(T, path):
+    """Every finite E4M3 code through the weight converter, compared exactly.
+
+    One expert, d = F = 256, every token x = e_0.  W1[:, 0] = 16.0 makes the gate
+    pre-activation 16, whose SiLU rounds to 16 in float32; then
+      down: W3[5, 0] = 1 only, so h = 16 e_5, and y[n] = 16 s2[n] v(W2[n, 5]);
+      up:   W3[f, 0] = code f, W2 = I, so y[n] = bf16(silu(16) v(code n)) = 16 v(code n).
+    Each y is a short binary fraction, exact in bf16.  T = 16 runs the decode
+    kernel (weights on the M side), T = 100 the token-tile kernel.  The value of a
+    code comes from the oracle's E4M3 table.
+    """
+    d = F = 256
+    rng = np.random.default_rng(8)
+    finite = np.setdiff1d(np.arange(256), _NAN_CODES).astype(np.uint8)
+    rand = lambda shape: rng.choice(finite, size=shape).astype(np.uint8)
+    q1, q3, q2 = rand((1, F, d)), rand((1, F, d)), rand((1, d, F))
+    s1, s3, s2 = np.ones((1, F), np.float32), np.ones((1, F), np.float32), np.ones((1, d), np.float32)
+    q1[0, :, 0] = 0x58                                   # 16.0
+    if path == "down":
+        q3[0, :, 0] = 0
+        q3[0, 5, 0] = 0x38                               # 1.0
+        q2[0, :, 5] = _all_codes(d)
+        s2[0] = 2.0 ** (np.arange(d) % 5 - 2)
+        expect = 16.0 * s2[0].astype(np.float64) * oracle.e4m3_value(q2[0, :, 5])
+    else:
+        q3[0, :, 0] = _all_codes(F)
+        q2[0] = 0
+        q2[0, np.arange(d), np.arange(d)] = 0x38
+        expect = 16.0 * oracle.e4m3_value(q3[0, :, 0])
+    x = np.zeros((T, d), np.float32)
+    x[:, 0] = 1.0
+    cfg = moe.make_config(T, d, 1, 1, F)
+    ws = torch.zeros(moe.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    y = torch.empty((T, d), dtype=torch.bfloat16, device="cuda")
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    offsets = dev(np.array([0, T], np.int32))
+    moe.moe_expert_ffn_fp8(cfg, torch.from_numpy(x).to(torch.bfloat16).cuda(), offsets, dev(q1), dev(s1), dev(q3),
+                           dev(s3), dev(q2), dev(s2), y, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_OK
+    got = y.float().cpu().numpy().astype(np.float64)
+    assert np.array_equal(got, np.broadcast_to(expect, got.shape))
 
 
 def _fp8_layer_check(inp, sample=None):
@@ -105,6 +177,17 @@ def _fp8_layer_check(inp, sample=None):
 def test_fp8_layer_small(kw):
     kw = dict(kw)
     wl = synth.Workload("fp8", 23, act=kw.pop("act", "swiglu"), gate=kw.pop("gate", "softmax"), dtype="bf16", **kw)
+    _fp8_layer_check(synth.make_inputs(wl))
+
+
+@pytest.mark.parametrize("kw", [
+    dict(T=16, d=256, N=8, k=2, F=384),
+    dict(T=48, d=512, N=16, k=4, F=256, gate="sigmoid", shared_F=384, sel_bias_range=0.05),
+    dict(T=30, d=256, N=8, k=3, F=128, capacity_factor=0.75, zipf_s=1.2, act="relu"),
+])
+def test_fp8_layer_decode_sized(kw):
+    kw = dict(kw)
+    wl = synth.Workload("fp8d", 29, act=kw.pop("act", "swiglu"), gate=kw.pop("gate", "softmax"), dtype="bf16", **kw)
     _fp8_layer_check(synth.make_inputs(wl))
 
 
