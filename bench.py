@@ -65,8 +65,11 @@ def layer_bytes(wl, touched_experts: int, fp8: bool = False) -> float:
 # dram__bytes_read.sum + dram__bytes_write.sum of the two grouped-GEMM launches of
 # one step, from one ncu capture of the kernel revision named here (None once the
 # kernel changes until it is captured again).
-NCU_TRAFFIC = {"mixtral_prefill": {"bytes": 3.819e9, "kernel_rev": "pair1"}}
-KERNEL_REV = "pair1"
+# DRAM bytes (read + write) of the expert-FFN launches per step, from ncu captures of
+# the kernels as they stand (profiles/); keyed by (workload, FP8 weights).
+NCU_TRAFFIC = {("mixtral_prefill", False): {"bytes": 3.689e9, "kernel_rev": "pair2"},
+               ("mixtral_decode", True): {"bytes": 1.420e9, "kernel_rev": "fp8dec1"}}
+KERNEL_REV = {False: "pair2", True: "fp8dec1"}
 
 
 def stage_work(wl, kept_rows: int, touched: int, fp8: bool = False) -> dict:
@@ -134,9 +137,9 @@ def blas_threads() -> int:
         return os.cpu_count() or 1
 
 
-def _traffic(name):
-    t = NCU_TRAFFIC.get(name)
-    return t["bytes"] if t and t["kernel_rev"] == KERNEL_REV else None
+def _traffic(name, fp8: bool = False):
+    t = NCU_TRAFFIC.get((name, fp8))
+    return t["bytes"] if t and t["kernel_rev"] == KERNEL_REV[fp8] else None
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -458,7 +461,7 @@ def run_ours(args, wl, dist, rank, local):
                                 alu=f32 and n in ("route", "expert_ffn", "shared_ffn")) for n in stages}
     ffn = stages["expert_ffn"]
     roof = {"bound": ffn["bound"], "achieved": ffn["achieved"], "peak": ffn["peak"], "unit": ffn["unit"],
-            "frac": ffn["frac"], "traffic": None if args.fp8 else _traffic(wl.name),
+            "frac": ffn["frac"], "traffic": _traffic(wl.name, args.fp8),
             "kernel": (("fp8_decode_kernel (tcgen05, E4M3 weights converted into tensor memory as the A operand)"
                         if wl.T <= 64 else
                         "grouped_gemm_fp8 (tcgen05, E4M3 weights converted into a shared-memory B operand)") +
