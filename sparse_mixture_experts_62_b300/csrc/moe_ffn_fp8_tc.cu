@@ -446,6 +446,19 @@ __device__ __forceinline__ void e4m3x4_to_bf16(uint32_t w, uint32_t &lo, uint32_
   lo = bf16x2_mul_exact((a & 0x80008000u) | ((a >> 4) & 0x07F007F0u), 0x7B807B80u);  // x 2^120
   hi = bf16x2_mul_exact((b & 0x80008000u) | ((b >> 4) & 0x07F007F0u), 0x7B807B80u);
 }
+// The same bits by integer multiply-add, which runs on the FMA pipe instead of the
+// integer-logic pipe: with x = code1 << 16 | code0, code << 4 puts exponent field
+// and mantissa at bits 10-4 and the sign at bit 11, and adding 0x7800 for a set
+// sign carries it to bit 15.  The decoders send one word in four this way: the
+// logic pipe is the busiest one in the gate/up launch (three quarters of its
+// cycles), and the multiply form's longer dependency chain costs more than it
+// saves when used for half the words or more (measured).
+__device__ __forceinline__ void e4m3x4_to_bf16_fma(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t a = __byte_perm(w, 0u, 0x4140);  // code1 << 16 | code0
+  const uint32_t b = __byte_perm(w, 0u, 0x4342);  // code3 << 16 | code2
+  lo = bf16x2_mul_exact(a * 16u + (a & 0x00800080u) * 240u, 0x7B807B80u);
+  hi = bf16x2_mul_exact(b * 16u + (b & 0x00800080u) * 240u, 0x7B807B80u);
+}
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {
   asm volatile(
@@ -643,7 +656,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             e4m3x4_to_bf16(v.x, o[8 * ch + 0], o[8 * ch + 1]);
             e4m3x4_to_bf16(v.y, o[8 * ch + 2], o[8 * ch + 3]);
             e4m3x4_to_bf16(v.z, o[8 * ch + 4], o[8 * ch + 5]);
-            e4m3x4_to_bf16(v.w, o[8 * ch + 6], o[8 * ch + 7]);
+            e4m3x4_to_bf16_fma(v.w, o[8 * ch + 6], o[8 * ch + 7]);
           }
           tmem_st32(lane_base + (uint32_t)(as * S::ACOLS + b * 32), o);
         }
