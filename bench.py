@@ -68,8 +68,8 @@ def layer_bytes(wl, touched_experts: int, fp8: bool = False) -> float:
 # DRAM bytes (read + write) of the expert-FFN launches per step, from ncu captures of
 # the kernels as they stand (profiles/); keyed by (workload, FP8 weights).
 NCU_TRAFFIC = {("mixtral_prefill", False): {"bytes": 3.689e9, "kernel_rev": "pair2"},
-               ("mixtral_decode", True): {"bytes": 1.420e9, "kernel_rev": "fp8dec1"}}
-KERNEL_REV = {False: "pair2", True: "fp8dec1"}
+               ("mixtral_decode", True): {"bytes": 1.4267e9, "kernel_rev": "fp8ffn1"}}
+KERNEL_REV = {False: "pair2", True: "fp8ffn1"}
 
 
 def stage_work(wl, kept_rows: int, touched: int, fp8: bool = False) -> dict:
@@ -462,10 +462,11 @@ def run_ours(args, wl, dist, rank, local):
     ffn = stages["expert_ffn"]
     roof = {"bound": ffn["bound"], "achieved": ffn["achieved"], "peak": ffn["peak"], "unit": ffn["unit"],
             "frac": ffn["frac"], "traffic": _traffic(wl.name, args.fp8),
-            "kernel": (("fp8_decode_kernel (tcgen05, E4M3 weights converted into tensor memory as the A operand)"
+            "kernel": (("fp8_ffn_decode_kernel (tcgen05, E4M3 weights converted into tensor memory as the A "
+                         "operand), moe_expert_ffn_fp8: gate/up and down in one cooperative launch")
                         if wl.T <= 64 else
-                        "grouped_gemm_fp8 (tcgen05, E4M3 weights converted into a shared-memory B operand)") +
-                       ", moe_expert_ffn_fp8: gate/up + down launches" if args.fp8 else
+                        "grouped_gemm_fp8 (tcgen05, E4M3 weights converted into a shared-memory B operand), "
+                        "moe_expert_ffn_fp8: gate/up + down launches") if args.fp8 else
                        "grouped_gemm (tcgen05), moe_expert_ffn: gate/up + down launches"),
             "peak_source": ("derived float32 CUDA-core peak (148 SMs x 128 lanes x 2 FLOP x 2032 MHz)"
                             if ffn["bound"] == "alu" else f"{peak_src} " + ("hbm_gbs" if ffn["bound"] == "hbm" else
@@ -547,7 +548,8 @@ def run_ours(args, wl, dist, rank, local):
 
     # route: split W_g + tensor-core logits + top-k (bf16) or logits + top-k (float32);
     # dispatch: histogram, scan, rank, gather; experts: 2; shared: 2; combine: 1; stats: 2
-    launches_per_step = (3 if wl.dtype == "bf16" else 2) + 4 + 2 + (2 if has_shared else 0) + 1 + 2
+    ffn_launches = 1 if (args.fp8 and wl.T <= 64) else 2  # FP8 decode: gate/up and down in one launch
+    launches_per_step = (3 if wl.dtype == "bf16" else 2) + 4 + ffn_launches + (2 if has_shared else 0) + 1 + 2
     if rank == 0:
         sys.stderr.write("per-stage ms: " + json.dumps({k: round(val, 4) for k, val in stage_ms.items()}) + "\n")
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,

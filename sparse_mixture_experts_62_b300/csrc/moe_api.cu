@@ -99,7 +99,7 @@ int layout(const moe_config *c, moe_ws_layout *L) {
   L->y_perm = take(rows * d * es);
   L->h_shared = take(Fs ? T * Fs * es : 0);
   L->y_shared = take(Fs ? T * d * es : 0);
-  L->scratch = take(align256(2 * nch_d * N * 4) + stats_bytes(c) + router_scratch_bytes(c));
+  L->scratch = take(align256(2 * nch_d * N * 4) + stats_bytes(c) + router_scratch_bytes(c) + align256(N * 4));
   L->total = o;
   return MOE_OK;
 }
@@ -134,6 +134,8 @@ struct Ws {
     const size_t Np = (size_t)router_tc_npad(c->N), dp = (size_t)router_tc_dpad(c->d);
     return at<float>(router_off(c) + align256(Np * 3 * dp * 2));
   }
+  // N counters of the one-launch FP8 decode FFN (zeroed before each launch)
+  int *fp8_dep(const moe_config *c) const { return at<int>(router_off(c) + router_scratch_bytes(c)); }
 };
 
 int make_ws(const moe_config *c, void *ws, Ws *w) {
@@ -190,10 +192,13 @@ int ffn_routed_fp8(const moe_config *c, const Ws &w, const void *x_perm, const i
   const int64_t rows = routed_rows(c);
   const int mode1 = c->act == MOE_ACT_SWIGLU ? 0 : 1;
   const int bound = group_bound(c);
+  if (fp8_decode_tile_rows(bound))  // decode-sized groups: both GEMMs in one launch, weights on the M side
+    return tc_expert_ffn_fp8_decode(mode1, x_perm, h, rows, c->d, c->ffn, bound, f.w1q, f.w1s, f.w3q, f.w3s, f.w2q,
+                                    f.w2s, offsets, c->N, y_perm, w.fp8_dep(c), w.status(), s);
   MOE_TRY(tc_grouped_gemm_fp8(mode1, x_perm, rows, c->d, f.w1q, f.w1s, f.w3q, f.w3s, (int64_t)c->N * c->ffn, c->ffn,
-                              offsets, c->N, 0, c->ffn, bound, h, w.status(), s));
+                              offsets, c->N, 0, c->ffn, h, w.status(), s));
   return tc_grouped_gemm_fp8(2, h, rows, c->ffn, f.w2q, f.w2s, nullptr, nullptr, (int64_t)c->N * c->d, c->d, offsets,
-                             c->N, 0, c->d, bound, y_perm, w.status(), s);
+                             c->N, 0, c->d, y_perm, w.status(), s);
 }
 
 int ffn_shared(const moe_config *c, const void *x, const void *sw1, const void *sw3, const void *sw2, void *h,

@@ -369,8 +369,9 @@ __global__ void __launch_bounds__(THREADS, 1)
 }  // namespace f8
 
 // ---------------------------------------------------------------------------
-// The same product for groups of at most a few dozen rows (decode): the weights
-// take the M side of the MMA and the group's tokens the N side,
+// The whole expert FFN for groups of at most a few dozen rows (decode), in one
+// persistent launch.  The weights take the M side of the MMA and the group's
+// tokens the N side,
 //   D[n, t] = sum_k q[n, k] A[t, k]   (M = 128 weight rows, N = NT tokens),
 // and the converted weights never touch shared memory: each converter thread
 // turns its weight row's codes into bf16 in registers and writes them with
@@ -380,51 +381,64 @@ __global__ void __launch_bounds__(THREADS, 1)
 // each in a ring of its own.
 //   warps 0-3    epilogue (one TMEM lane quadrant each)
 //   warps 4-11   converters, two sets of four taking alternate stages
-//   warp 12      TMA producer of the codes of one 128-wide K stage
+//   warp 12      TMA producer of the codes of a stage
 //   warp 13      TMEM owner and MMA issuer
 //   warp 14      TMA producer of the stage's token tile
-// One stage covers K = 128: 128 weight rows x 128 codes per weight (two 64-byte
-// boxes), and NT token rows x 128 bf16 (two 128-byte-swizzled boxes).
+// A stage is four 128 x 64-byte boxes of codes: W1 and W3 over K = 128 for the
+// SwiGLU gate/up product, else one weight over K = 256.
+//
+// Phase 0 (gate/up: h = act(x W1^T, x W3^T)) and phase 1 (down: y = h W2^T) run in
+// one tile list, phase 0 first, dealt round-robin to the CTAs, so that the last,
+// partial round of gate/up tiles overlaps down tiles instead of leaving SMs idle.
+// A down tile of expert g reads rows of h written by all gate/up tiles of g: each
+// gate/up epilogue warp counts its stores into dep[g] (fence, then an atomic add);
+// the token producer of a down tile waits until dep[g] is complete (acquire load,
+// bounded like every wait), then orders those writes before its TMA reads
+// (fence.proxy.async.global).  The launch is cooperative: all CTAs are resident,
+// and a CTA reaches its down tiles only after its own gate/up tiles, so the
+// counters always complete.
 namespace f8s {
 
-using f8::kPlain;
 using f8::kReLU;
 using f8::kSwiGLU;
 
-constexpr int BMW = 128, KS = 128, MAX_GROUPS = 257;
+constexpr int BMW = 128, MAX_GROUPS = 257;
 constexpr int W_TMA = 12, W_MMA = 13, W_TOK = 14, THREADS = 480;
-constexpr int BOX_BYTES = BMW * 64;  // one 128 x 64 box of codes
+constexpr int BOX_BYTES = BMW * 64;        // one 128 x 64 box of codes
+constexpr int CODE_BYTES = 4 * BOX_BYTES;  // one stage of codes
+constexpr int ACOLS = 128;                 // TMEM columns of one converted stage
 
-template <int MODE, int NT>
+template <int NT>
 struct Shape {
-  static constexpr int NW = MODE == kSwiGLU ? 2 : 1;  // weights streamed per stage
-  static constexpr int NB = 2 * NW;                   // 128 x 64 boxes of codes per stage
-  static constexpr int CODE_BYTES = NW * BMW * KS;
-  static constexpr int TOK_BYTES = NT * KS * 2;
+  static constexpr int TOK_BYTES = 4 * NT * 128;  // up to four 64-wide token boxes
   // Codes and tokens have rings of their own: a code stage is free once converted,
   // a token stage once its MMAs are done.
-  static constexpr int NTR = NT <= 32 ? 8 : 4;
-  static constexpr int NR_FIT = (196608 - NTR * TOK_BYTES) / CODE_BYTES;
-  static constexpr int NR = NR_FIT < 12 ? NR_FIT : 12;
+  static constexpr int NTR = NT <= 32 ? 4 : 3;
+  static constexpr int NR = (196608 - NTR * TOK_BYTES) / CODE_BYTES;
   static constexpr int RING = NR * CODE_BYTES + NTR * TOK_BYTES;
-  static constexpr int ACOLS = NW * KS / 2;  // TMEM columns of one converted stage
-  static constexpr int DCOLS = 4 * NT;       // two accumulators of 2 x NT columns
+  static constexpr int DCOLS = 4 * NT;  // two accumulators of 2 x NT columns
   static constexpr int NA = (512 - DCOLS) / ACOLS;
-  static constexpr size_t SMEM = 1024 + (size_t)RING + 512 + (size_t)(4 * MAX_GROUPS + 8) * 4;
-  static_assert(CODE_BYTES % 1024 == 0 && TOK_BYTES % 1024 == 0 && NA >= 2 && NR >= 3, "stage layout");
+  static constexpr size_t SMEM = 1024 + (size_t)RING + 512 + (size_t)(5 * MAX_GROUPS + 8) * 4;
+  static_assert(TOK_BYTES % 1024 == 0 && NA >= 2 && NR >= 3, "stage layout");
+};
+
+struct Phase {
+  int32_t n_out;   // output features
+  int32_t b_rows;  // weight rows per group
+  int32_t num_kb;  // stages
+  int32_t nw;      // weights per stage: 2 (W1 and W3, K = 128) or 1 (K = 256)
+  const float *s0;
+  const float *s1;
+  uint16_t *out;   // [a_rows, n_out] bf16
 };
 
 struct Args {
-  const int32_t *offsets;
+  const int32_t *offsets;  // [G + 1] group row offsets
   int32_t G;
-  int32_t M;
   int32_t a_rows;
-  int32_t n_out;
-  int32_t b_rows;
-  int32_t num_kb;   // stages of K = 128
-  const float *scale0;
-  const float *scale1;
-  uint16_t *out;
+  int32_t act;             // kSwiGLU or kReLU (phase 0)
+  Phase ph[2];
+  int *dep;                // [G] gate/up epilogue-warp completions per group, zero at launch
   int *status;
 };
 
@@ -496,17 +510,61 @@ __device__ __forceinline__ void tc_mma_bf16_ta(uint32_t tmem_d, uint32_t tmem_a,
       : "memory");
 }
 
-template <int MODE, int NT>
+// Wait until *counter >= target (acquire, GPU scope); false (and MOE_ERR_TIMEOUT)
+// past the wait limit.
+__device__ __forceinline__ bool wait_count(const int *counter, int target, int *status) {
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    if (v >= target) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      set_status(status, MOE_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(200);
+  }
+}
+
+// The tile list: phase-0 tiles of every group, then phase-1 tiles; within a phase
+// and group, weight tile-major over token tiles.
+struct Tiles {
+  const int *start0, *start1, *ttiles;  // per-group first tile of each phase; token tiles per group
+  int total0, total;
+  int w_tiles[2];
+  struct Tile {
+    int phase, g, wt, tt;
+  };
+  // Resolves tile t; `g` is a cursor that only moves forward within a phase.
+  __device__ Tile at(int t, int &g, int &phase_seen) const {
+    Tile r;
+    r.phase = t < total0 ? 0 : 1;
+    if (r.phase != phase_seen) {
+      phase_seen = r.phase;
+      g = 0;
+    }
+    const int *st = r.phase ? start1 : start0;
+    while (t >= st[g + 1]) ++g;
+    const int local = t - st[g];
+    r.g = g;
+    r.wt = local / ttiles[g];
+    r.tt = local - r.wt * ttiles[g];
+    return r;
+  }
+};
+
+template <int NT>
 __global__ void __launch_bounds__(THREADS, 1)
-    fp8_decode_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmQ0,
-                      const __grid_constant__ CUtensorMap tmQ1, const Args args) {
-  using S = Shape<MODE, NT>;
+    fp8_ffn_decode_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmH,
+                          const __grid_constant__ CUtensorMap tmQ1, const __grid_constant__ CUtensorMap tmQ3,
+                          const __grid_constant__ CUtensorMap tmQ2, const Args args) {
+  using S = Shape<NT>;
   constexpr int NR = S::NR, NA = S::NA, NTR = S::NTR;
   constexpr uint32_t IDESC = idesc_bf16_f32(BMW, NT);
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
-  uint8_t *tok_ring = smem + NR * S::CODE_BYTES;
+  uint8_t *tok_ring = smem + NR * CODE_BYTES;
   uint64_t *r_full = reinterpret_cast<uint64_t *>(smem + S::RING);
   uint64_t *r_empty = r_full + NR;
   uint64_t *k_full = r_empty + NR;
@@ -517,15 +575,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *tempty = tfull + 2;
   uint64_t *done = tempty + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
-  int *tile_start = reinterpret_cast<int *>(smem + S::RING + 512);
-  int *ttiles = tile_start + MAX_GROUPS + 1;
+  int *start0 = reinterpret_cast<int *>(smem + S::RING + 512);
+  int *start1 = start0 + MAX_GROUPS + 1;
+  int *ttiles = start1 + MAX_GROUPS + 1;
   int *rowbeg = ttiles + MAX_GROUPS;
   int *rowend = rowbeg + MAX_GROUPS;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = args.G;
-  const int w_tiles = (args.n_out + BMW - 1) / BMW;
-  const int num_kb = args.num_kb;
+  Tiles tl;
+  tl.w_tiles[0] = (args.ph[0].n_out + BMW - 1) / BMW;
+  tl.w_tiles[1] = (args.ph[1].n_out + BMW - 1) / BMW;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NR; ++s) {
@@ -546,10 +606,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     mbar_init(done, 1);
     fence_barrier_init();
-    int acc = 0;
+    int acc0 = 0, acc1 = 0;
     for (int g = 0; g < G; ++g) {
-      int b = args.offsets ? args.offsets[g] : 0;
-      int e = args.offsets ? args.offsets[g + 1] : args.M;
+      int b = args.offsets[g], e = args.offsets[g + 1];
       if (b < 0 || e < b || e > args.a_rows) {
         set_status(args.status, MOE_ERR_BOUNDS);
         b = e = 0;
@@ -558,23 +617,34 @@ __global__ void __launch_bounds__(THREADS, 1)
       rowend[g] = e;
       const int tt = (e - b + NT - 1) / NT;
       ttiles[g] = tt;
-      tile_start[g] = acc;
-      acc += tt * w_tiles;
+      start0[g] = acc0;
+      start1[g] = acc1;
+      acc0 += tt * tl.w_tiles[0];
+      acc1 += tt * tl.w_tiles[1];
     }
-    tile_start[G] = acc;
+    start0[G] = acc0;
+    start1[G] = acc1;
+    for (int g = 0; g <= G; ++g) start1[g] += acc0;  // phase-1 tiles follow all phase-0 tiles
   }
   if (warp == W_TMA && lane == 0) {
-    tma_prefetch_desc(&tmQ0);
-    if (MODE == kSwiGLU) tma_prefetch_desc(&tmQ1);
+    tma_prefetch_desc(&tmQ1);
+    if (args.act == kSwiGLU) tma_prefetch_desc(&tmQ3);
+    tma_prefetch_desc(&tmQ2);
   }
-  if (warp == W_TOK && lane == 0) tma_prefetch_desc(&tmA);
+  if (warp == W_TOK && lane == 0) {
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmH);
+  }
   if (warp == W_MMA) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-
-  const int total_tiles = tile_start[G];
+  tl.start0 = start0;
+  tl.start1 = start1;
+  tl.ttiles = ttiles;
+  tl.total0 = start0[G];
+  tl.total = start1[G];
 
   if (warp == W_TMA || warp == W_TOK) {
     // ------------------------------------------------------------ TMA producers: codes (W_TMA), tokens (W_TOK)
@@ -587,34 +657,42 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int s = 0; s < depth; ++s) issued_parity[s] = -1;
       int stage = 0;
       uint32_t phase = 0;
-      int g = 0;
+      int g = 0, seen = -1;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        while (t >= tile_start[g + 1]) ++g;
-        const int local = t - tile_start[g];
-        const int wt = local / ttiles[g];
-        const int tt = local - wt * ttiles[g];
-        const int w_row = g * args.b_rows + wt * BMW;
-        const int t_row = rowbeg[g] + tt * NT;
-        for (int kb = 0; kb < num_kb; ++kb) {
+      for (int t = blockIdx.x; ok && t < tl.total; t += gridDim.x) {
+        const Tiles::Tile tile = tl.at(t, g, seen);
+        const Phase &P = args.ph[tile.phase];
+        const int w_row = tile.g * P.b_rows + tile.wt * BMW;
+        const int t_row = rowbeg[tile.g] + tile.tt * NT;
+        const int ks = P.nw == 2 ? 128 : 256;  // K per stage
+        if (!codes && tile.phase == 1) {  // the h rows of this group are written by gate/up tiles
+          if (!wait_count(&args.dep[tile.g], 4 * tl.w_tiles[0] * ttiles[tile.g], args.status)) ok = false;
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        for (int kb = 0; ok && kb < P.num_kb; ++kb) {
           if (!mbar_wait(&emptyb[stage], phase ^ 1u, args.status)) {
             ok = false;
             break;
           }
           if (codes) {
-            uint8_t *st = smem + stage * S::CODE_BYTES;
-            mbar_arrive_expect_tx(&fullb[stage], S::CODE_BYTES);
+            uint8_t *st = smem + stage * CODE_BYTES;
+            mbar_arrive_expect_tx(&fullb[stage], CODE_BYTES);
+            if (P.nw == 2) {
+              tma_load_2d(st, &tmQ1, &fullb[stage], kb * ks, w_row);
+              tma_load_2d(st + BOX_BYTES, &tmQ1, &fullb[stage], kb * ks + 64, w_row);
+              tma_load_2d(st + 2 * BOX_BYTES, &tmQ3, &fullb[stage], kb * ks, w_row);
+              tma_load_2d(st + 3 * BOX_BYTES, &tmQ3, &fullb[stage], kb * ks + 64, w_row);
+            } else {
+              const CUtensorMap *q = tile.phase ? &tmQ2 : &tmQ1;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int x = kb * KS + h * 64;
-              tma_load_2d(st + h * BOX_BYTES, &tmQ0, &fullb[stage], x, w_row);
-              if (MODE == kSwiGLU) tma_load_2d(st + (2 + h) * BOX_BYTES, &tmQ1, &fullb[stage], x, w_row);
+              for (int b = 0; b < 4; ++b) tma_load_2d(st + b * BOX_BYTES, q, &fullb[stage], kb * ks + 64 * b, w_row);
             }
           } else {
             uint8_t *st = tok_ring + stage * S::TOK_BYTES;
-            mbar_arrive_expect_tx(&fullb[stage], S::TOK_BYTES);
-            tma_load_2d(st, &tmA, &fullb[stage], kb * KS, t_row);
-            tma_load_2d(st + NT * 128, &tmA, &fullb[stage], kb * KS + 64, t_row);
+            const int nb = ks / 64;
+            const CUtensorMap *m = tile.phase ? &tmH : &tmX;
+            mbar_arrive_expect_tx(&fullb[stage], (uint32_t)(nb * NT * 128));
+            for (int b = 0; b < nb; ++b) tma_load_2d(st + b * NT * 128, m, &fullb[stage], kb * ks + 64 * b, t_row);
           }
           issued_parity[stage] = (int)phase;
           if (++stage == depth) {
@@ -634,9 +712,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)S::DCOLS;
     const int swz = (r >> 1) & 3;
     int c = 0;  // stage counter of this CTA
+    int g = 0, seen = -1;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-      for (int kb = 0; kb < num_kb; ++kb, ++c) {
+    for (int t = blockIdx.x; ok && t < tl.total; t += gridDim.x) {
+      const Tiles::Tile tile = tl.at(t, g, seen);
+      const int nkb = args.ph[tile.phase].num_kb;
+      for (int kb = 0; kb < nkb; ++kb, ++c) {
         if ((c & 1) != set) continue;
         const int rs = c % NR, as = c % NA;
         const uint32_t rph = (uint32_t)(c / NR) & 1u, aph = (uint32_t)(c / NA) & 1u;
@@ -646,9 +727,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint8_t *st = smem + rs * S::CODE_BYTES + r * 64;
+        const uint8_t *st = smem + rs * CODE_BYTES + r * 64;
 #pragma unroll
-        for (int b = 0; b < S::NB; ++b) {  // boxes: weight b / 2, K half b % 2
+        for (int b = 0; b < 4; ++b) {  // box b -> TMEM columns [32 b, 32 b + 32) of the slot
           uint32_t o[32];
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
@@ -658,7 +739,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             e4m3x4_to_bf16(v.z, o[8 * ch + 4], o[8 * ch + 5]);
             e4m3x4_to_bf16_fma(v.w, o[8 * ch + 6], o[8 * ch + 7]);
           }
-          tmem_st32(lane_base + (uint32_t)(as * S::ACOLS + b * 32), o);
+          tmem_st32(lane_base + (uint32_t)(as * ACOLS + b * 32), o);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
@@ -675,27 +756,38 @@ __global__ void __launch_bounds__(THREADS, 1)
       int ks = 0, as = 0;
       uint32_t kph = 0, aph = 0;
       int it = 0;
+      int g = 0, seen = -1;
       bool ok = true, issued = false;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++it) {
+      for (int t = blockIdx.x; ok && t < tl.total; t += gridDim.x, ++it) {
+        const Tiles::Tile tile = tl.at(t, g, seen);
+        const Phase &P = args.ph[tile.phase];
         const int acc = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
         if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, args.status)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + (uint32_t)(acc * 2 * NT);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < P.num_kb; ++kb) {
           if (!mbar_wait(&k_full[ks], kph, args.status) || !mbar_wait(&a_full[as], aph, args.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = tmem_base + (uint32_t)(S::DCOLS + as * S::ACOLS);
+          const uint32_t a0 = tmem_base + (uint32_t)(S::DCOLS + as * ACOLS);
           const uint32_t tok = smem_u32(tok_ring + ks * S::TOK_BYTES);
+          if (P.nw == 2) {  // W1 in columns 0-63 and W3 in 64-127, K = 128
 #pragma unroll
-          for (int kk = 0; kk < KS / 16; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(tok + (uint32_t)((kk >> 2) * NT * 128)) + 2ull * (kk & 3);
-            const uint32_t accum = (kb | kk) != 0;
-            tc_mma_bf16_ta(d0, a0 + 8u * kk, bdesc, IDESC, accum);
-            if (MODE == kSwiGLU) tc_mma_bf16_ta(d0 + NT, a0 + 64u + 8u * kk, bdesc, IDESC, accum);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t bdesc = smem_desc_sw128(tok + (uint32_t)((kk >> 2) * NT * 128)) + 2ull * (kk & 3);
+              const uint32_t accum = (kb | kk) != 0;
+              tc_mma_bf16_ta(d0, a0 + 8u * kk, bdesc, IDESC, accum);
+              tc_mma_bf16_ta(d0 + NT, a0 + 64u + 8u * kk, bdesc, IDESC, accum);
+            }
+          } else {  // one weight, K = 256
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+              const uint64_t bdesc = smem_desc_sw128(tok + (uint32_t)((kk >> 2) * NT * 128)) + 2ull * (kk & 3);
+              tc_mma_bf16_ta(d0, a0 + 8u * kk, bdesc, IDESC, (kb | kk) != 0);
+            }
           }
           issued = true;
           tc_commit(&a_empty[as]);
@@ -716,32 +808,32 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_wait(done, 0, args.status);
       }
     }
-  } else {
+  } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue (warps 0-3)
     const int quad = warp;
-    int g = 0;
+    int g = 0, seen = -1;
     int it = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
-      while (t >= tile_start[g + 1]) ++g;
-      const int local = t - tile_start[g];
-      const int wt = local / ttiles[g];
-      const int tt = local - wt * ttiles[g];
-      const int t_row = rowbeg[g] + tt * NT;
-      const int nvalid = min(NT, rowend[g] - t_row);
-      const int f = wt * BMW + quad * 32 + lane;
-      const bool f_ok = f < args.n_out;
-      const float s0 = f_ok ? args.scale0[(size_t)g * args.b_rows + f] : 0.f;
-      const float s1 = (MODE == kSwiGLU && f_ok) ? args.scale1[(size_t)g * args.b_rows + f] : 0.f;
+    for (int t = blockIdx.x; t < tl.total; t += gridDim.x, ++it) {
+      const Tiles::Tile tile = tl.at(t, g, seen);
+      const Phase &P = args.ph[tile.phase];
+      const int t_row = rowbeg[tile.g] + tile.tt * NT;
+      const int nvalid = min(NT, rowend[tile.g] - t_row);
+      const int f = tile.wt * BMW + quad * 32 + lane;
+      const bool f_ok = f < P.n_out;
+      const bool glu = P.nw == 2;
+      const bool relu = tile.phase == 0 && args.act == kReLU;
+      const float s0 = f_ok ? P.s0[(size_t)tile.g * P.b_rows + f] : 0.f;
+      const float s1 = (glu && f_ok) ? P.s1[(size_t)tile.g * P.b_rows + f] : 0.f;
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       if (!mbar_wait(&tfull[acc], use & 1u, args.status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (uint32_t)(acc * 2 * NT) + ((uint32_t)(quad * 32) << 16);
-      uint16_t *ocol = args.out + (size_t)t_row * args.n_out + f;
+      uint16_t *ocol = P.out + (size_t)t_row * P.n_out + f;
 #pragma unroll 1
       for (int c = 0; c < NT; c += 16) {
         float a[16], u[16];
-        if (MODE == kSwiGLU) {
+        if (glu) {
           tmem_ld16x2(taddr + c, taddr + NT + c, a, u);
         } else {
           tmem_ld16(taddr + c, a);
@@ -751,18 +843,23 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int j = 0; j < 16; ++j) {
           if (c + j >= nvalid) break;
           float v;
-          if (MODE == kSwiGLU) {
+          if (glu) {
             v = f8::silu(a[j] * s0) * (u[j] * s1);
           } else {
             v = a[j] * s0;
-            if (MODE == kReLU) v = fmaxf(v, 0.f);
+            if (relu) v = fmaxf(v, 0.f);
           }
-          ocol[(size_t)(c + j) * args.n_out] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xFFFFu);
+          ocol[(size_t)(c + j) * P.n_out] = (uint16_t)(pack_bf16x2(v, 0.f) & 0xFFFFu);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (tile.phase == 0) {  // publish this warp's rows of h to the down tiles of the group
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(&args.dep[tile.g], 1);
+      }
     }
   }
 
@@ -902,17 +999,18 @@ static int launch(const CUtensorMap &ma, const CUtensorMap &mq0, const CUtensorM
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-template <int MODE, int NT>
-static int launch_decode(const CUtensorMap &ma, const CUtensorMap &mq0, const CUtensorMap &mq1,
-                         const f8s::Args &args, int dev, cudaStream_t stream) {
+template <int NT>
+static int launch_ffn_decode(const CUtensorMap &mx, const CUtensorMap &mh, const CUtensorMap &mq1,
+                             const CUtensorMap &mq3, const CUtensorMap &mq2, const f8s::Args &args, int dev,
+                             cudaStream_t stream) {
   static std::mutex mu;
   static std::vector<int> done;
-  constexpr size_t smem = f8s::Shape<MODE, NT>::SMEM;
+  constexpr size_t smem = f8s::Shape<NT>::SMEM;
   {
     std::lock_guard<std::mutex> lk(mu);
     if ((int)done.size() <= dev) done.resize(dev + 1, 0);
     if (!done[dev]) {
-      if (cudaFuncSetAttribute(f8s::fp8_decode_kernel<MODE, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      if (cudaFuncSetAttribute(f8s::fp8_ffn_decode_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem) != cudaSuccess)
         return MOE_ERR_CUDA;
       done[dev] = 1;
@@ -920,39 +1018,65 @@ static int launch_decode(const CUtensorMap &ma, const CUtensorMap &mq0, const CU
   }
   const int sms = device_sm_count(dev);
   if (sms <= 0) return MOE_ERR_CUDA;
-  f8s::fp8_decode_kernel<MODE, NT><<<sms, f8s::THREADS, smem, stream>>>(ma, mq0, mq1, args);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f8s::fp8_ffn_decode_kernel<NT>, f8s::THREADS, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    return MOE_ERR_CUDA;
+  // Cooperative: every CTA resident at once, since down tiles wait for gate/up tiles of other CTAs.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sms);
+  cfg.blockDim = dim3(f8s::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, f8s::fp8_ffn_decode_kernel<NT>, mx, mh, mq1, mq3, mq2, args) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }
 
 template <int NT>
-static int run_decode(int mode, const void *A, int64_t a_rows, int K, const uint8_t *Q0, const float *S0,
-                      const uint8_t *Q1, const float *S1, int64_t b_rows_total, int b_rows_per_group,
-                      const int32_t *offsets, int G, int M, int n_out, void *out, int *status, int dev,
-                      cudaStream_t stream) {
-  CUtensorMap ma, mq0, mq1;
+static int run_ffn_decode(int act, const void *x, const void *h, int64_t rows, int d, int F, const uint8_t *w1q,
+                          const float *w1s, const uint8_t *w3q, const float *w3s, const uint8_t *w2q,
+                          const float *w2s, const int32_t *offsets, int G, void *y, int *dep, int *status, int dev,
+                          cudaStream_t stream) {
+  CUtensorMap mx, mh, mq1, mq3, mq2;
   int rc;
-  if ((rc = make_map_tokens(&ma, A, (uint64_t)a_rows, (uint64_t)K, NT))) return rc;
-  if ((rc = make_map_u8_sw64(&mq0, Q0, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
-  if (mode == kSwiGLU) {
-    if ((rc = make_map_u8_sw64(&mq1, Q1, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
+  if ((rc = make_map_tokens(&mx, x, (uint64_t)rows, (uint64_t)d, NT))) return rc;
+  if ((rc = make_map_tokens(&mh, h, (uint64_t)rows, (uint64_t)F, NT))) return rc;
+  if ((rc = make_map_u8_sw64(&mq1, w1q, (uint64_t)G * F, (uint64_t)d))) return rc;
+  if (act == kSwiGLU) {
+    if ((rc = make_map_u8_sw64(&mq3, w3q, (uint64_t)G * F, (uint64_t)d))) return rc;
   } else {
-    mq1 = mq0;
+    mq3 = mq1;
   }
-  f8s::Args args{offsets, G, M, (int32_t)a_rows, n_out, b_rows_per_group, (K + f8s::KS - 1) / f8s::KS, S0, S1,
-                 static_cast<uint16_t *>(out), status};
-  switch (mode) {
-    case kSwiGLU: return launch_decode<kSwiGLU, NT>(ma, mq0, mq1, args, dev, stream);
-    case kReLU: return launch_decode<kReLU, NT>(ma, mq0, mq1, args, dev, stream);
-    default: return launch_decode<kPlain, NT>(ma, mq0, mq1, args, dev, stream);
-  }
+  if ((rc = make_map_u8_sw64(&mq2, w2q, (uint64_t)G * d, (uint64_t)F))) return rc;
+  const bool glu = act == kSwiGLU;
+  f8s::Args args{};
+  args.offsets = offsets;
+  args.G = G;
+  args.a_rows = (int32_t)rows;
+  args.act = act;
+  // phase 0: h = act(x W1^T [, x W3^T]); K = d in stages of 128 (two weights) or 256
+  args.ph[0] = f8s::Phase{F, F, glu ? (d + 127) / 128 : (d + 255) / 256, glu ? 2 : 1, w1s, glu ? w3s : nullptr,
+                          static_cast<uint16_t *>(const_cast<void *>(h))};
+  // phase 1: y = h W2^T; K = F in stages of 256
+  args.ph[1] = f8s::Phase{d, d, (F + 255) / 256, 1, w2s, nullptr, static_cast<uint16_t *>(y)};
+  args.dep = dep;
+  args.status = status;
+  if (cudaMemsetAsync(dep, 0, (size_t)G * sizeof(int), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return launch_ffn_decode<NT>(mx, mh, mq1, mq3, mq2, args, dev, stream);
 }
 
 }  // namespace f8
 
 int tc_grouped_gemm_fp8(int mode, const void *A, int64_t a_rows, int K, const uint8_t *Q0, const float *S0,
                         const uint8_t *Q1, const float *S1, int64_t b_rows_total, int b_rows_per_group,
-                        const int32_t *offsets, int G, int M, int n_out, int max_group_rows, void *out, int *status,
-                        cudaStream_t stream) {
+                        const int32_t *offsets, int G, int M, int n_out, void *out, int *status, cudaStream_t stream) {
   using namespace f8;
   if (G < 1 || G > MAX_GROUPS || K < 1 || n_out < 1 || a_rows < 1 || a_rows > INT32_MAX || b_rows_total < 1)
     return MOE_ERR_INVALID_ARG;
@@ -961,20 +1085,6 @@ int tc_grouped_gemm_fp8(int mode, const void *A, int64_t a_rows, int K, const ui
     return MOE_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  // Groups of at most 64 rows (decode): weights on the M side, read once per group.
-  // Any group size is still correct there (larger groups take several token tiles).
-  switch (fp8_decode_tile_rows(max_group_rows)) {
-    case 16:
-      return run_decode<16>(mode, A, a_rows, K, Q0, S0, Q1, S1, b_rows_total, b_rows_per_group, offsets, G, M, n_out,
-                            out, status, dev, stream);
-    case 32:
-      return run_decode<32>(mode, A, a_rows, K, Q0, S0, Q1, S1, b_rows_total, b_rows_per_group, offsets, G, M, n_out,
-                            out, status, dev, stream);
-    case 64:
-      return run_decode<64>(mode, A, a_rows, K, Q0, S0, Q1, S1, b_rows_total, b_rows_per_group, offsets, G, M, n_out,
-                            out, status, dev, stream);
-    default: break;
-  }
   CUtensorMap ma, mq0, mq1;
   int rc;
   if ((rc = make_map_bf16(&ma, A, (uint64_t)a_rows, (uint64_t)K))) return rc;
@@ -990,6 +1100,31 @@ int tc_grouped_gemm_fp8(int mode, const void *A, int64_t a_rows, int K, const ui
     case kSwiGLU: return launch<kSwiGLU>(ma, mq0, mq1, args, dev, stream);
     case kReLU: return launch<kReLU>(ma, mq0, mq1, args, dev, stream);
     default: return launch<kPlain>(ma, mq0, mq1, args, dev, stream);
+  }
+}
+
+int tc_expert_ffn_fp8_decode(int act, const void *x_perm, void *h, int64_t rows, int d, int F, int max_group_rows,
+                             const uint8_t *w1q, const float *w1s, const uint8_t *w3q, const float *w3s,
+                             const uint8_t *w2q, const float *w2s, const int32_t *offsets, int G, void *y, int *dep,
+                             int *status, cudaStream_t stream) {
+  using namespace f8;
+  if (G < 1 || G > f8s::MAX_GROUPS || rows < 1 || rows > INT32_MAX || d < 8 || F < 8 || (d % 8) || (F % 8) ||
+      !offsets || !dep || !w1q || !w1s || !w2q || !w2s || (act == kSwiGLU && (!w3q || !w3s)) ||
+      (act != kSwiGLU && act != kReLU))
+    return MOE_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  switch (fp8_decode_tile_rows(max_group_rows)) {
+    case 16:
+      return run_ffn_decode<16>(act, x_perm, h, rows, d, F, w1q, w1s, w3q, w3s, w2q, w2s, offsets, G, y, dep, status,
+                                dev, stream);
+    case 32:
+      return run_ffn_decode<32>(act, x_perm, h, rows, d, F, w1q, w1s, w3q, w3s, w2q, w2s, offsets, G, y, dep, status,
+                                dev, stream);
+    case 64:
+      return run_ffn_decode<64>(act, x_perm, h, rows, d, F, w1q, w1s, w3q, w3s, w2q, w2s, offsets, G, y, dep, status,
+                                dev, stream);
+    default: return MOE_ERR_INVALID_ARG;
   }
 }
 

@@ -38,15 +38,20 @@ int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *
                     void *out, int *status, bool pair_tiles, cudaStream_t stream);
 // The forward GEMM (modes 0-2) with FP8 E4M3 weights Q [G * b_rows, K] bytes and
 // per-row float32 scales S [G * b_rows]: out = EPI(S[n] * sum_k A[r, k] Q[n, k]).
-// Groups of at most 64 rows (max_group_rows >= 0) run the decode kernel (weights on
-// the M side) with token tiles of fp8_decode_tile_rows() rows (0: not a decode shape).
+// FP8 expert FFN: the two GEMMs for groups of any size, with tokens on the M side.
+int tc_grouped_gemm_fp8(int mode, const void *A, int64_t a_rows, int K, const uint8_t *Q0, const float *S0,
+                        const uint8_t *Q1, const float *S1, int64_t b_rows_total, int b_rows_per_group,
+                        const int32_t *offsets, int G, int M, int n_out, void *out, int *status, cudaStream_t stream);
+// The whole FP8 expert FFN in one launch when no group exceeds 64 rows (decode):
+// weights on the M side, token tiles of fp8_decode_tile_rows(max_group_rows) rows
+// (0: not a decode shape).  dep: G ints of scratch.
 inline int fp8_decode_tile_rows(int max_group_rows) {
   return max_group_rows < 0 ? 0 : max_group_rows <= 16 ? 16 : max_group_rows <= 32 ? 32 : max_group_rows <= 64 ? 64 : 0;
 }
-int tc_grouped_gemm_fp8(int mode, const void *A, int64_t a_rows, int K, const uint8_t *Q0, const float *S0,
-                        const uint8_t *Q1, const float *S1, int64_t b_rows_total, int b_rows_per_group,
-                        const int32_t *offsets, int G, int M, int n_out, int max_group_rows, void *out, int *status,
-                        cudaStream_t stream);
+int tc_expert_ffn_fp8_decode(int act, const void *x_perm, void *h, int64_t rows, int d, int F, int max_group_rows,
+                             const uint8_t *w1q, const float *w1s, const uint8_t *w3q, const float *w3s,
+                             const uint8_t *w2q, const float *w2s, const int32_t *offsets, int G, void *y, int *dep,
+                             int *status, cudaStream_t stream);
 int launch_quantize_fp8(const void *w, int64_t rows, int cols, uint8_t *q, float *scales, cudaStream_t s);
 // The gate/up GEMM recomputed for the backward with the activation's backward
 // fused into its epilogue: a = A W1_g^T (and u = A W3_g^T), dh [rows, F] read,
