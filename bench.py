@@ -462,12 +462,12 @@ def run_ours(args, wl, dist, rank, local):
     ffn = stages["expert_ffn"]
     roof = {"bound": ffn["bound"], "achieved": ffn["achieved"], "peak": ffn["peak"], "unit": ffn["unit"],
             "frac": ffn["frac"], "traffic": _traffic(wl.name, args.fp8),
-            "kernel": (("fp8_ffn_decode_kernel (tcgen05, E4M3 weights converted into tensor memory as the A "
-                         "operand), moe_expert_ffn_fp8: gate/up and down in one cooperative launch")
-                        if wl.T <= 64 else
-                        "grouped_gemm_fp8 (tcgen05, E4M3 weights converted into a shared-memory B operand), "
-                        "moe_expert_ffn_fp8: gate/up + down launches") if args.fp8 else
-                       "grouped_gemm (tcgen05), moe_expert_ffn: gate/up + down launches"),
+            "kernel": ((("fp8_ffn_decode_kernel (tcgen05, E4M3 weights converted into tensor memory as the A "
+                          "operand), moe_expert_ffn_fp8: gate/up and down in one cooperative launch")
+                         if wl.T <= 64 else
+                         ("grouped_gemm_fp8 (tcgen05, E4M3 weights converted into a shared-memory B operand), "
+                          "moe_expert_ffn_fp8: gate/up + down launches"))
+                        if args.fp8 else "grouped_gemm (tcgen05), moe_expert_ffn: gate/up + down launches"),
             "peak_source": ("derived float32 CUDA-core peak (148 SMs x 128 lanes x 2 FLOP x 2032 MHz)"
                             if ffn["bound"] == "alu" else f"{peak_src} " + ("hbm_gbs" if ffn["bound"] == "hbm" else
                             ("bf16_tflops_sustained (power cap seen in the timed region)" if sustained
