@@ -203,3 +203,44 @@ def test_fp8_rejects_unaligned_widths():
     with pytest.raises(moe.MoeError) as e:
         moe.moe_expert_ffn_fp8(cfg, t, t, t, t, t, t, t, t, t, ws)
     assert e.value.code == moe.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("T,N,C,shared_F", [(64, 8, 16, 0), (200, 8, 40, 256)])
+def test_fp8_expert_choice_layer(T, N, C, shared_F):
+    """Expert choice with FP8 weights: every group holds exactly C rows (C <= 64: the
+    one-launch decode FFN).  Reference: the oracle's routing and expert choice on its
+    own scores, its FFN on its own dequantised weights, the gate the score."""
+    from test_gpu_expert_choice import check_selection
+    wl = synth.Workload("ec8", T + N, T=T, d=256, N=N, k=1, F=384, act="swiglu", gate="softmax", dtype="bf16",
+                        shared_F=shared_F)
+    inp = synth.make_inputs(wl)
+    cfg = moe.make_config(T, wl.d, N, 1, wl.F, shared_F, capacity=C, routing=moe.ROUTING_EXPERT_CHOICE)
+    layer = moe.MoELayer(cfg, to_dev(inp.Wg, "f32"), to_dev(inp.w1, "bf16"), to_dev(inp.w3, "bf16"),
+                         to_dev(inp.w2, "bf16"), to_dev(inp.sw1, "bf16"), to_dev(inp.sw3, "bf16"),
+                         to_dev(inp.sw2, "bf16"))
+    layer.quantize_fp8()
+    out = layer.forward(to_dev(inp.x, "bf16"))
+    torch.cuda.synchronize()
+    assert layer.device_status() == 0
+    v = layer.views()
+    x64 = oracle.widen(inp.x, "bf16")
+    ec = oracle.expert_choice(oracle.router_logits(x64, inp.Wg, inp.logit_bias), C)
+    chosen = v["src_token"].cpu().numpy().reshape(N, C)
+    check_selection(ec.scores, chosen, C)
+    q = [oracle.quantize_fp8_rows(oracle.widen(w, "bf16")) for w in (inp.w1, inp.w3, inp.w2)]
+    ref = np.zeros((T, wl.d))
+    if shared_F:
+        ref += oracle.expert_ffn(x64, oracle.widen(inp.sw1, "bf16"), oracle.widen(inp.sw3, "bf16"),
+                                 oracle.widen(inp.sw2, "bf16"), "swiglu")
+    deq = lambda i, e: oracle.dequantize_fp8_rows(q[i][0][e], q[i][1][e])  # noqa: E731
+    for e in range(N):
+        toks = ec.chosen[e]
+        ref[toks] += ec.scores[toks, e][:, None] * oracle.expert_ffn(x64[toks], deq(0, e), deq(1, e), deq(2, e),
+                                                                     "swiglu")
+    mine = v["dest_row"].cpu().numpy() >= 0
+    theirs = np.zeros((T, N), bool)
+    for e in range(N):
+        theirs[ec.chosen[e], e] = True
+    agree = np.all(mine == theirs, axis=1)
+    assert np.sum(~agree) <= max(2, T // 100)
+    assert_close_out(to_np_f64(out)[agree], ref[agree], "bf16")
