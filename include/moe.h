@@ -300,9 +300,11 @@ MOE_API int moe_quantize_fp8(const void *w, int64_t rows, int32_t cols, uint8_t 
  * bf16 configs with d and ffn multiples of 16 (else MOE_ERR_UNSUPPORTED); token or
  * expert choice; the shared expert (sw1, sw3, sw2) stays bf16.  The two NaN codes
  * (0x7F, 0xFF) are not valid weights (moe_quantize_fp8 never writes them).  When
- * no group can exceed 64 rows (T, or the capacity, at most 64: decode) the weights
- * stream once per group with the tokens as the narrow side of the product; any
- * offsets still give the right result. */
+ * no group can exceed 64 rows (T, or the capacity, at most 64: decode) the whole
+ * expert FFN is one cooperative launch of one CTA per SM in which the weights
+ * stream once per group with the tokens as the narrow side of the product (any
+ * offsets still give the right result); if the device cannot run a cooperative
+ * launch the call returns MOE_ERR_CUDA. */
 MOE_API int moe_expert_ffn_fp8(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const uint8_t *w1q,
                                const float *w1s, const uint8_t *w3q, const float *w3s, const uint8_t *w2q,
                                const float *w2s, void *y_perm, void *ws, void *stream);
