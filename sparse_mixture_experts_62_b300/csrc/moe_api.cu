@@ -425,8 +425,7 @@ int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x, 
   MOE_TRY(launch_dispatch(topk_idx, cfg->T, cfg->k, cfg->N, cfg->capacity, w.hist(), w.chunk_base(cfg), counts_routed,
                           counts_kept, offsets, dest_row, src_token, w.status(), s));
   if (cfg->T == 0) return MOE_OK;
-  return launch_gather_rows(x, src_token, offsets + cfg->N, (int64_t)cfg->T * cfg->k, (int)(cfg->d * esize(cfg)),
-                            x_perm, s);
+  return launch_scatter_rows(x, dest_row, cfg->T, cfg->k, (int)(cfg->d * esize(cfg)), x_perm, s);
 }
 
 int moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *offsets, const void *w1, const void *w3,
@@ -501,8 +500,11 @@ int layer_forward_impl(const moe_config *cfg, const void *x, const float *Wg, co
                             w.at<int32_t>(L.counts_routed), w.at<int32_t>(L.counts_kept), offsets, dest_row,
                             src_token, w.status(), s));
   }
-  MOE_TRY(launch_gather_rows(x, src_token, offsets + cfg->N, routed_rows(cfg), (int)(cfg->d * esize(cfg)), x_perm,
-                             s));
+  if (is_ec(cfg))
+    MOE_TRY(launch_gather_rows(x, src_token, offsets + cfg->N, routed_rows(cfg), (int)(cfg->d * esize(cfg)), x_perm,
+                               s));
+  else
+    MOE_TRY(launch_scatter_rows(x, dest_row, cfg->T, cfg->k, (int)(cfg->d * esize(cfg)), x_perm, s));
   if (f8)
     MOE_TRY(ffn_routed_fp8(cfg, w, x_perm, offsets, *f8, w.at<void>(L.h), y_perm, s));
   else

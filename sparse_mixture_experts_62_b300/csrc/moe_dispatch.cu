@@ -123,19 +123,60 @@ __global__ void __launch_bounds__(CH) dispatch_rank_kernel(const int32_t *__rest
   }
 }
 
-// x_perm[row] = x[src_token[row]] for row < offsets[N]; one warp per row.
+// x_perm[row] = x[src_token[row]] for row < offsets[N]; one warp per row.  Each
+// lane issues four 16-byte loads before their stores, so that enough bytes are in
+// flight per SM to cover the memory latency.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t *__restrict__ x,
                                                           const int32_t *__restrict__ src_token,
                                                           const int32_t *__restrict__ offsets_end, int row_bytes,
                                                           uint8_t *__restrict__ x_perm) {
   const int rows = *offsets_end;
   const int nvec = row_bytes / 16;
+  const int lane = threadIdx.x & 31;
   const int warps_total = gridDim.x * (blockDim.x >> 5);
   for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < rows; row += warps_total) {
     const int t = src_token[row];
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * row_bytes);
     uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)row * row_bytes);
-    for (int v = threadIdx.x & 31; v < nvec; v += 32) dst[v] = src[v];
+    for (int v0 = lane; v0 < nvec; v0 += 128) {
+      uint4 buf[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + 32 * u < nvec) buf[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + 32 * u < nvec) dst[v0 + 32 * u] = buf[u];
+    }
+  }
+}
+
+// Token choice: x_perm[dest_row[t, j]] = x[t] for every kept slot j; one warp per
+// token, which reads its row of x once and writes it to each of its rows of x_perm
+// (a row gather would read x once per slot, from far-apart places once x no longer
+// fits in L2 beside the x_perm being written).
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const uint8_t *__restrict__ x,
+                                                           const int32_t *__restrict__ dest_row, int T, int k,
+                                                           int row_bytes, uint8_t *__restrict__ x_perm) {
+  const int nvec = row_bytes / 16;
+  const int lane = threadIdx.x & 31;
+  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps_total) {
+    const int my_row = lane < k ? dest_row[(size_t)t * k + lane] : -1;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * row_bytes);
+    for (int v0 = lane; v0 < nvec; v0 += 128) {
+      uint4 buf[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (v0 + 32 * u < nvec) buf[u] = __ldg(src + v0 + 32 * u);
+      for (int j = 0; j < k; ++j) {
+        const int row = __shfl_sync(0xffffffffu, my_row, j);
+        if (row < 0) continue;
+        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)row * row_bytes);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (v0 + 32 * u < nvec) dst[v0 + 32 * u] = buf[u];
+      }
+    }
   }
 }
 
@@ -163,6 +204,20 @@ int launch_gather_rows(const void *x, const int32_t *src_token, const int32_t *o
   if (blocks > cap) blocks = cap;
   gather_rows_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(x), src_token, offsets_end, row_bytes,
                                                   static_cast<uint8_t *>(x_perm));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_scatter_rows(const void *x, const int32_t *dest_row, int T, int k, int row_bytes, void *x_perm,
+                        cudaStream_t s) {
+  if (T <= 0) return MOE_OK;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int sms = device_sm_count(dev);
+  int64_t blocks = ((int64_t)T + 7) / 8;
+  const int64_t cap = (int64_t)(sms > 0 ? sms : 148) * 8;
+  if (blocks > cap) blocks = cap;
+  scatter_rows_kernel<<<(int)blocks, 256, 0, s>>>(static_cast<const uint8_t *>(x), dest_row, T, k, row_bytes,
+                                                   static_cast<uint8_t *>(x_perm));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -27,6 +27,9 @@ constexpr int kDispatchChunk = 128;  // tokens per histogram / rank chunk
 int launch_dispatch(const int32_t *idx, int T, int k, int N, int capacity, int32_t *hist, int32_t *chunk_base,
                     int32_t *counts_routed, int32_t *counts_kept, int32_t *offsets, int32_t *dest_row,
                     int32_t *src_token, int *status, cudaStream_t s);
+// Token choice: x_perm[dest_row[t, j]] = x[t] for the kept slots (k <= 32), x read once per token.
+int launch_scatter_rows(const void *x, const int32_t *dest_row, int T, int k, int row_bytes, void *x_perm,
+                        cudaStream_t s);
 int launch_gather_rows(const void *x, const int32_t *src_token, const int32_t *offsets_end, int64_t max_rows,
                        int row_bytes, void *x_perm, cudaStream_t s);
 

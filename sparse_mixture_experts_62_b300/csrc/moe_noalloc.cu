@@ -82,5 +82,5 @@ extern "C" MOE_API int moe_dispatch_noalloc(const moe_config *cfg, const int32_t
                        offsets, dest_row, src_token, reinterpret_cast<int *>(status), s);
   if (rc || cfg->T == 0) return rc;
   const int es = cfg->dtype == MOE_BF16 ? 2 : 4;
-  return launch_gather_rows(x, src_token, offsets + cfg->N, (int64_t)cfg->T * cfg->k, cfg->d * es, x_perm, s);
+  return launch_scatter_rows(x, dest_row, cfg->T, cfg->k, cfg->d * es, x_perm, s);
 }
