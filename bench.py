@@ -62,11 +62,9 @@ def layer_bytes(wl, touched_experts: int, fp8: bool = False) -> float:
     return float(w + sw + 2 * wl.T * wl.d * es + wl.d * wl.N * 4)
 
 
-# dram__bytes_read.sum + dram__bytes_write.sum of the two grouped-GEMM launches of
-# one step, from one ncu capture of the kernel revision named here (None once the
-# kernel changes until it is captured again).
-# DRAM bytes (read + write) of the expert-FFN launches per step, from ncu captures of
-# the kernels as they stand (profiles/); keyed by (workload, FP8 weights).
+# DRAM bytes (read + write) of the expert-FFN launches of one step, from ncu captures
+# of the kernel revision named here (profiles/); keyed by (workload, FP8 weights).
+# A workload whose kernel has changed since its capture reports None.
 NCU_TRAFFIC = {("mixtral_prefill", False): {"bytes": 3.689e9, "kernel_rev": "pair2"},
                ("mixtral_decode", True): {"bytes": 1.4267e9, "kernel_rev": "fp8ffn1"}}
 KERNEL_REV = {False: "pair2", True: "fp8ffn1"}

@@ -1,0 +1,84 @@
+"""The bench's algorithmic FLOP and byte counts and its roofline arithmetic (CPU).
+
+The counts are pinned against figures worked out independently from the model
+shapes: the active FLOPs and algorithmic bytes of the Mixtral-shaped prefill and
+decode layers, the DeepSeek-V3-shaped layer with its shared expert, and one
+expert's bytes in bf16 and in FP8 with row scales.
+"""
+import pytest
+
+import bench
+import synth
+
+W = synth.WORKLOADS
+
+
+def test_prefill_counts():
+    wl = W["mixtral_prefill"]
+    kept = wl.T * wl.k                                   # no capacity: every assignment kept
+    fl = bench.layer_flops(wl, kept)
+    # 8192 rows x (2 x 4096 x 14336 x 3) = 2.886 TFLOP; router 2 x 4096 x 4096 x 8
+    assert fl["expert_ffn"] == pytest.approx(2.886e12, rel=1e-3)
+    assert fl["router"] == 2 * 4096 * 4096 * 8
+    # weights of all 8 experts (2.819 GB) + x and out (2 x 33.5 MB) + W_g
+    assert bench.layer_bytes(wl, 8) == pytest.approx(2.886e9, rel=1e-3)
+    assert bench.expert_weight_bytes(wl, False) == 3 * 4096 * 14336 * 2
+
+
+def test_decode_counts():
+    wl = W["mixtral_decode"]
+    assert bench.expert_weight_bytes(wl, False) == pytest.approx(352.3e6, rel=1e-3)
+    # FP8: one byte per weight plus a float32 scale per row of W1, W3 (F rows) and W2 (d rows)
+    assert bench.expert_weight_bytes(wl, True) == 3 * 4096 * 14336 + (2 * 14336 + 4096) * 4
+    assert bench.layer_flops(wl, 32)["expert_ffn"] == pytest.approx(11.27e9, rel=1e-3)
+
+
+def test_dsv3_counts():
+    wl = W["dsv3_finegrained"]
+    fl = bench.layer_flops(wl, wl.T * wl.k)
+    # routed 65536 rows x 2 x 7168 x 2048 x 3 + shared 8192 rows of the same = 6.494 TFLOP
+    assert fl["expert_ffn"] + fl["shared_ffn"] == pytest.approx(6.494e12, rel=1e-3)
+    # 256 experts (22.55 GB) + the shared expert + x and out + W_g = 22.88 GB
+    assert bench.layer_bytes(wl, 256) == pytest.approx(22.88e9, rel=1e-3)
+
+
+def test_stage_work_matches_layer_counts():
+    wl = W["mixtral_prefill"]
+    kept = wl.T * wl.k
+    work = bench.stage_work(wl, kept, 8)
+    assert work["expert_ffn"][0] == bench.layer_flops(wl, kept)["expert_ffn"]
+    assert work["route"][0] == bench.layer_flops(wl, kept)["router"]
+    # expert FFN bytes: touched weights + x_perm read + y_perm written
+    assert work["expert_ffn"][1] == 8 * bench.expert_weight_bytes(wl, False) + 2 * kept * wl.d * 2
+    # combine: y_perm read, out written, ids + weights
+    assert work["combine"][1] == kept * wl.d * 2 + wl.T * wl.d * 2 + wl.T * wl.k * 8
+
+
+def test_stage_roofline_picks_the_longer_bound():
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1500.0}
+    # 3 TFLOP and 3 GB: 1.5 ms at the burst tensor peak, 0.5 ms at HBM -> tensor
+    r = bench.stage_roofline(3e12, 3e9, 2.0, peaks, sustained=False)
+    assert r["bound"] == "tensor" and r["peak"] == 2000.0
+    assert r["achieved"] == pytest.approx(1500.0) and r["frac"] == pytest.approx(0.75)
+    # the sustained peak when the power cap was seen
+    r = bench.stage_roofline(3e12, 3e9, 2.0, peaks, sustained=True)
+    assert r["peak"] == 1500.0 and r["frac"] == pytest.approx(1.0)
+    # 10 GFLOP and 3 GB: HBM governs
+    r = bench.stage_roofline(1e10, 3e9, 1.0, peaks, sustained=False)
+    assert r["bound"] == "hbm" and r["achieved"] == pytest.approx(3000.0) and r["frac"] == pytest.approx(0.5)
+    # float32 work against the CUDA-core peak
+    r = bench.stage_roofline(1e9, 1e6, 1.0, peaks, sustained=False, alu=True)
+    assert r["bound"] == "alu" and r["peak"] == pytest.approx(bench.F32_ALU_TFLOPS)
+
+
+def test_l2_flush_only_when_the_weights_fit():
+    assert bench.needs_l2_flush(W["shazeer_tiny_f32"])
+    for name in ("mixtral_prefill", "mixtral_decode", "dsv3_finegrained", "qwen3_skew_drop"):
+        assert not bench.needs_l2_flush(W[name]) and not bench.needs_l2_flush(W[name], True)
+
+
+def test_traffic_only_for_the_captured_kernel_revision(monkeypatch):
+    assert bench._traffic("mixtral_prefill") == bench.NCU_TRAFFIC[("mixtral_prefill", False)]["bytes"]
+    assert bench._traffic("dsv3_finegrained") is None
+    monkeypatch.setitem(bench.KERNEL_REV, False, "changed")
+    assert bench._traffic("mixtral_prefill") is None
