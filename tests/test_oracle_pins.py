@@ -677,3 +677,74 @@ def test_fp8_row_quantisation():
     ref = oracle.layer_forward(inp)
     f8 = oracle.layer_forward_fp8(inp, qs[0][0], qs[0][1], qs[1][0], qs[1][1], qs[2][0], qs[2][1])
     assert np.allclose(f8.out, ref.out, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- router helpers, pinned directly
+def test_router_logits_orientation_bias_and_single_rounding():
+    """z[t, e] = sum_j x[t, j] W[j, e] + beta_e, summed exactly (in double) and rounded
+    once: a one-hot x picks a row of W; 1e8 + 1 - 1e8 keeps its 1 (a float32 running
+    sum would lose it)."""
+    W = np.array([[1.0, 2.0, 3.0], [4.0, 5.0, 6.0]], dtype=np.float32)   # [d=2, N=3]
+    x = np.array([[0.0, 1.0], [1.0, 0.0]])
+    assert np.array_equal(oracle.router_logits(x, W, None), np.array([[4, 5, 6], [1, 2, 3]], np.float32))
+    beta = np.array([0.5, -1.0, 0.25], dtype=np.float32)
+    assert np.array_equal(oracle.router_logits(x, W, beta), np.array([[4.5, 4, 6.25], [1.5, 1, 3.25]], np.float32))
+    W2 = np.array([[1e8], [1.0], [-1e8]], dtype=np.float32)
+    z = oracle.router_logits(np.ones((1, 3)), W2, None)
+    assert z.dtype == np.float32 and z[0, 0] == 1.0
+
+
+def test_sigmoid_affinity_closed_forms():
+    z = np.array([0.0, np.log(3.0), -np.log(3.0), 40.0, -40.0], dtype=np.float32)
+    s = oracle.sigmoid_affinity(z)
+    assert s.dtype == np.float32
+    assert s[0] == 0.5 and s[1] == np.float32(0.75) and s[2] == np.float32(0.25)
+    assert s[3] == 1.0 and 0 < s[4] < 1e-17
+    zz = np.linspace(-8, 8, 101, dtype=np.float32)
+    assert np.all(np.abs(oracle.sigmoid_affinity(zz).astype(np.float64) +
+                         oracle.sigmoid_affinity(-zz).astype(np.float64) - 1.0) <= 2.0 ** -24)
+
+
+def test_selection_scores_by_gate():
+    z = np.array([[0.0, np.log(3.0)]], dtype=np.float32)
+    for gate in ("softmax", "softmax_full"):
+        sel, s = oracle.selection_scores(z, gate, None)
+        assert sel is z and s is None
+    sel, s = oracle.selection_scores(z, "sigmoid", None)
+    assert np.array_equal(sel, s) and s[0, 1] == np.float32(0.75)
+    b = np.array([0.375, 0.125], dtype=np.float32)
+    sel, s = oracle.selection_scores(z, "sigmoid", b)
+    assert np.array_equal(sel, np.array([[0.875, 0.875]], np.float32))     # 0.5 + 0.375, 0.75 + 0.125
+    assert np.array_equal(s, np.array([[0.5, 0.75]], np.float32))           # the bias does not enter s
+
+
+def test_router_probabilities_closed_forms():
+    z = np.array([[0.0, np.log(3.0)], [5.0, 5.0 + np.log(3.0)]], dtype=np.float32)
+    p = oracle.router_probabilities(z, "softmax")
+    assert np.allclose(p, [[0.25, 0.75], [0.25, 0.75]], rtol=0, atol=1e-7)  # shift invariance
+    assert np.array_equal(oracle.router_probabilities(z, "softmax_full"), p)
+    rng = np.random.default_rng(9)
+    zr = rng.standard_normal((7, 5)).astype(np.float32)
+    pr = oracle.router_probabilities(zr, "softmax")
+    assert np.allclose(pr.sum(axis=1), 1.0, atol=1e-14)
+    assert np.allclose(pr, np.exp(zr.astype(np.float64)) / np.exp(zr.astype(np.float64)).sum(1, keepdims=True),
+                       rtol=1e-13)
+    ps = oracle.router_probabilities(np.array([[0.0, np.log(3.0)]], np.float32), "sigmoid")
+    assert np.allclose(ps, [[0.5 / 1.25, 0.75 / 1.25]], rtol=1e-7)         # s_i / sum s, no bias
+
+
+def test_expert_choice_select_worked_example():
+    """Each expert takes its C highest-scoring tokens, ties to the lower token index,
+    rows in token order; C is clamped to T."""
+    sc = np.array([[0.9, 0.1],
+                   [0.5, 0.5],
+                   [0.5, 0.7],
+                   [0.2, 0.7]])
+    ec = oracle.expert_choice_select(sc, 2)
+    assert ec.chosen.tolist() == [[0, 1], [2, 3]]       # expert 0: 0.9 then the tie 0.5 -> token 1
+    assert ec.offsets.tolist() == [0, 2, 4]
+    dest = np.full((4, 2), -1)
+    dest[0, 0], dest[1, 0], dest[2, 1], dest[3, 1] = 0, 1, 2, 3
+    assert np.array_equal(ec.dest_row, dest)
+    ec5 = oracle.expert_choice_select(sc, 5)             # C > T: every token, once per expert
+    assert ec5.chosen.tolist() == [[0, 1, 2, 3], [0, 1, 2, 3]] and ec5.offsets.tolist() == [0, 4, 8]
