@@ -82,3 +82,27 @@ def test_traffic_only_for_the_captured_kernel_revision(monkeypatch):
     assert bench._traffic("dsv3_finegrained") is None
     monkeypatch.setitem(bench.KERNEL_REV, False, "changed")
     assert bench._traffic("mixtral_prefill") is None
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` times the oracle on host cores and prints one JSON
+    line with the same metric and config as the GPU arm, a cpu_baseline describing
+    the run, and an e2e of its own value with no host-device bytes."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload",
+                        "shazeer_tiny_f32", "--steps", "2", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["steps"] == 2 and d["warmup"] == 3
+    assert d["config"]["workload"] == "shazeer_tiny_f32" and d["vs_baseline"] is None
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
