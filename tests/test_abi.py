@@ -106,6 +106,31 @@ def test_null_and_misaligned_pointers_rejected_without_launch():
         assert e.value.code == moe.MOE_ERR_INVALID_ARG
 
 
+def test_fp8_entry_points_reject_bad_arguments_without_launch():
+    A = 1 << 20
+    cfg = moe.make_config(64, 64, 8, 2, 128)
+    invalid = [
+        lambda: moe._check(moe._lib.moe_quantize_fp8(None, 4, 16, A, A, None), "q"),       # no weights
+        lambda: moe._check(moe._lib.moe_quantize_fp8(A, -1, 16, A, A, None), "q"),         # negative rows
+        lambda: moe._check(moe._lib.moe_quantize_fp8(A, 4, 0, A, A, None), "q"),           # no columns
+        lambda: moe.moe_expert_ffn_fp8(cfg, A, A, A, A, None, None, A, A, A, A, 0),          # SwiGLU needs W3
+        lambda: moe.moe_expert_ffn_fp8(cfg, A, A, A + 8, A, A, A, A, A, A, A, 0),            # codes misaligned
+        lambda: moe.moe_expert_ffn_fp8(cfg, A, A, A, None, A, A, A, A, A, A, 0),             # no scales
+        lambda: moe.moe_expert_ffn_fp8(cfg, None, A, A, A, A, A, A, A, A, A, 0),             # no x_perm
+        lambda: moe.moe_layer_forward_fp8(cfg, A, A, None, None, None, A, A, A, A, A, None, None, None, A, A, 0),
+    ]
+    for fn in invalid:
+        with pytest.raises(moe.MoeError) as e:
+            fn()
+        assert e.value.code == moe.MOE_ERR_INVALID_ARG
+    # float32 configurations and widths whose code rows are not 16-byte multiples
+    for bad in (moe.make_config(64, 64, 8, 2, 128, dtype=moe.DTYPE_F32), moe.make_config(64, 72, 8, 2, 128),
+                moe.make_config(64, 64, 8, 2, 136)):
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_expert_ffn_fp8(bad, A, A, A, A, A, A, A, A, A, A, 0)
+        assert e.value.code == moe.MOE_ERR_UNSUPPORTED
+
+
 def test_expert_choice_config_sizes_the_workspace_for_N_times_C_rows():
     tc = moe.make_config(1000, 64, 16, 2, 128)
     ec = moe.make_config(1000, 64, 16, 1, 128, capacity=300, routing=moe.ROUTING_EXPERT_CHOICE)
