@@ -44,6 +44,16 @@ MUTATIONS = [
     ("E4M3 ties rounded up", "r = np.minimum(np.rint(a / quantum) * quantum, 448.0)",
      "r = np.minimum(np.floor(a / quantum + 0.5) * quantum, 448.0)"),
     ("FP8 scale from the wrong maximum", "(amax / np.float32(E4M3_MAX))", "(amax / np.float32(240.0))"),
+    # the backward pass (pinned by central differences)
+    ("SiLU derivative without a (1 - sig)", "da = dh * u * (sig * (1.0 + a * (1.0 - sig)))   # d SiLU(a) / da",
+     "da = dh * u * sig   # d SiLU(a) / da"),
+    ("up-projection gradient without a", "du = dh * a * sig\n        dW2 = dy.T @ h",
+     "du = dh * sig\n        dW2 = dy.T @ h"),
+    ("dW1 from the up-projection gradient", "dW1 = da.T @ xr", "dW1 = du.T @ xr"),
+    ("ReLU backward passes negatives", "    da = dh * (a > 0)\n    return da @ W1, da.T @ xr, None, dy.T @ h",
+     "    da = dh\n    return da @ W1, da.T @ xr, None, dy.T @ h"),
+    ("softmax gate Jacobian uncentred", "dz[idx_t] = w_t * (g - np.sum(w_t * g))", "dz[idx_t] = w_t * g"),
+    ("sigmoid derivative without (1 - s)", "dz[idx_t] = ds * s * (1.0 - s)", "dz[idx_t] = ds * s"),
 ]
 
 
