@@ -62,12 +62,46 @@ def layer_bytes(wl, touched_experts: int, fp8: bool = False) -> float:
     return float(w + sw + 2 * wl.T * wl.d * es + wl.d * wl.N * 4)
 
 
-# DRAM bytes (read + write) of the expert-FFN launches of one step, from ncu captures
-# of the kernel revision named here (profiles/); keyed by (workload, FP8 weights).
-# A workload whose kernel has changed since its capture reports None.
-NCU_TRAFFIC = {("mixtral_prefill", False): {"bytes": 3.689e9, "kernel_rev": "pair2"},
-               ("mixtral_decode", True): {"bytes": 1.4267e9, "kernel_rev": "fp8ffn1"}}
-KERNEL_REV = {False: "pair2", True: "fp8ffn1"}
+# DRAM bytes (read + write) per step of the expert-FFN launches come from an ncu
+# capture, listed in profiles/traffic.md with a hash of the kernel sources the
+# capture ran; a workload whose sources have changed since reports None.
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "traffic.md")
+KERNEL_SOURCES = {False: ("moe_ffn_tc.cu", "moe_common.cuh", "moe_api.cu"),
+                  True: ("moe_ffn_fp8_tc.cu", "moe_common.cuh", "moe_api.cu")}
+
+
+def kernel_source_hash(fp8: bool) -> str:
+    """First 16 hex digits of the SHA-256 of the expert-FFN kernel sources (and the
+    launcher that picks their tile forms), concatenated in a fixed order."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[fp8]:
+        with open(os.path.join(ROOT, "sparse_mixture_experts_62_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_table(path: str = TRAFFIC_TABLE) -> dict:
+    """{(workload, fp8): (bytes per step, source hash)} from the table rows
+    `| workload | bf16 or fp8 | source hash | bytes | ... |`."""
+    out = {}
+    if not os.path.exists(path):
+        return out
+    with open(path) as f:
+        for ln in f:
+            cells = [c.strip() for c in ln.strip().strip("|").split("|")]
+            if len(cells) < 4 or cells[1] not in ("bf16", "fp8"):
+                continue
+            try:
+                out[(cells[0], cells[1] == "fp8")] = (float(cells[3]), cells[2])
+            except ValueError:
+                continue
+    return out
+
+
+def _traffic(name, fp8: bool = False, table=None):
+    t = (traffic_table() if table is None else table).get((name, fp8))
+    return t[0] if t and t[1] == kernel_source_hash(fp8) else None
 
 
 def stage_work(wl, kept_rows: int, touched: int, fp8: bool = False) -> dict:
@@ -99,17 +133,26 @@ def stage_work(wl, kept_rows: int, touched: int, fp8: bool = False) -> dict:
 F32_ALU_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12
 
 
-def stage_roofline(flops, nbytes, ms, peaks, sustained, alu=False):
-    """The bound whose time is longer at peak; achieved rate and fraction of that peak."""
-    tf_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
-    if alu:
-        tf_peak = F32_ALU_TFLOPS
+def stage_roofline(flops, nbytes, ms, peaks, clocks=None, alu=False):
+    """The bound whose time is longer at peak; achieved rate and fraction of that peak.
+
+    Tensor-bound work is measured against the burst bf16 peak (`frac`), with two
+    extra readings: against the sustained (power-capped) peak (`frac_sustained`),
+    and against the burst peak scaled by the median SM clock sampled in the timed
+    region over the maximum clock (`frac_clock_norm`)."""
+    tf_peak = F32_ALU_TFLOPS if alu else peaks["bf16_tflops"]
     t_tensor = flops / (tf_peak * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     s = ms / 1e3
     if flops > 0 and t_tensor >= t_hbm:
-        return {"ms": ms, "bound": "alu" if alu else "tensor", "achieved": flops / s / 1e12, "peak": tf_peak,
-                "unit": "TFLOP/s", "frac": t_tensor / s}
+        ach = flops / s / 1e12
+        r = {"ms": ms, "bound": "alu" if alu else "tensor", "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
+             "frac": ach / tf_peak}
+        if not alu:
+            r["frac_sustained"] = ach / peaks["bf16_tflops_sustained"]
+            if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+                r["frac_clock_norm"] = ach / (tf_peak * clocks["sm_mhz"] / clocks["sm_max_mhz"])
+        return r
     return {"ms": ms, "bound": "hbm", "achieved": nbytes / s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": t_hbm / s}
 
@@ -134,10 +177,6 @@ def blas_threads() -> int:
                 return int(os.environ[var])
         return os.cpu_count() or 1
 
-
-def _traffic(name, fp8: bool = False):
-    t = NCU_TRAFFIC.get((name, fp8))
-    return t["bytes"] if t and t["kernel_rev"] == KERNEL_REV[fp8] else None
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -219,72 +258,68 @@ def max_over_ranks(dist, v: float) -> float:
 
 
 # ----------------------------------------------------------------------------- reference arm
-def run_reference(args, wl):
-    """The CPU oracle, as it stands, on a bounded sample of the same workload per step.
+def oracle_step(wl, inp, sample: int, rng):
+    """One bounded step of the oracle, as it stands, on the workload.
 
-    Without a capacity limit every token is routed and processed on its own, so a
-    step is the oracle's layer on `--ref-sample` seeded tokens taken as a layer of
-    their own (routing, gate, their experts, combine, statistics); with a capacity
-    limit the routing and dispatch of all tokens come first, then the experts on
-    the sampled tokens, extrapolated to all tokens."""
+    Without a capacity limit the tokens do not interact, so the step is the
+    whole layer (routing, gate, dispatch, the experts -- whose weights the oracle
+    widens to float64 on every call -- combine, statistics) on `sample` seeded
+    tokens taken as a batch of their own: tokens/s = sample / seconds.  With a
+    capacity limit the drop set couples all tokens: the step routes, dispatches
+    and takes the statistics of all T tokens, then runs the experts on `sample`
+    seeded tokens; tokens/s extrapolates the expert time linearly to T.
+    Returns (seconds spent, tokens/s, description)."""
     import dataclasses
     import oracle
-    inp = synth.make_inputs(wl)
-    sample = min(args.ref_sample, wl.T)
-    rng = np.random.default_rng(wl.seed)
-
-    def step():
-        toks = np.sort(rng.choice(wl.T, size=sample, replace=False))
-        if wl.capacity_factor <= 0:
-            sub = dataclasses.replace(inp, wl=wl.scaled(T=sample), x=inp.x[toks])
-            t0 = time.perf_counter()
-            oracle.layer_forward(sub)
-            return (time.perf_counter() - t0) * wl.T / sample                # seconds per full layer
-        t0 = time.perf_counter()
-        oracle.layer_forward(inp, tokens=np.array([], dtype=np.int64))      # routing + dispatch + stats, all T
-        t1 = time.perf_counter()
-        oracle.layer_forward(inp, tokens=toks)                                # + experts on the sample
-        t2 = time.perf_counter()
-        ffn_per_token = max(0.0, (t2 - t1) - (t1 - t0)) / len(toks)
-        return (t1 - t0) + ffn_per_token * wl.T                               # extrapolated full-layer seconds
-
-    for _ in range(args.warmup):
-        step()
-    secs = [step() for _ in range(args.steps)]
-    per_step = float(np.mean(secs))
-    cores = blas_threads()
-    value = wl.T / per_step
+    sample = min(sample, wl.T)
+    toks = np.sort(rng.choice(wl.T, size=sample, replace=False))
     if wl.capacity_factor <= 0:
-        desc = (f"oracle (numpy float64): each step the whole layer on {sample} seeded token(s) taken as a layer "
-                f"of their own (tokens are independent without a capacity limit), including the float64 widening "
-                f"of each touched expert's weights, scaled to {wl.T} tokens")
-    else:
-        desc = (f"oracle (numpy float64): routing, dispatch and statistics on all {wl.T} tokens, expert FFN on "
-                f"{sample} sampled tokens per step, extrapolated linearly to {wl.T} tokens")
+        sub = dataclasses.replace(inp, wl=wl.scaled(T=sample), x=inp.x[toks])
+        t0 = time.perf_counter()
+        oracle.layer_forward(sub)
+        dt = time.perf_counter() - t0
+        return dt, sample / dt, (f"numpy float64 oracle: the whole layer on {sample} seeded tokens of the "
+                                 f"{wl.T}-token batch per step, as a batch of their own (tokens are independent "
+                                 f"without a capacity limit), float64 widening of the touched experts' weights "
+                                 f"included")
+    t0 = time.perf_counter()
+    oracle.layer_forward(inp, tokens=np.array([], dtype=np.int64))      # routing + dispatch + stats, all T
+    t1 = time.perf_counter()
+    oracle.layer_forward(inp, tokens=toks)                                # + experts on the sample
+    t2 = time.perf_counter()
+    per_token = max(0.0, (t2 - t1) - (t1 - t0)) / len(toks)
+    est = (t1 - t0) + per_token * wl.T
+    return t2 - t0, wl.T / est, (f"numpy float64 oracle: routing, dispatch and statistics on all {wl.T} tokens, "
+                                 f"expert FFN on {sample} seeded tokens per step, extrapolated linearly to "
+                                 f"{wl.T} tokens (capacity couples the tokens)")
+
+
+def run_reference(args, wl):
+    """The reference arm: the CPU oracle timed per step on a bounded sample of the
+    same workload (oracle_step), on the host's cores."""
+    inp = synth.make_inputs(wl)
+    rng = np.random.default_rng(wl.seed)
+    for _ in range(args.warmup):
+        oracle_step(wl, inp, args.ref_sample, rng)
+    runs = [oracle_step(wl, inp, args.ref_sample, rng) for _ in range(args.steps)]
+    secs = float(np.mean([r[0] for r in runs]))
+    value = float(np.mean([r[1] for r in runs]))
+    cores = blas_threads()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_of(wl),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": runs[0][2]},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(wl, inp, budget_tokens: int):
-    import oracle
-    toks = np.sort(np.random.default_rng(wl.seed + 1).choice(wl.T, size=min(budget_tokens, wl.T), replace=False))
-    t0 = time.perf_counter()
-    oracle.layer_forward(inp, tokens=np.array([], dtype=np.int64))
-    t1 = time.perf_counter()
-    oracle.layer_forward(inp, tokens=toks)
-    t2 = time.perf_counter()
-    per_token = max(0.0, (t2 - t1) - (t1 - t0)) / len(toks)
-    est = (t1 - t0) + per_token * wl.T
-    cores = blas_threads()
-    return {"value": wl.T / est, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": (f"numpy float64 oracle: routing, dispatch and statistics on all {wl.T} tokens, expert FFN "
-                       f"on {len(toks)} sampled tokens, extrapolated linearly to {wl.T} tokens "
-                       f"({t2 - t0:.1f} s of CPU work)")}
+def cpu_baseline(wl, inp, sample: int):
+    """The oracle on the host's cores: one step of oracle_step (the reference arm's step)."""
+    secs, value, desc = oracle_step(wl, inp, sample, np.random.default_rng(wl.seed + 1))
+    return {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{desc} ({secs:.1f} s of CPU work)"}
 
 
 L2_BYTES = 126 << 20
@@ -327,95 +362,100 @@ def build_layer(moe, inp):
                         _to_dev(inp.logit_bias, "f32"), _to_dev(inp.sel_bias, "f32"))
 
 
-def run_ours(args, wl, dist, rank, local):
-    import torch
-
-    import sparse_mixture_experts_62_b300 as moe
-
-    torch.cuda.set_device(local)
-    inp = synth.make_inputs(wl)
-    to_dev = _to_dev
-    layer = build_layer(moe, inp)
-    if args.fp8:  # weights quantised once, outside the timed region (like any weight packing)
-        if wl.dtype != "bf16":
-            raise SystemExit("--fp8 needs a bf16 workload")
-        layer.quantize_fp8()
-        torch.cuda.synchronize()
-    x = to_dev(inp.x, wl.dtype)
-    out = torch.empty((wl.T, wl.d), dtype=x.dtype, device="cuda")
+def layer_stages(moe, layer, x, out, stats, wl):
+    """The launches of moe_layer_forward, stage by stage, plus the statistics; each
+    stage a function of no arguments issuing on torch's current stream (the
+    capture stream while a graph records)."""
     cfg, ws, v = layer.cfg, layer.ws, layer.views()
-    stream = torch.cuda.current_stream()
-    stats = torch.zeros(2 * wl.N + 4, dtype=torch.float32, device="cuda")
     has_shared = wl.shared_F > 0
-    stages = ["route", "dispatch", "expert_ffn"] + (["shared_ffn"] if has_shared else []) + ["combine", "load_stats"]
+    cur = lambda: __import__("torch").cuda.current_stream().cuda_stream  # noqa: E731
 
-    def step(ev=None):
-        # the launches of moe_layer_forward, stage by stage, + the statistics, on
-        # the current stream (which is the capture stream while a graph records)
-        cur = torch.cuda.current_stream()
-        s = cur.cuda_stream
-        rec = (lambda i: ev[i].record(cur)) if ev is not None else (lambda i: None)
-        rec(0)
+    def route():
         moe.moe_route(cfg, x, layer.Wg, layer.logit_bias, layer.sel_bias, v["logits"], v["topk_idx"], v["topk_w"],
-                      ws, s)
-        rec(1)
+                      ws, cur())
+
+    def dispatch():
         moe.moe_dispatch(cfg, v["topk_idx"], x, v["counts_routed"], v["counts_kept"], v["offsets"], v["dest_row"],
-                         v["src_token"], v["x_perm"], ws, s)
-        rec(2)
+                         v["src_token"], v["x_perm"], ws, cur())
+
+    def expert_ffn():
         if layer.fp8 is not None:
-            moe.moe_expert_ffn_fp8(cfg, v["x_perm"], v["offsets"], *layer.fp8, v["y_perm"], ws, s)
+            moe.moe_expert_ffn_fp8(cfg, v["x_perm"], v["offsets"], *layer.fp8, v["y_perm"], ws, cur())
         else:
-            moe.moe_expert_ffn(cfg, v["x_perm"], v["offsets"], layer.w1, layer.w3, layer.w2, v["y_perm"], ws, s)
-        i = 3
-        if has_shared:
-            rec(i)
-            moe.moe_shared_ffn(cfg, x, layer.sw1, layer.sw3, layer.sw2, v["y_shared"], ws, s)
-            i += 1
-        rec(i)
-        moe.moe_combine(cfg, v["y_perm"], v["dest_row"], v["topk_w"], v["y_shared"] if has_shared else None, out, s)
-        rec(i + 1)
+            moe.moe_expert_ffn(cfg, v["x_perm"], v["offsets"], layer.w1, layer.w3, layer.w2, v["y_perm"], ws, cur())
+
+    def shared_ffn():
+        moe.moe_shared_ffn(cfg, x, layer.sw1, layer.sw3, layer.sw2, v["y_shared"], ws, cur())
+
+    def combine():
+        moe.moe_combine(cfg, v["y_perm"], v["dest_row"], v["topk_w"], v["y_shared"] if has_shared else None, out,
+                        cur())
+
+    def load_stats():
         moe.moe_load_stats(cfg, v["logits"], v["counts_routed"], v["counts_kept"], stats[:wl.N],
-                           stats[wl.N:2 * wl.N], stats[2 * wl.N:2 * wl.N + 3], ws, s)
-        rec(i + 2)
+                           stats[wl.N:2 * wl.N], stats[2 * wl.N:2 * wl.N + 3], ws, cur())
+
+    st = [("route", route), ("dispatch", dispatch), ("expert_ffn", expert_ffn)]
+    if has_shared:
+        st.append(("shared_ffn", shared_ffn))
+    st += [("combine", combine), ("load_stats", load_stats)]
+    return st
+
+
+def time_layer(args, moe, layer, x, wl, stream, dist=None, clk_gpu=None):
+    """Warm-up, then the timed region: the whole step captured once as a CUDA graph
+    and replayed `args.steps` times (eager launches with --eager), bracketed by a
+    barrier and synchronisation; then, still inside the clock sampling, a stage
+    pass: each stage captured as a graph of its own and replayed in order for
+    `args.steps` steps, with CUDA events between the stages on the same stream.
+    Returns step_ms (per step), total_ms, stage_ms (mean per stage), graph flag,
+    clock summary."""
+    import torch
+    out = torch.empty((wl.T, wl.d), dtype=x.dtype, device="cuda")
+    stats = torch.zeros(2 * wl.N + 4, dtype=torch.float32, device="cuda")
+    stages = layer_stages(moe, layer, x, out, stats, wl)
+
+    def step():
+        for _, fn in stages:
+            fn()
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if layer.device_status() != 0:
         raise RuntimeError("device status not clean after warm-up")
-    # per-stage durations: an eager pass with events between the stages
-    nev = len(stages) + 1
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
-    for k in range(args.steps):
-        step(evs[k])
-    torch.cuda.synchronize()
-    stage_ms = {n: float(np.mean([evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(args.steps)]))
-                for j, n in enumerate(stages)}
-    # the timed region: the step captured once as a CUDA graph and replayed (the
-    # same launches, without the host's per-call overhead); eager if capture fails
-    graph = None
+    graph, stage_graphs = None, None
     if not args.eager:
         try:
             graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(graph):
                 step()
+            stage_graphs = []
+            for _, fn in stages:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    fn()
+                stage_graphs.append(g)
             for _ in range(args.warmup):
                 graph.replay()
             torch.cuda.synchronize()
         except RuntimeError as exc:  # pragma: no cover - reported, then timed eagerly
             sys.stderr.write(f"graph capture failed ({exc}); timing eager launches\n")
-            graph = None
+            graph, stage_graphs = None, None
     run = graph.replay if graph is not None else step
+    stage_runs = [g.replay for g in stage_graphs] if stage_graphs else [fn for _, fn in stages]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    flush = needs_l2_flush(wl, args.fp8)
+    flush = needs_l2_flush(wl, layer.fp8 is not None)
     if flush:  # each step timed on its own, after 256 MB of writes have evicted the layer from L2
         scratch = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=stream.device)
         begins = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(local) as clk:
+    nst = len(stages)
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(clk_gpu if clk_gpu is not None else torch.cuda.current_device()) as clk:
         start.record(stream)
         for k in range(args.steps):
             if flush:
@@ -425,51 +465,141 @@ def run_ours(args, wl, dist, rank, local):
             marks[k].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        # stage pass (not part of the step timing)
+        for k in range(args.steps):
+            if flush:
+                scratch.zero_()
+            for j, r in enumerate(stage_runs):
+                sev[k][j].record(stream)
+                r()
+            sev[k][nst].record(stream)
+        torch.cuda.synchronize()
     if flush:
         step_ms = [begins[k].elapsed_time(marks[k]) for k in range(args.steps)]
     else:
         step_ms = [start.elapsed_time(marks[0])] + [marks[k - 1].elapsed_time(marks[k])
                                                     for k in range(1, args.steps)]
-    if dist is not None:
-        dist.barrier()
     if layer.device_status() != 0:
         raise RuntimeError("device status not clean after the timed region")
+    stage_ms = {n: float(np.mean([sev[k][j].elapsed_time(sev[k][j + 1]) for k in range(args.steps)]))
+                for j, (n, _) in enumerate(stages)}
     total_ms = float(sum(step_ms)) if flush else start.elapsed_time(end)
-    t_max = max_over_ranks(dist, total_ms)
-    ms_per_step = t_max / args.steps
+    return {"step_ms": step_ms, "total_ms": total_ms, "stage_ms": stage_ms, "graph": graph is not None,
+            "clocks": clk.summary(), "out": out, "stats": stats, "launches": len(stages)}
+
+
+def ffn_kernel_label(wl, fp8: bool) -> str:
+    if fp8:
+        if wl.T <= 64:
+            return ("fp8_ffn_decode_kernel (tcgen05, E4M3 weights converted into tensor memory as the A operand), "
+                    "moe_expert_ffn_fp8: gate/up and down in one cooperative launch")
+        return ("grouped_gemm_fp8 (tcgen05, E4M3 weights converted into a shared-memory B operand), "
+                "moe_expert_ffn_fp8: gate/up + down launches")
+    if wl.dtype == "f32":
+        return "simt_gemm_kernel (float32 CUDA-core FMA), moe_expert_ffn: gate/up + down launches"
+    return "grouped_gemm (tcgen05), moe_expert_ffn: gate/up + down launches"
+
+
+def launches_per_step(wl, fp8: bool) -> int:
+    """Kernels of one step: route = split W_g + tensor-core logits + top-k (bf16) or
+    logits + top-k (float32); dispatch = histogram, scan, rank, copy; experts 2 (1
+    for the one-launch FP8 decode FFN); shared 2; combine 1; statistics 2."""
+    ffn = 1 if (fp8 and wl.T <= 64) else 2
+    return (3 if wl.dtype == "bf16" else 2) + 4 + ffn + (2 if wl.shared_F else 0) + 1 + 2
+
+
+def layer_report(wl, layer, t, peaks, peak_src, fp8: bool, steps: int, world: int = 1):
+    """Tokens/s, stage rooflines and the dominant kernel's roofline object of one
+    timed run `t` (time_layer's result)."""
+    v = layer.views()
+    counts_kept = v["counts_kept"].cpu().numpy()
+    kept_rows = int(counts_kept.sum())
+    touched = int(np.count_nonzero(counts_kept))
+    work = stage_work(wl, kept_rows, touched, fp8)
+    f32 = wl.dtype == "f32"
+    clocks = t["clocks"]
+    stages = {n: stage_roofline(work[n][0], work[n][1], ms, peaks, clocks,
+                                alu=f32 and n in ("route", "expert_ffn", "shared_ffn"))
+              for n, ms in t["stage_ms"].items()}
+    ffn = stages["expert_ffn"]
+    roof = {k: ffn[k] for k in ("bound", "achieved", "peak", "unit", "frac", "frac_clock_norm", "frac_sustained")
+            if k in ffn}
+    roof["traffic"] = _traffic(wl.name, fp8)
+    roof["kernel"] = ffn_kernel_label(wl, fp8)
+    roof["peak_source"] = ("derived float32 CUDA-core peak (148 SMs x 128 lanes x 2 FLOP x 2032 MHz)"
+                           if ffn["bound"] == "alu" else
+                           f"{peak_src} " + ("hbm_gbs" if ffn["bound"] == "hbm" else "bf16_tflops (burst)"))
+    ms_per_step = t["total_ms"] / steps
+    fl = layer_flops(wl, kept_rows)
+    lb = layer_bytes(wl, touched, fp8)
+    layer = {"flops": fl["total"], "tflops": fl["total"] / (ms_per_step / 1e3) / 1e12, "kept_rows": kept_rows,
+             "touched_experts": touched, "algorithmic_bytes": lb, "gbs": lb / (ms_per_step / 1e3) / 1e9,
+             "hbm_frac": lb / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"]}
+    return {"value": wl.T * steps * world / (t["total_ms"] / 1e3), "ms_per_step": ms_per_step,
+            "stages": stages, "roofline": roof, "layer": layer}
+
+
+def time_decode(args, moe, layer, peaks, peak_src, stream, fp8: bool):
+    """The Mixtral-shaped decode layer (T = 16, the prefill layer's own weights and
+    router) on the same GPU and process: its step, stages, and the layer's
+    algorithmic bytes over the step time against the measured HBM bandwidth."""
+    import torch
+    dwl = synth.WORKLOADS["mixtral_decode"]
+    x = _to_dev(synth.normal(dwl.seed, synth.TID_X, (dwl.T, dwl.d), 1.0, "bf16"), "bf16")
+    cfg = moe.make_config(dwl.T, dwl.d, dwl.N, dwl.k, dwl.F, 0, moe.GATE_SOFTMAX_TOPK, moe.ACT_SWIGLU,
+                          moe.DTYPE_BF16, 0)
+    dl = moe.MoELayer(cfg, layer.Wg, layer.w1, layer.w3, layer.w2)
+    if fp8:
+        dl.fp8 = layer.fp8 if layer.fp8 is not None else dl.quantize_fp8()
+        torch.cuda.synchronize()
+    t = time_layer(args, moe, dl, x, dwl, stream)
+    r = layer_report(dwl, dl, t, peaks, peak_src, fp8, args.steps)
+    return {"workload": dwl.name, "T": dwl.T, "expert_weights": "fp8 e4m3, one float32 scale per row" if fp8
+            else "bf16", "value": r["value"], "unit": "tokens/s", "ms_per_step": r["ms_per_step"],
+            "step_ms_p50": float(np.percentile(t["step_ms"], 50)),
+            "layer_bytes": r["layer"]["algorithmic_bytes"], "touched_experts": r["layer"]["touched_experts"],
+            "achieved_gbs": r["layer"]["gbs"], "peak_gbs": peaks["hbm_gbs"], "frac": r["layer"]["hbm_frac"],
+            "expert_ffn": r["stages"]["expert_ffn"], "roofline": r["roofline"], "clocks": t["clocks"]}
+
+
+def run_ours(args, wl, dist, rank, local):
+    import torch
+
+    import sparse_mixture_experts_62_b300 as moe
+
+    torch.cuda.set_device(local)
+    inp = synth.make_inputs(wl)
+    layer = build_layer(moe, inp)
+    if args.fp8:  # weights quantised once, outside the timed region (like any weight packing)
+        if wl.dtype != "bf16":
+            raise SystemExit("--fp8 needs a bf16 workload")
+        layer.quantize_fp8()
+        torch.cuda.synchronize()
+    x = _to_dev(inp.x, wl.dtype)
+    stream = torch.cuda.current_stream()
+    t = time_layer(args, moe, layer, x, wl, stream, dist, local)
+    t_max = max_over_ranks(dist, t["total_ms"])
     world = dist.get_world_size() if dist is not None else 1
-    value = wl.T * args.steps * world / (t_max / 1e3)
+    t["total_ms"] = t_max
+    peaks, peak_src = measured_peaks()
+    rep = layer_report(wl, layer, t, peaks, peak_src, args.fp8, args.steps, world)
+    out, stats = t["out"], t["stats"]
+    frac = rep["roofline"]["frac"]
+    if frac > 1.15:  # above a measured peak by this much, the timed kernel is not doing the work
+        raise RuntimeError(f"roofline fraction {frac:.3f} exceeds the measured peak: accounting error")
 
     # optional: the backward step (gradients of a fixed dout), graph-replayed
     bwd = None
     if args.backward:
         bwd = time_backward(args, moe, layer, x, wl, stream)
-
-    # routing facts of this run (for the algorithmic counts)
-    counts_kept = v["counts_kept"].cpu().numpy()
-    kept_rows = int(counts_kept.sum())
-    touched = int(np.count_nonzero(counts_kept))
-    fl = layer_flops(wl, kept_rows)
-    peaks, peak_src = measured_peaks()
-    clocks = clk.summary()
-    sustained = "sw_power_cap" in clocks.get("reasons", [])
-    work = stage_work(wl, kept_rows, touched, args.fp8)
-    f32 = wl.dtype == "f32"
-    stages = {n: stage_roofline(work[n][0], work[n][1], stage_ms[n], peaks, sustained,
-                                alu=f32 and n in ("route", "expert_ffn", "shared_ffn")) for n in stages}
-    ffn = stages["expert_ffn"]
-    roof = {"bound": ffn["bound"], "achieved": ffn["achieved"], "peak": ffn["peak"], "unit": ffn["unit"],
-            "frac": ffn["frac"], "traffic": _traffic(wl.name, args.fp8),
-            "kernel": ((("fp8_ffn_decode_kernel (tcgen05, E4M3 weights converted into tensor memory as the A "
-                          "operand), moe_expert_ffn_fp8: gate/up and down in one cooperative launch")
-                         if wl.T <= 64 else
-                         ("grouped_gemm_fp8 (tcgen05, E4M3 weights converted into a shared-memory B operand), "
-                          "moe_expert_ffn_fp8: gate/up + down launches"))
-                        if args.fp8 else "grouped_gemm (tcgen05), moe_expert_ffn: gate/up + down launches"),
-            "peak_source": ("derived float32 CUDA-core peak (148 SMs x 128 lanes x 2 FLOP x 2032 MHz)"
-                            if ffn["bound"] == "alu" else f"{peak_src} " + ("hbm_gbs" if ffn["bound"] == "hbm" else
-                            ("bf16_tflops_sustained (power cap seen in the timed region)" if sustained
-                             else "bf16_tflops (burst)")))}
+    # the decode-shaped layer on the prefill layer's weights, same process and GPU
+    decode = decode_fp8 = None
+    if wl.name == "mixtral_prefill" and not args.no_decode:
+        decode = time_decode(args, moe, layer, peaks, peak_src, stream, args.fp8)
+        if not args.fp8:  # the same decode step with the experts' weights in FP8 E4M3
+            decode_fp8 = time_decode(args, moe, layer, peaks, peak_src, stream, True)
 
     # End to end through the public API: every step copies its x in from pinned host
     # memory and its output and statistics back.  Copies run on their own streams
@@ -495,7 +625,7 @@ def run_ours(args, wl, dist, rank, local):
 
     # the compute of each buffer slot as a CUDA graph (the copies stay on their streams)
     slot_graphs = None
-    if graph is not None:
+    if t["graph"]:
         slot_graphs = []
         for b in range(2):
             compute(b)  # warm
@@ -544,28 +674,29 @@ def run_ours(args, wl, dist, rank, local):
     h2d = x.numel() * x.element_size()
     d2h = out.numel() * out.element_size() + stats.numel() * 4
 
-    # route: split W_g + tensor-core logits + top-k (bf16) or logits + top-k (float32);
-    # dispatch: histogram, scan, rank, gather; experts: 2; shared: 2; combine: 1; stats: 2
-    ffn_launches = 1 if (args.fp8 and wl.T <= 64) else 2  # FP8 decode: gate/up and down in one launch
-    launches_per_step = (3 if wl.dtype == "bf16" else 2) + 4 + ffn_launches + (2 if has_shared else 0) + 1 + 2
     if rank == 0:
-        sys.stderr.write("per-stage ms: " + json.dumps({k: round(val, 4) for k, val in stage_ms.items()}) + "\n")
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        sys.stderr.write("per-stage ms: " + json.dumps({k: round(val, 4) for k, val in t["stage_ms"].items()}) + "\n")
+        step_ms = t["step_ms"]
+        n_launch = launches_per_step(wl, args.fp8)
+        line = {"metric": METRIC, "value": rep["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": rep["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak",
                 "step_ms": {"p10": float(np.percentile(step_ms, 10)), "p50": float(np.percentile(step_ms, 50)),
                             "p90": float(np.percentile(step_ms, 90))},
                 "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-                "config": {**config_of(wl, args.fp8), "launch": "cuda_graph" if graph is not None else "eager",
+                "config": {**config_of(wl, args.fp8),
                            **({"expert_weights": "fp8 e4m3, one float32 scale per row"} if args.fp8 else {})},
-                "roofline": roof,
-                "stages": stages,
-                "layer": {"flops": fl["total"], "tflops": fl["total"] / (ms_per_step / 1e3) / 1e12,
-                          "kept_rows": kept_rows, "touched_experts": touched,
-                          "algorithmic_bytes": layer_bytes(wl, touched, args.fp8)},
+                "launch": "cuda_graph" if t["graph"] else "eager",
+                "roofline": rep["roofline"],
+                "stages": rep["stages"],
+                "layer": rep["layer"],
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-                "gpu_launches": launches_per_step * args.steps,
+                # timed region: one step's launches per replay; the stage pass replays the same launches again
+                "gpu_launches": n_launch * args.steps,
+                **({"decode": decode} if decode is not None else {}),
+                **({"decode_fp8": decode_fp8} if decode_fp8 is not None else {}),
                 **({"backward": bwd} if bwd is not None else {}),
-                "clocks": clocks}
+                "clocks": t["clocks"]}
         if args.cpu_baseline_tokens > 0:
             line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_baseline_tokens)
         print(json.dumps(line), flush=True)
@@ -623,12 +754,14 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-baseline-tokens", type=int, default=512,
-                    help="tokens the oracle runs the expert FFN on for cpu_baseline (0 = skip)")
-    ap.add_argument("--ref-sample", type=int, default=1, help="tokens per reference-arm step")
+                    help="tokens of the oracle's cpu_baseline step (as the reference arm's; 0 = skip)")
+    ap.add_argument("--ref-sample", type=int, default=512, help="tokens per reference-arm step")
     ap.add_argument("--override", nargs="*", default=[], help="workload fields to change, e.g. N=32 T=1024")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of a CUDA-graph replay")
     ap.add_argument("--backward", action="store_true", help="also time the backward step (bf16 token choice)")
     ap.add_argument("--fp8", action="store_true", help="FP8 E4M3 expert weights with per-row scales (bf16 workloads)")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode-shaped layer that the Mixtral prefill run also times")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

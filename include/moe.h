@@ -151,7 +151,11 @@ MOE_API int moe_route(const moe_config *cfg, const void *x, const float *Wg, con
  * assignments in ascending token order are kept, at rows offsets[e] + rank;
  * dest_row[t, j] = that row or -1 (dropped); src_token[row] = t; and
  * x_perm[row, :] = x[t, :].  x_perm needs room for T * k rows; rows at or
- * beyond offsets[N] are left untouched. */
+ * beyond offsets[N] are left untouched.  A token picks an expert at most once:
+ * an id in topk_idx outside [0, N) is skipped and sets MOE_ERR_BOUNDS, an id that
+ * repeats an earlier slot of the same token is skipped (not counted, dest_row
+ * -1) and sets MOE_ERR_INVALID_ARG, both in the device status word.  Token-choice
+ * configs only (MOE_ERR_INVALID_ARG for expert choice). */
 MOE_API int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x, int32_t *counts_routed,
                  int32_t *counts_kept, int32_t *offsets, int32_t *dest_row, int32_t *src_token,
                  void *x_perm, void *ws, void *stream);
@@ -161,9 +165,11 @@ MOE_API int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const v
  * host program that has already reserved the GPU's memory for its own pool and
  * whose interface hands the operator only its input and output buffers.  The
  * pages describe no such variant; it has no counterpart there.
- * Inputs, outputs and results are exactly those of moe_dispatch.  `status` is an
- * optional device int32 (may be NULL) in which bit MOE_ERR_BOUNDS is set when an
- * expert id is out of range; the caller clears it.
+ * Inputs, outputs and results are exactly those of moe_dispatch, token-choice
+ * configs only (MOE_ERR_INVALID_ARG for expert choice, as moe_dispatch).  `status`
+ * is an optional device int32 (may be NULL) in which bit MOE_ERR_BOUNDS is set
+ * when an expert id is out of range and bit MOE_ERR_INVALID_ARG when a token
+ * repeats an expert; the caller clears it.
  * Scratch: a fixed 1 MiB array inside the library (a `static __device__`
  * variable), resident on every GPU that loads the library until the process
  * exits.  It bounds the size: ceil(T / 128) * N <= 131072 (for example T up to

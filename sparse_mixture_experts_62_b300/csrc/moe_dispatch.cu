@@ -24,6 +24,16 @@ namespace {
 constexpr int CH = kDispatchChunk;  // tokens per chunk = threads per CTA
 constexpr int CH_WARPS = CH / 32;
 
+// A token picks an expert at most once.  A top-k input that lists expert e in
+// slot j and in an earlier slot keeps only the earlier one: the repeat is neither
+// counted nor given a row (dest_row = -1), so every counted assignment has a row.
+__device__ __forceinline__ bool repeats_earlier_slot(const int (&ex)[8], int j, int e) {
+  bool rep = false;
+#pragma unroll
+  for (int i = 0; i < 7; ++i) rep |= (i < j) && (ex[i] == e);
+  return rep;
+}
+
 __global__ void __launch_bounds__(CH) dispatch_hist_kernel(const int32_t *__restrict__ idx, int T, int k, int N,
                                                            int32_t *__restrict__ hist, int *status) {
   __shared__ int cnt[256];
@@ -31,10 +41,16 @@ __global__ void __launch_bounds__(CH) dispatch_hist_kernel(const int32_t *__rest
   __syncthreads();
   const int t = blockIdx.x * CH + threadIdx.x;
   if (t < T) {
+    int ex[8];
     for (int j = 0; j < k; ++j) {
       const int e = idx[(size_t)t * k + j];
+      ex[j] = e;
       if (e < 0 || e >= N) {
         set_status(status, MOE_ERR_BOUNDS);
+        continue;
+      }
+      if (repeats_earlier_slot(ex, j, e)) {  // counted once; the rank kernel drops the repeat
+        set_status(status, MOE_ERR_INVALID_ARG);
         continue;
       }
       atomicAdd(&cnt[e], 1);
@@ -91,7 +107,7 @@ __global__ void __launch_bounds__(CH) dispatch_rank_kernel(const int32_t *__rest
     ex[j] = -1;
     if (t < T) {
       const int e = idx[(size_t)t * k + j];
-      if (e >= 0 && e < N) {
+      if (e >= 0 && e < N && !repeats_earlier_slot(ex, j, e)) {
         ex[j] = e;
         atomicOr(&lanes_with[warp][e], 1u << lane);
       }

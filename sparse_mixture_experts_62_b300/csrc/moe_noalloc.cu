@@ -66,6 +66,8 @@ extern "C" MOE_API int moe_dispatch_noalloc(const moe_config *cfg, const int32_t
   size_t ws_bytes = 0;
   const int rc0 = moe_workspace_size(cfg, &ws_bytes);
   if (rc0) return rc0;
+  // expert choice routes and dispatches in moe_ec_route; moe_dispatch refuses it too
+  if (cfg->routing == MOE_ROUTING_EXPERT_CHOICE) return MOE_ERR_INVALID_ARG;
   if (!counts_routed || !counts_kept || !offsets) return MOE_ERR_INVALID_ARG;
   if (cfg->T > 0 && (!topk_idx || !x || !dest_row || !src_token || !x_perm ||
                      (reinterpret_cast<uintptr_t>(x) & 15) || (reinterpret_cast<uintptr_t>(x_perm) & 15)))

@@ -3,19 +3,28 @@
 The oracle always runs on the seeded inputs alone, with its own routing; nothing
 the GPU computed is ever fed to it.  Parity rules (bf16 workloads; the float32
 workload uses 1e-4 relative):
-  * top-k: every token whose oracle gap between the k-th and (k+1)-th selection
-    scores exceeds 1e-4 must have the oracle's set, and its order where the gaps
-    between adjacent selected scores also exceed 1e-4.  A token where the GPU's
-    choice differs from the oracle's must be a valid choice by the oracle's
-    scores (every expert above the k-th score + 1e-4 taken, nothing below the
-    k-th score - 1e-4, order descending up to 1e-4); such tokens must be rare
-    (at most max(1, T / 1000)) and are left out of the float comparisons below.
+  * top-k against the GPU's own logits: on every token, the GPU's experts and
+    their slot order are exactly the (selection score desc, index asc) top-k
+    of the selection scores that its own dumped float32 logits define, worked
+    out here in double (sigmoid rounded once to float32, then + b in float32);
+    its gate weights are within 1e-6 of the gate those logits define.  Exact
+    ties go to the lower index, so this also pins the tie-break.
+  * top-k against the oracle: every token whose oracle gap between the k-th and
+    (k+1)-th selection scores exceeds 1e-4 must have the oracle's set, and its
+    order where the gaps between adjacent selected scores also exceed 1e-4.  A
+    token where the GPU's choice differs from the oracle's must be a valid
+    choice by the oracle's scores (every expert above the k-th score + 1e-4
+    taken, nothing below the k-th score - 1e-4, order descending up to 1e-4);
+    such tokens must be rare (at most max(1, T / 1000)).
   * gate weights: within 1e-6 of the oracle's on tokens whose top-k equals it.
   * dispatch: equal to the oracle's where no differing token touches the expert;
     every expert's rows, counts and offsets satisfy the dispatch definition on the
     GPU's own top-k.
   * layer output: max|gpu - ref| <= 2e-2 * max|ref| + 1e-3 (bf16), <= 1e-4 * max|ref|
-    (float32), on tokens whose top-k and kept set equal the oracle's.
+    (float32).  A token whose top-k and kept set equal the oracle's is compared
+    with the oracle's output row; any other token with the sum, over the slots
+    the GPU kept, of the gate (from the GPU's logits) times the oracle's expert
+    output for the expert the GPU chose (plus the oracle's shared expert).
 """
 from __future__ import annotations
 
@@ -60,11 +69,59 @@ def layer_on_device(inp) -> moe.MoELayer:
                         f32(inp.sel_bias))
 
 
+def own_logit_routing(z_gpu: np.ndarray, gate: str, sel_bias, k: int):
+    """The top-k and gate weights that the GPU's dumped float32 logits define,
+    worked out here from the definitions (not by the oracle, which never sees a
+    GPU result): selection score z (softmax gates) or fl32(fl32(sigmoid(z)) + b)
+    (sigmoid gate, sigmoid in double); experts ordered by (score desc, index asc)
+    -- a stable sort keeps equal scores in index order, so exact ties go to the
+    lower index; gates: softmax over the selected logits, the full softmax kept
+    on the selected, or the raw affinities normalised over the selected.
+    Returns (idx [T, k] int32, w [T, k] float64, sel [T, N] float32)."""
+    z64 = z_gpu.astype(np.float64)
+    s = None
+    if gate == "sigmoid":
+        s = (1.0 / (1.0 + np.exp(-z64))).astype(np.float32)
+        sel = s if sel_bias is None else (s + np.asarray(sel_bias, np.float32)[None, :]).astype(np.float32)
+    else:
+        sel = z_gpu.astype(np.float32)
+    order = np.argsort(-sel, axis=1, kind="stable")
+    idx = order[:, :k].astype(np.int32)
+    rows = np.arange(z64.shape[0])[:, None]
+    if gate == "softmax":
+        zs = z64[rows, idx]
+        e = np.exp(zs - zs.max(axis=1, keepdims=True))
+        w = e / e.sum(axis=1, keepdims=True)
+    elif gate == "softmax_full":
+        m = z64.max(axis=1, keepdims=True)
+        e = np.exp(z64 - m)
+        w = e[rows, idx] / e.sum(axis=1, keepdims=True)
+    else:
+        ss = s.astype(np.float64)[rows, idx]
+        w = ss / ss.sum(axis=1, keepdims=True)
+    return idx, w, sel
+
+
+def check_own_logits(z_gpu: np.ndarray, idx_gpu: np.ndarray, w_gpu: np.ndarray, gate: str, sel_bias, k: int):
+    """Every token's top-k (set and slot order) bit-exact, and its gate weights
+    within 1e-6, against what the GPU's own logits define.  Returns the gate
+    weights those logits define (float64)."""
+    idx_own, w_own, _ = own_logit_routing(z_gpu, gate, sel_bias, k)
+    bad = np.nonzero(np.any(idx_gpu != idx_own, axis=1))[0]
+    assert bad.size == 0, (f"{bad.size} tokens' top-k differ from the top-k of the GPU's own logits "
+                           f"(first: token {bad[0]}: gpu {idx_gpu[bad[0]].tolist()}, "
+                           f"own logits {idx_own[bad[0]].tolist()})" if bad.size else "")
+    assert np.max(np.abs(w_gpu - w_own), initial=0.0) <= 1e-6, "gate weights differ from the GPU's own logits' gate"
+    return w_own
+
+
 def check_routing(inp, z_gpu: np.ndarray, idx_gpu: np.ndarray, w_gpu: np.ndarray, ref: oracle.LayerResult):
-    """Top-k and gate parity against the oracle's own routing `ref`.  Returns the
-    mask of tokens whose top-k equals the oracle's, slot by slot."""
+    """Top-k and gate parity: against the GPU's own logits on every token, and
+    against the oracle's own routing `ref`.  Returns the mask of tokens whose
+    top-k equals the oracle's, slot by slot."""
     wl = inp.wl
     k, N, T = wl.k, wl.N, wl.T
+    check_own_logits(z_gpu, idx_gpu, w_gpu, wl.gate, inp.sel_bias, k)
     # logits agree to float32 accumulation error
     assert np.max(np.abs(z_gpu.astype(np.float64) - ref.z.astype(np.float64))) < 1e-3, "router logits differ"
     assert np.all((idx_gpu >= 0) & (idx_gpu < N)), "expert index out of range"
@@ -152,6 +209,36 @@ def check_dispatch(wl, idx, counts_routed, counts_kept, offsets, dest_row, src_t
     S = int(d.offsets[-1])
     assert np.array_equal(src_token[:S], d.src_token)
     return d
+
+
+def rows_by_gpu_routing(inp, ref: oracle.LayerResult, tokens, z_gpu, idx_gpu, dest_row) -> np.ndarray:
+    """Expected output rows [len(tokens), d] for tokens whose routing or kept set
+    differs from the oracle's: the oracle's shared-expert row plus, over the slots
+    the GPU kept (dest_row >= 0), the gate that the GPU's logits define times the
+    oracle's output of the chosen expert on that token.  The chosen experts have
+    been checked to be valid by the oracle's own scores (check_routing) and the
+    kept slots to follow the dispatch definition (check_dispatch_definition)."""
+    wl = inp.wl
+    tokens = np.asarray(tokens, dtype=np.int64)
+    out = np.zeros((tokens.size, wl.d))
+    if tokens.size == 0:
+        return out
+    _, w_own, _ = own_logit_routing(z_gpu[tokens], wl.gate, inp.sel_bias, wl.k)
+    x64 = oracle.widen(inp.x[tokens], wl.dtype)
+    if ref.y_sh is not None:
+        out += ref.y_sh[tokens]
+    for e in np.unique(idx_gpu[tokens]):
+        hit = [(i, j) for i, t in enumerate(tokens) for j in range(wl.k)
+               if idx_gpu[t, j] == e and dest_row[t, j] >= 0]
+        if not hit:
+            continue
+        ii = np.array([i for i, _ in hit])
+        W3 = oracle.widen(inp.w3[e], wl.dtype) if inp.w3 is not None else None
+        y = oracle.expert_ffn(x64[ii], oracle.widen(inp.w1[e], wl.dtype), W3, oracle.widen(inp.w2[e], wl.dtype),
+                              wl.act)
+        for r, (i, j) in enumerate(hit):
+            out[i] += w_own[i, j] * y[r]
+    return out
 
 
 def assert_close_out(gpu: np.ndarray, ref: np.ndarray, dtype: str, what="output"):

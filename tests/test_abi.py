@@ -142,6 +142,12 @@ def test_expert_choice_config_sizes_the_workspace_for_N_times_C_rows():
     A = 1 << 20
     with pytest.raises(moe.MoeError):   # token-choice route on an expert-choice config
         moe.moe_route(ec, A, A, None, None, A, A, A, A, 0)
+    # both dispatch entry points refuse expert choice (it dispatches in moe_ec_route)
+    for fn in (lambda: moe.moe_dispatch(ec, A, A, A, A, A, A, A, A, A, 0),
+               lambda: moe.moe_dispatch_noalloc(ec, A, A, A, A, A, A, A, A, None, 0)):
+        with pytest.raises(moe.MoeError) as e:
+            fn()
+        assert e.value.code == moe.MOE_ERR_INVALID_ARG
 
 
 def test_zero_tokens_is_a_noop_for_the_layer():

@@ -56,18 +56,22 @@ def test_stage_work_matches_layer_counts():
 
 def test_stage_roofline_picks_the_longer_bound():
     peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1500.0}
-    # 3 TFLOP and 3 GB: 1.5 ms at the burst tensor peak, 0.5 ms at HBM -> tensor
-    r = bench.stage_roofline(3e12, 3e9, 2.0, peaks, sustained=False)
+    # 3 TFLOP and 3 GB: 1.5 ms at the burst tensor peak, 0.5 ms at HBM -> tensor, against the burst peak
+    r = bench.stage_roofline(3e12, 3e9, 2.0, peaks)
     assert r["bound"] == "tensor" and r["peak"] == 2000.0
     assert r["achieved"] == pytest.approx(1500.0) and r["frac"] == pytest.approx(0.75)
-    # the sustained peak when the power cap was seen
-    r = bench.stage_roofline(3e12, 3e9, 2.0, peaks, sustained=True)
-    assert r["peak"] == 1500.0 and r["frac"] == pytest.approx(1.0)
+    assert r["frac_sustained"] == pytest.approx(1.0) and "frac_clock_norm" not in r
+    # a power cap seen in the clock samples changes no peak; the clock-normalised reading
+    # divides by the burst peak scaled to the median sampled SM clock
+    clocks = {"sm_mhz": 1016.0, "sm_max_mhz": 2032.0, "reasons": ["sw_power_cap"]}
+    r = bench.stage_roofline(3e12, 3e9, 2.0, peaks, clocks)
+    assert r["peak"] == 2000.0 and r["frac"] == pytest.approx(0.75)
+    assert r["frac_clock_norm"] == pytest.approx(1.5)
     # 10 GFLOP and 3 GB: HBM governs
-    r = bench.stage_roofline(1e10, 3e9, 1.0, peaks, sustained=False)
+    r = bench.stage_roofline(1e10, 3e9, 1.0, peaks)
     assert r["bound"] == "hbm" and r["achieved"] == pytest.approx(3000.0) and r["frac"] == pytest.approx(0.5)
     # float32 work against the CUDA-core peak
-    r = bench.stage_roofline(1e9, 1e6, 1.0, peaks, sustained=False, alu=True)
+    r = bench.stage_roofline(1e9, 1e6, 1.0, peaks, alu=True)
     assert r["bound"] == "alu" and r["peak"] == pytest.approx(bench.F32_ALU_TFLOPS)
 
 
@@ -77,11 +81,26 @@ def test_l2_flush_only_when_the_weights_fit():
         assert not bench.needs_l2_flush(W[name]) and not bench.needs_l2_flush(W[name], True)
 
 
-def test_traffic_only_for_the_captured_kernel_revision(monkeypatch):
-    assert bench._traffic("mixtral_prefill") == bench.NCU_TRAFFIC[("mixtral_prefill", False)]["bytes"]
-    assert bench._traffic("dsv3_finegrained") is None
-    monkeypatch.setitem(bench.KERNEL_REV, False, "changed")
-    assert bench._traffic("mixtral_prefill") is None
+def test_traffic_only_for_the_captured_kernel_sources(tmp_path):
+    """The traffic table row counts only while the kernel sources hash as they did
+    when it was captured."""
+    h = bench.kernel_source_hash(False)
+    assert len(h) == 16 and h != bench.kernel_source_hash(True)
+    p = tmp_path / "traffic.md"
+    p.write_text("| workload | weights | sources | bytes | command |\n|---|---|---|---|---|\n"
+                 f"| mixtral_prefill | bf16 | {h} | 3.5e9 | ncu ... |\n"
+                 "| qwen3_skew_drop | bf16 | 0123456789abcdef | 1e9 | ncu ... |\n")
+    table = bench.traffic_table(str(p))
+    assert bench._traffic("mixtral_prefill", table=table) == 3.5e9
+    assert bench._traffic("qwen3_skew_drop", table=table) is None      # captured on other sources
+    assert bench._traffic("mixtral_prefill", True, table=table) is None
+    assert bench._traffic("dsv3_finegrained", table=table) is None
+
+
+def test_fp32_kernel_label():
+    assert "simt" in bench.ffn_kernel_label(W["shazeer_tiny_f32"], False)
+    assert "tcgen05" in bench.ffn_kernel_label(W["mixtral_prefill"], False)
+    assert "one cooperative launch" in bench.ffn_kernel_label(W["mixtral_decode"], True)
 
 
 def test_reference_arm_prints_the_contract_line():

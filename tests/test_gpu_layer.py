@@ -4,8 +4,11 @@ Small layers are compared on every output; the full-size workloads (the
 Mixtral-shaped prefill and decode layers, the DeepSeek-V3-shaped and the
 Qwen3-shaped layers) are run in the launch configuration the benchmark times,
 with routing, dispatch and statistics compared on all tokens and the layer
-output on all tokens or on a seeded sample of them.  The oracle routes on its
-own; the rules for the rare token the two route differently are in parity.py.
+output on all tokens -- except the DeepSeek-V3-shaped layer, whose output is
+compared on the tokens of the first and last row of every 128-row tile of every
+expert group and of the shared expert, plus a seeded sample.  The oracle routes
+on its own; the rules for the rare token the two route differently are in
+parity.py.
 """
 import numpy as np
 import pytest
@@ -13,12 +16,32 @@ import torch
 
 import oracle
 import synth
-from parity import assert_close_out, check_layer_dispatch, check_routing, layer_on_device, to_dev, to_np_f64
+from parity import (assert_close_out, check_layer_dispatch, check_routing, layer_on_device, rows_by_gpu_routing,
+                    to_dev, to_np_f64)
 
 pytestmark = pytest.mark.gpu
 
 
+def tile_edge_tokens(disp, T, extra, seed, tile=128):
+    """Tokens whose rows are the first or last row of a 128-row tile of an
+    expert group (in the oracle's own dispatch) or of the shared expert's rows
+    (token order), plus `extra` seeded tokens."""
+    toks = set()
+    off = disp.offsets
+    for e in range(len(off) - 1):
+        for r0 in range(int(off[e]), int(off[e + 1]), tile):
+            r1 = min(r0 + tile, int(off[e + 1])) - 1
+            toks.add(int(disp.src_token[r0]))
+            toks.add(int(disp.src_token[r1]))
+    for r0 in range(0, T, tile):
+        toks.update((r0, min(r0 + tile, T) - 1))
+    toks.update(np.random.default_rng(seed).choice(T, extra, replace=False).tolist())
+    return np.array(sorted(toks), dtype=np.int64)
+
+
 def run_and_check(inp, sample=None):
+    """sample: None (every token's output), an int (that many seeded tokens) or
+    "tiles" (tile_edge_tokens of the oracle's dispatch plus 256 seeded tokens)."""
     wl = inp.wl
     layer = layer_on_device(inp)
     x = to_dev(inp.x, wl.dtype)
@@ -30,7 +53,13 @@ def run_and_check(inp, sample=None):
     z = v["logits"].cpu().numpy()
     idx = v["topk_idx"].cpu().numpy()
     w = v["topk_w"].cpu().numpy().astype(np.float64)
-    tokens = None if sample is None else np.sort(np.random.default_rng(wl.seed).choice(wl.T, sample, replace=False))
+    if sample is None:
+        tokens = None
+    elif sample == "tiles":
+        own = oracle.layer_forward(inp, tokens=np.array([], dtype=np.int64))  # the oracle's own dispatch
+        tokens = tile_edge_tokens(own.disp, wl.T, 256, wl.seed)
+    else:
+        tokens = np.sort(np.random.default_rng(wl.seed).choice(wl.T, sample, replace=False))
     ref = oracle.layer_forward(inp, tokens=tokens)  # the oracle's own routing, from the inputs alone
     same = check_routing(inp, z, idx, w, ref)
     cap = layer.cfg.capacity
@@ -39,8 +68,14 @@ def run_and_check(inp, sample=None):
                                  v["src_token"].cpu().numpy(), cap, ref)
     got = to_np_f64(out)
     rows = np.arange(wl.T) if tokens is None else tokens
+    other = rows[~agree[rows]]
     rows = rows[agree[rows]]
     err, tol = assert_close_out(got[rows], ref.out[rows], wl.dtype)
+    # tokens routed (or kept) differently: the GPU's own routing with the oracle's experts
+    if other.size:
+        dest = v["dest_row"].cpu().numpy()
+        assert_close_out(got[other], rows_by_gpu_routing(inp, ref, other, z, idx, dest), wl.dtype,
+                         what="output of tokens routed differently from the oracle")
     # statistics: exact where no differing token touches an expert
     fg = f.cpu().numpy()
     if np.all(same):
@@ -97,11 +132,11 @@ def test_layer_qwen3_skew_drop_full():
 
 
 def test_layer_mixtral_prefill_full():
-    run_and_check(synth.make_inputs(synth.WORKLOADS["mixtral_prefill"]), sample=96)
+    run_and_check(synth.make_inputs(synth.WORKLOADS["mixtral_prefill"]))
 
 
 def test_layer_dsv3_finegrained_full():
-    run_and_check(synth.make_inputs(synth.WORKLOADS["dsv3_finegrained"]), sample=48)
+    run_and_check(synth.make_inputs(synth.WORKLOADS["dsv3_finegrained"]), sample="tiles")
 
 
 def test_layer_deterministic():

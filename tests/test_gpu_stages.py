@@ -163,6 +163,40 @@ def test_dispatch_parity(T, N, k, cap, dtype):
     assert torch.equal(xp[:S].cpu(), xt.cpu()[torch.from_numpy(ref.src_token.astype(np.int64))])
 
 
+def test_dispatch_repeated_expert_is_flagged_and_dropped():
+    """A top-k input that lists an expert twice for one token: the repeat is not
+    counted and gets no row, the device status reports MOE_ERR_INVALID_ARG, and
+    the rest is the dispatch of the input without the repeat."""
+    T, N, k, d = 300, 8, 3, 64
+    rng = np.random.default_rng(9)
+    idx = np.stack([rng.permutation(N)[:k] for _ in range(T)]).astype(np.int32)
+    idx[17, 2] = idx[17, 0]
+    idx[200, 1] = idx[200, 0]
+    cfg = moe.make_config(T, d, N, k, 64)
+    ws = _ws(cfg)
+    x = to_dev(synth.normal(5, 1, (T, d), 1.0, "bf16"), "bf16")
+    dev = lambda shape: torch.full(shape, -7, dtype=torch.int32, device="cuda")  # noqa: E731
+    cr, ck, off, dr, st = dev((N,)), dev((N,)), dev((N + 1,)), dev((T, k)), dev((T * k,))
+    xp = torch.zeros((T * k, d), dtype=torch.bfloat16, device="cuda")
+    moe.moe_dispatch(cfg, torch.from_numpy(idx).cuda(), x, cr, ck, off, dr, st, xp, ws)
+    assert moe.moe_get_device_status(ws) == moe.MOE_ERR_INVALID_ARG
+    dest = dr.cpu().numpy()
+    assert dest[17, 2] == -1 and dest[200, 1] == -1
+    # everything else: the oracle's dispatch with the repeats removed by hand
+    counts = np.bincount(idx.ravel(), minlength=N)
+    counts[idx[17, 0]] -= 1
+    counts[idx[200, 0]] -= 1
+    assert np.array_equal(cr.cpu().numpy(), counts)
+    offn = off.cpu().numpy()
+    assert np.array_equal(offn, np.concatenate([[0], np.cumsum(counts)]))
+    S = int(counts.sum())
+    src = st.cpu().numpy()[:S]
+    for e in range(N):
+        toks = [t for t in range(T) if e in idx[t].tolist()]
+        assert np.array_equal(src[offn[e]:offn[e + 1]], toks)
+    assert torch.equal(xp[:S].cpu(), x.cpu()[torch.from_numpy(src.astype(np.int64))])
+
+
 @pytest.mark.parametrize("dtype,shared", [("bf16", False), ("bf16", True), ("f32", False)])
 def test_combine_parity(dtype, shared):
     T, k, d = 300, 4, 256

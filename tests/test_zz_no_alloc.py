@@ -4,9 +4,10 @@ Some callers -- a plug-in inside a host program that has already reserved the
 GPU's memory and passes the plug-in only its inputs and outputs -- can neither
 call cudaMalloc nor provide a workspace.  moe_dispatch_noalloc keeps its scratch
 in a fixed array inside the library instead.  These tests check, through the C
-ABI, that it produces exactly what moe_dispatch produces, on two calls in a row
-(the second call must not see the first call's leftovers), and that sizes past
-the fixed scratch are refused.
+ABI, that it produces exactly what moe_dispatch produces and what the oracle's
+dispatch of the same top-k gives, on two calls in a row (the second call must not
+see the first call's leftovers), and that sizes past the fixed scratch are
+refused.
 """
 import numpy as np
 import pytest
@@ -48,7 +49,7 @@ def _dispatch_both(T, N, k, cap, seed):
             moe.moe_dispatch(cfg, idx, x, *bufs, xp, ws)
             torch.cuda.synchronize()
         outs.append([b.cpu() for b in bufs] + [xp.cpu()])
-    return outs
+    return outs, idx.cpu().numpy(), x.cpu()
 
 
 @pytest.mark.gpu
@@ -56,9 +57,17 @@ def test_noalloc_matches_moe_dispatch_on_two_calls_in_a_row():
     # a large call first (fills much of the fixed scratch), then a smaller one with
     # other experts: every output of both must equal moe_dispatch's exactly
     for (T, N, k, cap, seed) in [(6000, 128, 8, 300, 1), (333, 8, 2, 0, 2)]:
-        ref, got = _dispatch_both(T, N, k, cap, seed)
+        (ref, got), idx, x = _dispatch_both(T, N, k, cap, seed)
         S = int(ref[2][-1])
         for a, b in zip(ref[:4], got[:4]):
             assert torch.equal(a, b)
         assert torch.equal(ref[4][:S], got[4][:S])
         assert torch.equal(ref[5][:S], got[5][:S])
+        # and the dispatch definition itself, as the oracle computes it
+        d = oracle.dispatch(idx, N, cap)
+        assert np.array_equal(got[0].numpy(), d.counts_routed)
+        assert np.array_equal(got[1].numpy(), d.counts_kept)
+        assert np.array_equal(got[2].numpy(), d.offsets)
+        assert np.array_equal(got[3].numpy(), d.dest_row)
+        assert np.array_equal(got[4][:S].numpy(), d.src_token)
+        assert torch.equal(got[5][:S], x[torch.from_numpy(d.src_token.astype(np.int64))])
