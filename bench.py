@@ -403,55 +403,55 @@ def layer_stages(moe, layer, x, out, stats, wl):
 
 
 def time_layer(args, moe, layer, x, wl, stream, dist=None, clk_gpu=None):
-    """Warm-up, then the timed region: the whole step captured once as a CUDA graph
-    and replayed `args.steps` times (eager launches with --eager), bracketed by a
-    barrier and synchronisation; then, still inside the clock sampling, a stage
-    pass: each stage captured as a graph of its own and replayed in order for
-    `args.steps` steps, with CUDA events between the stages on the same stream.
-    Returns step_ms (per step), total_ms, stage_ms (mean per stage), graph flag,
-    clock summary."""
+    """Warm-up, then the timed region: `args.steps` steps, bracketed by a barrier
+    and synchronisation, with CUDA events on the launching stream.  Each step is a
+    CUDA graph of the whole step (one captured graph per step, so that each holds
+    its own event-record nodes between the stages: the stage times come from the
+    timed steps themselves); with --eager, the stages are launched directly with
+    events between them.  Returns step_ms (per step), total_ms, stage_ms (mean per
+    stage over the timed steps), graph flag, clock summary."""
     import torch
     out = torch.empty((wl.T, wl.d), dtype=x.dtype, device="cuda")
     stats = torch.zeros(2 * wl.N + 4, dtype=torch.float32, device="cuda")
     stages = layer_stages(moe, layer, x, out, stats, wl)
+    nst = len(stages)
 
-    def step():
-        for _, fn in stages:
+    def step(ev=None):
+        for j, (_, fn) in enumerate(stages):
+            if ev is not None:
+                ev[j].record()
             fn()
+        if ev is not None:
+            ev[nst].record()
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if layer.device_status() != 0:
         raise RuntimeError("device status not clean after warm-up")
-    graph, stage_graphs = None, None
+    sev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    graphs = None
     if not args.eager:
         try:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph):
-                step()
-            stage_graphs = []
-            for _, fn in stages:
+            graphs, pool = [], None
+            for k in range(args.steps):
                 g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g):
-                    fn()
-                stage_graphs.append(g)
-            for _ in range(args.warmup):
-                graph.replay()
+                with torch.cuda.graph(g, pool=pool):
+                    step(sev[k])
+                pool = g.pool()
+                graphs.append(g)
+            for k in range(min(args.warmup, args.steps)):
+                graphs[k].replay()
             torch.cuda.synchronize()
         except RuntimeError as exc:  # pragma: no cover - reported, then timed eagerly
             sys.stderr.write(f"graph capture failed ({exc}); timing eager launches\n")
-            graph, stage_graphs = None, None
-    run = graph.replay if graph is not None else step
-    stage_runs = [g.replay for g in stage_graphs] if stage_graphs else [fn for _, fn in stages]
+            graphs = None
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     flush = needs_l2_flush(wl, layer.fp8 is not None)
     if flush:  # each step timed on its own, after 256 MB of writes have evicted the layer from L2
         scratch = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=stream.device)
         begins = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    nst = len(stages)
-    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -461,21 +461,15 @@ def time_layer(args, moe, layer, x, wl, stream, dist=None, clk_gpu=None):
             if flush:
                 scratch.zero_()
                 begins[k].record(stream)
-            run()
+            if graphs is not None:
+                graphs[k].replay()
+            else:
+                step(sev[k])
             marks[k].record(stream)
         end.record(stream)
         torch.cuda.synchronize()
-        if dist is not None:
-            dist.barrier()
-        # stage pass (not part of the step timing)
-        for k in range(args.steps):
-            if flush:
-                scratch.zero_()
-            for j, r in enumerate(stage_runs):
-                sev[k][j].record(stream)
-                r()
-            sev[k][nst].record(stream)
-        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
     if flush:
         step_ms = [begins[k].elapsed_time(marks[k]) for k in range(args.steps)]
     else:
@@ -486,8 +480,8 @@ def time_layer(args, moe, layer, x, wl, stream, dist=None, clk_gpu=None):
     stage_ms = {n: float(np.mean([sev[k][j].elapsed_time(sev[k][j + 1]) for k in range(args.steps)]))
                 for j, (n, _) in enumerate(stages)}
     total_ms = float(sum(step_ms)) if flush else start.elapsed_time(end)
-    return {"step_ms": step_ms, "total_ms": total_ms, "stage_ms": stage_ms, "graph": graph is not None,
-            "clocks": clk.summary(), "out": out, "stats": stats, "launches": len(stages)}
+    return {"step_ms": step_ms, "total_ms": total_ms, "stage_ms": stage_ms, "graph": graphs is not None,
+            "clocks": clk.summary(), "out": out, "stats": stats, "launches": nst}
 
 
 def ffn_kernel_label(wl, fp8: bool) -> str:
@@ -691,7 +685,7 @@ def run_ours(args, wl, dist, rank, local):
                 "stages": rep["stages"],
                 "layer": rep["layer"],
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-                # timed region: one step's launches per replay; the stage pass replays the same launches again
+                # timed region: one step's launches per step
                 "gpu_launches": n_launch * args.steps,
                 **({"decode": decode} if decode is not None else {}),
                 **({"decode_fp8": decode_fp8} if decode_fp8 is not None else {}),

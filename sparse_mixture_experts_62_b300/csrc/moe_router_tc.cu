@@ -9,15 +9,16 @@
 // is computed on the tensor cores -- the bf16x3 method of Henry, Tang &
 // Heinecke, "Leveraging the bfloat16 artificial intelligence datatype for
 // higher-precision computations" (ARITH 2019).  Every product of two bf16
-// values is exact in float32; each 64-wide slice of K is summed by the tensor
-// core and the slices are added in float32 registers (see the kernel), so the
-// result carries float32 accumulation error only.  The three terms are laid out
-// along K: B = [hi | mid | lo], and the A tile of x for k-block kb is x's k-block
-// kb mod (d/64).
+// values is exact in float32; the hi term's 64-wide slices of K are summed by
+// the tensor core one at a time and added in float32 registers (see the
+// kernel), so the result carries float32 accumulation error only.  The three
+// terms are laid out along K: B = [hi | mid | lo], each dp = d rounded up to 64
+// columns wide.
 //
-// One CTA per (128-token tile, K split); the K splits fill the GPU when T is
-// small.  Each CTA writes its raw float32 partial sums; the top-k kernel adds
-// the splits in a fixed order (deterministic) plus the logit bias.
+// One CTA per (128-token tile, tile of up to 128 experts, K split); the K splits
+// fill the GPU when T is small.  Each CTA writes its raw float32 partial sums;
+// the top-k kernel adds the splits in a fixed order (deterministic) plus the
+// logit bias.
 #include <algorithm>
 #include <mutex>
 #include <vector>
@@ -28,15 +29,16 @@
 namespace moe {
 namespace rtc {
 
-constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
 
 struct Args {
   int T;
-  int Npad;     // experts padded to 32, 64, 128 or 256 (MMA N)
-  int nkb_d;    // k-blocks per copy of d
+  int Npad;     // experts padded to 32, 64, 128 or 256
+  int ntiles;   // N tiles of NT experts (Npad / NT)
+  int nkb_d;    // 64-wide k-blocks of d
   int kb_per;   // k-blocks per split
-  int nkb;      // 3 * nkb_d
+  int dp;       // d padded to 64: the column offset between the hi, mid and lo terms
   int S;        // splits
   uint32_t idesc;
   float *partial;  // [S][T][Npad]
@@ -73,22 +75,83 @@ __global__ void __launch_bounds__(256) split_wg_kernel(const float *__restrict__
 
 // The tensor core adds each MMA's products into its float32 accumulator with a
 // rounding that drifts by about one unit in the last place per MMA, always the
-// same way; over a K of several thousand that bias reaches 1e-4.  So the MMAs
-// of one k-block (K = 64, four MMAs) go into a fresh tensor-memory buffer and
-// the epilogue warps add that buffer into float32 registers (round to nearest)
-// while the MMAs of the next k-blocks fill the other buffers (up to eight in
-// rotation, so the MMAs are not held up by each buffer's round trip).
-template <int NP>
-__global__ void __launch_bounds__(64 + 32 * (NP > 128 ? 8 : 4), 1)
+// same way; over a K of several thousand that bias reaches 1e-4.  So the MMAs of
+// one k-block of the hi term (K = 64, four MMAs) go into a fresh tensor-memory
+// buffer, which the epilogue warps add into float32 registers (round to nearest)
+// while the next k-blocks fill the other buffers.  The mid and lo terms are 2^-8
+// and 2^-16 of the weights, so the same drift on their running sum is below
+// 2^-24 of the logit over any K here (at most 2 x 112 MMAs): they accumulate in
+// one buffer for the CTA's whole K range, drained once at the end.
+//
+// A stage holds one 64-wide k-block of x (128 tokens) and the same k-block of all
+// three weight terms for this CTA's NT experts, so x is read once per N tile.
+// MMAs per stage: 4 (hi, fresh buffer) + 8 (mid and lo, running buffer).
+template <int NT>
+struct RouterShape {
+  static constexpr int CPT = NT >= 64 ? 64 : 32;             // accumulator columns per epilogue thread
+  static constexpr int EW = 4 * (NT / CPT);                  // epilogue warps (4 lane quadrants)
+  static constexpr int THREADS = 64 + 32 * EW;
+  static constexpr int STAGES = NT == 32 ? 3 : (NT == 64 ? 4 : 3);
+  static constexpr int B_BYTES = NT * BK * 2;                // one term's k-block
+  static constexpr int STAGE_BYTES = A_BYTES + 3 * B_BYTES;
+  // two CTAs per SM (by shared memory) for NT = 32, one otherwise
+  static constexpr uint32_t TMEM_COLS = NT == 32 ? 256 : 512;
+  static constexpr int NBUF = (int)TMEM_COLS / NT - 1;       // hi buffers; the last NT columns hold mid + lo
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+};
+
+// 32 consecutive 32-bit TMEM columns of this thread's lane, waited for.
+MOE_DEV void tmem_ld32(uint32_t taddr, float *v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 64 columns with one wait.
+MOE_DEV void tmem_ld64(uint32_t taddr, float *v) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "r"(taddr + 32)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+template <int CPT>
+MOE_DEV void tmem_ld_cols(uint32_t taddr, float *v) {
+  if (CPT == 64)
+    tmem_ld64(taddr, v);
+  else
+    tmem_ld32(taddr, v);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(RouterShape<NT>::THREADS, 1)
     router_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
-  constexpr int EW = NP > 128 ? 8 : 4;          // epilogue warps
-  constexpr int COLS = NP / (EW / 4);           // accumulator columns per epilogue thread
-  constexpr int B_BYTES = NP * BK * 2;
-  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // tensor-memory buffers in rotation, sized so that the CTAs that fit on one SM
-  // by shared memory (two for NP <= 64, one above) share its 512 columns
-  constexpr int NBUF = NP == 32 ? 8 : (NP == 64 ? 4 : (NP == 128 ? 4 : 2));
-  constexpr uint32_t TMEM_COLS = NBUF * NP;
+  using Sh = RouterShape<NT>;
+  constexpr int CPT = Sh::CPT, EW = Sh::EW, STAGES = Sh::STAGES, NBUF = Sh::NBUF;
+  constexpr int B_BYTES = Sh::B_BYTES, STAGE_BYTES = Sh::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
@@ -96,12 +159,16 @@ __global__ void __launch_bounds__(64 + 32 * (NP > 128 ? 8 : 4), 1)
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + NBUF;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + NBUF);
+  uint64_t *mlfull = tempty + NBUF;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mlfull + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tile = blockIdx.x / a.S, split = blockIdx.x % a.S;
+  // blockIdx.x = (m_tile * ntiles + n_tile) * S + split
+  const int split = blockIdx.x % a.S;
+  const int mn = blockIdx.x / a.S;
+  const int n_tile = mn % a.ntiles, m_tile = mn / a.ntiles;
   const int kb0 = split * a.kb_per;
-  const int kb1 = min(kb0 + a.kb_per, a.nkb);
+  const int kb1 = min(kb0 + a.kb_per, a.nkb_d);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -112,17 +179,19 @@ __global__ void __launch_bounds__(64 + 32 * (NP > 128 ? 8 : 4), 1)
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], EW);
     }
+    mbar_init(mlfull, 1);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+  if (warp == 1) tmem_alloc(tmem_slot, Sh::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const uint32_t ml_col = (uint32_t)(NBUF * NT);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -130,12 +199,15 @@ __global__ void __launch_bounds__(64 + 32 * (NP > 128 ? 8 : 4), 1)
       for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
       int stage = 0;
       uint32_t phase = 0;
+      const int n0 = n_tile * NT;
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, a.status)) break;
         uint8_t *sa = smem + stage * STAGE_BYTES;
         mbar_arrive_expect_tx(&full[stage], (uint32_t)STAGE_BYTES);
-        tma_load_2d(sa, &tmA, &full[stage], (kb % a.nkb_d) * BK, m_tile * BM);
-        tma_load_2d(sa + A_BYTES, &tmB, &full[stage], kb * BK, 0);
+        tma_load_2d(sa, &tmA, &full[stage], kb * BK, m_tile * BM);
+#pragma unroll
+        for (int term = 0; term < 3; ++term)
+          tma_load_2d(sa + A_BYTES + term * B_BYTES, &tmB, &full[stage], term * a.dp + kb * BK, n0);
         issued_parity[stage] = (int)phase;
         if (++stage == STAGES) {
           stage = 0;
@@ -149,35 +221,48 @@ __global__ void __launch_bounds__(64 + 32 * (NP > 128 ? 8 : 4), 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      bool ok = true;
       for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
         const int b = it % NBUF;
         const uint32_t use = (uint32_t)(it / NBUF);
-        if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, a.status)) break;
-        if (!mbar_wait(&full[stage], phase, a.status)) break;
+        if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, a.status) || !mbar_wait(&full[stage], phase, a.status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
         const uint64_t adesc = smem_desc_sw128(sa);
-        const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
+        const uint64_t bhi = smem_desc_sw128(sa + A_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          tc_mma_bf16(tmem_base + (uint32_t)(b * NP), adesc + 2ull * kk, bdesc + 2ull * kk, a.idesc, kk > 0 ? 1u : 0u);
-        tc_commit(&empty[stage]);
+          tc_mma_bf16(tmem_base + (uint32_t)(b * NT), adesc + 2ull * kk, bhi + 2ull * kk, a.idesc, kk > 0 ? 1u : 0u);
         tc_commit(&tfull[b]);
+#pragma unroll
+        for (int term = 1; term < 3; ++term) {
+          const uint64_t bt = smem_desc_sw128(sa + A_BYTES + term * B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16(tmem_base + ml_col, adesc + 2ull * kk, bt + 2ull * kk, a.idesc,
+                        (it == 0 && term == 1 && kk == 0) ? 0u : 1u);
+        }
+        tc_commit(&empty[stage]);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
+      if (ok) tc_commit(mlfull);
     }
   } else {
     const int ew = warp - 2;
-    const int quad = warp & 3;
-    const int col0 = (ew / 4) * COLS;
+    const int quad = warp & 3;                  // TMEM lanes 32 quad .. 32 quad + 31
+    const int col0 = (ew / 4) * CPT;            // this thread's columns of the N tile
     const int r = quad * 32 + lane;
     const int t = m_tile * BM + r;
-    float acc[COLS];
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    float acc[CPT];
 #pragma unroll
-    for (int i = 0; i < COLS; ++i) acc[i] = 0.f;
+    for (int i = 0; i < CPT; ++i) acc[i] = 0.f;
     bool ok = true;
     for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
       const int b = it % NBUF;
@@ -187,31 +272,32 @@ __global__ void __launch_bounds__(64 + 32 * (NP > 128 ? 8 : 4), 1)
         break;
       }
       tc_fence_after();
-      const uint32_t taddr = tmem_base + (uint32_t)(b * NP + col0) + ((uint32_t)(quad * 32) << 16);
+      float v[CPT];
+      tmem_ld_cols<CPT>(tmem_base + (uint32_t)(b * NT + col0) + lane_off, v);
 #pragma unroll
-      for (int c = 0; c < COLS; c += 32) {
-        float v0[16], v1[16];
-        tmem_ld16x2(taddr + c, taddr + c + 16, v0, v1);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          acc[c + i] += v0[i];
-          acc[c + 16 + i] += v1[i];
-        }
-      }
+      for (int i = 0; i < CPT; ++i) acc[i] += v[i];
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[b]);
     }
-    if (ok && t < a.T) {
-      float4 *prow = reinterpret_cast<float4 *>(a.partial + ((size_t)split * a.T + t) * NP + col0);
+    if (ok && kb1 > kb0 && mbar_wait(mlfull, 0u, a.status)) {
+      tc_fence_after();
+      float v[CPT];
+      tmem_ld_cols<CPT>(tmem_base + ml_col + (uint32_t)col0 + lane_off, v);
+      if (t < a.T) {
+        float4 *prow = reinterpret_cast<float4 *>(a.partial + ((size_t)split * a.T + t) * a.Npad + n_tile * NT + col0);
 #pragma unroll
-      for (int q = 0; q < COLS / 4; ++q) prow[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+        for (int q = 0; q < CPT / 4; ++q)
+          prow[q] = make_float4(acc[4 * q] + v[4 * q], acc[4 * q + 1] + v[4 * q + 1], acc[4 * q + 2] + v[4 * q + 2],
+                                acc[4 * q + 3] + v[4 * q + 3]);
+      }
     }
   }
+  tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc(tmem_base, Sh::TMEM_COLS);
   }
 }
 
@@ -246,24 +332,26 @@ static int make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t co
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
-static size_t smem_bytes(int Npad) { return 1024 + (size_t)STAGES * (A_BYTES + Npad * BK * 2) + 256; }
-static int threads_for(int Npad) { return 64 + 32 * (Npad > 128 ? 8 : 4); }
+// N tile: every expert in one tile up to 128, two tiles of 128 for 256
+static int n_tile_width(int Npad) { return Npad > 128 ? 128 : Npad; }
+static int ctas_per_sm(int NT) { return NT == 32 ? 2 : 1; }
 
-template <int NP>
-static int launch_np(const CUtensorMap &ma, const CUtensorMap &mb, const Args &a, int grid, int dev, cudaStream_t s) {
+template <int NT>
+static int launch_nt(const CUtensorMap &ma, const CUtensorMap &mb, const Args &a, int grid, int dev, cudaStream_t s) {
+  using Sh = RouterShape<NT>;
   static std::mutex mu;
   static std::vector<int> done;
   {
     std::lock_guard<std::mutex> lk(mu);
     if ((int)done.size() <= dev) done.resize(dev + 1, 0);
     if (!done[dev]) {
-      if (cudaFuncSetAttribute(router_gemm_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem_bytes(NP)) != cudaSuccess)
+      if (cudaFuncSetAttribute(router_gemm_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM) !=
+          cudaSuccess)
         return MOE_ERR_CUDA;
       done[dev] = 1;
     }
   }
-  router_gemm_kernel<NP><<<grid, threads_for(NP), smem_bytes(NP), s>>>(ma, mb, a);
+  router_gemm_kernel<NT><<<grid, Sh::THREADS, Sh::SMEM, s>>>(ma, mb, a);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -274,16 +362,18 @@ int router_tc_dpad(int d) { return (d + 63) / 64 * 64; }
 // Largest split count the planner may choose (bounds the partial-sum scratch).
 int router_tc_max_splits(int T, int d) {
   const int mtiles = std::max(1, (T + 127) / 128);
-  const int nkb = 3 * (router_tc_dpad(d) / 64);
+  const int nkb = router_tc_dpad(d) / 64;
   return std::max(1, std::min(std::min(nkb, 64), 512 / mtiles));
 }
 
+// Split count with the fewest k-blocks on the busiest CTA slot: waves of CTAs
+// (CTAs per SM from shared memory) times k-blocks per CTA.
 static int plan_splits(int T, int d, int Npad, int sms) {
   const int mtiles = std::max(1, (T + 127) / 128);
-  const int nkb = 3 * (router_tc_dpad(d) / 64);
-  const size_t smem = rtc::smem_bytes(Npad);
-  const int per_sm = std::max(1, std::min(4, (int)((size_t)(227 * 1024) / smem)));
-  const long slots = (long)sms * per_sm;
+  const int NT = rtc::n_tile_width(Npad);
+  const int ntiles = Npad / NT;
+  const int nkb = router_tc_dpad(d) / 64;
+  const long slots = (long)sms * rtc::ctas_per_sm(NT);
   const int smax = router_tc_max_splits(T, d);
   int best = 1;
   long best_cost = -1;
@@ -291,7 +381,7 @@ static int plan_splits(int T, int d, int Npad, int sms) {
     const int kb_per = (nkb + S - 1) / S;
     const int S_eff = (nkb + kb_per - 1) / kb_per;
     if (S_eff != S) continue;  // every split non-empty
-    const long waves = ((long)mtiles * S + slots - 1) / slots;
+    const long waves = ((long)mtiles * ntiles * S + slots - 1) / slots;
     const long cost = waves * kb_per;
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
@@ -313,19 +403,19 @@ int launch_router_tc(const void *x, const float *Wg, int T, int d, int N, uint16
   const int sms = device_sm_count(dev);
   if (sms <= 0) return MOE_ERR_CUDA;
   const int S = plan_splits(T, d, Npad, sms);
-  const int nkb_d = dp / BK, nkb = 3 * nkb_d;
-  const int kb_per = (nkb + S - 1) / S;
+  const int NT = n_tile_width(Npad);
+  const int nkb_d = dp / BK;
+  const int kb_per = (nkb_d + S - 1) / S;
   CUtensorMap ma, mb;
   int rc;
   if ((rc = make_map(&ma, x, (uint64_t)T, (uint64_t)d, BM))) return rc;
-  if ((rc = make_map(&mb, wsplit, (uint64_t)Npad, (uint64_t)(3 * dp), (uint32_t)Npad))) return rc;
-  Args a{T, Npad, nkb_d, kb_per, nkb, S, idesc_bf16_f32(BM, Npad), partial, status};
-  const int grid = ((T + BM - 1) / BM) * S;
-  switch (Npad) {
-    case 32: rc = launch_np<32>(ma, mb, a, grid, dev, s); break;
-    case 64: rc = launch_np<64>(ma, mb, a, grid, dev, s); break;
-    case 128: rc = launch_np<128>(ma, mb, a, grid, dev, s); break;
-    default: rc = launch_np<256>(ma, mb, a, grid, dev, s); break;
+  if ((rc = make_map(&mb, wsplit, (uint64_t)Npad, (uint64_t)(3 * dp), (uint32_t)NT))) return rc;
+  Args a{T, Npad, Npad / NT, nkb_d, kb_per, dp, S, idesc_bf16_f32(BM, NT), partial, status};
+  const int grid = ((T + BM - 1) / BM) * (Npad / NT) * S;
+  switch (NT) {
+    case 32: rc = launch_nt<32>(ma, mb, a, grid, dev, s); break;
+    case 64: rc = launch_nt<64>(ma, mb, a, grid, dev, s); break;
+    default: rc = launch_nt<128>(ma, mb, a, grid, dev, s); break;
   }
   if (rc) return rc;
   *splits_out = S;
