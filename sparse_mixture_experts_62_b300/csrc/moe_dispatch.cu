@@ -60,35 +60,59 @@ __global__ void __launch_bounds__(CH) dispatch_hist_kernel(const int32_t *__rest
   for (int e = threadIdx.x; e < N; e += CH) hist[(size_t)blockIdx.x * N + e] = cnt[e];
 }
 
-// One CTA of 256 threads; thread e owns expert e.
-__global__ void __launch_bounds__(256) dispatch_scan_kernel(const int32_t *__restrict__ hist, int nchunks, int N,
-                                                            int capacity, int32_t *__restrict__ chunk_base,
-                                                            int32_t *__restrict__ counts_routed,
-                                                            int32_t *__restrict__ counts_kept,
-                                                            int32_t *__restrict__ offsets) {
+// One CTA of 1024 threads: G = 1024 / 256 = 4 (or, for N <= 128, 1024 / N rounded
+// down to a power of two, at most 32) adjacent threads per expert, each owning a
+// contiguous range of chunks.  Per expert: range sums, an exclusive scan of them
+// across the G threads (shuffles), then each chunk's starting rank; then the
+// capacity and the exclusive scan of the kept counts over the experts.
+constexpr int SCAN_THREADS = 1024;
+__global__ void __launch_bounds__(SCAN_THREADS) dispatch_scan_kernel(const int32_t *__restrict__ hist, int nchunks,
+                                                                     int N, int G, int capacity,
+                                                                     int32_t *__restrict__ chunk_base,
+                                                                     int32_t *__restrict__ counts_routed,
+                                                                     int32_t *__restrict__ counts_kept,
+                                                                     int32_t *__restrict__ offsets) {
   __shared__ int kept_s[256];
-  const int e = threadIdx.x;
-  int run = 0;
+  const int e = threadIdx.x / G, g = threadIdx.x % G;
+  const int per = (nchunks + G - 1) / G;
+  const int c0 = min(nchunks, g * per), c1 = min(nchunks, c0 + per);
+  int sum = 0;
+  if (e < N)
+    for (int c = c0; c < c1; ++c) sum += hist[(size_t)c * N + e];
+  // exclusive scan of the range sums across the expert's G threads (adjacent lanes)
+  int incl = sum;
+  for (int off = 1; off < G; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off, G);
+    if (g >= off) incl += v;
+  }
+  const int total = __shfl_sync(0xffffffffu, incl, G - 1, G);
   if (e < N) {
-    for (int c = 0; c < nchunks; ++c) {
+    int run = incl - sum;
+    for (int c = c0; c < c1; ++c) {
       chunk_base[(size_t)c * N + e] = run;
       run += hist[(size_t)c * N + e];
     }
-    counts_routed[e] = run;
   }
-  const int kept = (e < N) ? (capacity > 0 ? min(run, capacity) : run) : 0;
-  if (e < N) counts_kept[e] = kept;
-  kept_s[e] = kept;
+  if (threadIdx.x < 256) kept_s[threadIdx.x] = 0;
   __syncthreads();
-  // exclusive scan of kept over experts (Hillis-Steele in shared memory)
+  if (e < N && g == 0) {
+    counts_routed[e] = total;
+    const int kept = capacity > 0 ? min(total, capacity) : total;
+    counts_kept[e] = kept;
+    kept_s[e] = kept;
+  }
+  __syncthreads();
+  // exclusive scan of kept over experts (Hillis-Steele in shared memory, 256 threads)
+  const int t = threadIdx.x;
+  const int mine = t < 256 ? kept_s[t] : 0;
   for (int off = 1; off < 256; off <<= 1) {
-    const int v = (e >= off) ? kept_s[e - off] : 0;
+    const int v = (t < 256 && t >= off) ? kept_s[t - off] : 0;
     __syncthreads();
-    kept_s[e] += v;
+    if (t < 256) kept_s[t] += v;
     __syncthreads();
   }
-  if (e < N) offsets[e] = kept_s[e] - kept;
-  if (e == N - 1) offsets[N] = kept_s[e];
+  if (t < N) offsets[t] = kept_s[t] - mine;
+  if (t == N - 1) offsets[N] = kept_s[t];
 }
 
 __global__ void __launch_bounds__(CH) dispatch_rank_kernel(const int32_t *__restrict__ idx, int T, int k, int N,
@@ -203,7 +227,10 @@ int launch_dispatch(const int32_t *idx, int T, int k, int N, int capacity, int32
                     int32_t *src_token, int *status, cudaStream_t s) {
   const int nchunks = (T + CH - 1) / CH;
   if (nchunks > 0) dispatch_hist_kernel<<<nchunks, CH, 0, s>>>(idx, T, k, N, hist, status);
-  dispatch_scan_kernel<<<1, 256, 0, s>>>(hist, nchunks, N, capacity, chunk_base, counts_routed, counts_kept, offsets);
+  int G = 4;  // threads per expert: a power of two, G * 256 <= 1024 for N <= 256
+  while (G < 32 && 2 * G * N <= SCAN_THREADS) G *= 2;
+  dispatch_scan_kernel<<<1, SCAN_THREADS, 0, s>>>(hist, nchunks, N, G, capacity, chunk_base, counts_routed,
+                                                  counts_kept, offsets);
   if (nchunks > 0)
     dispatch_rank_kernel<<<nchunks, CH, 0, s>>>(idx, T, k, N, capacity, chunk_base, offsets, dest_row, src_token);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

@@ -151,12 +151,13 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t >= T) return;
-  const float *zr = logits + (size_t)t * N;
+  float zl[NV];  // this lane's logits, kept in registers
   float sel[NV];
   bool bad = false;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
+    zl[i] = -INFINITY;
     if (e < N) {
       // four independent running sums over the splits, combined in a fixed order
       const float *p = partial + (size_t)t * pstride + e;
@@ -173,15 +174,15 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, 
       float z = (z0 + z1) + (z2 + z3);
       if (logit_bias) z += logit_bias[e];
       logits[(size_t)t * N + e] = z;
+      zl[i] = z;
     }
   }
-  __syncwarp();
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
     sel[i] = -INFINITY;
     if (e < N) {
-      const float z = zr[e];
+      const float z = zl[i];
       if (!isfinite(z)) bad = true;
       float s = z;
       if (gate == MOE_GATE_SIGMOID_BIAS) {
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, 
         const int e = lane + 32 * i;
         if (e >= N) continue;
         if (sel[i] >= vk - kSelMargin) {
-          float se = sigmoid_f32(zr[e]);
+          float se = sigmoid_f32(zl[i]);
           if (sel_bias) se = se + sel_bias[e];
           key[i] = order_key(se);
         } else {
@@ -248,25 +249,34 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, 
     for (int j = 0; j < 8; ++j)
       if (j < k) chosen[j] = warp_select(key, taken, lane, &kmax);
   }
+  // the chosen experts' logits, from the lanes that hold them: lane j < k gets slot j's
+  float zj = 0.f, m = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < k) {
+      const int e = chosen[j];
+      float mine = zl[0];
+#pragma unroll
+      for (int i = 1; i < NV; ++i)
+        if ((e >> 5) == i) mine = zl[i];
+      const float ze = __shfl_sync(0xffffffffu, mine, e & 31);
+      if (lane == j) zj = ze;
+      if (j == 0) m = ze;  // the first pick has the largest logit (softmax gates)
+    }
+  }
   // full-softmax gate: the normaliser over all N experts (warp sum, fixed order)
   float full_den = 0.f;
   if (gate == MOE_GATE_SOFTMAX_FULL) {
-    const float m = zr[chosen[0]];  // the largest logit
 #pragma unroll
     for (int i = 0; i < NV; ++i)
-      if (lane + 32 * i < N) full_den += expf(zr[lane + 32 * i] - m);
+      if (lane + 32 * i < N) full_den += expf(zl[i] - m);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) full_den += __shfl_xor_sync(0xffffffffu, full_den, off);
   }
   // gate weights of the selected experts, in float32: lane j < k takes slot j;
   // the normaliser is a warp sum in a fixed order
-  float zj = 0.f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j)
-    if (j < k && lane == j) zj = zr[chosen[j]];
   float g = 0.f;
   if (gate == MOE_GATE_SOFTMAX_TOPK || gate == MOE_GATE_SOFTMAX_FULL) {
-    const float m = zr[chosen[0]];  // the first pick has the largest logit
     if (lane < k) g = expf(zj - m);
   } else if (lane < k) {
     g = 1.0f / (1.0f + expf(-zj));  // float32 affinity (within 3e-7 relative of the rounded exact one)
