@@ -36,6 +36,15 @@
 //               16-byte stores masked to the group's rows and the output width.
 // Tiles are enumerated group by group, n-tile-major within a group, so the
 // CTAs of one wave share each weight tile through L2.
+//
+// Small groups (forward modes, single-CTA form): a group of at most 128 rows
+// pays a whole 128-row MMA per tile however few its rows.  Its tiles run with the
+// operands swapped instead: the two 128-row halves of the stage's weight tile are
+// each the MMA's M side and the group's rows, padded to a multiple of 16, its N
+// side (D1, D2 = 128 weight rows x N_t in tensor memory), so the MMA work shrinks
+// to N_t / 128 of a tile while the same bytes stream through the same ring.  The
+// epilogue thread of weight row f writes output column f of every row of the
+// group (32 consecutive columns per warp store).
 #include <mutex>
 #include <vector>
 
@@ -61,6 +70,9 @@ constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
 enum Mode { kSwiGLU = 0, kReLU = 1, kPlain = 2, kPlainBT = 3, kDualBT = 4, kSwiGLUBwd = 5, kReLUBwd = 6 };
+// groups of at most this many rows run swapped tiles (forward modes, single-CTA form)
+constexpr int SWAP_ROWS = 128;
+__host__ __device__ constexpr bool swappable(int mode) { return mode == kSwiGLU || mode == kReLU || mode == kPlain; }
 // modes whose tile pairs W1 and W3 rows (128 output columns per tile)
 __host__ __device__ constexpr bool paired_b(int mode) { return mode == kSwiGLU || mode == kSwiGLUBwd; }
 constexpr uint32_t IDESC_BT = idesc_bf16_f32_major(BM, BN, false, true);
@@ -161,6 +173,37 @@ __device__ __forceinline__ void epilogue_row(uint32_t taddr, const Args &args, i
         }
         *reinterpret_cast<uint4 *>(orow + col) =
             make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+      }
+    }
+  }
+}
+
+// Epilogue of a swapped tile: this thread's TMEM lane is weight row f of the
+// tile (f = quad * 32 + lane); D1 in columns [0, nt), D2 in [nt, 2 nt), one
+// column per row of the group.  SwiGLU: out[row0 + j, n0 + f] = SiLU(D1) * D2;
+// ReLU / plain: out[row0 + j, n0 + f] = act(D1), out[row0 + j, n0 + 128 + f] = act(D2).
+template <int MODE>
+__device__ __forceinline__ void epilogue_swapped(uint32_t taddr, const Args &args, int row0, int rows, int nt,
+                                                 int n0, int f) {
+  const int c1 = n0 + f, c2 = n0 + 128 + f;
+  const bool ok1 = c1 < args.n_out;
+  const bool ok2 = MODE != kSwiGLU && c2 < args.n_out;
+#pragma unroll 1
+  for (int c = 0; c < nt; c += 16) {
+    float a[16], u[16];
+    tmem_ld16x2(taddr + c, taddr + nt + c, a, u);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int j = c + i;
+      if (j >= rows) break;
+      uint16_t *orow = args.out + (size_t)(row0 + j) * args.out_stride;
+      if (MODE == kSwiGLU) {
+        if (ok1) orow[c1] = (uint16_t)(pack_bf16x2(silu(a[i]) * u[i], 0.f) & 0xFFFFu);
+      } else {
+        const float v1 = MODE == kReLU ? fmaxf(a[i], 0.f) : a[i];
+        const float v2 = MODE == kReLU ? fmaxf(u[i], 0.f) : u[i];
+        if (ok1) orow[c1] = (uint16_t)(pack_bf16x2(v1, 0.f) & 0xFFFFu);
+        if (ok2) orow[c2] = (uint16_t)(pack_bf16x2(v2, 0.f) & 0xFFFFu);
       }
     }
   }
@@ -291,7 +334,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
+      int g = 0;
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
+        while (tile >= tile_start[g + 1]) ++g;
+        const int grows = rowend[g] - rowbeg[g];
+        const bool swapped = swappable(MODE) && grows <= SWAP_ROWS;
+        const int nt = (grows + 15) & ~15;  // N of the swapped MMAs
+        const uint32_t idesc_sw = idesc_bf16_f32(BM, nt > 0 ? nt : 16);
         const int acc = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
         if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, args.status)) break;
@@ -305,7 +354,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint64_t adesc = smem_desc_sw128(sa);
-          if (MODE == kPlainBT || MODE == kDualBT) {
+          if (swappable(MODE) && swapped) {
+            // weight halves as M (128 rows each), the group's rows as N
+            const uint64_t w1 = smem_desc_sw128(sa + A_BYTES);
+            const uint64_t w2 = smem_desc_sw128(sa + A_BYTES + B_BYTES / 2);
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              tc_mma_bf16(d_tmem, w1 + 2ull * kk, adesc + 2ull * kk, idesc_sw, (kb | kk) != 0);
+              tc_mma_bf16(d_tmem + (uint32_t)nt, w2 + 2ull * kk, adesc + 2ull * kk, idesc_sw, (kb | kk) != 0);
+            }
+          } else if (MODE == kPlainBT || MODE == kDualBT) {
             const uint64_t bdesc = smem_desc_sw128_mn(sa + A_BYTES, B_SLICE);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)  // A: +32 B along K; B: +16 rows = +2048 B
@@ -346,7 +404,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(&tfull[acc], use & 1u, args.status)) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(quad * 32) << 16);
-      epilogue_row<MODE>(taddr, args, row0 + r, r < rows_valid, n0);
+      const int grows = rowend[g] - rowbeg[g];
+      if (swappable(MODE) && grows <= SWAP_ROWS)
+        epilogue_swapped<MODE>(taddr, args, row0, grows, (grows + 15) & ~15, n0, r);
+      else
+        epilogue_row<MODE>(taddr, args, row0 + r, r < rows_valid, n0);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);

@@ -40,7 +40,8 @@ struct Args {
   int kb_per;   // k-blocks per split
   int dp;       // d padded to 64: the column offset between the hi, mid and lo terms
   int S;        // splits
-  uint32_t idesc;
+  uint32_t idesc;   // M = 128, N = NT
+  uint32_t idesc2;  // M = 128, N = 2 NT
   float *partial;  // [S][T][Npad]
   int *status;
 };
@@ -79,32 +80,29 @@ __global__ void __launch_bounds__(256) split_wg_kernel(const float *__restrict__
 // one k-block of the hi term (K = 64, four MMAs) go into a fresh tensor-memory
 // buffer, which the epilogue warps add into float32 registers (round to nearest)
 // while the next k-blocks fill the other buffers.  The mid and lo terms are 2^-8
-// and 2^-16 of the weights, so the same drift on their running sum is below
-// 2^-24 of the logit over any K here (at most 2 x 112 MMAs): they accumulate in
-// one buffer for the CTA's whole K range, drained once at the end.
+// and 2^-16 of the weights, so the same drift on their running sums is below
+// 2^-24 of the logit over any K here (at most 4 x 112 MMAs): they accumulate in
+// a running buffer (mid and lo side by side) for the CTA's whole K range,
+// drained once at the end.
 //
-// Two rings feed the MMAs: x tiles (one 64-wide k-block of 128 tokens, 16 KB)
-// stream from DRAM and get a deep ring; the three weight terms of the same
-// k-block for this CTA's NT experts (L2-resident after the first tile) get a
-// short one.  Each has its own producer warp, so the x loads run as far ahead as
-// their ring allows.  x is read once per N tile.  MMAs per k-block: 4 (hi, fresh
-// buffer) + 8 (mid and lo, running buffer).
+// A stage holds one 64-wide k-block of x (128 tokens) and the same k-block of all
+// three weight terms for this CTA's NT experts, so x is read once per N tile.
+// The mid and lo tiles sit back to back and form one 2 NT-row operand.  MMAs per
+// stage: 4 with N = NT (hi, fresh buffer) + 4 with N = 2 NT (mid and lo side by
+// side in the running buffer): each MMA re-reads the x tile from shared memory,
+// so fewer, wider MMAs move fewer shared-memory bytes per k-block.
 template <int NT>
 struct RouterShape {
   static constexpr int CPT = NT >= 64 ? 64 : 32;             // accumulator columns per epilogue thread
   static constexpr int EW = 4 * (NT / CPT);                  // epilogue warps (4 lane quadrants)
-  static constexpr int THREADS = 96 + 32 * EW;               // x producer, MMA, weight producer, epilogue
+  static constexpr int THREADS = 64 + 32 * EW;
+  static constexpr int STAGES = NT == 32 ? 3 : (NT == 64 ? 4 : 3);
   static constexpr int B_BYTES = NT * BK * 2;                // one term's k-block
-  static constexpr int BSTAGE_BYTES = 3 * B_BYTES;
-  static constexpr int ASTAGES = NT == 32 ? 4 : (NT == 64 ? 8 : 6);
-  static constexpr int BSTAGES = NT == 32 ? 3 : (NT == 64 ? 3 : 2);
+  static constexpr int STAGE_BYTES = A_BYTES + 3 * B_BYTES;
   // two CTAs per SM (by shared memory) for NT = 32, one otherwise
   static constexpr uint32_t TMEM_COLS = NT == 32 ? 256 : 512;
-  static constexpr int NBUF = (int)TMEM_COLS / NT - 1;       // hi buffers; the last NT columns hold mid + lo
-  // + alignment slack + barriers (2 ASTAGES + 2 BSTAGES + 2 NBUF + 1, at most 37) and the TMEM address
-  static constexpr size_t SMEM = 1024 + (size_t)ASTAGES * A_BYTES + (size_t)BSTAGES * BSTAGE_BYTES + 512;
-  static_assert((2 * ASTAGES + 2 * BSTAGES + 2 * NBUF + 1) * 8 + 4 <= 512, "barrier area");
-  static_assert(SMEM <= 227 * 1024, "shared memory");
+  static constexpr int NBUF = (int)TMEM_COLS / NT - 2;       // hi buffers; the last 2 NT columns hold mid, lo
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
 };
 
 // 32 consecutive 32-bit TMEM columns of this thread's lane, waited for.
@@ -157,18 +155,14 @@ template <int NT>
 __global__ void __launch_bounds__(RouterShape<NT>::THREADS, 1)
     router_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args a) {
   using Sh = RouterShape<NT>;
-  constexpr int CPT = Sh::CPT, EW = Sh::EW, ASTAGES = Sh::ASTAGES, BSTAGES = Sh::BSTAGES, NBUF = Sh::NBUF;
-  constexpr int B_BYTES = Sh::B_BYTES, BSTAGE_BYTES = Sh::BSTAGE_BYTES;
+  constexpr int CPT = Sh::CPT, EW = Sh::EW, STAGES = Sh::STAGES, NBUF = Sh::NBUF;
+  constexpr int B_BYTES = Sh::B_BYTES, STAGE_BYTES = Sh::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
-  uint8_t *sA = smem;                                      // [ASTAGES][A_BYTES]
-  uint8_t *sB = smem + ASTAGES * A_BYTES;                  // [BSTAGES][3 terms][B_BYTES]
-  uint64_t *afull = reinterpret_cast<uint64_t *>(sB + BSTAGES * BSTAGE_BYTES);
-  uint64_t *aempty = afull + ASTAGES;
-  uint64_t *bfull = aempty + ASTAGES;
-  uint64_t *bempty = bfull + BSTAGES;
-  uint64_t *tfull = bempty + BSTAGES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + NBUF;
   uint64_t *mlfull = tempty + NBUF;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mlfull + 1);
@@ -182,13 +176,9 @@ __global__ void __launch_bounds__(RouterShape<NT>::THREADS, 1)
   const int kb1 = min(kb0 + a.kb_per, a.nkb_d);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < ASTAGES; ++s) {
-      mbar_init(&afull[s], 1);
-      mbar_init(&aempty[s], 1);
-    }
-    for (int s = 0; s < BSTAGES; ++s) {
-      mbar_init(&bfull[s], 1);
-      mbar_init(&bempty[s], 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < NBUF; ++b) {
       mbar_init(&tfull[b], 1);
@@ -197,8 +187,10 @@ __global__ void __launch_bounds__(RouterShape<NT>::THREADS, 1)
     mbar_init(mlfull, 1);
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tmA);
-  if (warp == 2 && lane == 0) tma_prefetch_desc(&tmB);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
   if (warp == 1) tmem_alloc(tmem_slot, Sh::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -206,85 +198,65 @@ __global__ void __launch_bounds__(RouterShape<NT>::THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t ml_col = (uint32_t)(NBUF * NT);
 
-  if (warp == 0 || warp == 2) {
-    // ------------------------------------------------ producers: x (warp 0), weight terms (warp 2)
+  if (warp == 0) {
     if (lane == 0) {
-      const bool is_a = warp == 0;
-      const int NS = is_a ? ASTAGES : BSTAGES;
-      uint64_t *fullb = is_a ? afull : bfull;
-      uint64_t *emptyb = is_a ? aempty : bempty;
-      int issued_parity[8];
-      for (int s = 0; s < 8; ++s) issued_parity[s] = -1;
+      int issued_parity[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
       int stage = 0;
       uint32_t phase = 0;
       const int n0 = n_tile * NT;
       for (int kb = kb0; kb < kb1; ++kb) {
-        if (!mbar_wait(&emptyb[stage], phase ^ 1u, a.status)) break;
-        if (is_a) {
-          mbar_arrive_expect_tx(&fullb[stage], (uint32_t)A_BYTES);
-          tma_load_2d(sA + stage * A_BYTES, &tmA, &fullb[stage], kb * BK, m_tile * BM);
-        } else {
-          mbar_arrive_expect_tx(&fullb[stage], (uint32_t)BSTAGE_BYTES);
+        if (!mbar_wait(&empty[stage], phase ^ 1u, a.status)) break;
+        uint8_t *sa = smem + stage * STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[stage], (uint32_t)STAGE_BYTES);
+        tma_load_2d(sa, &tmA, &full[stage], kb * BK, m_tile * BM);
 #pragma unroll
-          for (int term = 0; term < 3; ++term)
-            tma_load_2d(sB + stage * BSTAGE_BYTES + term * B_BYTES, &tmB, &fullb[stage], term * a.dp + kb * BK, n0);
-        }
+        for (int term = 0; term < 3; ++term)
+          tma_load_2d(sa + A_BYTES + term * B_BYTES, &tmB, &full[stage], term * a.dp + kb * BK, n0);
         issued_parity[stage] = (int)phase;
-        if (++stage == NS) {
+        if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      // never leave the CTA with a bulk copy still writing its shared memory
-      for (int s = 0; s < NS; ++s)
-        if (issued_parity[s] >= 0) mbar_wait(&fullb[s], (uint32_t)issued_parity[s], a.status);
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_parity[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_parity[s], a.status);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int as = 0, bs = 0;
-      uint32_t aph = 0, bph = 0;
+      int stage = 0;
+      uint32_t phase = 0;
       bool ok = true;
       for (int kb = kb0, it = 0; kb < kb1; ++kb, ++it) {
         const int b = it % NBUF;
         const uint32_t use = (uint32_t)(it / NBUF);
-        if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, a.status) || !mbar_wait(&afull[as], aph, a.status) ||
-            !mbar_wait(&bfull[bs], bph, a.status)) {
+        if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, a.status) || !mbar_wait(&full[stage], phase, a.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t adesc = smem_desc_sw128(smem_u32(sA + as * A_BYTES));
-        const uint32_t sb = smem_u32(sB + bs * BSTAGE_BYTES);
-        const uint64_t bhi = smem_desc_sw128(sb);
+        const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+        const uint64_t adesc = smem_desc_sw128(sa);
+        const uint64_t bhi = smem_desc_sw128(sa + A_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           tc_mma_bf16(tmem_base + (uint32_t)(b * NT), adesc + 2ull * kk, bhi + 2ull * kk, a.idesc, kk > 0 ? 1u : 0u);
         tc_commit(&tfull[b]);
+        const uint64_t bml = smem_desc_sw128(sa + A_BYTES + B_BYTES);  // [mid; lo], 2 NT rows
 #pragma unroll
-        for (int term = 1; term < 3; ++term) {
-          const uint64_t bt = smem_desc_sw128(sb + term * B_BYTES);
-#pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk)
-            tc_mma_bf16(tmem_base + ml_col, adesc + 2ull * kk, bt + 2ull * kk, a.idesc,
-                        (it == 0 && term == 1 && kk == 0) ? 0u : 1u);
-        }
-        tc_commit(&aempty[as]);
-        tc_commit(&bempty[bs]);
-        if (++as == ASTAGES) {
-          as = 0;
-          aph ^= 1u;
-        }
-        if (++bs == BSTAGES) {
-          bs = 0;
-          bph ^= 1u;
+        for (int kk = 0; kk < BK / 16; ++kk)
+          tc_mma_bf16(tmem_base + ml_col, adesc + 2ull * kk, bml + 2ull * kk, a.idesc2,
+                      (it == 0 && kk == 0) ? 0u : 1u);
+        tc_commit(&empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
       if (ok) tc_commit(mlfull);
     }
   } else {
-    // ------------------------------------------------ epilogue
-    const int ew = warp - 3;
+    const int ew = warp - 2;
     const int quad = warp & 3;                  // TMEM lanes 32 quad .. 32 quad + 31
     const int col0 = (ew / 4) * CPT;            // this thread's columns of the N tile
     const int r = quad * 32 + lane;
@@ -313,7 +285,10 @@ __global__ void __launch_bounds__(RouterShape<NT>::THREADS, 1)
     if (ok && kb1 > kb0 && mbar_wait(mlfull, 0u, a.status)) {
       tc_fence_after();
       float v[CPT];
-      tmem_ld_cols<CPT>(tmem_base + ml_col + (uint32_t)col0 + lane_off, v);
+      tmem_ld_cols<CPT>(tmem_base + ml_col + (uint32_t)col0 + lane_off, v);  // mid
+#pragma unroll
+      for (int i = 0; i < CPT; ++i) acc[i] += v[i];
+      tmem_ld_cols<CPT>(tmem_base + ml_col + (uint32_t)(NT + col0) + lane_off, v);  // lo
       if (t < a.T) {
         float4 *prow = reinterpret_cast<float4 *>(a.partial + ((size_t)split * a.T + t) * a.Npad + n_tile * NT + col0);
 #pragma unroll
@@ -440,7 +415,7 @@ int launch_router_tc(const void *x, const float *Wg, int T, int d, int N, uint16
   int rc;
   if ((rc = make_map(&ma, x, (uint64_t)T, (uint64_t)d, BM))) return rc;
   if ((rc = make_map(&mb, wsplit, (uint64_t)Npad, (uint64_t)(3 * dp), (uint32_t)NT))) return rc;
-  Args a{T, Npad, Npad / NT, nkb_d, kb_per, dp, S, idesc_bf16_f32(BM, NT), partial, status};
+  Args a{T, Npad, Npad / NT, nkb_d, kb_per, dp, S, idesc_bf16_f32(BM, NT), idesc_bf16_f32(BM, 2 * NT), partial, status};
   const int grid = ((T + BM - 1) / BM) * (Npad / NT) * S;
   switch (NT) {
     case 32: rc = launch_nt<32>(ma, mb, a, grid, dev, s); break;
