@@ -124,15 +124,6 @@ MOE_DEV void tma_load_3d(void *smem_dst, const CUtensorMap *m, uint64_t *bar, in
       : "memory");
 }
 
-// Bulk prefetch of a 2-D tile into L2 (no shared memory, no barrier): the tile a
-// later tma_load_2d of the same coordinates will read, fetched from DRAM ahead of
-// time so that the load finds it in L2.
-MOE_DEV void tma_prefetch_l2_2d(const CUtensorMap *m, int32_t c0, int32_t c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(m)),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor for a K-major operand tile stored in the
 // 128-byte swizzled layout that TMA writes with CU_TENSOR_MAP_SWIZZLE_128B:

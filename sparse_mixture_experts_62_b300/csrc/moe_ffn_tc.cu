@@ -70,9 +70,6 @@ constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
 enum Mode { kSwiGLU = 0, kReLU = 1, kPlain = 2, kPlainBT = 3, kDualBT = 4, kSwiGLUBwd = 5, kReLUBwd = 6 };
-// forward modes: the producer prefetches A and B tiles into L2 this many k-blocks
-// ahead of its loads (past the ring's depth), so that DRAM latency hides behind L2
-constexpr int PREFETCH_KB = 8;
 // groups of at most this many rows run swapped tiles (forward modes, single-CTA form)
 constexpr int SWAP_ROWS = 128;
 __host__ __device__ constexpr bool swappable(int mode) { return mode == kSwiGLU || mode == kReLU || mode == kPlain; }
@@ -287,28 +284,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int g = 0;
       bool ok = true;
-      // L2 prefetch cursor, PREFETCH_KB k-blocks ahead of the loads (forward modes)
-      int pf_tile = blockIdx.x, pf_kb = 0, pf_g = 0;
-      auto prefetch_next = [&]() {
-        if constexpr (swappable(MODE)) {
-          if (pf_tile >= total_tiles) return;
-          while (pf_tile >= tile_start[pf_g + 1]) ++pf_g;
-          const int pl = pf_tile - tile_start[pf_g];
-          const int pn = pl / mtiles[pf_g], pm = pl - pn * mtiles[pf_g];
-          const int pb = pf_g * args.b_rows + pn * OUT_COLS;
-          tma_prefetch_l2_2d(&tmA, pf_kb * BK, rowbeg[pf_g] + pm * BM);
-          tma_prefetch_l2_2d(&tmB0, pf_kb * BK, pb);
-          if (paired_b(MODE))
-            tma_prefetch_l2_2d(&tmB1, pf_kb * BK, pb);
-          else
-            tma_prefetch_l2_2d(&tmB0, pf_kb * BK, pb + BN / 2);
-          if (++pf_kb == num_kb) {
-            pf_kb = 0;
-            pf_tile += gridDim.x;
-          }
-        }
-      };
-      for (int i = 0; i < PREFETCH_KB; ++i) prefetch_next();
       for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
         while (tile >= tile_start[g + 1]) ++g;
         const int local = tile - tile_start[g];
@@ -321,7 +296,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          prefetch_next();
           uint8_t *sa = smem + stage * STAGE_BYTES;
           uint8_t *sb = sa + A_BYTES;
           mbar_arrive_expect_tx(&full[stage], STAGE_TX);
@@ -555,25 +529,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       int g = 0;
       bool ok = true;
       const CUtensorMap *mb = (paired_b(MODE) && rank == 1) ? &tmB1 : &tmB0;
-      // L2 prefetch cursor, PREFETCH_KB k-blocks ahead of this CTA's loads (forward modes)
-      int pf_tile = pair_id, pf_kb = 0, pf_g = 0;
-      auto prefetch_next = [&]() {
-        if constexpr (swappable(MODE)) {
-          if (pf_tile >= total_tiles) return;
-          while (pf_tile >= tile_start[pf_g + 1]) ++pf_g;
-          const int pl = pf_tile - tile_start[pf_g];
-          const int pn = pl / mtiles[pf_g], pm = pl - pn * mtiles[pf_g];
-          const int pb = paired_b(MODE) ? pf_g * args.b_rows + pn * OUT_COLS
-                                        : pf_g * args.b_rows + pn * OUT_COLS + (int)rank * 128;
-          tma_prefetch_l2_2d(&tmA, pf_kb * BK, rowbeg[pf_g] + pm * 2 * BM + (int)rank * BM);
-          tma_prefetch_l2_2d(mb, pf_kb * BK, pb);
-          if (++pf_kb == num_kb) {
-            pf_kb = 0;
-            pf_tile += npairs;
-          }
-        }
-      };
-      for (int i = 0; i < PREFETCH_KB; ++i) prefetch_next();
       for (int tile = pair_id; tile < total_tiles && ok; tile += npairs) {
         while (tile >= tile_start[g + 1]) ++g;
         const int local = tile - tile_start[g];
@@ -587,7 +542,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          prefetch_next();
           uint8_t *sa = smem + stage * STAGE_BYTES;
           if (leader) mbar_arrive_expect_tx(&full[stage], 2u * STAGE_BYTES);
           const uint32_t fb = full_lead + 8u * stage;
