@@ -57,22 +57,16 @@ namespace tc {
 constexpr int BM = 128;              // rows per tile (TMEM lanes)
 constexpr int BN = 256;              // accumulator columns per tile
 constexpr int BK = 64;               // K per stage: 64 bf16 = one 128-byte swizzle row
-// Single-CTA form: the A tiles (token rows, mostly L2 hits) and the B tiles
-// (weight rows, streamed from DRAM) have rings of their own, so that more weight
-// bytes are in flight than one ring of {A, B} stages allows in shared memory.
-constexpr int A_STAGES = 3;
-constexpr int B_STAGES = 5;
-constexpr int A_LAG = B_STAGES - A_STAGES;      // A loads trail B loads by this many k-blocks
+constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB
 constexpr int B_BYTES = BN * BK * 2;            // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 48 KB
+constexpr uint32_t STAGE_TX = STAGE_BYTES;
 constexpr int MAX_GROUPS = 257;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;  // two 256-column accumulators
-constexpr size_t RING_BYTES = (size_t)A_STAGES * A_BYTES + (size_t)B_STAGES * B_BYTES;
-constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + RING_BYTES + 256 /*barriers*/ +
+constexpr size_t SMEM_BYTES = 1024 /*alignment slack*/ + (size_t)STAGES * STAGE_BYTES + 256 /*barriers*/ +
                               (size_t)(4 * MAX_GROUPS + 8) * 4;
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-static_assert((2 * A_STAGES + 2 * B_STAGES + 4) * 8 + 4 <= 256, "barrier area");
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
 enum Mode { kSwiGLU = 0, kReLU = 1, kPlain = 2, kPlainBT = 3, kDualBT = 4, kSwiGLUBwd = 5, kReLUBwd = 6 };
@@ -225,16 +219,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   // 1024-byte alignment for the swizzled operand tiles
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
-  uint8_t *sA = smem;                          // [A_STAGES][A_BYTES]
-  uint8_t *sB = smem + A_STAGES * A_BYTES;     // [B_STAGES][B_BYTES]
-  uint64_t *fullA = reinterpret_cast<uint64_t *>(smem + RING_BYTES);
-  uint64_t *emptyA = fullA + A_STAGES;
-  uint64_t *fullB = emptyA + A_STAGES;
-  uint64_t *emptyB = fullB + B_STAGES;
-  uint64_t *tfull = emptyB + B_STAGES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
+  uint64_t *empty = full + STAGES;
+  uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
-  int *tile_start = reinterpret_cast<int *>(smem + RING_BYTES + 256);  // [G + 1]
+  int *tile_start = reinterpret_cast<int *>(smem + STAGES * STAGE_BYTES + 256);  // [G + 1]
   int *mtiles = tile_start + MAX_GROUPS + 1;                                     // [G]
   int *rowbeg = mtiles + MAX_GROUPS;                                             // [G]
   int *rowend = rowbeg + MAX_GROUPS;                                             // [G]
@@ -246,13 +236,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int num_kb = args.num_kb;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < A_STAGES; ++s) {
-      mbar_init(&fullA[s], 1);
-      mbar_init(&emptyA[s], 1);
-    }
-    for (int s = 0; s < B_STAGES; ++s) {
-      mbar_init(&fullB[s], 1);
-      mbar_init(&emptyB[s], 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -291,105 +277,61 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    // One thread walks the (tile, k-block) steps twice: the B loads of step i and
-    // the A loads of step i - A_LAG are issued together, each ring waiting on its
-    // own empty barriers, so B runs B_STAGES steps ahead of the MMAs and A only
-    // A_STAGES.
     if (lane == 0) {
-      struct Cursor {
-        int tile, kb, g;
-      };
-      auto advance = [&](Cursor &c) {
-        if (++c.kb == num_kb) {
-          c.kb = 0;
-          c.tile += gridDim.x;
-        }
-      };
-      auto locate = [&](Cursor &c, int &n_tile, int &m_tile) {
-        while (c.tile >= tile_start[c.g + 1]) ++c.g;
-        const int local = c.tile - tile_start[c.g];
-        n_tile = local / mtiles[c.g];
-        m_tile = local - n_tile * mtiles[c.g];
-      };
-      int a_issued[A_STAGES], b_issued[B_STAGES];
-      for (int s = 0; s < A_STAGES; ++s) a_issued[s] = -1;
-      for (int s = 0; s < B_STAGES; ++s) b_issued[s] = -1;
-      int as = 0, bs = 0;
-      uint32_t aph = 0, bph = 0;
-      Cursor cb{(int)blockIdx.x, 0, 0}, ca{(int)blockIdx.x, 0, 0};
-      const long long steps = (long long)((total_tiles - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x) *
-                              (blockIdx.x < (unsigned)total_tiles ? num_kb : 0);
+      int issued_parity[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+      int stage = 0;
+      uint32_t phase = 0;
+      int g = 0;
       bool ok = true;
-      for (long long i = 0; i < steps + A_LAG && ok; ++i) {
-        if (i < steps) {  // B of step i
-          int n_tile, m_tile;
-          locate(cb, n_tile, m_tile);
-          if (!mbar_wait(&emptyB[bs], bph ^ 1u, args.status)) {
+      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+        while (tile >= tile_start[g + 1]) ++g;
+        const int local = tile - tile_start[g];
+        const int n_tile = local / mtiles[g];
+        const int m_tile = local - n_tile * mtiles[g];
+        const int a_row = rowbeg[g] + m_tile * BM;
+        const int b_row = g * args.b_rows + n_tile * OUT_COLS;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, args.status)) {
             ok = false;
             break;
           }
-          uint8_t *sb = sB + bs * B_BYTES;
-          mbar_arrive_expect_tx(&fullB[bs], (uint32_t)B_BYTES);
-          const int kb = cb.kb;
+          uint8_t *sa = smem + stage * STAGE_BYTES;
+          uint8_t *sb = sa + A_BYTES;
+          mbar_arrive_expect_tx(&full[stage], STAGE_TX);
           if (MODE == kPlainBT || MODE == kDualBT) {
             const bool second = MODE == kDualBT && kb >= args.kb1;
             const int k0 = (second ? kb - args.kb1 : kb) * BK;
             const CUtensorMap *mb = second ? &tmB1 : &tmB0;
+            tma_load_2d(sa, second ? &tmA2 : &tmA, &full[stage], k0, a_row);
 #pragma unroll
             for (int j = 0; j < BN / 64; ++j)
-              tma_load_3d(sb + j * B_SLICE, mb, &fullB[bs], n_tile * OUT_COLS + 64 * j, k0, cb.g);
+              tma_load_3d(sb + j * B_SLICE, mb, &full[stage], n_tile * OUT_COLS + 64 * j, k0, g);
+          } else if (paired_b(MODE)) {
+            tma_load_2d(sa, &tmA, &full[stage], kb * BK, a_row);
+            tma_load_2d(sb, &tmB0, &full[stage], kb * BK, b_row);
+            tma_load_2d(sb + B_BYTES / 2, &tmB1, &full[stage], kb * BK, b_row);
           } else {
-            const int b_row = cb.g * args.b_rows + n_tile * OUT_COLS;
-            tma_load_2d(sb, &tmB0, &fullB[bs], kb * BK, b_row);
-            if (paired_b(MODE))
-              tma_load_2d(sb + B_BYTES / 2, &tmB1, &fullB[bs], kb * BK, b_row);
-            else
-              tma_load_2d(sb + B_BYTES / 2, &tmB0, &fullB[bs], kb * BK, b_row + BN / 2);
+            tma_load_2d(sa, &tmA, &full[stage], kb * BK, a_row);
+            tma_load_2d(sb, &tmB0, &full[stage], kb * BK, b_row);
+            tma_load_2d(sb + B_BYTES / 2, &tmB0, &full[stage], kb * BK, b_row + BN / 2);
           }
-          b_issued[bs] = (int)bph;
-          if (++bs == B_STAGES) {
-            bs = 0;
-            bph ^= 1u;
+          issued_parity[stage] = (int)phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
-          advance(cb);
-        }
-        if (i >= A_LAG) {  // A of step i - A_LAG
-          int n_tile, m_tile;
-          locate(ca, n_tile, m_tile);
-          if (!mbar_wait(&emptyA[as], aph ^ 1u, args.status)) {
-            ok = false;
-            break;
-          }
-          uint8_t *sa = sA + as * A_BYTES;
-          mbar_arrive_expect_tx(&fullA[as], (uint32_t)A_BYTES);
-          const int kb = ca.kb;
-          const int a_row = rowbeg[ca.g] + m_tile * BM;
-          if (MODE == kPlainBT || MODE == kDualBT) {
-            const bool second = MODE == kDualBT && kb >= args.kb1;
-            const int k0 = (second ? kb - args.kb1 : kb) * BK;
-            tma_load_2d(sa, second ? &tmA2 : &tmA, &fullA[as], k0, a_row);
-          } else {
-            tma_load_2d(sa, &tmA, &fullA[as], kb * BK, a_row);
-          }
-          a_issued[as] = (int)aph;
-          if (++as == A_STAGES) {
-            as = 0;
-            aph ^= 1u;
-          }
-          advance(ca);
         }
       }
       // never leave the CTA with a bulk copy still writing its shared memory
-      for (int s = 0; s < A_STAGES; ++s)
-        if (a_issued[s] >= 0) mbar_wait(&fullA[s], (uint32_t)a_issued[s], args.status);
-      for (int s = 0; s < B_STAGES; ++s)
-        if (b_issued[s] >= 0) mbar_wait(&fullB[s], (uint32_t)b_issued[s], args.status);
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_parity[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_parity[s], args.status);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int as = 0, bs = 0;
-      uint32_t aph = 0, bph = 0;
+      int stage = 0;
+      uint32_t phase = 0;
       int it = 0;
       bool ok = true;
       int g = 0;
@@ -405,45 +347,39 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&fullA[as], aph, args.status) || !mbar_wait(&fullB[bs], bph, args.status)) {
+          if (!mbar_wait(&full[stage], phase, args.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(sA + as * A_BYTES);
-          const uint32_t sb = smem_u32(sB + bs * B_BYTES);
+          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
           const uint64_t adesc = smem_desc_sw128(sa);
           if (swappable(MODE) && swapped) {
             // weight halves as M (128 rows each), the group's rows as N
-            const uint64_t w1 = smem_desc_sw128(sb);
-            const uint64_t w2 = smem_desc_sw128(sb + B_BYTES / 2);
+            const uint64_t w1 = smem_desc_sw128(sa + A_BYTES);
+            const uint64_t w2 = smem_desc_sw128(sa + A_BYTES + B_BYTES / 2);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               tc_mma_bf16(d_tmem, w1 + 2ull * kk, adesc + 2ull * kk, idesc_sw, (kb | kk) != 0);
               tc_mma_bf16(d_tmem + (uint32_t)nt, w2 + 2ull * kk, adesc + 2ull * kk, idesc_sw, (kb | kk) != 0);
             }
           } else if (MODE == kPlainBT || MODE == kDualBT) {
-            const uint64_t bdesc = smem_desc_sw128_mn(sb, B_SLICE);
+            const uint64_t bdesc = smem_desc_sw128_mn(sa + A_BYTES, B_SLICE);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)  // A: +32 B along K; B: +16 rows = +2048 B
               tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 128ull * kk, IDESC_BT, (kb | kk) != 0);
           } else {
-            const uint64_t bdesc = smem_desc_sw128(sb);
+            const uint64_t bdesc = smem_desc_sw128(sa + A_BYTES);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
               // +32 bytes along K inside the 128-byte swizzle row = +2 in the address field
               tc_mma_bf16(d_tmem, adesc + 2ull * kk, bdesc + 2ull * kk, IDESC, (kb | kk) != 0);
             }
           }
-          tc_commit(&emptyA[as]);
-          tc_commit(&emptyB[bs]);
-          if (++as == A_STAGES) {
-            as = 0;
-            aph ^= 1u;
-          }
-          if (++bs == B_STAGES) {
-            bs = 0;
-            bph ^= 1u;
+          tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
           }
         }
         if (ok) tc_commit(&tfull[acc]);
