@@ -72,6 +72,15 @@ def test_tc_gemm_pair_tiles(act):
     _expert_ffn_case(3, [600, 1100, 301], d=320, F=520, act=act, seed=4)
 
 
+@pytest.mark.parametrize("act", ["swiglu", "relu"])
+def test_tc_gemm_wide_tiles(act):
+    """Groups averaging >= 128 rows with K >= 1024 run 256-row tiles on one CTA (two
+    128-row accumulators): a tile whose second half is empty or holds one row, a
+    group of at most 128 rows (swapped operands), an empty group, widths not
+    multiples of the tile."""
+    _expert_ffn_case(5, [300, 0, 129, 64, 513], d=1024, F=1088, act=act, seed=6)
+
+
 def test_tc_gemm_many_experts_deep_k():
     _expert_ffn_case(16, [3, 40, 0, 200, 129, 1, 77, 128, 256, 5, 0, 9, 64, 300, 17, 2], d=1024, F=512,
                      act="swiglu", seed=3)
