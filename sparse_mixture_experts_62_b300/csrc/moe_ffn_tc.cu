@@ -422,230 +422,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// ---------------------------------------------------------------- wide single-CTA form
-// Forward modes, groups averaging at least 128 rows and K of at least 1024: one
-// CTA computes 256 rows x 256 columns as two 128-row accumulators (the two halves
-// of tensor memory) that share each B stage.  A k-block then moves 64 KB into
-// shared memory for 8 MMAs, and the MMAs read 64 KB back out: about 128 B per
-// clock at the full MMA rate, against about 190 B per clock for a 128-row tile
-// (48 KB in, 48 KB out per 4 MMAs), which the shared-memory bandwidth caps near two
-// thirds of the tensor peak.  A tile whose second half holds no rows of its group
-// loads and multiplies only the first half, so the rows are still covered at a
-// 128-row granularity (a CTA pair, whose MMA is always 256 rows, pads to 256).
-// Without a second accumulator pair the next tile's MMAs wait for the epilogue,
-// which eight warps (two per lane quadrant, one per half) keep short.  Groups of
-// at most 128 rows run the swapped tiles of the 128-row form in the first half.
-namespace wide {
-constexpr int STAGES = 3;
-constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;  // 64 KB: A half 0, A half 1, B
-constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + (size_t)(4 * MAX_GROUPS + 8) * 4;
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
-}  // namespace wide
-
-template <int MODE>
-__global__ void __launch_bounds__(wide::THREADS, 1)
-    grouped_gemm_wide_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                             const __grid_constant__ CUtensorMap tmB1, const Args args) {
-  static_assert(swappable(MODE), "forward modes only");
-  constexpr int STAGES = wide::STAGES, STAGE_BYTES = wide::STAGE_BYTES;
-  constexpr int OUT_COLS = paired_b(MODE) ? 128 : 256;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t *smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + STAGES * STAGE_BYTES);
-  uint64_t *empty = full + STAGES;
-  uint64_t *tfull = empty + STAGES;
-  uint64_t *tempty = tfull + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 1);
-  int *tile_start = reinterpret_cast<int *>(smem + STAGES * STAGE_BYTES + 256);  // [G + 1]
-  int *mtiles = tile_start + MAX_GROUPS + 1;                                     // [G]
-  int *rowbeg = mtiles + MAX_GROUPS;                                             // [G]
-  int *rowend = rowbeg + MAX_GROUPS;                                             // [G]
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int G = args.G;
-  const int n_tiles = (args.n_out + OUT_COLS - 1) / OUT_COLS;
-  const int num_kb = args.num_kb;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(tfull, 1);
-    mbar_init(tempty, wide::EPI_WARPS);
-    fence_barrier_init();
-    int acc = 0;
-    for (int g = 0; g < G; ++g) {
-      int b = args.offsets ? args.offsets[g] : 0;
-      int e = args.offsets ? args.offsets[g + 1] : args.M;
-      if (b < 0 || e < b || e > args.a_rows) {  // malformed group: flag it, run nothing
-        set_status(args.status, MOE_ERR_BOUNDS);
-        b = e = 0;
-      }
-      rowbeg[g] = b;
-      rowend[g] = e;
-      const int mt = e > b ? (e - b + 2 * BM - 1) / (2 * BM) : 0;  // 256-row tiles (1 for swapped groups)
-      mtiles[g] = mt;
-      tile_start[g] = acc;
-      acc += mt * n_tiles;
-    }
-    tile_start[G] = acc;
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB0);
-    if (paired_b(MODE)) tma_prefetch_desc(&tmB1);
-  }
-  if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  const int total_tiles = tile_start[G];
-
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      int issued_parity[STAGES];
-      for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
-      int stage = 0;
-      uint32_t phase = 0;
-      int g = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-        while (tile >= tile_start[g + 1]) ++g;
-        const int local = tile - tile_start[g];
-        const int n_tile = local / mtiles[g];
-        const int m_tile = local - n_tile * mtiles[g];
-        const int a_row = rowbeg[g] + m_tile * 2 * BM;
-        const int halves = rowend[g] - a_row > BM ? 2 : 1;
-        const int b_row = g * args.b_rows + n_tile * OUT_COLS;
-        const uint32_t tx = (uint32_t)(halves * A_BYTES + B_BYTES);
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, args.status)) {
-            ok = false;
-            break;
-          }
-          uint8_t *sa = smem + stage * STAGE_BYTES;
-          uint8_t *sb = sa + 2 * A_BYTES;
-          mbar_arrive_expect_tx(&full[stage], tx);
-          tma_load_2d(sa, &tmA, &full[stage], kb * BK, a_row);
-          if (halves == 2) tma_load_2d(sa + A_BYTES, &tmA, &full[stage], kb * BK, a_row + BM);
-          tma_load_2d(sb, &tmB0, &full[stage], kb * BK, b_row);
-          if (paired_b(MODE))
-            tma_load_2d(sb + B_BYTES / 2, &tmB1, &full[stage], kb * BK, b_row);
-          else
-            tma_load_2d(sb + B_BYTES / 2, &tmB0, &full[stage], kb * BK, b_row + BN / 2);
-          issued_parity[stage] = (int)phase;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      // never leave the CTA with a bulk copy still writing its shared memory
-      for (int s = 0; s < STAGES; ++s)
-        if (issued_parity[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_parity[s], args.status);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int it = 0;
-      bool ok = true;
-      int g = 0;
-      for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x, ++it) {
-        while (tile >= tile_start[g + 1]) ++g;
-        const int grows = rowend[g] - rowbeg[g];
-        const bool swapped = grows <= SWAP_ROWS;
-        const int nt = (grows + 15) & ~15;  // N of the swapped MMAs
-        const uint32_t idesc_sw = idesc_bf16_f32(BM, nt > 0 ? nt : 16);
-        const int local = tile - tile_start[g];
-        const int m_tile = local - (local / mtiles[g]) * mtiles[g];
-        const int halves = rowend[g] - (rowbeg[g] + m_tile * 2 * BM) > BM ? 2 : 1;
-        // the epilogue has drained the previous tile's accumulators
-        if (!mbar_wait(tempty, ((uint32_t)it & 1u) ^ 1u, args.status)) break;
-        tc_fence_after();
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, args.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t sb = sa + 2 * A_BYTES;
-          if (swapped) {
-            // weight halves as M (128 rows each), the group's rows as N
-            const uint64_t tok = smem_desc_sw128(sa);
-            const uint64_t w1 = smem_desc_sw128(sb);
-            const uint64_t w2 = smem_desc_sw128(sb + B_BYTES / 2);
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              tc_mma_bf16(tmem_base, w1 + 2ull * kk, tok + 2ull * kk, idesc_sw, (kb | kk) != 0);
-              tc_mma_bf16(tmem_base + (uint32_t)nt, w2 + 2ull * kk, tok + 2ull * kk, idesc_sw, (kb | kk) != 0);
-            }
-          } else {
-            const uint64_t bdesc = smem_desc_sw128(sb);
-            for (int h = 0; h < halves; ++h) {
-              const uint64_t adesc = smem_desc_sw128(sa + (uint32_t)(h * A_BYTES));
-#pragma unroll
-              for (int kk = 0; kk < BK / 16; ++kk)
-                tc_mma_bf16(tmem_base + (uint32_t)(h * BN), adesc + 2ull * kk, bdesc + 2ull * kk, IDESC,
-                            (kb | kk) != 0);
-            }
-          }
-          tc_commit(&empty[stage]);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (ok) tc_commit(tfull);
-      }
-    }
-  } else {
-    // ------------------------------------------------------------ epilogue (8 warps)
-    const int ew = warp - 2;
-    const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
-    const int half = ew >> 2;   // accumulator (row half) this warp drains
-    const int r = quad * 32 + lane;
-    int g = 0;
-    int it = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x, ++it) {
-      while (tile >= tile_start[g + 1]) ++g;
-      const int local = tile - tile_start[g];
-      const int n_tile = local / mtiles[g];
-      const int m_tile = local - n_tile * mtiles[g];
-      const int grows = rowend[g] - rowbeg[g];
-      const int row0 = rowbeg[g] + m_tile * 2 * BM + half * BM;
-      const int rows_valid = min(BM, rowend[g] - row0);
-      const int n0 = n_tile * OUT_COLS;
-      if (!mbar_wait(tfull, (uint32_t)it & 1u, args.status)) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + (uint32_t)(half * BN) + ((uint32_t)(quad * 32) << 16);
-      if (grows <= SWAP_ROWS) {
-        if (half == 0) epilogue_swapped<MODE>(taddr, args, rowbeg[g], grows, (grows + 15) & ~15, n0, r);
-      } else if (rows_valid > 0) {
-        epilogue_row<MODE>(taddr, args, row0 + r, r < rows_valid, n0);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
-    }
-  }
-
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
-  }
-}
-
 // ---------------------------------------------------------------- CTA-pair form
 // The same grouped GEMM on pairs of SMs (a cluster of two CTAs) with
 // tcgen05.mma.cta_group::2: one pair computes a 256-row x 256-column tile.  Each
@@ -997,41 +773,9 @@ static int launch_single(const CUtensorMap &ma, const CUtensorMap &ma2, const CU
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-template <int MODE>
-static int launch_wide(const CUtensorMap &ma, const CUtensorMap &mb0, const CUtensorMap &mb1, const Args &args,
-                       int device, int sms, cudaStream_t stream) {
-  {
-    static std::mutex mu;
-    static std::vector<int> done;
-    std::lock_guard<std::mutex> lk(mu);
-    if ((int)done.size() <= device) done.resize(device + 1, 0);
-    if (!done[device]) {
-      if (cudaFuncSetAttribute(grouped_gemm_wide_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)wide::SMEM_BYTES) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      done[device] = 1;
-    }
-  }
-  grouped_gemm_wide_kernel<MODE><<<dim3(sms), dim3(wide::THREADS), wide::SMEM_BYTES, stream>>>(ma, mb0, mb1, args);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
-}
-
-// The wide single-CTA form pays off when the groups hold 256-row tiles and K is
-// long enough for the mainloop to dwarf the epilogue it cannot overlap.
-static bool use_wide(int mode, int64_t a_rows, int G, int num_kb) {
-  return swappable(mode) && num_kb >= 16 && a_rows >= (int64_t)128 * G;
-}
-
 static int launch_mode(int mode, const CUtensorMap &ma, const CUtensorMap &ma2, const CUtensorMap &mb0,
                        const CUtensorMap &mb1, const Args &args, int device, int sms, bool pair_tiles,
                        cudaStream_t stream) {
-  if (!pair_tiles && use_wide(mode, args.a_rows, args.G, args.num_kb)) {
-    switch (mode) {
-      case kSwiGLU: return launch_wide<kSwiGLU>(ma, mb0, mb1, args, device, sms, stream);
-      case kReLU: return launch_wide<kReLU>(ma, mb0, mb1, args, device, sms, stream);
-      default: return launch_wide<kPlain>(ma, mb0, mb1, args, device, sms, stream);
-    }
-  }
   if (pair_tiles) {
     switch (mode) {
       case kSwiGLU: return launch_pair<kSwiGLU>(ma, ma2, mb0, mb1, args, device, stream);

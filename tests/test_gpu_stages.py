@@ -73,11 +73,10 @@ def test_tc_gemm_pair_tiles(act):
 
 
 @pytest.mark.parametrize("act", ["swiglu", "relu"])
-def test_tc_gemm_wide_tiles(act):
-    """Groups averaging >= 128 rows with K >= 1024 run 256-row tiles on one CTA (two
-    128-row accumulators): a tile whose second half is empty or holds one row, a
-    group of at most 128 rows (swapped operands), an empty group, widths not
-    multiples of the tile."""
+def test_tc_gemm_long_k_mixed_groups(act):
+    """K >= 1024 with groups of 64 to 513 rows: tiles of one row past a 128-row
+    multiple, a group of at most 128 rows (swapped operands), an empty group, widths
+    not multiples of the tile."""
     _expert_ffn_case(5, [300, 0, 129, 64, 513], d=1024, F=1088, act=act, seed=6)
 
 
