@@ -1,5 +1,6 @@
 // C ABI of libmoe_b300: argument checks, workspace layout and the order of the
 // launches.  Every function returns a moe_status; argument errors launch nothing.
+#include <algorithm>
 #include <mutex>
 #include <string.h>
 #include <vector>
@@ -217,9 +218,25 @@ int ffn_shared(const moe_config *c, const void *x, const void *sw1, const void *
 }
 
 // logits, top-k and gate weights: tensor-core router for bf16 x, CUDA-core router for float32 x
+// A handful of tokens (decode): the tensor-core router's fixed costs (splitting W_g,
+// tensor memory, its pipeline) outweigh its work, so float32 FMA on the CUDA cores,
+// split along K over CTAs, computes the logits; the top-k kernel adds the splits.
+inline bool small_router(const moe_config *c) { return is_bf16(c) && c->T <= 64; }
+inline int small_router_splits(const moe_config *c) {
+  return std::min(router_tc_max_splits(c->T, c->d), (c->d + 127) / 128);
+}
+
 int route(const moe_config *c, const Ws &w, const void *x, const float *Wg, const float *logit_bias,
           const float *sel_bias, float *logits, int32_t *idx, float *gw, cudaStream_t s) {
   const float *sb = c->gate == MOE_GATE_SIGMOID_BIAS ? sel_bias : nullptr;
+  if (small_router(c)) {
+    const int S = small_router_splits(c);
+    float *part = w.router_partial(c);  // [S][T][N] within the [max splits][T][Npad] scratch
+    MOE_TRY(launch_router_logits(x, true, Wg, nullptr, c->T, c->d, c->N, S, part, s));
+    const int nkc = (c->d + 127) / 128, kc_per = (nkc + S - 1) / S;
+    return launch_router_topk(part, (nkc + kc_per - 1) / kc_per, c->N, logit_bias, logits, sb, c->T, c->N, c->k,
+                              c->gate, idx, gw, w.status(), s);
+  }
   if (is_bf16(c)) {
     int S = 1;
     float *part = w.router_partial(c);
@@ -227,7 +244,7 @@ int route(const moe_config *c, const Ws &w, const void *x, const float *Wg, cons
     return launch_router_topk(part, S, router_tc_npad(c->N), logit_bias, logits, sb, c->T, c->N, c->k, c->gate, idx,
                               gw, w.status(), s);
   }
-  MOE_TRY(launch_router_logits(x, false, Wg, logit_bias, c->T, c->d, c->N, logits, s));
+  MOE_TRY(launch_router_logits(x, false, Wg, logit_bias, c->T, c->d, c->N, 1, logits, s));
   return launch_router_topk(logits, 1, c->N, nullptr, logits, sb, c->T, c->N, c->k, c->gate, idx, gw, w.status(), s);
 }
 
@@ -240,7 +257,7 @@ int ec_route(const moe_config *c, const Ws &w, const void *x, const float *Wg, c
     MOE_TRY(launch_router_tc(x, Wg, c->T, c->d, c->N, w.router_wsplit(c), part, &S, w.status(), s));
     MOE_TRY(launch_router_sum(part, S, router_tc_npad(c->N), logit_bias, logits, c->T, c->N, s));
   } else {
-    MOE_TRY(launch_router_logits(x, false, Wg, logit_bias, c->T, c->d, c->N, logits, s));
+    MOE_TRY(launch_router_logits(x, false, Wg, logit_bias, c->T, c->d, c->N, 1, logits, s));
   }
   MOE_TRY(launch_expert_choice(logits, c->T, c->N, ec_c(c), scores, offsets, src_token, dest_row, s));
   return launch_fill_counts(w.at<int32_t>(w.L.counts_routed), w.at<int32_t>(w.L.counts_kept), c->N, ec_c(c), s);

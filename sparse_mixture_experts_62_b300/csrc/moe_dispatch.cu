@@ -163,6 +163,86 @@ __global__ void __launch_bounds__(CH) dispatch_rank_kernel(const int32_t *__rest
   }
 }
 
+// T <= 128 (one chunk, e.g. decode): histogram, capacity, offsets and ranks in
+// one CTA, the three steps above without the launches between them.
+__global__ void __launch_bounds__(CH) dispatch_one_chunk_kernel(const int32_t *__restrict__ idx, int T, int k, int N,
+                                                                int capacity, int32_t *__restrict__ counts_routed,
+                                                                int32_t *__restrict__ counts_kept,
+                                                                int32_t *__restrict__ offsets,
+                                                                int32_t *__restrict__ dest_row,
+                                                                int32_t *__restrict__ src_token, int *status) {
+  __shared__ uint32_t lanes_with[CH_WARPS][256];  // which lanes of the warp picked expert e
+  __shared__ int warp_before[CH_WARPS][256];      // assignments to e in earlier warps
+  __shared__ int kept_s[256];                     // kept counts, then their inclusive scan
+  __shared__ int off_s[256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int v = threadIdx.x; v < CH_WARPS * 256; v += CH) (&lanes_with[0][0])[v] = 0u;
+  __syncthreads();
+  const int t = threadIdx.x;
+  int ex[8];
+  for (int j = 0; j < k; ++j) {
+    ex[j] = -1;
+    if (t < T) {
+      const int e = idx[(size_t)t * k + j];
+      if (e < 0 || e >= N) {
+        set_status(status, MOE_ERR_BOUNDS);
+      } else if (repeats_earlier_slot(ex, j, e)) {
+        set_status(status, MOE_ERR_INVALID_ARG);
+      } else {
+        ex[j] = e;
+        atomicOr(&lanes_with[warp][e], 1u << lane);
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < 256; e += CH) {
+    int run = 0;
+    if (e < N)
+      for (int w = 0; w < CH_WARPS; ++w) {
+        warp_before[w][e] = run;
+        run += __popc(lanes_with[w][e]);
+      }
+    const int kept = (e < N) ? (capacity > 0 ? min(run, capacity) : run) : 0;
+    if (e < N) {
+      counts_routed[e] = run;
+      counts_kept[e] = kept;
+    }
+    kept_s[e] = kept;
+    off_s[e] = kept;
+  }
+  __syncthreads();
+  // inclusive scan of the kept counts over 256 entries, two per thread
+  for (int off = 1; off < 256; off <<= 1) {
+    const int a = threadIdx.x, b = threadIdx.x + CH;
+    const int va = a >= off ? kept_s[a - off] : 0;
+    const int vb = b >= off ? kept_s[b - off] : 0;
+    __syncthreads();
+    kept_s[a] += va;
+    kept_s[b] += vb;
+    __syncthreads();
+  }
+  for (int e = threadIdx.x; e < N; e += CH) {
+    off_s[e] = kept_s[e] - off_s[e];  // exclusive
+    offsets[e] = off_s[e];
+  }
+  if (threadIdx.x == 0) offsets[N] = kept_s[N - 1];
+  __syncthreads();
+  if (t >= T) return;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int j = 0; j < k; ++j) {
+    const int e = ex[j];
+    int row = -1;
+    if (e >= 0) {
+      const int rank = warp_before[warp][e] + __popc(lanes_with[warp][e] & lt_mask);
+      if (capacity <= 0 || rank < capacity) {
+        row = off_s[e] + rank;
+        src_token[row] = t;
+      }
+    }
+    dest_row[(size_t)t * k + j] = row;
+  }
+}
+
 // x_perm[row] = x[src_token[row]] for row < offsets[N]; one warp per row.  Each
 // lane issues four 16-byte loads before their stores, so that enough bytes are in
 // flight per SM to cover the memory latency.
@@ -226,6 +306,11 @@ int launch_dispatch(const int32_t *idx, int T, int k, int N, int capacity, int32
                     int32_t *counts_routed, int32_t *counts_kept, int32_t *offsets, int32_t *dest_row,
                     int32_t *src_token, int *status, cudaStream_t s) {
   const int nchunks = (T + CH - 1) / CH;
+  if (nchunks == 1) {
+    dispatch_one_chunk_kernel<<<1, CH, 0, s>>>(idx, T, k, N, capacity, counts_routed, counts_kept, offsets, dest_row,
+                                               src_token, status);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   if (nchunks > 0) dispatch_hist_kernel<<<nchunks, CH, 0, s>>>(idx, T, k, N, hist, status);
   int G = 4;  // threads per expert: a power of two, G * 256 <= 1024 for N <= 256
   while (G < 32 && 2 * G * N <= SCAN_THREADS) G *= 2;

@@ -18,10 +18,13 @@ constexpr int RT_WARPS = 8;  // each warp owns RT_KC / RT_WARPS consecutive k of
 
 // Logits for 32 tokens x EN experts.  Lane = token; the 8 warps split each K
 // chunk, and their partial sums are added in warp order (deterministic).
+// blockIdx.z picks a range of kc_per 128-wide K chunks; its sums go to
+// logits + blockIdx.z * T * N (split partials, added in split order by the
+// top-k kernel; the logit bias is then added there and logit_bias is null here).
 template <int EN, bool BF16>
 __global__ void __launch_bounds__(256) router_logits_kernel(const void *__restrict__ x, const float *__restrict__ Wg,
                                                             const float *__restrict__ logit_bias, int T, int d, int N,
-                                                            float *__restrict__ logits) {
+                                                            int kc_per, float *__restrict__ logits) {
   constexpr int XS_LD = RT_KC + 1;
   constexpr int XS_FLOATS = RT_TOK * XS_LD;
   constexpr int WS_FLOATS = RT_KC * EN;
@@ -38,13 +41,16 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const void *__restri
 #pragma unroll
   for (int e = 0; e < EN; ++e) acc[e] = 0.f;
 
-  for (int k0 = 0; k0 < d; k0 += RT_KC) {
+  const int kbeg = blockIdx.z * kc_per * RT_KC;
+  const int kend = min(d, kbeg + kc_per * RT_KC);
+  logits += (size_t)blockIdx.z * T * N;
+  for (int k0 = kbeg; k0 < kend; k0 += RT_KC) {
     // stage x[t0.., k0..k0+127] as float (8-element vectors; d % 8 == 0 / 4)
     for (int v = threadIdx.x; v < RT_TOK * (RT_KC / 8); v += blockDim.x) {
       const int tt = v / (RT_KC / 8), kk = (v % (RT_KC / 8)) * 8;
       const int t = t0 + tt, kg = k0 + kk;
       float f[8];
-      if (t < T && kg < d) {
+      if (t < T && kg < kend) {
         if (BF16) {
           const uint4 q = *reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + (size_t)t * d + kg);
           f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x); f[2] = bf16_lo(q.y); f[3] = bf16_hi(q.y);
@@ -66,7 +72,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const void *__restri
     for (int v = threadIdx.x; v < RT_KC * EN; v += blockDim.x) {
       const int kk = v / EN, e = v % EN;
       const int kg = k0 + kk, eg = e0 + e;
-      ws[v] = (kg < d && eg < N) ? Wg[(size_t)kg * N + eg] : 0.f;
+      ws[v] = (kg < kend && eg < N) ? Wg[(size_t)kg * N + eg] : 0.f;
     }
     __syncthreads();
     const int kb = warp * (RT_KC / RT_WARPS);
@@ -329,15 +335,19 @@ int launch_router_sum(const float *partial, int S, int pstride, const float *log
 }
 
 int launch_router_logits(const void *x, bool x_bf16, const float *Wg, const float *logit_bias, int T, int d, int N,
-                         float *logits, cudaStream_t s) {
+                         int splits, float *logits, cudaStream_t s) {
   if (T == 0) return MOE_OK;
   const int en = N <= 8 ? 8 : (N <= 16 ? 16 : 32);
-  dim3 grid((T + RT_TOK - 1) / RT_TOK, (N + en - 1) / en), block(256);
+  const int nkc = (d + RT_KC - 1) / RT_KC;
+  if (splits < 1) splits = 1;
+  const int kc_per = (nkc + splits - 1) / splits;
+  splits = (nkc + kc_per - 1) / kc_per;  // every split non-empty
+  dim3 grid((T + RT_TOK - 1) / RT_TOK, (N + en - 1) / en, splits), block(256);
 #define MOE_RL(EN)                                                                                           \
   if (x_bf16)                                                                                                \
-    router_logits_kernel<EN, true><<<grid, block, 0, s>>>(x, Wg, logit_bias, T, d, N, logits);              \
+    router_logits_kernel<EN, true><<<grid, block, 0, s>>>(x, Wg, logit_bias, T, d, N, kc_per, logits);      \
   else                                                                                                       \
-    router_logits_kernel<EN, false><<<grid, block, 0, s>>>(x, Wg, logit_bias, T, d, N, logits);
+    router_logits_kernel<EN, false><<<grid, block, 0, s>>>(x, Wg, logit_bias, T, d, N, kc_per, logits);
   if (en == 8) {
     MOE_RL(8)
   } else if (en == 16) {

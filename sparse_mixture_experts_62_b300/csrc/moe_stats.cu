@@ -160,6 +160,66 @@ __global__ void __launch_bounds__(1024) stats_final_kernel(const float *__restri
   }
 }
 
+// T <= 32 (one chunk, e.g. decode): the partial sums, P, f and the summary in one
+// CTA of 256 threads -- the same arithmetic, in the same order, as the two kernels
+// above, without the launch between them.
+__global__ void __launch_bounds__(256) stats_one_chunk_kernel(const float *__restrict__ logits, int T, int N, int gate,
+                                                              const int32_t *__restrict__ counts_routed,
+                                                              const int32_t *__restrict__ counts_kept,
+                                                              long long total, float *__restrict__ f,
+                                                              float *__restrict__ P, float *__restrict__ summary) {
+  __shared__ float red[8][256];
+  __shared__ float fp[256];
+  __shared__ int maxc[256];
+  __shared__ long long kept[256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  const bool softmax = gate != MOE_GATE_SIGMOID_BIAS;
+  for (int t = warp; t < T; t += 8) {
+    float v[8];
+    token_probs(logits + (size_t)t * N, N, softmax, lane, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += v[i];
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[warp][lane + 32 * i] = acc[i];
+  __syncthreads();
+  const int x = threadIdx.x;
+  float fe = 0.f, pe = 0.f;
+  int ce = 0;
+  long long ke = 0;
+  if (x < N) {
+    float sum = 0.f;
+    for (int w = 0; w < 8; ++w) sum += red[w][x];
+    pe = sum / (float)T;
+    fe = (float)((double)counts_routed[x] / (double)total);
+    P[x] = pe;
+    f[x] = fe;
+    ce = counts_routed[x];
+    ke = counts_kept[x];
+  }
+  fp[x] = fe * pe;
+  maxc[x] = ce;
+  kept[x] = ke;
+  __syncthreads();
+  for (int off = 128; off > 0; off >>= 1) {
+    if (x < off) {
+      fp[x] += fp[x + off];
+      maxc[x] = max(maxc[x], maxc[x + off]);
+      kept[x] += kept[x + off];
+    }
+    __syncthreads();
+  }
+  if (x == 0) {
+    const double tk = (double)total;
+    summary[0] = (float)N * fp[0];
+    summary[1] = (float)((double)maxc[0] / (tk / (double)N));
+    summary[2] = (float)(1.0 - (double)kept[0] / tk);
+  }
+}
+
 // One CTA per sequence (L >= 32): P_e L = the sequence's chunk partials added in
 // order, n_e = its assignments to e (counted from topk_idx), and
 // loss_s = N sum_e (n_e / (L k)) (P_e L / L).
@@ -322,6 +382,10 @@ int launch_load_stats(const float *logits, const int32_t *counts_routed, const i
                       cudaStream_t s) {
   if (T == 0) return MOE_OK;
   const int nchunks = (T + SC - 1) / SC;
+  if (nchunks == 1) {
+    stats_one_chunk_kernel<<<1, 256, 0, s>>>(logits, T, N, gate, counts_routed, counts_kept, total, f, P, summary);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   stats_partial_kernel<<<nchunks, 256, 0, s>>>(logits, T, N, gate, T, nchunks, partial, ticket);
   stats_final_kernel<<<(N + 31) / 32, 1024, 0, s>>>(partial, nchunks, counts_routed, counts_kept, T, N, total, f, P,
                                                     summary, ticket);

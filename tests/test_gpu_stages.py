@@ -146,6 +146,7 @@ def test_route_flags_nonfinite_logits():
 
 
 @pytest.mark.parametrize("T,N,k,cap,dtype", [(333, 8, 2, 0, "bf16"), (1000, 16, 4, 150, "bf16"),
+                                             (128, 256, 8, 3, "bf16"), (97, 8, 2, 20, "bf16"),
                                              (4096, 128, 8, 200, "bf16"), (257, 5, 5, 0, "f32"),
                                              (1, 4, 2, 0, "bf16"), (300, 3, 1, 1, "bf16"),
                                              (5000, 256, 8, 0, "bf16")])
@@ -171,15 +172,16 @@ def test_dispatch_parity(T, N, k, cap, dtype):
     assert torch.equal(xp[:S].cpu(), xt.cpu()[torch.from_numpy(ref.src_token.astype(np.int64))])
 
 
-def test_dispatch_repeated_expert_is_flagged_and_dropped():
+@pytest.mark.parametrize("T", [300, 100])  # several 128-token chunks; one chunk (a single fused kernel)
+def test_dispatch_repeated_expert_is_flagged_and_dropped(T):
     """A top-k input that lists an expert twice for one token: the repeat is not
     counted and gets no row, the device status reports MOE_ERR_INVALID_ARG, and
     the rest is the dispatch of the input without the repeat."""
-    T, N, k, d = 300, 8, 3, 64
+    N, k, d = 8, 3, 64
     rng = np.random.default_rng(9)
     idx = np.stack([rng.permutation(N)[:k] for _ in range(T)]).astype(np.int32)
     idx[17, 2] = idx[17, 0]
-    idx[200, 1] = idx[200, 0]
+    idx[T - 3, 1] = idx[T - 3, 0]
     cfg = moe.make_config(T, d, N, k, 64)
     ws = _ws(cfg)
     x = to_dev(synth.normal(5, 1, (T, d), 1.0, "bf16"), "bf16")
@@ -189,11 +191,11 @@ def test_dispatch_repeated_expert_is_flagged_and_dropped():
     moe.moe_dispatch(cfg, torch.from_numpy(idx).cuda(), x, cr, ck, off, dr, st, xp, ws)
     assert moe.moe_get_device_status(ws) == moe.MOE_ERR_INVALID_ARG
     dest = dr.cpu().numpy()
-    assert dest[17, 2] == -1 and dest[200, 1] == -1
+    assert dest[17, 2] == -1 and dest[T - 3, 1] == -1
     # everything else: the oracle's dispatch with the repeats removed by hand
     counts = np.bincount(idx.ravel(), minlength=N)
     counts[idx[17, 0]] -= 1
-    counts[idx[200, 0]] -= 1
+    counts[idx[T - 3, 0]] -= 1
     assert np.array_equal(cr.cpu().numpy(), counts)
     offn = off.cpu().numpy()
     assert np.array_equal(offn, np.concatenate([[0], np.cumsum(counts)]))
