@@ -138,8 +138,9 @@ def stage_roofline(flops, nbytes, ms, peaks, clocks=None, alu=False):
 
     Tensor-bound work is measured against the burst bf16 peak (`frac`), with two
     extra readings: against the sustained (power-capped) peak (`frac_sustained`),
-    and against the burst peak scaled by the median SM clock sampled in the timed
-    region over the maximum clock (`frac_clock_norm`)."""
+    and against the burst peak scaled by the median SM clock of the timed region
+    over the maximum clock (`frac_clock_norm`; the in-band probe's clock when there
+    is one, else nvidia-smi's)."""
     tf_peak = F32_ALU_TFLOPS if alu else peaks["bf16_tflops"]
     t_tensor = flops / (tf_peak * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
@@ -150,8 +151,10 @@ def stage_roofline(flops, nbytes, ms, peaks, clocks=None, alu=False):
              "frac": ach / tf_peak}
         if not alu:
             r["frac_sustained"] = ach / peaks["bf16_tflops_sustained"]
-            if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
-                r["frac_clock_norm"] = ach / (tf_peak * clocks["sm_mhz"] / clocks["sm_max_mhz"])
+            mhz = (clocks or {}).get("sm_mhz_in_band") or (clocks or {}).get("sm_mhz")
+            fmax = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz")
+            if mhz and fmax:
+                r["frac_clock_norm"] = ach / (tf_peak * min(mhz, fmax) / fmax)
         return r
     return {"ms": ms, "bound": "hbm", "achieved": nbytes / s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": t_hbm / s}
@@ -465,10 +468,22 @@ def time_layer(args, moe, layer, x, wl, stream, dist=None, clk_gpu=None):
     if flush:  # each step timed on its own, after 256 MB of writes have evicted the layer from L2
         scratch = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=stream.device)
         begins = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # SM clock sampled in-band during the timed steps: one sleeping thread on a side
+    # stream records (ns, cycles) pairs every 200 us for the expected duration
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    (graphs[0].replay() if graphs is not None else step(fev[0]))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    est_ms = e0.elapsed_time(e1) * args.steps * 1.5 + 2.0
+    n_probe = int(min(50000, max(8, est_ms * 5)))  # (n - 1) x 200 us stays under the probe's 10 s limit
+    probe = torch.zeros(2 * n_probe, dtype=torch.int64, device="cuda")
+    s_probe = torch.cuda.Stream()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(clk_gpu if clk_gpu is not None else torch.cuda.current_device()) as clk:
+        moe.moe_clock_probe(probe, n_probe, 200_000, s_probe)
         start.record(stream)
         for k in range(args.steps):
             if flush:
@@ -503,8 +518,28 @@ def time_layer(args, moe, layer, x, wl, stream, dist=None, clk_gpu=None):
     stage_ms = {n: float(np.mean([sev[k][j].elapsed_time(sev[k][j + 1]) for k in range(args.steps)]))
                 for j, (n, _) in enumerate(stages)}
     total_ms = float(sum(step_ms)) if flush else start.elapsed_time(end)
+    clocks = clk.summary()
+    clocks.update(probe_clock(probe.cpu().numpy(), start.elapsed_time(end)))
     return {"step_ms": step_ms, "total_ms": total_ms, "ffn_ms": ffn_ms, "stage_ms": stage_ms,
-            "graph": graphs is not None, "clocks": clk.summary(), "out": out, "stats": stats, "launches": nst}
+            "graph": graphs is not None, "clocks": clocks, "out": out, "stats": stats, "launches": nst}
+
+
+def probe_clock(samples, region_ms: float) -> dict:
+    """Median SM clock (MHz) over the probe's intervals that fall inside the timed
+    region (the probe starts with it), from (ns, cycles) sample pairs."""
+    s = np.asarray(samples, dtype=np.int64).reshape(-1, 2)
+    s = s[s[:, 0] > 0]
+    if len(s) < 2:
+        return {}
+    t, c = s[:, 0].astype(np.float64), s[:, 1].astype(np.float64)
+    keep = t <= t[0] + region_ms * 1e6
+    dt, dc = np.diff(t[keep]), np.diff(c[keep])
+    ok = dt > 0
+    if not np.any(ok):
+        return {}
+    mhz = dc[ok] / dt[ok] * 1e3
+    return {"sm_mhz_in_band": float(np.median(mhz)), "sm_mhz_in_band_p10": float(np.percentile(mhz, 10)),
+            "sm_mhz_in_band_p90": float(np.percentile(mhz, 90)), "in_band_intervals": int(ok.sum())}
 
 
 def ffn_kernel_label(wl, fp8: bool) -> str:

@@ -242,6 +242,15 @@ MOE_API int moe_load_stats(const moe_config *cfg, const float *logits, const int
  * have no counterpart: this only tests the library's failure handling. */
 MOE_API int moe_check_wait_timeout(void *ws, int64_t limit_ns, void *stream);
 
+/* Measurement aid: samples the SM clock while other work runs on other streams.
+ * One thread records n pairs (%globaltimer ns, clock64 cycles) into samples
+ * [2 n] (device uint64, 8-byte aligned), the i-th at i * interval_ns after the
+ * first, sleeping in between; the kernel ends by itself after (n - 1) *
+ * interval_ns.  Cycles over nanoseconds between two samples give the SM clock in
+ * that interval.  2 <= n <= 2^20, interval_ns >= 1000, (n - 1) * interval_ns <=
+ * 1e10, else MOE_ERR_INVALID_ARG.  The pages have no counterpart. */
+MOE_API int moe_clock_probe(uint64_t *samples, int n, int64_t interval_ns, void *stream);
+
 /* Backward pass of the layer, bf16 token-choice configs (Chapter 19, 19.6.2: the
  * top-k choice is discrete, so gradients reach the router through the gate weights
  * of the chosen, kept experts only, and each expert through the tokens it

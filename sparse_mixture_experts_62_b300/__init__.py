@@ -32,7 +32,7 @@ EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_works
            "moe_load_stats", "moe_get_device_status", "moe_dispatch_noalloc", "moe_check_wait_timeout",
            "moe_router_zloss", "moe_bias_update", "moe_ec_route", "moe_seq_balance_loss",
            "moe_backward_workspace_size", "moe_layer_backward", "moe_quantize_fp8", "moe_expert_ffn_fp8",
-           "moe_layer_forward_fp8")
+           "moe_layer_forward_fp8", "moe_clock_probe")
 
 
 class MoeConfig(ctypes.Structure):
@@ -83,6 +83,7 @@ def _load():
         "moe_quantize_fp8": [P, ctypes.c_int64, ctypes.c_int32, P, P, P],
         "moe_expert_ffn_fp8": [C] + [P] * 11,
         "moe_layer_forward_fp8": [C] + [P] * 16,
+        "moe_clock_probe": [P, ctypes.c_int32, ctypes.c_int64, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -250,6 +251,10 @@ def moe_bias_update(cfg, counts_routed, sel_bias, gamma: float, stream=None):
 
 def moe_check_wait_timeout(ws, limit_ns: int, stream=None):
     _check(_lib.moe_check_wait_timeout(_ptr(ws), int(limit_ns), _stream(stream)), "moe_check_wait_timeout")
+
+
+def moe_clock_probe(samples, n: int, interval_ns: int, stream=None):
+    _check(_lib.moe_clock_probe(_ptr(samples), int(n), int(interval_ns), _stream(stream)), "moe_clock_probe")
 
 
 def moe_get_device_status(ws, stream=None) -> int:

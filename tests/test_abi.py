@@ -131,6 +131,14 @@ def test_fp8_entry_points_reject_bad_arguments_without_launch():
         assert e.value.code == moe.MOE_ERR_UNSUPPORTED
 
 
+def test_clock_probe_rejects_bad_arguments_without_launch():
+    A = 1 << 20
+    for args in ((None, 10, 1000), (A + 4, 10, 1000), (A, 1, 1000), (A, 10, 999), (A, 50002, 200_000)):
+        with pytest.raises(moe.MoeError) as e:
+            moe.moe_clock_probe(*args, 0)
+        assert e.value.code == moe.MOE_ERR_INVALID_ARG
+
+
 def test_expert_choice_config_sizes_the_workspace_for_N_times_C_rows():
     tc = moe.make_config(1000, 64, 16, 2, 128)
     ec = moe.make_config(1000, 64, 16, 1, 128, capacity=300, routing=moe.ROUTING_EXPERT_CHOICE)

@@ -5,6 +5,7 @@ shapes: the active FLOPs and algorithmic bytes of the Mixtral-shaped prefill and
 decode layers, the DeepSeek-V3-shaped layer with its shared expert, and one
 expert's bytes in bf16 and in FP8 with row scales.
 """
+import numpy as np
 import pytest
 
 import bench
@@ -125,3 +126,22 @@ def test_reference_arm_prints_the_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_probe_clock_median_inside_the_timed_region():
+    # samples every 200 us: 1500 MHz for the first 1 ms, then 2000 MHz; region of 1 ms
+    t = np.arange(11) * 200_000
+    c = np.concatenate([[0], np.cumsum(np.where(np.arange(1, 11) <= 5, 1500 * 200, 2000 * 200))])
+    s = np.stack([t + 10**9, c], axis=1).ravel()
+    r = bench.probe_clock(s, 1.0)
+    assert r["sm_mhz_in_band"] == pytest.approx(1500.0) and r["in_band_intervals"] == 5
+    r = bench.probe_clock(s, 2.0)
+    assert r["in_band_intervals"] == 10
+    assert bench.probe_clock(np.zeros(8, np.int64), 1.0) == {}
+
+
+def test_clock_norm_prefers_the_in_band_clock():
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1500.0, "sm_max_mhz": 2000.0}
+    clocks = {"sm_mhz": 2000.0, "sm_max_mhz": 2000.0, "sm_mhz_in_band": 1500.0}
+    r = bench.stage_roofline(3e12, 3e9, 2.0, peaks, clocks)
+    assert r["frac"] == pytest.approx(0.75) and r["frac_clock_norm"] == pytest.approx(1.0)
