@@ -32,6 +32,12 @@ extern "C" MOE_API int moe_clock_probe(uint64_t *samples, int n, int64_t interva
   if (!samples || (reinterpret_cast<uintptr_t>(samples) & 7) || n < 2 || n > (1 << 20) || interval_ns < 1000 ||
       (int64_t)(n - 1) * interval_ns > 10000000000ll)
     return MOE_ERR_INVALID_ARG;
+  // The SM hosting the probe must keep its whole shared memory available to the kernels
+  // it shares the SM with: a probe resident under a small-shared-memory carveout
+  // would keep a 200 KB CTA of another kernel off its SM until the probe ends.
+  if (cudaFuncSetAttribute(clock_probe_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    return MOE_ERR_CUDA;
   clock_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(samples, n, (uint64_t)interval_ns);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
