@@ -32,7 +32,7 @@ EXPORTS = ("moe_status_string", "moe_capacity", "moe_workspace_size", "moe_works
            "moe_load_stats", "moe_get_device_status", "moe_dispatch_noalloc", "moe_check_wait_timeout",
            "moe_router_zloss", "moe_bias_update", "moe_ec_route", "moe_seq_balance_loss",
            "moe_backward_workspace_size", "moe_layer_backward", "moe_quantize_fp8", "moe_expert_ffn_fp8",
-           "moe_layer_forward_fp8", "moe_clock_probe")
+           "moe_layer_forward_fp8", "moe_clock_probe", "moe_expert_ffn_gather")
 
 
 class MoeConfig(ctypes.Structure):
@@ -84,6 +84,7 @@ def _load():
         "moe_expert_ffn_fp8": [C] + [P] * 11,
         "moe_layer_forward_fp8": [C] + [P] * 16,
         "moe_clock_probe": [P, ctypes.c_int32, ctypes.c_int64, P],
+        "moe_expert_ffn_gather": [C, P, P, P, P, P, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -170,6 +171,12 @@ def moe_dispatch_noalloc(cfg, topk_idx, x, counts_routed, counts_kept, offsets, 
 def moe_expert_ffn(cfg, x_perm, offsets, w1, w3, w2, y_perm, ws, stream=None):
     _check(_lib.moe_expert_ffn(ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(w1), _ptr(w3), _ptr(w2),
                                _ptr(y_perm), _ptr(ws), _stream(stream)), "moe_expert_ffn")
+
+
+def moe_expert_ffn_gather(cfg, x, src_token, offsets, w1, w3, w2, y_perm, ws, stream=None):
+    _check(_lib.moe_expert_ffn_gather(ctypes.byref(cfg), _ptr(x), _ptr(src_token), _ptr(offsets), _ptr(w1),
+                                      _ptr(w3), _ptr(w2), _ptr(y_perm), _ptr(ws), _stream(stream)),
+           "moe_expert_ffn_gather")
 
 
 def moe_shared_ffn(cfg, x, sw1, sw3, sw2, y_shared, ws, stream=None):

@@ -152,15 +152,23 @@ int make_ws(const moe_config *c, void *ws, Ws *w) {
     if (rc_) return rc_;  \
   } while (0)
 
-int ffn_routed(const moe_config *c, const void *x_perm, const int32_t *offsets, const void *w1, const void *w3,
-               const void *w2, void *h, void *y_perm, int *status, cudaStream_t s) {
+// The routed experts.  bf16 with x and src_token given (x_perm null): the gate/up
+// GEMM gathers each row of its A operand from x (row src_token[r]) instead of
+// reading a permuted copy.
+int ffn_routed(const moe_config *c, const void *x_perm, const void *x, const int32_t *src_token,
+               const int32_t *offsets, const void *w1, const void *w3, const void *w2, void *h, void *y_perm,
+               int *status, cudaStream_t s) {
   const int64_t rows = routed_rows(c);
   const int mode1 = c->act == MOE_ACT_SWIGLU ? 0 : 1;
   if (is_bf16(c)) {
     // expert choice gives every group exactly C rows: no capacity skew
     const bool pair = use_pair_tiles(rows, c->N, is_ec(c) ? 0 : c->capacity);
-    MOE_TRY(tc_grouped_gemm(mode1, x_perm, rows, c->d, w1, w3, (int64_t)c->N * c->ffn, c->ffn, offsets, c->N, 0,
-                            c->ffn, h, status, pair, s));
+    if (x_perm)
+      MOE_TRY(tc_grouped_gemm(mode1, x_perm, rows, c->d, w1, w3, (int64_t)c->N * c->ffn, c->ffn, offsets, c->N, 0,
+                              c->ffn, h, status, pair, s));
+    else
+      MOE_TRY(tc_grouped_gemm_gather(mode1, x, c->T, src_token, rows, c->d, w1, w3, (int64_t)c->N * c->ffn, c->ffn,
+                                     offsets, c->N, c->ffn, h, status, pair, s));
     MOE_TRY(tc_grouped_gemm(2, h, rows, c->ffn, w2, nullptr, (int64_t)c->N * c->d, c->d, offsets, c->N, 0, c->d,
                             y_perm, status, pair, s));
   } else {
@@ -437,11 +445,11 @@ int moe_dispatch(const moe_config *cfg, const int32_t *topk_idx, const void *x, 
   Ws w;
   MOE_TRY(make_ws(cfg, ws, &w));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cfg->T > 0 && (!topk_idx || !x || !dest_row || !src_token || !x_perm || !aligned16(x) || !aligned16(x_perm)))
+  if (cfg->T > 0 && (!topk_idx || !dest_row || !src_token || (x_perm && (!x || !aligned16(x) || !aligned16(x_perm)))))
     return MOE_ERR_INVALID_ARG;
   MOE_TRY(launch_dispatch(topk_idx, cfg->T, cfg->k, cfg->N, cfg->capacity, w.hist(), w.chunk_base(cfg), counts_routed,
                           counts_kept, offsets, dest_row, src_token, w.status(), s));
-  if (cfg->T == 0) return MOE_OK;
+  if (cfg->T == 0 || !x_perm) return MOE_OK;  // no permuted copy asked for
   return launch_scatter_rows(x, dest_row, cfg->T, cfg->k, (int)(cfg->d * esize(cfg)), x_perm, s);
 }
 
@@ -453,7 +461,20 @@ int moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int32_t *off
   if (!weights_ok(cfg, w1, w3, w2)) return MOE_ERR_INVALID_ARG;
   Ws w;
   MOE_TRY(make_ws(cfg, ws, &w));
-  return ffn_routed(cfg, x_perm, offsets, w1, w3, w2, w.at<void>(w.L.h), y_perm, w.status(),
+  return ffn_routed(cfg, x_perm, nullptr, nullptr, offsets, w1, w3, w2, w.at<void>(w.L.h), y_perm, w.status(),
+                    static_cast<cudaStream_t>(stream));
+}
+
+int moe_expert_ffn_gather(const moe_config *cfg, const void *x, const int32_t *src_token, const int32_t *offsets,
+                          const void *w1, const void *w3, const void *w2, void *y_perm, void *ws, void *stream) {
+  MOE_TRY(check_config(cfg));
+  if (!is_bf16(cfg)) return MOE_ERR_UNSUPPORTED;
+  if (cfg->T == 0) return MOE_OK;
+  if (!x || !src_token || !offsets || !y_perm || !aligned16(x) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(cfg, w1, w3, w2)) return MOE_ERR_INVALID_ARG;
+  Ws w;
+  MOE_TRY(make_ws(cfg, ws, &w));
+  return ffn_routed(cfg, nullptr, x, src_token, offsets, w1, w3, w2, w.at<void>(w.L.h), y_perm, w.status(),
                     static_cast<cudaStream_t>(stream));
 }
 
@@ -517,15 +538,21 @@ int layer_forward_impl(const moe_config *cfg, const void *x, const float *Wg, co
                             w.at<int32_t>(L.counts_routed), w.at<int32_t>(L.counts_kept), offsets, dest_row,
                             src_token, w.status(), s));
   }
-  if (is_ec(cfg))
-    MOE_TRY(launch_gather_rows(x, src_token, offsets + cfg->N, routed_rows(cfg), (int)(cfg->d * esize(cfg)), x_perm,
-                               s));
-  else
-    MOE_TRY(launch_scatter_rows(x, dest_row, cfg->T, cfg->k, (int)(cfg->d * esize(cfg)), x_perm, s));
+  // bf16 experts gather their token rows from x; FP8 and float32 experts read a permuted copy
+  const bool gathered = !f8 && is_bf16(cfg);
+  if (!gathered) {
+    if (is_ec(cfg))
+      MOE_TRY(launch_gather_rows(x, src_token, offsets + cfg->N, routed_rows(cfg), (int)(cfg->d * esize(cfg)), x_perm,
+                                 s));
+    else
+      MOE_TRY(launch_scatter_rows(x, dest_row, cfg->T, cfg->k, (int)(cfg->d * esize(cfg)), x_perm, s));
+  }
   if (f8)
     MOE_TRY(ffn_routed_fp8(cfg, w, x_perm, offsets, *f8, w.at<void>(L.h), y_perm, s));
+  else if (gathered)
+    MOE_TRY(ffn_routed(cfg, nullptr, x, src_token, offsets, w1, w3, w2, w.at<void>(L.h), y_perm, w.status(), s));
   else
-    MOE_TRY(ffn_routed(cfg, x_perm, offsets, w1, w3, w2, w.at<void>(L.h), y_perm, w.status(), s));
+    MOE_TRY(ffn_routed(cfg, x_perm, nullptr, nullptr, offsets, w1, w3, w2, w.at<void>(L.h), y_perm, w.status(), s));
   void *y_sh = nullptr;
   if (shared) {
     y_sh = w.at<void>(L.y_shared);
@@ -673,7 +700,9 @@ int moe_layer_backward(const moe_config *cfg, const void *x, const float *Wg, co
     MOE_TRY(tc_wgrad_gemm(x, d, bws + L.dz2, 2 * Np, T, nullptr, 1, d, 2 * Np, part, w.status(), s));
     MOE_TRY(launch_dwg_sum(part, d, N, Np, dWg, s));
   }
-  // routed experts
+  // routed experts: their input rows in expert order (the forward gathered them from x
+  // without writing the permuted copy, which the recompute and dW1 / dW3 read here)
+  MOE_TRY(launch_scatter_rows(x, dest_row, T, k, d * 2, w.at<void>(FL.x_perm), s));
   MOE_TRY(ffn_backward(cfg, false, N, R, offsets, offsets, w.at<void>(FL.x_perm), w.at<void>(FL.h), bws + L.dy, w1, w3,
                        w2, cfg->ffn, bws, L, dw1, dw3, dw2, bws + L.dxp, w.status(), s));
   // the shared expert: one group of all T rows, dy = dout

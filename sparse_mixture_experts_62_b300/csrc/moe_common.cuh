@@ -124,6 +124,20 @@ MOE_DEV void tma_load_3d(void *smem_dst, const CUtensorMap *m, uint64_t *bar, in
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 only (cp.async.cg); with
+// bytes = 0 nothing is read and the 16 bytes are zero-filled.
+MOE_DEV void cp_async_16(uint32_t saddr, const void *gptr, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(gptr), "r"(bytes) : "memory");
+}
+MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+MOE_DEV void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Orders this thread's earlier generic-proxy accesses to shared memory (cp.async
+// writes included, once complete) before later async-proxy accesses (TMA, MMA).
+MOE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor for a K-major operand tile stored in the
 // 128-byte swizzled layout that TMA writes with CU_TENSOR_MAP_SWIZZLE_128B:

@@ -92,6 +92,11 @@ struct Args {
   int32_t kb1;         // kDualBT: K blocks taken from the first (A, B) pair
   int32_t out_stride;  // elements between output rows
   const uint16_t *dh;  // kSwiGLUBwd / kReLUBwd: [rows, n_out] bf16 gradient of h
+  // Gathered A (forward modes): row r of A is row src[r] of gx [gx_rows, K] instead
+  // of row r of the A tensor map; null: A through its tensor map.
+  const uint16_t *gx;
+  const int32_t *gsrc;
+  int32_t gx_rows;
 };
 
 __device__ __forceinline__ float silu(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
@@ -235,9 +240,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_tiles = (args.n_out + OUT_COLS - 1) / OUT_COLS;
   const int num_kb = args.num_kb;
 
+  // gathered A: the producer warp's 32 lanes copy the token rows with cp.async and
+  // each arrives on the stage's full barrier (besides lane 0's expected bytes)
+  const bool gather = swappable(MODE) && args.gx != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], gather ? 33 : 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -275,7 +283,100 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t tmem_base = *tmem_slot;
   const int total_tiles = tile_start[G];
 
-  if (warp == 0) {
+  if (warp == 0 && gather) {
+    // ------------------------------------------------------------ producer, gathered A
+    // Lane 0 loads the B tile by TMA; every lane copies 4 rows x 8 16-byte chunks of
+    // the A tile with cp.async into the 128-byte-swizzled layout the MMA reads
+    // (chunk c of row i at i * 128 + (c ^ (i % 8)) * 16).  A stage's copies are
+    // signalled (fence to the async proxy, then an arrival) STAGES - 1 stages later,
+    // once cp.async.wait_group shows them complete, so the copies of STAGES stages
+    // are in flight together.
+    constexpr int LAG = STAGES - 1;
+    const int dchunks = args.K / 8;  // 16-byte chunks per row of x
+    int pend[STAGES] = {};           // stages issued but not yet signalled, oldest first
+    int npend = 0;
+    int issued_parity[STAGES];
+    for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+    int stage = 0;
+    uint32_t phase = 0;
+    int g = 0;
+    bool ok = true;
+    auto signal_oldest = [&]() {
+      fence_proxy_async_smem();
+      mbar_arrive(&full[pend[0]]);
+      for (int q = 1; q < npend; ++q) pend[q - 1] = pend[q];
+      --npend;
+    };
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      while (tile >= tile_start[g + 1]) ++g;
+      const int local = tile - tile_start[g];
+      const int n_tile = local / mtiles[g];
+      const int m_tile = local - n_tile * mtiles[g];
+      const int a_row = rowbeg[g] + m_tile * BM;
+      const int b_row = g * args.b_rows + n_tile * OUT_COLS;
+      const uint16_t *src_row[4];
+      bool valid[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = a_row + lane + 32 * j;
+        int t = -1;
+        if (r < rowend[g]) {
+          t = args.gsrc[r];
+          if (t < 0 || t >= args.gx_rows) {  // an index past x: zeros, flagged
+            set_status(args.status, MOE_ERR_BOUNDS);
+            t = -1;
+          }
+        }
+        valid[j] = t >= 0;
+        src_row[j] = args.gx + (size_t)(t >= 0 ? t : 0) * args.K;
+      }
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, args.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t *sa = smem + stage * STAGE_BYTES;
+        uint8_t *sb = sa + A_BYTES;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)B_BYTES);
+          tma_load_2d(sb, &tmB0, &full[stage], kb * BK, b_row);
+          if (paired_b(MODE))
+            tma_load_2d(sb + B_BYTES / 2, &tmB1, &full[stage], kb * BK, b_row);
+          else
+            tma_load_2d(sb + B_BYTES / 2, &tmB0, &full[stage], kb * BK, b_row + BN / 2);
+        }
+        const uint32_t sa32 = smem_u32(sa);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = lane + 32 * j;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int chunk = kb * 8 + c;
+            const bool v = valid[j] && chunk < dchunks;
+            cp_async_16(sa32 + (uint32_t)(i * 128 + ((c ^ (i & 7)) << 4)), v ? src_row[j] + chunk * 8 : args.gx,
+                        v ? 16u : 0u);
+          }
+        }
+        cp_async_commit();
+        pend[npend++] = stage;
+        issued_parity[stage] = (int)phase;
+        if (npend > LAG) {
+          cp_async_wait_group<LAG>();
+          signal_oldest();
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    cp_async_wait_group<0>();
+    while (npend > 0) signal_oldest();
+    // never leave the CTA with a bulk copy still writing its shared memory
+    if (lane == 0)
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_parity[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_parity[s], args.status);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int issued_parity[STAGES];
@@ -476,9 +577,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_tiles = (args.n_out + OUT_COLS - 1) / OUT_COLS;
   const int num_kb = args.num_kb;
 
+  // gathered A: each CTA's producer warp copies its 128 token rows with cp.async and
+  // its 32 lanes arrive on the leader's full barrier (besides the expected bytes)
+  const bool gather = swappable(MODE) && args.gx != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], gather ? 65 : 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -519,7 +623,96 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t full_lead = mapa_shared(smem_u32(&full[0]), 0);
   const uint32_t tempty_lead = mapa_shared(smem_u32(&tempty[0]), 0);
 
-  if (warp == 0) {
+  if (warp == 0 && gather) {
+    // ------------------------------------------------------------ producer, gathered A (both CTAs)
+    // As in the single-CTA form: lane 0 loads this CTA's half of B by TMA onto the
+    // leader's full barrier; the 32 lanes copy this CTA's 128 token rows with
+    // cp.async and, STAGES - 1 stages later, fence and arrive on the leader's full
+    // barrier (an arrival with cluster-scope release).
+    constexpr int LAG = STAGES - 1;
+    const int dchunks = args.K / 8;
+    int pend[STAGES] = {};
+    int npend = 0;
+    int issued_parity[STAGES];
+    for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
+    int stage = 0;
+    uint32_t phase = 0;
+    int g = 0;
+    bool ok = true;
+    const CUtensorMap *mb = (paired_b(MODE) && rank == 1) ? &tmB1 : &tmB0;
+    auto signal_oldest = [&]() {
+      fence_proxy_async_smem();
+      mbar_arrive_cluster(full_lead + 8u * (uint32_t)pend[0]);
+      for (int q = 1; q < npend; ++q) pend[q - 1] = pend[q];
+      --npend;
+    };
+    for (int tile = pair_id; tile < total_tiles && ok; tile += npairs) {
+      while (tile >= tile_start[g + 1]) ++g;
+      const int local = tile - tile_start[g];
+      const int n_tile = local / mtiles[g];
+      const int m_tile = local - n_tile * mtiles[g];
+      const int a_row = rowbeg[g] + m_tile * 2 * BM + (int)rank * BM;
+      const int b_row = paired_b(MODE) ? g * args.b_rows + n_tile * OUT_COLS
+                                       : g * args.b_rows + n_tile * OUT_COLS + (int)rank * 128;
+      const uint16_t *src_row[4];
+      bool valid[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = a_row + lane + 32 * j;
+        int t = -1;
+        if (r < rowend[g]) {
+          t = args.gsrc[r];
+          if (t < 0 || t >= args.gx_rows) {  // an index past x: zeros, flagged
+            set_status(args.status, MOE_ERR_BOUNDS);
+            t = -1;
+          }
+        }
+        valid[j] = t >= 0;
+        src_row[j] = args.gx + (size_t)(t >= 0 ? t : 0) * args.K;
+      }
+      for (int kb = 0; kb < num_kb; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, args.status)) {
+          ok = false;
+          break;
+        }
+        uint8_t *sa = smem + stage * STAGE_BYTES;
+        const uint32_t fb = full_lead + 8u * stage;
+        if (lane == 0) {
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)pair::BH_BYTES);
+          tma_load_2d_pair(sa + A_BYTES, mb, fb, kb * BK, b_row);
+        }
+        const uint32_t sa32 = smem_u32(sa);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = lane + 32 * j;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const int chunk = kb * 8 + c;
+            const bool v = valid[j] && chunk < dchunks;
+            cp_async_16(sa32 + (uint32_t)(i * 128 + ((c ^ (i & 7)) << 4)), v ? src_row[j] + chunk * 8 : args.gx,
+                        v ? 16u : 0u);
+          }
+        }
+        cp_async_commit();
+        pend[npend++] = stage;
+        issued_parity[stage] = (int)phase;
+        if (npend > LAG) {
+          cp_async_wait_group<LAG>();
+          signal_oldest();
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    cp_async_wait_group<0>();
+    while (npend > 0) signal_oldest();
+    // the leader's full barriers count both CTAs' copies: wait for the last ones
+    if (leader && lane == 0)
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_parity[s] >= 0) mbar_wait_cluster(&full[s], (uint32_t)issued_parity[s], args.status);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       int issued_parity[STAGES];
@@ -583,7 +776,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, args.status)) {
+          if (!(gather ? mbar_wait_cluster(&full[stage], phase, args.status)
+                      : mbar_wait(&full[stage], phase, args.status))) {
             ok = false;
             break;
           }
@@ -824,6 +1018,38 @@ int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *
   const int num_kb = (K + BK - 1) / BK;
   Args args{offsets, G, M, (int32_t)a_rows, n_out, K, b_rows_per_group, static_cast<uint16_t *>(out), status,
             num_kb, num_kb, n_out, nullptr};
+  return launch_mode(mode, ma, ma, mb0, mb1, args, dev, sms, pair_tiles, stream);
+}
+
+int tc_grouped_gemm_gather(int mode, const void *x, int64_t x_rows, const int32_t *src_token, int64_t rows, int K,
+                           const void *B0, const void *B1, int64_t b_rows_total, int b_rows_per_group,
+                           const int32_t *offsets, int G, int n_out, void *out, int *status, bool pair_tiles,
+                           cudaStream_t stream) {
+  using namespace tc;
+  if (G < 1 || G > MAX_GROUPS || K < 1 || n_out < 1 || rows < 1 || x_rows < 1 || b_rows_total < 1 || !src_token ||
+      !offsets)
+    return MOE_ERR_INVALID_ARG;
+  if (rows > INT32_MAX || x_rows > INT32_MAX || n_out > b_rows_per_group ||
+      (int64_t)G * b_rows_per_group > b_rows_total)
+    return MOE_ERR_INVALID_ARG;
+  if (mode < kSwiGLU || mode > kPlain || (mode == kSwiGLU && !B1)) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x) & 15) || K % 8) return MOE_ERR_UNSUPPORTED;
+  CUtensorMap ma, mb0, mb1;
+  int rc;
+  if ((rc = make_map(&ma, x, (uint64_t)x_rows, (uint64_t)K))) return rc;  // not read: A is gathered
+  if ((rc = make_map(&mb0, B0, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
+  if (mode == kSwiGLU) {
+    if ((rc = make_map(&mb1, B1, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
+  } else {
+    mb1 = mb0;
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  const int sms = device_sm_count(dev);
+  if (sms <= 0) return MOE_ERR_CUDA;
+  const int num_kb = (K + BK - 1) / BK;
+  Args args{offsets, G, 0, (int32_t)rows, n_out, K, b_rows_per_group, static_cast<uint16_t *>(out), status,
+            num_kb, num_kb, n_out, nullptr, static_cast<const uint16_t *>(x), src_token, (int32_t)x_rows};
   return launch_mode(mode, ma, ma, mb0, mb1, args, dev, sms, pair_tiles, stream);
 }
 

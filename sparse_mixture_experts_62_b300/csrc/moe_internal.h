@@ -39,6 +39,11 @@ int launch_gather_rows(const void *x, const int32_t *src_token, const int32_t *o
 int tc_grouped_gemm(int mode, const void *A, int64_t a_rows, int K, const void *B0, const void *B1,
                     int64_t b_rows_total, int b_rows_per_group, const int32_t *offsets, int G, int M, int n_out,
                     void *out, int *status, bool pair_tiles, cudaStream_t stream);
+// the same with A gathered: row r of A is row src_token[r] of x [x_rows, K] (forward modes)
+int tc_grouped_gemm_gather(int mode, const void *x, int64_t x_rows, const int32_t *src_token, int64_t rows, int K,
+                           const void *B0, const void *B1, int64_t b_rows_total, int b_rows_per_group,
+                           const int32_t *offsets, int G, int n_out, void *out, int *status, bool pair_tiles,
+                           cudaStream_t stream);
 // The forward GEMM (modes 0-2) with FP8 E4M3 weights Q [G * b_rows, K] bytes and
 // per-row float32 scales S [G * b_rows]: out = EPI(S[n] * sum_k A[r, k] Q[n, k]).
 // FP8 expert FFN: the two GEMMs for groups of any size, with tokens on the M side.

@@ -54,6 +54,59 @@ def _expert_ffn_case(N, counts, d, F, act, seed):
         assert_close_out(y[r0:r1], ref, "bf16", what=f"expert {e}")
 
 
+def _gather_case(N, counts, T, d, F, act, seed, bad_row=None):
+    """moe_expert_ffn_gather against the oracle's expert FFN on the gathered rows
+    x[src_token[r]] (src_token drawn with repeats); with bad_row, that entry of
+    src_token points past x: the row reads zeros and MOE_ERR_BOUNDS is recorded."""
+    rows = int(sum(counts))
+    cfg = moe.make_config(T, d, N, 1, F, 0, moe.GATE_SOFTMAX_TOPK,
+                          moe.ACT_SWIGLU if act == "swiglu" else moe.ACT_RELU, moe.DTYPE_BF16, 0)
+    # the workspace and the row bound follow T * k routed rows: give T * k >= rows
+    assert rows <= T
+    x = _rand_bf16((T, d), seed)
+    src = np.random.default_rng(seed).integers(0, T, rows).astype(np.int32)
+    if bad_row is not None:
+        src[bad_row] = T + 5
+    w1 = synth.normal(seed, 3, (N, F, d), d ** -0.5, "bf16")
+    w3 = synth.normal(seed, 4, (N, F, d), d ** -0.5, "bf16") if act == "swiglu" else None
+    w2 = synth.normal(seed, 5, (N, d, F), F ** -0.5, "bf16")
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    ws = _ws(cfg)
+    y = torch.full((T, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    moe.moe_expert_ffn_gather(cfg, to_dev(x, BF16), torch.from_numpy(src).cuda(), torch.from_numpy(offsets).cuda(),
+                              to_dev(w1, BF16), to_dev(w3, BF16), to_dev(w2, BF16), y, ws)
+    status = moe.moe_get_device_status(ws)
+    assert status == (moe.MOE_OK if bad_row is None else moe.MOE_ERR_BOUNDS)
+    y = to_np_f64(y)
+    x64 = oracle.widen(x, "bf16")
+    xg = np.where((src < T)[:, None], x64[np.minimum(src, T - 1)], 0.0)
+    for e in range(N):
+        r0, r1 = offsets[e], offsets[e + 1]
+        if r1 == r0:
+            continue
+        ref = oracle.expert_ffn(xg[r0:r1], oracle.widen(w1[e], "bf16"),
+                                oracle.widen(w3[e], "bf16") if w3 is not None else None,
+                                oracle.widen(w2[e], "bf16"), act)
+        assert_close_out(y[r0:r1], ref, "bf16", what=f"expert {e}")
+
+
+@pytest.mark.parametrize("act", ["swiglu", "relu"])
+def test_gathered_ffn_single_ctas(act):
+    """Rows gathered from x by index: ragged width (d = 192: the last k-block holds
+    24 of its 64 columns), empty, one-row, swapped and multi-tile groups."""
+    _gather_case(5, [0, 1, 130, 257, 64], T=600, d=192, F=320, act=act, seed=8)
+
+
+@pytest.mark.parametrize("act", ["swiglu", "relu"])
+def test_gathered_ffn_pair_tiles(act):
+    """Groups averaging >= 512 rows (CTA pairs): both CTAs of a pair gather their rows."""
+    _gather_case(3, [600, 1100, 301], T=2100, d=320, F=520, act=act, seed=9)
+
+
+def test_gathered_ffn_flags_a_row_index_past_x():
+    _gather_case(2, [70, 90], T=200, d=128, F=128, act="swiglu", seed=10, bad_row=75)
+
+
 def test_tc_gemm_single_tile():
     """One expert, 128 rows, K = 64: a single tile and a single K block."""
     _expert_ffn_case(1, [128], d=64, F=128, act="swiglu", seed=1)
