@@ -108,22 +108,18 @@ def stage_work(wl, kept_rows: int, touched: int, fp8: bool = False) -> dict:
     """Algorithmic (flops, bytes) per stage of one layer step.
 
     route: x read once, W_g, logits written, top-k ids + weights written;
-    dispatch: ids read, index arrays (and, without gathered bf16 experts, x rows read
-      once and x_perm written);
-    expert_ffn: kept rows' FLOPs; weights of touched experts, y_perm written, and the
-      input rows: x read once (bf16, gathered by row index) or x_perm;
+    dispatch: ids read, x rows read once, x_perm written, index arrays;
+    expert_ffn: kept rows' FLOPs; weights of touched experts, x_perm read, y_perm written;
     shared_ffn: every token; its weights, x read, y written;
     combine: y_perm (+ shared y) read, out written, ids + weights read;
     load_stats: logits and counts read."""
     es = 2 if wl.dtype == "bf16" else 4
     mats = 3 if wl.act == "swiglu" else 2
     T, d, N, k, F, S = wl.T, wl.d, wl.N, wl.k, wl.F, kept_rows
-    gathered = wl.dtype == "bf16" and not fp8  # bf16 experts read x by row index: no x_perm
     w = {
         "route": (2.0 * T * d * N, T * d * es + d * N * 4 + T * N * 4 + T * k * 8),
-        "dispatch": (0.0, T * k * 4 + T * k * 4 + S * 4 + 3 * N * 4 + (0 if gathered else T * d * es + S * d * es)),
-        "expert_ffn": (2.0 * S * d * F * mats, touched * expert_weight_bytes(wl, fp8) + S * d * es +
-                       (min(T, S) * d * es if gathered else S * d * es)),
+        "dispatch": (0.0, T * k * 4 + T * d * es + S * d * es + T * k * 4 + S * 4 + 3 * N * 4),
+        "expert_ffn": (2.0 * S * d * F * mats, touched * expert_weight_bytes(wl, fp8) + 2 * S * d * es),
         "combine": (0.0, S * d * es + T * d * es + T * k * 8 + (T * d * es if wl.shared_F else 0)),
         "load_stats": (0.0, T * N * 4 + 2 * N * 4),
     }
@@ -381,19 +377,13 @@ def layer_stages(moe, layer, x, out, stats, wl):
         moe.moe_route(cfg, x, layer.Wg, layer.logit_bias, layer.sel_bias, v["logits"], v["topk_idx"], v["topk_w"],
                       ws, cur())
 
-    # as moe_layer_forward: bf16 experts gather their rows from x (no permuted copy)
-    gathered = wl.dtype == "bf16" and layer.fp8 is None
-
     def dispatch():
         moe.moe_dispatch(cfg, v["topk_idx"], x, v["counts_routed"], v["counts_kept"], v["offsets"], v["dest_row"],
-                         v["src_token"], None if gathered else v["x_perm"], ws, cur())
+                         v["src_token"], v["x_perm"], ws, cur())
 
     def expert_ffn():
         if layer.fp8 is not None:
             moe.moe_expert_ffn_fp8(cfg, v["x_perm"], v["offsets"], *layer.fp8, v["y_perm"], ws, cur())
-        elif gathered:
-            moe.moe_expert_ffn_gather(cfg, x, v["src_token"], v["offsets"], layer.w1, layer.w3, layer.w2,
-                                      v["y_perm"], ws, cur())
         else:
             moe.moe_expert_ffn(cfg, v["x_perm"], v["offsets"], layer.w1, layer.w3, layer.w2, v["y_perm"], ws, cur())
 

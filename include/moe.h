@@ -152,7 +152,8 @@ MOE_API int moe_route(const moe_config *cfg, const void *x, const float *Wg, con
  * dest_row[t, j] = that row or -1 (dropped); src_token[row] = t; and
  * x_perm[row, :] = x[t, :].  x_perm needs room for T * k rows; rows at or
  * beyond offsets[N] are left untouched.  x_perm may be NULL: then the permuted
- * copy is not made (x is not read; moe_expert_ffn_gather reads x by src_token).  A token picks an expert at most once:
+ * copy is not made (x is not read; moe_expert_ffn_gather reads x by src_token).
+ * A token picks an expert at most once:
  * an id in topk_idx outside [0, N) is skipped and sets MOE_ERR_BOUNDS, an id that
  * repeats an earlier slot of the same token is skipped (not counted, dest_row
  * -1) and sets MOE_ERR_INVALID_ARG, both in the device status word.  Token-choice
@@ -195,9 +196,13 @@ MOE_API int moe_expert_ffn(const moe_config *cfg, const void *x_perm, const int3
 /* moe_expert_ffn reading its input rows straight from x: row r of expert e's
  * group (offsets[e] <= r < offsets[e+1]) is x[src_token[r], :], as moe_dispatch
  * would have copied it into x_perm; y_perm as moe_expert_ffn.  bf16 configs only
- * (MOE_ERR_UNSUPPORTED otherwise).  A src_token entry outside [0, T) reads zeros and
- * sets MOE_ERR_BOUNDS in the device status word.  moe_layer_forward runs its bf16
- * experts this way and never writes x_perm. */
+ * (MOE_ERR_UNSUPPORTED otherwise).  The rows are fetched by TMA row gathers
+ * (four indexed rows of x per copy) straight into the tensor cores' operand tiles.
+ * A src_token entry outside [0, T) sets MOE_ERR_BOUNDS in the device status word;
+ * that row's output is then unspecified (the other rows are unaffected).  It
+ * needs no x_perm buffer, at a cost: every N tile of the gate/up GEMM re-gathers
+ * its rows, four per TMA instruction, and on large groups that instruction rate
+ * limits the GEMM (moe_layer_forward copies x into x_perm once instead). */
 MOE_API int moe_expert_ffn_gather(const moe_config *cfg, const void *x, const int32_t *src_token,
                                   const int32_t *offsets, const void *w1, const void *w3, const void *w2,
                                   void *y_perm, void *ws, void *stream);

@@ -538,19 +538,15 @@ int layer_forward_impl(const moe_config *cfg, const void *x, const float *Wg, co
                             w.at<int32_t>(L.counts_routed), w.at<int32_t>(L.counts_kept), offsets, dest_row,
                             src_token, w.status(), s));
   }
-  // bf16 experts gather their token rows from x; FP8 and float32 experts read a permuted copy
-  const bool gathered = !f8 && is_bf16(cfg);
-  if (!gathered) {
-    if (is_ec(cfg))
-      MOE_TRY(launch_gather_rows(x, src_token, offsets + cfg->N, routed_rows(cfg), (int)(cfg->d * esize(cfg)), x_perm,
-                                 s));
-    else
-      MOE_TRY(launch_scatter_rows(x, dest_row, cfg->T, cfg->k, (int)(cfg->d * esize(cfg)), x_perm, s));
-  }
+  // the experts read a permuted copy of x: one coalesced pass here costs far less than
+  // gathering rows into the GEMM's operand tiles, which re-fetch them once per N tile
+  if (is_ec(cfg))
+    MOE_TRY(launch_gather_rows(x, src_token, offsets + cfg->N, routed_rows(cfg), (int)(cfg->d * esize(cfg)), x_perm,
+                               s));
+  else
+    MOE_TRY(launch_scatter_rows(x, dest_row, cfg->T, cfg->k, (int)(cfg->d * esize(cfg)), x_perm, s));
   if (f8)
     MOE_TRY(ffn_routed_fp8(cfg, w, x_perm, offsets, *f8, w.at<void>(L.h), y_perm, s));
-  else if (gathered)
-    MOE_TRY(ffn_routed(cfg, nullptr, x, src_token, offsets, w1, w3, w2, w.at<void>(L.h), y_perm, w.status(), s));
   else
     MOE_TRY(ffn_routed(cfg, x_perm, nullptr, nullptr, offsets, w1, w3, w2, w.at<void>(L.h), y_perm, w.status(), s));
   void *y_sh = nullptr;
@@ -700,9 +696,7 @@ int moe_layer_backward(const moe_config *cfg, const void *x, const float *Wg, co
     MOE_TRY(tc_wgrad_gemm(x, d, bws + L.dz2, 2 * Np, T, nullptr, 1, d, 2 * Np, part, w.status(), s));
     MOE_TRY(launch_dwg_sum(part, d, N, Np, dWg, s));
   }
-  // routed experts: their input rows in expert order (the forward gathered them from x
-  // without writing the permuted copy, which the recompute and dW1 / dW3 read here)
-  MOE_TRY(launch_scatter_rows(x, dest_row, T, k, d * 2, w.at<void>(FL.x_perm), s));
+  // routed experts
   MOE_TRY(ffn_backward(cfg, false, N, R, offsets, offsets, w.at<void>(FL.x_perm), w.at<void>(FL.h), bws + L.dy, w1, w3,
                        w2, cfg->ffn, bws, L, dw1, dw3, dw2, bws + L.dxp, w.status(), s));
   // the shared expert: one group of all T rows, dy = dout

@@ -124,19 +124,18 @@ MOE_DEV void tma_load_3d(void *smem_dst, const CUtensorMap *m, uint64_t *bar, in
       : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared through L2 only (cp.async.cg); with
-// bytes = 0 nothing is read and the 16 bytes are zero-filled.
-MOE_DEV void cp_async_16(uint32_t saddr, const void *gptr, uint32_t bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(gptr), "r"(bytes) : "memory");
+// Row gather (tile::gather4): four rows r0..r3 of a 2-D map whose box is one row
+// high, each `box columns` wide from column c0, land as four consecutive box rows
+// at smem_dst (the map's swizzle applied as for a tiled load).  c0 * element_size
+// is a multiple of 16 bytes; the rows are in range (callers clamp them).
+MOE_DEV void tma_gather4(void *smem_dst, const CUtensorMap *m, uint64_t *bar, int32_t c0, int32_t r0, int32_t r1,
+                         int32_t r2, int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
 }
-MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-MOE_DEV void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// Orders this thread's earlier generic-proxy accesses to shared memory (cp.async
-// writes included, once complete) before later async-proxy accesses (TMA, MMA).
-MOE_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // ---------------------------------------------------------------- tcgen05
 // Shared-memory matrix descriptor for a K-major operand tile stored in the
@@ -260,6 +259,14 @@ MOE_DEV void tma_load_2d_pair(void *smem_dst, const CUtensorMap *m, uint32_t mba
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::
           "r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(mbar_caddr), "r"(c0), "r"(c1)
+      : "memory");
+}
+MOE_DEV void tma_gather4_pair(void *smem_dst, const CUtensorMap *m, uint32_t mbar_caddr, int32_t c0, int32_t r0,
+                              int32_t r1, int32_t r2, int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(mbar_caddr), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
 MOE_DEV void tma_load_3d_pair(void *smem_dst, const CUtensorMap *m, uint32_t mbar_caddr, int32_t c0, int32_t c1,

@@ -240,12 +240,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_tiles = (args.n_out + OUT_COLS - 1) / OUT_COLS;
   const int num_kb = args.num_kb;
 
-  // gathered A: the producer warp's 32 lanes copy the token rows with cp.async and
-  // each arrives on the stage's full barrier (besides lane 0's expected bytes)
+  // gathered A: the A tensor map is a one-row-high map over x, read by TMA row
+  // gathers (see the producer below)
   const bool gather = swappable(MODE) && args.gx != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], gather ? 33 : 1);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -285,28 +285,17 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0 && gather) {
     // ------------------------------------------------------------ producer, gathered A
-    // Lane 0 loads the B tile by TMA; every lane copies 4 rows x 8 16-byte chunks of
-    // the A tile with cp.async into the 128-byte-swizzled layout the MMA reads
-    // (chunk c of row i at i * 128 + (c ^ (i % 8)) * 16).  A stage's copies are
-    // signalled (fence to the async proxy, then an arrival) STAGES - 1 stages later,
-    // once cp.async.wait_group shows them complete, so the copies of STAGES stages
-    // are in flight together.
-    constexpr int LAG = STAGES - 1;
-    const int dchunks = args.K / 8;  // 16-byte chunks per row of x
-    int pend[STAGES] = {};           // stages issued but not yet signalled, oldest first
-    int npend = 0;
+    // Lane 0 waits for the stage, sets its expected bytes (A and B, as for tiled
+    // loads) and loads the B tile; then each of the 32 lanes loads rows 4 * lane ..
+    // 4 * lane + 3 of the A tile with one TMA row gather: x's rows src[r] for the
+    // tile's rows r, 64 columns each, into the 128-byte-swizzled tile.  Rows past
+    // the group's end (not stored) and indices past x (flagged) read row 0 of x.
     int issued_parity[STAGES];
     for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
     int stage = 0;
     uint32_t phase = 0;
     int g = 0;
     bool ok = true;
-    auto signal_oldest = [&]() {
-      fence_proxy_async_smem();
-      mbar_arrive(&full[pend[0]]);
-      for (int q = 1; q < npend; ++q) pend[q - 1] = pend[q];
-      --npend;
-    };
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
       while (tile >= tile_start[g + 1]) ++g;
       const int local = tile - tile_start[g];
@@ -314,64 +303,46 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int m_tile = local - n_tile * mtiles[g];
       const int a_row = rowbeg[g] + m_tile * BM;
       const int b_row = g * args.b_rows + n_tile * OUT_COLS;
-      const uint16_t *src_row[4];
-      bool valid[4];
+      int t[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int r = a_row + lane + 32 * j;
-        int t = -1;
+        const int r = a_row + 4 * lane + j;
+        t[j] = 0;
         if (r < rowend[g]) {
-          t = args.gsrc[r];
-          if (t < 0 || t >= args.gx_rows) {  // an index past x: zeros, flagged
+          const int v = args.gsrc[r];
+          if (v < 0 || v >= args.gx_rows)
             set_status(args.status, MOE_ERR_BOUNDS);
-            t = -1;
-          }
+          else
+            t[j] = v;
         }
-        valid[j] = t >= 0;
-        src_row[j] = args.gx + (size_t)(t >= 0 ? t : 0) * args.K;
       }
       for (int kb = 0; kb < num_kb; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, args.status)) {
+        uint8_t *sa = smem + stage * STAGE_BYTES;
+        uint8_t *sb = sa + A_BYTES;
+        bool go = true;
+        if (lane == 0) {
+          go = mbar_wait(&empty[stage], phase ^ 1u, args.status);
+          if (go) {
+            mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+            tma_load_2d(sb, &tmB0, &full[stage], kb * BK, b_row);
+            if (paired_b(MODE))
+              tma_load_2d(sb + B_BYTES / 2, &tmB1, &full[stage], kb * BK, b_row);
+            else
+              tma_load_2d(sb + B_BYTES / 2, &tmB0, &full[stage], kb * BK, b_row + BN / 2);
+            issued_parity[stage] = (int)phase;
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) {
           ok = false;
           break;
         }
-        uint8_t *sa = smem + stage * STAGE_BYTES;
-        uint8_t *sb = sa + A_BYTES;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)B_BYTES);
-          tma_load_2d(sb, &tmB0, &full[stage], kb * BK, b_row);
-          if (paired_b(MODE))
-            tma_load_2d(sb + B_BYTES / 2, &tmB1, &full[stage], kb * BK, b_row);
-          else
-            tma_load_2d(sb + B_BYTES / 2, &tmB0, &full[stage], kb * BK, b_row + BN / 2);
-        }
-        const uint32_t sa32 = smem_u32(sa);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = lane + 32 * j;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int chunk = kb * 8 + c;
-            const bool v = valid[j] && chunk < dchunks;
-            cp_async_16(sa32 + (uint32_t)(i * 128 + ((c ^ (i & 7)) << 4)), v ? src_row[j] + chunk * 8 : args.gx,
-                        v ? 16u : 0u);
-          }
-        }
-        cp_async_commit();
-        pend[npend++] = stage;
-        issued_parity[stage] = (int)phase;
-        if (npend > LAG) {
-          cp_async_wait_group<LAG>();
-          signal_oldest();
-        }
+        tma_gather4(sa + lane * 512, &tmA, &full[stage], kb * BK, t[0], t[1], t[2], t[3]);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    cp_async_wait_group<0>();
-    while (npend > 0) signal_oldest();
     // never leave the CTA with a bulk copy still writing its shared memory
     if (lane == 0)
       for (int s = 0; s < STAGES; ++s)
@@ -577,12 +548,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_tiles = (args.n_out + OUT_COLS - 1) / OUT_COLS;
   const int num_kb = args.num_kb;
 
-  // gathered A: each CTA's producer warp copies its 128 token rows with cp.async and
-  // its 32 lanes arrive on the leader's full barrier (besides the expected bytes)
+  // gathered A: each CTA gathers its own 128 token rows by TMA (see the producer)
   const bool gather = swappable(MODE) && args.gx != nullptr;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], gather ? 65 : 1);
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -625,14 +595,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0 && gather) {
     // ------------------------------------------------------------ producer, gathered A (both CTAs)
-    // As in the single-CTA form: lane 0 loads this CTA's half of B by TMA onto the
-    // leader's full barrier; the 32 lanes copy this CTA's 128 token rows with
-    // cp.async and, STAGES - 1 stages later, fence and arrive on the leader's full
-    // barrier (an arrival with cluster-scope release).
-    constexpr int LAG = STAGES - 1;
-    const int dchunks = args.K / 8;
-    int pend[STAGES] = {};
-    int npend = 0;
+    // As in the single-CTA form: lane 0 waits for the stage and loads this CTA's
+    // half of B (the leader also sets the pair's expected bytes); then the 32 lanes
+    // gather this CTA's 128 token rows, 4 per lane, all counted on the leader's
+    // full barrier.
     int issued_parity[STAGES];
     for (int s = 0; s < STAGES; ++s) issued_parity[s] = -1;
     int stage = 0;
@@ -640,12 +606,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     int g = 0;
     bool ok = true;
     const CUtensorMap *mb = (paired_b(MODE) && rank == 1) ? &tmB1 : &tmB0;
-    auto signal_oldest = [&]() {
-      fence_proxy_async_smem();
-      mbar_arrive_cluster(full_lead + 8u * (uint32_t)pend[0]);
-      for (int q = 1; q < npend; ++q) pend[q - 1] = pend[q];
-      --npend;
-    };
     for (int tile = pair_id; tile < total_tiles && ok; tile += npairs) {
       while (tile >= tile_start[g + 1]) ++g;
       const int local = tile - tile_start[g];
@@ -654,64 +614,46 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int a_row = rowbeg[g] + m_tile * 2 * BM + (int)rank * BM;
       const int b_row = paired_b(MODE) ? g * args.b_rows + n_tile * OUT_COLS
                                        : g * args.b_rows + n_tile * OUT_COLS + (int)rank * 128;
-      const uint16_t *src_row[4];
-      bool valid[4];
+      int t[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int r = a_row + lane + 32 * j;
-        int t = -1;
+        const int r = a_row + 4 * lane + j;
+        t[j] = 0;
         if (r < rowend[g]) {
-          t = args.gsrc[r];
-          if (t < 0 || t >= args.gx_rows) {  // an index past x: zeros, flagged
+          const int v = args.gsrc[r];
+          if (v < 0 || v >= args.gx_rows)
             set_status(args.status, MOE_ERR_BOUNDS);
-            t = -1;
-          }
+          else
+            t[j] = v;
         }
-        valid[j] = t >= 0;
-        src_row[j] = args.gx + (size_t)(t >= 0 ? t : 0) * args.K;
       }
       for (int kb = 0; kb < num_kb; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, args.status)) {
+        uint8_t *sa = smem + stage * STAGE_BYTES;
+        const uint32_t fb = full_lead + 8u * stage;
+        bool go = true;
+        if (lane == 0) {
+          go = mbar_wait(&empty[stage], phase ^ 1u, args.status);
+          if (go) {
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2u * STAGE_BYTES);
+            tma_load_2d_pair(sa + A_BYTES, mb, fb, kb * BK, b_row);
+            issued_parity[stage] = (int)phase;
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) {
           ok = false;
           break;
         }
-        uint8_t *sa = smem + stage * STAGE_BYTES;
-        const uint32_t fb = full_lead + 8u * stage;
-        if (lane == 0) {
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)pair::BH_BYTES);
-          tma_load_2d_pair(sa + A_BYTES, mb, fb, kb * BK, b_row);
-        }
-        const uint32_t sa32 = smem_u32(sa);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = lane + 32 * j;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int chunk = kb * 8 + c;
-            const bool v = valid[j] && chunk < dchunks;
-            cp_async_16(sa32 + (uint32_t)(i * 128 + ((c ^ (i & 7)) << 4)), v ? src_row[j] + chunk * 8 : args.gx,
-                        v ? 16u : 0u);
-          }
-        }
-        cp_async_commit();
-        pend[npend++] = stage;
-        issued_parity[stage] = (int)phase;
-        if (npend > LAG) {
-          cp_async_wait_group<LAG>();
-          signal_oldest();
-        }
+        tma_gather4_pair(sa + lane * 512, &tmA, fb, kb * BK, t[0], t[1], t[2], t[3]);
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
         }
       }
     }
-    cp_async_wait_group<0>();
-    while (npend > 0) signal_oldest();
     // the leader's full barriers count both CTAs' copies: wait for the last ones
     if (leader && lane == 0)
       for (int s = 0; s < STAGES; ++s)
-        if (issued_parity[s] >= 0) mbar_wait_cluster(&full[s], (uint32_t)issued_parity[s], args.status);
+        if (issued_parity[s] >= 0) mbar_wait(&full[s], (uint32_t)issued_parity[s], args.status);
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
@@ -776,8 +718,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!(gather ? mbar_wait_cluster(&full[stage], phase, args.status)
-                      : mbar_wait(&full[stage], phase, args.status))) {
+          if (!mbar_wait(&full[stage], phase, args.status)) {
             ok = false;
             break;
           }
@@ -857,9 +798,10 @@ static EncodeTiledFn get_encode() {
 }
 
 // 2-D bf16 map over a [rows, cols] row-major matrix (row stride `stride`
-// elements, default cols), box 64 (cols) x 128 (rows), 128-byte swizzle;
-// out-of-range elements read as zero.
-static int make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint64_t stride = 0) {
+// elements, default cols), box 64 (cols) x box_rows (128 for tiles, 1 for row
+// gathers), 128-byte swizzle; out-of-range elements read as zero.
+static int make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint64_t stride = 0,
+                    uint32_t box_rows = BM) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return MOE_ERR_CUDA;
   if (!stride) stride = cols;
@@ -867,7 +809,7 @@ static int make_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t co
     return MOE_ERR_UNSUPPORTED;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {stride * 2};
-  cuuint32_t box[2] = {BK, BM};
+  cuuint32_t box[2] = {BK, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1036,7 +978,7 @@ int tc_grouped_gemm_gather(int mode, const void *x, int64_t x_rows, const int32_
   if ((reinterpret_cast<uintptr_t>(x) & 15) || K % 8) return MOE_ERR_UNSUPPORTED;
   CUtensorMap ma, mb0, mb1;
   int rc;
-  if ((rc = make_map(&ma, x, (uint64_t)x_rows, (uint64_t)K))) return rc;  // not read: A is gathered
+  if ((rc = make_map(&ma, x, (uint64_t)x_rows, (uint64_t)K, 0, 1))) return rc;  // one-row boxes: row gathers
   if ((rc = make_map(&mb0, B0, (uint64_t)b_rows_total, (uint64_t)K))) return rc;
   if (mode == kSwiGLU) {
     if ((rc = make_map(&mb1, B1, (uint64_t)b_rows_total, (uint64_t)K))) return rc;

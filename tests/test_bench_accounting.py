@@ -49,13 +49,8 @@ def test_stage_work_matches_layer_counts():
     work = bench.stage_work(wl, kept, 8)
     assert work["expert_ffn"][0] == bench.layer_flops(wl, kept)["expert_ffn"]
     assert work["route"][0] == bench.layer_flops(wl, kept)["router"]
-    # expert FFN bytes (bf16: rows gathered from x): touched weights + x read once + y_perm written
-    assert work["expert_ffn"][1] == 8 * bench.expert_weight_bytes(wl, False) + wl.T * wl.d * 2 + kept * wl.d * 2
-    # with FP8 weights the experts read the permuted copy: x_perm read + y_perm written
-    w8 = bench.stage_work(wl, kept, 8, fp8=True)
-    assert w8["expert_ffn"][1] == 8 * bench.expert_weight_bytes(wl, True) + 2 * kept * wl.d * 2
-    # the dispatch copies x into x_perm only when the experts do not gather
-    assert w8["dispatch"][1] - work["dispatch"][1] == wl.T * wl.d * 2 + kept * wl.d * 2
+    # expert FFN bytes: touched weights + x_perm read + y_perm written
+    assert work["expert_ffn"][1] == 8 * bench.expert_weight_bytes(wl, False) + 2 * kept * wl.d * 2
     # combine: y_perm read, out written, ids + weights
     assert work["combine"][1] == kept * wl.d * 2 + wl.T * wl.d * 2 + wl.T * wl.k * 8
 
