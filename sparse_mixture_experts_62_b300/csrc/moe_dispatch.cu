@@ -57,15 +57,20 @@ __global__ void __launch_bounds__(CH) dispatch_hist_kernel(const int32_t *__rest
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < N; e += CH) hist[(size_t)blockIdx.x * N + e] = cnt[e];
+  // expert-major ([N][nchunks]): the scan reads each expert's chunk counts contiguously
+  for (int e = threadIdx.x; e < N; e += CH) hist[(size_t)e * gridDim.x + blockIdx.x] = cnt[e];
 }
 
 // One CTA of 1024 threads: G = 1024 / 256 = 4 (or, for N <= 128, 1024 / N rounded
-// down to a power of two, at most 32) adjacent threads per expert, each owning a
-// contiguous range of chunks.  Per expert: range sums, an exclusive scan of them
-// across the G threads (shuffles), then each chunk's starting rank; then the
-// capacity and the exclusive scan of the kept counts over the experts.
+// down to a power of two, at most 32) adjacent threads per expert.  hist and
+// chunk_base are expert-major ([N][nchunks]); the expert's G threads take G
+// adjacent chunks at a time (one 32-byte sector per expert and load), eight such
+// rows of chunks in flight, and each row's exclusive scan (shuffles over the G
+// threads) plus the running total of the rows before gives each chunk's starting
+// rank.  Then the capacity and the exclusive scan of the kept counts over the
+// experts (warp scans).
 constexpr int SCAN_THREADS = 1024;
+constexpr int SCAN_ROWS = 8;
 __global__ void __launch_bounds__(SCAN_THREADS) dispatch_scan_kernel(const int32_t *__restrict__ hist, int nchunks,
                                                                      int N, int G, int capacity,
                                                                      int32_t *__restrict__ chunk_base,
@@ -73,24 +78,30 @@ __global__ void __launch_bounds__(SCAN_THREADS) dispatch_scan_kernel(const int32
                                                                      int32_t *__restrict__ counts_kept,
                                                                      int32_t *__restrict__ offsets) {
   __shared__ int kept_s[256];
+  __shared__ int warp_tot[8];
   const int e = threadIdx.x / G, g = threadIdx.x % G;
-  const int per = (nchunks + G - 1) / G;
-  const int c0 = min(nchunks, g * per), c1 = min(nchunks, c0 + per);
-  int sum = 0;
-  if (e < N)
-    for (int c = c0; c < c1; ++c) sum += hist[(size_t)c * N + e];
-  // exclusive scan of the range sums across the expert's G threads (adjacent lanes)
-  int incl = sum;
-  for (int off = 1; off < G; off <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, off, G);
-    if (g >= off) incl += v;
-  }
-  const int total = __shfl_sync(0xffffffffu, incl, G - 1, G);
-  if (e < N) {
-    int run = incl - sum;
-    for (int c = c0; c < c1; ++c) {
-      chunk_base[(size_t)c * N + e] = run;
-      run += hist[(size_t)c * N + e];
+  const bool live = e < N;
+  const int32_t *he = hist + (size_t)(live ? e : 0) * nchunks;
+  int32_t *cb = chunk_base + (size_t)(live ? e : 0) * nchunks;
+  int total = 0;  // the expert's assignments in the rows of chunks done so far
+  for (int r0 = 0; r0 * G < nchunks; r0 += SCAN_ROWS) {
+    int v[SCAN_ROWS];
+#pragma unroll
+    for (int i = 0; i < SCAN_ROWS; ++i) {
+      const int c = (r0 + i) * G + g;
+      v[i] = (live && c < nchunks) ? he[c] : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < SCAN_ROWS; ++i) {
+      if ((r0 + i) * G >= nchunks) break;  // the same for every lane
+      int incl = v[i];
+      for (int off = 1; off < G; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, off, G);
+        if (g >= off) incl += u;
+      }
+      const int c = (r0 + i) * G + g;
+      if (live && c < nchunks) cb[c] = total + incl - v[i];
+      total += __shfl_sync(0xffffffffu, incl, G - 1, G);
     }
   }
   if (threadIdx.x < 256) kept_s[threadIdx.x] = 0;
@@ -102,17 +113,28 @@ __global__ void __launch_bounds__(SCAN_THREADS) dispatch_scan_kernel(const int32
     kept_s[e] = kept;
   }
   __syncthreads();
-  // exclusive scan of kept over experts (Hillis-Steele in shared memory, 256 threads)
-  const int t = threadIdx.x;
-  const int mine = t < 256 ? kept_s[t] : 0;
-  for (int off = 1; off < 256; off <<= 1) {
-    const int v = (t < 256 && t >= off) ? kept_s[t - off] : 0;
-    __syncthreads();
-    if (t < 256) kept_s[t] += v;
-    __syncthreads();
+  // exclusive scan of kept over the (at most 256) experts: a scan per warp of 32,
+  // then the eight warp totals
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  int mine = 0, inc = 0;
+  if (t < 256) {
+    mine = kept_s[t];
+    inc = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += v;
+    }
+    if (lane == 31) warp_tot[w] = inc;
   }
-  if (t < N) offsets[t] = kept_s[t] - mine;
-  if (t == N - 1) offsets[N] = kept_s[t];
+  __syncthreads();
+  if (t < 256) {
+    int before = 0;
+    for (int i = 0; i < w; ++i) before += warp_tot[i];
+    inc += before;
+    if (t < N) offsets[t] = inc - mine;
+    if (t == N - 1) offsets[N] = inc;
+  }
 }
 
 __global__ void __launch_bounds__(CH) dispatch_rank_kernel(const int32_t *__restrict__ idx, int T, int k, int N,
@@ -122,8 +144,10 @@ __global__ void __launch_bounds__(CH) dispatch_rank_kernel(const int32_t *__rest
                                                            int32_t *__restrict__ src_token) {
   __shared__ uint32_t lanes_with[CH_WARPS][256];  // which lanes of the warp picked expert e
   __shared__ int warp_before[CH_WARPS][256];      // assignments to e in earlier warps of the chunk
+  __shared__ int base_s[256];                     // this chunk's starting rank per expert
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int v = threadIdx.x; v < CH_WARPS * 256; v += CH) (&lanes_with[0][0])[v] = 0u;
+  for (int e = threadIdx.x; e < N; e += CH) base_s[e] = chunk_base[(size_t)e * gridDim.x + blockIdx.x];
   __syncthreads();
   const int t = blockIdx.x * CH + threadIdx.x;
   int ex[8];
@@ -152,7 +176,7 @@ __global__ void __launch_bounds__(CH) dispatch_rank_kernel(const int32_t *__rest
     const int e = ex[j];
     int row = -1;
     if (e >= 0) {
-      const int rank = chunk_base[(size_t)blockIdx.x * N + e] + warp_before[warp][e] +
+      const int rank = base_s[e] + warp_before[warp][e] +
                        __popc(lanes_with[warp][e] & lt_mask);
       if (capacity <= 0 || rank < capacity) {
         row = offsets[e] + rank;

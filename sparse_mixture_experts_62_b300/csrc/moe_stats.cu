@@ -70,9 +70,10 @@ __global__ void __launch_bounds__(256) stats_partial_kernel(const float *__restr
   const long long tb = s0 + (long long)j * SC;
   const long long te = min(min(s0 + L, (long long)T), tb + SC);
   const bool softmax = gate != MOE_GATE_SIGMOID_BIAS;
-  for (int tt = warp; tt < SC; tt += 8) {  // SC / 8 tokens per warp
+  const int cnt = (int)max(0LL, te - tb);
+#pragma unroll 4
+  for (int tt = warp; tt < cnt; tt += 8) {  // SC / 8 tokens per warp, four in flight
     const long long t = tb + tt;
-    if (t >= te) break;
     float v[8];
     token_probs(logits + (size_t)t * N, N, softmax, lane, v);
 #pragma unroll
@@ -107,8 +108,10 @@ __global__ void __launch_bounds__(1024) stats_final_kernel(const float *__restri
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int e = blockIdx.x * 32 + lane;
   float s = 0.f;
-  if (e < N)
+  if (e < N) {
+#pragma unroll 8
     for (int c = warp; c < nchunks; c += 32) s += partial[(size_t)c * N + e];
+  }
   red[warp][lane] = s;
   __syncthreads();
   if (warp == 0 && e < N) {
