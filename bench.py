@@ -507,6 +507,19 @@ def time_layer(args, moe, layer, x, wl, stream, dist=None, clk_gpu=None):
             else:
                 step(sev[k], all_stages=True)
         torch.cuda.synchronize()
+    # kernel pass (not part of the step timing): device time of each kernel inside
+    # whole steps, from CUPTI records, without the event nodes' own cost
+    def replay(k):
+        if flush:
+            scratch.zero_()
+        if graphs is not None:
+            graphs[k].replay()
+        else:
+            step(fev[k])
+
+    nk = min(args.steps, 5)
+    recs = cupti_kernels(replay, nk)
+    kern = kernel_stage_us(recs, nk, wl.shared_F > 0) if recs else None
     if flush:
         step_ms = [begins[k].elapsed_time(marks[k]) for k in range(args.steps)]
     else:
@@ -521,7 +534,62 @@ def time_layer(args, moe, layer, x, wl, stream, dist=None, clk_gpu=None):
     clocks = clk.summary()
     clocks.update(probe_clock(probe.cpu().numpy(), start.elapsed_time(end)))
     return {"step_ms": step_ms, "total_ms": total_ms, "ffn_ms": ffn_ms, "stage_ms": stage_ms,
-            "graph": graphs is not None, "clocks": clocks, "out": out, "stats": stats, "launches": nst}
+            "graph": graphs is not None, "clocks": clocks, "out": out, "stats": stats, "launches": nst,
+            "kernels": kern}
+
+
+_STAGE_OF = (("route", ("router_", "split_wg", "ec_scores", "ec_select", "fill_counts")),
+             ("dispatch", ("dispatch_", "scatter_rows", "gather_rows")),
+             ("combine", ("combine",)),
+             ("load_stats", ("stats_",)))
+_GEMM_NAMES = ("grouped_gemm", "fp8_ffn", "simt_gemm")
+
+
+def kernel_stage_us(kernels, steps: int, shared: bool):
+    """Per-kernel and per-stage device time (us per step) and the library's kernel
+    launches per step, from (name, start_ns, duration_ns) records of `steps` whole
+    steps.  A kernel belongs to the stage its name names; the grouped GEMM launches
+    of a step are the routed experts' and, with a shared expert, its last two
+    launches the shared expert's."""
+    mine = sorted((k for k in kernels if "moe::" in k[0] and "clock_probe" not in k[0]), key=lambda k: k[1])
+    per_kernel, per_stage = {}, {}
+    gemms = [k for k in mine if any(g in k[0] for g in _GEMM_NAMES)]
+    period = len(gemms) // steps if steps else 0
+    for i, (name, _, dur) in enumerate(mine):
+        short = name.replace("(anonymous namespace)::", "").replace("void ", "").split("(")[0]
+        per_kernel[short] = per_kernel.get(short, 0.0) + dur / 1e3 / steps
+        stage = "other"
+        if any(g in name for g in _GEMM_NAMES):
+            pos = gemms.index((name, mine[i][1], dur)) % period if period else 0
+            stage = "shared_ffn" if shared and pos >= period - 2 else "expert_ffn"
+        else:
+            for st, keys in _STAGE_OF:
+                if any(key in name for key in keys):
+                    stage = st
+                    break
+        per_stage[stage] = per_stage.get(stage, 0.0) + dur / 1e3 / steps
+    return per_kernel, per_stage, len(mine) / steps if steps else 0.0
+
+
+def cupti_kernels(replay, steps: int):
+    """(name, start_ns, duration_ns) of every kernel the `steps` calls of replay()
+    launch, from CUPTI activity records (torch.profiler); None if unavailable."""
+    import torch
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            for k in range(steps):
+                replay(k)
+            torch.cuda.synchronize()
+        out = []
+        for ev in prof.events():
+            if ev.device_type == torch.autograd.DeviceType.CUDA:
+                tr = ev.time_range
+                out.append((ev.name, int(tr.start * 1000), int((tr.end - tr.start) * 1000)))
+        return out
+    except Exception as exc:  # pragma: no cover - reported; the event-timed stages remain
+        sys.stderr.write(f"CUPTI kernel records unavailable ({exc})\n")
+        return None
 
 
 def probe_clock(samples, region_ms: float) -> dict:
@@ -577,9 +645,18 @@ def layer_report(wl, layer, t, peaks, peak_src, fp8: bool, steps: int, world: in
     work = stage_work(wl, kept_rows, touched, fp8)
     f32 = wl.dtype == "f32"
     clocks = t["clocks"]
+    # per stage: its kernels' device time inside whole steps (CUPTI), else the time
+    # between the events around it in the stage pass
+    kern = t.get("kernels")
+    stage_ms = dict(t["stage_ms"])
+    if kern is not None:
+        stage_ms.update({n: us / 1e3 for n, us in kern[1].items() if n in stage_ms})
     stages = {n: stage_roofline(work[n][0], work[n][1], ms, peaks, clocks,
                                 alu=f32 and n in ("route", "expert_ffn", "shared_ffn"))
-              for n, ms in t["stage_ms"].items()}
+              for n, ms in stage_ms.items()}
+    for n in stages:
+        stages[n]["ms_events"] = t["stage_ms"][n]
+        stages[n]["timing"] = "cupti kernel time in whole steps" if kern is not None else "events, stage pass"
     # the dominant kernel against its bound, from the events around it in the timed steps
     ffn = stage_roofline(work["expert_ffn"][0], work["expert_ffn"][1], t["ffn_ms"], peaks, clocks,
                          alu=f32)
@@ -596,8 +673,11 @@ def layer_report(wl, layer, t, peaks, peak_src, fp8: bool, steps: int, world: in
     layer = {"flops": fl["total"], "tflops": fl["total"] / (ms_per_step / 1e3) / 1e12, "kept_rows": kept_rows,
              "touched_experts": touched, "algorithmic_bytes": lb, "gbs": lb / (ms_per_step / 1e3) / 1e9,
              "hbm_frac": lb / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"]}
-    return {"value": wl.T * steps * world / (t["total_ms"] / 1e3), "ms_per_step": ms_per_step,
-            "stages": stages, "roofline": roof, "layer": layer}
+    rep = {"value": wl.T * steps * world / (t["total_ms"] / 1e3), "ms_per_step": ms_per_step,
+           "stages": stages, "roofline": roof, "layer": layer}
+    if kern is not None:
+        rep["kernels_us"] = {k: round(v, 2) for k, v in sorted(kern[0].items(), key=lambda kv: -kv[1])}
+    return rep
 
 
 def time_decode(args, moe, layer, peaks, peak_src, stream, fp8: bool):
@@ -620,7 +700,8 @@ def time_decode(args, moe, layer, peaks, peak_src, stream, fp8: bool):
             "step_ms_p50": float(np.percentile(t["step_ms"], 50)),
             "layer_bytes": r["layer"]["algorithmic_bytes"], "touched_experts": r["layer"]["touched_experts"],
             "achieved_gbs": r["layer"]["gbs"], "peak_gbs": peaks["hbm_gbs"], "frac": r["layer"]["hbm_frac"],
-            "stages": r["stages"], "roofline": r["roofline"], "clocks": t["clocks"]}
+            "stages": r["stages"], "kernels_us": r.get("kernels_us"), "roofline": r["roofline"],
+            "clocks": t["clocks"]}
 
 
 def run_ours(args, wl, dist, rank, local):
@@ -736,7 +817,11 @@ def run_ours(args, wl, dist, rank, local):
     if rank == 0:
         sys.stderr.write("per-stage ms: " + json.dumps({k: round(val, 4) for k, val in t["stage_ms"].items()}) + "\n")
         step_ms = t["step_ms"]
+        # the library's kernels per step: counted from the CUPTI records where there
+        # are some, else from the launch plan; plus the clock probe's one launch
         n_launch = launches_per_step(wl, args.fp8)
+        if t.get("kernels") is not None:
+            n_launch = int(round(t["kernels"][2]))
         line = {"metric": METRIC, "value": rep["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": rep["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak",
@@ -750,8 +835,9 @@ def run_ours(args, wl, dist, rank, local):
                 "stages": rep["stages"],
                 "layer": rep["layer"],
                 "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-                # timed region: one step's launches per step
-                "gpu_launches": n_launch * args.steps,
+                "kernels_us": rep.get("kernels_us"),
+                # timed region: one step's launches per step, and the clock probe
+                "gpu_launches": n_launch * args.steps + 1,
                 **({"decode": decode} if decode is not None else {}),
                 **({"decode_fp8": decode_fp8} if decode_fp8 is not None else {}),
                 **({"backward": bwd} if bwd is not None else {}),

@@ -145,3 +145,35 @@ def test_clock_norm_prefers_the_in_band_clock():
     clocks = {"sm_mhz": 2000.0, "sm_max_mhz": 2000.0, "sm_mhz_in_band": 1500.0}
     r = bench.stage_roofline(3e12, 3e9, 2.0, peaks, clocks)
     assert r["frac"] == pytest.approx(0.75) and r["frac_clock_norm"] == pytest.approx(1.0)
+
+
+def test_kernel_records_to_stages():
+    """CUPTI-style (name, start, duration) records of two steps: stages by kernel
+    name, the last two grouped GEMM launches of each step to the shared expert, the
+    clock probe and foreign kernels left out."""
+    step = [("void moe::rtc::split_wg_kernel(float)", 2000), ("void moe::rtc::router_gemm_kernel<128>(x)", 10000),
+            ("void moe::(anonymous namespace)::router_topk_kernel<4>(x)", 5000),
+            ("void moe::(anonymous namespace)::dispatch_hist_kernel(x)", 1000),
+            ("void moe::(anonymous namespace)::scatter_rows_kernel(x)", 3000),
+            ("void moe::tc::grouped_gemm_kernel<0>(x)", 100000), ("void moe::tc::grouped_gemm_kernel<2>(x)", 50000),
+            ("void moe::tc::grouped_gemm_pair_kernel<0>(x)", 20000),
+            ("void moe::tc::grouped_gemm_pair_kernel<2>(x)", 10000),
+            ("void moe::(anonymous namespace)::combine_warp_kernel<true, 8>(x)", 4000),
+            ("void moe::(anonymous namespace)::stats_partial_kernel(x)", 700),
+            ("void moe::(anonymous namespace)::stats_final_kernel(x)", 800),
+            ("void at::native::elementwise_kernel<...>(x)", 9999)]
+    recs, t = [], 0
+    for _ in range(2):
+        for name, dur in step:
+            recs.append((name, t, dur))
+            t += dur + 100
+    recs.append(("void moe::(anonymous namespace)::clock_probe_kernel(x)", 0, 10**7))
+    per_kernel, per_stage, per_step = bench.kernel_stage_us(recs, 2, shared=True)
+    assert per_step == 12
+    assert per_stage["route"] == pytest.approx(17.0) and per_stage["dispatch"] == pytest.approx(4.0)
+    assert per_stage["expert_ffn"] == pytest.approx(150.0) and per_stage["shared_ffn"] == pytest.approx(30.0)
+    assert per_stage["combine"] == pytest.approx(4.0) and per_stage["load_stats"] == pytest.approx(1.5)
+    assert "other" not in per_stage and per_kernel["moe::tc::grouped_gemm_kernel<0>"] == pytest.approx(100.0)
+    # without a shared expert every grouped GEMM launch is the routed experts'
+    _, per_stage, _ = bench.kernel_stage_us(recs, 2, shared=False)
+    assert per_stage["expert_ffn"] == pytest.approx(180.0) and "shared_ffn" not in per_stage
