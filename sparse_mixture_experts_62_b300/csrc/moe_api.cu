@@ -237,6 +237,9 @@ inline int small_router_splits(const moe_config *c) {
 int route(const moe_config *c, const Ws &w, const void *x, const float *Wg, const float *logit_bias,
           const float *sel_bias, float *logits, int32_t *idx, float *gw, cudaStream_t s) {
   const float *sb = c->gate == MOE_GATE_SIGMOID_BIAS ? sel_bias : nullptr;
+  if (!is_bf16(c) && c->T > 64 && router_fused_fits(c->T, c->d, c->N) && aligned16(Wg))
+    return launch_router_fused(x, is_bf16(c), Wg, logit_bias, sb, c->T, c->d, c->N, c->k, c->gate, logits, idx, gw,
+                               w.status(), s);
   if (small_router(c)) {
     const int S = small_router_splits(c);
     float *part = w.router_partial(c);  // [S][T][N] within the [max splits][T][Npad] scratch

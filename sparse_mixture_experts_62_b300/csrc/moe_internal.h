@@ -12,6 +12,12 @@ int device_sm_count(int device);
 // router: logits = x . Wg (+ logit_bias); then top-k + gate weights
 int launch_router_logits(const void *x, bool x_bf16, const float *Wg, const float *logit_bias, int T, int d, int N,
                          int splits, float *logits, cudaStream_t s);
+// The whole route (logits, top-k, gate) in one launch on the CUDA cores for N = 4 or 8
+// (used for float32 activations).
+bool router_fused_fits(int T, int d, int N);
+int launch_router_fused(const void *x, bool x_bf16, const float *Wg, const float *logit_bias,
+                        const float *sel_bias, int T, int d, int N, int k, int gate, float *logits, int32_t *idx,
+                        float *w, int *status, cudaStream_t s);
 int launch_router_topk(const float *partial, int S, int pstride, const float *logit_bias, float *logits,
                        const float *sel_bias, int T, int N, int k, int gate, int32_t *idx, float *w, int *status,
                        cudaStream_t s);

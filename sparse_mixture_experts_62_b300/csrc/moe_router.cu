@@ -144,45 +144,15 @@ __device__ __forceinline__ float sigmoid_f32(float z) {
   return (float)(1.0 / (1.0 + exp(-(double)z)));
 }
 
-// One warp per token; lane l holds experts l, l+32, ... (N <= 256).  The logits
-// are the sum of S partial tiles (row stride pstride, tile stride T * pstride),
-// added in split order, plus the optional logit bias; they are written to
-// `logits` (which may alias the only partial when S == 1 and no bias is added).
-template <int NV>  // expert slots per lane: N <= 32 NV
-__global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, int S, int pstride,
-                                                          const float *__restrict__ logit_bias, float *logits,
-                                                          const float *__restrict__ sel_bias, int T, int N, int k,
-                                                          int gate, int32_t *__restrict__ idx, float *__restrict__ w,
-                                                          int *status) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + warp;
-  if (t >= T) return;
-  float zl[NV];  // this lane's logits, kept in registers
+// Top-k and gate of token t, called by a whole warp: lane l holds the logits of
+// experts l, l + 32, ... (N <= 32 NV; -inf past N).  Writes idx[t, :] and w[t, :];
+// a non-finite logit sets MOE_ERR_NONFINITE.
+template <int NV>
+__device__ __forceinline__ void route_token(const float (&zl)[NV], int t, int lane, int N, int k, int gate,
+                                            const float *__restrict__ sel_bias, int32_t *__restrict__ idx,
+                                            float *__restrict__ w, int *status) {
   float sel[NV];
   bool bad = false;
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int e = lane + 32 * i;
-    zl[i] = -INFINITY;
-    if (e < N) {
-      // four independent running sums over the splits, combined in a fixed order
-      const float *p = partial + (size_t)t * pstride + e;
-      const size_t tile = (size_t)T * pstride;
-      float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
-      int sp = 0;
-      for (; sp + 4 <= S; sp += 4) {
-        z0 += p[(sp + 0) * tile];
-        z1 += p[(sp + 1) * tile];
-        z2 += p[(sp + 2) * tile];
-        z3 += p[(sp + 3) * tile];
-      }
-      for (; sp < S; ++sp) z0 += p[sp * tile];
-      float z = (z0 + z1) + (z2 + z3);
-      if (logit_bias) z += logit_bias[e];
-      logits[(size_t)t * N + e] = z;
-      zl[i] = z;
-    }
-  }
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
@@ -301,6 +271,182 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, 
   }
 }
 
+// One warp per token; lane l holds experts l, l+32, ... (N <= 256).  The logits
+// are the sum of S partial tiles (row stride pstride, tile stride T * pstride),
+// added in split order, plus the optional logit bias; they are written to
+// `logits` (which may alias the only partial when S == 1 and no bias is added).
+template <int NV>  // expert slots per lane: N <= 32 NV
+__global__ void __launch_bounds__(256) router_topk_kernel(const float *partial, int S, int pstride,
+                                                          const float *__restrict__ logit_bias, float *logits,
+                                                          const float *__restrict__ sel_bias, int T, int N, int k,
+                                                          int gate, int32_t *__restrict__ idx, float *__restrict__ w,
+                                                          int *status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float zl[NV];  // this lane's logits, kept in registers
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    zl[i] = -INFINITY;
+    if (e < N) {
+      // four independent running sums over the splits, combined in a fixed order
+      const float *p = partial + (size_t)t * pstride + e;
+      const size_t tile = (size_t)T * pstride;
+      float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+      int sp = 0;
+      for (; sp + 4 <= S; sp += 4) {
+        z0 += p[(sp + 0) * tile];
+        z1 += p[(sp + 1) * tile];
+        z2 += p[(sp + 2) * tile];
+        z3 += p[(sp + 3) * tile];
+      }
+      for (; sp < S; ++sp) z0 += p[sp * tile];
+      float z = (z0 + z1) + (z2 + z3);
+      if (logit_bias) z += logit_bias[e];
+      logits[(size_t)t * N + e] = z;
+      zl[i] = z;
+    }
+  }
+  route_token<NV>(zl, t, lane, N, k, gate, sel_bias, idx, w, status);
+}
+
+// The whole route in one launch for a few experts (N = 4 or 8) and float32
+// activations past the decode sizes: logits on the CUDA cores, then top-k and gate
+// in the same CTA (the logits never make a round trip through memory before the
+// selection).  Used for float32 x, where it replaces the two-launch CUDA-core
+// route (9.0 us against 12.5 us on the 256-token, d = 512 float32 layer).  For
+// bf16 x the tensor-core route stays faster (18.8 us against 40.8 us on the
+// 4096-token Mixtral shape): every CTA reads each W_g row once, so those loads
+// miss L1, and with one CTA of eight warps per SM their latency is not hidden.
+//
+// CTA = 32 tokens x 8 warps.  Warp w takes the K range [w kw, (w + 1) kw) (kw a
+// multiple of 16); lane l takes tokens t0 + (l & 15) and t0 + 16 + (l & 15) and,
+// of every 16 consecutive k, the 8 at offset 8 (l >> 4), so a load of 8 values of
+// x is 16 bytes, the two half-warps together read 32-byte sectors whole, and each
+// W_g row (NW floats, 16-byte vectors, the same for the half-warp) feeds 2 NW
+// products.  Sums: per 128-wide block of K in float32 (fused multiply-adds in k
+// order), the blocks added in order, the two half-warps added (lower half first),
+// then the eight warps' sums in warp order plus the logit bias: deterministic.
+constexpr int RF_TOK = 32;
+constexpr int RF_WARPS = 8;
+constexpr int RF_GROUPS = 8;  // 16-wide groups of K per block: 128 k, 8 loads of x in flight per lane
+
+// 8 consecutive values of x at element offset `off`, raw: one 16-byte vector of
+// bf16 or two of float32; value j of a raw vector as float32.
+template <bool BF16>
+struct XRaw {
+  uint4 q[BF16 ? 1 : 2];
+};
+template <bool BF16>
+__device__ __forceinline__ XRaw<BF16> load_x8(const void *x, size_t off) {
+  XRaw<BF16> r;
+  if (BF16) {
+    r.q[0] = __ldg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + off));
+  } else {
+    const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const float *>(x) + off);
+    r.q[0] = __ldg(p);
+    r.q[BF16 ? 0 : 1] = __ldg(p + 1);
+  }
+  return r;
+}
+template <bool BF16>
+__device__ __forceinline__ float x_at(const XRaw<BF16> &r, int j) {
+  if (BF16) {
+    const uint32_t wv = j < 2 ? r.q[0].x : (j < 4 ? r.q[0].y : (j < 6 ? r.q[0].z : r.q[0].w));
+    return (j & 1) ? bf16_hi(wv) : bf16_lo(wv);
+  }
+  const uint4 &q = r.q[j >> 2];
+  const uint32_t wv = (j & 3) == 0 ? q.x : ((j & 3) == 1 ? q.y : ((j & 3) == 2 ? q.z : q.w));
+  return __uint_as_float(wv);
+}
+
+template <bool BF16, int NW>
+__global__ void __launch_bounds__(256) router_fused_kernel(const void *__restrict__ x, const float *__restrict__ Wg,
+                                                           const float *__restrict__ logit_bias,
+                                                           const float *__restrict__ sel_bias, int T, int d, int k,
+                                                           int gate, int kw, float *__restrict__ logits,
+                                                           int32_t *__restrict__ idx, float *__restrict__ w,
+                                                           int *status) {
+  __shared__ float red[RF_WARPS][RF_TOK][NW];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tl = lane & 15, h = lane >> 4;
+  const int t0 = blockIdx.x * RF_TOK;
+  const int ta = t0 + tl, tb = t0 + 16 + tl;
+  const bool va = ta < T, vb = tb < T;
+  const int kbeg = warp * kw, kend = min(d, kbeg + kw);
+  float acc[2][NW];
+#pragma unroll
+  for (int e = 0; e < NW; ++e) acc[0][e] = acc[1][e] = 0.f;
+  for (int k0 = kbeg; k0 < kend; k0 += 16 * RF_GROUPS) {
+    XRaw<BF16> xa[RF_GROUPS], xb[RF_GROUPS];
+#pragma unroll
+    for (int g = 0; g < RF_GROUPS; ++g) {
+      const int kk = k0 + 16 * g + 8 * h;
+      const bool in = kk < kend;  // the group's 8 values are all in or all out (d % 8 == 0)
+      xa[g] = (in && va) ? load_x8<BF16>(x, (size_t)ta * d + kk) : XRaw<BF16>{};
+      xb[g] = (in && vb) ? load_x8<BF16>(x, (size_t)tb * d + kk) : XRaw<BF16>{};
+    }
+    float ca[NW], cb[NW];
+#pragma unroll
+    for (int e = 0; e < NW; ++e) ca[e] = cb[e] = 0.f;
+#pragma unroll
+    for (int g = 0; g < RF_GROUPS; ++g) {
+      const int kk = k0 + 16 * g + 8 * h;
+      if (kk >= kend) continue;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 *wr = reinterpret_cast<const float4 *>(Wg + (size_t)(kk + j) * NW);
+        const float xja = x_at<BF16>(xa[g], j), xjb = x_at<BF16>(xb[g], j);
+#pragma unroll
+        for (int q = 0; q < NW / 4; ++q) {
+          const float4 w4 = __ldg(wr + q);
+          ca[4 * q + 0] = fmaf(xja, w4.x, ca[4 * q + 0]);
+          ca[4 * q + 1] = fmaf(xja, w4.y, ca[4 * q + 1]);
+          ca[4 * q + 2] = fmaf(xja, w4.z, ca[4 * q + 2]);
+          ca[4 * q + 3] = fmaf(xja, w4.w, ca[4 * q + 3]);
+          cb[4 * q + 0] = fmaf(xjb, w4.x, cb[4 * q + 0]);
+          cb[4 * q + 1] = fmaf(xjb, w4.y, cb[4 * q + 1]);
+          cb[4 * q + 2] = fmaf(xjb, w4.z, cb[4 * q + 2]);
+          cb[4 * q + 3] = fmaf(xjb, w4.w, cb[4 * q + 3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < NW; ++e) {
+      acc[0][e] += ca[e];
+      acc[1][e] += cb[e];
+    }
+  }
+  // the two halves of K, lower half first
+#pragma unroll
+  for (int e = 0; e < NW; ++e) {
+    const float ua = __shfl_down_sync(0xffffffffu, acc[0][e], 16);
+    const float ub = __shfl_down_sync(0xffffffffu, acc[1][e], 16);
+    if (h == 0) {
+      red[warp][tl][e] = acc[0][e] + ua;
+      red[warp][16 + tl][e] = acc[1][e] + ub;
+    }
+  }
+  __syncthreads();
+  // warp w routes tokens 4 w .. 4 w + 3 of the CTA; lane e < NW holds expert e
+  for (int i = 0; i < RF_TOK / RF_WARPS; ++i) {
+    const int tt = warp * (RF_TOK / RF_WARPS) + i;
+    const int t = t0 + tt;
+    if (t >= T) break;
+    float zl[1] = {-INFINITY};
+    if (lane < NW) {
+      float z = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < RF_WARPS; ++ww) z += red[ww][tt][lane];
+      if (logit_bias) z += logit_bias[lane];
+      logits[(size_t)t * NW + lane] = z;
+      zl[0] = z;
+    }
+    route_token<1>(zl, t, lane, NW, k, gate, sel_bias, idx, w, status);
+  }
+}
+
 // logits[t, e] = sum of the S split partials in split order + logit bias
 __global__ void __launch_bounds__(256) router_sum_kernel(const float *__restrict__ partial, int S, int pstride,
                                                          const float *__restrict__ logit_bias,
@@ -356,6 +502,28 @@ int launch_router_logits(const void *x, bool x_bf16, const float *Wg, const floa
     MOE_RL(32)
   }
 #undef MOE_RL
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+bool router_fused_fits(int T, int d, int N) { return T > 0 && (N == 4 || N == 8) && d % 8 == 0 && d > 0; }
+
+int launch_router_fused(const void *x, bool x_bf16, const float *Wg, const float *logit_bias,
+                        const float *sel_bias, int T, int d, int N, int k, int gate, float *logits, int32_t *idx,
+                        float *w, int *status, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  if (!router_fused_fits(T, d, N) || (reinterpret_cast<uintptr_t>(Wg) & 15) ||
+      (reinterpret_cast<uintptr_t>(x) & 15))
+    return MOE_ERR_UNSUPPORTED;
+  const int kw = (d + 16 * RF_WARPS - 1) / (16 * RF_WARPS) * 16;
+  const dim3 grid((T + RF_TOK - 1) / RF_TOK), block(32 * RF_WARPS);
+#define MOE_RF(B, NW) \
+  router_fused_kernel<B, NW><<<grid, block, 0, s>>>(x, Wg, logit_bias, sel_bias, T, d, k, gate, kw, logits, idx, w, status)
+  if (x_bf16) {
+    if (N == 8) MOE_RF(true, 8); else MOE_RF(true, 4);
+  } else {
+    if (N == 8) MOE_RF(false, 8); else MOE_RF(false, 4);
+  }
+#undef MOE_RF
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -164,6 +164,15 @@ ROUTER_CASES = [
     dict(T=100, d=512, N=8, k=2, gate="softmax", dtype="f32", act="relu"),
     dict(T=300, d=256, N=16, k=4, gate="softmax_full"),
     dict(T=64, d=128, N=64, k=1, gate="softmax"),                        # Switch-style top-1
+    # few experts, long K, every gate (bf16: the tensor-core route)
+    dict(T=200, d=4096, N=8, k=2, gate="softmax_full"),
+    dict(T=1000, d=4096, N=8, k=2, gate="sigmoid", sel_bias_range=0.05),
+    dict(T=97, d=1000, N=4, k=2, gate="softmax", zipf_s=1.2),
+    # one-launch CUDA-core route (float32 x, N = 4 or 8, more than 64 tokens): long
+    # K, a K range ending inside a warp's share (d = 1000), a ragged last CTA, gates
+    dict(T=65, d=4096, N=8, k=1, gate="softmax", dtype="f32", act="relu"),
+    dict(T=97, d=1000, N=4, k=2, gate="sigmoid", sel_bias_range=0.05, dtype="f32", act="relu"),
+    dict(T=300, d=512, N=8, k=3, gate="softmax_full", dtype="f32", act="relu"),
 ]
 
 
