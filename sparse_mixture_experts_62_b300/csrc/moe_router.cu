@@ -122,20 +122,24 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // key, the lowest index among equal keys (warp max of the keys, then warp min of
 // the indices holding it).  Every valid key is > 0; key 0 marks "none".
 template <int NV>
-__device__ __forceinline__ int warp_select(const uint32_t (&key)[NV], uint32_t &taken, int lane, uint32_t *kmax) {
+__device__ __forceinline__ int warp_select(const uint32_t (&key)[NV], const float (&zl)[NV], uint32_t &taken,
+                                           int lane, uint32_t *kmax, float *zwin) {
   uint32_t best = 0;
   int bi = 0;
+  float zb = 0.f;
 #pragma unroll
   for (int i = 0; i < NV; ++i)
     if (!((taken >> i) & 1u) && key[i] > best) {  // strict: the lowest i wins a tie within the lane
       best = key[i];
       bi = i;
+      zb = zl[i];
     }
   const uint32_t m = __reduce_max_sync(0xffffffffu, best);
   const uint32_t cand = (best == m && m != 0u) ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu;
   const int e = (int)__reduce_min_sync(0xffffffffu, cand);
   if ((e & 31) == lane) taken |= 1u << (e >> 5);
   *kmax = m;
+  *zwin = __shfl_sync(0xffffffffu, zb, e & 31);  // the winner's logit, from the lane holding it
   return e;
 }
 
@@ -172,7 +176,9 @@ __device__ __forceinline__ void route_token(const float (&zl)[NV], int t, int la
   uint32_t key[NV];
 #pragma unroll
   for (int i = 0; i < NV; ++i) key[i] = (lane + 32 * i < N) ? order_key(sel[i]) : 0u;
-  int chosen[8];
+  // slot j's expert and logit are kept by lane j (j < k), as each round picks them
+  int ej = 0;
+  float zj = 0.f, m = 0.f;
   bool done = false;
   if (gate == MOE_GATE_SIGMOID_BIAS) {
     // The selection score is fl32(s + b) with s = fl32(sigmoid(z)) evaluated in
@@ -185,25 +191,27 @@ __device__ __forceinline__ void route_token(const float (&zl)[NV], int t, int la
     // of the k-th estimate is evaluated in double and ranked again; the rest
     // cannot be in the top k.
     constexpr float kEstErr = 5.4e-7f, kSelMargin = 4e-6f;
-    uint32_t taken0 = 0, kv[9];
-    int ch0[9];
+    uint32_t taken0 = 0, kprev = 0, kk = 0;
+    bool clear = true;
     const int rounds = min(k + 1, N);
 #pragma unroll
-    for (int j = 0; j < 9; ++j)
-      if (j < rounds) ch0[j] = warp_select(key, taken0, lane, &kv[j]);
-    bool clear = true;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)  // 4 kEstErr: twice the bound, covering the rounding of the gap itself
-      if (j + 1 < rounds) clear = clear && (key_value(kv[j]) - key_value(kv[j + 1]) > 4.0f * kEstErr);
+    for (int j = 0; j < 9; ++j) {
+      if (j >= rounds) break;
+      uint32_t kw;
+      float zw;
+      const int e = warp_select(key, zl, taken0, lane, &kw, &zw);
+      // 4 kEstErr: twice the bound, covering the rounding of the gap itself
+      if (j > 0) clear = clear && (key_value(kprev) - key_value(kw) > 4.0f * kEstErr);
+      if (j == k - 1) kk = kw;
+      if (j < k && lane == j) {
+        ej = e;
+        zj = zw;
+      }
+      kprev = kw;
+    }
     if (clear) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) chosen[j] = ch0[j];
       done = true;
     } else {
-      uint32_t kk = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j == k - 1) kk = kv[j];
       const float vk = key_value(kk);
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
@@ -220,25 +228,21 @@ __device__ __forceinline__ void route_token(const float (&zl)[NV], int t, int la
     }
   }
   if (!done) {
-    uint32_t taken = 0, kmax;
+    uint32_t taken = 0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < k) chosen[j] = warp_select(key, taken, lane, &kmax);
-  }
-  // the chosen experts' logits, from the lanes that hold them: lane j < k gets slot j's
-  float zj = 0.f, m = 0.f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if (j < k) {
-      const int e = chosen[j];
-      float mine = zl[0];
-#pragma unroll
-      for (int i = 1; i < NV; ++i)
-        if ((e >> 5) == i) mine = zl[i];
-      const float ze = __shfl_sync(0xffffffffu, mine, e & 31);
-      if (lane == j) zj = ze;
-      if (j == 0) m = ze;  // the first pick has the largest logit (softmax gates)
+    for (int j = 0; j < 8; ++j) {
+      if (j >= k) break;
+      uint32_t kw;
+      float zw;
+      const int e = warp_select(key, zl, taken, lane, &kw, &zw);
+      if (lane == j) {
+        ej = e;
+        zj = zw;
+      }
+      if (j == 0) m = zw;  // the first pick has the largest logit (softmax gates)
     }
+  } else {
+    m = __shfl_sync(0xffffffffu, zj, 0);
   }
   // full-softmax gate: the normaliser over all N experts (warp sum, fixed order)
   float full_den = 0.f;
@@ -262,11 +266,7 @@ __device__ __forceinline__ void route_token(const float (&zl)[NV], int t, int la
   for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
   if (gate == MOE_GATE_SOFTMAX_FULL) sum = full_den;
   if (lane < k) {
-    int cj = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-      if (j < k && lane == j) cj = chosen[j];
-    idx[(size_t)t * k + lane] = cj;
+    idx[(size_t)t * k + lane] = ej;
     w[(size_t)t * k + lane] = g / sum;
   }
 }
