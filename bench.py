@@ -624,12 +624,15 @@ def ffn_kernel_label(wl, fp8: bool) -> str:
 
 def launches_per_step(wl, fp8: bool) -> int:
     """Kernels of one step: route = split W_g + tensor-core logits + top-k (bf16, more
-    than 64 tokens) or CUDA-core logits + top-k; dispatch = histogram, scan, rank,
-    copy (one fused kernel + copy for at most 128 tokens); experts 2 (1 for the
-    one-launch FP8 decode FFN); shared 2; combine 1; statistics 2 (1 for at most 32
-    tokens)."""
+    than 64 tokens), one kernel (float32, 4 or 8 experts, more than 64 tokens) or
+    CUDA-core logits + top-k; dispatch = histogram, scan, rank, copy (one fused
+    kernel + copy for at most 128 tokens); experts 2 (1 for the one-launch FP8
+    decode FFN); shared 2; combine 1; statistics 2 (1 for at most 32 tokens)."""
     ffn = 1 if (fp8 and wl.T <= 64) else 2
-    route = 3 if (wl.dtype == "bf16" and wl.T > 64) else 2
+    if wl.dtype == "bf16":
+        route = 3 if wl.T > 64 else 2
+    else:
+        route = 1 if (wl.T > 64 and wl.N in (4, 8)) else 2
     dispatch = 4 if wl.T > 128 else 2
     stats = 2 if wl.T > 32 else 1
     return route + dispatch + ffn + (2 if wl.shared_F else 0) + 1 + stats
