@@ -9,7 +9,8 @@
 //
 //   out[r, n] = EPI( sum_k A[r, k] * B_g[n, k] )        for rows r of group g
 //
-// A: [rows, K] bf16 row-major (x_perm or h), one TMA map over all groups.
+// A: [rows, K] bf16 row-major (x_perm or h), one TMA map over all groups (or the
+//    rows of x gathered by index, see below).
 // B_g: rows [g * b_rows, (g + 1) * b_rows) of a [G * b_rows, K] bf16 view of the
 //      stacked expert weights (K-major, i.e. the "W x" layout).
 // Modes:
@@ -45,6 +46,12 @@
 // to N_t / 128 of a tile while the same bytes stream through the same ring.  The
 // epilogue thread of weight row f writes output column f of every row of the
 // group (32 consecutive columns per warp store).
+//
+// Gathered A (forward modes, `tc_grouped_gemm_gather`): instead of x_perm, the A
+// tile's rows are rows src_token[r] of x, fetched by TMA row gathers
+// (`tile::gather4` on a one-row-high map over x: four indexed 128-byte rows per
+// copy, 32 copies per 128-row stage, one per producer lane) into the same
+// 128-byte-swizzled layout; the rest of the kernel is unchanged.
 #include <mutex>
 #include <vector>
 
