@@ -520,6 +520,8 @@ def time_layer(args, moe, layer, x, wl, stream, dist=None, clk_gpu=None):
     nk = min(args.steps, 5)
     recs = cupti_kernels(replay, nk)
     kern = kernel_stage_us(recs, nk, wl.shared_F > 0) if recs else None
+    if kern is not None and not kern[0]:  # no kernel of the library among the records
+        kern = None
     if flush:
         step_ms = [begins[k].elapsed_time(marks[k]) for k in range(args.steps)]
     else:
