@@ -156,8 +156,19 @@ def stage_roofline(flops, nbytes, ms, peaks, clocks=None, alu=False):
             if mhz and fmax:
                 r["frac_clock_norm"] = ach / (tf_peak * min(mhz, fmax) / fmax)
         return r
-    return {"ms": ms, "bound": "hbm", "achieved": nbytes / s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": t_hbm / s}
+    r = {"ms": ms, "bound": "hbm", "achieved": nbytes / s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+         "frac": t_hbm / s}
+    if flops > 0 and not alu:
+        # a contraction at the ridge: its tensor rate as well, against the burst peak
+        # and against the burst peak scaled to the measured SM clock
+        ach = flops / s / 1e12
+        r["tflops"] = ach
+        r["tensor_frac"] = ach / tf_peak
+        mhz = (clocks or {}).get("sm_mhz_in_band") or (clocks or {}).get("sm_mhz")
+        fmax = (clocks or {}).get("sm_max_mhz") or peaks.get("sm_max_mhz")
+        if mhz and fmax:
+            r["tensor_frac_clock_norm"] = ach / (tf_peak * min(mhz, fmax) / fmax)
+    return r
 
 
 def measured_peaks():
@@ -666,7 +677,7 @@ def layer_report(wl, layer, t, peaks, peak_src, fp8: bool, steps: int, world: in
     ffn = stage_roofline(work["expert_ffn"][0], work["expert_ffn"][1], t["ffn_ms"], peaks, clocks,
                          alu=f32)
     roof = {k: ffn[k] for k in ("bound", "achieved", "peak", "unit", "frac", "frac_clock_norm", "frac_sustained",
-                                "ms") if k in ffn}
+                                "tflops", "tensor_frac", "tensor_frac_clock_norm", "ms") if k in ffn}
     roof["traffic"] = _traffic(wl.name, fp8)
     roof["kernel"] = ffn_kernel_label(wl, fp8)
     roof["peak_source"] = ("derived float32 CUDA-core peak (148 SMs x 128 lanes x 2 FLOP x 2032 MHz)"

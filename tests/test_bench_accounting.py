@@ -68,9 +68,13 @@ def test_stage_roofline_picks_the_longer_bound():
     r = bench.stage_roofline(3e12, 3e9, 2.0, peaks, clocks)
     assert r["peak"] == 2000.0 and r["frac"] == pytest.approx(0.75)
     assert r["frac_clock_norm"] == pytest.approx(1.5)
-    # 10 GFLOP and 3 GB: HBM governs
+    # 10 GFLOP and 3 GB: HBM governs; the tensor rate rides along
     r = bench.stage_roofline(1e10, 3e9, 1.0, peaks)
     assert r["bound"] == "hbm" and r["achieved"] == pytest.approx(3000.0) and r["frac"] == pytest.approx(0.5)
+    assert r["tflops"] == pytest.approx(10.0) and r["tensor_frac"] == pytest.approx(0.005)
+    r = bench.stage_roofline(1e12, 6e9, 1.0, peaks, clocks)  # 1 PFLOP/s at half the maximum clock
+    assert r["bound"] == "hbm" and r["tensor_frac"] == pytest.approx(0.5)
+    assert r["tensor_frac_clock_norm"] == pytest.approx(1.0)
     # float32 work against the CUDA-core peak
     r = bench.stage_roofline(1e9, 1e6, 1.0, peaks, alu=True)
     assert r["bound"] == "alu" and r["peak"] == pytest.approx(bench.F32_ALU_TFLOPS)
