@@ -104,6 +104,9 @@ struct Args {
   const uint16_t *gx;
   const int32_t *gsrc;
   int32_t gx_rows;
+  // CTA-pair form: tiles are taken from this counter in issue order (zeroed before
+  // each launch)
+  int *tile_counter;
 };
 
 __device__ __forceinline__ float silu(float a) { return __fdividef(a, 1.0f + __expf(-a)); }
@@ -522,6 +525,12 @@ constexpr int STAGE_BYTES = A_BYTES + BH_BYTES;  // 32 KB
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 256 + (size_t)(4 * MAX_GROUPS + 8) * 4;
 constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
 constexpr uint32_t IDESC_BT = idesc_bf16_f32_major(2 * BM, BN, false, true);
+// Tile queue: the leader's producer takes the next tile from the counter and writes
+// it to slot q of both CTAs (TQ slots), arriving on tq_full[q] of each; the leader's
+// MMA thread, both CTAs' four epilogue warps and the peer's producer read it and
+// arrive on the leader's tq_empty[q].
+constexpr int TQ = 4;
+constexpr uint32_t TQ_READERS = 1 + 4 + 1 + 4;
 }  // namespace pair
 
 template <int MODE>
@@ -540,7 +549,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t *empty = full + STAGES;
   uint64_t *tfull = empty + STAGES;
   uint64_t *tempty = tfull + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+  uint64_t *tq_full = tempty + 2;          // [TQ]
+  uint64_t *tq_empty = tq_full + pair::TQ;  // [TQ], the leader's
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tq_empty + pair::TQ);
+  volatile int *tq = reinterpret_cast<volatile int *>(tmem_slot + 2);  // [TQ] tile ids
+  static_assert((2 * STAGES + 4 + 2 * pair::TQ) * 8 + 8 + 4 * pair::TQ <= 256, "barrier area");
   int *tile_start = reinterpret_cast<int *>(smem + STAGES * STAGE_BYTES + 256);
   int *mtiles = tile_start + MAX_GROUPS + 1;
   int *rowbeg = mtiles + MAX_GROUPS;
@@ -550,7 +563,6 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
-  const int pair_id = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int G = args.G;
   const int n_tiles = (args.n_out + OUT_COLS - 1) / OUT_COLS;
   const int num_kb = args.num_kb;
@@ -565,6 +577,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 8);
+    }
+    for (int q = 0; q < pair::TQ; ++q) {
+      mbar_init(&tq_full[q], 1);
+      mbar_init(&tq_empty[q], pair::TQ_READERS);
     }
     fence_barrier_init();
     int acc = 0;
@@ -599,6 +615,32 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int total_tiles = tile_start[G];
   const uint32_t full_lead = mapa_shared(smem_u32(&full[0]), 0);
   const uint32_t tempty_lead = mapa_shared(smem_u32(&tempty[0]), 0);
+  const uint32_t tqe_lead = mapa_shared(smem_u32(&tq_empty[0]), 0);
+  const uint32_t tqf_peer = mapa_shared(smem_u32(&tq_full[0]), 1);
+  const uint32_t tq_peer = mapa_shared(smem_u32(const_cast<int *>(&tq[0])), 1);
+  // The tile sequence, the same for every role of the pair: the leader's producer
+  // publishes (publish = true), every other role reads.  One thread calls it; false
+  // on a wait past its time limit.
+  auto next_tile = [&](bool publish, int &q, uint32_t &qph, int &tile) -> bool {
+    if (publish) {
+      if (!mbar_wait_cluster(&tq_empty[q], qph ^ 1u, args.status)) return false;
+      tile = atomicAdd(args.tile_counter, 1);
+      if (tile >= total_tiles) tile = -1;
+      tq[q] = tile;
+      st_shared_cluster_u32(tq_peer + 4u * (uint32_t)q, (uint32_t)tile);
+      mbar_arrive(&tq_full[q]);
+      mbar_arrive_cluster(tqf_peer + 8u * (uint32_t)q);
+    } else {
+      if (!mbar_wait_cluster(&tq_full[q], qph, args.status)) return false;
+      tile = tq[q];
+      mbar_arrive_cluster(tqe_lead + 8u * (uint32_t)q);
+    }
+    if (++q == pair::TQ) {
+      q = 0;
+      qph ^= 1u;
+    }
+    return true;
+  };
 
   if (warp == 0 && gather) {
     // ------------------------------------------------------------ producer, gathered A (both CTAs)
@@ -613,7 +655,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     int g = 0;
     bool ok = true;
     const CUtensorMap *mb = (paired_b(MODE) && rank == 1) ? &tmB1 : &tmB0;
-    for (int tile = pair_id; tile < total_tiles && ok; tile += npairs) {
+    int tq_q = 0;
+    uint32_t tq_ph = 0;
+    while (ok) {
+      int tile = -1;
+      bool got = true;
+      if (lane == 0) got = next_tile(leader, tq_q, tq_ph, tile);
+      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) break;
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (tile < 0) break;
       while (tile >= tile_start[g + 1]) ++g;
       const int local = tile - tile_start[g];
       const int n_tile = local / mtiles[g];
@@ -671,7 +721,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       int g = 0;
       bool ok = true;
       const CUtensorMap *mb = (paired_b(MODE) && rank == 1) ? &tmB1 : &tmB0;
-      for (int tile = pair_id; tile < total_tiles && ok; tile += npairs) {
+      int tq_q = 0;
+      uint32_t tq_ph = 0;
+      while (ok) {
+        int tile = -1;
+        if (!next_tile(leader, tq_q, tq_ph, tile) || tile < 0) break;
         while (tile >= tile_start[g + 1]) ++g;
         const int local = tile - tile_start[g];
         const int n_tile = local / mtiles[g];
@@ -718,7 +772,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = pair_id; tile < total_tiles && ok; tile += npairs, ++it) {
+      int tq_q = 0;
+      uint32_t tq_ph = 0;
+      for (; ok; ++it) {
+        int tile = -1;
+        if (!next_tile(false, tq_q, tq_ph, tile) || tile < 0) break;
         const int acc = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
         if (!mbar_wait_cluster(&tempty[acc], (use & 1u) ^ 1u, args.status)) break;
@@ -758,7 +816,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int r = quad * 32 + lane;
     int g = 0;
     int it = 0;
-    for (int tile = pair_id; tile < total_tiles; tile += npairs, ++it) {
+    int tq_q = 0;
+    uint32_t tq_ph = 0;
+    for (;; ++it) {
+      // one tile id per warp: lane 0 reads the slot, frees it and passes the id on
+      int tile = -1;
+      bool got = true;
+      if (lane == 0) got = next_tile(false, tq_q, tq_ph, tile);
+      if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) break;
+      tile = __shfl_sync(0xffffffffu, tile, 0);
+      if (tile < 0) break;
       while (tile >= tile_start[g + 1]) ++g;
       const int local = tile - tile_start[g];
       const int n_tile = local / mtiles[g];
@@ -887,7 +954,11 @@ static int launch_pair(const CUtensorMap &ma, const CUtensorMap &ma2, const CUte
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ma, ma2, mb0, mb1, args) != cudaSuccess)
+  // the tile counter is the int after the workspace status word
+  Args a = args;
+  a.tile_counter = args.status + 1;
+  if (cudaMemsetAsync(a.tile_counter, 0, sizeof(int), stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, grouped_gemm_pair_kernel<MODE>, ma, ma2, mb0, mb1, a) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
