@@ -24,7 +24,8 @@
  *  - Every tensor argument is a DEVICE pointer to caller-owned memory on the
  *    current CUDA device; the library never allocates device memory.  Scratch
  *    comes from a caller-provided workspace `ws` of moe_workspace_size() bytes
- *    (256-byte aligned).  The workspace also holds the device status word.
+ *    (256-byte aligned).  The workspace also holds the device status word (and,
+ *    after it, a counter the grouped GEMM resets before each launch).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work
  *    is enqueued asynchronously on it; no call synchronises except
  *    moe_get_device_status.  Results are deterministic: the same inputs give

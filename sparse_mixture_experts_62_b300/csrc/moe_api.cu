@@ -86,7 +86,7 @@ int layout(const moe_config *c, moe_ws_layout *L) {
     o = align256(o + (bytes ? bytes : 1));
     return at;
   };
-  L->status = take(4);
+  L->status = take(8);  // the status word, then the CTA-pair GEMM's tile counter
   L->logits = take(T * N * 4);
   L->topk_idx = take(T * k * 4);
   L->topk_w = take(T * sl * 4);
