@@ -70,14 +70,24 @@ KERNEL_SOURCES = {False: ("moe_ffn_tc.cu", "moe_common.cuh", "moe_api.cu"),
                   True: ("moe_ffn_fp8_tc.cu", "moe_common.cuh", "moe_api.cu")}
 
 
+def code_of(text: str) -> str:
+    """C/CUDA source without its comments, whitespace runs collapsed to one space
+    (the sources hold no comment markers inside string literals)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(fp8: bool) -> str:
-    """First 16 hex digits of the SHA-256 of the expert-FFN kernel sources (and the
-    launcher that picks their tile forms), concatenated in a fixed order."""
+    """First 16 hex digits of the SHA-256 of the code of the expert-FFN kernel
+    sources (and the launcher that picks their tile forms), concatenated in a fixed
+    order; comments do not count."""
     import hashlib
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[fp8]:
-        with open(os.path.join(ROOT, "sparse_mixture_experts_62_b300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "sparse_mixture_experts_62_b300", "csrc", name)) as f:
+            h.update(code_of(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -36,7 +36,9 @@
 //   warps 2..5  epilogue: tcgen05.ld of its 32-lane quadrant, activation,
 //               16-byte stores masked to the group's rows and the output width.
 // Tiles are enumerated group by group, n-tile-major within a group, so the
-// CTAs of one wave share each weight tile through L2.
+// CTAs of one wave share each weight tile through L2.  Single CTAs take tiles
+// round robin; CTA pairs take them in issue order from a counter (see the tile
+// queue below), so the pairs that share a weight tile run it together.
 //
 // Small groups (forward modes, single-CTA form): a group of at most 128 rows
 // pays a whole 128-row MMA per tile however few its rows.  Its tiles run with the

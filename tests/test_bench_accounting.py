@@ -102,6 +102,13 @@ def test_traffic_only_for_the_captured_kernel_sources(tmp_path):
     assert bench._traffic("dsv3_finegrained", table=table) is None
 
 
+def test_source_hash_ignores_comments_only():
+    a = "int f(int x) {  // one\n  return x + 1; /* two\n lines */ }\n"
+    b = "int f(int x) {\n  return x + 1;\n}\n"
+    c = "int f(int x) { return x + 2; }"
+    assert bench.code_of(a) == bench.code_of(b) != bench.code_of(c)
+
+
 def test_fp32_kernel_label():
     assert "simt" in bench.ffn_kernel_label(W["shazeer_tiny_f32"], False)
     assert "tcgen05" in bench.ffn_kernel_label(W["mixtral_prefill"], False)
